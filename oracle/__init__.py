@@ -1,0 +1,187 @@
+"""CPU oracle for the submanifold sparse convolution layer.
+
+TEST INFRASTRUCTURE ONLY: only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import this
+package.  The CUDA library never imports, links or calls it, and it imports
+nothing from the CUDA library.
+
+The arithmetic lives in ``oracle.cpp`` (plain C++17, fp64, ``std::unordered_map``
+keyed on coordinates, a nested loop over outputs x offsets).  This module only
+marshals numpy arrays into it and derives the tuple set and per-offset lists
+from the neighbour table, which is a relabelling, not a computation.
+
+Pins (tests/test_oracle_pins.py): the pages' worked examples (the 4x5 and 5x5
+grids, the 11-tuple map with its 2/1/5/1/2 split, the quiz answer Q = (2, 2)),
+the (2L+1)^d dilation counts, mirror symmetry, brute force over all point
+pairs, and an fp64 dense convolution from ``torch.nn.functional`` read at the
+active sites.  No function here is parity-unpinned.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.cpp")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+STATUS = {0: "ok", 1: "bad argument", 2: "coordinate out of range", 3: "duplicate coordinate"}
+
+
+class OracleError(RuntimeError):
+    def __init__(self, code):
+        super().__init__(f"oracle: {STATUS.get(code, code)}")
+        self.code = code
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.cpp into liboracle.so next to it (g++, OpenMP)."""
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        cmd = ["g++", "-O2", "-std=c++17", "-fopenmp", "-fPIC", "-shared", _SRC, "-o", tmp]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB_PATH)
+        P = ctypes.c_void_p
+        lib.oracle_kmap.argtypes = [P, ctypes.c_int64, ctypes.c_int, ctypes.c_int, P, P, ctypes.c_int]
+        lib.oracle_kmap.restype = ctypes.c_int
+        lib.oracle_subm_conv.argtypes = [P, ctypes.c_int64, ctypes.c_int, ctypes.c_int, P, P, P,
+                                         ctypes.c_int, ctypes.c_int, ctypes.c_int, P, ctypes.c_int64,
+                                         P, ctypes.c_int]
+        lib.oracle_subm_conv.restype = ctypes.c_int
+        lib.oracle_max_threads.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return a.ctypes.data_as(ctypes.c_void_p) if a is not None else None
+
+
+def _coords(coords):
+    return np.ascontiguousarray(np.asarray(coords, dtype=np.int32).reshape(-1, 4))
+
+
+def _dims(dims):
+    d = np.ones(3, dtype=np.int32)
+    d[: len(dims)] = dims
+    return d
+
+
+def volume(ndim: int, K: int) -> int:
+    return K ** ndim
+
+
+def offset_index(delta, K: int) -> int:
+    """Lexicographic offset index, first spatial axis slowest."""
+    r = (K - 1) // 2
+    idx = 0
+    for d in delta:
+        idx = idx * K + (int(d) + r)
+    return idx
+
+
+def offset_of(idx: int, ndim: int, K: int) -> tuple:
+    r = (K - 1) // 2
+    d = []
+    for _ in range(ndim):
+        d.append(idx % K - r)
+        idx //= K
+    return tuple(reversed(d))
+
+
+def max_threads() -> int:
+    return int(_load().oracle_max_threads())
+
+
+def kmap(coords, ndim: int, K: int, dims, threads: int = 0) -> np.ndarray:
+    """Neighbour table int32 [N, K^ndim]: input row at c_q + d, or -1."""
+    c = _coords(coords)
+    n = c.shape[0]
+    V = volume(ndim, K)
+    nbr = np.empty((n, V), dtype=np.int32)
+    st = _load().oracle_kmap(_ptr(c), n, ndim, K, _ptr(_dims(dims)), _ptr(nbr), threads)
+    if st:
+        raise OracleError(st)
+    return nbr
+
+
+def tuples(nbr: np.ndarray) -> np.ndarray:
+    """The map M as an int64 array of (offset, out, in) rows, sorted."""
+    q, v = np.nonzero(nbr >= 0)
+    p = nbr[q, v]
+    t = np.stack([v.astype(np.int64), q.astype(np.int64), p.astype(np.int64)], axis=1)
+    order = np.lexsort((t[:, 2], t[:, 1], t[:, 0]))
+    return t[order]
+
+
+def offset_lists(nbr: np.ndarray) -> list:
+    """Per-offset lists [(in_rows, out_rows)] ordered by output row."""
+    out = []
+    for v in range(nbr.shape[1]):
+        q = np.nonzero(nbr[:, v] >= 0)[0]
+        out.append((nbr[q, v].astype(np.int64), q.astype(np.int64)))
+    return out
+
+
+def subm_conv(coords, feats, W, ndim: int, K: int, dims, relu: bool = False,
+              rows=None, threads: int = 0) -> np.ndarray:
+    """fp64 output features [len(rows) or N, C_out] of one submanifold layer."""
+    c = _coords(coords)
+    n = c.shape[0]
+    f = np.ascontiguousarray(np.asarray(feats, dtype=np.float64).reshape(n, -1))
+    w = np.ascontiguousarray(np.asarray(W, dtype=np.float64))
+    V, c_in, c_out = w.shape
+    if V != volume(ndim, K) or f.shape[1] != c_in:
+        raise OracleError(1)
+    r = None if rows is None else np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    nrows = n if r is None else r.shape[0]
+    out = np.empty((nrows, c_out), dtype=np.float64)
+    st = _load().oracle_subm_conv(_ptr(c), n, ndim, K, _ptr(_dims(dims)), _ptr(f), _ptr(w),
+                                  c_in, c_out, int(bool(relu)), _ptr(r), nrows, _ptr(out), threads)
+    if st:
+        raise OracleError(st)
+    return out
+
+
+def round_to(x: np.ndarray, dtype: str) -> np.ndarray:
+    """Round fp64 values once to a storage dtype (RN-even), returned as fp64."""
+    if dtype == "f32":
+        return x.astype(np.float32).astype(np.float64)
+    if dtype == "f16":
+        return x.astype(np.float16).astype(np.float64)
+    if dtype == "bf16":
+        # bfloat16 keeps 8 significant bits and fp32's exponent range: round
+        # the fp64 value straight to a multiple of its bf16 quantum, ties to
+        # even (np.rint), with the quantum floored at 2^-133 (subnormals).
+        x = np.asarray(x, dtype=np.float64)
+        _, e = np.frexp(x)
+        e = np.maximum(e, -125)
+        return np.ldexp(np.rint(np.ldexp(x, 8 - e)), e - 8)
+    raise ValueError(dtype)
+
+
+def subm_conv_stack(coords, feats, Ws, ndim: int, K: int, dims, dtype: str,
+                    threads: int = 0) -> list:
+    """Layer outputs of a stack sharing one map: ReLU between layers, none
+    after the last; each layer's output rounded once to ``dtype`` (as stored)
+    before it feeds the next layer."""
+    outs = []
+    x = np.asarray(feats, dtype=np.float64)
+    for li, W in enumerate(Ws):
+        y = subm_conv(coords, x, W, ndim, K, dims, relu=(li + 1 < len(Ws)), threads=threads)
+        y = round_to(y, dtype)
+        outs.append(y)
+        x = y
+    return outs

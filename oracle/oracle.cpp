@@ -1,0 +1,193 @@
+// CPU oracle for the submanifold sparse convolution layer.
+//
+// TEST INFRASTRUCTURE ONLY.  Only tests/, __graft_entry__.smoke() and the
+// cpu_baseline / reference legs of bench.py may load or call this code.  It
+// shares nothing with the CUDA library: no headers, no helpers, no tables.
+//
+// It is the plain definition of the layer, written out:
+//
+//   * Sparse representation: a coordinate list and a feature list, row i of
+//     one belonging to row i of the other ("SparseConvNet: from hash table to
+//     rulebook", section 1).
+//   * Submanifold output set: an output exists exactly where an input exists,
+//     P_out = P_in ("Sparse inputs and sparse convolution", section "The fix";
+//     exam sheet "Sparse convolution for point clouds", definition).
+//   * Kernel map: for every output q and every offset d, look up the input at
+//     coordinate q + d in a hash table on coordinates; a hit p adds the tuple
+//     (p, q, W_d) ("Sparse inputs and sparse convolution", section "The map is
+//     the computation").  Sign convention: input P sits at output Q shifted by
+//     the offset, P = Q + d (same page, section "Follow the boxed point"; exam
+//     sheet, "The map and the update rule").
+//   * Update rule: f_out(Q) += f_in(P) x W_d for every tuple (exam sheet, "The
+//     map and the update rule").  Accumulated here in fp64.
+//
+// Offsets are indexed lexicographically with the first spatial axis slowest:
+// idx(d) = sum_k (d_k + r) * K^(ndim-1-k), r = (K-1)/2.  In 2D the offsets act
+// on (x, y) only and z is carried unchanged.
+//
+// Parity pins: every function here is pinned by tests under tests/ against the
+// pages' worked examples, brute force over point pairs, and an fp64 dense
+// convolution from a library routine.  Nothing here is "parity unpinned".
+
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <unordered_map>
+#include <vector>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+namespace {
+
+// Status codes returned to the Python wrapper.
+enum { OR_OK = 0, OR_BAD_ARG = 1, OR_OUT_OF_RANGE = 2, OR_DUPLICATE = 3 };
+
+// The oracle's own coordinate key: four 16-bit fields, batch highest.
+inline uint64_t pack_key(int64_t b, int64_t x, int64_t y, int64_t z) {
+  return (uint64_t(b) << 48) | (uint64_t(x) << 32) | (uint64_t(y) << 16) | uint64_t(z);
+}
+
+struct Problem {
+  const int32_t* coords;  // [n, 4] = (batch, x, y, z)
+  int64_t n;
+  int ndim;                // 2 or 3
+  int K;                   // odd kernel size
+  int32_t dims[3];         // spatial extents
+  int volume;              // K^ndim
+  std::unordered_map<uint64_t, int32_t> table;
+};
+
+int check_args(const int32_t* coords, int64_t n, int ndim, int K, const int32_t* dims) {
+  if (n < 0 || (n > 0 && !coords) || !dims) return OR_BAD_ARG;
+  if (ndim != 2 && ndim != 3) return OR_BAD_ARG;
+  if (K < 1 || (K % 2) == 0) return OR_BAD_ARG;
+  for (int a = 0; a < 3; ++a)
+    if (dims[a] < 1 || dims[a] > 65535) return OR_BAD_ARG;
+  return OR_OK;
+}
+
+// Step 1: put every coordinate into a hash table, row id as the value.
+int build_table(Problem& P) {
+  P.table.clear();
+  P.table.reserve(size_t(P.n) * 2 + 1);
+  for (int64_t i = 0; i < P.n; ++i) {
+    const int32_t* c = P.coords + 4 * i;
+    if (c[0] < 0 || c[0] >= 65535) return OR_OUT_OF_RANGE;
+    for (int a = 0; a < 3; ++a)
+      if (c[1 + a] < 0 || c[1 + a] >= P.dims[a]) return OR_OUT_OF_RANGE;
+    auto ins = P.table.emplace(pack_key(c[0], c[1], c[2], c[3]), int32_t(i));
+    if (!ins.second) return OR_DUPLICATE;
+  }
+  return OR_OK;
+}
+
+// The spatial offset with lexicographic index idx (first axis slowest).
+void offset_of(int idx, int ndim, int K, int d[3]) {
+  const int r = (K - 1) / 2;
+  d[0] = d[1] = d[2] = 0;
+  for (int k = ndim - 1; k >= 0; --k) {
+    d[k] = idx % K - r;
+    idx /= K;
+  }
+}
+
+// Step 2: the input row at coordinate c_q + d, or -1 if none is active there
+// (outside the grid counts as absent: zero padding).
+int32_t neighbour(const Problem& P, int64_t q, const int d[3]) {
+  const int32_t* c = P.coords + 4 * q;
+  int64_t x = int64_t(c[1]) + d[0];
+  int64_t y = int64_t(c[2]) + d[1];
+  int64_t z = int64_t(c[3]) + d[2];
+  if (x < 0 || x >= P.dims[0] || y < 0 || y >= P.dims[1] || z < 0 || z >= P.dims[2]) return -1;
+  auto it = P.table.find(pack_key(c[0], x, y, z));
+  return it == P.table.end() ? -1 : it->second;
+}
+
+int setup(Problem& P, const int32_t* coords, int64_t n, int ndim, int K, const int32_t* dims) {
+  int st = check_args(coords, n, ndim, K, dims);
+  if (st) return st;
+  P.coords = coords;
+  P.n = n;
+  P.ndim = ndim;
+  P.K = K;
+  for (int a = 0; a < 3; ++a) P.dims[a] = dims[a];
+  P.volume = 1;
+  for (int a = 0; a < ndim; ++a) P.volume *= K;
+  return build_table(P);
+}
+
+int threads_to_use(int nthreads) {
+#ifdef _OPENMP
+  return nthreads > 0 ? nthreads : omp_get_max_threads();
+#else
+  (void)nthreads;
+  return 1;
+#endif
+}
+
+}  // namespace
+
+extern "C" {
+
+// Neighbour table: nbr[q * V + idx(d)] = row of the input at c_q + d, or -1.
+// Built by the double loop over outputs and offsets.
+int oracle_kmap(const int32_t* coords, int64_t n, int ndim, int K, const int32_t* dims,
+                int32_t* nbr, int nthreads) {
+  Problem P;
+  int st = setup(P, coords, n, ndim, K, dims);
+  if (st) return st;
+  const int V = P.volume;
+  std::vector<int> offs(size_t(V) * 3);
+  for (int v = 0; v < V; ++v) offset_of(v, ndim, K, &offs[3 * v]);
+  const int nt = threads_to_use(nthreads);
+#pragma omp parallel for schedule(static) num_threads(nt)
+  for (int64_t q = 0; q < n; ++q)
+    for (int v = 0; v < V; ++v) nbr[q * V + v] = neighbour(P, q, &offs[3 * v]);
+  return OR_OK;
+}
+
+// Output features for the listed output rows (all rows if rows == NULL):
+// out[k, :] = sum over offsets d with an input p at c_q + d of f[p, :] W[d],
+// q = rows[k], accumulated in fp64, then max(., 0) if relu != 0.
+// feats [n, c_in], W [V, c_in, c_out], out [nrows, c_out], all fp64.
+int oracle_subm_conv(const int32_t* coords, int64_t n, int ndim, int K, const int32_t* dims,
+                     const double* feats, const double* W, int c_in, int c_out, int relu,
+                     const int64_t* rows, int64_t nrows, double* out, int nthreads) {
+  Problem P;
+  int st = setup(P, coords, n, ndim, K, dims);
+  if (st) return st;
+  if (c_in < 1 || c_out < 1 || !W || (n > 0 && !feats) || !out) return OR_BAD_ARG;
+  if (!rows) nrows = n;
+  const int V = P.volume;
+  std::vector<int> offs(size_t(V) * 3);
+  for (int v = 0; v < V; ++v) offset_of(v, ndim, K, &offs[3 * v]);
+  for (int64_t k = 0; k < nrows; ++k)
+    if (rows && (rows[k] < 0 || rows[k] >= n)) return OR_BAD_ARG;
+  const int nt = threads_to_use(nthreads);
+#pragma omp parallel for schedule(dynamic, 64) num_threads(nt)
+  for (int64_t k = 0; k < nrows; ++k) {
+    const int64_t q = rows ? rows[k] : k;
+    double* acc = out + k * c_out;
+    for (int co = 0; co < c_out; ++co) acc[co] = 0.0;
+    for (int v = 0; v < V; ++v) {
+      const int32_t p = neighbour(P, q, &offs[3 * v]);
+      if (p < 0) continue;
+      const double* f = feats + int64_t(p) * c_in;
+      const double* w = W + int64_t(v) * c_in * c_out;
+      for (int ci = 0; ci < c_in; ++ci) {
+        const double a = f[ci];
+        const double* wrow = w + int64_t(ci) * c_out;
+        for (int co = 0; co < c_out; ++co) acc[co] += a * wrow[co];
+      }
+    }
+    if (relu)
+      for (int co = 0; co < c_out; ++co) acc[co] = acc[co] > 0.0 ? acc[co] : 0.0;
+  }
+  return OR_OK;
+}
+
+// Number of threads the OpenMP runtime would use by default.
+int oracle_max_threads(void) { return threads_to_use(0); }
+
+}  // extern "C"

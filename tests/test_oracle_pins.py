@@ -1,0 +1,362 @@
+"""Pins for the CPU oracle, against what the pages and the mathematics fix.
+
+Each test checks the oracle against something other than itself: the pages'
+worked examples (tests/golden/), brute force over all point pairs, and an fp64
+dense convolution computed by torch.nn.functional on a dense grid.
+"""
+import itertools
+
+import numpy as np
+import pytest
+import torch
+
+from conftest import read_golden
+
+import oracle
+from submanifold_sparse_convolution_hash_gb300 import scenes
+
+
+# ---------------------------------------------------------------------------
+# helpers (independent of the oracle)
+# ---------------------------------------------------------------------------
+
+def grid_points(golden):
+    pts = {}
+    grid = None
+    for row in golden:
+        if row[0] == "grid":
+            grid = (int(row[1]), int(row[2]))
+        elif row[0] == "point":
+            pts[row[1]] = (int(row[2]), int(row[3]))
+    names = sorted(pts, key=lambda s: int(s[1:]))
+    coords = np.array([[0, pts[n][0], pts[n][1], 0] for n in names], dtype=np.int32)
+    return grid, names, coords
+
+
+def dense_dilate(active, K):
+    """Regular output definition on a grid: an output is active when any
+    active input lies inside its KxK(xK) window, the window clipped to the
+    grid (same padding)."""
+    r = K // 2
+    out = np.zeros_like(active)
+    for idx in np.argwhere(active):
+        sl = tuple(slice(max(i - r, 0), min(i + r + 1, s)) for i, s in zip(idx, active.shape))
+        out[sl] = True
+    return out
+
+
+def brute_force_tuples(coords, ndim, K, dims):
+    """All (offset, out, in) with c_in - c_out = d, |d|_inf <= r, same batch."""
+    r = K // 2
+    n = coords.shape[0]
+    res = []
+    for q in range(n):
+        for p in range(n):
+            if coords[p, 0] != coords[q, 0]:
+                continue
+            d = coords[p, 1:1 + ndim] - coords[q, 1:1 + ndim]
+            if ndim == 2 and coords[p, 3] != coords[q, 3]:
+                continue
+            if np.all(np.abs(d) <= r):
+                res.append((oracle.offset_index(d, K), q, p))
+    res.sort()
+    return np.array(res, dtype=np.int64).reshape(-1, 3)
+
+
+def random_scene(seed, n, dims, ndim, batches=1):
+    rng = scenes.SplitMix64(seed, 99)
+    X, Y, Z = dims
+    tot = X * Y * (Z if ndim == 3 else 1)
+    pts = []
+    for b in range(batches):
+        cells = rng.permutation(tot)[:n]
+        if ndim == 3:
+            x, rem = cells // (Y * Z), cells % (Y * Z)
+            y, z = rem // Z, rem % Z
+        else:
+            x, y, z = cells // Y, cells % Y, np.zeros_like(cells)
+        pts.append(np.stack([np.full_like(x, b), x, y, z], axis=1))
+    c = np.concatenate(pts).astype(np.int32)
+    return c[rng.permutation(c.shape[0])]
+
+
+def dense_conv_reference(coords, feats, W, ndim, K, dims):
+    """fp64 dense convolution (torch, cross-correlation, zero padding) over the
+    whole grid, read back at the active sites."""
+    r = K // 2
+    n, c_in = feats.shape
+    c_out = W.shape[2]
+    out = np.zeros((n, c_out))
+    for b in np.unique(coords[:, 0]):
+        sel = np.nonzero(coords[:, 0] == b)[0]
+        if ndim == 3:
+            grid = torch.zeros((1, c_in) + tuple(dims), dtype=torch.float64)
+            c = torch.from_numpy(coords[sel].astype(np.int64))
+            grid[0, :, c[:, 1], c[:, 2], c[:, 3]] = torch.from_numpy(feats[sel]).T
+            w = torch.from_numpy(W).reshape(K, K, K, c_in, c_out).permute(4, 3, 0, 1, 2).contiguous()
+            y = torch.nn.functional.conv3d(grid, w, padding=r)
+            out[sel] = y[0, :, c[:, 1], c[:, 2], c[:, 3]].T.numpy()
+        else:
+            grid = torch.zeros((1, c_in, dims[0], dims[1]), dtype=torch.float64)
+            c = torch.from_numpy(coords[sel].astype(np.int64))
+            grid[0, :, c[:, 1], c[:, 2]] = torch.from_numpy(feats[sel]).T
+            w = torch.from_numpy(W).reshape(K, K, c_in, c_out).permute(3, 2, 0, 1).contiguous()
+            y = torch.nn.functional.conv2d(grid, w, padding=r)
+            out[sel] = y[0, :, c[:, 1], c[:, 2]].T.numpy()
+    return out
+
+
+# ---------------------------------------------------------------------------
+# the pages' worked examples
+# ---------------------------------------------------------------------------
+
+def test_five_point_map_matches_worked_example():
+    g = read_golden("five_point_map.txt")
+    grid, names, coords = grid_points(g)
+    nbr = oracle.kmap(coords, 2, 3, (grid[0], grid[1], 1))
+    got = {tuple(t) for t in oracle.tuples(nbr).tolist()}
+    want = set()
+    for row in g:
+        if row[0] == "tuple":
+            p, q = int(row[1][1:]), int(row[2][1:])
+            want.add((oracle.offset_index((int(row[3]), int(row[4])), 3), q, p))
+    assert got == want
+    total = [int(r[1]) for r in g if r[0] == "total"][0]
+    assert len(got) == total == 11
+    counts = np.bincount(oracle.tuples(nbr)[:, 0], minlength=9)
+    nonempty = [int(r[1]) for r in g if r[0] == "nonempty_offsets"][0]
+    assert int((counts > 0).sum()) == nonempty == 5
+    split = [r[1:] for r in g if r[0] == "rows_per_nonempty_offset"][0]
+    for item in split:
+        d, k = item.split(":")
+        dx, dy = (int(v) for v in d.split(","))
+        assert counts[oracle.offset_index((dx, dy), 3)] == int(k)
+    # the isolated point P2 appears only in the centre group
+    t = oracle.tuples(nbr)
+    assert set(map(tuple, t[(t[:, 1] == 2) | (t[:, 2] == 2)].tolist())) == {(4, 2, 2)}
+
+
+def test_five_point_update_rule_closed_form():
+    """The weight-stationary equations printed under the gather/scatter figure
+    (f1 += f0 W(-1,-1), f4 += f3 W(-1,-1)) are the W(-1,-1) part of the
+    oracle's output; with W zero elsewhere they are the whole output."""
+    g = read_golden("five_point_map.txt")
+    grid, names, coords = grid_points(g)
+    rng = np.random.default_rng(5)
+    f = rng.standard_normal((5, 4))
+    W = np.zeros((9, 4, 3))
+    W[oracle.offset_index((-1, -1), 3)] = rng.standard_normal((4, 3))
+    out = oracle.subm_conv(coords, f, W, 2, 3, (5, 5, 1))
+    Wm = W[oracle.offset_index((-1, -1), 3)]
+    want = np.zeros((5, 3))
+    want[1] = f[0] @ Wm
+    want[4] = f[3] @ Wm
+    np.testing.assert_allclose(out, want, rtol=0, atol=1e-14)
+    # full weights: Q1 receives (P0, W(-1,-1)), (P1, W(0,0)), (P3, W(1,0))
+    W = rng.standard_normal((9, 4, 3))
+    out = oracle.subm_conv(coords, f, W, 2, 3, (5, 5, 1))
+    oi = lambda d: oracle.offset_index(d, 3)
+    want_q1 = f[0] @ W[oi((-1, -1))] + f[1] @ W[oi((0, 0))] + f[3] @ W[oi((1, 0))]
+    np.testing.assert_allclose(out[1], want_q1, rtol=1e-13, atol=1e-13)
+
+
+def test_sign_convention_quiz():
+    g = read_golden("sign_quiz.txt")
+    kv = {r[0]: r[1:] for r in g if r[0] in ("input", "offset", "output")}
+    g5 = read_golden("five_point_map.txt")
+    grid, names, coords = grid_points(g5)
+    nbr = oracle.kmap(coords, 2, 3, (5, 5, 1))
+    pin = [i for i in range(5) if tuple(coords[i, 1:3]) == tuple(int(v) for v in kv["input"])][0]
+    qout = [i for i in range(5) if tuple(coords[i, 1:3]) == tuple(int(v) for v in kv["output"])][0]
+    v = oracle.offset_index(tuple(int(x) for x in kv["offset"]), 3)
+    assert nbr[qout, v] == pin  # (P3, Q1, W(1,0))
+    assert (pin, qout) == (3, 1)
+    # P0's dense window: the output at (0,0) uses W(1,1), the one at (2,2) W(-1,-1)
+    for row in g:
+        if row[0] in ("window_corner", "window_centre"):
+            qx, qy, dx, dy = (int(x) for x in row[1:])
+            assert (1 - qx, 1 - qy) == (dx, dy)
+
+
+def test_four_point_grid_counts():
+    g = read_golden("four_point_grid.txt")
+    kv = {r[0]: r[1:] for r in g}
+    grid, names, coords = grid_points(g)
+    active = np.zeros(grid, dtype=bool)
+    active[coords[:, 1], coords[:, 2]] = True
+    one = dense_dilate(active, 3)
+    two = dense_dilate(one, 3)
+    assert one.sum() == int(kv["dense_active_after_1"][0])
+    assert {f"{i},{j}" for i, j in np.argwhere(~one)} == set(kv["dense_empty_after_1"])
+    assert two.sum() == int(kv["dense_active_after_2"][0])
+    # submanifold: the output set is the input set, layer after layer
+    nbr = oracle.kmap(coords, 2, 3, (4, 5, 1))
+    assert nbr.shape[0] == int(kv["submanifold_outputs"][0])
+    m = len(oracle.tuples(nbr))
+    assert m == int(kv["entries_submanifold"][0])
+    # zero-skipping entries: every in-grid output of each active input's window
+    zs = sum(int(dense_dilate(np.eye(1, 20, 5 * i + j, dtype=bool).reshape(4, 5), 3).sum())
+             for i, j in coords[:, 1:3])
+    assert zs == int(kv["entries_zero_skipping"][0])
+    assert 20 * 9 == int(kv["entries_dense"][0])
+    per = int(kv["macs_per_entry_c64"][0])
+    assert per == 64 * 64
+    assert m * per == int(kv["macs_submanifold_c64"][0])
+    assert zs * per == int(kv["macs_zero_skipping_c64"][0])
+    assert 180 * per == int(kv["macs_dense_c64"][0])
+    # P0's window keeps exactly the two listed tuples
+    t = oracle.tuples(nbr)
+    p0 = {(int(v), int(q)) for v, q, p in t.tolist() if p == 0}
+    want = {(oracle.offset_index((int(r[3]), int(r[4])), 3), int(r[2][1:])) for r in g if r[0] == "p0_tuple"}
+    assert p0 == want
+
+
+def test_dilation_counts():
+    for row in read_golden("dilation.txt"):
+        ndim, L, want = int(row[1]), int(row[2]), int(row[3])
+        shape = (11,) * ndim
+        a = np.zeros(shape, dtype=bool)
+        a[(5,) * ndim] = True
+        for _ in range(L):
+            a = dense_dilate(a, 3)
+        assert a.sum() == want == (2 * L + 1) ** ndim
+    # submanifold never dilates: one site stays one site with one tuple
+    for ndim, K in ((3, 3), (3, 5), (2, 3)):
+        nbr = oracle.kmap(np.array([[0, 5, 5, 5 if ndim == 3 else 0]]), ndim, K, (11, 11, 11 if ndim == 3 else 1))
+        assert nbr.shape == (1, K ** ndim) and (nbr >= 0).sum() == 1 and nbr[0, (K ** ndim - 1) // 2] == 0
+
+
+# ---------------------------------------------------------------------------
+# brute force and invariants
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("ndim,K,dims,n,batches", [
+    (2, 3, (12, 9, 1), 40, 1), (2, 5, (10, 10, 1), 35, 2),
+    (3, 3, (6, 7, 5), 60, 2), (3, 5, (6, 6, 6), 50, 1), (3, 1, (4, 4, 4), 10, 1),
+])
+def test_kmap_equals_brute_force(ndim, K, dims, n, batches):
+    coords = random_scene(ndim * 100 + K * 10 + n, n, dims, ndim, batches)
+    nbr = oracle.kmap(coords, ndim, K, dims)
+    np.testing.assert_array_equal(oracle.tuples(nbr), brute_force_tuples(coords, ndim, K, dims))
+
+
+def test_kmap_invariants_on_lidar_like_scene():
+    s = scenes.lidar_scan(7, 3000, (120, 120, 41))
+    nbr = oracle.kmap(s.coords, 3, 3, s.dims)
+    V = 27
+    counts = (nbr >= 0).sum(axis=0)
+    # centre column is the identity, and only it
+    np.testing.assert_array_equal(nbr[:, V // 2], np.arange(s.n))
+    # count(d) == count(-d); (p, q, d) in M <=> (q, p, -d) in M
+    np.testing.assert_array_equal(counts, counts[::-1])
+    t = oracle.tuples(nbr)
+    mirrored = np.stack([V - 1 - t[:, 0], t[:, 2], t[:, 1]], axis=1)
+    mirrored = mirrored[np.lexsort((mirrored[:, 2], mirrored[:, 1], mirrored[:, 0]))]
+    np.testing.assert_array_equal(t, mirrored)
+    # translation invariance (shift kept inside the grid)
+    c2 = s.coords.copy()
+    c2[:, 1] += 3
+    c2[:, 2] -= 2
+    np.testing.assert_array_equal(oracle.kmap(c2, 3, 3, s.dims), nbr)
+    # permutation equivariance of row ids
+    perm = np.random.default_rng(1).permutation(s.n)
+    inv = np.argsort(perm)
+    nbr_p = oracle.kmap(s.coords[perm], 3, 3, s.dims)
+    expect = np.where(nbr[perm] >= 0, inv[np.maximum(nbr[perm], 0)], -1)
+    np.testing.assert_array_equal(nbr_p, expect)
+
+
+def test_kmap_errors():
+    c = np.array([[0, 1, 1, 1], [0, 1, 1, 1]])
+    with pytest.raises(oracle.OracleError) as e:
+        oracle.kmap(c, 3, 3, (4, 4, 4))
+    assert e.value.code == 3
+    with pytest.raises(oracle.OracleError) as e:
+        oracle.kmap(np.array([[0, 4, 1, 1]]), 3, 3, (4, 4, 4))
+    assert e.value.code == 2
+    with pytest.raises(oracle.OracleError) as e:
+        oracle.kmap(np.array([[0, 1, 1, 1]]), 3, 4, (4, 4, 4))
+    assert e.value.code == 1
+    assert oracle.kmap(np.zeros((0, 4)), 3, 3, (4, 4, 4)).shape == (0, 27)
+
+
+# ---------------------------------------------------------------------------
+# features
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("ndim,K,dims,n,batches,cin,cout", [
+    (2, 3, (9, 11, 1), 30, 2, 5, 3), (3, 3, (7, 6, 5), 70, 2, 4, 6), (3, 5, (7, 7, 6), 60, 1, 3, 2),
+])
+def test_conv_equals_dense_conv(ndim, K, dims, n, batches, cin, cout):
+    coords = random_scene(7 + n, n, dims, ndim, batches)
+    rng = np.random.default_rng(n)
+    f = rng.standard_normal((coords.shape[0], cin))
+    W = rng.standard_normal((K ** ndim, cin, cout))
+    got = oracle.subm_conv(coords, f, W, ndim, K, dims)
+    want = dense_conv_reference(coords, f, W, ndim, K, dims)
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
+
+
+def test_conv_single_site_two_sites_linearity_relu():
+    rng = np.random.default_rng(3)
+    W = rng.standard_normal((27, 4, 5))
+    f = rng.standard_normal((2, 4))
+    one = oracle.subm_conv(np.array([[0, 2, 2, 2]]), f[:1], W, 3, 3, (5, 5, 5))
+    np.testing.assert_allclose(one[0], f[0] @ W[13], rtol=1e-14)
+    # q at (2,2,2), p at q + d with d = (1,0,-1): out_q = f_q Wc + f_p W_d,
+    # out_p = f_p Wc + f_q W_{-d}
+    c = np.array([[0, 2, 2, 2], [0, 3, 2, 1]])
+    d = oracle.offset_index((1, 0, -1), 3)
+    md = oracle.offset_index((-1, 0, 1), 3)
+    two = oracle.subm_conv(c, f, W, 3, 3, (5, 5, 5))
+    np.testing.assert_allclose(two[0], f[0] @ W[13] + f[1] @ W[d], rtol=1e-13)
+    np.testing.assert_allclose(two[1], f[1] @ W[13] + f[0] @ W[md], rtol=1e-13)
+    # linearity in features and in weights
+    s = scenes.lidar_scan(11, 800, (60, 60, 41))
+    f1, f2 = rng.standard_normal((2, s.n, 4))
+    W2 = rng.standard_normal(W.shape)
+    conv = lambda ff, ww: oracle.subm_conv(s.coords, ff, ww, 3, 3, s.dims)
+    np.testing.assert_allclose(conv(2 * f1 - f2, W), 2 * conv(f1, W) - conv(f2, W), rtol=1e-11, atol=1e-11)
+    np.testing.assert_allclose(conv(f1, W + W2), conv(f1, W) + conv(f1, W2), rtol=1e-11, atol=1e-11)
+    # ReLU and row subsets
+    full = conv(f1, W)
+    rl = oracle.subm_conv(s.coords, f1, W, 3, 3, s.dims, relu=True)
+    np.testing.assert_array_equal(rl, np.maximum(full, 0))
+    rows = np.array([5, 0, s.n - 1, 5])
+    np.testing.assert_array_equal(oracle.subm_conv(s.coords, f1, W, 3, 3, s.dims, rows=rows), full[rows])
+
+
+def test_mac_count_independent_of_grouping():
+    s = scenes.lidar_scan(12, 1500, (80, 80, 41))
+    nbr = oracle.kmap(s.coords, 3, 3, s.dims)
+    per_offset = (nbr >= 0).sum(axis=0)
+    m = int(per_offset.sum())
+    assert m == len(oracle.tuples(nbr))
+    assert per_offset[13] == s.n  # the centre map has one entry per point
+    # grouping offsets into any partition leaves the MAC total unchanged
+    groups = [list(range(0, 13)), [13], list(range(14, 27))]
+    assert sum(int(per_offset[g].sum()) for g in groups) * 32 * 32 == m * 32 * 32
+
+
+def test_round_to_matches_library_rounding():
+    x = np.random.default_rng(0).standard_normal(20000) * 10
+    x32 = x.astype(np.float32).astype(np.float64)  # exactly representable in fp32
+    want = torch.from_numpy(x32).float().to(torch.bfloat16).double().numpy()
+    np.testing.assert_array_equal(oracle.round_to(x32, "bf16"), want)
+    np.testing.assert_array_equal(oracle.round_to(x, "f16"), x.astype(np.float16).astype(np.float64))
+    # ties go to even: 1 + 2^-8 lies halfway between 1 and 1 + 2^-7 in bf16
+    assert oracle.round_to(np.array([1 + 2 ** -8, 1 + 3 * 2 ** -8]), "bf16").tolist() == [1.0, 1 + 2 ** -6]
+
+
+def test_stack_rounds_between_layers():
+    s = scenes.lidar_scan(13, 600, (50, 50, 41))
+    rng = np.random.default_rng(4)
+    f = rng.standard_normal((s.n, 8)).astype(np.float16).astype(np.float64)
+    Ws = [rng.standard_normal((27, 8, 8)) / 8 for _ in range(3)]
+    outs = oracle.subm_conv_stack(s.coords, f, Ws, 3, 3, s.dims, "f16")
+    x = f
+    for li, W in enumerate(Ws):
+        y = oracle.subm_conv(s.coords, x, W, 3, 3, s.dims, relu=li < 2).astype(np.float16).astype(np.float64)
+        np.testing.assert_array_equal(outs[li], y)
+        x = y
+    assert (outs[0] >= 0).all() and (outs[1] >= 0).all() and (outs[2] < 0).any()
