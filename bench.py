@@ -1,0 +1,439 @@
+#!/usr/bin/env python3
+"""Benchmark of the submanifold sparse convolution hot path on one GPU.
+
+One step = one pass of the whole path over one synthetic scene:
+    sc_hash_build -> sc_kmap_build -> sc_subm_conv_fwd
+on the LiDAR-like workload (1440x1440x41 grid, ~100k voxels, 3x3x3 kernel,
+C_in = C_out = 32, fp16 features and weights, fp32 accumulation).
+
+Prints one JSON line.  `value` is Mvoxels/s over the timed steps with inputs
+resident in device memory and L2 flushed (a 256 MB write) before every step,
+outside the per-step CUDA events.  `e2e` is the same metric with pinned host
+inputs copied in and the output copied back inside every step, through the
+default (synchronising) API calls.  `roofline` reports the dominant kernel's
+algorithmic bytes over its average event-timed launch duration against the
+measured HBM copy bandwidth.  `cpu_baseline` times the CPU oracle on the same
+scene on this host's cores.
+
+--impl reference times the CPU oracle alone (the reference arm).
+Under torchrun (WORLD_SIZE > 1) every rank runs an independent replica on
+its own scene (replicas only; no data-path collective).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "subm-conv layer effective TFLOP/s, Mvoxels/s & % roofline; kernel-map build ms"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=1)
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def make_workload(idx: int, rank: int):
+    from submanifold_sparse_convolution_hash_gb300 import scenes
+    w, s = scenes.workload(idx)
+    if rank > 0:  # replicas draw their own scene of the same recipe
+        if idx == 1:
+            s = scenes.lidar_scan(1001 + 7919 * rank, 100_000, s.dims)
+        else:
+            raise SystemExit("replicas are defined for workload 1")
+    return w, s
+
+
+def layer_tensors(w, s):
+    from submanifold_sparse_convolution_hash_gb300 import scenes
+    V = w.K ** s.ndim
+    c_in, c_out = w.channels[0], w.channels[1]
+    f = scenes.features(w.seed, s.n, c_in)
+    W = scenes.weights(w.seed, V, c_in, c_out, std=1.0 if w.w_std_unit else None)
+    return f, W
+
+
+# ------------------------------------------------------------- algorithmic bytes --
+def algo_bytes(kernel: str, N: int, V: int, M: int, c_in: int, c_out: int, s: int, ntiles: int) -> float | None:
+    """Bytes each kernel must move at minimum (per launch)."""
+    lists = 8 * (M - N)
+    table = {
+        "hash_insert": 16 * N + 16 * N + 8 * N,            # coords in; N slots + row keys out
+        "kmap_probe": 8 * N + 4 * N * V + 4 * V * ntiles,  # row keys in; neighbour table + counts out
+        "kmap_scan": 8 * V * ntiles,
+        "kmap_fill": 4 * N * V + 4 * V * ntiles + lists,   # neighbour table in; (in, out) lists out
+        "pack_weights": 2 * V * c_in * c_out * s,
+        # gathered neighbour rows + one write per output row + neighbour table + weights
+        "subm_conv_fused": M * c_in * s + N * c_out * s + 4 * N * V + V * c_in * c_out * s,
+        "subm_conv_ws_centre": N * c_in * s + 4 * N * c_out + V * c_in * c_out * s // V,
+        "subm_conv_ws_scatter": (M - N) * c_in * s + 8 * (M - N) + 8 * (M - N) * c_out,
+        "cast_out": 4 * N * c_out + N * c_out * s,
+        "subm_conv_simt": M * c_in * s + N * c_out * s + 4 * N * V + V * c_in * c_out * s,
+    }
+    return table.get(kernel)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"], "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch from a committed ncu summary, or None if absent
+    or taken on a different version of the kernel's source file."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(kernel)
+    if not d:
+        return None
+    src = os.path.join(ROOT, d["source"])
+    if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest() != d["sha256"]:
+        return None
+    return d["dram_bytes_per_launch"]
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------- CPU --
+def cpu_oracle_run(s, K, f, W, seconds: float):
+    """Times the oracle (map + layer) on the full scene, repeated to ~`seconds`."""
+    import oracle
+    f64 = f.astype(np.float64)
+    W64 = W.astype(np.float64)
+    t0 = time.perf_counter()
+    passes = 0
+    while True:
+        oracle.kmap(s.coords, s.ndim, K, s.dims)
+        oracle.subm_conv(s.coords, f64, W64, s.ndim, K, s.dims)
+        passes += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or el * (passes + 1) / passes > 3 * seconds:
+            break
+    return {"value": s.n * passes / el / 1e6, "unit": "Mvoxels/s", "cores": oracle.max_threads(),
+            "kind": "oracle",
+            "sample": f"full scene (N={s.n}) x {passes} pass(es): hash + map + fp64 layer, {el:.1f} s"}
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle, as it stands, on this host's cores.
+
+    Each step builds the oracle's coordinate table over the whole scene and
+    computes the map and the fp64 layer for a fixed sample of output rows
+    (evenly spaced); the step's time is scaled to the whole scene as
+    t_table + (t_step - t_table) * N / rows, with t_table measured alone.
+    The sample is sized so that warm-up plus timed steps take a few minutes.
+    """
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    w, s = make_workload(args.workload, 0)
+    f, W = layer_tensors(w, s)
+    if w.dtype == "f16":
+        f = f.astype(np.float16).astype(np.float32)
+        W = W.astype(np.float16).astype(np.float32)
+    f64, W64 = f.astype(np.float64), W.astype(np.float64)
+    t_tab = []
+    for _ in range(3):
+        t0 = time.perf_counter()
+        oracle.hash_only(s.coords, s.ndim, w.K, s.dims)
+        t_tab.append(time.perf_counter() - t0)
+    t_table = statistics.median(t_tab)
+    probe = np.linspace(0, s.n - 1, min(s.n, 4000)).astype(np.int64)
+    t0 = time.perf_counter()
+    oracle.subm_conv(s.coords, f64, W64, s.ndim, w.K, s.dims, rows=probe)
+    per_row = max((time.perf_counter() - t0 - t_table) / len(probe), 1e-9)
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    k = int(max(256, min(s.n, (budget - t_table) / per_row)))
+    rows = np.linspace(0, s.n - 1, k).astype(np.int64)
+    for _ in range(args.warmup):
+        oracle.subm_conv(s.coords, f64, W64, s.ndim, w.K, s.dims, rows=rows)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.subm_conv(s.coords, f64, W64, s.ndim, w.K, s.dims, rows=rows)
+        el = time.perf_counter() - t0
+        times.append(t_table + max(el - t_table, 0.0) * s.n / k)
+    ms = 1e3 * statistics.mean(times)
+    value = s.n / (ms / 1e3) / 1e6
+    sample = (f"coordinate table over all N={s.n} + map and fp64 layer for {k} evenly spaced output rows per "
+              f"step, scaled to N")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "Mvoxels/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "N": s.n, "K": w.K, "c_in": w.channels[0], "c_out": w.channels[1]},
+        "cpu_baseline": {"value": round(value, 4), "unit": "Mvoxels/s", "cores": oracle.max_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "Mvoxels/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------- GPU --
+def run_ours(args):
+    import torch
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+    __graft_entry__.build()
+    from submanifold_sparse_convolution_hash_gb300 import binding as sc
+
+    w, s = make_workload(args.workload, rank)
+    f_np, W_np = layer_tensors(w, s)
+    tdt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[w.dtype]
+    esize = 4 if w.dtype == "f32" else 2
+    V = w.K ** s.ndim
+    c_in, c_out = w.channels[0], w.channels[1]
+    coords = torch.from_numpy(s.coords).to(dev)
+    feats = torch.from_numpy(f_np).to(tdt).to(dev)
+    Wt = torch.from_numpy(W_np).to(tdt).to(dev)
+    out = torch.empty((s.n, c_out), dtype=tdt, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    # variant chosen from measured time on this map
+    h0 = sc.sc_hash_build(coords)
+    m0 = sc.sc_kmap_build(h0, s.ndim, w.K, s.dims)
+    M = m0.map_size()
+    variant = sc.sc_subm_conv_tune(m0, feats, Wt, out=out, reps=5)
+    ntiles = (s.n + 63) // 64
+
+    def step():
+        h = sc.sc_hash_build(coords)
+        m = sc.sc_kmap_build(h, s.ndim, w.K, s.dims, sync=False)
+        sc.sc_subm_conv_fwd(m, feats, Wt, out=out, variant=variant)
+        return h, m
+
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    keep = []
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sc.profile_reset()
+    sc.profile_enable(True)
+    launches0 = sc.launch_count()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            keep.append(step())
+            ends[i].record(stream)
+            if len(keep) > 4:
+                keep.pop(0)
+        torch.cuda.synchronize()
+    launches = sc.launch_count() - launches0
+    sc.profile_enable(False)
+    prof = sc.profile_collect()
+    keep.clear()
+    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    total_s = sum(step_ms) / 1e3
+    if world > 1:
+        t = torch.tensor([total_s], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_s = float(t.item())
+        n_all = torch.tensor([s.n], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(n_all)
+        n_total = float(n_all.item())
+    else:
+        n_total = float(s.n)
+    # error status of the last map (outside the timed region)
+    h_chk, m_chk = step()
+    m_chk.check()
+    torch.cuda.synchronize()
+
+    value = n_total * args.steps / total_s / 1e6
+    ms_per_step = 1e3 * total_s / args.steps
+    flops = 2.0 * M * c_in * c_out
+    per_kernel = {}
+    for k, (n_l, tot) in prof.items():
+        per_kernel[k] = {"launches": n_l, "avg_us": round(1e3 * tot / max(n_l, 1), 3), "share": None}
+    tot_all = sum(v[1] for v in prof.values()) or 1.0
+    for k, (n_l, tot) in prof.items():
+        per_kernel[k]["share"] = round(tot / tot_all, 4)
+    conv_k = [k for k in prof if k.startswith("subm_conv")]
+    conv_ms = sum(prof[k][1] for k in conv_k) / args.steps
+    map_ms = sum(prof[k][1] for k in ("hash_insert", "kmap_probe", "kmap_scan", "kmap_fill") if k in prof) / args.steps
+    dom = max(prof, key=lambda k: prof[k][1])
+    peaks = load_peaks()
+    ab = algo_bytes(dom, s.n, V, M, c_in, c_out, esize, ntiles)
+    avg_s = prof[dom][1] / prof[dom][0] / 1e3
+    achieved = ab / avg_s / 1e9 if ab else None
+    roofline = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1) if achieved else None,
+                "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / peaks["hbm_gbs"], 4) if achieved else None,
+                "traffic": recorded_traffic(dom), "peak_source": f"{peaks['source']} hbm_gbs",
+                "algorithmic_bytes_per_launch": ab}
+    conv_roof_s = max(flops / (peaks["bf16_tflops"] * 1e12),
+                      (algo_bytes("subm_conv_fused", s.n, V, M, c_in, c_out, esize, ntiles)) / (peaks["hbm_gbs"] * 1e9))
+
+    line = {
+        "metric": METRIC, "value": round(value, 4), "unit": "Mvoxels/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": w.name, "N": s.n, "map_size": M, "K": w.K, "c_in": c_in, "c_out": c_out,
+                   "variant": variant, "l2": "flushed before every step (256 MB write, outside the events)",
+                   "kmap_sync": False, "parallelism": "replicas" if world > 1 else "single"},
+        "layer_tflops": round(flops / (conv_ms / 1e3) / 1e12, 3) if conv_ms else None,
+        "layer_ms": round(conv_ms, 5),
+        "layer_roofline_frac": round(conv_roof_s / (conv_ms / 1e3), 4) if conv_ms else None,
+        "kmap_build_ms": round(map_ms, 5),
+        "roofline": roofline,
+        "per_kernel": per_kernel,
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+    }
+
+    if not args.no_e2e and rank == 0:
+        line["e2e"] = run_e2e(args, w, s, f_np, W_np, tdt, dev, variant, world)
+    if not args.no_cpu_baseline and rank == 0:
+        line["cpu_baseline"] = cpu_oracle_run(s, w.K, feats.float().cpu().numpy(), W_np, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+def run_e2e(args, w, s, f_np, W_np, tdt, dev, variant, world):
+    """Same metric through the public calls, host buffers in and out."""
+    import torch
+    from submanifold_sparse_convolution_hash_gb300 import binding as sc
+    c_h = torch.from_numpy(s.coords).pin_memory()
+    f_h = torch.from_numpy(f_np).to(tdt).pin_memory()
+    W_h = torch.from_numpy(W_np).to(tdt).pin_memory()
+    o_h = torch.empty((s.n, W_np.shape[2]), dtype=tdt).pin_memory()
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        c = c_h.to(dev, non_blocking=True)
+        f = f_h.to(dev, non_blocking=True)
+        W = W_h.to(dev, non_blocking=True)
+        h = sc.sc_hash_build(c)
+        m = sc.sc_kmap_build(h, s.ndim, w.K, s.dims)  # default: synchronises and checks errors
+        o = sc.sc_subm_conv_fwd(m, f, W, variant=variant)
+        o_h.copy_(o, non_blocking=True)
+        return h, m
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.e2e_steps):
+        step()
+    b.record(stream)
+    b.synchronize()
+    ms = a.elapsed_time(b) / args.e2e_steps
+    bi = c_h.numel() * 4 + f_h.numel() * f_h.element_size() + W_h.numel() * W_h.element_size()
+    bo = o_h.numel() * o_h.element_size()
+    return {"value": round(s.n / (ms / 1e3) / 1e6, 4), "unit": "Mvoxels/s", "ms_per_step": round(ms, 4),
+            "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo), "steps": args.e2e_steps}
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,224 @@
+/*
+ * sc.h -- C ABI of libsc: submanifold sparse convolution on one GPU
+ * (sm_103a).  Plain pointers and sizes only; no C++ or framework types.
+ *
+ * The layer (after "Sparse inputs and sparse convolution", sections "The fix"
+ * and "The map is the computation", and the exam sheet "Sparse convolution
+ * for point clouds", sections "Submanifold sparse convolution" and "The map
+ * and the update rule"):
+ *
+ *   points   coords[i] = (batch, x, y, z), features feats[i, 0:C_in]
+ *   offsets  d in [-r, r]^ndim, r = (K-1)/2, K odd, stride 1
+ *   map      M = {(p, q, d) : coords[p] = coords[q] + d}       (P = Q + d)
+ *   layer    out[q, :] = sum_{(p, q, d) in M} feats[p, :] @ W[d]
+ *
+ * The output point set equals the input point set (P_out = P_in): out has the
+ * same N rows, in the same order, as feats.
+ *
+ * Offset index: lexicographic over (dx, dy[, dz]) with the first axis
+ * slowest, idx = sum_k (d_k + r) * K^(ndim-1-k); the centre offset is
+ * (V-1)/2 and the mirror of idx is V-1-idx, V = K^ndim.  In 2D (ndim = 2)
+ * offsets move x and y only; z is carried unchanged as part of the key.
+ *
+ * Pointers.  Arguments named d_* are device pointers (cudaMalloc'd or
+ * equivalent); the library never dereferences them on the host.  Arguments of
+ * sc_kmap_export may be device or host pointers (UVA).  All calls are
+ * asynchronous on the given stream unless stated.  Errors in the arguments
+ * are returned synchronously; no call aborts, throws or traps.
+ *
+ * Memory.  Handles own their device buffers, allocated stream-ordered
+ * (cudaMallocAsync) on the stream passed at build time and released
+ * stream-ordered on the stream passed to *_destroy.  The caller owns coords,
+ * feats, W and out.
+ */
+#ifndef SC_H_
+#define SC_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* sc_stream;
+
+typedef enum {
+  SC_OK = 0,
+  SC_ERR_INVALID_ARG = 1,     /* bad pointer, size, alignment, K, ndim, dims */
+  SC_ERR_OUT_OF_RANGE = 2,    /* a coordinate outside [0, dims) or batch outside [0, 65535) */
+  SC_ERR_DUPLICATE_COORD = 3, /* two rows share one (batch, x, y, z) */
+  SC_ERR_TABLE_FULL = 4,      /* hash insert gave up after probing every slot */
+  SC_ERR_UNSUPPORTED = 5,     /* channel counts or dtype the kernels do not cover */
+  SC_ERR_CUDA = 6,            /* a CUDA runtime call failed; see sc_last_error() */
+  SC_ERR_OOM = 7,             /* device allocation failed */
+  SC_ERR_TIMEOUT = 8          /* a bounded device-side wait gave up (kernel bug) */
+} sc_status;
+
+typedef enum { SC_F32 = 0, SC_F16 = 1, SC_BF16 = 2 } sc_dtype;
+
+/* flags for sc_subm_conv_fwd / sc_subm_conv_tune */
+#define SC_RELU 0x1u            /* max(out, 0) before the cast to the output dtype */
+#define SC_VARIANT_FUSED 0x10u  /* force the output-stationary tcgen05 kernel */
+#define SC_VARIANT_WS 0x20u     /* force the weight-stationary gather/GEMM/scatter kernels */
+#define SC_VARIANT_SIMT 0x40u   /* force the CUDA-core kernel (the only one for SC_F32) */
+#define SC_VARIANT_MASK 0x70u
+
+/* flags for sc_kmap_build */
+#define SC_KMAP_NO_SYNC 0x100u  /* do not synchronise; check errors later with sc_kmap_check */
+
+typedef struct sc_hash_s* sc_hash;
+typedef struct sc_kmap_s* sc_kmap;
+
+/* ---------------------------------------------------------------- hash -- */
+
+/*
+ * Coordinate hash table: key (batch, x, y, z) -> row id i.
+ * After "SparseConvNet: from hash table to rulebook", section 2 (each unique
+ * input coordinate gets an incremental index) and "Sparse inputs and sparse
+ * convolution", section "Gather, matmul, scatter" (the map is built on the
+ * GPU, not copied from a CPU hash).
+ *
+ * d_coords  int32 [n, 4] row-major (batch, x, y, z), 16-byte aligned.
+ *           batch in [0, 65535), x, y, z in [0, 65535).
+ * n         number of points, 0 <= n < 2^31.
+ * out       receives the handle.
+ *
+ * Open addressing, linear probing, capacity = next power of two >= 2n, keys
+ * packed into 64 bits (16 bits per field, batch highest).  Asynchronous: a
+ * duplicate or out-of-range coordinate is latched in the handle and reported
+ * by sc_hash_check, sc_kmap_build or sc_kmap_check.
+ */
+sc_status sc_hash_build(const int32_t* d_coords, int64_t n, sc_stream stream, sc_hash* out);
+
+/* Row id of each query coordinate, -1 where it is not in the table.
+ * d_query int32 [m, 4] (16-byte aligned), d_rows int32 [m]. Asynchronous. */
+sc_status sc_hash_query(sc_hash h, const int32_t* d_query, int64_t m, int32_t* d_rows, sc_stream stream);
+
+/* Number of points and table capacity (host values, no synchronisation). */
+sc_status sc_hash_info(sc_hash h, int64_t* n, int64_t* capacity);
+
+/* Synchronises the stream and returns the latched insert status. */
+sc_status sc_hash_check(sc_hash h, sc_stream stream);
+
+/* Releases the handle's buffers stream-ordered on `stream`. */
+sc_status sc_hash_destroy(sc_hash h, sc_stream stream);
+
+/* ---------------------------------------------------------- kernel map -- */
+
+/*
+ * Kernel map (rulebook) for a K^ndim submanifold convolution.
+ * After "Sparse inputs and sparse convolution", section "The map is the
+ * computation" (for each output q and offset d, look up q + d in the hash);
+ * "TorchSparse optimizations", opening section (the centre offset maps every
+ * point to itself at stride 1 and is not searched); "SparseConvNet: from hash
+ * table to rulebook", section 3 (the rulebook is grouped by weight offset).
+ *
+ * ndim      2 or 3.
+ * K         odd, K >= 1, with V = K^ndim <= 343 (K <= 7 in 3D, K <= 17 in 2D).
+ * dims      spatial extents (x, y, z), each in [1, 65535]; every point must
+ *           lie inside; neighbours outside are absent (zero padding).
+ * flags     0 or SC_KMAP_NO_SYNC.
+ *
+ * Products, owned by the handle:
+ *   nbr      int32 [n, V]: nbr[q*V + idx(d)] = row p with coords[p] =
+ *            coords[q] + d, or -1.  Column (V-1)/2 is the identity.
+ *   offs     int64 [V+1]: per-offset segments of the (in, out) lists.  The
+ *            centre segment is empty: its tuples are (i, i) for every i.
+ *   in/out   int32 [offs[V]]: list entries (p, q); within a segment ordered
+ *            by q.
+ *   map size |M| = n + offs[V] tuples, centre included.
+ *
+ * Without SC_KMAP_NO_SYNC the call synchronises the stream once and returns
+ * the hash's latched errors and its own (SC_ERR_OUT_OF_RANGE when a point
+ * lies outside dims).  With it the call is fully asynchronous and errors
+ * surface in sc_kmap_check.
+ */
+sc_status sc_kmap_build(sc_hash h, int ndim, int K, const int32_t dims[3], unsigned flags,
+                        sc_stream stream, sc_kmap* out);
+
+/* n, V and |M| (centre included).  Synchronises the stream when |M| is not
+ * yet known on the host. */
+sc_status sc_kmap_info(sc_kmap m, int64_t* n, int32_t* volume, int64_t* map_size, sc_stream stream);
+
+/* Synchronises and returns the latched hash and map status. */
+sc_status sc_kmap_check(sc_kmap m, sc_stream stream);
+
+/*
+ * Copies the products into caller buffers (device or host pointers; any may
+ * be NULL to skip): nbr int32 [n*V], offs int64 [V+1], in_rows and out_rows
+ * int32 [offs[V]].  Asynchronous for device destinations.
+ */
+sc_status sc_kmap_export(sc_kmap m, int32_t* nbr, int64_t* offs, int32_t* in_rows, int32_t* out_rows,
+                         sc_stream stream);
+
+/* Releases the handle's buffers stream-ordered on `stream`. */
+sc_status sc_kmap_destroy(sc_kmap m, sc_stream stream);
+
+/* ---------------------------------------------------------- convolution -- */
+
+/*
+ * One submanifold convolution layer on a built map:
+ *   out[q, :] = act( sum_{(p, q, d) in M} feats[p, :] @ W[d] )
+ * with fp32 accumulation and one rounding to the output dtype; act is
+ * max(., 0) with SC_RELU, else the identity.  Update rule after the exam
+ * sheet "Sparse convolution for point clouds", section "The map and the
+ * update rule", and "Sparse inputs and sparse convolution", section "The map
+ * is the computation".
+ *
+ * d_feats  [n, c_in] row-major, dtype; 16-byte aligned.
+ * d_W      [V, c_in, c_out] row-major, dtype (W[idx(d)] is the c_in x c_out
+ *          matrix of offset d); 16-byte aligned.
+ * d_out    [n, c_out] row-major, dtype; 16-byte aligned; must not alias
+ *          d_feats.  Every row is written exactly once.
+ * c_in, c_out  multiples of 16 in [16, 256].
+ * dtype    SC_F16 / SC_BF16 (tensor-core kernels) or SC_F32 (CUDA cores).
+ * flags    SC_RELU, optionally one SC_VARIANT_* to force a kernel family.
+ *
+ * The fused kernel covers V <= 125; larger kernels use the weight-stationary
+ * one.  Variant: forced by flags, else the one sc_subm_conv_tune measured fastest
+ * for (c_in, c_out, dtype) on this map, else the fused output-stationary
+ * kernel (f16/bf16) or the CUDA-core kernel (f32).  Temporary device memory
+ * (packed weights, the fp32 accumulator of the weight-stationary variant) is
+ * allocated and freed stream-ordered on `stream`.
+ */
+sc_status sc_subm_conv_fwd(sc_kmap m, const void* d_feats, const void* d_W, void* d_out, int c_in,
+                           int c_out, sc_dtype dtype, unsigned flags, sc_stream stream);
+
+/*
+ * Times every variant that supports (c_in, c_out, dtype) on this map with
+ * CUDA events (`reps` runs each after one warm-up; synchronises), caches the
+ * fastest in the handle for sc_subm_conv_fwd, and stores its SC_VARIANT_*
+ * flag in *chosen.  d_out receives the last variant's result.
+ */
+sc_status sc_subm_conv_tune(sc_kmap m, const void* d_feats, const void* d_W, void* d_out, int c_in,
+                            int c_out, sc_dtype dtype, unsigned flags, int reps, sc_stream stream,
+                            unsigned* chosen);
+
+/* ---------------------------------------------------------- diagnostics -- */
+
+const char* sc_status_str(sc_status s);
+
+/* Text of the last error raised on the calling host thread ("" if none). */
+const char* sc_last_error(void);
+
+/* Total number of kernels this library has launched in this process. */
+int64_t sc_launch_count(void);
+
+/*
+ * Per-kernel device timing.  While enabled, every launch is bracketed with a
+ * pair of CUDA events on its stream.  sc_profile_collect synchronises those
+ * events and folds them into per-kernel totals; sc_profile_get reads entry
+ * `index` (0-based; returns SC_ERR_INVALID_ARG past the end).
+ */
+void sc_profile_enable(int on);
+sc_status sc_profile_collect(void);
+void sc_profile_reset(void);
+sc_status sc_profile_get(int index, const char** name, int64_t* launches, double* total_ms);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SC_H_ */

@@ -61,6 +61,8 @@ def _load():
                                          P, ctypes.c_int]
         lib.oracle_subm_conv.restype = ctypes.c_int
         lib.oracle_max_threads.restype = ctypes.c_int
+        lib.oracle_hash_only.argtypes = [P, ctypes.c_int64, ctypes.c_int, ctypes.c_int, P]
+        lib.oracle_hash_only.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -103,6 +105,14 @@ def offset_of(idx: int, ndim: int, K: int) -> tuple:
 
 def max_threads() -> int:
     return int(_load().oracle_max_threads())
+
+
+def hash_only(coords, ndim: int, K: int, dims) -> None:
+    """Builds (and drops) the oracle's coordinate table: step 1 alone."""
+    c = _coords(coords)
+    st = _load().oracle_hash_only(_ptr(c), c.shape[0], ndim, K, _ptr(_dims(dims)))
+    if st:
+        raise OracleError(st)
 
 
 def kmap(coords, ndim: int, K: int, dims, threads: int = 0) -> np.ndarray:

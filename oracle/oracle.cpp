@@ -187,6 +187,12 @@ int oracle_subm_conv(const int32_t* coords, int64_t n, int ndim, int K, const in
   return OR_OK;
 }
 
+// Step 1 alone (the coordinate hash table), for timing the oracle's phases.
+int oracle_hash_only(const int32_t* coords, int64_t n, int ndim, int K, const int32_t* dims) {
+  Problem P;
+  return setup(P, coords, n, ndim, K, dims);
+}
+
 // Number of threads the OpenMP runtime would use by default.
 int oracle_max_threads(void) { return threads_to_use(0); }
 

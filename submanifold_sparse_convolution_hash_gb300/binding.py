@@ -1,0 +1,277 @@
+"""Thin ctypes binding over libsc (include/sc.h), with the same names.
+
+Argument marshalling only: torch tensors become device pointers, sizes and a
+stream; every step of the layer runs in libsc's CUDA kernels.  There is no
+CPU path: if libsc.so is missing, or a tensor is not on a CUDA device, the
+calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libsc.so")
+_lib = None
+
+SC_RELU = 0x1
+SC_VARIANT_FUSED = 0x10
+SC_VARIANT_WS = 0x20
+SC_VARIANT_SIMT = 0x40
+SC_KMAP_NO_SYNC = 0x100
+VARIANTS = {"fused": SC_VARIANT_FUSED, "ws": SC_VARIANT_WS, "simt": SC_VARIANT_SIMT}
+VARIANT_NAMES = {v: k for k, v in VARIANTS.items()}
+_DTYPES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+STATUS = {0: "SC_OK", 1: "SC_ERR_INVALID_ARG", 2: "SC_ERR_OUT_OF_RANGE", 3: "SC_ERR_DUPLICATE_COORD",
+          4: "SC_ERR_TABLE_FULL", 5: "SC_ERR_UNSUPPORTED", 6: "SC_ERR_CUDA", 7: "SC_ERR_OOM",
+          8: "SC_ERR_TIMEOUT"}
+
+
+class ScError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{STATUS.get(code, code)}: {msg}")
+        self.code = code
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def lib():
+    """The loaded libsc.so; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError("libsc.so is not built: run `python -m submanifold_sparse_convolution_hash_gb300.build`"
+                               " or __graft_entry__.build()")
+        L = ctypes.CDLL(_LIB_PATH)
+        P, I64, I32, U = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint
+        sig = {
+            "sc_hash_build": ([P, I64, P, P], I32),
+            "sc_hash_query": ([P, P, I64, P, P], I32),
+            "sc_hash_info": ([P, P, P], I32),
+            "sc_hash_check": ([P, P], I32),
+            "sc_hash_destroy": ([P, P], I32),
+            "sc_kmap_build": ([P, I32, I32, P, U, P, P], I32),
+            "sc_kmap_info": ([P, P, P, P, P], I32),
+            "sc_kmap_check": ([P, P], I32),
+            "sc_kmap_export": ([P, P, P, P, P, P], I32),
+            "sc_kmap_destroy": ([P, P], I32),
+            "sc_subm_conv_fwd": ([P, P, P, P, I32, I32, I32, U, P], I32),
+            "sc_subm_conv_tune": ([P, P, P, P, I32, I32, I32, U, I32, P, P], I32),
+            "sc_status_str": ([I32], ctypes.c_char_p),
+            "sc_last_error": ([], ctypes.c_char_p),
+            "sc_launch_count": ([], I64),
+            "sc_profile_enable": ([I32], None),
+            "sc_profile_collect": ([], I32),
+            "sc_profile_reset": ([], None),
+            "sc_profile_get": ([I32, P, P, P], I32),
+        }
+        for name, (args, res) in sig.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = res
+        _lib = L
+    return _lib
+
+
+def exported_symbols() -> list:
+    return [n for n in ("sc_hash_build", "sc_hash_query", "sc_hash_info", "sc_hash_check", "sc_hash_destroy",
+                        "sc_kmap_build", "sc_kmap_info", "sc_kmap_check", "sc_kmap_export", "sc_kmap_destroy",
+                        "sc_subm_conv_fwd", "sc_subm_conv_tune", "sc_status_str", "sc_last_error",
+                        "sc_launch_count", "sc_profile_enable", "sc_profile_collect", "sc_profile_reset",
+                        "sc_profile_get")]
+
+
+def _check(st: int, what: str):
+    if st != 0:
+        raise ScError(st, f"{what}: {lib().sc_last_error().decode()}")
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dev(t: torch.Tensor, name: str) -> torch.Tensor:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+class Hash:
+    """Handle of a coordinate hash table built by sc_hash_build."""
+
+    def __init__(self, handle, n: int, capacity: int, device):
+        self._h = handle
+        self.n = n
+        self.capacity = capacity
+        self.device = device
+
+    def query(self, coords: torch.Tensor, stream=None) -> torch.Tensor:
+        """Row id of each (batch, x, y, z) query, -1 when absent (sc_hash_query)."""
+        q = _dev(coords, "coords")
+        rows = torch.empty(q.shape[0], dtype=torch.int32, device=q.device)
+        _check(lib().sc_hash_query(self._h, _ptr(q), q.shape[0], _ptr(rows), _stream(stream)), "sc_hash_query")
+        return rows
+
+    def check(self, stream=None):
+        _check(lib().sc_hash_check(self._h, _stream(stream)), "sc_hash_check")
+
+    def destroy(self, stream=None):
+        if self._h:
+            lib().sc_hash_destroy(self._h, _stream(stream))
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass
+
+
+class KernelMap:
+    """Handle of a kernel map built by sc_kmap_build."""
+
+    def __init__(self, handle, n: int, ndim: int, K: int, dims, device):
+        self._h = handle
+        self.n = n
+        self.ndim = ndim
+        self.K = K
+        self.volume = K ** ndim
+        self.dims = tuple(dims)
+        self.device = device
+
+    def map_size(self, stream=None) -> int:
+        """|M|, centre tuples included (sc_kmap_info)."""
+        m = ctypes.c_int64(0)
+        _check(lib().sc_kmap_info(self._h, None, None, ctypes.byref(m), _stream(stream)), "sc_kmap_info")
+        return m.value
+
+    def check(self, stream=None):
+        _check(lib().sc_kmap_check(self._h, _stream(stream)), "sc_kmap_check")
+
+    def nbr(self, stream=None) -> torch.Tensor:
+        out = torch.empty((self.n, self.volume), dtype=torch.int32, device=self.device)
+        _check(lib().sc_kmap_export(self._h, _ptr(out), None, None, None, _stream(stream)), "sc_kmap_export")
+        return out
+
+    def offsets(self, stream=None) -> torch.Tensor:
+        out = torch.empty(self.volume + 1, dtype=torch.int64, device=self.device)
+        _check(lib().sc_kmap_export(self._h, None, _ptr(out), None, None, _stream(stream)), "sc_kmap_export")
+        return out
+
+    def lists(self, stream=None):
+        """(offs [V+1], in_rows [L], out_rows [L]) of the non-centre offsets."""
+        offs = self.offsets(stream)
+        L = self.map_size(stream) - self.n
+        i = torch.empty(max(L, 0), dtype=torch.int32, device=self.device)
+        o = torch.empty(max(L, 0), dtype=torch.int32, device=self.device)
+        _check(lib().sc_kmap_export(self._h, None, None, _ptr(i) if L else None, _ptr(o) if L else None,
+                                    _stream(stream)), "sc_kmap_export")
+        return offs, i, o
+
+    def destroy(self, stream=None):
+        if self._h:
+            lib().sc_kmap_destroy(self._h, _stream(stream))
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass
+
+
+def sc_hash_build(coords: torch.Tensor, stream=None) -> Hash:
+    """Hash table over int32 coords [N, 4] = (batch, x, y, z) on a CUDA device."""
+    c = _dev(coords, "coords")
+    if c.dtype != torch.int32 or c.dim() != 2 or c.shape[1] != 4:
+        raise ValueError("coords must be int32 [N, 4]")
+    h = ctypes.c_void_p()
+    _check(lib().sc_hash_build(_ptr(c), c.shape[0], _stream(stream), ctypes.byref(h)), "sc_hash_build")
+    n = ctypes.c_int64()
+    cap = ctypes.c_int64()
+    lib().sc_hash_info(h, ctypes.byref(n), ctypes.byref(cap))
+    return Hash(h, n.value, cap.value, c.device)
+
+
+def sc_kmap_build(h: Hash, ndim: int, K: int, dims, sync: bool = True, stream=None) -> KernelMap:
+    """Kernel map of a K^ndim submanifold convolution over the hashed points."""
+    d = (ctypes.c_int32 * 3)(*(list(dims) + [1] * (3 - len(dims))))
+    m = ctypes.c_void_p()
+    flags = 0 if sync else SC_KMAP_NO_SYNC
+    _check(lib().sc_kmap_build(h._h, ndim, K, d, flags, _stream(stream), ctypes.byref(m)), "sc_kmap_build")
+    return KernelMap(m, h.n, ndim, K, list(d), h.device)
+
+
+def _conv_args(kmap, feats, W, out):
+    f = _dev(feats, "feats")
+    w = _dev(W, "W")
+    if f.dtype not in _DTYPES or w.dtype != f.dtype:
+        raise ValueError("feats and W must share one dtype: float32, float16 or bfloat16")
+    if w.dim() != 3 or w.shape[0] != kmap.volume or f.dim() != 2 or f.shape[1] != w.shape[1] or f.shape[0] != kmap.n:
+        raise ValueError("shapes must be feats [N, C_in], W [K^ndim, C_in, C_out]")
+    c_out = w.shape[2]
+    if out is None:
+        out = torch.empty((kmap.n, c_out), dtype=f.dtype, device=f.device)
+    else:
+        _dev(out, "out")
+        if out.dtype != f.dtype or tuple(out.shape) != (kmap.n, c_out):
+            raise ValueError("out must be [N, C_out] of the feats dtype")
+    return f, w, out, f.shape[1], c_out, _DTYPES[f.dtype]
+
+
+def sc_subm_conv_fwd(kmap: KernelMap, feats: torch.Tensor, W: torch.Tensor, out: torch.Tensor | None = None,
+                     relu: bool = False, variant: str | None = None, stream=None) -> torch.Tensor:
+    """out[q] = act(sum over map tuples (p, q, d) of feats[p] @ W[d]); same rows as feats."""
+    f, w, out, c_in, c_out, dt = _conv_args(kmap, feats, W, out)
+    flags = (SC_RELU if relu else 0) | (VARIANTS[variant] if variant else 0)
+    _check(lib().sc_subm_conv_fwd(kmap._h, _ptr(f), _ptr(w), _ptr(out), c_in, c_out, dt, flags,
+                                  _stream(stream)), "sc_subm_conv_fwd")
+    return out
+
+
+def sc_subm_conv_tune(kmap: KernelMap, feats: torch.Tensor, W: torch.Tensor, out: torch.Tensor | None = None,
+                      relu: bool = False, reps: int = 3, stream=None) -> str:
+    """Times the variants on this map, caches the fastest, returns its name."""
+    f, w, out, c_in, c_out, dt = _conv_args(kmap, feats, W, out)
+    chosen = ctypes.c_uint(0)
+    _check(lib().sc_subm_conv_tune(kmap._h, _ptr(f), _ptr(w), _ptr(out), c_in, c_out, dt,
+                                   SC_RELU if relu else 0, reps, _stream(stream), ctypes.byref(chosen)),
+           "sc_subm_conv_tune")
+    return VARIANT_NAMES[chosen.value]
+
+
+def launch_count() -> int:
+    return int(lib().sc_launch_count())
+
+
+def profile_enable(on: bool = True):
+    lib().sc_profile_enable(1 if on else 0)
+
+
+def profile_reset():
+    lib().sc_profile_reset()
+
+
+def profile_collect() -> dict:
+    """{kernel name: (launches, total ms)} accumulated since the last reset."""
+    L = lib()
+    _check(L.sc_profile_collect(), "sc_profile_collect")
+    out = {}
+    i = 0
+    name = ctypes.c_char_p()
+    n = ctypes.c_int64()
+    ms = ctypes.c_double()
+    while L.sc_profile_get(i, ctypes.byref(name), ctypes.byref(n), ctypes.byref(ms)) == 0:
+        out[name.value.decode()] = (n.value, ms.value)
+        i += 1
+    return out

@@ -1,0 +1,542 @@
+// C ABI of libsc (declared in include/sc.h): argument checks, handle
+// ownership, stream-ordered allocation, variant choice, launch bookkeeping.
+// Every step of the layer runs in this library's kernels; there is no host
+// or CPU path for any of them.
+
+#include <atomic>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "sc_internal.cuh"
+
+// The opaque handle types of sc.h.
+struct sc_hash_s {
+  sc::HashTable t;
+};
+struct sc_kmap_s {
+  sc::KernelMap k;
+};
+
+namespace sc {
+
+// --------------------------------------------------------------- errors --
+namespace {
+thread_local std::string g_last_error;
+std::atomic<int64_t> g_launches{0};
+}  // namespace
+
+sc_status set_error(sc_status s, const char* msg) {
+  g_last_error = msg ? msg : "";
+  return s;
+}
+
+sc_status set_cuda_error(cudaError_t e, const char* where) {
+  std::string m = where ? where : "";
+  m += ": ";
+  m += cudaGetErrorString(e);
+  g_last_error = m;
+  return e == cudaErrorMemoryAllocation ? SC_ERR_OOM : SC_ERR_CUDA;
+}
+
+// ---------------------------------------------------------- bookkeeping --
+namespace {
+struct Pending {
+  int id;
+  cudaEvent_t a, b;
+};
+struct Profiler {
+  std::mutex mu;
+  bool on = false;
+  std::vector<std::string> names;
+  std::vector<int64_t> launches;
+  std::vector<double> ms;
+  std::vector<Pending> pending;
+  std::vector<cudaEvent_t> pool;
+  cudaEvent_t take() {
+    if (!pool.empty()) {
+      cudaEvent_t e = pool.back();
+      pool.pop_back();
+      return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+  }
+};
+Profiler& prof() {
+  static Profiler* p = new Profiler();  // never destroyed: safe at process exit
+  return *p;
+}
+}  // namespace
+
+int prof_begin(const char* name, cudaStream_t s) {
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  Profiler& P = prof();
+  if (!P.on) return -1;
+  std::lock_guard<std::mutex> lk(P.mu);
+  int id = -1;
+  for (size_t i = 0; i < P.names.size(); ++i)
+    if (P.names[i] == name) id = static_cast<int>(i);
+  if (id < 0) {
+    P.names.emplace_back(name);
+    P.launches.push_back(0);
+    P.ms.push_back(0.0);
+    id = static_cast<int>(P.names.size() - 1);
+  }
+  Pending pd{id, P.take(), nullptr};
+  cudaEventRecord(pd.a, s);
+  P.pending.push_back(pd);
+  return static_cast<int>(P.pending.size() - 1);
+}
+
+void prof_end(int token, cudaStream_t s) {
+  if (token < 0) return;
+  Profiler& P = prof();
+  std::lock_guard<std::mutex> lk(P.mu);
+  if (token >= static_cast<int>(P.pending.size())) return;
+  P.pending[token].b = P.take();
+  cudaEventRecord(P.pending[token].b, s);
+}
+
+int device_sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (!cache[dev]) {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev] = v > 0 ? v : 1;
+  }
+  return cache[dev];
+}
+
+// The device's default stream-ordered pool keeps freed blocks for reuse
+// (release threshold = unlimited) instead of trimming them at every
+// synchronisation; set once per device on first use.
+void keep_pool_memory() {
+  static bool done[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || done[dev]) return;
+  cudaMemPool_t pool;
+  if (cudaDeviceGetDefaultMemPool(&pool, dev) == cudaSuccess) {
+    uint64_t thr = ~0ull;
+    cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &thr);
+  }
+  done[dev] = true;
+}
+
+sc_status dev_alloc(void** p, size_t bytes, cudaStream_t s) {
+  *p = nullptr;
+  keep_pool_memory();
+  if (bytes == 0) bytes = 16;
+  cudaError_t e = cudaMallocAsync(p, bytes, s);
+  if (e != cudaSuccess) {
+    *p = nullptr;
+    return set_cuda_error(e, "cudaMallocAsync");
+  }
+  return SC_OK;
+}
+
+void dev_free(void* p, cudaStream_t s) {
+  if (p) cudaFreeAsync(p, s);
+}
+
+namespace {
+
+// A device (or managed) pointer with the given alignment; host memory is
+// refused: the library has no host path.
+sc_status check_dev_ptr(const void* p, size_t align, const char* what) {
+  if (!p) return set_error(SC_ERR_INVALID_ARG, (std::string(what) + " is NULL").c_str());
+  if (reinterpret_cast<uintptr_t>(p) % align)
+    return set_error(SC_ERR_INVALID_ARG, (std::string(what) + " is not 16-byte aligned").c_str());
+  cudaPointerAttributes at;
+  cudaError_t e = cudaPointerGetAttributes(&at, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return set_error(SC_ERR_INVALID_ARG, (std::string(what) + " is not a CUDA pointer").c_str());
+  }
+  if (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged)
+    return set_error(SC_ERR_INVALID_ARG, (std::string(what) + " is not device memory").c_str());
+  return SC_OK;
+}
+
+sc_status status_from_bits(int bits) {
+  if (bits & kDevErrDup) return set_error(SC_ERR_DUPLICATE_COORD, "duplicate coordinate");
+  if (bits & kDevErrRange) return set_error(SC_ERR_OUT_OF_RANGE, "coordinate out of range");
+  if (bits & kDevErrFull) return set_error(SC_ERR_TABLE_FULL, "hash table full");
+  if (bits & kDevErrTimeout) return set_error(SC_ERR_TIMEOUT, "device-side wait timed out");
+  return SC_OK;
+}
+
+// Reads the map's status words, segment offsets and weight-stationary tile
+// prefix into host mirrors; synchronises the stream.
+sc_status sync_host(KernelMap* m, cudaStream_t s) {
+  int bits[2] = {0, 0};
+  m->offs_host.assign(m->V + 1, 0);
+  m->ws_tiles_host.assign(m->V + 1, 0);
+  int64_t ms = 0;
+  cudaError_t e = cudaMemcpyAsync(bits, m->status, 2 * sizeof(int), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(m->offs_host.data(), m->offs, sizeof(int64_t) * (m->V + 1), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(m->ws_tiles_host.data(), m->ws_tiles, sizeof(int) * (m->V + 1), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&ms, m->map_size, sizeof(int64_t), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return set_cuda_error(e, "kmap synchronise");
+  m->map_size_host = ms;
+  m->host_valid = true;
+  return status_from_bits(bits[0] | bits[1]);
+}
+
+bool valid_dtype(int d) { return d == SC_F32 || d == SC_F16 || d == SC_BF16; }
+size_t dtype_bytes(sc_dtype d) { return d == SC_F32 ? 4 : 2; }
+
+sc_status check_conv_args(sc_kmap m, const void* feats, const void* W, const void* out, int c_in, int c_out,
+                          sc_dtype dtype) {
+  if (!m) return set_error(SC_ERR_INVALID_ARG, "kmap handle is NULL");
+  if (!valid_dtype(dtype)) return set_error(SC_ERR_INVALID_ARG, "unknown dtype");
+  if (c_in < 16 || c_out < 16 || c_in > 256 || c_out > 256 || c_in % 16 || c_out % 16)
+    return set_error(SC_ERR_UNSUPPORTED, "c_in and c_out must be multiples of 16 in [16, 256]");
+  sc_status st = check_dev_ptr(W, 16, "W");
+  if (st) return st;
+  if (m->k.n == 0) return SC_OK;
+  if ((st = check_dev_ptr(feats, 16, "feats"))) return st;
+  if ((st = check_dev_ptr(out, 16, "out"))) return st;
+  const size_t eb = dtype_bytes(dtype);
+  const uintptr_t f0 = reinterpret_cast<uintptr_t>(feats), f1 = f0 + m->k.n * c_in * eb;
+  const uintptr_t o0 = reinterpret_cast<uintptr_t>(out), o1 = o0 + m->k.n * c_out * eb;
+  if (f0 < o1 && o0 < f1) return set_error(SC_ERR_INVALID_ARG, "out overlaps feats");
+  return SC_OK;
+}
+
+unsigned default_variant(KernelMap* m, const ConvArgs& a) {
+  if (a.dtype == SC_F32) return SC_VARIANT_SIMT;
+  for (const ConvChoice& c : m->tuned)
+    if (c.c_in == a.c_in && c.c_out == a.c_out && c.dtype == a.dtype) return c.variant;
+  return fused_supported(a) ? SC_VARIANT_FUSED : SC_VARIANT_WS;
+}
+
+sc_status run_variant(KernelMap* m, const ConvArgs& a, unsigned variant) {
+  if (a.dtype == SC_F32 && variant != SC_VARIANT_SIMT)
+    return set_error(SC_ERR_UNSUPPORTED, "fp32 layers run on the CUDA-core kernel only");
+  switch (variant) {
+    case SC_VARIANT_FUSED:
+      return conv_fused(a);
+    case SC_VARIANT_WS:
+      if (!m->host_valid) {
+        sc_status st = sync_host(m, a.stream);
+        if (st) return st;
+      }
+      return conv_weight_stationary(a);
+    case SC_VARIANT_SIMT:
+      return conv_simt(a);
+  }
+  return set_error(SC_ERR_INVALID_ARG, "more than one variant flag");
+}
+
+}  // namespace
+}  // namespace sc
+
+using namespace sc;
+
+extern "C" {
+
+const char* sc_status_str(sc_status s) {
+  switch (s) {
+    case SC_OK: return "ok";
+    case SC_ERR_INVALID_ARG: return "invalid argument";
+    case SC_ERR_OUT_OF_RANGE: return "coordinate out of range";
+    case SC_ERR_DUPLICATE_COORD: return "duplicate coordinate";
+    case SC_ERR_TABLE_FULL: return "hash table full";
+    case SC_ERR_UNSUPPORTED: return "unsupported configuration";
+    case SC_ERR_CUDA: return "CUDA error";
+    case SC_ERR_OOM: return "out of device memory";
+    case SC_ERR_TIMEOUT: return "device-side wait timed out";
+  }
+  return "unknown status";
+}
+
+const char* sc_last_error(void) { return g_last_error.c_str(); }
+
+int64_t sc_launch_count(void) { return g_launches.load(); }
+
+void sc_profile_enable(int on) { prof().on = on != 0; }
+
+sc_status sc_profile_collect(void) {
+  Profiler& P = prof();
+  std::lock_guard<std::mutex> lk(P.mu);
+  for (Pending& pd : P.pending) {
+    if (pd.b) {
+      cudaError_t e = cudaEventSynchronize(pd.b);
+      if (e != cudaSuccess) return set_cuda_error(e, "profile event");
+      float ms = 0.f;
+      cudaEventElapsedTime(&ms, pd.a, pd.b);
+      P.ms[pd.id] += ms;
+      P.launches[pd.id] += 1;
+      P.pool.push_back(pd.b);
+    }
+    P.pool.push_back(pd.a);
+  }
+  P.pending.clear();
+  return SC_OK;
+}
+
+void sc_profile_reset(void) {
+  Profiler& P = prof();
+  std::lock_guard<std::mutex> lk(P.mu);
+  for (size_t i = 0; i < P.ms.size(); ++i) {
+    P.ms[i] = 0.0;
+    P.launches[i] = 0;
+  }
+}
+
+sc_status sc_profile_get(int index, const char** name, int64_t* launches, double* total_ms) {
+  Profiler& P = prof();
+  std::lock_guard<std::mutex> lk(P.mu);
+  if (index < 0 || index >= static_cast<int>(P.names.size())) return SC_ERR_INVALID_ARG;
+  if (name) *name = P.names[index].c_str();
+  if (launches) *launches = P.launches[index];
+  if (total_ms) *total_ms = P.ms[index];
+  return SC_OK;
+}
+
+// ------------------------------------------------------------------ hash --
+sc_status sc_hash_build(const int32_t* d_coords, int64_t n, sc_stream stream, sc_hash* out) {
+  if (!out) return set_error(SC_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (n < 0 || n >= (int64_t(1) << 31)) return set_error(SC_ERR_INVALID_ARG, "n must be in [0, 2^31)");
+  if (n > 0) {
+    sc_status st = check_dev_ptr(d_coords, 16, "coords");
+    if (st) return st;
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  sc_hash h = new sc_hash_s();
+  HashTable& t = h->t;
+  t.n = n;
+  int64_t cap = 16;
+  while (cap < 2 * n) cap <<= 1;
+  t.capacity = cap;
+  sc_status st = dev_alloc(reinterpret_cast<void**>(&t.table), sizeof(Slot) * cap, s);
+  if (!st) st = dev_alloc(reinterpret_cast<void**>(&t.keys), sizeof(unsigned long long) * (n > 0 ? n : 1), s);
+  if (!st) st = dev_alloc(reinterpret_cast<void**>(&t.status), sizeof(int) * 4, s);
+  if (!st) st = launch_hash_insert(d_coords, n, &t, s);
+  if (st) {
+    sc_hash_destroy(h, stream);
+    return st;
+  }
+  *out = h;
+  return SC_OK;
+}
+
+sc_status sc_hash_query(sc_hash h, const int32_t* d_query, int64_t m, int32_t* d_rows, sc_stream stream) {
+  if (!h || m < 0) return set_error(SC_ERR_INVALID_ARG, "bad hash handle or size");
+  if (m == 0) return SC_OK;
+  sc_status st = check_dev_ptr(d_query, 16, "query");
+  if (!st) st = check_dev_ptr(d_rows, 4, "rows");
+  if (st) return st;
+  return launch_hash_query(&h->t, d_query, m, d_rows, reinterpret_cast<cudaStream_t>(stream));
+}
+
+sc_status sc_hash_info(sc_hash h, int64_t* n, int64_t* capacity) {
+  if (!h) return set_error(SC_ERR_INVALID_ARG, "hash handle is NULL");
+  if (n) *n = h->t.n;
+  if (capacity) *capacity = h->t.capacity;
+  return SC_OK;
+}
+
+sc_status sc_hash_check(sc_hash h, sc_stream stream) {
+  if (!h) return set_error(SC_ERR_INVALID_ARG, "hash handle is NULL");
+  int bits = 0;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(&bits, h->t.status, sizeof(int), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return set_cuda_error(e, "hash check");
+  return status_from_bits(bits);
+}
+
+sc_status sc_hash_destroy(sc_hash h, sc_stream stream) {
+  if (!h) return SC_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  dev_free(h->t.table, s);
+  dev_free(h->t.keys, s);
+  dev_free(h->t.status, s);
+  delete h;
+  return SC_OK;
+}
+
+// ------------------------------------------------------------------- map --
+sc_status sc_kmap_destroy(sc_kmap m, sc_stream stream) {
+  if (!m) return SC_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  KernelMap& k = m->k;
+  for (void* p : {static_cast<void*>(k.nbr), static_cast<void*>(k.offs), static_cast<void*>(k.in_rows),
+                  static_cast<void*>(k.out_rows), static_cast<void*>(k.counts), static_cast<void*>(k.totals),
+                  static_cast<void*>(k.ws_tiles), static_cast<void*>(k.map_size), static_cast<void*>(k.status)})
+    dev_free(p, s);
+  delete m;
+  return SC_OK;
+}
+
+sc_status sc_kmap_build(sc_hash h, int ndim, int K, const int32_t dims[3], unsigned flags, sc_stream stream,
+                        sc_kmap* out) {
+  if (!out) return set_error(SC_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (!h) return set_error(SC_ERR_INVALID_ARG, "hash handle is NULL");
+  if (ndim != 2 && ndim != 3) return set_error(SC_ERR_INVALID_ARG, "ndim must be 2 or 3");
+  if (K < 1 || K % 2 == 0) return set_error(SC_ERR_INVALID_ARG, "K must be odd and >= 1");
+  int V = 1;
+  for (int a = 0; a < ndim; ++a) {
+    V *= K;
+    if (V > 343) return set_error(SC_ERR_UNSUPPORTED, "K^ndim must be <= 343");
+  }
+  if (!dims) return set_error(SC_ERR_INVALID_ARG, "dims is NULL");
+  for (int a = 0; a < 3; ++a)
+    if (dims[a] < 1 || dims[a] > 65535) return set_error(SC_ERR_INVALID_ARG, "dims must be in [1, 65535]");
+  if (flags & ~SC_KMAP_NO_SYNC) return set_error(SC_ERR_INVALID_ARG, "unknown kmap flag");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  sc_kmap m = new sc_kmap_s();
+  KernelMap& k = m->k;
+  k.n = h->t.n;
+  k.ndim = ndim;
+  k.K = K;
+  k.V = V;
+  for (int a = 0; a < 3; ++a) k.dims[a] = dims[a];
+  const int tile = kmap_probe_tile();
+  k.ntiles = static_cast<int>((k.n + tile - 1) / tile);
+  const size_t nV = static_cast<size_t>(k.n) * V;
+  const size_t lists = static_cast<size_t>(k.n) * (V - 1);
+  sc_status st = dev_alloc(reinterpret_cast<void**>(&k.nbr), sizeof(int) * nV, s);
+  if (!st) st = dev_alloc(reinterpret_cast<void**>(&k.offs), sizeof(int64_t) * (V + 1), s);
+  if (!st) st = dev_alloc(reinterpret_cast<void**>(&k.in_rows), sizeof(int) * lists, s);
+  if (!st) st = dev_alloc(reinterpret_cast<void**>(&k.out_rows), sizeof(int) * lists, s);
+  if (!st) st = dev_alloc(reinterpret_cast<void**>(&k.counts), sizeof(int) * static_cast<size_t>(V) * k.ntiles, s);
+  if (!st) st = dev_alloc(reinterpret_cast<void**>(&k.totals), sizeof(int) * V, s);
+  if (!st) st = dev_alloc(reinterpret_cast<void**>(&k.ws_tiles), sizeof(int) * (V + 1), s);
+  if (!st) st = dev_alloc(reinterpret_cast<void**>(&k.map_size), sizeof(int64_t), s);
+  if (!st) st = dev_alloc(reinterpret_cast<void**>(&k.status), sizeof(int) * 4, s);
+  // status[1] carries the hash's latched insert status from here on
+  if (!st) {
+    cudaError_t e = cudaMemcpyAsync(k.status + 1, h->t.status, sizeof(int), cudaMemcpyDeviceToDevice, s);
+    if (e != cudaSuccess) st = set_cuda_error(e, "copy hash status");
+  }
+  if (!st) st = launch_kmap_build(&h->t, &k, s);
+  if (!st && !(flags & SC_KMAP_NO_SYNC)) st = sync_host(&k, s);
+  if (st) {
+    sc_kmap_destroy(m, stream);
+    return st;
+  }
+  *out = m;
+  return SC_OK;
+}
+
+sc_status sc_kmap_info(sc_kmap m, int64_t* n, int32_t* volume, int64_t* map_size, sc_stream stream) {
+  if (!m) return set_error(SC_ERR_INVALID_ARG, "kmap handle is NULL");
+  if (n) *n = m->k.n;
+  if (volume) *volume = m->k.V;
+  if (map_size) {
+    if (!m->k.host_valid) {
+      sc_status st = sync_host(&m->k, reinterpret_cast<cudaStream_t>(stream));
+      if (st) return st;
+    }
+    *map_size = m->k.map_size_host;
+  }
+  return SC_OK;
+}
+
+sc_status sc_kmap_check(sc_kmap m, sc_stream stream) {
+  if (!m) return set_error(SC_ERR_INVALID_ARG, "kmap handle is NULL");
+  return sync_host(&m->k, reinterpret_cast<cudaStream_t>(stream));
+}
+
+sc_status sc_kmap_export(sc_kmap m, int32_t* nbr, int64_t* offs, int32_t* in_rows, int32_t* out_rows,
+                         sc_stream stream) {
+  if (!m) return set_error(SC_ERR_INVALID_ARG, "kmap handle is NULL");
+  KernelMap& k = m->k;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if ((in_rows || out_rows) && !k.host_valid) {
+    sc_status st = sync_host(&k, s);
+    if (st) return st;
+  }
+  cudaError_t e = cudaSuccess;
+  if (nbr && k.n) e = cudaMemcpyAsync(nbr, k.nbr, sizeof(int) * k.n * k.V, cudaMemcpyDefault, s);
+  if (e == cudaSuccess && offs) e = cudaMemcpyAsync(offs, k.offs, sizeof(int64_t) * (k.V + 1), cudaMemcpyDefault, s);
+  const int64_t L = k.host_valid ? k.offs_host[k.V] : 0;
+  if (e == cudaSuccess && in_rows && L) e = cudaMemcpyAsync(in_rows, k.in_rows, sizeof(int) * L, cudaMemcpyDefault, s);
+  if (e == cudaSuccess && out_rows && L)
+    e = cudaMemcpyAsync(out_rows, k.out_rows, sizeof(int) * L, cudaMemcpyDefault, s);
+  return e == cudaSuccess ? SC_OK : set_cuda_error(e, "kmap export");
+}
+
+// ----------------------------------------------------------- convolution --
+sc_status sc_subm_conv_fwd(sc_kmap m, const void* d_feats, const void* d_W, void* d_out, int c_in, int c_out,
+                           sc_dtype dtype, unsigned flags, sc_stream stream) {
+  sc_status st = check_conv_args(m, d_feats, d_W, d_out, c_in, c_out, dtype);
+  if (st) return st;
+  if (flags & ~(SC_RELU | SC_VARIANT_MASK)) return set_error(SC_ERR_INVALID_ARG, "unknown conv flag");
+  ConvArgs a{&m->k, d_feats, d_W, d_out, c_in, c_out, dtype, (flags & SC_RELU) != 0,
+             reinterpret_cast<cudaStream_t>(stream)};
+  unsigned variant = flags & SC_VARIANT_MASK;
+  if (!variant) variant = default_variant(&m->k, a);
+  return run_variant(&m->k, a, variant);
+}
+
+sc_status sc_subm_conv_tune(sc_kmap m, const void* d_feats, const void* d_W, void* d_out, int c_in, int c_out,
+                            sc_dtype dtype, unsigned flags, int reps, sc_stream stream, unsigned* chosen) {
+  sc_status st = check_conv_args(m, d_feats, d_W, d_out, c_in, c_out, dtype);
+  if (st) return st;
+  if (flags & ~SC_RELU) return set_error(SC_ERR_INVALID_ARG, "tune takes SC_RELU only");
+  if (reps < 1) reps = 1;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  ConvArgs a{&m->k, d_feats, d_W, d_out, c_in, c_out, dtype, (flags & SC_RELU) != 0, s};
+  std::vector<unsigned> cands;
+  if (dtype == SC_F32) {
+    cands.push_back(SC_VARIANT_SIMT);
+  } else {
+    if (fused_supported(a)) cands.push_back(SC_VARIANT_FUSED);
+    cands.push_back(SC_VARIANT_WS);
+  }
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  cudaEventCreate(&e0);
+  cudaEventCreate(&e1);
+  unsigned best = cands[0];
+  float best_ms = 1e30f;
+  for (unsigned v : cands) {
+    st = run_variant(&m->k, a, v);  // warm-up
+    if (st) break;
+    cudaEventRecord(e0, s);
+    for (int r = 0; r < reps && !st; ++r) st = run_variant(&m->k, a, v);
+    cudaEventRecord(e1, s);
+    if (st) break;
+    cudaError_t e = cudaEventSynchronize(e1);
+    if (e != cudaSuccess) {
+      st = set_cuda_error(e, "tune timing");
+      break;
+    }
+    float ms = 0.f;
+    cudaEventElapsedTime(&ms, e0, e1);
+    if (ms < best_ms) {
+      best_ms = ms;
+      best = v;
+    }
+  }
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  if (st) return st;
+  bool found = false;
+  for (ConvChoice& c : m->k.tuned)
+    if (c.c_in == c_in && c.c_out == c_out && c.dtype == dtype) {
+      c.variant = best;
+      found = true;
+    }
+  if (!found) m->k.tuned.push_back({c_in, c_out, static_cast<int>(dtype), best});
+  if (chosen) *chosen = best;
+  // leave d_out holding the chosen variant's result
+  return run_variant(&m->k, a, best);
+}
+
+}  // extern "C"

@@ -1,0 +1,630 @@
+// Tensor-core (tcgen05) submanifold convolution kernels for sm_103a.
+//
+// Update rule: out[q] += feats[p] @ W[d] for every tuple (p, q, d) of the map
+// (exam sheet "Sparse convolution for point clouds", "The map and the update
+// rule"; "Sparse inputs and sparse convolution", "The map is the computation").
+//
+// Two dataflows share one CTA mainloop:
+//
+//  * Output-stationary implicit GEMM ("TorchSparse optimizations", section
+//    "TorchSparse++": each block owns a tile of output rows, walks the
+//    weights, fetches the matching input rows on demand and writes each
+//    output once).  A CTA owns 128 output rows.  Its K dimension is the
+//    concatenation over offsets d of the C_in input channels; an offset with
+//    no neighbour in any of the 128 rows is skipped for the whole tile
+//    (the lockstep redundancy of that section is what remains).  Absent
+//    neighbours are zero rows (cp.async with source size 0).
+//
+//  * Weight-stationary gather -> GEMM -> scatter ("Sparse inputs and sparse
+//    convolution", section "Gather, matmul, scatter"; "TorchSparse
+//    optimizations", opening section).  A CTA owns 128 tuples of one offset,
+//    gathers their input rows, multiplies by W[d] and scatter-adds fp32
+//    results with vector atomics.  The centre offset (identity map) writes its
+//    product with plain stores first.
+//
+// CTA layout (160 threads):
+//   warps 0-3  gather A rows with cp.async into a 128B/64B/32B-swizzled
+//              K-major tile, then run the epilogue (TMEM lane = row).
+//   warp 4     allocates TMEM; lane 0 issues tcgen05.mma (M=128, N=C_out,
+//              K=16) from shared-memory descriptors and commits each stage
+//              back to the producers.
+// W slices arrive by cp.async.bulk from a pre-swizzled image in global memory
+// (one image per (offset, 16/32/64-channel panel)), so A and B share one
+// K-major layout.  Accumulators live in TMEM (C_out fp32 columns).
+//
+// Every mbarrier wait is bounded (about two seconds of %globaltimer); on
+// expiry the CTA latches kDevErrTimeout, stops, and still frees its TMEM.
+
+#include "sc_internal.cuh"
+
+namespace sc {
+namespace {
+
+constexpr int kRows = 128;        // rows per CTA tile (MMA M)
+constexpr int kThreads = 160;     // 4 producer/epilogue warps + 1 MMA warp
+constexpr int kLag = 2;           // cp.async groups kept in flight per producer thread
+constexpr int kMaxStages = 6;
+constexpr unsigned long long kWaitNs = 2000000000ull;
+
+enum Mode { kOutputStationary = 0, kWsScatter = 1, kWsCentre = 2 };
+
+// ------------------------------------------------------------ PTX helpers --
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for the phase of `parity` to complete; false on timeout/abort.
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  for (uint32_t it = 1; it < (1u << 30); ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer() - t0 > kWaitNs) return false;
+    }
+  }
+  return false;
+}
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+// 16 consecutive fp32 columns of this thread's TMEM lane; waits for the load.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor for a K-major, swizzled operand: rows of
+// `row_bytes` (= the swizzle width) stacked densely, 8-row groups `8*row_bytes`
+// apart (stride byte offset); leading byte offset unused; version 1.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t sbo_bytes, uint32_t layout) {
+  uint64_t d = static_cast<uint64_t>((addr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>(1) << 16;
+  d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(layout) << 61;
+  return d;
+}
+// Instruction descriptor, kind::f16: fp32 accumulator, A and B of one type
+// (f16 or bf16), both K-major, M and N as given.
+__host__ __device__ constexpr uint32_t make_idesc(bool bf16, int M, int N) {
+  return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Swizzle of 16-byte chunk positions inside a row of the K-major tile:
+// address bits [4, 4+b) XOR bits [7, 7+b) with row pitch = swizzle width.
+template <int BK>
+__host__ __device__ __forceinline__ int swz(int row) {
+  if constexpr (BK == 64) return row & 7;          // 128-byte rows
+  else if constexpr (BK == 32) return (row >> 1) & 3;  // 64-byte rows
+  else return (row >> 2) & 1;                      // 32-byte rows
+}
+template <int BK>
+constexpr uint32_t layout_code() {
+  return BK == 64 ? 2u : (BK == 32 ? 4u : 6u);  // SWIZZLE_128B / 64B / 32B
+}
+
+struct TcParams {
+  const uint8_t* feats;      // [n, c_in] 2-byte elements
+  const uint8_t* wimg;       // packed weight images [V][P][c_out rows][BK*2 bytes]
+  uint8_t* out;              // output-stationary: [n, c_out] 2-byte elements
+  float* acc;                // weight-stationary: fp32 [n, c_out]
+  const int* nbr;            // [n, V]
+  const int* in_rows;        // weight-stationary lists
+  const int* out_rows;
+  const int64_t* offs;       // [V+1]
+  const int* ws_tiles;       // [V+1]
+  int64_t n;
+  int V, c_in, c_out, relu, stages, tmem_cols;
+  int* status;
+};
+
+__device__ __forceinline__ int next_present(const uint32_t* mask, int v, int V) {
+  for (int u = v + 1; u < V; ++u)
+    if (mask[u >> 5] & (1u << (u & 31))) return u;
+  return V;
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  if constexpr (BF16) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  } else {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+}
+
+template <int BK, int MODE, bool BF16>
+__global__ void __launch_bounds__(kThreads) k_conv_tc(const TcParams p) {
+  constexpr int ROWB = BK * 2;        // bytes per tile row (= swizzle width)
+  constexpr int CPR = ROWB / 16;      // 16-byte chunks per row
+  constexpr int A_BYTES = kRows * ROWB;
+  constexpr uint32_t LAYOUT = layout_code<BK>();
+  constexpr uint32_t SBO = 8 * ROWB;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int S = p.stages;
+  const int B_BYTES = p.c_out * ROWB;
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + S * A_BYTES;
+  int* sRows = reinterpret_cast<int*>(sB + S * B_BYTES);
+  const int rows_ints = MODE == kOutputStationary ? kRows * p.V : 2 * kRows;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sRows + ((rows_ints + 1) & ~1));
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2 * S + 1);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+  uint32_t* s_mask = s_tmem + 2;  // up to 4 words: offsets present in the tile
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int P = p.c_in / BK;
+  const int V = p.V;
+  const int centre = (V - 1) / 2;
+
+  // ---- tile bounds
+  int64_t row0 = 0, lb = 0;
+  int nrows = 0, v_ws = centre;
+  if (MODE == kWsScatter) {
+    int lo = 0, hi = V;  // largest v with ws_tiles[v] <= blockIdx.x
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (__ldg(p.ws_tiles + mid) <= static_cast<int>(blockIdx.x)) lo = mid; else hi = mid;
+    }
+    v_ws = lo;
+    const int64_t seg_end = __ldg(p.offs + v_ws + 1);
+    lb = __ldg(p.offs + v_ws) + static_cast<int64_t>(blockIdx.x - __ldg(p.ws_tiles + v_ws)) * kRows;
+    nrows = static_cast<int>(min(static_cast<int64_t>(kRows), seg_end - lb));
+  } else {
+    row0 = static_cast<int64_t>(blockIdx.x) * kRows;
+    nrows = static_cast<int>(min(static_cast<int64_t>(kRows), p.n - row0));
+  }
+
+  // ---- setup: barriers, TMEM, rows of the tile
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S), accum_bar = smem_u32(bars + 2 * S);
+  if (threadIdx.x == 128) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full0 + 8 * s, 5);   // 4 producer warps + the expect_tx arrival
+      mbar_init(empty0 + 8 * s, 1);  // one tcgen05.commit
+    }
+    mbar_init(accum_bar, 1);
+    *s_abort = 0;
+    s_mask[0] = s_mask[1] = s_mask[2] = s_mask[3] = 0;
+    fence_mbar_init();
+  }
+  if (warp == 4) {
+    tmem_alloc(smem_u32(s_tmem), static_cast<uint32_t>(p.tmem_cols));
+    tmem_relinquish();
+  }
+  if (threadIdx.x < kRows) {
+    if (MODE == kOutputStationary) {
+      const int valid = nrows * V;
+      const int* src = p.nbr + row0 * V;
+      for (int e = threadIdx.x; e < kRows * V; e += kRows) sRows[e] = e < valid ? __ldg(src + e) : -1;
+    } else if (MODE == kWsScatter) {
+      const int r = threadIdx.x;
+      sRows[r] = r < nrows ? __ldg(p.in_rows + lb + r) : -1;
+      sRows[kRows + r] = r < nrows ? __ldg(p.out_rows + lb + r) : -1;
+    } else {
+      const int r = threadIdx.x;
+      sRows[r] = r < nrows ? static_cast<int>(row0 + r) : -1;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+
+  int nkb;
+  int v_first;
+  if (MODE == kOutputStationary) {
+    if (warp < 4) {
+      for (int v = warp; v < V; v += 4) {
+        bool any = false;
+        for (int r = lane; r < kRows; r += 32) any |= sRows[r * V + v] >= 0;
+        if (__any_sync(0xffffffffu, any) && lane == 0) atomicOr(&s_mask[v >> 5], 1u << (v & 31));
+      }
+    }
+    __syncthreads();
+    nkb = (__popc(s_mask[0]) + __popc(s_mask[1]) + __popc(s_mask[2]) + __popc(s_mask[3])) * P;
+    v_first = next_present(s_mask, -1, V);
+  } else {
+    nkb = P;
+    v_first = v_ws;
+  }
+
+  if (warp < 4) {
+    // ================= producers: gather A rows, request B slices
+    int v = v_first, pnl = 0;
+    bool ok = true;
+    for (int i = 0; i < nkb; ++i) {
+      const int s = i % S;
+      const uint32_t ph = static_cast<uint32_t>(i / S) & 1u;
+      if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, s_abort)) {
+        ok = false;
+        break;
+      }
+      if (threadIdx.x == 0) {
+        mbar_arrive_expect_tx(full0 + 8 * s, static_cast<uint32_t>(B_BYTES));
+        bulk_g2s(smem_u32(sB + s * B_BYTES), p.wimg + (static_cast<size_t>(v) * P + pnl) * B_BYTES,
+                 static_cast<uint32_t>(B_BYTES), full0 + 8 * s);
+      }
+      const uint32_t a_base = smem_u32(sA + s * A_BYTES);
+#pragma unroll
+      for (int k = 0; k < CPR; ++k) {
+        const int e = threadIdx.x + kRows * k;
+        const int r = e / CPR, c = e % CPR;
+        const int j = MODE == kOutputStationary ? sRows[r * V + v] : sRows[r];
+        const uint8_t* src =
+            p.feats + (static_cast<size_t>(j < 0 ? 0 : j) * p.c_in + static_cast<size_t>(pnl) * BK) * 2 + c * 16;
+        cp_async_16(a_base + r * ROWB + ((c ^ swz<BK>(r)) << 4), src, j >= 0 ? 16u : 0u);
+      }
+      cp_async_commit();
+      if (i >= kLag) {
+        cp_async_wait<kLag>();
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(full0 + 8 * ((i - kLag) % S));
+      }
+      if (++pnl == P) {
+        pnl = 0;
+        v = MODE == kOutputStationary ? next_present(s_mask, v, V) : v;
+      }
+    }
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (ok && lane == 0)
+      for (int i = (nkb > kLag ? nkb - kLag : 0); i < nkb; ++i) mbar_arrive(full0 + 8 * (i % S));
+    if (!ok) *s_abort = 1;
+
+    // ================= epilogue: TMEM lane (warp*32 + lane) holds tile row r
+    const bool done = ok && mbar_wait(accum_bar, 0, s_abort);
+    tc_fence_after();
+    const int r = warp * 32 + lane;
+    const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    for (int c0 = 0; c0 < p.c_out; c0 += 16) {
+      float acc[16];
+      tmem_ld16(trow + static_cast<uint32_t>(c0), acc);
+      if (!done || r >= nrows) continue;
+      if (MODE == kOutputStationary) {
+        if (p.relu) {
+#pragma unroll
+          for (int k = 0; k < 16; ++k) acc[k] = fmaxf(acc[k], 0.0f);
+        }
+        uint4 lo, hi;
+        lo.x = pack2<BF16>(acc[0], acc[1]);
+        lo.y = pack2<BF16>(acc[2], acc[3]);
+        lo.z = pack2<BF16>(acc[4], acc[5]);
+        lo.w = pack2<BF16>(acc[6], acc[7]);
+        hi.x = pack2<BF16>(acc[8], acc[9]);
+        hi.y = pack2<BF16>(acc[10], acc[11]);
+        hi.z = pack2<BF16>(acc[12], acc[13]);
+        hi.w = pack2<BF16>(acc[14], acc[15]);
+        uint4* dst = reinterpret_cast<uint4*>(p.out + ((row0 + r) * p.c_out + c0) * 2);
+        dst[0] = lo;
+        dst[1] = hi;
+      } else if (MODE == kWsScatter) {
+        float4* dst = reinterpret_cast<float4*>(p.acc + static_cast<int64_t>(sRows[kRows + r]) * p.c_out + c0);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) atomicAdd(dst + k, make_float4(acc[4 * k], acc[4 * k + 1], acc[4 * k + 2], acc[4 * k + 3]));
+      } else {
+        float4* dst = reinterpret_cast<float4*>(p.acc + (row0 + r) * p.c_out + c0);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) dst[k] = make_float4(acc[4 * k], acc[4 * k + 1], acc[4 * k + 2], acc[4 * k + 3]);
+      }
+    }
+    if (!done) *s_abort = 1;
+  } else {
+    // ================= MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = make_idesc(BF16, kRows, p.c_out);
+      for (int i = 0; i < nkb; ++i) {
+        const int s = i % S;
+        const uint32_t ph = static_cast<uint32_t>(i / S) & 1u;
+        if (!mbar_wait(full0 + 8 * s, ph, s_abort)) {
+          *s_abort = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a_addr = smem_u32(sA + s * A_BYTES);
+        const uint32_t b_addr = smem_u32(sB + s * B_BYTES);
+#pragma unroll
+        for (int k = 0; k < BK / 16; ++k)
+          tc_mma(tmem, smem_desc(a_addr + 32 * k, SBO, LAYOUT), smem_desc(b_addr + 32 * k, SBO, LAYOUT), idesc,
+                 (i | k) != 0 ? 1u : 0u);
+        tc_commit(empty0 + 8 * s);
+      }
+      tc_commit(accum_bar);  // arrives once every MMA issued above has completed
+    }
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 4) {
+    tc_fence_after();
+    tmem_dealloc(tmem, static_cast<uint32_t>(p.tmem_cols));
+  }
+  if (threadIdx.x == 0 && *s_abort) atomicOr(p.status, kDevErrTimeout);
+}
+
+// W [V, c_in, c_out] -> per (offset, panel) image of c_out rows x BK channels,
+// K-major, chunk-swizzled exactly as the kernel's shared-memory B tile.
+template <int BK>
+__global__ void __launch_bounds__(256) k_pack_weights(const uint16_t* __restrict__ W, uint8_t* __restrict__ img,
+                                                      int V, int c_in, int c_out) {
+  constexpr int ROWB = BK * 2, CPR = ROWB / 16;
+  const int P = c_in / BK;
+  const int64_t total = static_cast<int64_t>(V) * P * c_out * CPR;
+  for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int c = static_cast<int>(idx % CPR);
+    const int co = static_cast<int>((idx / CPR) % c_out);
+    const int64_t vp = idx / (static_cast<int64_t>(CPR) * c_out);
+    const int pnl = static_cast<int>(vp % P);
+    const int v = static_cast<int>(vp / P);
+    uint16_t e[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int ci = pnl * BK + c * 8 + k;
+      e[k] = __ldg(W + (static_cast<int64_t>(v) * c_in + ci) * c_out + co);
+    }
+    uint4 w;
+    w.x = e[0] | (static_cast<uint32_t>(e[1]) << 16);
+    w.y = e[2] | (static_cast<uint32_t>(e[3]) << 16);
+    w.z = e[4] | (static_cast<uint32_t>(e[5]) << 16);
+    w.w = e[6] | (static_cast<uint32_t>(e[7]) << 16);
+    *reinterpret_cast<uint4*>(img + vp * (static_cast<int64_t>(c_out) * ROWB) + static_cast<int64_t>(co) * ROWB +
+                              ((c ^ swz<BK>(co)) << 4)) = w;
+  }
+}
+
+// fp32 accumulator -> output dtype (optional ReLU), 4 values per thread step.
+template <bool BF16>
+__global__ void __launch_bounds__(256) k_cast_out(const float4* __restrict__ acc, uint2* __restrict__ out, int64_t n4,
+                                                  int relu) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    float4 a = __ldg(acc + i);
+    if (relu) {
+      a.x = fmaxf(a.x, 0.f);
+      a.y = fmaxf(a.y, 0.f);
+      a.z = fmaxf(a.z, 0.f);
+      a.w = fmaxf(a.w, 0.f);
+    }
+    out[i] = make_uint2(pack2<BF16>(a.x, a.y), pack2<BF16>(a.z, a.w));
+  }
+}
+
+// ------------------------------------------------------------ host side --
+struct Plan {
+  int bk;
+  int stages;
+  size_t smem;
+  int tmem_cols;
+};
+
+int pick_bk(int c_in) { return c_in % 64 == 0 ? 64 : (c_in % 32 == 0 ? 32 : 16); }
+
+bool make_plan(int mode, int V, int c_in, int c_out, Plan* pl) {
+  pl->bk = pick_bk(c_in);
+  const size_t a = static_cast<size_t>(kRows) * pl->bk * 2;
+  const size_t b = static_cast<size_t>(c_out) * pl->bk * 2;
+  const size_t rows = sizeof(int) * ((mode == kOutputStationary ? static_cast<size_t>(kRows) * V : 2 * kRows) + 1);
+  const size_t fixed = 1024 /*alignment slack*/ + 8 * (2 * kMaxStages + 1) + 64;
+  const size_t budget = 220 * 1024;
+  if (rows + fixed + 3 * (a + b) > budget) return false;
+  int s = static_cast<int>((budget - rows - fixed) / (a + b));
+  if (s > 4) s = 4;
+  pl->stages = s;
+  pl->smem = fixed + rows + s * (a + b);
+  int cols = 32;
+  while (cols < c_out) cols <<= 1;
+  pl->tmem_cols = cols;
+  return true;
+}
+
+template <int BK, int MODE, bool BF16>
+sc_status launch_tc(const TcParams& prm, const Plan& pl, int grid, cudaStream_t s, const char* name) {
+  auto kern = k_conv_tc<BK, MODE, BF16>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(pl.smem));
+  if (e != cudaSuccess) return set_cuda_error(e, "conv smem attribute");
+  SC_LAUNCH(name, s, kern<<<grid, kThreads, pl.smem, s>>>(prm));
+  e = cudaGetLastError();
+  return e == cudaSuccess ? SC_OK : set_cuda_error(e, name);
+}
+
+template <int MODE>
+sc_status dispatch_tc(const TcParams& prm, const Plan& pl, bool bf16, int grid, cudaStream_t s, const char* name) {
+  if (grid <= 0) return SC_OK;
+  switch (pl.bk) {
+    case 64:
+      return bf16 ? launch_tc<64, MODE, true>(prm, pl, grid, s, name) : launch_tc<64, MODE, false>(prm, pl, grid, s, name);
+    case 32:
+      return bf16 ? launch_tc<32, MODE, true>(prm, pl, grid, s, name) : launch_tc<32, MODE, false>(prm, pl, grid, s, name);
+    default:
+      return bf16 ? launch_tc<16, MODE, true>(prm, pl, grid, s, name) : launch_tc<16, MODE, false>(prm, pl, grid, s, name);
+  }
+}
+
+sc_status pack_weights(const ConvArgs& a, int bk, uint8_t* img) {
+  const int V = a.m->V;
+  const int64_t chunks = static_cast<int64_t>(V) * (a.c_in / bk) * a.c_out * (bk * 2 / 16);
+  int grid = static_cast<int>((chunks + 255) / 256);
+  if (grid > device_sm_count() * 16) grid = device_sm_count() * 16;
+  if (grid < 1) grid = 1;
+  const uint16_t* W = static_cast<const uint16_t*>(a.W);
+  switch (bk) {
+    case 64: SC_LAUNCH("pack_weights", a.stream, k_pack_weights<64><<<grid, 256, 0, a.stream>>>(W, img, V, a.c_in, a.c_out)); break;
+    case 32: SC_LAUNCH("pack_weights", a.stream, k_pack_weights<32><<<grid, 256, 0, a.stream>>>(W, img, V, a.c_in, a.c_out)); break;
+    default: SC_LAUNCH("pack_weights", a.stream, k_pack_weights<16><<<grid, 256, 0, a.stream>>>(W, img, V, a.c_in, a.c_out)); break;
+  }
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? SC_OK : set_cuda_error(e, "pack_weights launch");
+}
+
+TcParams base_params(const ConvArgs& a, const Plan& pl, const uint8_t* img) {
+  TcParams p{};
+  p.feats = static_cast<const uint8_t*>(a.feats);
+  p.wimg = img;
+  p.out = static_cast<uint8_t*>(a.out);
+  p.nbr = a.m->nbr;
+  p.in_rows = a.m->in_rows;
+  p.out_rows = a.m->out_rows;
+  p.offs = a.m->offs;
+  p.ws_tiles = a.m->ws_tiles;
+  p.n = a.m->n;
+  p.V = a.m->V;
+  p.c_in = a.c_in;
+  p.c_out = a.c_out;
+  p.relu = a.relu ? 1 : 0;
+  p.stages = pl.stages;
+  p.tmem_cols = pl.tmem_cols;
+  p.status = a.m->status;
+  return p;
+}
+
+}  // namespace
+
+bool fused_supported(const ConvArgs& a) {
+  Plan pl;
+  return a.dtype != SC_F32 && a.m->V <= 128 && make_plan(kOutputStationary, a.m->V, a.c_in, a.c_out, &pl);
+}
+
+sc_status conv_fused(const ConvArgs& a) {
+  Plan pl;
+  if (a.dtype == SC_F32 || a.m->V > 128 || !make_plan(kOutputStationary, a.m->V, a.c_in, a.c_out, &pl))
+    return set_error(SC_ERR_UNSUPPORTED, "fused kernel: f16/bf16 only, V <= 128, tile must fit shared memory");
+  if (a.m->n == 0) return SC_OK;
+  const size_t img_bytes = static_cast<size_t>(a.m->V) * a.c_in * a.c_out * 2;
+  void* img = nullptr;
+  sc_status st = dev_alloc(&img, img_bytes, a.stream);
+  if (st) return st;
+  st = pack_weights(a, pl.bk, static_cast<uint8_t*>(img));
+  if (!st) {
+    TcParams prm = base_params(a, pl, static_cast<const uint8_t*>(img));
+    const int grid = static_cast<int>((a.m->n + kRows - 1) / kRows);
+    st = dispatch_tc<kOutputStationary>(prm, pl, a.dtype == SC_BF16, grid, a.stream, "subm_conv_fused");
+  }
+  dev_free(img, a.stream);
+  return st;
+}
+
+sc_status conv_weight_stationary(const ConvArgs& a) {
+  Plan pl;
+  if (a.dtype == SC_F32 || !make_plan(kWsScatter, a.m->V, a.c_in, a.c_out, &pl))
+    return set_error(SC_ERR_UNSUPPORTED, "weight-stationary kernel: f16/bf16 only");
+  if (a.m->n == 0) return SC_OK;
+  if (!a.m->host_valid) return set_error(SC_ERR_INVALID_ARG, "weight-stationary kernel needs the map's host counts");
+  const size_t img_bytes = static_cast<size_t>(a.m->V) * a.c_in * a.c_out * 2;
+  const size_t acc_bytes = static_cast<size_t>(a.m->n) * a.c_out * sizeof(float);
+  void* img = nullptr;
+  void* acc = nullptr;
+  sc_status st = dev_alloc(&img, img_bytes, a.stream);
+  if (st) return st;
+  st = dev_alloc(&acc, acc_bytes, a.stream);
+  if (st) {
+    dev_free(img, a.stream);
+    return st;
+  }
+  st = pack_weights(a, pl.bk, static_cast<uint8_t*>(img));
+  TcParams prm = base_params(a, pl, static_cast<const uint8_t*>(img));
+  prm.acc = static_cast<float*>(acc);
+  const bool bf16 = a.dtype == SC_BF16;
+  if (!st) {
+    const int grid = static_cast<int>((a.m->n + kRows - 1) / kRows);
+    st = dispatch_tc<kWsCentre>(prm, pl, bf16, grid, a.stream, "subm_conv_ws_centre");
+  }
+  if (!st) st = dispatch_tc<kWsScatter>(prm, pl, bf16, a.m->ws_tiles_host[a.m->V], a.stream, "subm_conv_ws_scatter");
+  if (!st) {
+    const int64_t n4 = a.m->n * a.c_out / 4;
+    int grid = static_cast<int>((n4 + 255) / 256);
+    if (grid > device_sm_count() * 16) grid = device_sm_count() * 16;
+    if (bf16)
+      SC_LAUNCH("cast_out", a.stream, k_cast_out<true><<<grid, 256, 0, a.stream>>>(static_cast<const float4*>(acc), static_cast<uint2*>(a.out), n4, a.relu));
+    else
+      SC_LAUNCH("cast_out", a.stream, k_cast_out<false><<<grid, 256, 0, a.stream>>>(static_cast<const float4*>(acc), static_cast<uint2*>(a.out), n4, a.relu));
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) st = set_cuda_error(e, "cast_out launch");
+  }
+  dev_free(acc, a.stream);
+  dev_free(img, a.stream);
+  return st;
+}
+
+}  // namespace sc

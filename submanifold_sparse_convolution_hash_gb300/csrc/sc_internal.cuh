@@ -1,0 +1,136 @@
+// Internal declarations shared by the libsc translation units.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <vector>
+
+#include "sc.h"
+
+namespace sc {
+
+// ---------------------------------------------------------------- status --
+// Bits latched by kernels in a device status word.
+enum : int {
+  kDevErrRange = 1,    // coordinate outside its field / outside dims
+  kDevErrDup = 2,      // duplicate coordinate at insert
+  kDevErrFull = 4,     // insert probed every slot without finding room
+  kDevErrTimeout = 8,  // a bounded mbarrier wait gave up
+};
+
+// ------------------------------------------------------------ hash table --
+// 64-bit key: batch in bits 48..63, x in 32..47, y in 16..31, z in 0..15.
+// Every field is < 65535, so the all-ones word never occurs as a key and
+// marks an empty slot.
+constexpr unsigned long long kEmptyKey = ~0ull;
+
+struct __align__(16) Slot {
+  unsigned long long key;
+  int val;
+  int pad;
+};
+
+__host__ __device__ __forceinline__ unsigned long long pack_key(uint32_t b, uint32_t x, uint32_t y,
+                                                                uint32_t z) {
+  return (static_cast<unsigned long long>(b) << 48) | (static_cast<unsigned long long>(x) << 32) |
+         (static_cast<unsigned long long>(y) << 16) | static_cast<unsigned long long>(z);
+}
+
+// MurmurHash3's 64-bit finaliser (Appleby): a bijective mix, so distinct
+// keys stay distinct before the mask.
+__host__ __device__ __forceinline__ unsigned long long hash_mix(unsigned long long k) {
+  k ^= k >> 33;
+  k *= 0xff51afd7ed558ccdULL;
+  k ^= k >> 33;
+  k *= 0xc4ceb9fe1a85ec53ULL;
+  k ^= k >> 33;
+  return k;
+}
+
+// ------------------------------------------------------------- handles --
+struct HashTable {
+  int64_t n = 0;
+  int64_t capacity = 0;              // power of two
+  Slot* table = nullptr;             // [capacity]
+  unsigned long long* keys = nullptr;  // [n]  packed key of each row (kEmptyKey if invalid)
+  int* status = nullptr;             // device status word
+};
+
+struct ConvChoice {
+  int c_in, c_out, dtype;
+  unsigned variant;
+};
+
+struct KernelMap {
+  int64_t n = 0;
+  int ndim = 3, K = 3, V = 27;
+  int dims[3] = {1, 1, 1};
+  int ntiles = 0;                    // probe/fill tiles
+  int* nbr = nullptr;                // [n, V]
+  int64_t* offs = nullptr;           // [V+1]
+  int* in_rows = nullptr;            // [n*(V-1)] capacity, offs[V] used
+  int* out_rows = nullptr;
+  int* counts = nullptr;             // [V, ntiles] per-tile counts -> exclusive bases
+  int* totals = nullptr;             // [V]
+  int* ws_tiles = nullptr;           // [V+1] prefix of ceil(count/128) per offset
+  int64_t* map_size = nullptr;       // device: n + offs[V]
+  int* status = nullptr;             // device status word (map build)
+  int* hash_status = nullptr;        // borrowed pointer to the hash's word at build time
+  // host mirrors, valid once synchronised
+  bool host_valid = false;
+  std::vector<int64_t> offs_host;    // [V+1]
+  std::vector<int> ws_tiles_host;    // [V+1]
+  int64_t map_size_host = -1;
+  std::vector<ConvChoice> tuned;
+};
+
+// ------------------------------------------------------------ launching --
+// Launch bookkeeping shared by every translation unit: counts launches and,
+// while profiling is on, brackets each launch with CUDA events.
+int prof_begin(const char* name, cudaStream_t s);
+void prof_end(int token, cudaStream_t s);
+
+// Records a failing CUDA call's text for sc_last_error().
+sc_status set_cuda_error(cudaError_t e, const char* where);
+sc_status set_error(sc_status s, const char* msg);
+
+int device_sm_count();
+
+// kernels: hash + map (hash_kmap.cu)
+sc_status launch_hash_insert(const int32_t* coords, int64_t n, HashTable* h, cudaStream_t s);
+sc_status launch_hash_query(const HashTable* h, const int32_t* q, int64_t m, int32_t* rows,
+                            cudaStream_t s);
+sc_status launch_kmap_build(const HashTable* h, KernelMap* m, cudaStream_t s);
+int kmap_probe_tile();
+
+// kernels: convolution (conv_tc.cu, conv_simt.cu)
+struct ConvArgs {
+  const KernelMap* m;
+  const void* feats;
+  const void* W;
+  void* out;
+  int c_in, c_out;
+  sc_dtype dtype;
+  bool relu;
+  cudaStream_t stream;
+};
+sc_status conv_fused(const ConvArgs& a);
+sc_status conv_weight_stationary(const ConvArgs& a);
+sc_status conv_simt(const ConvArgs& a);
+bool fused_supported(const ConvArgs& a);
+
+// stream-ordered allocation helpers
+sc_status dev_alloc(void** p, size_t bytes, cudaStream_t s);
+void dev_free(void* p, cudaStream_t s);
+
+}  // namespace sc
+
+#define SC_LAUNCH(name, stream, ...)                   \
+  do {                                                 \
+    int _tok = ::sc::prof_begin(name, stream);         \
+    __VA_ARGS__;                                       \
+    ::sc::prof_end(_tok, stream);                      \
+  } while (0)

@@ -2,7 +2,7 @@
 
 This module only draws inputs: coordinates, features and weights.  It holds
 none of the layer's arithmetic (no hashing, no neighbour search, no
-convolution), so both the CPU oracle's tests and the CUDA path can take their
+convolution), so the CPU reference checks and the CUDA path can both take their
 inputs from here without sharing any computation.
 
 Random numbers come from SplitMix64 (Steele, Lea and Flood, "Fast splittable

@@ -1,0 +1,281 @@
+"""GPU parity: hash table, kernel map and convolution against the CPU oracle.
+
+Sizes here finish in the oracle within seconds and still span several
+128-row tiles plus a ragged tail.  Maps must match bit for bit; features
+within max|gpu - ref| <= 5e-3 * max(1, max|ref|) (f16/bf16 inputs, fp32
+accumulation) or 1e-5 * max(1, max|ref|) (fp32).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import assert_close, gpu_lists_by_offset, layer_inputs
+from submanifold_sparse_convolution_hash_gb300 import ScError, scenes
+from submanifold_sparse_convolution_hash_gb300 import binding as sc
+
+pytestmark = pytest.mark.gpu
+
+
+def small_scenes():
+    return {
+        "uniform2d": scenes.uniform_2d(1000, (64, 64), 200),
+        "uniform2d_dense": scenes.uniform_2d(21, (40, 40), 900),
+        "lidar": scenes.lidar_scan(31, 3000, (160, 160, 41)),
+        "indoor": scenes.indoor_scene(32, 4000, (48, 48, 32), extent=(8, 40), radius=(3, 10)),
+        "batch": scenes.batch_of_scans(33, 3, 1200, (120, 120, 41)),
+    }
+
+
+SCENES = small_scenes()
+
+
+def build(scene, K, sync=True):
+    c = torch.from_numpy(scene.coords).cuda()
+    h = sc.sc_hash_build(c)
+    m = sc.sc_kmap_build(h, scene.ndim, K, scene.dims, sync=sync)
+    return c, h, m
+
+
+# ------------------------------------------------------------------ hash --
+
+def test_hash_query_finds_every_row_and_misses_absent_keys():
+    s = SCENES["lidar"]
+    c, h, m = build(s, 3)
+    rows = h.query(c).cpu().numpy()
+    np.testing.assert_array_equal(rows, np.arange(s.n))
+    # shifted coordinates: present iff the shifted point is in the set
+    q = s.coords.copy()
+    q[:, 3] += 1
+    present = {tuple(r) for r in s.coords.tolist()}
+    index = {tuple(r): i for i, r in enumerate(s.coords.tolist())}
+    want = np.array([index.get(tuple(r), -1) for r in q.tolist()])
+    np.testing.assert_array_equal(h.query(torch.from_numpy(q).cuda()).cpu().numpy(), want)
+    assert (want >= 0).any() and (want < 0).any()
+    # other batch, out-of-field values
+    q2 = np.array([[1, 10, 10, 10], [-1, 0, 0, 0], [0, 65535, 0, 0], [0, -3, 1, 1]], dtype=np.int32)
+    np.testing.assert_array_equal(h.query(torch.from_numpy(q2).cuda()).cpu().numpy(), [-1, -1, -1, -1])
+    assert len(present) == s.n
+    assert h.capacity >= 2 * s.n and (h.capacity & (h.capacity - 1)) == 0
+
+
+# ------------------------------------------------------------------- map --
+
+@pytest.mark.parametrize("name,K", [("uniform2d", 3), ("uniform2d_dense", 5), ("lidar", 3), ("indoor", 3),
+                                    ("indoor", 5), ("batch", 3), ("lidar", 1), ("indoor", 7)])
+@pytest.mark.parametrize("sync", [True, False])
+def test_kmap_bit_exact(name, K, sync):
+    s = SCENES[name]
+    c, h, m = build(s, K, sync)
+    if not sync:
+        m.check()
+    ref = oracle.kmap(s.coords, s.ndim, K, s.dims)
+    nbr = m.nbr().cpu().numpy()
+    np.testing.assert_array_equal(nbr, ref)
+    lists, offs = gpu_lists_by_offset(m)
+    ref_lists = oracle.offset_lists(ref)
+    centre = (K ** s.ndim - 1) // 2
+    for v, ((gi, go), (ri, ro)) in enumerate(zip(lists, ref_lists)):
+        if v == centre:
+            assert len(gi) == 0  # the identity is implied, not listed
+            np.testing.assert_array_equal(ri, np.arange(s.n))
+            continue
+        np.testing.assert_array_equal(go, ro)  # ordered by output row
+        np.testing.assert_array_equal(gi, ri)
+    assert m.map_size() == len(oracle.tuples(ref))
+    assert offs[-1] == m.map_size() - s.n
+
+
+def test_kmap_is_deterministic():
+    s = SCENES["lidar"]
+    _, _, m1 = build(s, 3)
+    _, _, m2 = build(s, 3)
+    assert torch.equal(m1.nbr(), m2.nbr())
+    for a, b in zip(m1.lists(), m2.lists()):
+        assert torch.equal(a, b)
+
+
+def test_five_point_worked_example_on_gpu():
+    coords = np.array([[0, 1, 1, 0], [0, 2, 2, 0], [0, 2, 4, 0], [0, 3, 2, 0], [0, 4, 3, 0]], dtype=np.int32)
+    h = sc.sc_hash_build(torch.from_numpy(coords).cuda())
+    m = sc.sc_kmap_build(h, 2, 3, (5, 5, 1))
+    assert m.map_size() == 11
+    offs = m.offsets().cpu().numpy()
+    counts = np.diff(offs)
+    counts[4] = 5  # centre: the identity over the five points
+    oi = lambda d: oracle.offset_index(d, 3)
+    assert counts[oi((-1, -1))] == 2 and counts[oi((-1, 0))] == 1 and counts[oi((0, 0))] == 5
+    assert counts[oi((1, 0))] == 1 and counts[oi((1, 1))] == 2 and int((counts > 0).sum()) == 5
+
+
+# -------------------------------------------------------------- features --
+
+CONV_CASES = [
+    # scene, K, c_in, c_out, dtype, relu, variant
+    ("lidar", 3, 32, 32, "f16", False, "fused"),
+    ("lidar", 3, 32, 32, "f16", True, "ws"),
+    ("indoor", 3, 64, 64, "bf16", False, "fused"),
+    ("indoor", 3, 64, 64, "bf16", True, "ws"),
+    ("batch", 3, 32, 64, "f16", True, "fused"),
+    ("batch", 3, 64, 128, "f16", False, "fused"),
+    ("batch", 3, 128, 256, "f16", True, "fused"),
+    ("batch", 3, 256, 256, "f16", False, "fused"),
+    ("batch", 3, 256, 256, "f16", False, "ws"),
+    ("indoor", 5, 128, 128, "bf16", False, "fused"),
+    ("indoor", 5, 128, 128, "bf16", False, "ws"),
+    ("uniform2d", 3, 16, 16, "f16", False, "fused"),
+    ("uniform2d_dense", 5, 16, 48, "bf16", True, "fused"),
+    ("uniform2d_dense", 5, 48, 16, "bf16", True, "ws"),
+    ("lidar", 1, 32, 32, "f16", False, "fused"),
+    ("lidar", 1, 32, 32, "f16", False, "ws"),
+    ("indoor", 7, 32, 32, "bf16", False, None),  # V = 343: auto picks weight-stationary
+    ("lidar", 3, 32, 32, "f16", False, "simt"),
+    ("uniform2d", 3, 16, 16, "f32", False, None),
+    ("uniform2d", 3, 16, 16, "f32", True, "simt"),
+    ("lidar", 3, 32, 16, "f32", False, None),
+]
+
+
+@pytest.mark.parametrize("name,K,c_in,c_out,dtype,relu,variant", CONV_CASES)
+def test_conv_matches_oracle(name, K, c_in, c_out, dtype, relu, variant):
+    s = SCENES[name]
+    c, h, m = build(s, K)
+    f, w, f64, w64 = layer_inputs(s, K, c_in, c_out, dtype, seed=7 + c_in + K,
+                                  w_std=1.0 if dtype == "f32" else None)
+    out = sc.sc_subm_conv_fwd(m, f, w, relu=relu, variant=variant)
+    torch.cuda.synchronize()
+    ref = oracle.subm_conv(s.coords, f64, w64, s.ndim, K, s.dims, relu=relu)
+    assert_close(out, ref, dtype, f"{name} K={K} {c_in}->{c_out} {dtype} {variant}")
+    m.check()
+
+
+def test_every_row_written_once_no_stale_values():
+    """Output buffer pre-filled with NaN: every row must be overwritten."""
+    s = SCENES["lidar"]
+    c, h, m = build(s, 3)
+    f, w, f64, w64 = layer_inputs(s, 3, 32, 32, "f16", seed=3)
+    ref = oracle.subm_conv(s.coords, f64, w64, 3, 3, s.dims)
+    for variant in ("fused", "ws", "simt"):
+        out = torch.full((s.n, 32), float("nan"), dtype=torch.float16, device="cuda")
+        sc.sc_subm_conv_fwd(m, f, w, out=out, variant=variant)
+        assert_close(out, ref, "f16", variant)
+
+
+def test_tune_picks_a_variant_and_result_matches():
+    s = SCENES["indoor"]
+    c, h, m = build(s, 3)
+    f, w, f64, w64 = layer_inputs(s, 3, 64, 64, "bf16", seed=4)
+    out = torch.empty((s.n, 64), dtype=torch.bfloat16, device="cuda")
+    name = sc.sc_subm_conv_tune(m, f, w, out=out, reps=2)
+    assert name in ("fused", "ws")
+    ref = oracle.subm_conv(s.coords, f64, w64, 3, 3, s.dims)
+    assert_close(out, ref, "bf16", "tuned")
+    out2 = sc.sc_subm_conv_fwd(m, f, w)
+    assert_close(out2, ref, "bf16", "after tune")
+
+
+def test_map_reused_across_a_layer_stack():
+    """One map, several layers, ReLU between them; each layer checked with
+    the oracle fed the GPU's own input, and the stack end to end."""
+    s = SCENES["batch"]
+    c, h, m = build(s, 3)
+    widths = [32, 32, 64, 64, 128]
+    x = torch.from_numpy(scenes.features(11, s.n, widths[0])).half().cuda()
+    x0 = x.double().cpu().numpy()
+    Ws = [torch.from_numpy(scenes.weights(12 + i, 27, widths[i], widths[i + 1])).half().cuda()
+          for i in range(len(widths) - 1)]
+    for i, W in enumerate(Ws):
+        relu = i + 1 < len(Ws)
+        y = sc.sc_subm_conv_fwd(m, x, W, relu=relu)
+        ref = oracle.subm_conv(s.coords, x.double().cpu().numpy(), W.double().cpu().numpy(), 3, 3, s.dims,
+                               relu=relu)
+        assert_close(y, ref, "f16", f"layer {i}")
+        x = y
+    ref_stack = oracle.subm_conv_stack(s.coords, x0, [W.double().cpu().numpy() for W in Ws], 3, 3, s.dims, "f16")
+    assert_close(x, ref_stack[-1], "f16", "stack end to end")
+
+
+# ------------------------------------------------------------ edge cases --
+
+def test_empty_and_single_point():
+    h = sc.sc_hash_build(torch.zeros((0, 4), dtype=torch.int32, device="cuda"))
+    m = sc.sc_kmap_build(h, 3, 3, (8, 8, 8))
+    assert m.map_size() == 0
+    f = torch.zeros((0, 32), dtype=torch.float16, device="cuda")
+    W = torch.randn((27, 32, 32), dtype=torch.float16, device="cuda")
+    assert sc.sc_subm_conv_fwd(m, f, W).shape == (0, 32)
+    one = torch.tensor([[0, 3, 3, 3]], dtype=torch.int32, device="cuda")
+    m1 = sc.sc_kmap_build(sc.sc_hash_build(one), 3, 3, (8, 8, 8))
+    assert m1.map_size() == 1
+    f1 = torch.randn((1, 32), device="cuda").half()
+    for v in ("fused", "ws", "simt"):
+        out = sc.sc_subm_conv_fwd(m1, f1, W, variant=v)
+        ref = f1.double().cpu().numpy() @ W[13].double().cpu().numpy()
+        assert_close(out, ref, "f16", v)
+
+
+@pytest.mark.parametrize("n", [127, 128, 129, 255, 257, 1000])
+def test_ragged_tile_counts(n):
+    s = scenes.uniform_2d(500 + n, (64, 64), n)
+    c, h, m = build(s, 3)
+    f, w, f64, w64 = layer_inputs(s, 3, 16, 32, "bf16", seed=n)
+    ref = oracle.subm_conv(s.coords, f64, w64, 2, 3, s.dims)
+    for v in ("fused", "ws"):
+        assert_close(sc.sc_subm_conv_fwd(m, f, w, variant=v), ref, "bf16", f"n={n} {v}")
+
+
+def test_error_reporting():
+    dup = torch.tensor([[0, 1, 1, 1], [0, 2, 2, 2], [0, 1, 1, 1]], dtype=torch.int32, device="cuda")
+    h = sc.sc_hash_build(dup)
+    with pytest.raises(ScError) as e:
+        h.check()
+    assert e.value.code == 3
+    with pytest.raises(ScError) as e:
+        sc.sc_kmap_build(h, 3, 3, (4, 4, 4))
+    assert e.value.code == 3
+    ok = torch.tensor([[0, 1, 1, 1], [0, 5, 2, 2]], dtype=torch.int32, device="cuda")
+    with pytest.raises(ScError) as e:
+        sc.sc_kmap_build(sc.sc_hash_build(ok), 3, 3, (4, 4, 4))  # x = 5 outside dims
+    assert e.value.code == 2
+    neg = torch.tensor([[0, -1, 1, 1]], dtype=torch.int32, device="cuda")
+    with pytest.raises(ScError) as e:
+        sc.sc_hash_build(neg).check()
+    assert e.value.code == 2
+    h2 = sc.sc_hash_build(torch.tensor([[0, 1, 1, 1]], dtype=torch.int32, device="cuda"))
+    with pytest.raises(ScError) as e:
+        sc.sc_kmap_build(h2, 3, 4, (4, 4, 4))
+    assert e.value.code == 1
+    with pytest.raises(ScError) as e:
+        sc.sc_kmap_build(h2, 4, 3, (4, 4, 4))
+    assert e.value.code == 1
+    m = sc.sc_kmap_build(h2, 3, 3, (4, 4, 4))
+    f = torch.zeros((1, 24), dtype=torch.float16, device="cuda")
+    with pytest.raises(ScError) as e:
+        sc.sc_subm_conv_fwd(m, f, torch.zeros((27, 24, 24), dtype=torch.float16, device="cuda"))
+    assert e.value.code == 5
+    with pytest.raises(ScError) as e:  # fp32 on the tensor-core kernel
+        sc.sc_subm_conv_fwd(m, torch.zeros((1, 16), device="cuda"), torch.zeros((27, 16, 16), device="cuda"),
+                            variant="fused")
+    assert e.value.code == 5
+    with pytest.raises(ValueError):
+        sc.sc_hash_build(torch.zeros((4, 4), dtype=torch.int32))  # host tensor: no CPU path
+    # the library is still usable after every error above
+    assert sc.sc_kmap_build(sc.sc_hash_build(ok), 3, 3, (8, 8, 8)).map_size() == 2
+
+
+def test_launch_count_and_profile():
+    s = SCENES["lidar"]
+    before = sc.launch_count()
+    sc.profile_reset()
+    sc.profile_enable(True)
+    try:
+        c, h, m = build(s, 3)
+        f, w, _, _ = layer_inputs(s, 3, 32, 32, "f16", seed=1)
+        sc.sc_subm_conv_fwd(m, f, w, variant="fused")
+        prof = sc.profile_collect()
+    finally:
+        sc.profile_enable(False)
+    launched = sc.launch_count() - before
+    assert launched >= 6
+    for k in ("hash_insert", "kmap_probe", "kmap_scan", "kmap_fill", "pack_weights", "subm_conv_fused"):
+        assert k in prof and prof[k][0] >= 1 and prof[k][1] > 0
