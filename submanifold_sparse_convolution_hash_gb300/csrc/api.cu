@@ -318,8 +318,11 @@ sc_status sc_hash_build(const int32_t* d_coords, int64_t n, sc_stream stream, sc
   sc_hash h = new sc_hash_s();
   HashTable& t = h->t;
   t.n = n;
+  // load factor <= 1/4 while the table stays small enough to live in L2,
+  // <= 1/2 beyond that
   int64_t cap = 16;
-  while (cap < 2 * n) cap <<= 1;
+  const int64_t want = 4 * n * static_cast<int64_t>(sizeof(Slot)) <= (int64_t(32) << 20) ? 4 * n : 2 * n;
+  while (cap < want) cap <<= 1;
   t.capacity = cap;
   sc_status st = dev_alloc(reinterpret_cast<void**>(&t.table), sizeof(Slot) * cap, s);
   if (!st) st = dev_alloc(reinterpret_cast<void**>(&t.keys), sizeof(unsigned long long) * (n > 0 ? n : 1), s);
@@ -375,7 +378,7 @@ sc_status sc_kmap_destroy(sc_kmap m, sc_stream stream) {
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   KernelMap& k = m->k;
   for (void* p : {static_cast<void*>(k.nbr), static_cast<void*>(k.offs), static_cast<void*>(k.in_rows),
-                  static_cast<void*>(k.out_rows), static_cast<void*>(k.counts), static_cast<void*>(k.totals),
+                  static_cast<void*>(k.out_rows), static_cast<void*>(k.masks), static_cast<void*>(k.bases), static_cast<void*>(k.totals),
                   static_cast<void*>(k.ws_tiles), static_cast<void*>(k.map_size), static_cast<void*>(k.status)})
     dev_free(p, s);
   delete m;
@@ -414,15 +417,17 @@ sc_status sc_kmap_build(sc_hash h, int ndim, int K, const int32_t dims[3], unsig
   if (!st) st = dev_alloc(reinterpret_cast<void**>(&k.offs), sizeof(int64_t) * (V + 1), s);
   if (!st) st = dev_alloc(reinterpret_cast<void**>(&k.in_rows), sizeof(int) * lists, s);
   if (!st) st = dev_alloc(reinterpret_cast<void**>(&k.out_rows), sizeof(int) * lists, s);
-  if (!st) st = dev_alloc(reinterpret_cast<void**>(&k.counts), sizeof(int) * static_cast<size_t>(V) * k.ntiles, s);
+  if (!st) st = dev_alloc(reinterpret_cast<void**>(&k.masks), sizeof(unsigned) * static_cast<size_t>(V) * k.ntiles, s);
+  if (!st) st = dev_alloc(reinterpret_cast<void**>(&k.bases), sizeof(int) * static_cast<size_t>(V) * k.ntiles, s);
   if (!st) st = dev_alloc(reinterpret_cast<void**>(&k.totals), sizeof(int) * V, s);
   if (!st) st = dev_alloc(reinterpret_cast<void**>(&k.ws_tiles), sizeof(int) * (V + 1), s);
   if (!st) st = dev_alloc(reinterpret_cast<void**>(&k.map_size), sizeof(int64_t), s);
   if (!st) st = dev_alloc(reinterpret_cast<void**>(&k.status), sizeof(int) * 4, s);
   // status[1] carries the hash's latched insert status from here on
   if (!st) {
-    cudaError_t e = cudaMemcpyAsync(k.status + 1, h->t.status, sizeof(int), cudaMemcpyDeviceToDevice, s);
-    if (e != cudaSuccess) st = set_cuda_error(e, "copy hash status");
+    cudaError_t e = cudaMemsetAsync(k.status, 0, sizeof(int) * 4, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(k.status + 1, h->t.status, sizeof(int), cudaMemcpyDeviceToDevice, s);
+    if (e != cudaSuccess) st = set_cuda_error(e, "kmap status init");
   }
   if (!st) st = launch_kmap_build(&h->t, &k, s);
   if (!st && !(flags & SC_KMAP_NO_SYNC)) st = sync_host(&k, s);

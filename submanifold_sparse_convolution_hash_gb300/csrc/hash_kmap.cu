@@ -12,35 +12,41 @@
 // Lists are grouped by offset ("SparseConvNet: from hash table to rulebook",
 // section 3) and, within an offset, ordered by output row.
 //
-// Three kernels build the map:
-//   probe  one block per tile of 64 points; the block's threads take the
-//          tile's (point, offset) pairs in row-major order, each thread keeps
-//          eight first-slot loads in flight, and the tile's [64, V] slice of
-//          the neighbour table is written with coalesced 16-byte stores.  Per
-//          tile and offset it also counts hits (warp ballots).
-//   scan   one block per offset: exclusive prefix of the per-tile counts.
-//   fill   one block per tile: re-reads its neighbour slice and writes the
-//          (in, out) list entries at their final positions, warp-ballot
-//          compacted, so every list is ordered by output row.
+// Points are taken in tiles of 32 rows.  Three kernels build the map:
+//   probe  one block per tile: the tile's 32 x V (point, offset) pairs are
+//          spread over the block's threads, four per thread with their
+//          first-slot loads in flight together.  Results go straight to the
+//          neighbour table (coalesced), and each hit sets bit p of the
+//          (offset, tile) mask.
+//   scan   one block per offset: exclusive prefix of the masks' popcounts
+//          over tiles.  The last block to finish (a ticket counter) turns the
+//          per-offset totals into the segment offsets, the weight-stationary
+//          tile prefix and |M|.
+//   fill   each warp takes one (tile, offset) pair: lane p holds point p's
+//          neighbour, a ballot ranks the hits, and the (in, out) entries are
+//          written to consecutive positions of the offset's segment.
 
 #include "sc_internal.cuh"
 
 namespace sc {
 namespace {
 
-constexpr int kTile = 64;       // points per probe/fill tile
-constexpr int kThreads = 256;   // threads per probe/fill block
-constexpr int kIlp = 8;         // outstanding first-slot probes per thread
-constexpr int kWsRows = 128;    // rows per weight-stationary tile
+constexpr int kTile = 32;        // points per tile (one bitmask word)
+constexpr int kThreads = 256;    // threads per probe / fill block
+constexpr int kIlp = 4;          // pairs per thread with loads in flight together
+constexpr int kWsRows = 128;     // rows per weight-stationary tile
+constexpr int kScanThreads = 512;  // >= the largest V (343)
+constexpr int kScanPer = 8;        // tiles per scan thread per chunk
 
-__device__ __forceinline__ ulonglong2 load_slot(const Slot* __restrict__ t, unsigned long long i) {
+__device__ __forceinline__ ulonglong2 load_slot(const Slot* __restrict__ t, uint32_t i) {
   return __ldg(reinterpret_cast<const ulonglong2*>(t + i));
 }
 
-__device__ __forceinline__ int table_find(const Slot* __restrict__ table, unsigned long long mask,
-                                          unsigned long long key, unsigned long long h, ulonglong2 cur) {
-  for (unsigned long long probe = 0; probe <= mask; ++probe) {
-    if (cur.x == key) return static_cast<int>(static_cast<unsigned>(cur.y & 0xffffffffull));
+// Resolves a lookup whose first slot `cur` (index h) is already loaded.
+__device__ __forceinline__ int table_find(const Slot* __restrict__ table, uint32_t mask, unsigned long long key,
+                                          uint32_t h, ulonglong2 cur) {
+  for (uint32_t probe = 0; probe <= mask; ++probe) {
+    if (cur.x == key) return static_cast<int>(static_cast<uint32_t>(cur.y));
     if (cur.x == kEmptyKey) return -1;
     h = (h + 1) & mask;
     cur = load_slot(table, h);
@@ -48,52 +54,67 @@ __device__ __forceinline__ int table_find(const Slot* __restrict__ table, unsign
   return -1;
 }
 
+__device__ __forceinline__ bool coord_fields_ok(int4 c) {
+  return static_cast<unsigned>(c.x) < 65535u && static_cast<unsigned>(c.y) < 65535u &&
+         static_cast<unsigned>(c.z) < 65535u && static_cast<unsigned>(c.w) < 65535u;
+}
+
+// Linear-probing insert.  Each round reads a window of four slots from L2
+// and CASes the first empty one, so a collision usually costs no extra atomic
+// round trip; a lost CAS is re-examined before moving on.
 __global__ void __launch_bounds__(256) k_hash_insert(const int4* __restrict__ coords, int64_t n,
-                                                     Slot* __restrict__ table, unsigned long long mask,
+                                                     Slot* __restrict__ table, uint32_t mask,
                                                      unsigned long long* __restrict__ keys,
                                                      int* __restrict__ status) {
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
     const int4 c = __ldg(coords + i);
-    if (static_cast<unsigned>(c.x) >= 65535u || static_cast<unsigned>(c.y) >= 65535u ||
-        static_cast<unsigned>(c.z) >= 65535u || static_cast<unsigned>(c.w) >= 65535u) {
+    if (!coord_fields_ok(c)) {
       keys[i] = kEmptyKey;
       atomicOr(status, kDevErrRange);
       continue;
     }
     const unsigned long long key = pack_key(c.x, c.y, c.z, c.w);
     keys[i] = key;
-    unsigned long long h = hash_mix(key) & mask;
-    bool placed = false;
-    for (unsigned long long probe = 0; probe <= mask; ++probe) {
-      const unsigned long long prev = atomicCAS(&table[h].key, kEmptyKey, key);
-      if (prev == kEmptyKey) {
-        table[h].val = static_cast<int>(i);
-        placed = true;
-        break;
+    uint32_t h = static_cast<uint32_t>(hash_mix(key)) & mask;
+    int outcome = 0;  // 1 placed, 2 duplicate
+    for (uint32_t seen = 0; seen <= mask && !outcome;) {
+      unsigned long long w[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) w[t] = __ldcg(&table[(h + t) & mask].key);
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        if (outcome || seen > mask) break;
+        const uint32_t slot = (h + t) & mask;
+        unsigned long long k = w[t];
+        if (k == kEmptyKey) {
+          k = atomicCAS(&table[slot].key, kEmptyKey, key);
+          if (k == kEmptyKey) {
+            table[slot].val = static_cast<int>(i);
+            outcome = 1;
+            break;
+          }
+        }
+        if (k == key) outcome = 2;
+        ++seen;
       }
-      if (prev == key) {
-        atomicOr(status, kDevErrDup);
-        placed = true;
-        break;
-      }
-      h = (h + 1) & mask;
+      h = (h + 4) & mask;
     }
-    if (!placed) atomicOr(status, kDevErrFull);
+    if (outcome == 2) atomicOr(status, kDevErrDup);
+    if (outcome == 0) atomicOr(status, kDevErrFull);
   }
 }
 
 __global__ void __launch_bounds__(256) k_hash_query(const int4* __restrict__ q, int64_t m,
-                                                    const Slot* __restrict__ table, unsigned long long mask,
+                                                    const Slot* __restrict__ table, uint32_t mask,
                                                     int* __restrict__ rows) {
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < m; i += stride) {
     const int4 c = __ldg(q + i);
     int r = -1;
-    if (static_cast<unsigned>(c.x) < 65535u && static_cast<unsigned>(c.y) < 65535u &&
-        static_cast<unsigned>(c.z) < 65535u && static_cast<unsigned>(c.w) < 65535u) {
+    if (coord_fields_ok(c)) {
       const unsigned long long key = pack_key(c.x, c.y, c.z, c.w);
-      const unsigned long long h = hash_mix(key) & mask;
+      const uint32_t h = static_cast<uint32_t>(hash_mix(key)) & mask;
       r = table_find(table, mask, key, h, load_slot(table, h));
     }
     rows[i] = r;
@@ -104,18 +125,20 @@ __global__ void __launch_bounds__(256) k_hash_query(const int4* __restrict__ q, 
 __device__ __forceinline__ int unpack_off(int o, int axis) { return ((o >> (10 * axis)) & 1023) - 512; }
 
 __global__ void __launch_bounds__(kThreads) k_kmap_probe(
-    const unsigned long long* __restrict__ keys, int64_t n, const Slot* __restrict__ table,
-    unsigned long long mask, int V, int K, int ndim, int dimx, int dimy, int dimz, int* __restrict__ nbr,
-    int* __restrict__ counts, int ntiles, int* __restrict__ status) {
-  extern __shared__ int4 smem4[];
-  int* s_nbr = reinterpret_cast<int*>(smem4);  // [kTile * V]
-  int* s_off = s_nbr + kTile * V;              // [V]
+    const unsigned long long* __restrict__ keys, int64_t n, const Slot* __restrict__ table, uint32_t mask, int V,
+    int K, int ndim, int dimx, int dimy, int dimz, int* __restrict__ nbr, unsigned* __restrict__ masks, int ntiles,
+    int* __restrict__ status) {
+  extern __shared__ int smem_i[];
+  int* s_off = smem_i;                                   // [V] packed offsets
+  unsigned* s_mask = reinterpret_cast<unsigned*>(smem_i + V);  // [V]
   const int tid = threadIdx.x;
   const int tile = blockIdx.x;
   const int64_t i0 = static_cast<int64_t>(tile) * kTile;
   const int np = static_cast<int>(min(static_cast<int64_t>(kTile), n - i0));
   const int r = (K - 1) / 2;
   const int centre = (V - 1) / 2;
+  // e / V as a multiply-shift: exact for e < 2^16 and V < 2^16
+  const unsigned long long magic = (1ull << 32) / static_cast<unsigned>(V) + 1ull;
   for (int v = tid; v < V; v += kThreads) {
     int d[3] = {0, 0, 0};
     int t = v;
@@ -124,25 +147,31 @@ __global__ void __launch_bounds__(kThreads) k_kmap_probe(
       t /= K;
     }
     s_off[v] = (d[0] + 512) | ((d[1] + 512) << 10) | ((d[2] + 512) << 20);
+    s_mask[v] = 0u;
   }
   __syncthreads();
 
   const int items = np * V;
+  int* dst = nbr + i0 * V;
   for (int base = 0; base < items; base += kThreads * kIlp) {
-    unsigned long long key[kIlp], slot[kIlp];
-    ulonglong2 cur[kIlp];
-    int res[kIlp];
+    unsigned long long key[kIlp];
+    uint32_t slot[kIlp];
     bool act[kIlp];
+    int res[kIlp], pnt[kIlp], off[kIlp];
 #pragma unroll
     for (int k = 0; k < kIlp; ++k) {
       const int e = base + tid + k * kThreads;
-      act[k] = false;
       res[k] = -1;
-      key[k] = 0;
+      act[k] = false;
       slot[k] = 0;
+      key[k] = 0;
+      pnt[k] = 0;
+      off[k] = 0;
       if (e < items) {
-        const int p = e / V;
+        const int p = static_cast<int>((static_cast<unsigned long long>(e) * magic) >> 32);
         const int v = e - p * V;
+        pnt[k] = p;
+        off[k] = v;
         const unsigned long long ck = __ldg(keys + i0 + p);
         if (ck != kEmptyKey) {
           int x = static_cast<int>((ck >> 32) & 0xFFFF);
@@ -160,133 +189,148 @@ __global__ void __launch_bounds__(kThreads) k_kmap_probe(
                 static_cast<unsigned>(y) < static_cast<unsigned>(dimy) &&
                 static_cast<unsigned>(z) < static_cast<unsigned>(dimz)) {
               key[k] = (ck & 0xFFFF000000000000ull) | pack_key(0, x, y, z);
-              slot[k] = hash_mix(key[k]) & mask;
+              slot[k] = static_cast<uint32_t>(hash_mix(key[k])) & mask;
               act[k] = true;
             }
           }
         }
       }
     }
+    ulonglong2 cur[kIlp];
 #pragma unroll
     for (int k = 0; k < kIlp; ++k)
       if (act[k]) cur[k] = load_slot(table, slot[k]);
 #pragma unroll
     for (int k = 0; k < kIlp; ++k) {
-      if (act[k]) res[k] = table_find(table, mask, key[k], slot[k], cur[k]);
       const int e = base + tid + k * kThreads;
-      if (e < items) s_nbr[e] = res[k];
+      if (act[k]) {
+        res[k] = table_find(table, mask, key[k], slot[k], cur[k]);
+        if (res[k] >= 0) atomicOr(&s_mask[off[k]], 1u << pnt[k]);
+      }
+      if (e < items) dst[e] = res[k];
     }
   }
   __syncthreads();
-
-  // The tile's slice of nbr is contiguous: i0*V*4 bytes is a multiple of 256.
-  int* dst = nbr + i0 * V;
-  const int n4 = items >> 2;
-  for (int e = tid; e < n4; e += kThreads)
-    reinterpret_cast<int4*>(dst)[e] = reinterpret_cast<const int4*>(s_nbr)[e];
-  for (int e = (n4 << 2) + tid; e < items; e += kThreads) dst[e] = s_nbr[e];
-
-  const int warp = tid >> 5, lane = tid & 31;
-  for (int v = warp; v < V; v += kThreads / 32) {
-    int cnt = 0;
-    if (v != centre) {
-      for (int p0 = 0; p0 < np; p0 += 32) {
-        const int p = p0 + lane;
-        cnt += __popc(__ballot_sync(0xffffffffu, p < np && s_nbr[p * V + v] >= 0));
-      }
-    }
-    if (lane == 0) counts[static_cast<int64_t>(v) * ntiles + tile] = cnt;
-  }
+  for (int v = tid; v < V; v += kThreads) masks[static_cast<int64_t>(v) * ntiles + tile] = s_mask[v];
 }
 
-// Exclusive prefix of counts[v, 0:ntiles] in place; totals[v] = sum.
-__global__ void __launch_bounds__(1024) k_kmap_scan(int* __restrict__ counts, int ntiles, int* __restrict__ totals) {
-  __shared__ int warp_sums[32];
-  const int v = blockIdx.x;
-  int* c = counts + static_cast<int64_t>(v) * ntiles;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  int carry = 0;
-  for (int base = 0; base < ntiles; base += blockDim.x) {
-    const int i = base + threadIdx.x;
-    const int x = i < ntiles ? c[i] : 0;
-    int y = x;
+// Block-wide inclusive scan of one value per thread (blockDim <= 1024).
+template <typename T>
+__device__ __forceinline__ T block_inclusive_scan(T x, T* warp_sums, T* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const T t = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += t;
+  }
+  if (lane == 31) warp_sums[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    T w = lane < nw ? warp_sums[lane] : T(0);
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int t = __shfl_up_sync(0xffffffffu, y, o);
-      if (lane >= o) y += t;
+      const T t = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += t;
     }
-    if (lane == 31) warp_sums[warp] = y;
-    __syncthreads();
-    if (warp == 0) {
-      int w = lane < nw ? warp_sums[lane] : 0;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int t = __shfl_up_sync(0xffffffffu, w, o);
-        if (lane >= o) w += t;
-      }
-      warp_sums[lane] = w;
-    }
-    __syncthreads();
-    if (i < ntiles) c[i] = carry + (warp > 0 ? warp_sums[warp - 1] : 0) + y - x;
-    carry += warp_sums[nw - 1];
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) totals[v] = carry;
-}
-
-__global__ void __launch_bounds__(kThreads) k_kmap_fill(
-    const int* __restrict__ nbr, int64_t n, int V, const int* __restrict__ bases, const int* __restrict__ totals,
-    int ntiles, int64_t* __restrict__ offs, int* __restrict__ ws_tiles, int64_t* __restrict__ map_size,
-    int* __restrict__ in_rows, int* __restrict__ out_rows) {
-  extern __shared__ int4 smem4[];
-  int* s_nbr = reinterpret_cast<int*>(smem4);                               // [kTile * V]
-  long long* s_offs = reinterpret_cast<long long*>(s_nbr + ((kTile * V + 1) & ~1));  // [V+1]
-  const int tid = threadIdx.x;
-  const int tile = blockIdx.x;
-  const int64_t i0 = static_cast<int64_t>(tile) * kTile;
-  const int np = static_cast<int>(min(static_cast<int64_t>(kTile), n - i0));
-  const int centre = (V - 1) / 2;
-  const int items = np * V;
-  const int* src = nbr + i0 * V;
-  const int n4 = items >> 2;
-  for (int e = tid; e < n4; e += kThreads)
-    reinterpret_cast<int4*>(s_nbr)[e] = __ldg(reinterpret_cast<const int4*>(src) + e);
-  for (int e = (n4 << 2) + tid; e < items; e += kThreads) s_nbr[e] = __ldg(src + e);
-  if (tid == 0) {
-    long long acc = 0;
-    for (int v = 0; v < V; ++v) {
-      s_offs[v] = acc;
-      acc += totals[v];
-    }
-    s_offs[V] = acc;
+    warp_sums[lane] = w;
   }
   __syncthreads();
-  if (tile == 0) {
-    for (int v = tid; v <= V; v += kThreads) offs[v] = s_offs[v];
-    if (tid == 0) {
-      *map_size = n + s_offs[V];
-      int t = 0;
-      for (int v = 0; v < V; ++v) {
-        ws_tiles[v] = t;
-        t += (totals[v] + kWsRows - 1) / kWsRows;
-      }
-      ws_tiles[V] = t;
+  if (warp > 0) x += warp_sums[warp - 1];
+  *total = warp_sums[nw - 1];
+  __syncthreads();
+  return x;
+}
+
+__global__ void __launch_bounds__(kScanThreads) k_kmap_scan(
+    const unsigned* __restrict__ masks, int ntiles, int V, int64_t n, int* __restrict__ bases,
+    int* __restrict__ totals, int64_t* __restrict__ offs, int* __restrict__ ws_tiles, int64_t* __restrict__ map_size,
+    int* __restrict__ ticket) {
+  __shared__ long long warp_sums[32];
+  __shared__ int s_last;
+  const int v = blockIdx.x;
+  const unsigned* m = masks + static_cast<int64_t>(v) * ntiles;
+  int* b = bases + static_cast<int64_t>(v) * ntiles;
+  // each thread takes kScanPer consecutive tiles: all loads of a chunk are in
+  // flight together, then one block scan of the per-thread sums
+  long long carry = 0;
+  for (int base = 0; base < ntiles; base += kScanThreads * kScanPer) {
+    const int i0 = base + threadIdx.x * kScanPer;
+    int c[kScanPer];
+#pragma unroll
+    for (int k = 0; k < kScanPer; ++k) c[k] = i0 + k < ntiles ? __popc(__ldg(m + i0 + k)) : 0;
+    int sum = 0;
+#pragma unroll
+    for (int k = 0; k < kScanPer; ++k) sum += c[k];
+    long long total;
+    const long long inc = block_inclusive_scan<long long>(sum, warp_sums, &total);
+    int run = static_cast<int>(carry + inc - sum);
+#pragma unroll
+    for (int k = 0; k < kScanPer; ++k) {
+      if (i0 + k < ntiles) b[i0 + k] = run;
+      run += c[k];
     }
+    carry += total;
   }
-  const int warp = tid >> 5, lane = tid & 31;
-  for (int v = warp; v < V; v += kThreads / 32) {
+  if (threadIdx.x == 0) {
+    totals[v] = static_cast<int>(carry);
+    __threadfence();
+    s_last = atomicAdd(ticket, 1) == V - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  // the last block: segment offsets, weight-stationary tile prefix, |M|
+  __threadfence();
+  const int t = threadIdx.x;
+  const long long cnt = t < V ? static_cast<long long>(__ldcg(totals + t)) : 0;
+  long long tot1, tot2;
+  const long long inc = block_inclusive_scan<long long>(cnt, warp_sums, &tot1);
+  const long long tl = (cnt + kWsRows - 1) / kWsRows;
+  const long long inc2 = block_inclusive_scan<long long>(tl, warp_sums, &tot2);
+  if (t < V) {
+    offs[t] = inc - cnt;
+    ws_tiles[t] = static_cast<int>(inc2 - tl);
+  }
+  if (t == 0) {
+    offs[V] = tot1;
+    ws_tiles[V] = static_cast<int>(tot2);
+    *map_size = n + tot1;
+    *ticket = 0;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) k_kmap_fill(const int* __restrict__ nbr, int64_t n, int V, int ntiles,
+                                                        int tiles_per_block, const int* __restrict__ bases,
+                                                        const int64_t* __restrict__ offs, int* __restrict__ in_rows,
+                                                        int* __restrict__ out_rows) {
+  extern __shared__ int smem_i[];
+  long long* s_offs = reinterpret_cast<long long*>(smem_i);    // [V]
+  int* s_base = smem_i + 2 * V;                                // [tiles_per_block * V]
+  int* s_nbr = s_base + tiles_per_block * V;                   // [tiles_per_block * 32 * V]
+  const int tile0 = blockIdx.x * tiles_per_block;
+  const int ntl = min(tiles_per_block, ntiles - tile0);
+  const int64_t i0 = static_cast<int64_t>(tile0) * kTile;
+  const int np = static_cast<int>(min(static_cast<int64_t>(ntl) * kTile, n - i0));
+  const int items = np * V;
+  const int* src = nbr + i0 * V;
+  for (int e = threadIdx.x; e < items; e += kThreads) s_nbr[e] = __ldg(src + e);
+  for (int v = threadIdx.x; v < V; v += kThreads) s_offs[v] = __ldg(offs + v);
+  for (int q = threadIdx.x; q < ntl * V; q += kThreads) {
+    const int tl = q / V, v = q - tl * V;
+    s_base[q] = __ldg(bases + static_cast<int64_t>(v) * ntiles + tile0 + tl);
+  }
+  __syncthreads();
+  const int centre = (V - 1) / 2;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int q = warp; q < ntl * V; q += kThreads / 32) {
+    const int tl = q / V, v = q - tl * V;
     if (v == centre) continue;
-    long long pos = s_offs[v] + bases[static_cast<int64_t>(v) * ntiles + tile];
-    for (int p0 = 0; p0 < np; p0 += 32) {
-      const int p = p0 + lane;
-      const int j = p < np ? s_nbr[p * V + v] : -1;
-      const unsigned b = __ballot_sync(0xffffffffu, j >= 0);
-      if (j >= 0) {
-        const long long at = pos + __popc(b & ((1u << lane) - 1u));
-        in_rows[at] = j;
-        out_rows[at] = static_cast<int>(i0 + p);
-      }
-      pos += __popc(b);
+    const int p = tl * kTile + lane;
+    const int j = p < np ? s_nbr[p * V + v] : -1;
+    const unsigned bal = __ballot_sync(0xffffffffu, j >= 0);
+    if (j >= 0) {
+      const long long at = s_offs[v] + s_base[q] + __popc(bal & ((1u << lane) - 1u));
+      in_rows[at] = j;
+      out_rows[at] = static_cast<int>(i0 + p);
     }
   }
 }
@@ -296,6 +340,11 @@ int grid_for(int64_t n, int threads) {
   int64_t g = (n + threads - 1) / threads;
   if (g > cap) g = cap;
   return static_cast<int>(g < 1 ? 1 : g);
+}
+
+int fill_tiles_per_block(int V) {
+  int t = 8192 / (kTile * V);
+  return t < 1 ? 1 : (t > 8 ? 8 : t);
 }
 
 }  // namespace
@@ -310,8 +359,8 @@ sc_status launch_hash_insert(const int32_t* coords, int64_t n, HashTable* h, cud
   if (n == 0) return SC_OK;
   SC_LAUNCH("hash_insert", s,
             k_hash_insert<<<grid_for(n, 256), 256, 0, s>>>(reinterpret_cast<const int4*>(coords), n, h->table,
-                                                           static_cast<unsigned long long>(h->capacity - 1),
-                                                           h->keys, h->status));
+                                                           static_cast<uint32_t>(h->capacity - 1), h->keys,
+                                                           h->status));
   e = cudaGetLastError();
   return e == cudaSuccess ? SC_OK : set_cuda_error(e, "hash_insert launch");
 }
@@ -320,48 +369,39 @@ sc_status launch_hash_query(const HashTable* h, const int32_t* q, int64_t m, int
   if (m == 0) return SC_OK;
   SC_LAUNCH("hash_query", s,
             k_hash_query<<<grid_for(m, 256), 256, 0, s>>>(reinterpret_cast<const int4*>(q), m, h->table,
-                                                          static_cast<unsigned long long>(h->capacity - 1),
-                                                          rows));
+                                                          static_cast<uint32_t>(h->capacity - 1), rows));
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? SC_OK : set_cuda_error(e, "hash_query launch");
 }
 
 sc_status launch_kmap_build(const HashTable* h, KernelMap* m, cudaStream_t s) {
-  cudaError_t e = cudaMemsetAsync(m->status, 0, sizeof(int), s);
-  if (e != cudaSuccess) return set_cuda_error(e, "kmap status clear");
   const int V = m->V;
+  cudaError_t e;
   if (m->n == 0) {
     e = cudaMemsetAsync(m->offs, 0, sizeof(int64_t) * (V + 1), s);
     if (e == cudaSuccess) e = cudaMemsetAsync(m->ws_tiles, 0, sizeof(int) * (V + 1), s);
     if (e == cudaSuccess) e = cudaMemsetAsync(m->map_size, 0, sizeof(int64_t), s);
     return e == cudaSuccess ? SC_OK : set_cuda_error(e, "empty kmap init");
   }
-  const size_t probe_smem = sizeof(int) * (static_cast<size_t>(kTile) * V + V);
-  const size_t fill_smem = sizeof(int) * ((static_cast<size_t>(kTile) * V + 1) & ~static_cast<size_t>(1)) +
-                           sizeof(long long) * (V + 1);
-  static bool attrs_set = false;
-  if (!attrs_set) {
-    const int max_smem = 200 * 1024;
-    cudaFuncSetAttribute(k_kmap_probe, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
-    cudaFuncSetAttribute(k_kmap_fill, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
-    attrs_set = true;
-  }
-  const unsigned long long mask = static_cast<unsigned long long>(h->capacity - 1);
+  const int tpb = fill_tiles_per_block(V);
+  const size_t probe_smem = sizeof(int) * 2 * V;
+  const size_t fill_smem = sizeof(int) * (2 * V + static_cast<size_t>(tpb) * V + static_cast<size_t>(tpb) * kTile * V);
+  const uint32_t mask = static_cast<uint32_t>(h->capacity - 1);
   SC_LAUNCH("kmap_probe", s,
             k_kmap_probe<<<m->ntiles, kThreads, probe_smem, s>>>(h->keys, m->n, h->table, mask, V, m->K, m->ndim,
                                                                   m->dims[0], m->dims[1], m->dims[2], m->nbr,
-                                                                  m->counts, m->ntiles, m->status));
+                                                                  m->masks, m->ntiles, m->status));
   e = cudaGetLastError();
   if (e != cudaSuccess) return set_cuda_error(e, "kmap_probe launch");
-  int scan_threads = 1024;
-  if (m->ntiles <= 256) scan_threads = 256;
-  SC_LAUNCH("kmap_scan", s, k_kmap_scan<<<V, scan_threads, 0, s>>>(m->counts, m->ntiles, m->totals));
+  SC_LAUNCH("kmap_scan", s,
+            k_kmap_scan<<<V, kScanThreads, 0, s>>>(m->masks, m->ntiles, V, m->n, m->bases, m->totals, m->offs,
+                                                   m->ws_tiles, m->map_size, m->status + 2));
   e = cudaGetLastError();
   if (e != cudaSuccess) return set_cuda_error(e, "kmap_scan launch");
+  const int fill_blocks = (m->ntiles + tpb - 1) / tpb;
   SC_LAUNCH("kmap_fill", s,
-            k_kmap_fill<<<m->ntiles, kThreads, fill_smem, s>>>(m->nbr, m->n, V, m->counts, m->totals, m->ntiles,
-                                                                m->offs, m->ws_tiles, m->map_size, m->in_rows,
-                                                                m->out_rows));
+            k_kmap_fill<<<fill_blocks, kThreads, fill_smem, s>>>(m->nbr, m->n, V, m->ntiles, tpb, m->bases, m->offs,
+                                                                  m->in_rows, m->out_rows));
   e = cudaGetLastError();
   return e == cudaSuccess ? SC_OK : set_cuda_error(e, "kmap_fill launch");
 }

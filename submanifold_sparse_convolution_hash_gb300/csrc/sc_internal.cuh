@@ -68,17 +68,17 @@ struct KernelMap {
   int64_t n = 0;
   int ndim = 3, K = 3, V = 27;
   int dims[3] = {1, 1, 1};
-  int ntiles = 0;                    // probe/fill tiles
+  int ntiles = 0;                    // 32-point tiles of the map build
   int* nbr = nullptr;                // [n, V]
   int64_t* offs = nullptr;           // [V+1]
   int* in_rows = nullptr;            // [n*(V-1)] capacity, offs[V] used
   int* out_rows = nullptr;
-  int* counts = nullptr;             // [V, ntiles] per-tile counts -> exclusive bases
+  unsigned* masks = nullptr;         // [V, ntiles] hit bitmask of each tile's 32 points
+  int* bases = nullptr;              // [V, ntiles] exclusive prefix of the mask popcounts
   int* totals = nullptr;             // [V]
   int* ws_tiles = nullptr;           // [V+1] prefix of ceil(count/128) per offset
   int64_t* map_size = nullptr;       // device: n + offs[V]
-  int* status = nullptr;             // device status word (map build)
-  int* hash_status = nullptr;        // borrowed pointer to the hash's word at build time
+  int* status = nullptr;             // [4]: map status, copy of the hash status, scan ticket
   // host mirrors, valid once synchronised
   bool host_valid = false;
   std::vector<int64_t> offs_host;    // [V+1]
