@@ -196,6 +196,35 @@ sc_status sc_subm_conv_tune(sc_kmap m, const void* d_feats, const void* d_W, voi
                             int c_out, sc_dtype dtype, unsigned flags, int reps, sc_stream stream,
                             unsigned* chosen);
 
+/*
+ * The layer of sc_subm_conv_fwd, computed by its fused tensor-core kernel,
+ * without allocating any memory.  The source pages have no counterpart: this
+ * entry point exists for callers that cannot call cudaMalloc (or any
+ * allocator) at this point, such as programs that plan all device memory up
+ * front and hand kernels fixed buffers, runtimes that own every allocation
+ * themselves, or latency-critical code where an allocation that may block or
+ * fail is not acceptable.
+ *
+ * The fused kernel needs temporary device memory for the weights repacked
+ * into its shared-memory layout.  Here that memory is one fixed 4 MiB device
+ * array inside the library, present on every GPU that loads the library
+ * until the process exits.  The caller still passes every input and output.
+ *
+ * Limits: f16/bf16 only; V <= 128; V * c_in * c_out * 2 bytes <= 4 MiB
+ * (4,194,304), else SC_ERR_UNSUPPORTED with a message in sc_last_error().
+ * flags: 0 or SC_RELU.  Other arguments as for sc_subm_conv_fwd.
+ *
+ * The first call on each device looks up the array's device address with
+ * cudaGetSymbolAddress while that device is current; make that first call
+ * before any stream capture.  Every call reuses the one array and overwrites
+ * all of the packed weights it uses, so nothing carries over between calls
+ * except stale bytes that are never read.  Calls whose GPU work overlaps (on
+ * different streams, or from different threads) race on the array: order
+ * them on one stream or synchronise between them.
+ */
+sc_status sc_subm_conv_fwd_noalloc(sc_kmap m, const void* d_feats, const void* d_W, void* d_out, int c_in,
+                                   int c_out, sc_dtype dtype, unsigned flags, sc_stream stream);
+
 /* ---------------------------------------------------------- diagnostics -- */
 
 const char* sc_status_str(sc_status s);

@@ -60,6 +60,7 @@ def lib():
             "sc_kmap_destroy": ([P, P], I32),
             "sc_subm_conv_fwd": ([P, P, P, P, I32, I32, I32, U, P], I32),
             "sc_subm_conv_tune": ([P, P, P, P, I32, I32, I32, U, I32, P, P], I32),
+            "sc_subm_conv_fwd_noalloc": ([P, P, P, P, I32, I32, I32, U, P], I32),
             "sc_status_str": ([I32], ctypes.c_char_p),
             "sc_last_error": ([], ctypes.c_char_p),
             "sc_launch_count": ([], I64),
@@ -79,7 +80,8 @@ def lib():
 def exported_symbols() -> list:
     return [n for n in ("sc_hash_build", "sc_hash_query", "sc_hash_info", "sc_hash_check", "sc_hash_destroy",
                         "sc_kmap_build", "sc_kmap_info", "sc_kmap_check", "sc_kmap_export", "sc_kmap_destroy",
-                        "sc_subm_conv_fwd", "sc_subm_conv_tune", "sc_status_str", "sc_last_error",
+                        "sc_subm_conv_fwd", "sc_subm_conv_tune", "sc_subm_conv_fwd_noalloc",
+                        "sc_status_str", "sc_last_error",
                         "sc_launch_count", "sc_profile_enable", "sc_profile_collect", "sc_profile_reset",
                         "sc_profile_get")]
 

@@ -490,6 +490,16 @@ sc_status sc_subm_conv_fwd(sc_kmap m, const void* d_feats, const void* d_W, void
   return run_variant(&m->k, a, variant);
 }
 
+sc_status sc_subm_conv_fwd_noalloc(sc_kmap m, const void* d_feats, const void* d_W, void* d_out, int c_in,
+                                   int c_out, sc_dtype dtype, unsigned flags, sc_stream stream) {
+  sc_status st = check_conv_args(m, d_feats, d_W, d_out, c_in, c_out, dtype);
+  if (st) return st;
+  if (flags & ~SC_RELU) return set_error(SC_ERR_INVALID_ARG, "the no-allocation conv takes SC_RELU only");
+  ConvArgs a{&m->k, d_feats, d_W, d_out, c_in, c_out, dtype, (flags & SC_RELU) != 0,
+             reinterpret_cast<cudaStream_t>(stream)};
+  return conv_fused_noalloc(a);
+}
+
 sc_status sc_subm_conv_tune(sc_kmap m, const void* d_feats, const void* d_W, void* d_out, int c_in, int c_out,
                             sc_dtype dtype, unsigned flags, int reps, sc_stream stream, unsigned* chosen) {
   sc_status st = check_conv_args(m, d_feats, d_W, d_out, c_in, c_out, dtype);

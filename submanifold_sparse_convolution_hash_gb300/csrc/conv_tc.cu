@@ -35,7 +35,14 @@
 // Every mbarrier wait is bounded (about two seconds of %globaltimer); on
 // expiry the CTA latches kDevErrTimeout, stops, and still frees its TMEM.
 
+#include <mutex>
+
 #include "sc_internal.cuh"
+
+// Packed-weight buffer of sc_subm_conv_fwd_noalloc: a fixed, file-scope
+// device array, so that entry point needs no allocation.  Every GPU that
+// loads the library holds it until the process exits.
+static __device__ __align__(256) uint8_t g_noalloc_weights[sc::kNoAllocWeightBytes];
 
 namespace sc {
 namespace {
@@ -560,6 +567,47 @@ TcParams base_params(const ConvArgs& a, const Plan& pl, const uint8_t* img) {
 }
 
 }  // namespace
+
+// Device address of g_noalloc_weights on the current device, looked up once
+// per device (host code only holds a stand-in for the symbol, which is not a
+// device address).
+static sc_status noalloc_weights_ptr(void** out) {
+  static std::mutex mu;
+  static void* addr[64] = {nullptr};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return set_cuda_error(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return set_error(SC_ERR_UNSUPPORTED, "device index above 63");
+  std::lock_guard<std::mutex> lk(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_weights);
+    if (e != cudaSuccess || !p) return set_cuda_error(e, "cudaGetSymbolAddress(g_noalloc_weights)");
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return SC_OK;
+}
+
+sc_status conv_fused_noalloc(const ConvArgs& a) {
+  // set-up first, so the first call on a device always performs it
+  void* img = nullptr;
+  sc_status st = noalloc_weights_ptr(&img);
+  if (st) return st;
+  Plan pl;
+  if (a.dtype == SC_F32 || a.m->V > 128 || !make_plan(kOutputStationary, a.m->V, a.c_in, a.c_out, &pl))
+    return set_error(SC_ERR_UNSUPPORTED, "no-allocation conv: f16/bf16 only, V <= 128, tile must fit shared memory");
+  const size_t img_bytes = static_cast<size_t>(a.m->V) * a.c_in * a.c_out * 2;
+  if (img_bytes > kNoAllocWeightBytes)
+    return set_error(SC_ERR_UNSUPPORTED,
+                     "no-allocation conv: packed weights (V * c_in * c_out * 2 bytes) exceed the 4 MiB fixed buffer");
+  if (a.m->n == 0) return SC_OK;
+  st = pack_weights(a, pl.bk, static_cast<uint8_t*>(img));
+  if (st) return st;
+  TcParams prm = base_params(a, pl, static_cast<const uint8_t*>(img));
+  const int grid = static_cast<int>((a.m->n + kRows - 1) / kRows);
+  return dispatch_tc<kOutputStationary>(prm, pl, a.dtype == SC_BF16, grid, a.stream, "subm_conv_fused");
+}
 
 bool fused_supported(const ConvArgs& a) {
   Plan pl;

@@ -87,6 +87,9 @@ struct KernelMap {
   std::vector<ConvChoice> tuned;
 };
 
+// Size of the fixed packed-weight buffer behind sc_subm_conv_fwd_noalloc.
+constexpr size_t kNoAllocWeightBytes = size_t(4) << 20;
+
 // ------------------------------------------------------------ launching --
 // Launch bookkeeping shared by every translation unit: counts launches and,
 // while profiling is on, brackets each launch with CUDA events.
@@ -121,6 +124,7 @@ sc_status conv_fused(const ConvArgs& a);
 sc_status conv_weight_stationary(const ConvArgs& a);
 sc_status conv_simt(const ConvArgs& a);
 bool fused_supported(const ConvArgs& a);
+sc_status conv_fused_noalloc(const ConvArgs& a);
 
 // stream-ordered allocation helpers
 sc_status dev_alloc(void** p, size_t bytes, cudaStream_t s);
