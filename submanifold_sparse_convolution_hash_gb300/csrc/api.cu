@@ -378,7 +378,7 @@ sc_status sc_kmap_destroy(sc_kmap m, sc_stream stream) {
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   KernelMap& k = m->k;
   for (void* p : {static_cast<void*>(k.nbr), static_cast<void*>(k.offs), static_cast<void*>(k.in_rows),
-                  static_cast<void*>(k.out_rows), static_cast<void*>(k.masks), static_cast<void*>(k.bases), static_cast<void*>(k.totals),
+                  static_cast<void*>(k.out_rows), static_cast<void*>(k.masks), static_cast<void*>(k.present), static_cast<void*>(k.bases), static_cast<void*>(k.totals),
                   static_cast<void*>(k.ws_tiles), static_cast<void*>(k.map_size), static_cast<void*>(k.status)})
     dev_free(p, s);
   delete m;
@@ -419,6 +419,7 @@ sc_status sc_kmap_build(sc_hash h, int ndim, int K, const int32_t dims[3], unsig
   if (!st) st = dev_alloc(reinterpret_cast<void**>(&k.out_rows), sizeof(int) * lists, s);
   if (!st) st = dev_alloc(reinterpret_cast<void**>(&k.masks), sizeof(unsigned) * static_cast<size_t>(V) * k.ntiles, s);
   if (!st) st = dev_alloc(reinterpret_cast<void**>(&k.bases), sizeof(int) * static_cast<size_t>(V) * k.ntiles, s);
+  if (!st) st = dev_alloc(reinterpret_cast<void**>(&k.present), sizeof(unsigned) * 4 * ((k.n + 127) / 128), s);
   if (!st) st = dev_alloc(reinterpret_cast<void**>(&k.totals), sizeof(int) * V, s);
   if (!st) st = dev_alloc(reinterpret_cast<void**>(&k.ws_tiles), sizeof(int) * (V + 1), s);
   if (!st) st = dev_alloc(reinterpret_cast<void**>(&k.map_size), sizeof(int64_t), s);

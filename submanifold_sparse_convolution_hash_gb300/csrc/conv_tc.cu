@@ -4,36 +4,47 @@
 // (exam sheet "Sparse convolution for point clouds", "The map and the update
 // rule"; "Sparse inputs and sparse convolution", "The map is the computation").
 //
-// Two dataflows share one CTA mainloop:
+// Two dataflows share one persistent, warp-specialised kernel:
 //
 //  * Output-stationary implicit GEMM ("TorchSparse optimizations", section
 //    "TorchSparse++": each block owns a tile of output rows, walks the
-//    weights, fetches the matching input rows on demand and writes each
-//    output once).  A CTA owns 128 output rows.  Its K dimension is the
-//    concatenation over offsets d of the C_in input channels; an offset with
-//    no neighbour in any of the 128 rows is skipped for the whole tile
-//    (the lockstep redundancy of that section is what remains).  Absent
-//    neighbours are zero rows (cp.async with source size 0).
+//    weights, fetches the matching input rows on demand and writes each output
+//    once).  A tile is 128 output rows; its K dimension is the concatenation
+//    over offsets d of the C_in input channels.  An offset with no neighbour
+//    in any of the tile's rows is skipped (the map build records, per tile,
+//    which offsets occur); absent neighbours inside a present offset are zero
+//    rows.  That remaining waste is the lockstep redundancy the section
+//    describes.
 //
 //  * Weight-stationary gather -> GEMM -> scatter ("Sparse inputs and sparse
-//    convolution", section "Gather, matmul, scatter"; "TorchSparse
-//    optimizations", opening section).  A CTA owns 128 tuples of one offset,
-//    gathers their input rows, multiplies by W[d] and scatter-adds fp32
-//    results with vector atomics.  The centre offset (identity map) writes its
-//    product with plain stores first.
+//    convolution", section "Gather, matmul, scatter").  A tile is 128 tuples
+//    of one offset: gather their input rows, multiply by W[d], scatter-add the
+//    fp32 products with vector atomics.  The centre offset (identity map)
+//    writes its product with plain stores first.
 //
-// CTA layout (160 threads):
-//   warps 0-3  gather A rows with cp.async into a 128B/64B/32B-swizzled
-//              K-major tile, then run the epilogue (TMEM lane = row).
-//   warp 4     allocates TMEM; lane 0 issues tcgen05.mma (M=128, N=C_out,
-//              K=16) from shared-memory descriptors and commits each stage
-//              back to the producers.
-// W slices arrive by cp.async.bulk from a pre-swizzled image in global memory
-// (one image per (offset, 16/32/64-channel panel)), so A and B share one
-// K-major layout.  Accumulators live in TMEM (C_out fp32 columns).
+// CTA (288 threads; as many per SM as shared memory and TMEM allow, each
+// taking tiles round-robin):
+//   warps 0-3  producers: per pipeline stage, each thread cp.asyncs 16-byte
+//              chunks of its tile rows' neighbour feature rows into a
+//              swizzled K-major tile (four lanes per 64-byte row, so a warp
+//              instruction covers whole rows; a missing neighbour is a
+//              zero-filled copy of size 0); thread 0 bulk-copies the matching
+//              W slices from a pre-swizzled image.  A stage holds G (offset,
+//              channel-panel) sub-blocks.  Each warp signals a stage LAG
+//              stages later, after its copies landed and a proxy fence.
+//   warp 4     allocates TMEM (two accumulators of C_out fp32 columns); lane 0
+//              issues tcgen05.mma (M = 128, N = C_out, K = 16) and commits.
+//   warps 5-8  epilogue: TMEM lane quadrant (warp % 4) -> registers -> global,
+//              overlapping the next tile's mainloop through the second
+//              accumulator.
+// The row gathers use the load/store path: a TMA tile::gather4 moves four
+// rows per instruction but its row rate, not its byte rate, bounds it, and
+// for 32-256 byte rows that rate is several times below what cp.async from
+// four warps sustains.
 //
 // Every mbarrier wait is bounded (about two seconds of %globaltimer); on
-// expiry the CTA latches kDevErrTimeout, stops, and still frees its TMEM.
+// expiry the CTA latches kDevErrTimeout, stops issuing work, waits (bounded)
+// for what it issued, and still frees its TMEM.
 
 #include <mutex>
 
@@ -47,10 +58,11 @@ static __device__ __align__(256) uint8_t g_noalloc_weights[sc::kNoAllocWeightByt
 namespace sc {
 namespace {
 
-constexpr int kRows = 128;        // rows per CTA tile (MMA M)
-constexpr int kThreads = 160;     // 4 producer/epilogue warps + 1 MMA warp
-constexpr int kLag = 2;           // cp.async groups kept in flight per producer thread
-constexpr int kMaxStages = 6;
+constexpr int kRows = 128;        // rows per tile (MMA M)
+constexpr int kThreads = 288;     // 4 producer warps, MMA warp, 4 epilogue warps
+constexpr int kProducers = 128;
+constexpr int kMaxStages = 8;
+constexpr int kBarriers = 2 * kMaxStages + 5;  // full[S], empty[S], acc_full[2], acc_empty[2], done
 constexpr unsigned long long kWaitNs = 2000000000ull;
 
 enum Mode { kOutputStationary = 0, kWsScatter = 1, kWsCentre = 2 };
@@ -100,21 +112,39 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile i
   }
   return false;
 }
-__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+// Same bound, ignoring the abort flag: used to drain work already issued.
+__device__ __noinline__ bool mbar_drain(uint32_t bar, uint32_t parity) {
+  const unsigned long long t0 = globaltimer();
+  for (uint32_t it = 0; it < (1u << 30); ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63) == 63 && globaltimer() - t0 > kWaitNs) return false;
+  }
+  return false;
 }
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                "l"(src), "r"(bytes), "r"(bar)
                : "memory");
+}
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Waits until at most `n` (0..4) of this thread's cp.async groups are pending.
+__device__ __forceinline__ void cp_async_wait_dyn(int n) {
+  switch (n) {
+    case 0: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
+    case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
+    case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
+    case 3: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
+    default: asm volatile("cp.async.wait_group 4;" ::: "memory"); break;
+  }
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
@@ -176,9 +206,9 @@ __host__ __device__ constexpr uint32_t make_idesc(bool bf16, int M, int N) {
 // address bits [4, 4+b) XOR bits [7, 7+b) with row pitch = swizzle width.
 template <int BK>
 __host__ __device__ __forceinline__ int swz(int row) {
-  if constexpr (BK == 64) return row & 7;          // 128-byte rows
-  else if constexpr (BK == 32) return (row >> 1) & 3;  // 64-byte rows
-  else return (row >> 2) & 1;                      // 32-byte rows
+  if constexpr (BK == 64) return row & 7;               // 128-byte rows
+  else if constexpr (BK == 32) return (row >> 1) & 3;   // 64-byte rows
+  else return (row >> 2) & 1;                           // 32-byte rows
 }
 template <int BK>
 constexpr uint32_t layout_code() {
@@ -191,19 +221,43 @@ struct TcParams {
   uint8_t* out;              // output-stationary: [n, c_out] 2-byte elements
   float* acc;                // weight-stationary: fp32 [n, c_out]
   const int* nbr;            // [n, V]
+  const uint4* present;      // [tiles]: 128-bit mask of the offsets present in each 128-row tile
   const int* in_rows;        // weight-stationary lists
   const int* out_rows;
   const int64_t* offs;       // [V+1]
   const int* ws_tiles;       // [V+1]
   int64_t n;
-  int V, c_in, c_out, relu, stages, tmem_cols;
+  int num_tiles;
+  int V, c_in, c_out, relu, stages, group, lag, acc_cols, tmem_cols;
   int* status;
 };
 
-__device__ __forceinline__ int next_present(const uint32_t* mask, int v, int V) {
-  for (int u = v + 1; u < V; ++u)
-    if (mask[u >> 5] & (1u << (u & 31))) return u;
+// Next offset after v whose bit is set in the 4-word mask m (V if none).
+__device__ __forceinline__ int next_present(const uint4& m, int v, int V) {
+  const int u = v + 1;
+  const uint32_t w[4] = {m.x, m.y, m.z, m.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int lo = 32 * k;
+    if (u < lo + 32) {
+      const uint32_t x = u <= lo ? w[k] : (w[k] & (0xFFFFFFFFu << (u - lo)));
+      if (x) {
+        const int r = lo + __ffs(x) - 1;
+        return r < V ? r : V;
+      }
+    }
+  }
   return V;
+}
+
+// The tile's present-offset mask with the centre offset added (every tile has
+// at least one row, and every row has itself as a neighbour).
+__device__ __forceinline__ uint4 tile_mask(const TcParams& p, int tile) {
+  uint4 m = __ldg(p.present + tile);
+  const int c = (p.V - 1) / 2;
+  const uint32_t bit = 1u << (c & 31);
+  if (c < 32) m.x |= bit; else if (c < 64) m.y |= bit; else if (c < 96) m.z |= bit; else m.w |= bit;
+  return m;
 }
 
 template <bool BF16>
@@ -217,208 +271,293 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
   }
 }
 
+// Rows, list base and (for the weight-stationary scatter) offset of a tile.
+struct TileInfo {
+  int64_t row0;  // first output row (output-stationary, centre)
+  int64_t lb;    // first list entry (weight-stationary scatter)
+  int nrows;
+  int v;         // the offset of a weight-stationary tile
+};
+
+template <int MODE>
+__device__ __forceinline__ TileInfo tile_info(const TcParams& p, int tile) {
+  TileInfo t;
+  t.row0 = 0;
+  t.lb = 0;
+  t.v = (p.V - 1) / 2;
+  if (MODE == kWsScatter) {
+    int lo = 0, hi = p.V;  // largest v with ws_tiles[v] <= tile
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (__ldg(p.ws_tiles + mid) <= tile) lo = mid; else hi = mid;
+    }
+    t.v = lo;
+    const int64_t seg_end = __ldg(p.offs + lo + 1);
+    t.lb = __ldg(p.offs + lo) + static_cast<int64_t>(tile - __ldg(p.ws_tiles + lo)) * kRows;
+    t.nrows = static_cast<int>(min(static_cast<int64_t>(kRows), seg_end - t.lb));
+  } else {
+    t.row0 = static_cast<int64_t>(tile) * kRows;
+    t.nrows = static_cast<int>(min(static_cast<int64_t>(kRows), p.n - t.row0));
+  }
+  return t;
+}
+
+template <int MODE>
+__device__ __forceinline__ int tile_kblocks(const TcParams& p, int tile, int P) {
+  if (MODE != kOutputStationary) return P;
+  const uint4 m = tile_mask(p, tile);
+  return (__popc(m.x) + __popc(m.y) + __popc(m.z) + __popc(m.w)) * P;
+}
+
 template <int BK, int MODE, bool BF16>
 __global__ void __launch_bounds__(kThreads) k_conv_tc(const TcParams p) {
-  constexpr int ROWB = BK * 2;        // bytes per tile row (= swizzle width)
-  constexpr int CPR = ROWB / 16;      // 16-byte chunks per row
-  constexpr int A_BYTES = kRows * ROWB;
+  constexpr int ROWB = BK * 2;          // bytes per tile row (= swizzle width)
+  constexpr int A_SUB = kRows * ROWB;   // one (offset, panel) sub-block of A
+  constexpr int CPR = ROWB / 16;        // 16-byte chunks per row
+  constexpr int RPT = CPR;              // rows per producer thread
+  constexpr int RSTEP = kProducers / CPR;
   constexpr uint32_t LAYOUT = layout_code<BK>();
   constexpr uint32_t SBO = 8 * ROWB;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int S = p.stages;
-  const int B_BYTES = p.c_out * ROWB;
+  const int S = p.stages, G = p.group;
+  const int B_SUB = p.c_out * ROWB;
   uint8_t* sA = smem;
-  uint8_t* sB = sA + S * A_BYTES;
-  int* sRows = reinterpret_cast<int*>(sB + S * B_BYTES);
-  const int rows_ints = MODE == kOutputStationary ? kRows * p.V : 2 * kRows;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sRows + ((rows_ints + 1) & ~1));
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2 * S + 1);
+  uint8_t* sB = sA + S * G * A_SUB;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + S * G * B_SUB);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + kBarriers);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
-  uint32_t* s_mask = s_tmem + 2;  // up to 4 words: offsets present in the tile
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int P = p.c_in / BK;
   const int V = p.V;
-  const int centre = (V - 1) / 2;
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kMaxStages);
+  const uint32_t accf0 = smem_u32(bars + 2 * kMaxStages), acce0 = smem_u32(bars + 2 * kMaxStages + 2);
+  const uint32_t done_bar = smem_u32(bars + 2 * kMaxStages + 4);
 
-  // ---- tile bounds
-  int64_t row0 = 0, lb = 0;
-  int nrows = 0, v_ws = centre;
-  if (MODE == kWsScatter) {
-    int lo = 0, hi = V;  // largest v with ws_tiles[v] <= blockIdx.x
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (__ldg(p.ws_tiles + mid) <= static_cast<int>(blockIdx.x)) lo = mid; else hi = mid;
-    }
-    v_ws = lo;
-    const int64_t seg_end = __ldg(p.offs + v_ws + 1);
-    lb = __ldg(p.offs + v_ws) + static_cast<int64_t>(blockIdx.x - __ldg(p.ws_tiles + v_ws)) * kRows;
-    nrows = static_cast<int>(min(static_cast<int64_t>(kRows), seg_end - lb));
-  } else {
-    row0 = static_cast<int64_t>(blockIdx.x) * kRows;
-    nrows = static_cast<int>(min(static_cast<int64_t>(kRows), p.n - row0));
-  }
-
-  // ---- setup: barriers, TMEM, rows of the tile
-  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S), accum_bar = smem_u32(bars + 2 * S);
-  if (threadIdx.x == 128) {
+  if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(full0 + 8 * s, 5);   // 4 producer warps + the expect_tx arrival
+      mbar_init(full0 + 8 * s, 5);   // 4 producer warps + the expect_tx arrival (+ weight bytes)
       mbar_init(empty0 + 8 * s, 1);  // one tcgen05.commit
     }
-    mbar_init(accum_bar, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accf0 + 8 * b, 1);   // one tcgen05.commit per tile
+      mbar_init(acce0 + 8 * b, 4);   // one arrival per epilogue warp
+    }
+    mbar_init(done_bar, 1);
     *s_abort = 0;
-    s_mask[0] = s_mask[1] = s_mask[2] = s_mask[3] = 0;
     fence_mbar_init();
   }
   if (warp == 4) {
     tmem_alloc(smem_u32(s_tmem), static_cast<uint32_t>(p.tmem_cols));
     tmem_relinquish();
   }
-  if (threadIdx.x < kRows) {
-    if (MODE == kOutputStationary) {
-      const int valid = nrows * V;
-      const int* src = p.nbr + row0 * V;
-      for (int e = threadIdx.x; e < kRows * V; e += kRows) sRows[e] = e < valid ? __ldg(src + e) : -1;
-    } else if (MODE == kWsScatter) {
-      const int r = threadIdx.x;
-      sRows[r] = r < nrows ? __ldg(p.in_rows + lb + r) : -1;
-      sRows[kRows + r] = r < nrows ? __ldg(p.out_rows + lb + r) : -1;
-    } else {
-      const int r = threadIdx.x;
-      sRows[r] = r < nrows ? static_cast<int>(row0 + r) : -1;
-    }
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
 
-  int nkb;
-  int v_first;
-  if (MODE == kOutputStationary) {
-    if (warp < 4) {
-      for (int v = warp; v < V; v += 4) {
-        bool any = false;
-        for (int r = lane; r < kRows; r += 32) any |= sRows[r * V + v] >= 0;
-        if (__any_sync(0xffffffffu, any) && lane == 0) atomicOr(&s_mask[v >> 5], 1u << (v & 31));
-      }
-    }
-    __syncthreads();
-    nkb = (__popc(s_mask[0]) + __popc(s_mask[1]) + __popc(s_mask[2]) + __popc(s_mask[3])) * P;
-    v_first = next_present(s_mask, -1, V);
-  } else {
-    nkb = P;
-    v_first = v_ws;
-  }
-
   if (warp < 4) {
-    // ================= producers: gather A rows, request B slices
-    int v = v_first, pnl = 0;
-    bool ok = true;
-    for (int i = 0; i < nkb; ++i) {
-      const int s = i % S;
-      const uint32_t ph = static_cast<uint32_t>(i / S) & 1u;
-      if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, s_abort)) {
-        ok = false;
-        break;
+    // ======================================================= producers
+    const int pt = threadIdx.x;         // 0..127
+    const int chunk = pt % CPR;         // 16-byte chunk of a row
+    const int rbase = pt / CPR;         // rows rbase + RSTEP * k, k < RPT
+    const int lag = p.lag;
+    uint32_t it = 0;
+    if (MODE == kOutputStationary && pt == 0 && static_cast<int>(blockIdx.x) < p.num_tiles) {
+      const TileInfo t0 = tile_info<MODE>(p, blockIdx.x);
+      const uint32_t bytes = (static_cast<uint32_t>(t0.nrows) * V * 4) & ~15u;
+      if (bytes) bulk_prefetch_l2(p.nbr + t0.row0 * V, bytes);
+    }
+    for (int tile = blockIdx.x; tile < p.num_tiles && !*s_abort; tile += gridDim.x) {
+      const TileInfo t = tile_info<MODE>(p, tile);
+      uint4 m = make_uint4(0, 0, 0, 0);
+      int v = t.v;
+      if (MODE == kOutputStationary) {
+        m = tile_mask(p, tile);
+        v = next_present(m, -1, V);
+        const int nt = tile + gridDim.x;
+        if (pt == 0 && nt < p.num_tiles) {
+          const TileInfo tn = tile_info<MODE>(p, nt);
+          const uint32_t bytes = (static_cast<uint32_t>(tn.nrows) * V * 4) & ~15u;
+          if (bytes) bulk_prefetch_l2(p.nbr + tn.row0 * V, bytes);
+        }
       }
-      if (threadIdx.x == 0) {
-        mbar_arrive_expect_tx(full0 + 8 * s, static_cast<uint32_t>(B_BYTES));
-        bulk_g2s(smem_u32(sB + s * B_BYTES), p.wimg + (static_cast<size_t>(v) * P + pnl) * B_BYTES,
-                 static_cast<uint32_t>(B_BYTES), full0 + 8 * s);
-      }
-      const uint32_t a_base = smem_u32(sA + s * A_BYTES);
+      const int nkb = tile_kblocks<MODE>(p, tile, P);
+      // source rows of this thread's tile rows for the current offset
+      int src[RPT];
+      auto load_rows = [&](int vv) {
 #pragma unroll
-      for (int k = 0; k < CPR; ++k) {
-        const int e = threadIdx.x + kRows * k;
-        const int r = e / CPR, c = e % CPR;
-        const int j = MODE == kOutputStationary ? sRows[r * V + v] : sRows[r];
-        const uint8_t* src =
-            p.feats + (static_cast<size_t>(j < 0 ? 0 : j) * p.c_in + static_cast<size_t>(pnl) * BK) * 2 + c * 16;
-        cp_async_16(a_base + r * ROWB + ((c ^ swz<BK>(r)) << 4), src, j >= 0 ? 16u : 0u);
-      }
-      cp_async_commit();
-      if (i >= kLag) {
-        cp_async_wait<kLag>();
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(full0 + 8 * ((i - kLag) % S));
-      }
-      if (++pnl == P) {
-        pnl = 0;
-        v = MODE == kOutputStationary ? next_present(s_mask, v, V) : v;
+        for (int k = 0; k < RPT; ++k) {
+          const int r = rbase + RSTEP * k;
+          int j = -1;
+          if (r < t.nrows) {
+            if (MODE == kOutputStationary) j = __ldg(p.nbr + (t.row0 + r) * V + vv);
+            else if (MODE == kWsScatter) j = __ldg(p.in_rows + t.lb + r);
+            else j = static_cast<int>(t.row0 + r);
+          }
+          src[k] = j;
+        }
+      };
+      load_rows(v);
+      int pnl = 0;
+      for (int kb = 0; kb < nkb; kb += G, ++it) {
+        const int s = static_cast<int>(it % S);
+        const uint32_t ph = (it / S) & 1u;
+        if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, s_abort)) {
+          *s_abort = 1;
+          break;
+        }
+        const int gc = min(G, nkb - kb);
+        if (pt == 0) mbar_arrive_expect_tx(full0 + 8 * s, static_cast<uint32_t>(gc * B_SUB));
+        int bv = v, bp = pnl;  // the W slices follow the same (offset, panel) sequence
+        for (int g = 0; g < gc; ++g) {
+          if (pt == 0) {
+            bulk_g2s(smem_u32(sB + (s * G + g) * B_SUB), p.wimg + (static_cast<size_t>(bv) * P + bp) * B_SUB,
+                     static_cast<uint32_t>(B_SUB), full0 + 8 * s);
+            if (++bp == P) {
+              bp = 0;
+              if (MODE == kOutputStationary) bv = next_present(m, bv, V);
+            }
+          }
+          const uint32_t a_base = smem_u32(sA + (s * G + g) * A_SUB);
+#pragma unroll
+          for (int k = 0; k < RPT; ++k) {
+            const int r = rbase + RSTEP * k;
+            const int j = src[k];
+            const uint8_t* g_src = p.feats + (static_cast<size_t>(j < 0 ? 0 : j) * p.c_in +
+                                              static_cast<size_t>(pnl) * BK) * 2 + chunk * 16;
+            cp_async_16(a_base + r * ROWB + ((chunk ^ swz<BK>(r)) << 4), g_src, j >= 0 ? 16u : 0u);
+          }
+          if (++pnl == P) {
+            pnl = 0;
+            if (MODE == kOutputStationary) {
+              v = next_present(m, v, V);
+              if (v < V) load_rows(v);
+            }
+          }
+        }
+        cp_async_commit();
+        if (it >= static_cast<uint32_t>(lag)) {
+          cp_async_wait_dyn(lag);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(full0 + 8 * ((it - lag) % S));
+        }
       }
     }
-    cp_async_wait<0>();
+    // signal the stages still owed, once their copies have landed
+    cp_async_wait_dyn(0);
     fence_proxy_async_smem();
     __syncwarp();
-    if (ok && lane == 0)
-      for (int i = (nkb > kLag ? nkb - kLag : 0); i < nkb; ++i) mbar_arrive(full0 + 8 * (i % S));
-    if (!ok) *s_abort = 1;
-
-    // ================= epilogue: TMEM lane (warp*32 + lane) holds tile row r
-    const bool done = ok && mbar_wait(accum_bar, 0, s_abort);
-    tc_fence_after();
-    const int r = warp * 32 + lane;
-    const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    for (int c0 = 0; c0 < p.c_out; c0 += 16) {
-      float acc[16];
-      tmem_ld16(trow + static_cast<uint32_t>(c0), acc);
-      if (!done || r >= nrows) continue;
-      if (MODE == kOutputStationary) {
-        if (p.relu) {
-#pragma unroll
-          for (int k = 0; k < 16; ++k) acc[k] = fmaxf(acc[k], 0.0f);
-        }
-        uint4 lo, hi;
-        lo.x = pack2<BF16>(acc[0], acc[1]);
-        lo.y = pack2<BF16>(acc[2], acc[3]);
-        lo.z = pack2<BF16>(acc[4], acc[5]);
-        lo.w = pack2<BF16>(acc[6], acc[7]);
-        hi.x = pack2<BF16>(acc[8], acc[9]);
-        hi.y = pack2<BF16>(acc[10], acc[11]);
-        hi.z = pack2<BF16>(acc[12], acc[13]);
-        hi.w = pack2<BF16>(acc[14], acc[15]);
-        uint4* dst = reinterpret_cast<uint4*>(p.out + ((row0 + r) * p.c_out + c0) * 2);
-        dst[0] = lo;
-        dst[1] = hi;
-      } else if (MODE == kWsScatter) {
-        float4* dst = reinterpret_cast<float4*>(p.acc + static_cast<int64_t>(sRows[kRows + r]) * p.c_out + c0);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) atomicAdd(dst + k, make_float4(acc[4 * k], acc[4 * k + 1], acc[4 * k + 2], acc[4 * k + 3]));
-      } else {
-        float4* dst = reinterpret_cast<float4*>(p.acc + (row0 + r) * p.c_out + c0);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) dst[k] = make_float4(acc[4 * k], acc[4 * k + 1], acc[4 * k + 2], acc[4 * k + 3]);
-      }
+    if (lane == 0)
+      for (uint32_t k = it > static_cast<uint32_t>(lag) ? it - lag : 0; k < it; ++k) mbar_arrive(full0 + 8 * (k % S));
+    // the weight bulk copies of the last stages have landed before the CTA may exit
+    if (pt == 0) {
+      const uint32_t first = it > static_cast<uint32_t>(S) ? it - S : 0;
+      for (uint32_t k = first; k < it; ++k)
+        if (!mbar_drain(full0 + 8 * (k % S), (k / S) & 1u)) *s_abort = 1;
     }
-    if (!done) *s_abort = 1;
-  } else {
-    // ================= MMA issuer
+  } else if (warp == 4) {
+    // ======================================================= MMA issuer
     if (lane == 0) {
       const uint32_t idesc = make_idesc(BF16, kRows, p.c_out);
-      for (int i = 0; i < nkb; ++i) {
-        const int s = i % S;
-        const uint32_t ph = static_cast<uint32_t>(i / S) & 1u;
-        if (!mbar_wait(full0 + 8 * s, ph, s_abort)) {
+      uint32_t it = 0;
+      int j = 0;
+      for (int tile = blockIdx.x; tile < p.num_tiles && !*s_abort; tile += gridDim.x, ++j) {
+        const int nkb = tile_kblocks<MODE>(p, tile, P);
+        const int b = j & 1;
+        if (!mbar_wait(acce0 + 8 * b, ((j >> 1) & 1) ^ 1, s_abort)) {
           *s_abort = 1;
           break;
         }
         tc_fence_after();
-        const uint32_t a_addr = smem_u32(sA + s * A_BYTES);
-        const uint32_t b_addr = smem_u32(sB + s * B_BYTES);
+        const uint32_t d = tmem + static_cast<uint32_t>(b * p.acc_cols);
+        uint32_t accumulate = 0;
+        for (int kb = 0; kb < nkb; kb += G, ++it) {
+          const int s = static_cast<int>(it % S);
+          const uint32_t ph = (it / S) & 1u;
+          if (!mbar_wait(full0 + 8 * s, ph, s_abort)) {
+            *s_abort = 1;
+            break;
+          }
+          tc_fence_after();
+          const int gc = min(G, nkb - kb);
+          for (int g = 0; g < gc; ++g) {
+            const uint32_t a_addr = smem_u32(sA + (s * G + g) * A_SUB);
+            const uint32_t b_addr = smem_u32(sB + (s * G + g) * B_SUB);
 #pragma unroll
-        for (int k = 0; k < BK / 16; ++k)
-          tc_mma(tmem, smem_desc(a_addr + 32 * k, SBO, LAYOUT), smem_desc(b_addr + 32 * k, SBO, LAYOUT), idesc,
-                 (i | k) != 0 ? 1u : 0u);
-        tc_commit(empty0 + 8 * s);
+            for (int k = 0; k < BK / 16; ++k) {
+              tc_mma(d, smem_desc(a_addr + 32 * k, SBO, LAYOUT), smem_desc(b_addr + 32 * k, SBO, LAYOUT), idesc,
+                     accumulate);
+              accumulate = 1;
+            }
+          }
+          tc_commit(empty0 + 8 * s);
+        }
+        tc_commit(accf0 + 8 * b);  // arrives once every MMA of the tile has completed
       }
-      tc_commit(accum_bar);  // arrives once every MMA issued above has completed
+      // all tcgen05 work of this thread has completed before TMEM is released
+      tc_commit(done_bar);
+      if (!mbar_drain(done_bar, 0)) *s_abort = 1;
     }
     __syncwarp();
+  } else {
+    // ======================================================= epilogue
+    const int q = warp & 3;             // TMEM lane quadrant of this warp
+    const int r = q * 32 + lane;        // tile row held by this thread
+    int j = 0;
+    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++j) {
+      const TileInfo t = tile_info<MODE>(p, tile);
+      const int b = j & 1;
+      if (*s_abort || !mbar_wait(accf0 + 8 * b, (j >> 1) & 1, s_abort)) {
+        *s_abort = 1;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t trow = tmem + static_cast<uint32_t>(b * p.acc_cols) + (static_cast<uint32_t>(q * 32) << 16);
+      int dst_row = -1;
+      if (r < t.nrows) {
+        if (MODE == kWsScatter) dst_row = __ldg(p.out_rows + t.lb + r);
+        else dst_row = static_cast<int>(t.row0 + r);
+      }
+      for (int c0 = 0; c0 < p.c_out; c0 += 16) {
+        float a[16];
+        tmem_ld16(trow + static_cast<uint32_t>(c0), a);
+        if (dst_row < 0) continue;
+        if (MODE == kOutputStationary) {
+          if (p.relu) {
+#pragma unroll
+            for (int k = 0; k < 16; ++k) a[k] = fmaxf(a[k], 0.0f);
+          }
+          uint4 lo, hi;
+          lo.x = pack2<BF16>(a[0], a[1]);
+          lo.y = pack2<BF16>(a[2], a[3]);
+          lo.z = pack2<BF16>(a[4], a[5]);
+          lo.w = pack2<BF16>(a[6], a[7]);
+          hi.x = pack2<BF16>(a[8], a[9]);
+          hi.y = pack2<BF16>(a[10], a[11]);
+          hi.z = pack2<BF16>(a[12], a[13]);
+          hi.w = pack2<BF16>(a[14], a[15]);
+          uint4* dst = reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(dst_row) * p.c_out + c0) * 2);
+          dst[0] = lo;
+          dst[1] = hi;
+        } else if (MODE == kWsScatter) {
+          float4* dst = reinterpret_cast<float4*>(p.acc + static_cast<int64_t>(dst_row) * p.c_out + c0);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            atomicAdd(dst + k, make_float4(a[4 * k], a[4 * k + 1], a[4 * k + 2], a[4 * k + 3]));
+        } else {
+          float4* dst = reinterpret_cast<float4*>(p.acc + static_cast<int64_t>(dst_row) * p.c_out + c0);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) dst[k] = make_float4(a[4 * k], a[4 * k + 1], a[4 * k + 2], a[4 * k + 3]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acce0 + 8 * b);
+    }
   }
 
   tc_fence_before();
@@ -481,51 +620,70 @@ __global__ void __launch_bounds__(256) k_cast_out(const float4* __restrict__ acc
 // ------------------------------------------------------------ host side --
 struct Plan {
   int bk;
+  int group;
   int stages;
+  int lag;
+  int ctas_per_sm;
   size_t smem;
+  int acc_cols;
   int tmem_cols;
 };
 
 int pick_bk(int c_in) { return c_in % 64 == 0 ? 64 : (c_in % 32 == 0 ? 32 : 16); }
 
-bool make_plan(int mode, int V, int c_in, int c_out, Plan* pl) {
+// Pipeline shape.  Gathers are latency bound, and measured throughput grows
+// with the number of producer warps per SM, not with pipeline depth, so the
+// plan keeps three stages (one cp.async group in flight per producer thread
+// beyond the one being filled) and fits as many CTAs per SM as shared memory
+// (about 220 KB) and TMEM (512 columns, two accumulators per CTA) allow.
+bool make_plan(int c_in, int c_out, Plan* pl) {
   pl->bk = pick_bk(c_in);
   const size_t a = static_cast<size_t>(kRows) * pl->bk * 2;
   const size_t b = static_cast<size_t>(c_out) * pl->bk * 2;
-  const size_t rows = sizeof(int) * ((mode == kOutputStationary ? static_cast<size_t>(kRows) * V : 2 * kRows) + 1);
-  const size_t fixed = 1024 /*alignment slack*/ + 8 * (2 * kMaxStages + 1) + 64;
-  const size_t budget = 220 * 1024;
-  if (rows + fixed + 3 * (a + b) > budget) return false;
-  int s = static_cast<int>((budget - rows - fixed) / (a + b));
-  if (s > 4) s = 4;
-  pl->stages = s;
-  pl->smem = fixed + rows + s * (a + b);
+  // sub-blocks per stage: stages of about 24 KB
+  int g = static_cast<int>((24 * 1024) / (a + b));
+  if (g < 1) g = 1;
+  if (g > 4) g = 4;
+  pl->group = g;
+  const size_t stage = g * (a + b);
+  const size_t fixed = 1024 /*alignment slack*/ + 8 * kBarriers + 16;
+  pl->stages = 3;
+  pl->lag = 1;
+  pl->smem = fixed + pl->stages * stage;
+  if (pl->smem > 220 * 1024) return false;
   int cols = 32;
   while (cols < c_out) cols <<= 1;
-  pl->tmem_cols = cols;
+  pl->acc_cols = cols;
+  pl->tmem_cols = 2 * cols;
+  int cps = static_cast<int>((220 * 1024) / pl->smem);
+  if (cps * pl->tmem_cols > 512) cps = 512 / pl->tmem_cols;
+  if (cps * kThreads > 2048) cps = 2048 / kThreads;
+  pl->ctas_per_sm = cps < 1 ? 1 : cps;
   return true;
 }
 
 template <int BK, int MODE, bool BF16>
-sc_status launch_tc(const TcParams& prm, const Plan& pl, int grid, cudaStream_t s, const char* name) {
+sc_status launch_tc(const TcParams& prm, const Plan& pl, cudaStream_t s, const char* name) {
   auto kern = k_conv_tc<BK, MODE, BF16>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(pl.smem));
   if (e != cudaSuccess) return set_cuda_error(e, "conv smem attribute");
+  const int slots = device_sm_count() * pl.ctas_per_sm;
+  const int grid = prm.num_tiles < slots ? prm.num_tiles : slots;
   SC_LAUNCH(name, s, kern<<<grid, kThreads, pl.smem, s>>>(prm));
   e = cudaGetLastError();
   return e == cudaSuccess ? SC_OK : set_cuda_error(e, name);
 }
 
 template <int MODE>
-sc_status dispatch_tc(const TcParams& prm, const Plan& pl, bool bf16, int grid, cudaStream_t s, const char* name) {
-  if (grid <= 0) return SC_OK;
+sc_status dispatch_tc(const TcParams& prm, const Plan& pl, bool bf16, cudaStream_t s, const char* name) {
+  if (prm.num_tiles <= 0) return SC_OK;
   switch (pl.bk) {
     case 64:
-      return bf16 ? launch_tc<64, MODE, true>(prm, pl, grid, s, name) : launch_tc<64, MODE, false>(prm, pl, grid, s, name);
+      return bf16 ? launch_tc<64, MODE, true>(prm, pl, s, name) : launch_tc<64, MODE, false>(prm, pl, s, name);
     case 32:
-      return bf16 ? launch_tc<32, MODE, true>(prm, pl, grid, s, name) : launch_tc<32, MODE, false>(prm, pl, grid, s, name);
+      return bf16 ? launch_tc<32, MODE, true>(prm, pl, s, name) : launch_tc<32, MODE, false>(prm, pl, s, name);
     default:
-      return bf16 ? launch_tc<16, MODE, true>(prm, pl, grid, s, name) : launch_tc<16, MODE, false>(prm, pl, grid, s, name);
+      return bf16 ? launch_tc<16, MODE, true>(prm, pl, s, name) : launch_tc<16, MODE, false>(prm, pl, s, name);
   }
 }
 
@@ -551,22 +709,99 @@ TcParams base_params(const ConvArgs& a, const Plan& pl, const uint8_t* img) {
   p.wimg = img;
   p.out = static_cast<uint8_t*>(a.out);
   p.nbr = a.m->nbr;
+  p.present = reinterpret_cast<const uint4*>(a.m->present);
   p.in_rows = a.m->in_rows;
   p.out_rows = a.m->out_rows;
   p.offs = a.m->offs;
   p.ws_tiles = a.m->ws_tiles;
   p.n = a.m->n;
+  p.num_tiles = static_cast<int>((a.m->n + kRows - 1) / kRows);
   p.V = a.m->V;
   p.c_in = a.c_in;
   p.c_out = a.c_out;
   p.relu = a.relu ? 1 : 0;
   p.stages = pl.stages;
+  p.group = pl.group;
+  p.lag = pl.lag;
+  p.acc_cols = pl.acc_cols;
   p.tmem_cols = pl.tmem_cols;
   p.status = a.m->status;
   return p;
 }
 
+bool fused_ok(const ConvArgs& a, Plan* pl) {
+  return a.dtype != SC_F32 && a.m->V <= 128 && make_plan(a.c_in, a.c_out, pl);
+}
+
+// The output-stationary launch on an already packed weight image.
+sc_status run_fused(const ConvArgs& a, const Plan& pl, const uint8_t* img) {
+  TcParams prm = base_params(a, pl, img);
+  return dispatch_tc<kOutputStationary>(prm, pl, a.dtype == SC_BF16, a.stream, "subm_conv_fused");
+}
+
 }  // namespace
+
+bool fused_supported(const ConvArgs& a) {
+  Plan pl;
+  return fused_ok(a, &pl);
+}
+
+sc_status conv_fused(const ConvArgs& a) {
+  Plan pl;
+  if (!fused_ok(a, &pl))
+    return set_error(SC_ERR_UNSUPPORTED, "fused kernel: f16/bf16 only, V <= 128, tile must fit shared memory");
+  if (a.m->n == 0) return SC_OK;
+  const size_t img_bytes = static_cast<size_t>(a.m->V) * a.c_in * a.c_out * 2;
+  void* img = nullptr;
+  sc_status st = dev_alloc(&img, img_bytes, a.stream);
+  if (st) return st;
+  st = pack_weights(a, pl.bk, static_cast<uint8_t*>(img));
+  if (!st) st = run_fused(a, pl, static_cast<const uint8_t*>(img));
+  dev_free(img, a.stream);
+  return st;
+}
+
+sc_status conv_weight_stationary(const ConvArgs& a) {
+  Plan pl;
+  if (a.dtype == SC_F32 || !make_plan(a.c_in, a.c_out, &pl))
+    return set_error(SC_ERR_UNSUPPORTED, "weight-stationary kernel: f16/bf16 only");
+  if (a.m->n == 0) return SC_OK;
+  if (!a.m->host_valid) return set_error(SC_ERR_INVALID_ARG, "weight-stationary kernel needs the map's host counts");
+  const size_t img_bytes = static_cast<size_t>(a.m->V) * a.c_in * a.c_out * 2;
+  const size_t acc_bytes = static_cast<size_t>(a.m->n) * a.c_out * sizeof(float);
+  void* img = nullptr;
+  void* acc = nullptr;
+  sc_status st = dev_alloc(&img, img_bytes, a.stream);
+  if (st) return st;
+  st = dev_alloc(&acc, acc_bytes, a.stream);
+  if (st) {
+    dev_free(img, a.stream);
+    return st;
+  }
+  st = pack_weights(a, pl.bk, static_cast<uint8_t*>(img));
+  TcParams prm = base_params(a, pl, static_cast<const uint8_t*>(img));
+  prm.acc = static_cast<float*>(acc);
+  const bool bf16 = a.dtype == SC_BF16;
+  if (!st) st = dispatch_tc<kWsCentre>(prm, pl, bf16, a.stream, "subm_conv_ws_centre");
+  if (!st) {
+    prm.num_tiles = a.m->ws_tiles_host[a.m->V];
+    st = dispatch_tc<kWsScatter>(prm, pl, bf16, a.stream, "subm_conv_ws_scatter");
+  }
+  if (!st) {
+    const int64_t n4 = a.m->n * a.c_out / 4;
+    int grid = static_cast<int>((n4 + 255) / 256);
+    if (grid > device_sm_count() * 16) grid = device_sm_count() * 16;
+    if (bf16)
+      SC_LAUNCH("cast_out", a.stream, k_cast_out<true><<<grid, 256, 0, a.stream>>>(static_cast<const float4*>(acc), static_cast<uint2*>(a.out), n4, a.relu));
+    else
+      SC_LAUNCH("cast_out", a.stream, k_cast_out<false><<<grid, 256, 0, a.stream>>>(static_cast<const float4*>(acc), static_cast<uint2*>(a.out), n4, a.relu));
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) st = set_cuda_error(e, "cast_out launch");
+  }
+  dev_free(acc, a.stream);
+  dev_free(img, a.stream);
+  return st;
+}
 
 // Device address of g_noalloc_weights on the current device, looked up once
 // per device (host code only holds a stand-in for the symbol, which is not a
@@ -595,7 +830,7 @@ sc_status conv_fused_noalloc(const ConvArgs& a) {
   sc_status st = noalloc_weights_ptr(&img);
   if (st) return st;
   Plan pl;
-  if (a.dtype == SC_F32 || a.m->V > 128 || !make_plan(kOutputStationary, a.m->V, a.c_in, a.c_out, &pl))
+  if (!fused_ok(a, &pl))
     return set_error(SC_ERR_UNSUPPORTED, "no-allocation conv: f16/bf16 only, V <= 128, tile must fit shared memory");
   const size_t img_bytes = static_cast<size_t>(a.m->V) * a.c_in * a.c_out * 2;
   if (img_bytes > kNoAllocWeightBytes)
@@ -604,75 +839,7 @@ sc_status conv_fused_noalloc(const ConvArgs& a) {
   if (a.m->n == 0) return SC_OK;
   st = pack_weights(a, pl.bk, static_cast<uint8_t*>(img));
   if (st) return st;
-  TcParams prm = base_params(a, pl, static_cast<const uint8_t*>(img));
-  const int grid = static_cast<int>((a.m->n + kRows - 1) / kRows);
-  return dispatch_tc<kOutputStationary>(prm, pl, a.dtype == SC_BF16, grid, a.stream, "subm_conv_fused");
-}
-
-bool fused_supported(const ConvArgs& a) {
-  Plan pl;
-  return a.dtype != SC_F32 && a.m->V <= 128 && make_plan(kOutputStationary, a.m->V, a.c_in, a.c_out, &pl);
-}
-
-sc_status conv_fused(const ConvArgs& a) {
-  Plan pl;
-  if (a.dtype == SC_F32 || a.m->V > 128 || !make_plan(kOutputStationary, a.m->V, a.c_in, a.c_out, &pl))
-    return set_error(SC_ERR_UNSUPPORTED, "fused kernel: f16/bf16 only, V <= 128, tile must fit shared memory");
-  if (a.m->n == 0) return SC_OK;
-  const size_t img_bytes = static_cast<size_t>(a.m->V) * a.c_in * a.c_out * 2;
-  void* img = nullptr;
-  sc_status st = dev_alloc(&img, img_bytes, a.stream);
-  if (st) return st;
-  st = pack_weights(a, pl.bk, static_cast<uint8_t*>(img));
-  if (!st) {
-    TcParams prm = base_params(a, pl, static_cast<const uint8_t*>(img));
-    const int grid = static_cast<int>((a.m->n + kRows - 1) / kRows);
-    st = dispatch_tc<kOutputStationary>(prm, pl, a.dtype == SC_BF16, grid, a.stream, "subm_conv_fused");
-  }
-  dev_free(img, a.stream);
-  return st;
-}
-
-sc_status conv_weight_stationary(const ConvArgs& a) {
-  Plan pl;
-  if (a.dtype == SC_F32 || !make_plan(kWsScatter, a.m->V, a.c_in, a.c_out, &pl))
-    return set_error(SC_ERR_UNSUPPORTED, "weight-stationary kernel: f16/bf16 only");
-  if (a.m->n == 0) return SC_OK;
-  if (!a.m->host_valid) return set_error(SC_ERR_INVALID_ARG, "weight-stationary kernel needs the map's host counts");
-  const size_t img_bytes = static_cast<size_t>(a.m->V) * a.c_in * a.c_out * 2;
-  const size_t acc_bytes = static_cast<size_t>(a.m->n) * a.c_out * sizeof(float);
-  void* img = nullptr;
-  void* acc = nullptr;
-  sc_status st = dev_alloc(&img, img_bytes, a.stream);
-  if (st) return st;
-  st = dev_alloc(&acc, acc_bytes, a.stream);
-  if (st) {
-    dev_free(img, a.stream);
-    return st;
-  }
-  st = pack_weights(a, pl.bk, static_cast<uint8_t*>(img));
-  TcParams prm = base_params(a, pl, static_cast<const uint8_t*>(img));
-  prm.acc = static_cast<float*>(acc);
-  const bool bf16 = a.dtype == SC_BF16;
-  if (!st) {
-    const int grid = static_cast<int>((a.m->n + kRows - 1) / kRows);
-    st = dispatch_tc<kWsCentre>(prm, pl, bf16, grid, a.stream, "subm_conv_ws_centre");
-  }
-  if (!st) st = dispatch_tc<kWsScatter>(prm, pl, bf16, a.m->ws_tiles_host[a.m->V], a.stream, "subm_conv_ws_scatter");
-  if (!st) {
-    const int64_t n4 = a.m->n * a.c_out / 4;
-    int grid = static_cast<int>((n4 + 255) / 256);
-    if (grid > device_sm_count() * 16) grid = device_sm_count() * 16;
-    if (bf16)
-      SC_LAUNCH("cast_out", a.stream, k_cast_out<true><<<grid, 256, 0, a.stream>>>(static_cast<const float4*>(acc), static_cast<uint2*>(a.out), n4, a.relu));
-    else
-      SC_LAUNCH("cast_out", a.stream, k_cast_out<false><<<grid, 256, 0, a.stream>>>(static_cast<const float4*>(acc), static_cast<uint2*>(a.out), n4, a.relu));
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) st = set_cuda_error(e, "cast_out launch");
-  }
-  dev_free(acc, a.stream);
-  dev_free(img, a.stream);
-  return st;
+  return run_fused(a, pl, static_cast<const uint8_t*>(img));
 }
 
 }  // namespace sc

@@ -126,8 +126,8 @@ __device__ __forceinline__ int unpack_off(int o, int axis) { return ((o >> (10 *
 
 __global__ void __launch_bounds__(kThreads) k_kmap_probe(
     const unsigned long long* __restrict__ keys, int64_t n, const Slot* __restrict__ table, uint32_t mask, int V,
-    int K, int ndim, int dimx, int dimy, int dimz, int* __restrict__ nbr, unsigned* __restrict__ masks, int ntiles,
-    int* __restrict__ status) {
+    int K, int ndim, int dimx, int dimy, int dimz, int* __restrict__ nbr, unsigned* __restrict__ masks,
+    unsigned* __restrict__ present, int ntiles, int* __restrict__ status) {
   extern __shared__ int smem_i[];
   int* s_off = smem_i;                                   // [V] packed offsets
   unsigned* s_mask = reinterpret_cast<unsigned*>(smem_i + V);  // [V]
@@ -211,7 +211,12 @@ __global__ void __launch_bounds__(kThreads) k_kmap_probe(
     }
   }
   __syncthreads();
-  for (int v = tid; v < V; v += kThreads) masks[static_cast<int64_t>(v) * ntiles + tile] = s_mask[v];
+  // per-offset masks, and the offsets present in this tile's 128-row group
+  for (int v = tid; v < V; v += kThreads) {
+    const unsigned mk = s_mask[v];
+    masks[static_cast<int64_t>(v) * ntiles + tile] = mk;
+    if (mk && v < 128) atomicOr(&present[(tile >> 2) * 4 + (v >> 5)], 1u << (v & 31));
+  }
 }
 
 // Block-wide inclusive scan of one value per thread (blockDim <= 1024).
@@ -387,10 +392,12 @@ sc_status launch_kmap_build(const HashTable* h, KernelMap* m, cudaStream_t s) {
   const size_t probe_smem = sizeof(int) * 2 * V;
   const size_t fill_smem = sizeof(int) * (2 * V + static_cast<size_t>(tpb) * V + static_cast<size_t>(tpb) * kTile * V);
   const uint32_t mask = static_cast<uint32_t>(h->capacity - 1);
+  e = cudaMemsetAsync(m->present, 0, sizeof(unsigned) * 4 * ((m->n + 127) / 128), s);
+  if (e != cudaSuccess) return set_cuda_error(e, "kmap presence clear");
   SC_LAUNCH("kmap_probe", s,
             k_kmap_probe<<<m->ntiles, kThreads, probe_smem, s>>>(h->keys, m->n, h->table, mask, V, m->K, m->ndim,
                                                                   m->dims[0], m->dims[1], m->dims[2], m->nbr,
-                                                                  m->masks, m->ntiles, m->status));
+                                                                  m->masks, m->present, m->ntiles, m->status));
   e = cudaGetLastError();
   if (e != cudaSuccess) return set_cuda_error(e, "kmap_probe launch");
   SC_LAUNCH("kmap_scan", s,

@@ -74,6 +74,7 @@ struct KernelMap {
   int* in_rows = nullptr;            // [n*(V-1)] capacity, offs[V] used
   int* out_rows = nullptr;
   unsigned* masks = nullptr;         // [V, ntiles] hit bitmask of each tile's 32 points
+  unsigned* present = nullptr;       // [ceil(n/128), 4] offsets (< 128) with a hit in each 128-row tile
   int* bases = nullptr;              // [V, ntiles] exclusive prefix of the mask popcounts
   int* totals = nullptr;             // [V]
   int* ws_tiles = nullptr;           // [V+1] prefix of ceil(count/128) per offset
