@@ -67,6 +67,8 @@ typedef enum { SC_F32 = 0, SC_F16 = 1, SC_BF16 = 2 } sc_dtype;
 
 /* flags for sc_kmap_build */
 #define SC_KMAP_NO_SYNC 0x100u  /* do not synchronise; check errors later with sc_kmap_check */
+#define SC_KMAP_ORDER 0x200u    /* always compute the locality order (default: n >= 262144) */
+#define SC_KMAP_NO_ORDER 0x400u /* never compute it: tiles follow the input row order */
 
 typedef struct sc_hash_s* sc_hash;
 typedef struct sc_kmap_s* sc_kmap;
@@ -119,15 +121,24 @@ sc_status sc_hash_destroy(sc_hash h, sc_stream stream);
  * K         odd, K >= 1, with V = K^ndim <= 343 (K <= 7 in 3D, K <= 17 in 2D).
  * dims      spatial extents (x, y, z), each in [1, 65535]; every point must
  *           lie inside; neighbours outside are absent (zero padding).
- * flags     0 or SC_KMAP_NO_SYNC.
+ * flags     0, SC_KMAP_NO_SYNC, and at most one of SC_KMAP_ORDER /
+ *           SC_KMAP_NO_ORDER.
+ *
+ * Locality order: for n >= 262144 (or with SC_KMAP_ORDER) the build first
+ * sorts the points into spatially compact groups (a counting sort on the top
+ * 20 bits of a Morton code of (batch, x, y, z)); the convolution's 128-row
+ * tiles are runs of that order, so they touch fewer offsets and reuse
+ * neighbour rows.  It changes no result: outputs still land on their own
+ * rows and nbr stays in input row order.
  *
  * Products, owned by the handle:
  *   nbr      int32 [n, V]: nbr[q*V + idx(d)] = row p with coords[p] =
  *            coords[q] + d, or -1.  Column (V-1)/2 is the identity.
  *   offs     int64 [V+1]: per-offset segments of the (in, out) lists.  The
  *            centre segment is empty: its tuples are (i, i) for every i.
- *   in/out   int32 [offs[V]]: list entries (p, q); within a segment ordered
- *            by q.
+ *   in/out   int32 [offs[V]]: list entries (p, q); within a segment the
+ *            entries follow the row order (input order, or the locality
+ *            order), which is not part of the result.
  *   map size |M| = n + offs[V] tuples, centre included.
  *
  * Without SC_KMAP_NO_SYNC the call synchronises the stream once and returns

@@ -377,13 +377,16 @@ sc_status sc_kmap_destroy(sc_kmap m, sc_stream stream) {
   if (!m) return SC_OK;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   KernelMap& k = m->k;
-  for (void* p : {static_cast<void*>(k.nbr), static_cast<void*>(k.offs), static_cast<void*>(k.in_rows),
+  for (void* p : {static_cast<void*>(k.order), static_cast<void*>(k.buckets), static_cast<void*>(k.nbr), static_cast<void*>(k.offs), static_cast<void*>(k.in_rows),
                   static_cast<void*>(k.out_rows), static_cast<void*>(k.masks), static_cast<void*>(k.present), static_cast<void*>(k.bases), static_cast<void*>(k.totals),
                   static_cast<void*>(k.ws_tiles), static_cast<void*>(k.map_size), static_cast<void*>(k.status)})
     dev_free(p, s);
   delete m;
   return SC_OK;
 }
+
+// Inputs at least this large get a locality order by default.
+constexpr int64_t kOrderMinPoints = 262144;
 
 sc_status sc_kmap_build(sc_hash h, int ndim, int K, const int32_t dims[3], unsigned flags, sc_stream stream,
                         sc_kmap* out) {
@@ -400,7 +403,10 @@ sc_status sc_kmap_build(sc_hash h, int ndim, int K, const int32_t dims[3], unsig
   if (!dims) return set_error(SC_ERR_INVALID_ARG, "dims is NULL");
   for (int a = 0; a < 3; ++a)
     if (dims[a] < 1 || dims[a] > 65535) return set_error(SC_ERR_INVALID_ARG, "dims must be in [1, 65535]");
-  if (flags & ~SC_KMAP_NO_SYNC) return set_error(SC_ERR_INVALID_ARG, "unknown kmap flag");
+  if (flags & ~(SC_KMAP_NO_SYNC | SC_KMAP_ORDER | SC_KMAP_NO_ORDER))
+    return set_error(SC_ERR_INVALID_ARG, "unknown kmap flag");
+  if ((flags & SC_KMAP_ORDER) && (flags & SC_KMAP_NO_ORDER))
+    return set_error(SC_ERR_INVALID_ARG, "SC_KMAP_ORDER and SC_KMAP_NO_ORDER together");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   sc_kmap m = new sc_kmap_s();
   KernelMap& k = m->k;
@@ -414,6 +420,11 @@ sc_status sc_kmap_build(sc_hash h, int ndim, int K, const int32_t dims[3], unsig
   const size_t nV = static_cast<size_t>(k.n) * V;
   const size_t lists = static_cast<size_t>(k.n) * (V - 1);
   sc_status st = dev_alloc(reinterpret_cast<void**>(&k.nbr), sizeof(int) * nV, s);
+  const bool ordered = (flags & SC_KMAP_ORDER) || (!(flags & SC_KMAP_NO_ORDER) && k.n >= kOrderMinPoints);
+  if (!st && ordered && k.n > 0) {
+    st = dev_alloc(reinterpret_cast<void**>(&k.order), sizeof(int) * static_cast<size_t>(k.n), s);
+    if (!st) st = dev_alloc(reinterpret_cast<void**>(&k.buckets), sizeof(int) * kmap_order_buckets(), s);
+  }
   if (!st) st = dev_alloc(reinterpret_cast<void**>(&k.offs), sizeof(int64_t) * (V + 1), s);
   if (!st) st = dev_alloc(reinterpret_cast<void**>(&k.in_rows), sizeof(int) * lists, s);
   if (!st) st = dev_alloc(reinterpret_cast<void**>(&k.out_rows), sizeof(int) * lists, s);

@@ -221,6 +221,7 @@ struct TcParams {
   uint8_t* out;              // output-stationary: [n, c_out] 2-byte elements
   float* acc;                // weight-stationary: fp32 [n, c_out]
   const int* nbr;            // [n, V]
+  const int* order;          // [n] input rows in locality order, or null: output-stationary tiles are runs of it
   const uint4* present;      // [tiles]: 128-bit mask of the offsets present in each 128-row tile
   const int* in_rows;        // weight-stationary lists
   const int* out_rows;
@@ -365,7 +366,7 @@ __global__ void __launch_bounds__(kThreads) k_conv_tc(const TcParams p) {
     const int rbase = pt / CPR;         // rows rbase + RSTEP * k, k < RPT
     const int lag = p.lag;
     uint32_t it = 0;
-    if (MODE == kOutputStationary && pt == 0 && static_cast<int>(blockIdx.x) < p.num_tiles) {
+    if (MODE == kOutputStationary && !p.order && pt == 0 && static_cast<int>(blockIdx.x) < p.num_tiles) {
       const TileInfo t0 = tile_info<MODE>(p, blockIdx.x);
       const uint32_t bytes = (static_cast<uint32_t>(t0.nrows) * V * 4) & ~15u;
       if (bytes) bulk_prefetch_l2(p.nbr + t0.row0 * V, bytes);
@@ -378,14 +379,22 @@ __global__ void __launch_bounds__(kThreads) k_conv_tc(const TcParams p) {
         m = tile_mask(p, tile);
         v = next_present(m, -1, V);
         const int nt = tile + gridDim.x;
-        if (pt == 0 && nt < p.num_tiles) {
+        if (!p.order && pt == 0 && nt < p.num_tiles) {
           const TileInfo tn = tile_info<MODE>(p, nt);
           const uint32_t bytes = (static_cast<uint32_t>(tn.nrows) * V * 4) & ~15u;
           if (bytes) bulk_prefetch_l2(p.nbr + tn.row0 * V, bytes);
         }
       }
       const int nkb = tile_kblocks<MODE>(p, tile, P);
-      // source rows of this thread's tile rows for the current offset
+      // this thread's tile rows (input row ids) and their sources for the current offset
+      int row_id[RPT];
+#pragma unroll
+      for (int k = 0; k < RPT; ++k) {
+        const int r = rbase + RSTEP * k;
+        row_id[k] = 0;
+        if (MODE == kOutputStationary && r < t.nrows)
+          row_id[k] = p.order ? __ldg(p.order + t.row0 + r) : static_cast<int>(t.row0 + r);
+      }
       int src[RPT];
       auto load_rows = [&](int vv) {
 #pragma unroll
@@ -393,7 +402,7 @@ __global__ void __launch_bounds__(kThreads) k_conv_tc(const TcParams p) {
           const int r = rbase + RSTEP * k;
           int j = -1;
           if (r < t.nrows) {
-            if (MODE == kOutputStationary) j = __ldg(p.nbr + (t.row0 + r) * V + vv);
+            if (MODE == kOutputStationary) j = __ldg(p.nbr + static_cast<int64_t>(row_id[k]) * V + vv);
             else if (MODE == kWsScatter) j = __ldg(p.in_rows + t.lb + r);
             else j = static_cast<int>(t.row0 + r);
           }
@@ -520,6 +529,7 @@ __global__ void __launch_bounds__(kThreads) k_conv_tc(const TcParams p) {
       int dst_row = -1;
       if (r < t.nrows) {
         if (MODE == kWsScatter) dst_row = __ldg(p.out_rows + t.lb + r);
+        else if (MODE == kOutputStationary && p.order) dst_row = __ldg(p.order + t.row0 + r);
         else dst_row = static_cast<int>(t.row0 + r);
       }
       for (int c0 = 0; c0 < p.c_out; c0 += 16) {
@@ -709,6 +719,7 @@ TcParams base_params(const ConvArgs& a, const Plan& pl, const uint8_t* img) {
   p.wimg = img;
   p.out = static_cast<uint8_t*>(a.out);
   p.nbr = a.m->nbr;
+  p.order = a.m->order;
   p.present = reinterpret_cast<const uint4*>(a.m->present);
   p.in_rows = a.m->in_rows;
   p.out_rows = a.m->out_rows;

@@ -10,9 +10,21 @@
 // gives the tuple (p, q, W_d).  The centre offset is the identity at stride 1
 // and is written, not searched ("TorchSparse optimizations", opening section).
 // Lists are grouped by offset ("SparseConvNet: from hash table to rulebook",
-// section 3) and, within an offset, ordered by output row.
+// section 3).
 //
-// Points are taken in tiles of 32 rows.  Three kernels build the map:
+// Locality order.  Rows arrive in any order, but the probe, the per-offset
+// lists and the convolution's 128-row tiles work best on spatially compact
+// groups of points: a compact tile touches fewer offsets and reuses the same
+// neighbour rows.  For large inputs the map build therefore counting-sorts the
+// points on a 20-bit bucket, the top bits of a Morton code of (batch, x, y, z)
+// whose per-axis widths follow the grid extents and the largest batch id.
+// Buckets are small (a few dozen points on surface data), consecutive buckets
+// are neighbouring cells, and the order inside a bucket is whatever the
+// atomics give; no result depends on it.  Without the order, rows are taken
+// in input order.
+//
+// Points are taken in tiles of 32 positions of that order.  Three kernels
+// build the map:
 //   probe  one block per tile: the tile's 32 x V (point, offset) pairs are
 //          spread over the block's threads, four per thread with their
 //          first-slot loads in flight together.  Results go straight to the
@@ -24,7 +36,8 @@
 //          tile prefix and |M|.
 //   fill   each warp takes one (tile, offset) pair: lane p holds point p's
 //          neighbour, a ballot ranks the hits, and the (in, out) entries are
-//          written to consecutive positions of the offset's segment.
+//          written to consecutive positions of the offset's segment, which
+//          therefore follows the row order.
 
 #include "sc_internal.cuh"
 
@@ -37,6 +50,10 @@ constexpr int kIlp = 4;          // pairs per thread with loads in flight togeth
 constexpr int kWsRows = 128;     // rows per weight-stationary tile
 constexpr int kScanThreads = 512;  // >= the largest V (343)
 constexpr int kScanPer = 8;        // tiles per scan thread per chunk
+constexpr int kBucketBits = 20;    // locality-order buckets
+constexpr int kBuckets = 1 << kBucketBits;
+constexpr int kBucketBlocks = 256;                   // blocks of the bucket scan
+constexpr int kBucketChunk = kBuckets / kBucketBlocks;  // 4096 buckets per block
 
 __device__ __forceinline__ ulonglong2 load_slot(const Slot* __restrict__ t, uint32_t i) {
   return __ldg(reinterpret_cast<const ulonglong2*>(t + i));
@@ -76,6 +93,11 @@ __global__ void __launch_bounds__(256) k_hash_insert(const int4* __restrict__ co
     }
     const unsigned long long key = pack_key(c.x, c.y, c.z, c.w);
     keys[i] = key;
+    {  // largest batch id, one atomic per warp
+      const unsigned am = __activemask();
+      const int mb = __reduce_max_sync(am, c.x);
+      if ((threadIdx.x & 31) == __ffs(am) - 1 && mb > 0) atomicMax(status + 1, mb);
+    }
     uint32_t h = static_cast<uint32_t>(hash_mix(key)) & mask;
     int outcome = 0;  // 1 placed, 2 duplicate
     for (uint32_t seen = 0; seen <= mask && !outcome;) {
@@ -121,16 +143,133 @@ __global__ void __launch_bounds__(256) k_hash_query(const int4* __restrict__ q, 
   }
 }
 
+// Bits needed to hold values 0..v.
+__device__ __forceinline__ int bits_for(int v) { return v > 0 ? 32 - __clz(v) : 0; }
+
+struct OrderBits {
+  int bx, by, bz;  // widths of the x, y, z extents
+};
+
+// Locality bucket of a packed key: the top kBucketBits bits of the Morton
+// code (x, y, z interleaved from the lowest bit, each axis as wide as its
+// extent), with the batch id above the spatial bits.
+__device__ __forceinline__ int order_bucket(unsigned long long key, const OrderBits& ob, int total_bits) {
+  if (key == kEmptyKey) return 0;
+  const uint32_t x = static_cast<uint32_t>((key >> 32) & 0xFFFF), y = static_cast<uint32_t>((key >> 16) & 0xFFFF),
+                 z = static_cast<uint32_t>(key & 0xFFFF), b = static_cast<uint32_t>(key >> 48);
+  unsigned long long code = 0;
+  int pos = 0;
+  const int L = max(ob.bx, max(ob.by, ob.bz));
+  for (int l = 0; l < L; ++l) {
+    if (l < ob.bx) code |= static_cast<unsigned long long>((x >> l) & 1u) << pos++;
+    if (l < ob.by) code |= static_cast<unsigned long long>((y >> l) & 1u) << pos++;
+    if (l < ob.bz) code |= static_cast<unsigned long long>((z >> l) & 1u) << pos++;
+  }
+  code |= static_cast<unsigned long long>(b) << pos;
+  const int shift = total_bits > kBucketBits ? total_bits - kBucketBits : 0;
+  return static_cast<int>((code >> shift) & (kBuckets - 1));
+}
+
+__device__ __forceinline__ int order_total_bits(const OrderBits& ob, const int* hash_status) {
+  return ob.bx + ob.by + ob.bz + bits_for(__ldg(hash_status + 1));
+}
+
+__global__ void __launch_bounds__(256) k_order_count(const unsigned long long* __restrict__ keys, int64_t n,
+                                                     OrderBits ob, const int* __restrict__ hash_status,
+                                                     int* __restrict__ buckets) {
+  const int tb = order_total_bits(ob, hash_status);
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride)
+    atomicAdd(buckets + order_bucket(__ldg(keys + i), ob, tb), 1);
+}
+
+// Scan phase 1: the total of each block's chunk of buckets.
+__global__ void __launch_bounds__(256) k_order_partials(const int* __restrict__ buckets, int* __restrict__ partial) {
+  __shared__ int warp_sums[8];
+  const int4* b = reinterpret_cast<const int4*>(buckets + blockIdx.x * kBucketChunk);
+  int sum = 0;
+  for (int k = threadIdx.x; k < kBucketChunk / 4; k += 256) {
+    const int4 c = __ldg(b + k);
+    sum += c.x + c.y + c.z + c.w;
+  }
+  sum = __reduce_add_sync(0xffffffffu, sum);
+  if ((threadIdx.x & 31) == 0) warp_sums[threadIdx.x >> 5] = sum;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int t = 0;
+    for (int w = 0; w < 8; ++w) t += warp_sums[w];
+    partial[blockIdx.x] = t;
+  }
+}
+
+// Scan phase 2: exclusive prefix of the bucket counts, in place.  Each block
+// adds the partials of the blocks before it, then scans its chunk in shared
+// memory (16 consecutive buckets per thread).
+__global__ void __launch_bounds__(256) k_order_apply(int* __restrict__ buckets, const int* __restrict__ partial) {
+  __shared__ int s_c[kBucketChunk];
+  __shared__ int warp_sums[8];
+  __shared__ int s_base;
+  constexpr int per = kBucketChunk / 256;
+  int4* b = reinterpret_cast<int4*>(buckets + blockIdx.x * kBucketChunk);
+  for (int k = threadIdx.x; k < kBucketChunk / 4; k += 256) reinterpret_cast<int4*>(s_c)[k] = b[k];
+  if (threadIdx.x < 32) {
+    int base = 0;
+    for (int j = threadIdx.x; j < static_cast<int>(blockIdx.x); j += 32) base += __ldg(partial + j);
+    base = __reduce_add_sync(0xffffffffu, base);
+    if (threadIdx.x == 0) s_base = base;
+  }
+  __syncthreads();
+  int c[per];
+  int sum = 0;
+#pragma unroll
+  for (int k = 0; k < per; ++k) {
+    c[k] = s_c[threadIdx.x * per + k];
+    sum += c[k];
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += t;
+  }
+  if (lane == 31) warp_sums[warp] = x;
+  __syncthreads();
+  int before = s_base;
+  for (int w = 0; w < warp; ++w) before += warp_sums[w];
+  int run = before + x - sum;
+#pragma unroll
+  for (int k = 0; k < per; ++k) {
+    s_c[threadIdx.x * per + k] = run;
+    run += c[k];
+  }
+  __syncthreads();
+  for (int k = threadIdx.x; k < kBucketChunk / 4; k += 256) b[k] = reinterpret_cast<const int4*>(s_c)[k];
+}
+
+__global__ void __launch_bounds__(256) k_order_scatter(const unsigned long long* __restrict__ keys, int64_t n,
+                                                       OrderBits ob, const int* __restrict__ hash_status,
+                                                       int* __restrict__ cursors, int* __restrict__ order) {
+  const int tb = order_total_bits(ob, hash_status);
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+    const int pos = atomicAdd(cursors + order_bucket(__ldg(keys + i), ob, tb), 1);
+    order[pos] = static_cast<int>(i);
+  }
+}
+
 // Offsets are packed 10 bits per axis with a bias of 512.
 __device__ __forceinline__ int unpack_off(int o, int axis) { return ((o >> (10 * axis)) & 1023) - 512; }
 
 __global__ void __launch_bounds__(kThreads) k_kmap_probe(
-    const unsigned long long* __restrict__ keys, int64_t n, const Slot* __restrict__ table, uint32_t mask, int V,
-    int K, int ndim, int dimx, int dimy, int dimz, int* __restrict__ nbr, unsigned* __restrict__ masks,
-    unsigned* __restrict__ present, int ntiles, int* __restrict__ status) {
+    const unsigned long long* __restrict__ keys, const int* __restrict__ order, int64_t n,
+    const Slot* __restrict__ table, uint32_t mask, int V, int K, int ndim, int dimx, int dimy, int dimz,
+    int* __restrict__ nbr, unsigned* __restrict__ masks, unsigned* __restrict__ present, int ntiles,
+    int* __restrict__ status) {
   extern __shared__ int smem_i[];
-  int* s_off = smem_i;                                   // [V] packed offsets
+  int* s_off = smem_i;                                         // [V] packed offsets
   unsigned* s_mask = reinterpret_cast<unsigned*>(smem_i + V);  // [V]
+  int* s_row = smem_i + 2 * V;                                 // [kTile] input rows of this tile
   const int tid = threadIdx.x;
   const int tile = blockIdx.x;
   const int64_t i0 = static_cast<int64_t>(tile) * kTile;
@@ -149,10 +288,10 @@ __global__ void __launch_bounds__(kThreads) k_kmap_probe(
     s_off[v] = (d[0] + 512) | ((d[1] + 512) << 10) | ((d[2] + 512) << 20);
     s_mask[v] = 0u;
   }
+  if (tid < np) s_row[tid] = order ? __ldg(order + i0 + tid) : static_cast<int>(i0 + tid);
   __syncthreads();
 
   const int items = np * V;
-  int* dst = nbr + i0 * V;
   for (int base = 0; base < items; base += kThreads * kIlp) {
     unsigned long long key[kIlp];
     uint32_t slot[kIlp];
@@ -172,13 +311,13 @@ __global__ void __launch_bounds__(kThreads) k_kmap_probe(
         const int v = e - p * V;
         pnt[k] = p;
         off[k] = v;
-        const unsigned long long ck = __ldg(keys + i0 + p);
+        const unsigned long long ck = __ldg(keys + s_row[p]);
         if (ck != kEmptyKey) {
           int x = static_cast<int>((ck >> 32) & 0xFFFF);
           int y = static_cast<int>((ck >> 16) & 0xFFFF);
           int z = static_cast<int>(ck & 0xFFFF);
           if (v == centre) {
-            res[k] = static_cast<int>(i0 + p);
+            res[k] = s_row[p];
             if (x >= dimx || y >= dimy || z >= dimz) atomicOr(status, kDevErrRange);
           } else {
             const int o = s_off[v];
@@ -207,7 +346,7 @@ __global__ void __launch_bounds__(kThreads) k_kmap_probe(
         res[k] = table_find(table, mask, key[k], slot[k], cur[k]);
         if (res[k] >= 0) atomicOr(&s_mask[off[k]], 1u << pnt[k]);
       }
-      if (e < items) dst[e] = res[k];
+      if (e < items) nbr[static_cast<int64_t>(s_row[pnt[k]]) * V + off[k]] = res[k];
     }
   }
   __syncthreads();
@@ -303,21 +442,27 @@ __global__ void __launch_bounds__(kScanThreads) k_kmap_scan(
   }
 }
 
-__global__ void __launch_bounds__(kThreads) k_kmap_fill(const int* __restrict__ nbr, int64_t n, int V, int ntiles,
+__global__ void __launch_bounds__(kThreads) k_kmap_fill(const int* __restrict__ nbr, const int* __restrict__ order,
+                                                        int64_t n, int V, int ntiles,
                                                         int tiles_per_block, const int* __restrict__ bases,
                                                         const int64_t* __restrict__ offs, int* __restrict__ in_rows,
                                                         int* __restrict__ out_rows) {
   extern __shared__ int smem_i[];
   long long* s_offs = reinterpret_cast<long long*>(smem_i);    // [V]
   int* s_base = smem_i + 2 * V;                                // [tiles_per_block * V]
-  int* s_nbr = s_base + tiles_per_block * V;                   // [tiles_per_block * 32 * V]
+  int* s_row = s_base + tiles_per_block * V;                   // [tiles_per_block * 32]
+  int* s_nbr = s_row + tiles_per_block * kTile;                // [tiles_per_block * 32 * V]
   const int tile0 = blockIdx.x * tiles_per_block;
   const int ntl = min(tiles_per_block, ntiles - tile0);
   const int64_t i0 = static_cast<int64_t>(tile0) * kTile;
   const int np = static_cast<int>(min(static_cast<int64_t>(ntl) * kTile, n - i0));
   const int items = np * V;
-  const int* src = nbr + i0 * V;
-  for (int e = threadIdx.x; e < items; e += kThreads) s_nbr[e] = __ldg(src + e);
+  for (int p = threadIdx.x; p < np; p += kThreads) s_row[p] = order ? __ldg(order + i0 + p) : static_cast<int>(i0 + p);
+  __syncthreads();
+  for (int e = threadIdx.x; e < items; e += kThreads) {
+    const int p = e / V;
+    s_nbr[e] = __ldg(nbr + static_cast<int64_t>(s_row[p]) * V + (e - p * V));
+  }
   for (int v = threadIdx.x; v < V; v += kThreads) s_offs[v] = __ldg(offs + v);
   for (int q = threadIdx.x; q < ntl * V; q += kThreads) {
     const int tl = q / V, v = q - tl * V;
@@ -335,7 +480,7 @@ __global__ void __launch_bounds__(kThreads) k_kmap_fill(const int* __restrict__ 
     if (j >= 0) {
       const long long at = s_offs[v] + s_base[q] + __popc(bal & ((1u << lane) - 1u));
       in_rows[at] = j;
-      out_rows[at] = static_cast<int>(i0 + p);
+      out_rows[at] = s_row[p];
     }
   }
 }
@@ -348,18 +493,19 @@ int grid_for(int64_t n, int threads) {
 }
 
 int fill_tiles_per_block(int V) {
-  int t = 8192 / (kTile * V);
+  int t = 8000 / (kTile * (V + 1));
   return t < 1 ? 1 : (t > 8 ? 8 : t);
 }
 
 }  // namespace
 
 int kmap_probe_tile() { return kTile; }
+int kmap_order_buckets() { return kBuckets + kBucketBlocks; }
 
 sc_status launch_hash_insert(const int32_t* coords, int64_t n, HashTable* h, cudaStream_t s) {
   cudaError_t e = cudaMemsetAsync(h->table, 0xFF, sizeof(Slot) * h->capacity, s);
   if (e != cudaSuccess) return set_cuda_error(e, "hash table clear");
-  e = cudaMemsetAsync(h->status, 0, sizeof(int), s);
+  e = cudaMemsetAsync(h->status, 0, sizeof(int) * 4, s);
   if (e != cudaSuccess) return set_cuda_error(e, "hash status clear");
   if (n == 0) return SC_OK;
   SC_LAUNCH("hash_insert", s,
@@ -389,13 +535,41 @@ sc_status launch_kmap_build(const HashTable* h, KernelMap* m, cudaStream_t s) {
     return e == cudaSuccess ? SC_OK : set_cuda_error(e, "empty kmap init");
   }
   const int tpb = fill_tiles_per_block(V);
-  const size_t probe_smem = sizeof(int) * 2 * V;
-  const size_t fill_smem = sizeof(int) * (2 * V + static_cast<size_t>(tpb) * V + static_cast<size_t>(tpb) * kTile * V);
+  const size_t probe_smem = sizeof(int) * (2 * V + kTile);
+  const size_t fill_smem =
+      sizeof(int) * (2 * V + static_cast<size_t>(tpb) * V + static_cast<size_t>(tpb) * kTile * (V + 1));
   const uint32_t mask = static_cast<uint32_t>(h->capacity - 1);
+  if (m->order) {  // locality order: count, two-phase scan, scatter
+    OrderBits ob;
+    int b[3];
+    for (int a = 0; a < 3; ++a) {
+      int v = m->dims[a] - 1, c = 0;
+      while (v > 0) {
+        ++c;
+        v >>= 1;
+      }
+      b[a] = c;
+    }
+    ob.bx = b[0];
+    ob.by = b[1];
+    ob.bz = b[2];
+    e = cudaMemsetAsync(m->buckets, 0, sizeof(int) * kBuckets, s);
+    if (e != cudaSuccess) return set_cuda_error(e, "order bucket clear");
+    const int og = grid_for(m->n, 256);
+    int* partial = m->buckets + kBuckets;
+    SC_LAUNCH("order_count", s, k_order_count<<<og, 256, 0, s>>>(h->keys, m->n, ob, h->status, m->buckets));
+    SC_LAUNCH("order_partials", s, k_order_partials<<<kBucketBlocks, 256, 0, s>>>(m->buckets, partial));
+    SC_LAUNCH("order_apply", s, k_order_apply<<<kBucketBlocks, 256, 0, s>>>(m->buckets, partial));
+    SC_LAUNCH("order_scatter", s,
+              k_order_scatter<<<og, 256, 0, s>>>(h->keys, m->n, ob, h->status, m->buckets, m->order));
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return set_cuda_error(e, "locality order launch");
+  }
   e = cudaMemsetAsync(m->present, 0, sizeof(unsigned) * 4 * ((m->n + 127) / 128), s);
   if (e != cudaSuccess) return set_cuda_error(e, "kmap presence clear");
   SC_LAUNCH("kmap_probe", s,
-            k_kmap_probe<<<m->ntiles, kThreads, probe_smem, s>>>(h->keys, m->n, h->table, mask, V, m->K, m->ndim,
+            k_kmap_probe<<<m->ntiles, kThreads, probe_smem, s>>>(h->keys, m->order, m->n, h->table, mask, V, m->K,
+                                                                  m->ndim,
                                                                   m->dims[0], m->dims[1], m->dims[2], m->nbr,
                                                                   m->masks, m->present, m->ntiles, m->status));
   e = cudaGetLastError();
@@ -407,7 +581,8 @@ sc_status launch_kmap_build(const HashTable* h, KernelMap* m, cudaStream_t s) {
   if (e != cudaSuccess) return set_cuda_error(e, "kmap_scan launch");
   const int fill_blocks = (m->ntiles + tpb - 1) / tpb;
   SC_LAUNCH("kmap_fill", s,
-            k_kmap_fill<<<fill_blocks, kThreads, fill_smem, s>>>(m->nbr, m->n, V, m->ntiles, tpb, m->bases, m->offs,
+            k_kmap_fill<<<fill_blocks, kThreads, fill_smem, s>>>(m->nbr, m->order, m->n, V, m->ntiles, tpb, m->bases,
+                                                                  m->offs,
                                                                   m->in_rows, m->out_rows));
   e = cudaGetLastError();
   return e == cudaSuccess ? SC_OK : set_cuda_error(e, "kmap_fill launch");

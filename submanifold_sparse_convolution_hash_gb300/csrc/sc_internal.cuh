@@ -56,7 +56,7 @@ struct HashTable {
   int64_t capacity = 0;              // power of two
   Slot* table = nullptr;             // [capacity]
   unsigned long long* keys = nullptr;  // [n]  packed key of each row (kEmptyKey if invalid)
-  int* status = nullptr;             // device status word
+  int* status = nullptr;             // [4]: latched errors, largest batch id
 };
 
 struct ConvChoice {
@@ -69,12 +69,14 @@ struct KernelMap {
   int ndim = 3, K = 3, V = 27;
   int dims[3] = {1, 1, 1};
   int ntiles = 0;                    // 32-point tiles of the map build
+  int* order = nullptr;              // [n] input rows in locality order, or null: input order
+  int* buckets = nullptr;            // counting-sort buckets of that order (+ scan partials)
   int* nbr = nullptr;                // [n, V]
   int64_t* offs = nullptr;           // [V+1]
   int* in_rows = nullptr;            // [n*(V-1)] capacity, offs[V] used
   int* out_rows = nullptr;
   unsigned* masks = nullptr;         // [V, ntiles] hit bitmask of each tile's 32 points
-  unsigned* present = nullptr;       // [ceil(n/128), 4] offsets (< 128) with a hit in each 128-row tile
+  unsigned* present = nullptr;       // [ceil(n/128), 4] offsets (< 128) with a hit in each 128-row tile of the row order
   int* bases = nullptr;              // [V, ntiles] exclusive prefix of the mask popcounts
   int* totals = nullptr;             // [V]
   int* ws_tiles = nullptr;           // [V+1] prefix of ceil(count/128) per offset
@@ -109,6 +111,7 @@ sc_status launch_hash_query(const HashTable* h, const int32_t* q, int64_t m, int
                             cudaStream_t s);
 sc_status launch_kmap_build(const HashTable* h, KernelMap* m, cudaStream_t s);
 int kmap_probe_tile();
+int kmap_order_buckets();
 
 // kernels: convolution (conv_tc.cu, conv_simt.cu)
 struct ConvArgs {

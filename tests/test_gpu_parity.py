@@ -30,10 +30,10 @@ def small_scenes():
 SCENES = small_scenes()
 
 
-def build(scene, K, sync=True):
+def build(scene, K, sync=True, order=None):
     c = torch.from_numpy(scene.coords).cuda()
     h = sc.sc_hash_build(c)
-    m = sc.sc_kmap_build(h, scene.ndim, K, scene.dims, sync=sync)
+    m = sc.sc_kmap_build(h, scene.ndim, K, scene.dims, sync=sync, order=order)
     return c, h, m
 
 
@@ -63,10 +63,10 @@ def test_hash_query_finds_every_row_and_misses_absent_keys():
 
 @pytest.mark.parametrize("name,K", [("uniform2d", 3), ("uniform2d_dense", 5), ("lidar", 3), ("indoor", 3),
                                     ("indoor", 5), ("batch", 3), ("lidar", 1), ("indoor", 7)])
-@pytest.mark.parametrize("sync", [True, False])
-def test_kmap_bit_exact(name, K, sync):
+@pytest.mark.parametrize("sync,order", [(True, False), (False, False), (True, True), (False, True)])
+def test_kmap_bit_exact(name, K, sync, order):
     s = SCENES[name]
-    c, h, m = build(s, K, sync)
+    c, h, m = build(s, K, sync, order)
     if not sync:
         m.check()
     ref = oracle.kmap(s.coords, s.ndim, K, s.dims)
@@ -80,19 +80,30 @@ def test_kmap_bit_exact(name, K, sync):
             assert len(gi) == 0  # the identity is implied, not listed
             np.testing.assert_array_equal(ri, np.arange(s.n))
             continue
-        np.testing.assert_array_equal(go, ro)  # ordered by output row
-        np.testing.assert_array_equal(gi, ri)
+        # segments follow the row order (input or locality): compare as sets
+        k = np.lexsort((gi, go))
+        np.testing.assert_array_equal(go[k], ro)
+        np.testing.assert_array_equal(gi[k], ri)
+        if not order:
+            np.testing.assert_array_equal(go, ro)  # input order: sorted by output row
     assert m.map_size() == len(oracle.tuples(ref))
     assert offs[-1] == m.map_size() - s.n
 
 
-def test_kmap_is_deterministic():
+@pytest.mark.parametrize("order", [False, True])
+def test_kmap_is_deterministic(order):
+    """The neighbour table and segment sizes repeat exactly; each segment
+    holds the same pairs (inside a segment the locality order may differ
+    among points of one bucket)."""
     s = SCENES["lidar"]
-    _, _, m1 = build(s, 3)
-    _, _, m2 = build(s, 3)
+    _, _, m1 = build(s, 3, order=order)
+    _, _, m2 = build(s, 3, order=order)
     assert torch.equal(m1.nbr(), m2.nbr())
-    for a, b in zip(m1.lists(), m2.lists()):
-        assert torch.equal(a, b)
+    (o1, i1, q1), (o2, i2, q2) = m1.lists(), m2.lists()
+    assert torch.equal(o1, o2)
+    for v in range(len(o1) - 1):
+        a, b = int(o1[v]), int(o1[v + 1])
+        assert sorted(zip(q1[a:b].tolist(), i1[a:b].tolist())) == sorted(zip(q2[a:b].tolist(), i2[a:b].tolist()))
 
 
 def test_five_point_worked_example_on_gpu():
@@ -136,10 +147,11 @@ CONV_CASES = [
 ]
 
 
+@pytest.mark.parametrize("order", [False, True])
 @pytest.mark.parametrize("name,K,c_in,c_out,dtype,relu,variant", CONV_CASES)
-def test_conv_matches_oracle(name, K, c_in, c_out, dtype, relu, variant):
+def test_conv_matches_oracle(name, K, c_in, c_out, dtype, relu, variant, order):
     s = SCENES[name]
-    c, h, m = build(s, K)
+    c, h, m = build(s, K, order=order)
     f, w, f64, w64 = layer_inputs(s, K, c_in, c_out, dtype, seed=7 + c_in + K,
                                   w_std=1.0 if dtype == "f32" else None)
     out = sc.sc_subm_conv_fwd(m, f, w, relu=relu, variant=variant)
