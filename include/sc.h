@@ -87,8 +87,11 @@ typedef struct sc_kmap_s* sc_kmap;
  * n         number of points, 0 <= n < 2^31.
  * out       receives the handle.
  *
- * Open addressing, linear probing, capacity = next power of two >= 2n, keys
- * packed into 64 bits (16 bits per field, batch highest).  Asynchronous: a
+ * Keys are packed into 64 bits (16 bits per field, batch highest).  The
+ * table is open addressing with linear probing over entries of one 2x2x2
+ * block of voxels each: the block's key (the voxel key with the low bit of x,
+ * y, z cleared) and the rows of its 8 voxels.  Capacity = next power of two
+ * >= 2n entries (>= n when that would exceed 256 MB).  Asynchronous: a
  * duplicate or out-of-range coordinate is latched in the handle and reported
  * by sc_hash_check, sc_kmap_build or sc_kmap_check.
  */
@@ -98,7 +101,8 @@ sc_status sc_hash_build(const int32_t* d_coords, int64_t n, sc_stream stream, sc
  * d_query int32 [m, 4] (16-byte aligned), d_rows int32 [m]. Asynchronous. */
 sc_status sc_hash_query(sc_hash h, const int32_t* d_query, int64_t m, int32_t* d_rows, sc_stream stream);
 
-/* Number of points and table capacity (host values, no synchronisation). */
+/* Number of points and table capacity in block entries (host values, no
+ * synchronisation). */
 sc_status sc_hash_info(sc_hash h, int64_t* n, int64_t* capacity);
 
 /* Synchronises the stream and returns the latched insert status. */

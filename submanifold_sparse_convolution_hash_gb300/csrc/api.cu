@@ -318,13 +318,14 @@ sc_status sc_hash_build(const int32_t* d_coords, int64_t n, sc_stream stream, sc
   sc_hash h = new sc_hash_s();
   HashTable& t = h->t;
   t.n = n;
-  // load factor <= 1/4 while the table stays small enough to live in L2,
-  // <= 1/2 beyond that
+  // one entry per occupied 2x2x2 block, at most n of them: 2n entries while
+  // the table stays within 256 MB, n beyond that (surface data fills a block
+  // with several points, so the load stays well below 1/2 either way)
   int64_t cap = 16;
-  const int64_t want = 4 * n * static_cast<int64_t>(sizeof(Slot)) <= (int64_t(32) << 20) ? 4 * n : 2 * n;
+  const int64_t want = 2 * n * static_cast<int64_t>(sizeof(BlockEntry)) <= (int64_t(256) << 20) ? 2 * n : n;
   while (cap < want) cap <<= 1;
   t.capacity = cap;
-  sc_status st = dev_alloc(reinterpret_cast<void**>(&t.table), sizeof(Slot) * cap, s);
+  sc_status st = dev_alloc(reinterpret_cast<void**>(&t.table), sizeof(BlockEntry) * cap, s);
   if (!st) st = dev_alloc(reinterpret_cast<void**>(&t.keys), sizeof(unsigned long long) * (n > 0 ? n : 1), s);
   if (!st) st = dev_alloc(reinterpret_cast<void**>(&t.status), sizeof(int) * 4, s);
   if (!st) st = launch_hash_insert(d_coords, n, &t, s);
@@ -480,7 +481,18 @@ sc_status sc_kmap_export(sc_kmap m, int32_t* nbr, int64_t* offs, int32_t* in_row
     if (st) return st;
   }
   cudaError_t e = cudaSuccess;
-  if (nbr && k.n) e = cudaMemcpyAsync(nbr, k.nbr, sizeof(int) * k.n * k.V, cudaMemcpyDefault, s);
+  if (nbr && k.n) {
+    if (!k.order) {
+      e = cudaMemcpyAsync(nbr, k.nbr, sizeof(int) * k.n * k.V, cudaMemcpyDefault, s);
+    } else {  // the table is stored in the locality order: put rows back in input order
+      int* tmp = nullptr;
+      sc_status st = dev_alloc(reinterpret_cast<void**>(&tmp), sizeof(int) * k.n * k.V, s);
+      if (!st) st = kmap_unpermute_nbr(&k, tmp, s);
+      if (!st) e = cudaMemcpyAsync(nbr, tmp, sizeof(int) * k.n * k.V, cudaMemcpyDefault, s);
+      dev_free(tmp, s);
+      if (st) return st;
+    }
+  }
   if (e == cudaSuccess && offs) e = cudaMemcpyAsync(offs, k.offs, sizeof(int64_t) * (k.V + 1), cudaMemcpyDefault, s);
   const int64_t L = k.host_valid ? k.offs_host[k.V] : 0;
   if (e == cudaSuccess && in_rows && L) e = cudaMemcpyAsync(in_rows, k.in_rows, sizeof(int) * L, cudaMemcpyDefault, s);

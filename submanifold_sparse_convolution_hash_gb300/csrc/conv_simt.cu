@@ -1,4 +1,4 @@
-// CUDA-core submanifold convolution: one thread per (output row, output
+// CUDA-core submanifold convolution: one thread per (table row, output
 // channel), walking the row's neighbour-table entries in offset order and
 // accumulating feats[p, ci] * W[d, ci, co] with fp32 FMAs (exam sheet
 // "Sparse convolution for point clouds", "The map and the update rule").
@@ -32,8 +32,9 @@ __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) { return
 
 template <typename T>
 __global__ void __launch_bounds__(256) k_conv_simt(const T* __restrict__ feats, const T* __restrict__ W,
-                                                   T* __restrict__ out, const int* __restrict__ nbr, int64_t n, int V,
-                                                   int c_in, int c_out, int relu) {
+                                                   T* __restrict__ out, const int* __restrict__ nbr,
+                                                   const int* __restrict__ order, int64_t n, int V, int c_in,
+                                                   int c_out, int relu) {
   const int64_t total = n * c_out;
   for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
        idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -48,7 +49,8 @@ __global__ void __launch_bounds__(256) k_conv_simt(const T* __restrict__ feats, 
       for (int ci = 0; ci < c_in; ++ci) acc = fmaf(to_f(f[ci]), to_f(w[static_cast<int64_t>(ci) * c_out]), acc);
     }
     if (relu) acc = fmaxf(acc, 0.0f);
-    out[idx] = from_f<T>(acc);
+    const int64_t dst = order ? static_cast<int64_t>(__ldg(order + q)) : q;
+    out[dst * c_out + co] = from_f<T>(acc);
   }
 }
 
@@ -61,7 +63,7 @@ sc_status launch(const ConvArgs& a) {
   SC_LAUNCH("subm_conv_simt", a.stream,
             k_conv_simt<T><<<static_cast<int>(g), 256, 0, a.stream>>>(
                 static_cast<const T*>(a.feats), static_cast<const T*>(a.W), static_cast<T*>(a.out), a.m->nbr,
-                a.m->n, a.m->V, a.c_in, a.c_out, a.relu ? 1 : 0));
+                a.m->order, a.m->n, a.m->V, a.c_in, a.c_out, a.relu ? 1 : 0));
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? SC_OK : set_cuda_error(e, "subm_conv_simt launch");
 }

@@ -221,7 +221,7 @@ struct TcParams {
   uint8_t* out;              // output-stationary: [n, c_out] 2-byte elements
   float* acc;                // weight-stationary: fp32 [n, c_out]
   const int* nbr;            // [n, V]
-  const int* order;          // [n] input rows in locality order, or null: output-stationary tiles are runs of it
+  const int* order;          // [n] input row of each table row (null: identity); tiles are runs of table rows
   const uint4* present;      // [tiles]: 128-bit mask of the offsets present in each 128-row tile
   const int* in_rows;        // weight-stationary lists
   const int* out_rows;
@@ -366,7 +366,7 @@ __global__ void __launch_bounds__(kThreads) k_conv_tc(const TcParams p) {
     const int rbase = pt / CPR;         // rows rbase + RSTEP * k, k < RPT
     const int lag = p.lag;
     uint32_t it = 0;
-    if (MODE == kOutputStationary && !p.order && pt == 0 && static_cast<int>(blockIdx.x) < p.num_tiles) {
+    if (MODE == kOutputStationary && pt == 0 && static_cast<int>(blockIdx.x) < p.num_tiles) {
       const TileInfo t0 = tile_info<MODE>(p, blockIdx.x);
       const uint32_t bytes = (static_cast<uint32_t>(t0.nrows) * V * 4) & ~15u;
       if (bytes) bulk_prefetch_l2(p.nbr + t0.row0 * V, bytes);
@@ -379,22 +379,15 @@ __global__ void __launch_bounds__(kThreads) k_conv_tc(const TcParams p) {
         m = tile_mask(p, tile);
         v = next_present(m, -1, V);
         const int nt = tile + gridDim.x;
-        if (!p.order && pt == 0 && nt < p.num_tiles) {
+        if (pt == 0 && nt < p.num_tiles) {
           const TileInfo tn = tile_info<MODE>(p, nt);
           const uint32_t bytes = (static_cast<uint32_t>(tn.nrows) * V * 4) & ~15u;
           if (bytes) bulk_prefetch_l2(p.nbr + tn.row0 * V, bytes);
         }
       }
       const int nkb = tile_kblocks<MODE>(p, tile, P);
-      // this thread's tile rows (input row ids) and their sources for the current offset
-      int row_id[RPT];
-#pragma unroll
-      for (int k = 0; k < RPT; ++k) {
-        const int r = rbase + RSTEP * k;
-        row_id[k] = 0;
-        if (MODE == kOutputStationary && r < t.nrows)
-          row_id[k] = p.order ? __ldg(p.order + t.row0 + r) : static_cast<int>(t.row0 + r);
-      }
+      // source rows of this thread's tile rows for the current offset (the
+      // tile's block of the neighbour table is contiguous)
       int src[RPT];
       auto load_rows = [&](int vv) {
 #pragma unroll
@@ -402,7 +395,7 @@ __global__ void __launch_bounds__(kThreads) k_conv_tc(const TcParams p) {
           const int r = rbase + RSTEP * k;
           int j = -1;
           if (r < t.nrows) {
-            if (MODE == kOutputStationary) j = __ldg(p.nbr + static_cast<int64_t>(row_id[k]) * V + vv);
+            if (MODE == kOutputStationary) j = __ldg(p.nbr + (t.row0 + r) * V + vv);
             else if (MODE == kWsScatter) j = __ldg(p.in_rows + t.lb + r);
             else j = static_cast<int>(t.row0 + r);
           }

@@ -23,13 +23,15 @@
 // atomics give; no result depends on it.  Without the order, rows are taken
 // in input order.
 //
-// Points are taken in tiles of 32 positions of that order.  Three kernels
-// build the map:
-//   probe  one block per tile: the tile's 32 x V (point, offset) pairs are
-//          spread over the block's threads, four per thread with their
-//          first-slot loads in flight together.  Results go straight to the
-//          neighbour table (coalesced), and each hit sets bit p of the
-//          (offset, tile) mask.
+// Points are taken in tiles of 32 positions of that order, and the neighbour
+// table is stored in that order too (row k belongs to input row order[k]), so
+// a tile's 32 x V block is contiguous.  Three kernels build the map:
+//   probe  one block per tile, lane = point in every warp: the warps split
+//          the 2x2x2 blocks that cover each point's neighbourhood (8 for a
+//          3x3x3 kernel, 27 for 5x5x5); one lookup returns a block's 8 rows,
+//          which are filed under their offsets in a shared-memory copy of the
+//          tile's block of the table; a ballot per offset gives the tile's
+//          hit bitmask; the block is written with coalesced 16-byte stores.
 //   scan   one block per offset: exclusive prefix of the masks' popcounts
 //          over tiles.  The last block to finish (a ticket counter) turns the
 //          per-offset totals into the segment offsets, the weight-stationary
@@ -46,7 +48,6 @@ namespace {
 
 constexpr int kTile = 32;        // points per tile (one bitmask word)
 constexpr int kThreads = 256;    // threads per probe / fill block
-constexpr int kIlp = 4;          // pairs per thread with loads in flight together
 constexpr int kWsRows = 128;     // rows per weight-stationary tile
 constexpr int kScanThreads = 512;  // >= the largest V (343)
 constexpr int kScanPer = 8;        // tiles per scan thread per chunk
@@ -55,20 +56,31 @@ constexpr int kBuckets = 1 << kBucketBits;
 constexpr int kBucketBlocks = 256;                   // blocks of the bucket scan
 constexpr int kBucketChunk = kBuckets / kBucketBlocks;  // 4096 buckets per block
 
-__device__ __forceinline__ ulonglong2 load_slot(const Slot* __restrict__ t, uint32_t i) {
-  return __ldg(reinterpret_cast<const ulonglong2*>(t + i));
+// Looks up block key bk; on a hit, r0/r1 hold the rows of its 8 voxels.
+// Each probed entry's key and rows are loaded together (one 64-byte entry).
+__device__ __forceinline__ bool lookup_block(const BlockEntry* __restrict__ table, uint32_t mask,
+                                             unsigned long long bk, int4& r0, int4& r1) {
+  uint32_t h = block_home(bk, mask);
+  for (uint32_t probe = 0; probe <= mask; ++probe) {
+    const BlockEntry* e = table + h;
+    const unsigned long long k = __ldg(&e->key);
+    r0 = __ldg(reinterpret_cast<const int4*>(e->rows));
+    r1 = __ldg(reinterpret_cast<const int4*>(e->rows + 4));
+    if (k == bk) return true;
+    if (k == kEmptyKey) return false;
+    h = (h + 1) & mask;
+  }
+  return false;
 }
 
-// Resolves a lookup whose first slot `cur` (index h) is already loaded.
-__device__ __forceinline__ int table_find(const Slot* __restrict__ table, uint32_t mask, unsigned long long key,
-                                          uint32_t h, ulonglong2 cur) {
-  for (uint32_t probe = 0; probe <= mask; ++probe) {
-    if (cur.x == key) return static_cast<int>(static_cast<uint32_t>(cur.y));
-    if (cur.x == kEmptyKey) return -1;
-    h = (h + 1) & mask;
-    cur = load_slot(table, h);
+__device__ __forceinline__ int pick(const int4& r0, const int4& r1, int l) {
+  const int4& q = l < 4 ? r0 : r1;
+  switch (l & 3) {
+    case 0: return q.x;
+    case 1: return q.y;
+    case 2: return q.z;
+    default: return q.w;
   }
-  return -1;
 }
 
 __device__ __forceinline__ bool coord_fields_ok(int4 c) {
@@ -76,11 +88,11 @@ __device__ __forceinline__ bool coord_fields_ok(int4 c) {
          static_cast<unsigned>(c.z) < 65535u && static_cast<unsigned>(c.w) < 65535u;
 }
 
-// Linear-probing insert.  Each round reads a window of four slots from L2
-// and CASes the first empty one, so a collision usually costs no extra atomic
-// round trip; a lost CAS is re-examined before moving on.
+// Insert: find or claim the entry of the voxel's block (CAS on the block
+// key), then CAS the voxel's row slot from -1 to its row id; a slot that is
+// already taken means two rows share the coordinate.
 __global__ void __launch_bounds__(256) k_hash_insert(const int4* __restrict__ coords, int64_t n,
-                                                     Slot* __restrict__ table, uint32_t mask,
+                                                     BlockEntry* __restrict__ table, uint32_t mask,
                                                      unsigned long long* __restrict__ keys,
                                                      int* __restrict__ status) {
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -98,37 +110,31 @@ __global__ void __launch_bounds__(256) k_hash_insert(const int4* __restrict__ co
       const int mb = __reduce_max_sync(am, c.x);
       if ((threadIdx.x & 31) == __ffs(am) - 1 && mb > 0) atomicMax(status + 1, mb);
     }
-    uint32_t h = static_cast<uint32_t>(hash_mix(key)) & mask;
-    int outcome = 0;  // 1 placed, 2 duplicate
-    for (uint32_t seen = 0; seen <= mask && !outcome;) {
-      unsigned long long w[4];
-#pragma unroll
-      for (int t = 0; t < 4; ++t) w[t] = __ldcg(&table[(h + t) & mask].key);
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        if (outcome || seen > mask) break;
-        const uint32_t slot = (h + t) & mask;
-        unsigned long long k = w[t];
-        if (k == kEmptyKey) {
-          k = atomicCAS(&table[slot].key, kEmptyKey, key);
-          if (k == kEmptyKey) {
-            table[slot].val = static_cast<int>(i);
-            outcome = 1;
-            break;
-          }
-        }
-        if (k == key) outcome = 2;
-        ++seen;
+    const unsigned long long bk = block_key(key);
+    uint32_t h = block_home(bk, mask);
+    int e = -1;
+    for (uint32_t probe = 0; probe <= mask; ++probe) {
+      unsigned long long k = __ldcg(&table[h].key);
+      if (k == kEmptyKey) {
+        k = atomicCAS(&table[h].key, kEmptyKey, bk);
+        if (k == kEmptyKey) k = bk;
       }
-      h = (h + 4) & mask;
+      if (k == bk) {
+        e = static_cast<int>(h);
+        break;
+      }
+      h = (h + 1) & mask;
     }
-    if (outcome == 2) atomicOr(status, kDevErrDup);
-    if (outcome == 0) atomicOr(status, kDevErrFull);
+    if (e < 0) {
+      atomicOr(status, kDevErrFull);
+      continue;
+    }
+    if (atomicCAS(&table[e].rows[block_local(key)], -1, static_cast<int>(i)) != -1) atomicOr(status, kDevErrDup);
   }
 }
 
 __global__ void __launch_bounds__(256) k_hash_query(const int4* __restrict__ q, int64_t m,
-                                                    const Slot* __restrict__ table, uint32_t mask,
+                                                    const BlockEntry* __restrict__ table, uint32_t mask,
                                                     int* __restrict__ rows) {
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < m; i += stride) {
@@ -136,8 +142,8 @@ __global__ void __launch_bounds__(256) k_hash_query(const int4* __restrict__ q, 
     int r = -1;
     if (coord_fields_ok(c)) {
       const unsigned long long key = pack_key(c.x, c.y, c.z, c.w);
-      const uint32_t h = static_cast<uint32_t>(hash_mix(key)) & mask;
-      r = table_find(table, mask, key, h, load_slot(table, h));
+      int4 r0, r1;
+      if (lookup_block(table, mask, block_key(key), r0, r1)) r = pick(r0, r1, block_local(key));
     }
     rows[i] = r;
   }
@@ -258,103 +264,88 @@ __global__ void __launch_bounds__(256) k_order_scatter(const unsigned long long*
   }
 }
 
-// Offsets are packed 10 bits per axis with a bias of 512.
-__device__ __forceinline__ int unpack_off(int o, int axis) { return ((o >> (10 * axis)) & 1023) - 512; }
 
 __global__ void __launch_bounds__(kThreads) k_kmap_probe(
     const unsigned long long* __restrict__ keys, const int* __restrict__ order, int64_t n,
-    const Slot* __restrict__ table, uint32_t mask, int V, int K, int ndim, int dimx, int dimy, int dimz,
+    const BlockEntry* __restrict__ table, uint32_t mask, int V, int K, int ndim, int dimx, int dimy, int dimz,
     int* __restrict__ nbr, unsigned* __restrict__ masks, unsigned* __restrict__ present, int ntiles,
     int* __restrict__ status) {
-  extern __shared__ int smem_i[];
-  int* s_off = smem_i;                                         // [V] packed offsets
-  unsigned* s_mask = reinterpret_cast<unsigned*>(smem_i + V);  // [V]
-  int* s_row = smem_i + 2 * V;                                 // [kTile] input rows of this tile
-  const int tid = threadIdx.x;
+  extern __shared__ int4 smem4[];
+  int* s_tile = reinterpret_cast<int*>(smem4);  // [32 * V] the tile's block of the table
+  __shared__ unsigned s_pres[4];
+  constexpr int kWarps = kThreads / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = (K - 1) / 2;
+  const int rz = ndim == 3 ? r : 0;
+  const int centre = (V - 1) / 2;
+  for (int e = threadIdx.x; e < kTile * V; e += kThreads) s_tile[e] = -1;
+  if (threadIdx.x < 4) s_pres[threadIdx.x] = 0u;
   const int tile = blockIdx.x;
   const int64_t i0 = static_cast<int64_t>(tile) * kTile;
   const int np = static_cast<int>(min(static_cast<int64_t>(kTile), n - i0));
-  const int r = (K - 1) / 2;
-  const int centre = (V - 1) / 2;
-  // e / V as a multiply-shift: exact for e < 2^16 and V < 2^16
-  const unsigned long long magic = (1ull << 32) / static_cast<unsigned>(V) + 1ull;
-  for (int v = tid; v < V; v += kThreads) {
-    int d[3] = {0, 0, 0};
-    int t = v;
-    for (int k = ndim - 1; k >= 0; --k) {
-      d[k] = t % K - r;
-      t /= K;
-    }
-    s_off[v] = (d[0] + 512) | ((d[1] + 512) << 10) | ((d[2] + 512) << 20);
-    s_mask[v] = 0u;
+  // lane = point of the tile (every warp holds the same 32 points)
+  const bool live = lane < np;
+  const int row = live ? (order ? __ldg(order + i0 + lane) : static_cast<int>(i0 + lane)) : 0;
+  const unsigned long long ck = live ? __ldg(keys + row) : kEmptyKey;
+  bool valid = ck != kEmptyKey;
+  const int x = static_cast<int>((ck >> 32) & 0xFFFF), y = static_cast<int>((ck >> 16) & 0xFFFF),
+            z = static_cast<int>(ck & 0xFFFF);
+  if (valid && (x >= dimx || y >= dimy || z >= dimz)) {
+    if (warp == 0) atomicOr(status, kDevErrRange);
+    valid = false;
   }
-  if (tid < np) s_row[tid] = order ? __ldg(order + i0 + tid) : static_cast<int>(i0 + tid);
+  const unsigned long long batch = ck & 0xFFFF000000000000ull;
+  // the blocks covering the neighbourhood [x-r, x+r] x [y-r, y+r] x [z-rz, z+rz]
+  const int xlo = max(x - r, 0) >> 1, xhi = min(x + r, dimx - 1) >> 1;
+  const int ylo = max(y - r, 0) >> 1, yhi = min(y + r, dimy - 1) >> 1;
+  const int zlo = max(z - rz, 0) >> 1, zhi = min(z + rz, dimz - 1) >> 1;
   __syncthreads();
-
-  const int items = np * V;
-  for (int base = 0; base < items; base += kThreads * kIlp) {
-    unsigned long long key[kIlp];
-    uint32_t slot[kIlp];
-    bool act[kIlp];
-    int res[kIlp], pnt[kIlp], off[kIlp];
+  // warp w looks up block triples w, w + kWarps, ... and files each voxel of
+  // the block that lies in the neighbourhood under its offset
+  const int nb = r + 1, nbz = rz + 1;  // blocks per axis, at most
+  for (int t = warp; t < nb * nb * nbz; t += kWarps) {
+    const int bx = xlo + t / (nb * nbz), by = ylo + (t / nbz) % nb, bz = zlo + t % nbz;
+    if (valid && bx <= xhi && by <= yhi && bz <= zhi) {
+      int4 r0, r1;
+      if (lookup_block(table, mask, batch | pack_key(0, 2 * bx, 2 * by, 2 * bz), r0, r1)) {
 #pragma unroll
-    for (int k = 0; k < kIlp; ++k) {
-      const int e = base + tid + k * kThreads;
-      res[k] = -1;
-      act[k] = false;
-      slot[k] = 0;
-      key[k] = 0;
-      pnt[k] = 0;
-      off[k] = 0;
-      if (e < items) {
-        const int p = static_cast<int>((static_cast<unsigned long long>(e) * magic) >> 32);
-        const int v = e - p * V;
-        pnt[k] = p;
-        off[k] = v;
-        const unsigned long long ck = __ldg(keys + s_row[p]);
-        if (ck != kEmptyKey) {
-          int x = static_cast<int>((ck >> 32) & 0xFFFF);
-          int y = static_cast<int>((ck >> 16) & 0xFFFF);
-          int z = static_cast<int>(ck & 0xFFFF);
-          if (v == centre) {
-            res[k] = s_row[p];
-            if (x >= dimx || y >= dimy || z >= dimz) atomicOr(status, kDevErrRange);
-          } else {
-            const int o = s_off[v];
-            x += unpack_off(o, 0);
-            y += unpack_off(o, 1);
-            z += unpack_off(o, 2);
-            if (static_cast<unsigned>(x) < static_cast<unsigned>(dimx) &&
-                static_cast<unsigned>(y) < static_cast<unsigned>(dimy) &&
-                static_cast<unsigned>(z) < static_cast<unsigned>(dimz)) {
-              key[k] = (ck & 0xFFFF000000000000ull) | pack_key(0, x, y, z);
-              slot[k] = static_cast<uint32_t>(hash_mix(key[k])) & mask;
-              act[k] = true;
-            }
+        for (int l = 0; l < 8; ++l) {
+          const int dx = 2 * bx + (l >> 2) - x, dy = 2 * by + ((l >> 1) & 1) - y, dz = 2 * bz + (l & 1) - z;
+          if (dx >= -r && dx <= r && dy >= -r && dy <= r && dz >= -rz && dz <= rz) {
+            const int v = ndim == 3 ? ((dx + r) * K + (dy + r)) * K + (dz + r) : (dx + r) * K + (dy + r);
+            s_tile[lane * V + v] = pick(r0, r1, l);
           }
         }
       }
     }
-    ulonglong2 cur[kIlp];
-#pragma unroll
-    for (int k = 0; k < kIlp; ++k)
-      if (act[k]) cur[k] = load_slot(table, slot[k]);
-#pragma unroll
-    for (int k = 0; k < kIlp; ++k) {
-      const int e = base + tid + k * kThreads;
-      if (act[k]) {
-        res[k] = table_find(table, mask, key[k], slot[k], cur[k]);
-        if (res[k] >= 0) atomicOr(&s_mask[off[k]], 1u << pnt[k]);
-      }
-      if (e < items) nbr[static_cast<int64_t>(s_row[pnt[k]]) * V + off[k]] = res[k];
+  }
+  __syncthreads();
+  // per-offset hit masks of the tile; offsets present in its 128-row group
+  for (int v = warp; v < V; v += kWarps) {
+    const unsigned b = __ballot_sync(0xffffffffu, v != centre && s_tile[lane * V + v] >= 0);
+    if (lane == 0) {
+      masks[static_cast<int64_t>(v) * ntiles + tile] = b;
+      if (b && v < 128) atomicOr(s_pres + (v >> 5), 1u << (v & 31));
     }
   }
   __syncthreads();
-  // per-offset masks, and the offsets present in this tile's 128-row group
-  for (int v = tid; v < V; v += kThreads) {
-    const unsigned mk = s_mask[v];
-    masks[static_cast<int64_t>(v) * ntiles + tile] = mk;
-    if (mk && v < 128) atomicOr(&present[(tile >> 2) * 4 + (v >> 5)], 1u << (v & 31));
+  // the tile's block of the table is contiguous: i0 * V * 4 bytes is a multiple of 128
+  int* dst = nbr + i0 * V;
+  const int items = np * V;
+  const int n4 = items >> 2;
+  for (int e = threadIdx.x; e < n4; e += kThreads) reinterpret_cast<int4*>(dst)[e] = reinterpret_cast<const int4*>(s_tile)[e];
+  for (int e = (n4 << 2) + threadIdx.x; e < items; e += kThreads) dst[e] = s_tile[e];
+  if (threadIdx.x < 4 && s_pres[threadIdx.x]) atomicOr(present + (tile >> 2) * 4 + threadIdx.x, s_pres[threadIdx.x]);
+}
+
+// Rows of the table in input order: dst[order[k], :] = nbr[k, :].
+__global__ void __launch_bounds__(256) k_unpermute_rows(const int* __restrict__ nbr, const int* __restrict__ order,
+                                                        int64_t n, int V, int* __restrict__ dst) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  const int64_t stride = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t k = warp; k < n; k += stride) {
+    const int64_t q = __ldg(order + k);
+    for (int v = lane; v < V; v += 32) dst[q * V + v] = __ldg(nbr + k * V + v);
   }
 }
 
@@ -447,22 +438,23 @@ __global__ void __launch_bounds__(kThreads) k_kmap_fill(const int* __restrict__ 
                                                         int tiles_per_block, const int* __restrict__ bases,
                                                         const int64_t* __restrict__ offs, int* __restrict__ in_rows,
                                                         int* __restrict__ out_rows) {
-  extern __shared__ int smem_i[];
-  long long* s_offs = reinterpret_cast<long long*>(smem_i);    // [V]
-  int* s_base = smem_i + 2 * V;                                // [tiles_per_block * V]
-  int* s_row = s_base + tiles_per_block * V;                   // [tiles_per_block * 32]
-  int* s_nbr = s_row + tiles_per_block * kTile;                // [tiles_per_block * 32 * V]
+  extern __shared__ int4 smem_fill[];
+  int* smem_i = reinterpret_cast<int*>(smem_fill);
+  int* s_nbr = smem_i;                                          // [tiles_per_block * 32 * V], 16-byte aligned
+  long long* s_offs = reinterpret_cast<long long*>(s_nbr + ((tiles_per_block * kTile * V + 3) & ~3));  // [V]
+  int* s_base = reinterpret_cast<int*>(s_offs + V);             // [tiles_per_block * V]
+  int* s_row = s_base + tiles_per_block * V;                    // [tiles_per_block * 32]
   const int tile0 = blockIdx.x * tiles_per_block;
   const int ntl = min(tiles_per_block, ntiles - tile0);
   const int64_t i0 = static_cast<int64_t>(tile0) * kTile;
   const int np = static_cast<int>(min(static_cast<int64_t>(ntl) * kTile, n - i0));
   const int items = np * V;
   for (int p = threadIdx.x; p < np; p += kThreads) s_row[p] = order ? __ldg(order + i0 + p) : static_cast<int>(i0 + p);
-  __syncthreads();
-  for (int e = threadIdx.x; e < items; e += kThreads) {
-    const int p = e / V;
-    s_nbr[e] = __ldg(nbr + static_cast<int64_t>(s_row[p]) * V + (e - p * V));
-  }
+  const int* src = nbr + i0 * V;
+  const int n4 = items >> 2;
+  for (int e = threadIdx.x; e < n4; e += kThreads)
+    reinterpret_cast<int4*>(s_nbr)[e] = __ldg(reinterpret_cast<const int4*>(src) + e);
+  for (int e = (n4 << 2) + threadIdx.x; e < items; e += kThreads) s_nbr[e] = __ldg(src + e);
   for (int v = threadIdx.x; v < V; v += kThreads) s_offs[v] = __ldg(offs + v);
   for (int q = threadIdx.x; q < ntl * V; q += kThreads) {
     const int tl = q / V, v = q - tl * V;
@@ -502,8 +494,16 @@ int fill_tiles_per_block(int V) {
 int kmap_probe_tile() { return kTile; }
 int kmap_order_buckets() { return kBuckets + kBucketBlocks; }
 
+sc_status kmap_unpermute_nbr(const KernelMap* m, int* dst, cudaStream_t s) {
+  if (m->n == 0) return SC_OK;
+  SC_LAUNCH("kmap_unpermute", s,
+            k_unpermute_rows<<<grid_for(m->n * 32, 256), 256, 0, s>>>(m->nbr, m->order, m->n, m->V, dst));
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? SC_OK : set_cuda_error(e, "kmap_unpermute launch");
+}
+
 sc_status launch_hash_insert(const int32_t* coords, int64_t n, HashTable* h, cudaStream_t s) {
-  cudaError_t e = cudaMemsetAsync(h->table, 0xFF, sizeof(Slot) * h->capacity, s);
+  cudaError_t e = cudaMemsetAsync(h->table, 0xFF, sizeof(BlockEntry) * h->capacity, s);
   if (e != cudaSuccess) return set_cuda_error(e, "hash table clear");
   e = cudaMemsetAsync(h->status, 0, sizeof(int) * 4, s);
   if (e != cudaSuccess) return set_cuda_error(e, "hash status clear");
@@ -535,9 +535,9 @@ sc_status launch_kmap_build(const HashTable* h, KernelMap* m, cudaStream_t s) {
     return e == cudaSuccess ? SC_OK : set_cuda_error(e, "empty kmap init");
   }
   const int tpb = fill_tiles_per_block(V);
-  const size_t probe_smem = sizeof(int) * (2 * V + kTile);
+  const size_t probe_smem = sizeof(int) * kTile * V;
   const size_t fill_smem =
-      sizeof(int) * (2 * V + static_cast<size_t>(tpb) * V + static_cast<size_t>(tpb) * kTile * (V + 1));
+      sizeof(int) * (4 + 2 * V + static_cast<size_t>(tpb) * V + static_cast<size_t>(tpb) * kTile * (V + 1));
   const uint32_t mask = static_cast<uint32_t>(h->capacity - 1);
   if (m->order) {  // locality order: count, two-phase scan, scatter
     OrderBits ob;
@@ -568,7 +568,8 @@ sc_status launch_kmap_build(const HashTable* h, KernelMap* m, cudaStream_t s) {
   e = cudaMemsetAsync(m->present, 0, sizeof(unsigned) * 4 * ((m->n + 127) / 128), s);
   if (e != cudaSuccess) return set_cuda_error(e, "kmap presence clear");
   SC_LAUNCH("kmap_probe", s,
-            k_kmap_probe<<<m->ntiles, kThreads, probe_smem, s>>>(h->keys, m->order, m->n, h->table, mask, V, m->K,
+            k_kmap_probe<<<m->ntiles, kThreads, probe_smem, s>>>(h->keys, m->order, m->n, h->table, mask, V,
+                                                                  m->K,
                                                                   m->ndim,
                                                                   m->dims[0], m->dims[1], m->dims[2], m->nbr,
                                                                   m->masks, m->present, m->ntiles, m->status));

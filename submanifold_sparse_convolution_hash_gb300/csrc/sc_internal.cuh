@@ -27,34 +27,44 @@ enum : int {
 // marks an empty slot.
 constexpr unsigned long long kEmptyKey = ~0ull;
 
-struct __align__(16) Slot {
-  unsigned long long key;
-  int val;
-  int pad;
-};
-
 __host__ __device__ __forceinline__ unsigned long long pack_key(uint32_t b, uint32_t x, uint32_t y,
                                                                 uint32_t z) {
   return (static_cast<unsigned long long>(b) << 48) | (static_cast<unsigned long long>(x) << 32) |
          (static_cast<unsigned long long>(y) << 16) | static_cast<unsigned long long>(z);
 }
 
-// MurmurHash3's 64-bit finaliser (Appleby): a bijective mix, so distinct
-// keys stay distinct before the mask.
-__host__ __device__ __forceinline__ unsigned long long hash_mix(unsigned long long k) {
-  k ^= k >> 33;
-  k *= 0xff51afd7ed558ccdULL;
-  k ^= k >> 33;
-  k *= 0xc4ceb9fe1a85ec53ULL;
-  k ^= k >> 33;
-  return k;
+// The table holds one entry per occupied 2x2x2 block of voxels: the block's
+// packed key (the voxel key with the low bit of x, y and z cleared) and the
+// row ids of its eight voxels (-1 where absent).  A voxel's position in its
+// block is 4*(x&1) + 2*(y&1) + (z&1).  64-byte entries, two per cache line.
+// Open addressing with linear probing over entries, home entry = Fibonacci
+// (multiplicative) hash of the block key.  A point's 3x3x3 neighbourhood
+// spans exactly 8 blocks and its 5x5x5 neighbourhood 27, so a few lookups
+// return every neighbour, present or absent.
+struct __align__(64) BlockEntry {
+  unsigned long long key;
+  unsigned long long pad0;
+  int rows[8];
+  int pad1[4];
+};
+
+constexpr unsigned long long kBlockLowBits = 0x0000000100010001ull;
+
+__host__ __device__ __forceinline__ unsigned long long block_key(unsigned long long key) {
+  return key & ~kBlockLowBits;
+}
+__host__ __device__ __forceinline__ int block_local(unsigned long long key) {
+  return static_cast<int>(((key >> 30) & 4u) | ((key >> 15) & 2u) | (key & 1u));
+}
+__host__ __device__ __forceinline__ uint32_t block_home(unsigned long long bkey, uint32_t mask) {
+  return static_cast<uint32_t>((bkey * 0x9E3779B97F4A7C15ull) >> 32) & mask;
 }
 
 // ------------------------------------------------------------- handles --
 struct HashTable {
   int64_t n = 0;
-  int64_t capacity = 0;              // power of two
-  Slot* table = nullptr;             // [capacity]
+  int64_t capacity = 0;              // block entries, a power of two
+  BlockEntry* table = nullptr;       // [capacity]
   unsigned long long* keys = nullptr;  // [n]  packed key of each row (kEmptyKey if invalid)
   int* status = nullptr;             // [4]: latched errors, largest batch id
 };
@@ -71,7 +81,7 @@ struct KernelMap {
   int ntiles = 0;                    // 32-point tiles of the map build
   int* order = nullptr;              // [n] input rows in locality order, or null: input order
   int* buckets = nullptr;            // counting-sort buckets of that order (+ scan partials)
-  int* nbr = nullptr;                // [n, V]
+  int* nbr = nullptr;                // [n, V], rows in the row order (position k = input row order[k])
   int64_t* offs = nullptr;           // [V+1]
   int* in_rows = nullptr;            // [n*(V-1)] capacity, offs[V] used
   int* out_rows = nullptr;
@@ -127,6 +137,8 @@ struct ConvArgs {
 sc_status conv_fused(const ConvArgs& a);
 sc_status conv_weight_stationary(const ConvArgs& a);
 sc_status conv_simt(const ConvArgs& a);
+// nbr rows in input order (undoing the row order) into a device buffer
+sc_status kmap_unpermute_nbr(const KernelMap* m, int* dst, cudaStream_t s);
 bool fused_supported(const ConvArgs& a);
 sc_status conv_fused_noalloc(const ConvArgs& a);
 

@@ -56,7 +56,7 @@ def test_hash_query_finds_every_row_and_misses_absent_keys():
     q2 = np.array([[1, 10, 10, 10], [-1, 0, 0, 0], [0, 65535, 0, 0], [0, -3, 1, 1]], dtype=np.int32)
     np.testing.assert_array_equal(h.query(torch.from_numpy(q2).cuda()).cpu().numpy(), [-1, -1, -1, -1])
     assert len(present) == s.n
-    assert h.capacity >= 2 * s.n and (h.capacity & (h.capacity - 1)) == 0
+    assert h.capacity >= s.n and (h.capacity & (h.capacity - 1)) == 0
 
 
 # ------------------------------------------------------------------- map --
