@@ -43,7 +43,7 @@ L2_FLUSH_BYTES = 256 << 20
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=1)
@@ -60,13 +60,7 @@ def dist_env():
 
 def make_workload(idx: int, rank: int):
     from submanifold_sparse_convolution_hash_gb300 import scenes
-    w, s = scenes.workload(idx)
-    if rank > 0:  # replicas draw their own scene of the same recipe
-        if idx == 1:
-            s = scenes.lidar_scan(1001 + 7919 * rank, 100_000, s.dims)
-        else:
-            raise SystemExit("replicas are defined for workload 1")
-    return w, s
+    return scenes.workload(idx, replica=rank)  # each replica draws its own scene of the recipe
 
 
 def layer_tensors(w, s):
@@ -79,21 +73,25 @@ def layer_tensors(w, s):
 
 
 # ------------------------------------------------------------- algorithmic bytes --
-def algo_bytes(kernel: str, N: int, V: int, M: int, c_in: int, c_out: int, s: int, ntiles: int) -> float | None:
-    """Bytes each kernel must move at minimum (per launch)."""
+def algo_bytes_step(kernel: str, N: int, V: int, M: int, layers, s: int, ntiles: int):
+    """Bytes a kernel must move at minimum in one step (summed over its
+    launches in that step); None for kernels without a stated model."""
     lists = 8 * (M - N)
+    conv = sum(M * ci * s + N * co * s + 4 * N * V + V * ci * co * s for ci, co in layers)
     table = {
-        "hash_insert": 16 * N + 16 * N + 8 * N,            # coords in; N slots + row keys out
-        "kmap_probe": 8 * N + 4 * N * V + 4 * V * ntiles,  # row keys in; neighbour table + counts out
+        # coords in; row keys out; one row slot per point
+        "hash_insert": 16 * N + 8 * N + 4 * N,
+        # row keys in; neighbour table and per-tile hit masks out
+        "kmap_probe": 8 * N + 4 * N * V + 4 * V * ntiles,
         "kmap_scan": 8 * V * ntiles,
-        "kmap_fill": 4 * N * V + 4 * V * ntiles + lists,   # neighbour table in; (in, out) lists out
-        "pack_weights": 2 * V * c_in * c_out * s,
+        # neighbour table in; (in, out) lists out
+        "kmap_fill": 4 * N * V + 4 * V * ntiles + lists,
+        "order_count": 8 * N,
+        "order_scatter": 8 * N + 4 * N,
+        "pack_weights": sum(2 * V * ci * co * s for ci, co in layers),
         # gathered neighbour rows + one write per output row + neighbour table + weights
-        "subm_conv_fused": M * c_in * s + N * c_out * s + 4 * N * V + V * c_in * c_out * s,
-        "subm_conv_ws_centre": N * c_in * s + 4 * N * c_out + V * c_in * c_out * s // V,
-        "subm_conv_ws_scatter": (M - N) * c_in * s + 8 * (M - N) + 8 * (M - N) * c_out,
-        "cast_out": 4 * N * c_out + N * c_out * s,
-        "subm_conv_simt": M * c_in * s + N * c_out * s + 4 * N * V + V * c_in * c_out * s,
+        "subm_conv_fused": conv,
+        "subm_conv_simt": conv,
     }
     return table.get(kernel)
 
@@ -255,6 +253,21 @@ def run_reference(args):
 
 
 # ---------------------------------------------------------------------- GPU --
+def reduce_over_ranks(total_s: float, n_units: int, device, world: int):
+    """(slowest rank's timed seconds, voxels processed by all ranks).  Each
+    rank is an independent replica; this is the only collective and it runs
+    after the timed region."""
+    if world <= 1:
+        return float(total_s), float(n_units)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(total_s), float(n_units)], dtype=torch.float64, device=device)
+    tmax = t.clone()
+    dist.all_reduce(tmax, op=dist.ReduceOp.MAX)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(tmax[0].item()), float(t[1].item())
+
+
 def run_ours(args):
     import torch
 
@@ -269,29 +282,41 @@ def run_ours(args):
     from submanifold_sparse_convolution_hash_gb300 import binding as sc
 
     w, s = make_workload(args.workload, rank)
-    f_np, W_np = layer_tensors(w, s)
+    from submanifold_sparse_convolution_hash_gb300 import scenes as sc_scenes
     tdt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[w.dtype]
     esize = 4 if w.dtype == "f32" else 2
     V = w.K ** s.ndim
-    c_in, c_out = w.channels[0], w.channels[1]
+    layers = list(zip(w.channels[:-1], w.channels[1:]))  # (c_in, c_out) of each layer on the one map
+    f_np, W0 = layer_tensors(w, s)
+    Ws = [torch.from_numpy(W0).to(tdt).to(dev)]
+    for li, (ci, co) in enumerate(layers[1:], start=1):
+        Ws.append(torch.from_numpy(sc_scenes.weights(w.seed + li, V, ci, co)).to(tdt).to(dev))
+    c_in, c_out = layers[0]
     coords = torch.from_numpy(s.coords).to(dev)
     feats = torch.from_numpy(f_np).to(tdt).to(dev)
-    Wt = torch.from_numpy(W_np).to(tdt).to(dev)
-    out = torch.empty((s.n, c_out), dtype=tdt, device=dev)
+    outs = [torch.empty((s.n, co), dtype=tdt, device=dev) for _, co in layers]
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
-    # variant chosen from measured time on this map
+    # variant of each layer chosen from measured time on this map
     h0 = sc.sc_hash_build(coords)
     m0 = sc.sc_kmap_build(h0, s.ndim, w.K, s.dims)
     M = m0.map_size()
-    variant = sc.sc_subm_conv_tune(m0, feats, Wt, out=out, reps=5)
-    ntiles = (s.n + 63) // 64
+    variants = []
+    x = feats
+    for li, W in enumerate(Ws):
+        relu = li + 1 < len(Ws)
+        variants.append(sc.sc_subm_conv_tune(m0, x, W, out=outs[li], relu=relu, reps=5))
+        x = outs[li]
+    ntiles = (s.n + 31) // 32
 
     def step():
         h = sc.sc_hash_build(coords)
         m = sc.sc_kmap_build(h, s.ndim, w.K, s.dims, sync=False)
-        sc.sc_subm_conv_fwd(m, feats, Wt, out=out, variant=variant)
+        xin = feats
+        for li, W in enumerate(Ws):
+            sc.sc_subm_conv_fwd(m, xin, W, out=outs[li], relu=li + 1 < len(Ws), variant=variants[li])
+            xin = outs[li]
         return h, m
 
     for _ in range(max(args.warmup, 3)):
@@ -323,15 +348,7 @@ def run_ours(args):
     keep.clear()
     step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
     total_s = sum(step_ms) / 1e3
-    if world > 1:
-        t = torch.tensor([total_s], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_s = float(t.item())
-        n_all = torch.tensor([s.n], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(n_all)
-        n_total = float(n_all.item())
-    else:
-        n_total = float(s.n)
+    total_s, n_total = reduce_over_ranks(total_s, s.n, dev, world)
     # error status of the last map (outside the timed region)
     h_chk, m_chk = step()
     m_chk.check()
@@ -339,7 +356,7 @@ def run_ours(args):
 
     value = n_total * args.steps / total_s / 1e6
     ms_per_step = 1e3 * total_s / args.steps
-    flops = 2.0 * M * c_in * c_out
+    flops = sum(2.0 * M * ci * co for ci, co in layers)
     per_kernel = {}
     for k, (n_l, tot) in prof.items():
         per_kernel[k] = {"launches": n_l, "avg_us": round(1e3 * tot / max(n_l, 1), 3), "share": None}
@@ -351,7 +368,9 @@ def run_ours(args):
     map_ms = sum(prof[k][1] for k in ("hash_insert", "kmap_probe", "kmap_scan", "kmap_fill") if k in prof) / args.steps
     dom = max(prof, key=lambda k: prof[k][1])
     peaks = load_peaks()
-    ab = algo_bytes(dom, s.n, V, M, c_in, c_out, esize, ntiles)
+    ab_step = algo_bytes_step(dom, s.n, V, M, layers, esize, ntiles)
+    launches_per_step = prof[dom][0] / args.steps
+    ab = ab_step / launches_per_step if ab_step else None
     avg_s = prof[dom][1] / prof[dom][0] / 1e3
     achieved = ab / avg_s / 1e9 if ab else None
     roofline = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1) if achieved else None,
@@ -359,15 +378,18 @@ def run_ours(args):
                 "frac": round(achieved / peaks["hbm_gbs"], 4) if achieved else None,
                 "traffic": recorded_traffic(dom), "peak_source": f"{peaks['source']} hbm_gbs",
                 "algorithmic_bytes_per_launch": ab}
-    conv_roof_s = max(flops / (peaks["bf16_tflops"] * 1e12),
-                      (algo_bytes("subm_conv_fused", s.n, V, M, c_in, c_out, esize, ntiles)) / (peaks["hbm_gbs"] * 1e9))
+    # each layer's roofline time: the slower of its FLOPs at tensor peak and
+    # its gathered bytes at HBM bandwidth; summed over the layers of a step
+    conv_roof_s = sum(max(2.0 * M * ci * co / (peaks["bf16_tflops"] * 1e12),
+                          algo_bytes_step("subm_conv_fused", s.n, V, M, [(ci, co)], esize, ntiles)
+                          / (peaks["hbm_gbs"] * 1e9)) for ci, co in layers)
 
     line = {
         "metric": METRIC, "value": round(value, 4), "unit": "Mvoxels/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": {"workload": w.name, "N": s.n, "map_size": M, "K": w.K, "c_in": c_in, "c_out": c_out,
-                   "variant": variant, "l2": "flushed before every step (256 MB write, outside the events)",
+        "config": {"workload": w.name, "N": s.n, "map_size": M, "K": w.K, "layers": layers,
+                   "variant": variants, "l2": "flushed before every step (256 MB write, outside the events)",
                    "kmap_sync": False, "parallelism": "replicas" if world > 1 else "single"},
         "layer_tflops": round(flops / (conv_ms / 1e3) / 1e12, 3) if conv_ms else None,
         "layer_ms": round(conv_ms, 5),
@@ -380,9 +402,9 @@ def run_ours(args):
     }
 
     if not args.no_e2e and rank == 0:
-        line["e2e"] = run_e2e(args, w, s, f_np, W_np, tdt, dev, variant, world)
+        line["e2e"] = run_e2e(args, w, s, f_np, Ws, tdt, dev, variants, world)
     if not args.no_cpu_baseline and rank == 0:
-        line["cpu_baseline"] = cpu_oracle_run(s, w.K, feats.float().cpu().numpy(), W_np, args.cpu_seconds)
+        line["cpu_baseline"] = cpu_oracle_run(s, w.K, feats.float().cpu().numpy(), W0, args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -390,24 +412,28 @@ def run_ours(args):
         torch.distributed.destroy_process_group()
 
 
-def run_e2e(args, w, s, f_np, W_np, tdt, dev, variant, world):
-    """Same metric through the public calls, host buffers in and out."""
+def run_e2e(args, w, s, f_np, Ws_dev, tdt, dev, variants, world):
+    """Same metric through the public calls, host buffers in and out: every
+    step copies coords, features and all layer weights from pinned host
+    memory, builds the map with the default (synchronising, error-checking)
+    call, runs every layer and copies the last layer's output back."""
     import torch
     from submanifold_sparse_convolution_hash_gb300 import binding as sc
     c_h = torch.from_numpy(s.coords).pin_memory()
     f_h = torch.from_numpy(f_np).to(tdt).pin_memory()
-    W_h = torch.from_numpy(W_np).to(tdt).pin_memory()
-    o_h = torch.empty((s.n, W_np.shape[2]), dtype=tdt).pin_memory()
+    W_h = [W.cpu().pin_memory() for W in Ws_dev]
+    o_h = torch.empty((s.n, Ws_dev[-1].shape[2]), dtype=tdt).pin_memory()
     stream = torch.cuda.current_stream(dev)
 
     def step():
         c = c_h.to(dev, non_blocking=True)
-        f = f_h.to(dev, non_blocking=True)
-        W = W_h.to(dev, non_blocking=True)
+        x = f_h.to(dev, non_blocking=True)
+        Ws = [W.to(dev, non_blocking=True) for W in W_h]
         h = sc.sc_hash_build(c)
         m = sc.sc_kmap_build(h, s.ndim, w.K, s.dims)  # default: synchronises and checks errors
-        o = sc.sc_subm_conv_fwd(m, f, W, variant=variant)
-        o_h.copy_(o, non_blocking=True)
+        for li, W in enumerate(Ws):
+            x = sc.sc_subm_conv_fwd(m, x, W, relu=li + 1 < len(Ws), variant=variants[li])
+        o_h.copy_(x, non_blocking=True)
         return h, m
 
     for _ in range(3):
@@ -421,7 +447,7 @@ def run_e2e(args, w, s, f_np, W_np, tdt, dev, variant, world):
     b.record(stream)
     b.synchronize()
     ms = a.elapsed_time(b) / args.e2e_steps
-    bi = c_h.numel() * 4 + f_h.numel() * f_h.element_size() + W_h.numel() * W_h.element_size()
+    bi = c_h.numel() * 4 + f_h.numel() * f_h.element_size() + sum(W.numel() * W.element_size() for W in W_h)
     bo = o_h.numel() * o_h.element_size()
     return {"value": round(s.n / (ms / 1e3) / 1e6, 4), "unit": "Mvoxels/s", "ms_per_step": round(ms, 4),
             "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo), "steps": args.e2e_steps}

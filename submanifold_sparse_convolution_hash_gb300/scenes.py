@@ -27,6 +27,8 @@ removed.
 from __future__ import annotations
 
 import math
+import os
+from concurrent.futures import ThreadPoolExecutor
 from dataclasses import dataclass, field
 
 import numpy as np
@@ -314,10 +316,29 @@ def features(seed: int, n: int, c: int, std: float = 1.0) -> np.ndarray:
     """float32 [n, c] ~ N(0, std^2)."""
     rng = SplitMix64(seed, 10)
     out = np.empty(n * c, dtype=np.float32)
-    step = 1 << 24
+    step = 1 << 22
+    # chunk k starts at the counter the serial draw would reach there (each
+    # normal(m) call consumes 2 * ceil(m / 2) counters), so the chunks can be
+    # drawn on threads and the values equal one serial pass
+    jobs = []
+    state = rng.state
     for s in range(0, n * c, step):
         m = min(step, n * c - s)
-        out[s:s + m] = (rng.normal(m) * std).astype(np.float32)
+        jobs.append((s, m, state))
+        state = (state + 2 * ((m + 1) // 2) * _GAMMA) & _M64
+
+    def draw(job):
+        s, m, st = job
+        r = SplitMix64.__new__(SplitMix64)
+        r.state = st
+        out[s:s + m] = (r.normal(m) * std).astype(np.float32)
+
+    if len(jobs) > 1:
+        with ThreadPoolExecutor(max_workers=min(len(jobs), os.cpu_count() or 1)) as ex:
+            list(ex.map(draw, jobs))
+    else:
+        for j in jobs:
+            draw(j)
     return out.reshape(n, c)
 
 
@@ -344,8 +365,10 @@ class Workload:
     w_std_unit: bool = False  # True: W ~ N(0,1) instead of 1/sqrt(V*C_in)
 
 
-def workload(idx: int, scale: float = 1.0) -> tuple:
+def workload(idx: int, scale: float = 1.0, replica: int = 0) -> tuple:
     """(Workload, Scene) for workload ``idx`` (0..4); ``scale`` < 1 shrinks N and grid.
+    ``replica`` > 0 draws another scene of the same recipe (scene seed shifted
+    by 7919 * replica; weights unchanged), one per independent replica.
 
     0: 2D 64x64, 200 cells, 3x3, C 16, fp32, W ~ N(0,1)
     1: LiDAR-like 1440x1440x41, ~100k, 3x3x3, C 32, fp16
@@ -353,24 +376,26 @@ def workload(idx: int, scale: float = 1.0) -> tuple:
     3: 4 LiDAR-like scans ~120k each, 3x3x3, 8 layers 32->...->256, fp16
     4: 2048x2048x64, ~2M, 5x5x5, C 128, bf16
     """
+    r = 7919 * replica
+
     def sdims(d, keep_z=True):
         f = math.sqrt(scale)
         return tuple(max(16, int(d[a] * f)) if (a < 2 or not keep_z) else d[a] for a in range(3))
 
     if idx == 0:
         w = Workload("2d_uniform_64x64_n200_k3_c16_f32", None, 3, (16, 16), "f32", 1000, True)
-        return w, uniform_2d(1000, (64, 64), max(8, int(200 * scale)) if scale < 1 else 200)
+        return w, uniform_2d(1000 + r, (64, 64), max(8, int(200 * scale)) if scale < 1 else 200)
     if idx == 1:
         w = Workload("lidar_1440x1440x41_n100k_k3_c32_f16", None, 3, (32, 32), "f16", 1001)
-        return w, lidar_scan(1001, int(100_000 * scale), sdims((1440, 1440, 41)))
+        return w, lidar_scan(1001 + r, int(100_000 * scale), sdims((1440, 1440, 41)))
     if idx == 2:
         w = Workload("indoor_512x512x128_n1m_k3_c64_bf16", None, 3, (64, 64), "bf16", 1002)
-        return w, indoor_scene(1002, int(1_000_000 * scale), sdims((512, 512, 128)))
+        return w, indoor_scene(1002 + r, int(1_000_000 * scale), sdims((512, 512, 128)))
     if idx == 3:
         w = Workload("lidar_batch4x120k_k3_8layers_32to256_f16", None, 3,
                      (32, 32, 64, 64, 128, 128, 256, 256, 256), "f16", 1003)
-        return w, batch_of_scans(1003, 4, int(120_000 * scale), sdims((1440, 1440, 41)))
+        return w, batch_of_scans(1003 + r, 4, int(120_000 * scale), sdims((1440, 1440, 41)))
     if idx == 4:
         w = Workload("surfaces_2048x2048x64_n2m_k5_c128_bf16", None, 5, (128, 128), "bf16", 1004)
-        return w, indoor_scene(1004, int(2_000_000 * scale), sdims((2048, 2048, 64)))
+        return w, indoor_scene(1004 + r, int(2_000_000 * scale), sdims((2048, 2048, 64)))
     raise ValueError(idx)

@@ -1,0 +1,143 @@
+"""Parity at the full sizes of the four GPU workloads, in the launch
+configuration the benchmark times: one asynchronous map build (no host sync
+inside it; errors read afterwards), the default row order, then the layer
+with the variant the tuner picks, and each variant forced.
+
+The oracle computes the whole neighbour table at these sizes (a nested loop
+over points x offsets), so the map is compared in full: the neighbour table
+element by element and the per-offset lists as pair sets.  The features are
+compared on sampled output rows that the oracle computes one by one: evenly
+spaced rows, the last 128-row tile (ragged at every workload), and a seeded
+random draw.  Workload 3 runs its eight layers on one map; each layer is
+checked with the oracle fed the GPU's own input to that layer.  The whole
+stack end to end is checked at a reduced scale, where the oracle can run
+every row of every layer.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import TORCH_DT, assert_close
+from submanifold_sparse_convolution_hash_gb300 import binding as sc
+from submanifold_sparse_convolution_hash_gb300 import scenes
+
+pytestmark = pytest.mark.gpu
+
+
+def sample_rows(n, seed, k_even=1024, k_rand=512):
+    even = np.linspace(0, n - 1, min(n, k_even)).astype(np.int64)
+    tail = np.arange(max(0, (n - 1) // 128 * 128), n, dtype=np.int64)
+    rnd = scenes.SplitMix64(seed, 99).integers(0, n, k_rand)
+    return np.unique(np.concatenate([even, tail, rnd]))
+
+
+class Full:
+    def __init__(self, idx):
+        self.w, self.s = scenes.workload(idx)
+        self.V = self.w.K ** self.s.ndim
+        self.coords = torch.from_numpy(self.s.coords).cuda()
+        self.h = sc.sc_hash_build(self.coords)
+        self.m = sc.sc_kmap_build(self.h, self.s.ndim, self.w.K, self.s.dims, sync=False)
+        self.m.check()
+        self.rows = sample_rows(self.s.n, self.w.seed)
+
+    def layer(self, li, x=None):
+        """(feats, W) of layer li as device tensors; x overrides the input."""
+        ci, co = self.w.channels[li], self.w.channels[li + 1]
+        dt = TORCH_DT[self.w.dtype]
+        if x is None:
+            x = torch.from_numpy(scenes.features(self.w.seed, self.s.n, ci)).to(dt).cuda()
+        W = scenes.weights(self.w.seed + li, self.V, ci, co, std=1.0 if self.w.w_std_unit else None)
+        return x, torch.from_numpy(W).to(dt).cuda()
+
+
+_CACHE = {}
+
+
+def full(idx):
+    if idx not in _CACHE:
+        _CACHE.clear()  # one workload resident at a time
+        torch.cuda.empty_cache()
+        _CACHE[idx] = Full(idx)
+    return _CACHE[idx]
+
+
+@pytest.mark.parametrize("idx", [1, 2, 3, 4])
+def test_full_size_kmap_matches_oracle(idx):
+    F = full(idx)
+    s = F.s
+    ref = oracle.kmap(s.coords, s.ndim, F.w.K, s.dims)
+    nbr = F.m.nbr().cpu().numpy()
+    assert nbr.shape == ref.shape
+    assert np.array_equal(nbr, ref), f"workload {idx}: {int((nbr != ref).sum())} neighbour entries differ"
+    centre = (F.V - 1) // 2
+    assert np.array_equal(ref[:, centre], np.arange(s.n, dtype=np.int32))
+    # per-offset lists: same counts, every pair a real neighbour pair, no
+    # output row twice in a segment -- together the same set as the oracle's
+    offs, ins, outs = (t.cpu().numpy() for t in F.m.lists())
+    counts = (ref >= 0).sum(axis=0)
+    counts[centre] = 0
+    assert np.array_equal(np.diff(offs), counts)
+    assert F.m.map_size() == int(counts.sum()) + s.n
+    for v in range(F.V):
+        i = ins[offs[v]:offs[v + 1]].astype(np.int64)
+        o = outs[offs[v]:offs[v + 1]].astype(np.int64)
+        assert np.array_equal(ref[o, v], i), f"offset {v}: a listed pair is not a neighbour pair"
+        seen = np.zeros(s.n, dtype=bool)
+        seen[o] = True
+        assert int(seen.sum()) == len(o), f"offset {v}: an output row is listed twice"
+
+
+@pytest.mark.parametrize("variant", [None, "fused", "ws"])
+@pytest.mark.parametrize("idx", [1, 2, 4])
+def test_full_size_layer_on_sampled_rows(idx, variant):
+    F = full(idx)
+    s, w = F.s, F.w
+    x, W = F.layer(0)
+    if variant is None:
+        out = torch.empty((s.n, W.shape[2]), dtype=W.dtype, device="cuda")
+        variant = sc.sc_subm_conv_tune(F.m, x, W, out=out, reps=2)
+    out = sc.sc_subm_conv_fwd(F.m, x, W, variant=variant)
+    torch.cuda.synchronize()
+    ref = oracle.subm_conv(s.coords, x.double().cpu().numpy(), W.double().cpu().numpy(), s.ndim, w.K, s.dims,
+                           rows=F.rows)
+    assert_close(out[torch.from_numpy(F.rows).cuda()], ref, w.dtype, f"workload {idx} {variant}")
+    F.m.check()
+
+
+def test_full_size_eight_layer_stack_per_layer():
+    F = full(3)
+    s, w = F.s, F.w
+    x = None
+    for li in range(len(w.channels) - 1):
+        x, W = F.layer(li, x)
+        relu = li + 2 < len(w.channels)
+        out = torch.empty((s.n, W.shape[2]), dtype=W.dtype, device="cuda")
+        variant = sc.sc_subm_conv_tune(F.m, x, W, out=out, relu=relu, reps=2)
+        y = sc.sc_subm_conv_fwd(F.m, x, W, relu=relu, variant=variant)
+        torch.cuda.synchronize()
+        ref = oracle.subm_conv(s.coords, x.double().cpu().numpy(), W.double().cpu().numpy(), s.ndim, w.K,
+                               s.dims, relu=relu, rows=F.rows)
+        assert_close(y[torch.from_numpy(F.rows).cuda()], ref, w.dtype, f"layer {li} ({variant})")
+        x = y
+    F.m.check()
+
+
+def test_eight_layer_stack_end_to_end_reduced_scale():
+    w, s = scenes.workload(3, scale=0.005)
+    V = w.K ** s.ndim
+    dt = TORCH_DT[w.dtype]
+    h = sc.sc_hash_build(torch.from_numpy(s.coords).cuda())
+    m = sc.sc_kmap_build(h, s.ndim, w.K, s.dims, sync=False)
+    x = torch.from_numpy(scenes.features(w.seed, s.n, w.channels[0])).to(dt).cuda()
+    x0 = x.double().cpu().numpy()
+    Ws = [torch.from_numpy(scenes.weights(w.seed + li, V, ci, co)).to(dt).cuda()
+          for li, (ci, co) in enumerate(zip(w.channels[:-1], w.channels[1:]))]
+    for li, W in enumerate(Ws):
+        x = sc.sc_subm_conv_fwd(m, x, W, relu=li + 1 < len(Ws))
+    torch.cuda.synchronize()
+    ref = oracle.subm_conv_stack(s.coords, x0, [W.double().cpu().numpy() for W in Ws], s.ndim, w.K, s.dims,
+                                 w.dtype)
+    assert_close(x, ref[-1], w.dtype, "eight layers end to end")
+    m.check()

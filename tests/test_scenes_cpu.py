@@ -62,3 +62,15 @@ def test_features_and_weights():
     assert w.shape == (27, 32, 64)
     assert abs(w.std() * np.sqrt(27 * 32) - 1) < 0.05
     np.testing.assert_array_equal(f, scenes.features(1, 100, 32))
+
+
+def test_threaded_feature_draw_equals_one_serial_pass():
+    """Features are drawn in 2^22-value chunks on threads; each chunk starts
+    at the counter a serial pass reaches there."""
+    n, c = 70_000, 64  # two chunks, the second one short
+    f = scenes.features(5, n, c)
+    rng = scenes.SplitMix64(5, 10)
+    parts = []
+    for s in range(0, n * c, 1 << 22):
+        parts.append(rng.normal(min(1 << 22, n * c - s)).astype(np.float32))
+    np.testing.assert_array_equal(f.reshape(-1), np.concatenate(parts))
