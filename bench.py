@@ -51,6 +51,8 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--variant", choices=["fused", "ws", "simt"], default=None,
+                    help="run every layer with this variant instead of the measured choice")
     return ap.parse_args()
 
 
@@ -306,7 +308,10 @@ def run_ours(args):
     x = feats
     for li, W in enumerate(Ws):
         relu = li + 1 < len(Ws)
-        variants.append(sc.sc_subm_conv_tune(m0, x, W, out=outs[li], relu=relu, reps=5))
+        if args.variant:
+            variants.append(args.variant)
+        else:
+            variants.append(sc.sc_subm_conv_tune(m0, x, W, out=outs[li], relu=relu, reps=5))
         x = outs[li]
     ntiles = (s.n + 31) // 32
 
@@ -389,7 +394,7 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": w.name, "N": s.n, "map_size": M, "K": w.K, "layers": layers,
-                   "variant": variants, "l2": "flushed before every step (256 MB write, outside the events)",
+                   "variant": variants, "variant_choice": "given" if args.variant else "measured", "l2": "flushed before every step (256 MB write, outside the events)",
                    "kmap_sync": False, "parallelism": "replicas" if world > 1 else "single"},
         "layer_tflops": round(flops / (conv_ms / 1e3) / 1e12, 3) if conv_ms else None,
         "layer_ms": round(conv_ms, 5),

@@ -22,19 +22,23 @@
 //    fp32 products with vector atomics.  The centre offset (identity map)
 //    writes its product with plain stores first.
 //
-// CTA (288 threads; as many per SM as shared memory and TMEM allow, each
+// CTA ((NPW + 6) warps; as many per SM as shared memory and TMEM allow, each
 // taking tiles round-robin):
-//   warps 0-3  producers: per pipeline stage, each thread cp.asyncs 16-byte
-//              chunks of its tile rows' neighbour feature rows into a
-//              swizzled K-major tile (four lanes per 64-byte row, so a warp
-//              instruction covers whole rows; a missing neighbour is a
-//              zero-filled copy of size 0); thread 0 bulk-copies the matching
-//              W slices from a pre-swizzled image.  A stage holds G (offset,
-//              channel-panel) sub-blocks.  Each warp signals a stage LAG
-//              stages later, after its copies landed and a proxy fence.
-//   warp 4     allocates TMEM (two accumulators of C_out fp32 columns); lane 0
+//   NPW producer warps (4, 8 or 16): per pipeline stage, each thread
+//              cp.asyncs 16-byte chunks of its warp's tile rows' neighbour
+//              feature rows into a swizzled K-major tile (a warp instruction
+//              covers whole rows; a missing neighbour is a zero-filled copy of
+//              size 0, skipped when that row of the buffer is already zero).
+//              A stage holds G (offset, channel-panel) sub-blocks.  Each
+//              thread's arrival on the stage barrier fires when its copies
+//              land (cp.async.mbarrier.arrive.noinc), so a warp never waits
+//              for its own copies.
+//   1 warp     weight loader: one thread bulk-copies the matching W slices
+//              from a pre-swizzled image into each stage and prefetches the
+//              next tile's neighbour-table block into L2.
+//   1 warp     MMA issuer: allocates TMEM (two accumulators of C_out fp32 columns); lane 0
 //              issues tcgen05.mma (M = 128, N = C_out, K = 16) and commits.
-//   warps 5-8  epilogue: TMEM lane quadrant (warp % 4) -> registers -> global,
+//   4 warps    epilogue: TMEM lane quadrant (warp % 4) -> registers -> global,
 //              overlapping the next tile's mainloop through the second
 //              accumulator.
 // The row gathers use the load/store path: a TMA tile::gather4 moves four
@@ -46,6 +50,8 @@
 // expiry the CTA latches kDevErrTimeout, stops issuing work, waits (bounded)
 // for what it issued, and still frees its TMEM.
 
+#include <cstdio>
+#include <cstdlib>
 #include <mutex>
 
 #include "sc_internal.cuh"
@@ -59,8 +65,6 @@ namespace sc {
 namespace {
 
 constexpr int kRows = 128;        // rows per tile (MMA M)
-constexpr int kThreads = 288;     // 4 producer warps, MMA warp, 4 epilogue warps
-constexpr int kProducers = 128;
 constexpr int kMaxStages = 8;
 constexpr int kBarriers = 2 * kMaxStages + 5;  // full[S], empty[S], acc_full[2], acc_empty[2], done
 constexpr unsigned long long kWaitNs = 2000000000ull;
@@ -132,17 +136,14 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-// Waits until at most `n` (0..4) of this thread's cp.async groups are pending.
-__device__ __forceinline__ void cp_async_wait_dyn(int n) {
-  switch (n) {
-    case 0: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
-    case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
-    case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
-    case 3: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
-    default: asm volatile("cp.async.wait_group 4;" ::: "memory"); break;
-  }
+// Arrive on an mbarrier once every cp.async this thread issued so far has
+// landed, without incrementing its pending count (the arrival is counted in
+// the barrier's expected count).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
+// Waits until every cp.async this thread issued has landed.
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -158,13 +159,18 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                       uint32_t accumulate) {
+// D[tmem] (+)= A * B for one K = 16 step (M = 128, kind::f16, cta_group::1);
+// the two shared-memory descriptors are passed as (low, high) 32-bit halves
+// that share the high half.
+__device__ __forceinline__ void tc_mma_lohi(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t hi,
+                                            uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+      "mov.b64 da, {%1, %3};\n\t"
+      "mov.b64 db, {%2, %3};\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
@@ -228,8 +234,10 @@ struct TcParams {
   const int64_t* offs;       // [V+1]
   const int* ws_tiles;       // [V+1]
   int64_t n;
-  int num_tiles;
-  int V, c_in, c_out, relu, stages, group, lag, acc_cols, tmem_cols;
+  int num_tiles;             // 128-row tiles (output-stationary) or tuple tiles (weight-stationary scatter)
+  int num_units;             // work units: ceil(num_tiles / T)
+  int V, c_in, c_out, relu, stages, group, acc_cols, tmem_cols;
+  int nbuf;                  // accumulator buffers (2: the epilogue overlaps the next unit)
   int* status;
 };
 
@@ -272,63 +280,88 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
   }
 }
 
-// Rows, list base and (for the weight-stationary scatter) offset of a tile.
+// A work unit: T consecutive 128-row tiles (output-stationary; the T tiles
+// share every weight slice the CTA loads) or one 128-row tile of tuples
+// (weight-stationary, T = 1).
 struct TileInfo {
   int64_t row0;  // first output row (output-stationary, centre)
   int64_t lb;    // first list entry (weight-stationary scatter)
-  int nrows;
+  int nrows;     // rows of the unit, up to 128 T
   int v;         // the offset of a weight-stationary tile
 };
 
-template <int MODE>
-__device__ __forceinline__ TileInfo tile_info(const TcParams& p, int tile) {
+template <int MODE, int T>
+__device__ __forceinline__ TileInfo tile_info(const TcParams& p, int u) {
   TileInfo t;
   t.row0 = 0;
   t.lb = 0;
   t.v = (p.V - 1) / 2;
   if (MODE == kWsScatter) {
-    int lo = 0, hi = p.V;  // largest v with ws_tiles[v] <= tile
+    int lo = 0, hi = p.V;  // largest v with ws_tiles[v] <= u
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
-      if (__ldg(p.ws_tiles + mid) <= tile) lo = mid; else hi = mid;
+      if (__ldg(p.ws_tiles + mid) <= u) lo = mid; else hi = mid;
     }
     t.v = lo;
     const int64_t seg_end = __ldg(p.offs + lo + 1);
-    t.lb = __ldg(p.offs + lo) + static_cast<int64_t>(tile - __ldg(p.ws_tiles + lo)) * kRows;
+    t.lb = __ldg(p.offs + lo) + static_cast<int64_t>(u - __ldg(p.ws_tiles + lo)) * kRows;
     t.nrows = static_cast<int>(min(static_cast<int64_t>(kRows), seg_end - t.lb));
   } else {
-    t.row0 = static_cast<int64_t>(tile) * kRows;
-    t.nrows = static_cast<int>(min(static_cast<int64_t>(kRows), p.n - t.row0));
+    t.row0 = static_cast<int64_t>(u) * kRows * T;
+    t.nrows = static_cast<int>(min(static_cast<int64_t>(kRows) * T, p.n - t.row0));
   }
   return t;
 }
 
-template <int MODE>
-__device__ __forceinline__ int tile_kblocks(const TcParams& p, int tile, int P) {
+// Offsets present in any tile of an output-stationary unit, centre included.
+template <int T>
+__device__ __forceinline__ uint4 unit_mask(const TcParams& p, int u) {
+  uint4 m = tile_mask(p, u * T);
+#pragma unroll
+  for (int k = 1; k < T; ++k) {
+    if (u * T + k < p.num_tiles) {
+      const uint4 x = tile_mask(p, u * T + k);
+      m.x |= x.x;
+      m.y |= x.y;
+      m.z |= x.z;
+      m.w |= x.w;
+    }
+  }
+  return m;
+}
+
+template <int MODE, int T>
+__device__ __forceinline__ int unit_kblocks(const TcParams& p, int u, int P) {
   if (MODE != kOutputStationary) return P;
-  const uint4 m = tile_mask(p, tile);
+  const uint4 m = unit_mask<T>(p, u);
   return (__popc(m.x) + __popc(m.y) + __popc(m.z) + __popc(m.w)) * P;
 }
 
-template <int BK, int MODE, bool BF16>
-__global__ void __launch_bounds__(kThreads) k_conv_tc(const TcParams p) {
+// Register budget: 4 producer warps run three CTAs per SM, 8 run two, 16 one.
+template <int BK, int MODE, bool BF16, int NPW, int T>
+__global__ void __launch_bounds__((NPW + 6) * 32, NPW == 4 ? 3 : (NPW == 8 ? 2 : 1)) k_conv_tc(const TcParams p) {
   constexpr int ROWB = BK * 2;          // bytes per tile row (= swizzle width)
-  constexpr int A_SUB = kRows * ROWB;   // one (offset, panel) sub-block of A
+  constexpr int A_PART = kRows * ROWB;  // one 128-row MMA operand of a sub-block
+  constexpr int A_SUB = T * A_PART;     // one (offset, panel) sub-block of A
   constexpr int CPR = ROWB / 16;        // 16-byte chunks per row
-  constexpr int RPT = CPR;              // rows per producer thread
-  constexpr int RSTEP = kProducers / CPR;
+  constexpr int RW = kRows * T / NPW;   // unit rows per producer warp
+  constexpr int RSTEP = 32 / CPR;       // rows covered by one warp instruction
+  constexpr int RPT = RW / RSTEP;       // copy instructions per producer thread and sub-block
+  static_assert(RPT >= 1 && RW <= 32 && kRows % RW == 0, "producer warps must cover whole rows of one part");
+  static_assert(MODE == kOutputStationary || T == 1, "weight-stationary units are single tiles");
   constexpr uint32_t LAYOUT = layout_code<BK>();
   constexpr uint32_t SBO = 8 * ROWB;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int S = p.stages, G = p.group;
+  const int S = p.stages, G = p.group, NB = p.nbuf;
   const int B_SUB = p.c_out * ROWB;
   uint8_t* sA = smem;
   uint8_t* sB = sA + S * G * A_SUB;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sB + S * G * B_SUB);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + kBarriers);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+  uint32_t* s_dirty = s_tmem + 4;  // [NPW][S * G] zero-row masks of the producer warps
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int P = p.c_in / BK;
@@ -339,18 +372,19 @@ __global__ void __launch_bounds__(kThreads) k_conv_tc(const TcParams p) {
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(full0 + 8 * s, 5);   // 4 producer warps + the expect_tx arrival (+ weight bytes)
+      // one copy-completion arrival per producer thread + the weight loader's expect_tx
+      mbar_init(full0 + 8 * s, NPW * 32 + 1);
       mbar_init(empty0 + 8 * s, 1);  // one tcgen05.commit
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(accf0 + 8 * b, 1);   // one tcgen05.commit per tile
+      mbar_init(accf0 + 8 * b, 1);   // one tcgen05.commit per unit
       mbar_init(acce0 + 8 * b, 4);   // one arrival per epilogue warp
     }
     mbar_init(done_bar, 1);
     *s_abort = 0;
     fence_mbar_init();
   }
-  if (warp == 4) {
+  if (warp == NPW) {
     tmem_alloc(smem_u32(s_tmem), static_cast<uint32_t>(p.tmem_cols));
     tmem_relinquish();
   }
@@ -359,63 +393,126 @@ __global__ void __launch_bounds__(kThreads) k_conv_tc(const TcParams p) {
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
 
-  if (warp < 4) {
+  if (warp < NPW) {
     // ======================================================= producers
-    const int pt = threadIdx.x;         // 0..127
-    const int chunk = pt % CPR;         // 16-byte chunk of a row
-    const int rbase = pt / CPR;         // rows rbase + RSTEP * k, k < RPT
-    const int lag = p.lag;
+    const int chunk = lane % CPR;      // 16-byte chunk of a row
+    const int rw0 = RW * warp;         // this warp's unit rows: rw0 .. rw0 + RW - 1, all in one part
+    const int part_off = (rw0 / kRows) * A_PART;
+    const int rp0 = rw0 % kRows;       // first of them within the part
+    // per (stage, sub-block): bit j set while row rw0 + j of that buffer may
+    // hold data; clear bits are rows known to be zero, which an absent
+    // neighbour then needs no zero-filling copy for
+    uint32_t* dirty = s_dirty + warp * S * G;
+    for (int e = lane; e < S * G; e += 32) dirty[e] = 0xFFFFFFFFu;
+    __syncwarp();
     uint32_t it = 0;
-    if (MODE == kOutputStationary && pt == 0 && static_cast<int>(blockIdx.x) < p.num_tiles) {
-      const TileInfo t0 = tile_info<MODE>(p, blockIdx.x);
-      const uint32_t bytes = (static_cast<uint32_t>(t0.nrows) * V * 4) & ~15u;
-      if (bytes) bulk_prefetch_l2(p.nbr + t0.row0 * V, bytes);
-    }
-    for (int tile = blockIdx.x; tile < p.num_tiles && !*s_abort; tile += gridDim.x) {
-      const TileInfo t = tile_info<MODE>(p, tile);
+    for (int u = blockIdx.x; u < p.num_units && !*s_abort; u += gridDim.x) {
+      const TileInfo t = tile_info<MODE, T>(p, u);
       uint4 m = make_uint4(0, 0, 0, 0);
       int v = t.v;
       if (MODE == kOutputStationary) {
-        m = tile_mask(p, tile);
+        m = unit_mask<T>(p, u);
         v = next_present(m, -1, V);
-        const int nt = tile + gridDim.x;
-        if (pt == 0 && nt < p.num_tiles) {
-          const TileInfo tn = tile_info<MODE>(p, nt);
-          const uint32_t bytes = (static_cast<uint32_t>(tn.nrows) * V * 4) & ~15u;
-          if (bytes) bulk_prefetch_l2(p.nbr + tn.row0 * V, bytes);
-        }
       }
-      const int nkb = tile_kblocks<MODE>(p, tile, P);
-      // source rows of this thread's tile rows for the current offset (the
-      // tile's block of the neighbour table is contiguous)
-      int src[RPT];
-      auto load_rows = [&](int vv) {
-#pragma unroll
-        for (int k = 0; k < RPT; ++k) {
-          const int r = rbase + RSTEP * k;
-          int j = -1;
-          if (r < t.nrows) {
-            if (MODE == kOutputStationary) j = __ldg(p.nbr + (t.row0 + r) * V + vv);
-            else if (MODE == kWsScatter) j = __ldg(p.in_rows + t.lb + r);
-            else j = static_cast<int>(t.row0 + r);
-          }
-          src[k] = j;
-        }
+      const int nkb = unit_kblocks<MODE, T>(p, u, P);
+      // Lane j < RW of warp w fetches the source row of unit row RW w + j for
+      // an offset; the warp's lanes then take the rows they copy by shuffle,
+      // so each offset costs one index load per row, issued an offset ahead.
+      auto fetch = [&](int vv) -> int {
+        const int r = rw0 + lane;
+        if (vv >= V || lane >= RW || r >= t.nrows) return -1;
+        if (MODE == kOutputStationary) return __ldg(p.nbr + (t.row0 + r) * V + vv);
+        if (MODE == kWsScatter) return __ldg(p.in_rows + t.lb + r);
+        return static_cast<int>(t.row0 + r);
       };
-      load_rows(v);
+      int src[RPT];
+      uint32_t valid = 0;  // bit j: row rw0 + j has a neighbour for the current offset
+      auto spread = [&](int cur) {
+        valid = __ballot_sync(0xffffffffu, cur >= 0);
+#pragma unroll
+        for (int k = 0; k < RPT; ++k) src[k] = __shfl_sync(0xffffffffu, cur, lane / CPR + RSTEP * k);
+      };
+      spread(fetch(v));
+      int nxt = MODE == kOutputStationary ? fetch(next_present(m, v, V)) : -1;
       int pnl = 0;
       for (int kb = 0; kb < nkb; kb += G, ++it) {
         const int s = static_cast<int>(it % S);
         const uint32_t ph = (it / S) & 1u;
-        if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, s_abort)) {
+        if (!__all_sync(0xffffffffu, mbar_wait(empty0 + 8 * s, ph ^ 1u, s_abort))) {
           *s_abort = 1;
           break;
         }
         const int gc = min(G, nkb - kb);
-        if (pt == 0) mbar_arrive_expect_tx(full0 + 8 * s, static_cast<uint32_t>(gc * B_SUB));
-        int bv = v, bp = pnl;  // the W slices follow the same (offset, panel) sequence
         for (int g = 0; g < gc; ++g) {
-          if (pt == 0) {
+          const uint32_t a_base = smem_u32(sA + (s * G + g) * A_SUB + part_off);
+          const uint32_t was = dirty[s * G + g];
+#pragma unroll
+          for (int k = 0; k < RPT; ++k) {
+            const int rl = lane / CPR + RSTEP * k;
+            const int r = rp0 + rl;  // row within the part
+            const int j = src[k];
+            if (((valid | was) >> rl) & 1u) {
+              const uint8_t* g_src = p.feats + (static_cast<size_t>(j < 0 ? 0 : j) * p.c_in +
+                                                static_cast<size_t>(pnl) * BK) * 2 + chunk * 16;
+              cp_async_16(a_base + r * ROWB + ((chunk ^ swz<BK>(r)) << 4), g_src, j >= 0 ? 16u : 0u);
+            }
+          }
+          __syncwarp();
+          if (lane == 0) dirty[s * G + g] = valid;
+          if (++pnl == P) {
+            pnl = 0;
+            if (MODE == kOutputStationary) {
+              v = next_present(m, v, V);
+              if (v < V) {
+                spread(nxt);
+                nxt = fetch(next_present(m, v, V));
+              }
+            }
+          }
+        }
+        // every thread's arrival fires once its copies of this stage landed
+        cp_async_arrive_noinc(full0 + 8 * s);
+      }
+    }
+    cp_async_wait_all();
+  } else if (warp == NPW + 5) {
+    // ======================================================= weight loader
+    // One thread walks the producers' (unit, offset, panel) sequence and
+    // bulk-copies the matching W slices into each stage, arming the stage's
+    // barrier with their byte count; it also prefetches each next unit's block
+    // of the neighbour table into L2.
+    if (lane == 0) {
+      uint32_t it = 0;
+      if (MODE == kOutputStationary && static_cast<int>(blockIdx.x) < p.num_units) {
+        const TileInfo t0 = tile_info<MODE, T>(p, blockIdx.x);
+        const uint32_t bytes = (static_cast<uint32_t>(t0.nrows) * V * 4) & ~15u;
+        if (bytes) bulk_prefetch_l2(p.nbr + t0.row0 * V, bytes);
+      }
+      for (int u = blockIdx.x; u < p.num_units && !*s_abort; u += gridDim.x) {
+        uint4 m = make_uint4(0, 0, 0, 0);
+        int bv = tile_info<MODE, T>(p, u).v;
+        if (MODE == kOutputStationary) {
+          m = unit_mask<T>(p, u);
+          bv = next_present(m, -1, V);
+          const int nu = u + gridDim.x;
+          if (nu < p.num_units) {
+            const TileInfo tn = tile_info<MODE, T>(p, nu);
+            const uint32_t bytes = (static_cast<uint32_t>(tn.nrows) * V * 4) & ~15u;
+            if (bytes) bulk_prefetch_l2(p.nbr + tn.row0 * V, bytes);
+          }
+        }
+        const int nkb = unit_kblocks<MODE, T>(p, u, P);
+        int bp = 0;
+        for (int kb = 0; kb < nkb; kb += G, ++it) {
+          const int s = static_cast<int>(it % S);
+          const uint32_t ph = (it / S) & 1u;
+          if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, s_abort)) {
+            *s_abort = 1;
+            break;
+          }
+          const int gc = min(G, nkb - kb);
+          mbar_arrive_expect_tx(full0 + 8 * s, static_cast<uint32_t>(gc * B_SUB));
+          for (int g = 0; g < gc; ++g) {
             bulk_g2s(smem_u32(sB + (s * G + g) * B_SUB), p.wimg + (static_cast<size_t>(bv) * P + bp) * B_SUB,
                      static_cast<uint32_t>(B_SUB), full0 + 8 * s);
             if (++bp == P) {
@@ -423,59 +520,36 @@ __global__ void __launch_bounds__(kThreads) k_conv_tc(const TcParams p) {
               if (MODE == kOutputStationary) bv = next_present(m, bv, V);
             }
           }
-          const uint32_t a_base = smem_u32(sA + (s * G + g) * A_SUB);
-#pragma unroll
-          for (int k = 0; k < RPT; ++k) {
-            const int r = rbase + RSTEP * k;
-            const int j = src[k];
-            const uint8_t* g_src = p.feats + (static_cast<size_t>(j < 0 ? 0 : j) * p.c_in +
-                                              static_cast<size_t>(pnl) * BK) * 2 + chunk * 16;
-            cp_async_16(a_base + r * ROWB + ((chunk ^ swz<BK>(r)) << 4), g_src, j >= 0 ? 16u : 0u);
-          }
-          if (++pnl == P) {
-            pnl = 0;
-            if (MODE == kOutputStationary) {
-              v = next_present(m, v, V);
-              if (v < V) load_rows(v);
-            }
-          }
-        }
-        cp_async_commit();
-        if (it >= static_cast<uint32_t>(lag)) {
-          cp_async_wait_dyn(lag);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(full0 + 8 * ((it - lag) % S));
         }
       }
-    }
-    // signal the stages still owed, once their copies have landed
-    cp_async_wait_dyn(0);
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0)
-      for (uint32_t k = it > static_cast<uint32_t>(lag) ? it - lag : 0; k < it; ++k) mbar_arrive(full0 + 8 * (k % S));
-    // the weight bulk copies of the last stages have landed before the CTA may exit
-    if (pt == 0) {
+      // the weight copies of the last stages have landed before the CTA may exit
       const uint32_t first = it > static_cast<uint32_t>(S) ? it - S : 0;
       for (uint32_t k = first; k < it; ++k)
         if (!mbar_drain(full0 + 8 * (k % S), (k / S) & 1u)) *s_abort = 1;
     }
-  } else if (warp == 4) {
+    __syncwarp();
+  } else if (warp == NPW) {
     // ======================================================= MMA issuer
     if (lane == 0) {
       const uint32_t idesc = make_idesc(BF16, kRows, p.c_out);
+      // descriptor halves: low = start address >> 4 (14 bits; shared memory
+      // is below 256 KB, so offsets add without carry) | LBO 1; high = SBO,
+      // version 1, swizzle layout
+      const uint64_t d0 = smem_desc(smem_u32(sA), SBO, LAYOUT);
+      const uint32_t desc_hi = static_cast<uint32_t>(d0 >> 32);
+      const uint32_t a_lo0 = static_cast<uint32_t>(d0);
+      const uint32_t b_lo0 = static_cast<uint32_t>(smem_desc(smem_u32(sB), SBO, LAYOUT));
       uint32_t it = 0;
       int j = 0;
-      for (int tile = blockIdx.x; tile < p.num_tiles && !*s_abort; tile += gridDim.x, ++j) {
-        const int nkb = tile_kblocks<MODE>(p, tile, P);
-        const int b = j & 1;
-        if (!mbar_wait(acce0 + 8 * b, ((j >> 1) & 1) ^ 1, s_abort)) {
+      for (int u = blockIdx.x; u < p.num_units && !*s_abort; u += gridDim.x, ++j) {
+        const int nkb = unit_kblocks<MODE, T>(p, u, P);
+        const int b = j % NB;
+        if (!mbar_wait(acce0 + 8 * b, ((j / NB) & 1) ^ 1, s_abort)) {
           *s_abort = 1;
           break;
         }
         tc_fence_after();
-        const uint32_t d = tmem + static_cast<uint32_t>(b * p.acc_cols);
+        const uint32_t d = tmem + static_cast<uint32_t>(b * T * p.acc_cols);
         uint32_t accumulate = 0;
         for (int kb = 0; kb < nkb; kb += G, ++it) {
           const int s = static_cast<int>(it % S);
@@ -484,21 +558,26 @@ __global__ void __launch_bounds__(kThreads) k_conv_tc(const TcParams p) {
             *s_abort = 1;
             break;
           }
+          // the producers' cp.async writes are generic-proxy writes: order
+          // them before the tensor core's (async-proxy) reads
+          fence_proxy_async_smem();
           tc_fence_after();
           const int gc = min(G, nkb - kb);
           for (int g = 0; g < gc; ++g) {
-            const uint32_t a_addr = smem_u32(sA + (s * G + g) * A_SUB);
-            const uint32_t b_addr = smem_u32(sB + (s * G + g) * B_SUB);
+            const uint32_t a_lo = a_lo0 + static_cast<uint32_t>(((s * G + g) * A_SUB) >> 4);
+            const uint32_t b_lo = b_lo0 + static_cast<uint32_t>(((s * G + g) * B_SUB) >> 4);
 #pragma unroll
             for (int k = 0; k < BK / 16; ++k) {
-              tc_mma(d, smem_desc(a_addr + 32 * k, SBO, LAYOUT), smem_desc(b_addr + 32 * k, SBO, LAYOUT), idesc,
-                     accumulate);
+#pragma unroll
+              for (int tp = 0; tp < T; ++tp)
+                tc_mma_lohi(d + static_cast<uint32_t>(tp * p.acc_cols), a_lo + tp * (A_PART >> 4) + 2 * k,
+                            b_lo + 2 * k, desc_hi, idesc, accumulate);
               accumulate = 1;
             }
           }
           tc_commit(empty0 + 8 * s);
         }
-        tc_commit(accf0 + 8 * b);  // arrives once every MMA of the tile has completed
+        tc_commit(accf0 + 8 * b);  // arrives once every MMA of the unit has completed
       }
       // all tcgen05 work of this thread has completed before TMEM is released
       tc_commit(done_bar);
@@ -506,55 +585,59 @@ __global__ void __launch_bounds__(kThreads) k_conv_tc(const TcParams p) {
     }
     __syncwarp();
   } else {
-    // ======================================================= epilogue
+    // ======================================================= epilogue (warps NPW+1 .. NPW+4)
     const int q = warp & 3;             // TMEM lane quadrant of this warp
-    const int r = q * 32 + lane;        // tile row held by this thread
     int j = 0;
-    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++j) {
-      const TileInfo t = tile_info<MODE>(p, tile);
-      const int b = j & 1;
-      if (*s_abort || !mbar_wait(accf0 + 8 * b, (j >> 1) & 1, s_abort)) {
+    for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++j) {
+      const TileInfo t = tile_info<MODE, T>(p, u);
+      const int b = j % NB;
+      if (*s_abort || !mbar_wait(accf0 + 8 * b, (j / NB) & 1, s_abort)) {
         *s_abort = 1;
         break;
       }
       tc_fence_after();
-      const uint32_t trow = tmem + static_cast<uint32_t>(b * p.acc_cols) + (static_cast<uint32_t>(q * 32) << 16);
-      int dst_row = -1;
-      if (r < t.nrows) {
-        if (MODE == kWsScatter) dst_row = __ldg(p.out_rows + t.lb + r);
-        else if (MODE == kOutputStationary && p.order) dst_row = __ldg(p.order + t.row0 + r);
-        else dst_row = static_cast<int>(t.row0 + r);
-      }
-      for (int c0 = 0; c0 < p.c_out; c0 += 16) {
-        float a[16];
-        tmem_ld16(trow + static_cast<uint32_t>(c0), a);
-        if (dst_row < 0) continue;
-        if (MODE == kOutputStationary) {
-          if (p.relu) {
+#pragma unroll 1
+      for (int tp = 0; tp < T; ++tp) {
+        const int r = tp * kRows + q * 32 + lane;  // unit row held by this thread
+        const uint32_t trow = tmem + static_cast<uint32_t>((b * T + tp) * p.acc_cols) +
+                              (static_cast<uint32_t>(q * 32) << 16);
+        int dst_row = -1;
+        if (r < t.nrows) {
+          if (MODE == kWsScatter) dst_row = __ldg(p.out_rows + t.lb + r);
+          else if (MODE == kOutputStationary && p.order) dst_row = __ldg(p.order + t.row0 + r);
+          else dst_row = static_cast<int>(t.row0 + r);
+        }
+        for (int c0 = 0; c0 < p.c_out; c0 += 16) {
+          float a[16];
+          tmem_ld16(trow + static_cast<uint32_t>(c0), a);
+          if (dst_row < 0) continue;
+          if (MODE == kOutputStationary) {
+            if (p.relu) {
 #pragma unroll
-            for (int k = 0; k < 16; ++k) a[k] = fmaxf(a[k], 0.0f);
+              for (int k = 0; k < 16; ++k) a[k] = fmaxf(a[k], 0.0f);
+            }
+            uint4 lo, hi;
+            lo.x = pack2<BF16>(a[0], a[1]);
+            lo.y = pack2<BF16>(a[2], a[3]);
+            lo.z = pack2<BF16>(a[4], a[5]);
+            lo.w = pack2<BF16>(a[6], a[7]);
+            hi.x = pack2<BF16>(a[8], a[9]);
+            hi.y = pack2<BF16>(a[10], a[11]);
+            hi.z = pack2<BF16>(a[12], a[13]);
+            hi.w = pack2<BF16>(a[14], a[15]);
+            uint4* dst = reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(dst_row) * p.c_out + c0) * 2);
+            dst[0] = lo;
+            dst[1] = hi;
+          } else if (MODE == kWsScatter) {
+            float4* dst = reinterpret_cast<float4*>(p.acc + static_cast<int64_t>(dst_row) * p.c_out + c0);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              atomicAdd(dst + k, make_float4(a[4 * k], a[4 * k + 1], a[4 * k + 2], a[4 * k + 3]));
+          } else {
+            float4* dst = reinterpret_cast<float4*>(p.acc + static_cast<int64_t>(dst_row) * p.c_out + c0);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) dst[k] = make_float4(a[4 * k], a[4 * k + 1], a[4 * k + 2], a[4 * k + 3]);
           }
-          uint4 lo, hi;
-          lo.x = pack2<BF16>(a[0], a[1]);
-          lo.y = pack2<BF16>(a[2], a[3]);
-          lo.z = pack2<BF16>(a[4], a[5]);
-          lo.w = pack2<BF16>(a[6], a[7]);
-          hi.x = pack2<BF16>(a[8], a[9]);
-          hi.y = pack2<BF16>(a[10], a[11]);
-          hi.z = pack2<BF16>(a[12], a[13]);
-          hi.w = pack2<BF16>(a[14], a[15]);
-          uint4* dst = reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(dst_row) * p.c_out + c0) * 2);
-          dst[0] = lo;
-          dst[1] = hi;
-        } else if (MODE == kWsScatter) {
-          float4* dst = reinterpret_cast<float4*>(p.acc + static_cast<int64_t>(dst_row) * p.c_out + c0);
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            atomicAdd(dst + k, make_float4(a[4 * k], a[4 * k + 1], a[4 * k + 2], a[4 * k + 3]));
-        } else {
-          float4* dst = reinterpret_cast<float4*>(p.acc + static_cast<int64_t>(dst_row) * p.c_out + c0);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) dst[k] = make_float4(a[4 * k], a[4 * k + 1], a[4 * k + 2], a[4 * k + 3]);
         }
       }
       tc_fence_before();
@@ -565,7 +648,7 @@ __global__ void __launch_bounds__(kThreads) k_conv_tc(const TcParams p) {
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 4) {
+  if (warp == NPW) {
     tc_fence_after();
     tmem_dealloc(tmem, static_cast<uint32_t>(p.tmem_cols));
   }
@@ -622,11 +705,13 @@ __global__ void __launch_bounds__(256) k_cast_out(const float4* __restrict__ acc
 
 // ------------------------------------------------------------ host side --
 struct Plan {
-  int bk;
-  int group;
+  int bk;           // channels per K panel (16, 32 or 64)
+  int group;        // (offset, panel) sub-blocks per pipeline stage
   int stages;
-  int lag;
-  int ctas_per_sm;
+  int npw;          // producer warps per CTA (4, 8 or 16)
+  int t;            // 128-row tiles per output-stationary work unit (1 or 2)
+  int nbuf;         // accumulator buffers
+  int ctas_per_sm;  // as shared memory, TMEM and threads allow
   size_t smem;
   int acc_cols;
   int tmem_cols;
@@ -634,59 +719,135 @@ struct Plan {
 
 int pick_bk(int c_in) { return c_in % 64 == 0 ? 64 : (c_in % 32 == 0 ? 32 : 16); }
 
-// Pipeline shape.  Gathers are latency bound, and measured throughput grows
-// with the number of producer warps per SM, not with pipeline depth, so the
-// plan keeps three stages (one cp.async group in flight per producer thread
-// beyond the one being filled) and fits as many CTAs per SM as shared memory
-// (about 220 KB) and TMEM (512 columns, two accumulators per CTA) allow.
-bool make_plan(int c_in, int c_out, Plan* pl) {
+size_t plan_smem(const Plan& pl, size_t stage_bytes) {  // stage_bytes: one stage's A and B
+  return 1024 /*alignment slack*/ + 8 * kBarriers + 16 + static_cast<size_t>(pl.npw) * pl.stages * pl.group * 4 +
+         pl.stages * stage_bytes;
+}
+
+// Pipeline shape.  The gathers are bound by how many cp.async instructions
+// the SM's warps keep issuing: one warp sustains about 3 B/clk of 128-byte
+// rows whatever its depth, and the SM's rate grows with its producer warps
+// (measured up to about 13 TB/s per GPU).  Per stage the tensor core reads
+// A (gathered rows) and B (a weight slice); B is re-read for every unit, so
+// at C_out = 256 two tiles share it.  The plan keeps three stages, fits as
+// many CTAs per SM as shared memory (about 220 KB) and TMEM (512 columns)
+// allow, and gives each CTA 4 producer warps at three CTAs per SM, else 8.
+// Developer overrides for measurement sweeps (environment, read per call):
+// SC_DEV_BK, SC_DEV_T, SC_DEV_STAGES, SC_DEV_GROUP, SC_DEV_NPW, SC_DEV_CPS
+// (an upper bound), SC_DEV_FORCECPS (launch that many CTAs per SM) and
+// SC_DEV_VERBOSE (print each launch's plan).  None changes the result.
+bool make_plan(int c_in, int c_out, bool output_stationary, Plan* pl) {
   pl->bk = pick_bk(c_in);
-  const size_t a = static_cast<size_t>(kRows) * pl->bk * 2;
+  if (const char* e = getenv("SC_DEV_BK")) { const int bk = atoi(e); if ((bk == 16 || bk == 32 || bk == 64) && c_in % bk == 0) pl->bk = bk; }
+  int cols = 32;
+  while (cols < c_out) cols <<= 1;
+  pl->acc_cols = cols;
+  // At C_out = 256 a stage moves twice as many weight bytes as feature
+  // bytes; two tiles per unit share each weight slice (measured: a third
+  // less time at 128->256 and 256->256; no gain at C_out = 128, where two
+  // CTAs per SM with one tile each do better).
+  pl->t = (output_stationary && pl->bk == 64 && c_out >= 256) ? 2 : 1;
+  if (const char* e = getenv("SC_DEV_T")) pl->t = (atoi(e) == 2 && output_stationary && pl->bk >= 32) ? 2 : 1;
+  pl->nbuf = 2 * pl->t * cols <= 512 ? 2 : 1;
+  pl->tmem_cols = pl->nbuf * pl->t * cols;
+  if (pl->tmem_cols > 512) return false;
+  const size_t a = static_cast<size_t>(kRows) * pl->bk * 2 * pl->t;
   const size_t b = static_cast<size_t>(c_out) * pl->bk * 2;
   // sub-blocks per stage: stages of about 24 KB
   int g = static_cast<int>((24 * 1024) / (a + b));
   if (g < 1) g = 1;
   if (g > 4) g = 4;
   pl->group = g;
-  const size_t stage = g * (a + b);
-  const size_t fixed = 1024 /*alignment slack*/ + 8 * kBarriers + 16;
   pl->stages = 3;
-  pl->lag = 1;
-  pl->smem = fixed + pl->stages * stage;
+  if (const char* e = getenv("SC_DEV_STAGES")) pl->stages = atoi(e);
+  if (const char* e = getenv("SC_DEV_GROUP")) pl->group = atoi(e);
+  pl->stages = pl->stages < 2 ? 2 : (pl->stages > kMaxStages ? kMaxStages : pl->stages);
+  pl->group = pl->group < 1 ? 1 : (pl->group > 4 ? 4 : pl->group);
+  const size_t stage = pl->group * (a + b);
+  // a warp instruction covers whole rows, and a warp's rows lie in one tile
+  const int rstep = 32 / (pl->bk * 2 / 16);
+  const int max_npw = kRows * pl->t / rstep < 16 ? kRows * pl->t / rstep : 16;
+  const int min_npw = pl->t == 2 ? 8 : 4;
+  pl->npw = min_npw;
+  pl->smem = plan_smem(*pl, stage);
   if (pl->smem > 220 * 1024) return false;
-  int cols = 32;
-  while (cols < c_out) cols <<= 1;
-  pl->acc_cols = cols;
-  pl->tmem_cols = 2 * cols;
   int cps = static_cast<int>((220 * 1024) / pl->smem);
   if (cps * pl->tmem_cols > 512) cps = 512 / pl->tmem_cols;
-  if (cps * kThreads > 2048) cps = 2048 / kThreads;
+  if (cps < 1) cps = 1;
+  pl->npw = cps >= 3 ? 4 : 8;  // measured: 16 producer warps were never faster than 8
+  if (const char* e = getenv("SC_DEV_NPW")) pl->npw = atoi(e);
+  if (pl->npw != 4 && pl->npw != 8 && pl->npw != 16) pl->npw = 4;
+  if (pl->npw > max_npw) pl->npw = max_npw;
+  if (pl->npw < min_npw) pl->npw = min_npw;
+  pl->smem = plan_smem(*pl, stage);
+  if (pl->smem > 220 * 1024) return false;
+  cps = static_cast<int>((220 * 1024) / pl->smem);
+  if (cps * pl->tmem_cols > 512) cps = 512 / pl->tmem_cols;
+  const int threads = (pl->npw + 6) * 32;
+  if (cps * threads > 2048) cps = 2048 / threads;
+  if (const char* e = getenv("SC_DEV_CPS")) { int c = atoi(e); if (c < cps) cps = c; }
   pl->ctas_per_sm = cps < 1 ? 1 : cps;
   return true;
 }
 
-template <int BK, int MODE, bool BF16>
+template <int BK, int MODE, bool BF16, int NPW, int T>
 sc_status launch_tc(const TcParams& prm, const Plan& pl, cudaStream_t s, const char* name) {
-  auto kern = k_conv_tc<BK, MODE, BF16>;
+  auto kern = k_conv_tc<BK, MODE, BF16, NPW, T>;
+  constexpr int threads = (NPW + 6) * 32;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(pl.smem));
   if (e != cudaSuccess) return set_cuda_error(e, "conv smem attribute");
-  const int slots = device_sm_count() * pl.ctas_per_sm;
-  const int grid = prm.num_tiles < slots ? prm.num_tiles : slots;
-  SC_LAUNCH(name, s, kern<<<grid, kThreads, pl.smem, s>>>(prm));
+  // the kernel lives in shared memory: ask for the largest carveout (the
+  // occupancy query below also assumes it)
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return set_cuda_error(e, "conv carveout attribute");
+  // resident CTAs per SM: the plan's count, or fewer if registers say so
+  cudaFuncAttributes fa{};
+  e = cudaFuncGetAttributes(&fa, kern);
+  if (e != cudaSuccess) return set_cuda_error(e, "conv attribute query");
+  const int regs_cta = ((fa.numRegs + 7) / 8) * 8 * threads;
+  const int fit = regs_cta > 0 ? 65536 / regs_cta : pl.ctas_per_sm;
+  int cps = fit < pl.ctas_per_sm ? (fit < 1 ? 1 : fit) : pl.ctas_per_sm;
+  if (const char* ev = getenv("SC_DEV_FORCECPS")) cps = atoi(ev);
+  const int slots = device_sm_count() * cps;
+  const int grid = prm.num_units < slots ? prm.num_units : slots;
+  if (getenv("SC_DEV_VERBOSE")) {
+    fprintf(stderr, "%s: bk %d npw %d t %d nbuf %d group %d stages %d smem %zu plan cps %d fit %d grid %d regs %d\n",
+            name, BK, NPW, T, pl.nbuf, pl.group, pl.stages, pl.smem, pl.ctas_per_sm, fit, grid, fa.numRegs);
+  }
+  SC_LAUNCH(name, s, kern<<<grid, threads, pl.smem, s>>>(prm));
   e = cudaGetLastError();
   return e == cudaSuccess ? SC_OK : set_cuda_error(e, name);
 }
 
+template <int BK, int MODE, bool BF16>
+sc_status launch_npw(const TcParams& prm, const Plan& pl, cudaStream_t s, const char* name) {
+  if constexpr (BK == 16) {
+    return pl.npw == 8 ? launch_tc<BK, MODE, BF16, 8, 1>(prm, pl, s, name)
+                       : launch_tc<BK, MODE, BF16, 4, 1>(prm, pl, s, name);
+  } else {
+    if constexpr (MODE == kOutputStationary) {
+      if (pl.t == 2)
+        return pl.npw == 16 ? launch_tc<BK, MODE, BF16, 16, 2>(prm, pl, s, name)
+                            : launch_tc<BK, MODE, BF16, 8, 2>(prm, pl, s, name);
+    }
+    switch (pl.npw) {
+      case 16: return launch_tc<BK, MODE, BF16, 16, 1>(prm, pl, s, name);
+      case 8: return launch_tc<BK, MODE, BF16, 8, 1>(prm, pl, s, name);
+      default: return launch_tc<BK, MODE, BF16, 4, 1>(prm, pl, s, name);
+    }
+  }
+}
+
 template <int MODE>
 sc_status dispatch_tc(const TcParams& prm, const Plan& pl, bool bf16, cudaStream_t s, const char* name) {
-  if (prm.num_tiles <= 0) return SC_OK;
+  if (prm.num_units <= 0) return SC_OK;
   switch (pl.bk) {
     case 64:
-      return bf16 ? launch_tc<64, MODE, true>(prm, pl, s, name) : launch_tc<64, MODE, false>(prm, pl, s, name);
+      return bf16 ? launch_npw<64, MODE, true>(prm, pl, s, name) : launch_npw<64, MODE, false>(prm, pl, s, name);
     case 32:
-      return bf16 ? launch_tc<32, MODE, true>(prm, pl, s, name) : launch_tc<32, MODE, false>(prm, pl, s, name);
+      return bf16 ? launch_npw<32, MODE, true>(prm, pl, s, name) : launch_npw<32, MODE, false>(prm, pl, s, name);
     default:
-      return bf16 ? launch_tc<16, MODE, true>(prm, pl, s, name) : launch_tc<16, MODE, false>(prm, pl, s, name);
+      return bf16 ? launch_npw<16, MODE, true>(prm, pl, s, name) : launch_npw<16, MODE, false>(prm, pl, s, name);
   }
 }
 
@@ -720,21 +881,22 @@ TcParams base_params(const ConvArgs& a, const Plan& pl, const uint8_t* img) {
   p.ws_tiles = a.m->ws_tiles;
   p.n = a.m->n;
   p.num_tiles = static_cast<int>((a.m->n + kRows - 1) / kRows);
+  p.num_units = (p.num_tiles + pl.t - 1) / pl.t;
   p.V = a.m->V;
   p.c_in = a.c_in;
   p.c_out = a.c_out;
   p.relu = a.relu ? 1 : 0;
   p.stages = pl.stages;
   p.group = pl.group;
-  p.lag = pl.lag;
   p.acc_cols = pl.acc_cols;
   p.tmem_cols = pl.tmem_cols;
+  p.nbuf = pl.nbuf;
   p.status = a.m->status;
   return p;
 }
 
 bool fused_ok(const ConvArgs& a, Plan* pl) {
-  return a.dtype != SC_F32 && a.m->V <= 128 && make_plan(a.c_in, a.c_out, pl);
+  return a.dtype != SC_F32 && a.m->V <= 128 && make_plan(a.c_in, a.c_out, true, pl);
 }
 
 // The output-stationary launch on an already packed weight image.
@@ -767,7 +929,7 @@ sc_status conv_fused(const ConvArgs& a) {
 
 sc_status conv_weight_stationary(const ConvArgs& a) {
   Plan pl;
-  if (a.dtype == SC_F32 || !make_plan(a.c_in, a.c_out, &pl))
+  if (a.dtype == SC_F32 || !make_plan(a.c_in, a.c_out, false, &pl))
     return set_error(SC_ERR_UNSUPPORTED, "weight-stationary kernel: f16/bf16 only");
   if (a.m->n == 0) return SC_OK;
   if (!a.m->host_valid) return set_error(SC_ERR_INVALID_ARG, "weight-stationary kernel needs the map's host counts");
@@ -789,6 +951,7 @@ sc_status conv_weight_stationary(const ConvArgs& a) {
   if (!st) st = dispatch_tc<kWsCentre>(prm, pl, bf16, a.stream, "subm_conv_ws_centre");
   if (!st) {
     prm.num_tiles = a.m->ws_tiles_host[a.m->V];
+    prm.num_units = prm.num_tiles;
     st = dispatch_tc<kWsScatter>(prm, pl, bf16, a.stream, "subm_conv_ws_scatter");
   }
   if (!st) {
