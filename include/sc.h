@@ -140,9 +140,10 @@ sc_status sc_hash_destroy(sc_hash h, sc_stream stream);
  *            coords[q] + d, or -1.  Column (V-1)/2 is the identity.
  *   offs     int64 [V+1]: per-offset segments of the (in, out) lists.  The
  *            centre segment is empty: its tuples are (i, i) for every i.
- *   in/out   int32 [offs[V]]: list entries (p, q); within a segment the
- *            entries follow the row order (input order, or the locality
- *            order), which is not part of the result.
+ *   in/out   int32 [offs[V]]: list entries (p, q).  The order of the
+ *            entries inside a segment is not part of the result and may
+ *            differ between builds (runs of up to 128 consecutive rows stay
+ *            together, in row order).
  *   map size |M| = n + offs[V] tuples, centre included.
  *
  * Without SC_KMAP_NO_SYNC the call synchronises the stream once and returns
@@ -257,6 +258,11 @@ int64_t sc_launch_count(void);
  * `index` (0-based; returns SC_ERR_INVALID_ARG past the end).
  */
 void sc_profile_enable(int on);
+/* Restrict the bracketing to kernels whose profile name starts with
+ * `name_prefix` (for example "subm_conv"), so that timing one kernel adds no
+ * events around the others.  NULL or "" restores all kernels.  The string is
+ * copied. */
+void sc_profile_only(const char* name_prefix);
 sc_status sc_profile_collect(void);
 void sc_profile_reset(void);
 sc_status sc_profile_get(int index, const char** name, int64_t* launches, double* total_ms);

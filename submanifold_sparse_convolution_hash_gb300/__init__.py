@@ -11,6 +11,7 @@ from .binding import (  # noqa: F401
     lib,
     profile_collect,
     profile_enable,
+    profile_only,
     profile_reset,
     sc_hash_build,
     sc_kmap_build,

@@ -67,6 +67,7 @@ def lib():
             "sc_last_error": ([], ctypes.c_char_p),
             "sc_launch_count": ([], I64),
             "sc_profile_enable": ([I32], None),
+            "sc_profile_only": ([ctypes.c_char_p], None),
             "sc_profile_collect": ([], I32),
             "sc_profile_reset": ([], None),
             "sc_profile_get": ([I32, P, P, P], I32),
@@ -268,6 +269,11 @@ def launch_count() -> int:
 
 def profile_enable(on: bool = True):
     lib().sc_profile_enable(1 if on else 0)
+
+
+def profile_only(name_prefix: str | None = None):
+    """Time only kernels whose profile name starts with `name_prefix`."""
+    lib().sc_profile_only(name_prefix.encode() if name_prefix else None)
 
 
 def profile_reset():

@@ -15,9 +15,11 @@
 // The opaque handle types of sc.h.
 struct sc_hash_s {
   sc::HashTable t;
+  void* arena = nullptr;  // one device allocation: table, keys, status
 };
 struct sc_kmap_s {
   sc::KernelMap k;
+  void* arena = nullptr;  // one device allocation holding every buffer of k
 };
 
 namespace sc {
@@ -50,6 +52,7 @@ struct Pending {
 struct Profiler {
   std::mutex mu;
   bool on = false;
+  std::string only;  // bracket only kernels whose name starts with this ("" = all)
   std::vector<std::string> names;
   std::vector<int64_t> launches;
   std::vector<double> ms;
@@ -77,6 +80,7 @@ int prof_begin(const char* name, cudaStream_t s) {
   Profiler& P = prof();
   if (!P.on) return -1;
   std::lock_guard<std::mutex> lk(P.mu);
+  if (!P.only.empty() && std::strncmp(name, P.only.c_str(), P.only.size()) != 0) return -1;
   int id = -1;
   for (size_t i = 0; i < P.names.size(); ++i)
     if (P.names[i] == name) id = static_cast<int>(i);
@@ -267,6 +271,12 @@ int64_t sc_launch_count(void) { return g_launches.load(); }
 
 void sc_profile_enable(int on) { prof().on = on != 0; }
 
+void sc_profile_only(const char* name_prefix) {
+  Profiler& P = prof();
+  std::lock_guard<std::mutex> lk(P.mu);
+  P.only = name_prefix ? name_prefix : "";
+}
+
 sc_status sc_profile_collect(void) {
   Profiler& P = prof();
   std::lock_guard<std::mutex> lk(P.mu);
@@ -325,9 +335,15 @@ sc_status sc_hash_build(const int32_t* d_coords, int64_t n, sc_stream stream, sc
   const int64_t want = 2 * n * static_cast<int64_t>(sizeof(BlockEntry)) <= (int64_t(256) << 20) ? 2 * n : n;
   while (cap < want) cap <<= 1;
   t.capacity = cap;
-  sc_status st = dev_alloc(reinterpret_cast<void**>(&t.table), sizeof(BlockEntry) * cap, s);
-  if (!st) st = dev_alloc(reinterpret_cast<void**>(&t.keys), sizeof(unsigned long long) * (n > 0 ? n : 1), s);
-  if (!st) st = dev_alloc(reinterpret_cast<void**>(&t.status), sizeof(int) * 4, s);
+  const size_t tb = sizeof(BlockEntry) * static_cast<size_t>(cap);
+  const size_t kb = (sizeof(unsigned long long) * static_cast<size_t>(n > 0 ? n : 1) + 255) & ~size_t(255);
+  sc_status st = dev_alloc(&h->arena, tb + kb + 256, s);
+  if (!st) {
+    uint8_t* b = static_cast<uint8_t*>(h->arena);
+    t.table = reinterpret_cast<BlockEntry*>(b);
+    t.keys = reinterpret_cast<unsigned long long*>(b + tb);
+    t.status = reinterpret_cast<int*>(b + tb + kb);
+  }
   if (!st) st = launch_hash_insert(d_coords, n, &t, s);
   if (st) {
     sc_hash_destroy(h, stream);
@@ -366,9 +382,7 @@ sc_status sc_hash_check(sc_hash h, sc_stream stream) {
 sc_status sc_hash_destroy(sc_hash h, sc_stream stream) {
   if (!h) return SC_OK;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  dev_free(h->t.table, s);
-  dev_free(h->t.keys, s);
-  dev_free(h->t.status, s);
+  dev_free(h->arena, s);
   delete h;
   return SC_OK;
 }
@@ -377,11 +391,7 @@ sc_status sc_hash_destroy(sc_hash h, sc_stream stream) {
 sc_status sc_kmap_destroy(sc_kmap m, sc_stream stream) {
   if (!m) return SC_OK;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  KernelMap& k = m->k;
-  for (void* p : {static_cast<void*>(k.order), static_cast<void*>(k.buckets), static_cast<void*>(k.nbr), static_cast<void*>(k.offs), static_cast<void*>(k.in_rows),
-                  static_cast<void*>(k.out_rows), static_cast<void*>(k.masks), static_cast<void*>(k.present), static_cast<void*>(k.bases), static_cast<void*>(k.totals),
-                  static_cast<void*>(k.ws_tiles), static_cast<void*>(k.map_size), static_cast<void*>(k.status)})
-    dev_free(p, s);
+  dev_free(m->arena, s);
   delete m;
   return SC_OK;
 }
@@ -416,26 +426,37 @@ sc_status sc_kmap_build(sc_hash h, int ndim, int K, const int32_t dims[3], unsig
   k.K = K;
   k.V = V;
   for (int a = 0; a < 3; ++a) k.dims[a] = dims[a];
-  const int tile = kmap_probe_tile();
-  k.ntiles = static_cast<int>((k.n + tile - 1) / tile);
-  const size_t nV = static_cast<size_t>(k.n) * V;
-  const size_t lists = static_cast<size_t>(k.n) * (V - 1);
-  sc_status st = dev_alloc(reinterpret_cast<void**>(&k.nbr), sizeof(int) * nV, s);
+  k.up = kmap_unit_points(V);
+  k.nunits = static_cast<int>((k.n + k.up - 1) / k.up);
   const bool ordered = (flags & SC_KMAP_ORDER) || (!(flags & SC_KMAP_NO_ORDER) && k.n >= kOrderMinPoints);
-  if (!st && ordered && k.n > 0) {
-    st = dev_alloc(reinterpret_cast<void**>(&k.order), sizeof(int) * static_cast<size_t>(k.n), s);
-    if (!st) st = dev_alloc(reinterpret_cast<void**>(&k.buckets), sizeof(int) * kmap_order_buckets(), s);
+  // every buffer of the map carved from one allocation, each 256-byte aligned
+  const size_t n = static_cast<size_t>(k.n);
+  struct Part {
+    void** dst;
+    size_t bytes;
+  } parts[] = {
+      {reinterpret_cast<void**>(&k.nbr), sizeof(int) * n * V},
+      {reinterpret_cast<void**>(&k.in_rows), sizeof(int) * n * V},
+      {reinterpret_cast<void**>(&k.out_rows), sizeof(int) * n * V},
+      {reinterpret_cast<void**>(&k.cursors), sizeof(int) * V},
+      {reinterpret_cast<void**>(&k.present), sizeof(unsigned) * 4 * ((n + 127) / 128)},
+      {reinterpret_cast<void**>(&k.offs), sizeof(int64_t) * (V + 1)},
+      {reinterpret_cast<void**>(&k.ws_tiles), sizeof(int) * (V + 1)},
+      {reinterpret_cast<void**>(&k.map_size), sizeof(int64_t)},
+      {reinterpret_cast<void**>(&k.status), sizeof(int) * 4},
+      {reinterpret_cast<void**>(&k.order), ordered && k.n > 0 ? sizeof(int) * n : 0},
+      {reinterpret_cast<void**>(&k.buckets), ordered && k.n > 0 ? sizeof(int) * kmap_order_buckets() : 0},
+  };
+  size_t total = 0;
+  for (const Part& pt : parts) total += (pt.bytes + 255) & ~size_t(255);
+  sc_status st = dev_alloc(&m->arena, total, s);
+  if (!st) {
+    uint8_t* base = static_cast<uint8_t*>(m->arena);
+    for (const Part& pt : parts) {
+      *pt.dst = pt.bytes ? base : nullptr;
+      base += (pt.bytes + 255) & ~size_t(255);
+    }
   }
-  if (!st) st = dev_alloc(reinterpret_cast<void**>(&k.offs), sizeof(int64_t) * (V + 1), s);
-  if (!st) st = dev_alloc(reinterpret_cast<void**>(&k.in_rows), sizeof(int) * lists, s);
-  if (!st) st = dev_alloc(reinterpret_cast<void**>(&k.out_rows), sizeof(int) * lists, s);
-  if (!st) st = dev_alloc(reinterpret_cast<void**>(&k.masks), sizeof(unsigned) * static_cast<size_t>(V) * k.ntiles, s);
-  if (!st) st = dev_alloc(reinterpret_cast<void**>(&k.bases), sizeof(int) * static_cast<size_t>(V) * k.ntiles, s);
-  if (!st) st = dev_alloc(reinterpret_cast<void**>(&k.present), sizeof(unsigned) * 4 * ((k.n + 127) / 128), s);
-  if (!st) st = dev_alloc(reinterpret_cast<void**>(&k.totals), sizeof(int) * V, s);
-  if (!st) st = dev_alloc(reinterpret_cast<void**>(&k.ws_tiles), sizeof(int) * (V + 1), s);
-  if (!st) st = dev_alloc(reinterpret_cast<void**>(&k.map_size), sizeof(int64_t), s);
-  if (!st) st = dev_alloc(reinterpret_cast<void**>(&k.status), sizeof(int) * 4, s);
   // status[1] carries the hash's latched insert status from here on
   if (!st) {
     cudaError_t e = cudaMemsetAsync(k.status, 0, sizeof(int) * 4, s);
@@ -495,10 +516,22 @@ sc_status sc_kmap_export(sc_kmap m, int32_t* nbr, int64_t* offs, int32_t* in_row
   }
   if (e == cudaSuccess && offs) e = cudaMemcpyAsync(offs, k.offs, sizeof(int64_t) * (k.V + 1), cudaMemcpyDefault, s);
   const int64_t L = k.host_valid ? k.offs_host[k.V] : 0;
-  if (e == cudaSuccess && in_rows && L) e = cudaMemcpyAsync(in_rows, k.in_rows, sizeof(int) * L, cudaMemcpyDefault, s);
-  if (e == cudaSuccess && out_rows && L)
-    e = cudaMemcpyAsync(out_rows, k.out_rows, sizeof(int) * L, cudaMemcpyDefault, s);
-  return e == cudaSuccess ? SC_OK : set_cuda_error(e, "kmap export");
+  if (e != cudaSuccess) return set_cuda_error(e, "kmap export");
+  // the lists are stored in strides of n per offset: compact them into CSR
+  for (int which = 0; which < 2 && L; ++which) {
+    int32_t* dst = which == 0 ? in_rows : out_rows;
+    if (!dst) continue;
+    int* tmp = nullptr;
+    sc_status st = dev_alloc(reinterpret_cast<void**>(&tmp), sizeof(int) * L, s);
+    if (!st) st = kmap_compact_lists(&k, which == 0 ? k.in_rows : k.out_rows, tmp, L, s);
+    if (!st) {
+      e = cudaMemcpyAsync(dst, tmp, sizeof(int) * L, cudaMemcpyDefault, s);
+      if (e != cudaSuccess) st = set_cuda_error(e, "kmap export");
+    }
+    dev_free(tmp, s);
+    if (st) return st;
+  }
+  return SC_OK;
 }
 
 // ----------------------------------------------------------- convolution --

@@ -229,7 +229,7 @@ struct TcParams {
   const int* nbr;            // [n, V]
   const int* order;          // [n] input row of each table row (null: identity); tiles are runs of table rows
   const uint4* present;      // [tiles]: 128-bit mask of the offsets present in each 128-row tile
-  const int* in_rows;        // weight-stationary lists
+  const int* in_rows;        // weight-stationary lists: offset v's at v * n
   const int* out_rows;
   const int64_t* offs;       // [V+1]
   const int* ws_tiles;       // [V+1]
@@ -303,8 +303,10 @@ __device__ __forceinline__ TileInfo tile_info(const TcParams& p, int u) {
       if (__ldg(p.ws_tiles + mid) <= u) lo = mid; else hi = mid;
     }
     t.v = lo;
-    const int64_t seg_end = __ldg(p.offs + lo + 1);
-    t.lb = __ldg(p.offs + lo) + static_cast<int64_t>(u - __ldg(p.ws_tiles + lo)) * kRows;
+    // offset lo's list starts at lo * n and holds offs[lo + 1] - offs[lo] entries
+    const int64_t seg = static_cast<int64_t>(lo) * p.n;
+    const int64_t seg_end = seg + (__ldg(p.offs + lo + 1) - __ldg(p.offs + lo));
+    t.lb = seg + static_cast<int64_t>(u - __ldg(p.ws_tiles + lo)) * kRows;
     t.nrows = static_cast<int>(min(static_cast<int64_t>(kRows), seg_end - t.lb));
   } else {
     t.row0 = static_cast<int64_t>(u) * kRows * T;

@@ -23,34 +23,38 @@
 // atomics give; no result depends on it.  Without the order, rows are taken
 // in input order.
 //
-// Points are taken in tiles of 32 positions of that order, and the neighbour
-// table is stored in that order too (row k belongs to input row order[k]), so
-// a tile's 32 x V block is contiguous.  Three kernels build the map:
-//   probe  one block per tile, lane = point in every warp: the warps split
-//          the 2x2x2 blocks that cover each point's neighbourhood (8 for a
-//          3x3x3 kernel, 27 for 5x5x5); one lookup returns a block's 8 rows,
-//          which are filed under their offsets in a shared-memory copy of the
-//          tile's block of the table; a ballot per offset gives the tile's
-//          hit bitmask; the block is written with coalesced 16-byte stores.
-//   scan   one block per offset: exclusive prefix of the masks' popcounts
-//          over tiles.  The last block to finish (a ticket counter) turns the
-//          per-offset totals into the segment offsets, the weight-stationary
-//          tile prefix and |M|.
-//   fill   each warp takes one (tile, offset) pair: lane p holds point p's
-//          neighbour, a ballot ranks the hits, and the (in, out) entries are
-//          written to consecutive positions of the offset's segment, which
-//          therefore follows the row order.
+// Points are taken in units of 128 positions of that order (32 when the
+// kernel has more than 128 offsets), and the neighbour table is stored in
+// that order too (row k belongs to input row order[k]), so a unit's
+// 128 x V block is contiguous.  One kernel builds the map, one block per
+// unit:
+//   * probe: the block's threads split the 2x2x2 blocks that cover each
+//     point's neighbourhood (8 for a 3x3x3 kernel, 27 for 5x5x5); one lookup
+//     returns a block's 8 rows, which are filed under their offsets in a
+//     shared-memory copy of the unit's block of the table;
+//   * count: a ballot per (offset, 32 points) gives the hits; one atomic
+//     per offset on that offset's cursor reserves the unit's run of entries;
+//   * emit: the (in, out) entries go to offset v's list at v * n + the
+//     reserved start + rank, so a unit's entries stay together in row order
+//     (the order of units inside a list is the order their atomics ran); the
+//     table block is written with 16-byte stores, and the unit's 128-bit mask
+//     of present offsets with it.
+// The last block to finish turns the per-offset totals into the segment
+// offsets, the weight-stationary tile prefix and |M|.  The lists live in
+// fixed strides of n entries per offset; the CSR that the boundary exports is
+// their compaction.
 
 #include "sc_internal.cuh"
 
 namespace sc {
 namespace {
 
-constexpr int kTile = 32;        // points per tile (one bitmask word)
-constexpr int kThreads = 256;    // threads per probe / fill block
+constexpr int kThreads = 256;    // threads per map-build block
+constexpr int kLookups = 2;      // hash lookups in flight per map-build thread
 constexpr int kWsRows = 128;     // rows per weight-stationary tile
-constexpr int kScanThreads = 512;  // >= the largest V (343)
-constexpr int kScanPer = 8;        // tiles per scan thread per chunk
+// shared memory of a build block: 128 points x V <= 128 (or 32 x V <= 343)
+// neighbour slots, the ballots and the per-offset bases
+constexpr int kBuildSmemMax = 4 * (128 * 128 + 128 * 4 + 128);
 constexpr int kBucketBits = 20;    // locality-order buckets
 constexpr int kBuckets = 1 << kBucketBits;
 constexpr int kBucketBlocks = 256;                   // blocks of the bucket scan
@@ -265,90 +269,6 @@ __global__ void __launch_bounds__(256) k_order_scatter(const unsigned long long*
 }
 
 
-__global__ void __launch_bounds__(kThreads) k_kmap_probe(
-    const unsigned long long* __restrict__ keys, const int* __restrict__ order, int64_t n,
-    const BlockEntry* __restrict__ table, uint32_t mask, int V, int K, int ndim, int dimx, int dimy, int dimz,
-    int* __restrict__ nbr, unsigned* __restrict__ masks, unsigned* __restrict__ present, int ntiles,
-    int* __restrict__ status) {
-  extern __shared__ int4 smem4[];
-  int* s_tile = reinterpret_cast<int*>(smem4);  // [32 * V] the tile's block of the table
-  __shared__ unsigned s_pres[4];
-  constexpr int kWarps = kThreads / 32;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r = (K - 1) / 2;
-  const int rz = ndim == 3 ? r : 0;
-  const int centre = (V - 1) / 2;
-  for (int e = threadIdx.x; e < kTile * V; e += kThreads) s_tile[e] = -1;
-  if (threadIdx.x < 4) s_pres[threadIdx.x] = 0u;
-  const int tile = blockIdx.x;
-  const int64_t i0 = static_cast<int64_t>(tile) * kTile;
-  const int np = static_cast<int>(min(static_cast<int64_t>(kTile), n - i0));
-  // lane = point of the tile (every warp holds the same 32 points)
-  const bool live = lane < np;
-  const int row = live ? (order ? __ldg(order + i0 + lane) : static_cast<int>(i0 + lane)) : 0;
-  const unsigned long long ck = live ? __ldg(keys + row) : kEmptyKey;
-  bool valid = ck != kEmptyKey;
-  const int x = static_cast<int>((ck >> 32) & 0xFFFF), y = static_cast<int>((ck >> 16) & 0xFFFF),
-            z = static_cast<int>(ck & 0xFFFF);
-  if (valid && (x >= dimx || y >= dimy || z >= dimz)) {
-    if (warp == 0) atomicOr(status, kDevErrRange);
-    valid = false;
-  }
-  const unsigned long long batch = ck & 0xFFFF000000000000ull;
-  // the blocks covering the neighbourhood [x-r, x+r] x [y-r, y+r] x [z-rz, z+rz]
-  const int xlo = max(x - r, 0) >> 1, xhi = min(x + r, dimx - 1) >> 1;
-  const int ylo = max(y - r, 0) >> 1, yhi = min(y + r, dimy - 1) >> 1;
-  const int zlo = max(z - rz, 0) >> 1, zhi = min(z + rz, dimz - 1) >> 1;
-  __syncthreads();
-  // warp w looks up block triples w, w + kWarps, ... and files each voxel of
-  // the block that lies in the neighbourhood under its offset
-  const int nb = r + 1, nbz = rz + 1;  // blocks per axis, at most
-  for (int t = warp; t < nb * nb * nbz; t += kWarps) {
-    const int bx = xlo + t / (nb * nbz), by = ylo + (t / nbz) % nb, bz = zlo + t % nbz;
-    if (valid && bx <= xhi && by <= yhi && bz <= zhi) {
-      int4 r0, r1;
-      if (lookup_block(table, mask, batch | pack_key(0, 2 * bx, 2 * by, 2 * bz), r0, r1)) {
-#pragma unroll
-        for (int l = 0; l < 8; ++l) {
-          const int dx = 2 * bx + (l >> 2) - x, dy = 2 * by + ((l >> 1) & 1) - y, dz = 2 * bz + (l & 1) - z;
-          if (dx >= -r && dx <= r && dy >= -r && dy <= r && dz >= -rz && dz <= rz) {
-            const int v = ndim == 3 ? ((dx + r) * K + (dy + r)) * K + (dz + r) : (dx + r) * K + (dy + r);
-            s_tile[lane * V + v] = pick(r0, r1, l);
-          }
-        }
-      }
-    }
-  }
-  __syncthreads();
-  // per-offset hit masks of the tile; offsets present in its 128-row group
-  for (int v = warp; v < V; v += kWarps) {
-    const unsigned b = __ballot_sync(0xffffffffu, v != centre && s_tile[lane * V + v] >= 0);
-    if (lane == 0) {
-      masks[static_cast<int64_t>(v) * ntiles + tile] = b;
-      if (b && v < 128) atomicOr(s_pres + (v >> 5), 1u << (v & 31));
-    }
-  }
-  __syncthreads();
-  // the tile's block of the table is contiguous: i0 * V * 4 bytes is a multiple of 128
-  int* dst = nbr + i0 * V;
-  const int items = np * V;
-  const int n4 = items >> 2;
-  for (int e = threadIdx.x; e < n4; e += kThreads) reinterpret_cast<int4*>(dst)[e] = reinterpret_cast<const int4*>(s_tile)[e];
-  for (int e = (n4 << 2) + threadIdx.x; e < items; e += kThreads) dst[e] = s_tile[e];
-  if (threadIdx.x < 4 && s_pres[threadIdx.x]) atomicOr(present + (tile >> 2) * 4 + threadIdx.x, s_pres[threadIdx.x]);
-}
-
-// Rows of the table in input order: dst[order[k], :] = nbr[k, :].
-__global__ void __launch_bounds__(256) k_unpermute_rows(const int* __restrict__ nbr, const int* __restrict__ order,
-                                                        int64_t n, int V, int* __restrict__ dst) {
-  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-  const int64_t stride = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-  for (int64_t k = warp; k < n; k += stride) {
-    const int64_t q = __ldg(order + k);
-    for (int v = lane; v < V; v += 32) dst[q * V + v] = __ldg(nbr + k * V + v);
-  }
-}
-
 // Block-wide inclusive scan of one value per thread (blockDim <= 1024).
 template <typename T>
 __device__ __forceinline__ T block_inclusive_scan(T x, T* warp_sums, T* total) {
@@ -376,105 +296,204 @@ __device__ __forceinline__ T block_inclusive_scan(T x, T* warp_sums, T* total) {
   return x;
 }
 
-__global__ void __launch_bounds__(kScanThreads) k_kmap_scan(
-    const unsigned* __restrict__ masks, int ntiles, int V, int64_t n, int* __restrict__ bases,
-    int* __restrict__ totals, int64_t* __restrict__ offs, int* __restrict__ ws_tiles, int64_t* __restrict__ map_size,
-    int* __restrict__ ticket) {
-  __shared__ long long warp_sums[32];
+struct BuildArgs {
+  const unsigned long long* keys;  // [n] packed key of each input row
+  const int* order;                // [n] or null
+  int64_t n;
+  const BlockEntry* table;
+  uint32_t mask;                   // table capacity - 1
+  int V, K, ndim, dimx, dimy, dimz;
+  int up;                          // points per unit (128, or 32 when V > 128)
+  int nunits;
+  int* nbr;                        // [n, V] in row order
+  unsigned* present;               // [nunits, 4] (up == 128 only)
+  int* in_rows;                    // [V, n] strided lists
+  int* out_rows;
+  int* cursors;                    // [V] entries reserved so far in each offset's list
+  int* status;                     // [4]: map status, hash status copy, -, done counter
+  int64_t* offs;                   // [V+1]
+  int* ws_tiles;                   // [V+1]
+  int64_t* map_size;
+};
+
+// Dynamic shared memory: s_tile [up * V] ints, s_bal [V * up / 32], s_base [V].
+// Five blocks per SM (register budget): 2560 lookups in flight per SM.
+__global__ void __launch_bounds__(kThreads, 5) k_kmap_build(const BuildArgs a) {
+  extern __shared__ int4 smem4[];
+  const int up = a.up, V = a.V;
+  const int ngroups = up / 32;
+  int* s_tile = reinterpret_cast<int*>(smem4);
+  unsigned* s_bal = reinterpret_cast<unsigned*>(s_tile + up * V);
+  int* s_base = reinterpret_cast<int*>(s_bal + V * ngroups);
   __shared__ int s_last;
-  const int v = blockIdx.x;
-  const unsigned* m = masks + static_cast<int64_t>(v) * ntiles;
-  int* b = bases + static_cast<int64_t>(v) * ntiles;
-  // each thread takes kScanPer consecutive tiles: all loads of a chunk are in
-  // flight together, then one block scan of the per-thread sums
-  long long carry = 0;
-  for (int base = 0; base < ntiles; base += kScanThreads * kScanPer) {
-    const int i0 = base + threadIdx.x * kScanPer;
-    int c[kScanPer];
-#pragma unroll
-    for (int k = 0; k < kScanPer; ++k) c[k] = i0 + k < ntiles ? __popc(__ldg(m + i0 + k)) : 0;
-    int sum = 0;
-#pragma unroll
-    for (int k = 0; k < kScanPer; ++k) sum += c[k];
-    long long total;
-    const long long inc = block_inclusive_scan<long long>(sum, warp_sums, &total);
-    int run = static_cast<int>(carry + inc - sum);
-#pragma unroll
-    for (int k = 0; k < kScanPer; ++k) {
-      if (i0 + k < ntiles) b[i0 + k] = run;
-      run += c[k];
+  __shared__ int s_row[128];
+  __shared__ unsigned s_pres[4];
+  __shared__ long long warp_sums[32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int kWarps = kThreads / 32;
+  if (threadIdx.x < 4) s_pres[threadIdx.x] = 0u;
+  for (int e = threadIdx.x; e < up * V; e += kThreads) s_tile[e] = -1;
+  __syncthreads();
+  const int u = blockIdx.x;
+  const int64_t i0 = static_cast<int64_t>(u) * up;
+  const int np = static_cast<int>(min(static_cast<int64_t>(up), a.n - i0));
+  const int r = (a.K - 1) / 2;
+  const int rz = a.ndim == 3 ? r : 0;
+  const int centre = (V - 1) / 2;
+
+  // ---- probe: thread = (point p, part); parts split the covering blocks
+  {
+    const int p = threadIdx.x % up, part = threadIdx.x / up, nparts = kThreads / up;
+    const bool live = p < np;
+    const int row = live ? (a.order ? __ldg(a.order + i0 + p) : static_cast<int>(i0 + p)) : -1;
+    if (part == 0 && p < up) s_row[p] = row;
+    const unsigned long long ck = live ? __ldg(a.keys + row) : kEmptyKey;
+    bool valid = ck != kEmptyKey;
+    const int x = static_cast<int>((ck >> 32) & 0xFFFF), y = static_cast<int>((ck >> 16) & 0xFFFF),
+              z = static_cast<int>(ck & 0xFFFF);
+    if (valid && (x >= a.dimx || y >= a.dimy || z >= a.dimz)) {
+      if (part == 0) atomicOr(a.status, kDevErrRange);
+      valid = false;
     }
-    carry += total;
-  }
-  if (threadIdx.x == 0) {
-    totals[v] = static_cast<int>(carry);
-    __threadfence();
-    s_last = atomicAdd(ticket, 1) == V - 1;
+    const unsigned long long batch = ck & 0xFFFF000000000000ull;
+    const int xlo = max(x - r, 0) >> 1, xhi = min(x + r, a.dimx - 1) >> 1;
+    const int ylo = max(y - r, 0) >> 1, yhi = min(y + r, a.dimy - 1) >> 1;
+    const int zlo = max(z - rz, 0) >> 1, zhi = min(z + rz, a.dimz - 1) >> 1;
+    const int nb = r + 1, nbz = rz + 1;  // covering blocks per axis, at most
+    const int ntrip = nb * nb * nbz;
+    {
+      // kLookups lookups in flight per thread: home entries first, then the
+      // (rare) further probes of each
+      for (int t0 = part; t0 < ntrip; t0 += kLookups * nparts) {
+        unsigned long long bk[kLookups], kk[kLookups];
+        uint32_t hh[kLookups];
+        int4 r0[kLookups], r1[kLookups];
+        bool act[kLookups];
+#pragma unroll
+        for (int q = 0; q < kLookups; ++q) {
+          const int t = t0 + q * nparts;
+          const int bx = xlo + t / (nb * nbz), by = ylo + (t / nbz) % nb, bz = zlo + t % nbz;
+          act[q] = valid && t < ntrip && bx <= xhi && by <= yhi && bz <= zhi;
+          bk[q] = batch | pack_key(0, 2 * bx, 2 * by, 2 * bz);
+          hh[q] = block_home(bk[q], a.mask);
+          if (act[q]) {
+            const BlockEntry* e = a.table + hh[q];
+            kk[q] = __ldg(&e->key);
+            r0[q] = __ldg(reinterpret_cast<const int4*>(e->rows));
+            r1[q] = __ldg(reinterpret_cast<const int4*>(e->rows + 4));
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < kLookups; ++q) {
+          if (!act[q]) continue;
+          bool hit = kk[q] == bk[q];
+          if (!hit && kk[q] != kEmptyKey) hit = lookup_block(a.table, a.mask, bk[q], r0[q], r1[q]);
+          if (!hit) continue;
+          const int t = t0 + q * nparts;
+          const int bx = xlo + t / (nb * nbz), by = ylo + (t / nbz) % nb, bz = zlo + t % nbz;
+#pragma unroll
+          for (int l = 0; l < 8; ++l) {
+            const int dx = 2 * bx + (l >> 2) - x, dy = 2 * by + ((l >> 1) & 1) - y, dz = 2 * bz + (l & 1) - z;
+            if (dx >= -r && dx <= r && dy >= -r && dy <= r && dz >= -rz && dz <= rz) {
+              const int v = a.ndim == 3 ? ((dx + r) * a.K + (dy + r)) * a.K + (dz + r) : (dx + r) * a.K + (dy + r);
+              s_tile[p * V + v] = pick(r0[q], r1[q], l);
+            }
+          }
+        }
+      }
+    }
   }
   __syncthreads();
-  if (!s_last) return;
-  // the last block: segment offsets, weight-stationary tile prefix, |M|
-  __threadfence();
-  const int t = threadIdx.x;
-  const long long cnt = t < V ? static_cast<long long>(__ldcg(totals + t)) : 0;
-  long long tot1, tot2;
-  const long long inc = block_inclusive_scan<long long>(cnt, warp_sums, &tot1);
-  const long long tl = (cnt + kWsRows - 1) / kWsRows;
-  const long long inc2 = block_inclusive_scan<long long>(tl, warp_sums, &tot2);
-  if (t < V) {
-    offs[t] = inc - cnt;
-    ws_tiles[t] = static_cast<int>(inc2 - tl);
+
+  // ---- count: hit ballots per (offset, 32 points); reserve each offset's
+  // run of list entries with one atomic on that offset's cursor
+  for (int q = warp; q < V * ngroups; q += kWarps) {
+    const int v = q / ngroups, g = q - v * ngroups;
+    const int j = s_tile[(g * 32 + lane) * V + v];
+    const unsigned b = __ballot_sync(0xffffffffu, v != centre && j >= 0);
+    if (lane == 0) s_bal[q] = b;
   }
-  if (t == 0) {
-    offs[V] = tot1;
-    ws_tiles[V] = static_cast<int>(tot2);
-    *map_size = n + tot1;
-    *ticket = 0;
+  __syncthreads();
+  for (int v = threadIdx.x; v < V; v += kThreads) {
+    int cnt = 0;
+    for (int g = 0; g < ngroups; ++g) cnt += __popc(s_bal[v * ngroups + g]);
+    s_base[v] = cnt ? atomicAdd(a.cursors + v, cnt) : 0;
+    if (cnt && v < 128 && up == 128) atomicOr(s_pres + (v >> 5), 1u << (v & 31));
+  }
+  __syncthreads();
+
+  // ---- emit: lists, the table block, the unit's present offsets
+  for (int q = warp; q < V * ngroups; q += kWarps) {
+    const unsigned b = s_bal[q];
+    if (!b) continue;
+    const int v = q / ngroups, g = q - v * ngroups;
+    int before = s_base[v];
+    for (int gg = 0; gg < g; ++gg) before += __popc(s_bal[v * ngroups + gg]);
+    if ((b >> lane) & 1u) {
+      const int64_t at = static_cast<int64_t>(v) * a.n + before + __popc(b & ((1u << lane) - 1u));
+      a.in_rows[at] = s_tile[(g * 32 + lane) * V + v];
+      a.out_rows[at] = s_row[g * 32 + lane];
+    }
+  }
+  {
+    // the unit's block of the table is contiguous: i0 * V * 4 bytes is a multiple of 128
+    int* dst = a.nbr + i0 * V;
+    const int items = np * V;
+    const int n4 = items >> 2;
+    for (int e = threadIdx.x; e < n4; e += kThreads) reinterpret_cast<int4*>(dst)[e] = reinterpret_cast<const int4*>(s_tile)[e];
+    for (int e = (n4 << 2) + threadIdx.x; e < items; e += kThreads) dst[e] = s_tile[e];
+  }
+  if (up == 128 && threadIdx.x < 4) a.present[static_cast<int64_t>(u) * 4 + threadIdx.x] = s_pres[threadIdx.x];
+
+  // ---- the last block: segment offsets, weight-stationary tile prefix, |M|
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(a.status + 3, 1) == a.nunits - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  // per-offset totals (the cursors' final values), scanned over offsets
+  long long carry = 0, carry_t = 0;
+  for (int v0 = 0; v0 < V; v0 += kThreads) {
+    const int v = v0 + threadIdx.x;
+    const long long cnt = v < V ? static_cast<long long>(__ldcg(a.cursors + v)) : 0;
+    long long tot, tot_t;
+    const long long inc = block_inclusive_scan<long long>(cnt, warp_sums, &tot);
+    const long long tl = (cnt + kWsRows - 1) / kWsRows;
+    const long long inc_t = block_inclusive_scan<long long>(tl, warp_sums, &tot_t);
+    if (v < V) {
+      a.offs[v] = carry + inc - cnt;
+      a.ws_tiles[v] = static_cast<int>(carry_t + inc_t - tl);
+    }
+    carry += tot;
+    carry_t += tot_t;
+  }
+  if (threadIdx.x == 0) {
+    a.offs[V] = carry;
+    a.ws_tiles[V] = static_cast<int>(carry_t);
+    *a.map_size = a.n + carry;
   }
 }
 
-__global__ void __launch_bounds__(kThreads) k_kmap_fill(const int* __restrict__ nbr, const int* __restrict__ order,
-                                                        int64_t n, int V, int ntiles,
-                                                        int tiles_per_block, const int* __restrict__ bases,
-                                                        const int64_t* __restrict__ offs, int* __restrict__ in_rows,
-                                                        int* __restrict__ out_rows) {
-  extern __shared__ int4 smem_fill[];
-  int* smem_i = reinterpret_cast<int*>(smem_fill);
-  int* s_nbr = smem_i;                                          // [tiles_per_block * 32 * V], 16-byte aligned
-  long long* s_offs = reinterpret_cast<long long*>(s_nbr + ((tiles_per_block * kTile * V + 3) & ~3));  // [V]
-  int* s_base = reinterpret_cast<int*>(s_offs + V);             // [tiles_per_block * V]
-  int* s_row = s_base + tiles_per_block * V;                    // [tiles_per_block * 32]
-  const int tile0 = blockIdx.x * tiles_per_block;
-  const int ntl = min(tiles_per_block, ntiles - tile0);
-  const int64_t i0 = static_cast<int64_t>(tile0) * kTile;
-  const int np = static_cast<int>(min(static_cast<int64_t>(ntl) * kTile, n - i0));
-  const int items = np * V;
-  for (int p = threadIdx.x; p < np; p += kThreads) s_row[p] = order ? __ldg(order + i0 + p) : static_cast<int>(i0 + p);
-  const int* src = nbr + i0 * V;
-  const int n4 = items >> 2;
-  for (int e = threadIdx.x; e < n4; e += kThreads)
-    reinterpret_cast<int4*>(s_nbr)[e] = __ldg(reinterpret_cast<const int4*>(src) + e);
-  for (int e = (n4 << 2) + threadIdx.x; e < items; e += kThreads) s_nbr[e] = __ldg(src + e);
-  for (int v = threadIdx.x; v < V; v += kThreads) s_offs[v] = __ldg(offs + v);
-  for (int q = threadIdx.x; q < ntl * V; q += kThreads) {
-    const int tl = q / V, v = q - tl * V;
-    s_base[q] = __ldg(bases + static_cast<int64_t>(v) * ntiles + tile0 + tl);
+// Rows of the table in input order: dst[order[k], :] = nbr[k, :].
+__global__ void __launch_bounds__(256) k_unpermute_rows(const int* __restrict__ nbr, const int* __restrict__ order,
+                                                        int64_t n, int V, int* __restrict__ dst) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  const int64_t stride = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t k = warp; k < n; k += stride) {
+    const int64_t q = __ldg(order + k);
+    for (int v = lane; v < V; v += 32) dst[q * V + v] = __ldg(nbr + k * V + v);
   }
-  __syncthreads();
-  const int centre = (V - 1) / 2;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int q = warp; q < ntl * V; q += kThreads / 32) {
-    const int tl = q / V, v = q - tl * V;
-    if (v == centre) continue;
-    const int p = tl * kTile + lane;
-    const int j = p < np ? s_nbr[p * V + v] : -1;
-    const unsigned bal = __ballot_sync(0xffffffffu, j >= 0);
-    if (j >= 0) {
-      const long long at = s_offs[v] + s_base[q] + __popc(bal & ((1u << lane) - 1u));
-      in_rows[at] = j;
-      out_rows[at] = s_row[p];
-    }
-  }
+}
+
+// The strided lists (offset v at v * n) compacted into CSR order.
+__global__ void __launch_bounds__(256) k_compact_lists(const int* __restrict__ src, const int64_t* __restrict__ offs,
+                                                       int64_t n, int* __restrict__ dst) {
+  const int v = blockIdx.y;
+  const int64_t b = __ldg(offs + v), cnt = __ldg(offs + v + 1) - b;
+  for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < cnt;
+       e += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    dst[b + e] = __ldg(src + static_cast<int64_t>(v) * n + e);
 }
 
 int grid_for(int64_t n, int threads) {
@@ -484,14 +503,9 @@ int grid_for(int64_t n, int threads) {
   return static_cast<int>(g < 1 ? 1 : g);
 }
 
-int fill_tiles_per_block(int V) {
-  int t = 8000 / (kTile * (V + 1));
-  return t < 1 ? 1 : (t > 8 ? 8 : t);
-}
-
 }  // namespace
 
-int kmap_probe_tile() { return kTile; }
+int kmap_unit_points(int V) { return V <= 128 ? 128 : 32; }
 int kmap_order_buckets() { return kBuckets + kBucketBlocks; }
 
 sc_status kmap_unpermute_nbr(const KernelMap* m, int* dst, cudaStream_t s) {
@@ -534,11 +548,6 @@ sc_status launch_kmap_build(const HashTable* h, KernelMap* m, cudaStream_t s) {
     if (e == cudaSuccess) e = cudaMemsetAsync(m->map_size, 0, sizeof(int64_t), s);
     return e == cudaSuccess ? SC_OK : set_cuda_error(e, "empty kmap init");
   }
-  const int tpb = fill_tiles_per_block(V);
-  const size_t probe_smem = sizeof(int) * kTile * V;
-  const size_t fill_smem =
-      sizeof(int) * (4 + 2 * V + static_cast<size_t>(tpb) * V + static_cast<size_t>(tpb) * kTile * (V + 1));
-  const uint32_t mask = static_cast<uint32_t>(h->capacity - 1);
   if (m->order) {  // locality order: count, two-phase scan, scatter
     OrderBits ob;
     int b[3];
@@ -565,28 +574,54 @@ sc_status launch_kmap_build(const HashTable* h, KernelMap* m, cudaStream_t s) {
     e = cudaGetLastError();
     if (e != cudaSuccess) return set_cuda_error(e, "locality order launch");
   }
-  e = cudaMemsetAsync(m->present, 0, sizeof(unsigned) * 4 * ((m->n + 127) / 128), s);
-  if (e != cudaSuccess) return set_cuda_error(e, "kmap presence clear");
-  SC_LAUNCH("kmap_probe", s,
-            k_kmap_probe<<<m->ntiles, kThreads, probe_smem, s>>>(h->keys, m->order, m->n, h->table, mask, V,
-                                                                  m->K,
-                                                                  m->ndim,
-                                                                  m->dims[0], m->dims[1], m->dims[2], m->nbr,
-                                                                  m->masks, m->present, m->ntiles, m->status));
+  e = cudaMemsetAsync(m->cursors, 0, sizeof(int) * V, s);
+  if (e != cudaSuccess) return set_cuda_error(e, "kmap cursor clear");
+  BuildArgs a;
+  a.keys = h->keys;
+  a.order = m->order;
+  a.n = m->n;
+  a.table = h->table;
+  a.mask = static_cast<uint32_t>(h->capacity - 1);
+  a.V = V;
+  a.K = m->K;
+  a.ndim = m->ndim;
+  a.dimx = m->dims[0];
+  a.dimy = m->dims[1];
+  a.dimz = m->dims[2];
+  a.up = m->up;
+  a.nunits = m->nunits;
+  a.nbr = m->nbr;
+  a.present = m->present;
+  a.in_rows = m->in_rows;
+  a.out_rows = m->out_rows;
+  a.cursors = m->cursors;
+  a.status = m->status;
+  a.offs = m->offs;
+  a.ws_tiles = m->ws_tiles;
+  a.map_size = m->map_size;
+  const size_t smem = sizeof(int) * (static_cast<size_t>(m->up) * V + static_cast<size_t>(V) * (m->up / 32) + V);
+  if (smem > 48 * 1024) {  // set once per device: the largest the build ever asks for
+    static bool done[64] = {false};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64 || !done[dev]) {
+      e = cudaFuncSetAttribute(k_kmap_build, cudaFuncAttributeMaxDynamicSharedMemorySize, kBuildSmemMax);
+      if (e != cudaSuccess) return set_cuda_error(e, "kmap_build smem attribute");
+      if (dev >= 0 && dev < 64) done[dev] = true;
+    }
+  }
+  SC_LAUNCH("kmap_build", s, k_kmap_build<<<m->nunits, kThreads, smem, s>>>(a));
   e = cudaGetLastError();
-  if (e != cudaSuccess) return set_cuda_error(e, "kmap_probe launch");
-  SC_LAUNCH("kmap_scan", s,
-            k_kmap_scan<<<V, kScanThreads, 0, s>>>(m->masks, m->ntiles, V, m->n, m->bases, m->totals, m->offs,
-                                                   m->ws_tiles, m->map_size, m->status + 2));
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return set_cuda_error(e, "kmap_scan launch");
-  const int fill_blocks = (m->ntiles + tpb - 1) / tpb;
-  SC_LAUNCH("kmap_fill", s,
-            k_kmap_fill<<<fill_blocks, kThreads, fill_smem, s>>>(m->nbr, m->order, m->n, V, m->ntiles, tpb, m->bases,
-                                                                  m->offs,
-                                                                  m->in_rows, m->out_rows));
-  e = cudaGetLastError();
-  return e == cudaSuccess ? SC_OK : set_cuda_error(e, "kmap_fill launch");
+  return e == cudaSuccess ? SC_OK : set_cuda_error(e, "kmap_build launch");
+}
+
+sc_status kmap_compact_lists(const KernelMap* m, const int* src, int* dst, int64_t total, cudaStream_t s) {
+  if (total == 0) return SC_OK;
+  int64_t per = (m->n + 255) / 256;
+  dim3 grid(static_cast<unsigned>(per < 64 ? per : 64), static_cast<unsigned>(m->V));
+  SC_LAUNCH("kmap_compact", s, k_compact_lists<<<grid, 256, 0, s>>>(src, m->offs, m->n, dst));
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? SC_OK : set_cuda_error(e, "kmap_compact launch");
 }
 
 }  // namespace sc

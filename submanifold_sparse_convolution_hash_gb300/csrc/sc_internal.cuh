@@ -78,17 +78,16 @@ struct KernelMap {
   int64_t n = 0;
   int ndim = 3, K = 3, V = 27;
   int dims[3] = {1, 1, 1};
-  int ntiles = 0;                    // 32-point tiles of the map build
+  int up = 128;                      // points per map-build unit (128; 32 when V > 128)
+  int nunits = 0;                    // map-build units
   int* order = nullptr;              // [n] input rows in locality order, or null: input order
   int* buckets = nullptr;            // counting-sort buckets of that order (+ scan partials)
   int* nbr = nullptr;                // [n, V], rows in the row order (position k = input row order[k])
   int64_t* offs = nullptr;           // [V+1]
-  int* in_rows = nullptr;            // [n*(V-1)] capacity, offs[V] used
+  int* in_rows = nullptr;            // [V, n]: offset v's list at v * n, offs[v+1] - offs[v] entries
   int* out_rows = nullptr;
-  unsigned* masks = nullptr;         // [V, ntiles] hit bitmask of each tile's 32 points
   unsigned* present = nullptr;       // [ceil(n/128), 4] offsets (< 128) with a hit in each 128-row tile of the row order
-  int* bases = nullptr;              // [V, ntiles] exclusive prefix of the mask popcounts
-  int* totals = nullptr;             // [V]
+  int* cursors = nullptr;            // [V] list entries reserved per offset during the build
   int* ws_tiles = nullptr;           // [V+1] prefix of ceil(count/128) per offset
   int64_t* map_size = nullptr;       // device: n + offs[V]
   int* status = nullptr;             // [4]: map status, copy of the hash status, scan ticket
@@ -120,7 +119,8 @@ sc_status launch_hash_insert(const int32_t* coords, int64_t n, HashTable* h, cud
 sc_status launch_hash_query(const HashTable* h, const int32_t* q, int64_t m, int32_t* rows,
                             cudaStream_t s);
 sc_status launch_kmap_build(const HashTable* h, KernelMap* m, cudaStream_t s);
-int kmap_probe_tile();
+int kmap_unit_points(int V);
+sc_status kmap_compact_lists(const KernelMap* m, const int* src, int* dst, int64_t total, cudaStream_t s);
 int kmap_order_buckets();
 
 // kernels: convolution (conv_tc.cu, conv_simt.cu)
