@@ -85,7 +85,8 @@ def exported_symbols() -> list:
                         "sc_kmap_build", "sc_kmap_info", "sc_kmap_check", "sc_kmap_export", "sc_kmap_destroy",
                         "sc_subm_conv_fwd", "sc_subm_conv_tune", "sc_subm_conv_fwd_noalloc",
                         "sc_status_str", "sc_last_error",
-                        "sc_launch_count", "sc_profile_enable", "sc_profile_collect", "sc_profile_reset",
+                        "sc_launch_count", "sc_profile_enable", "sc_profile_only", "sc_profile_collect",
+                        "sc_profile_reset",
                         "sc_profile_get")]
 
 
