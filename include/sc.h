@@ -69,6 +69,8 @@ typedef enum { SC_F32 = 0, SC_F16 = 1, SC_BF16 = 2 } sc_dtype;
 #define SC_KMAP_NO_SYNC 0x100u  /* do not synchronise; check errors later with sc_kmap_check */
 #define SC_KMAP_ORDER 0x200u    /* always compute the locality order (default: n >= 262144) */
 #define SC_KMAP_NO_ORDER 0x400u /* never compute it: tiles follow the input row order */
+#define SC_KMAP_SORT 0x800u     /* always sort the convolution's rows by signature (default: n >= 262144, V <= 32) */
+#define SC_KMAP_NO_SORT 0x1000u /* never sort them */
 
 typedef struct sc_hash_s* sc_hash;
 typedef struct sc_kmap_s* sc_kmap;
@@ -125,8 +127,9 @@ sc_status sc_hash_destroy(sc_hash h, sc_stream stream);
  * K         odd, K >= 1, with V = K^ndim <= 343 (K <= 7 in 3D, K <= 17 in 2D).
  * dims      spatial extents (x, y, z), each in [1, 65535]; every point must
  *           lie inside; neighbours outside are absent (zero padding).
- * flags     0, SC_KMAP_NO_SYNC, and at most one of SC_KMAP_ORDER /
- *           SC_KMAP_NO_ORDER.
+ * flags     0, SC_KMAP_NO_SYNC, at most one of SC_KMAP_ORDER /
+ *           SC_KMAP_NO_ORDER, and at most one of SC_KMAP_SORT /
+ *           SC_KMAP_NO_SORT.
  *
  * Locality order: for n >= 262144 (or with SC_KMAP_ORDER) the build first
  * sorts the points into spatially compact groups (a counting sort on the top
@@ -134,6 +137,14 @@ sc_status sc_hash_destroy(sc_hash h, sc_stream stream);
  * tiles are runs of that order, so they touch fewer offsets and reuse
  * neighbour rows.  It changes no result: outputs still land on their own
  * rows and nbr stays in input row order.
+ *
+ * Signature sort (V <= 32; for n >= 262144 or with SC_KMAP_SORT): inside
+ * windows of 65536 consecutive rows of that order, the convolution's rows
+ * are counting-sorted by a 16-bit signature, which of the 16 least frequent
+ * offsets (over the whole map) the row has a neighbour under.  Rows that
+ * touch the same rare offsets then share 128-row tiles, and a tile walks
+ * fewer offsets (the bitmask reordering of "TorchSparse optimizations",
+ * section "TorchSparse++").  It too changes no result.
  *
  * Products, owned by the handle:
  *   nbr      int32 [n, V]: nbr[q*V + idx(d)] = row p with coords[p] =

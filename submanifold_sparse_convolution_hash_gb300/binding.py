@@ -22,6 +22,8 @@ SC_VARIANT_SIMT = 0x40
 SC_KMAP_NO_SYNC = 0x100
 SC_KMAP_ORDER = 0x200
 SC_KMAP_NO_ORDER = 0x400
+SC_KMAP_SORT = 0x800
+SC_KMAP_NO_SORT = 0x1000
 VARIANTS = {"fused": SC_VARIANT_FUSED, "ws": SC_VARIANT_WS, "simt": SC_VARIANT_SIMT}
 VARIANT_NAMES = {v: k for k, v in VARIANTS.items()}
 _DTYPES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
@@ -210,11 +212,13 @@ def sc_hash_build(coords: torch.Tensor, stream=None) -> Hash:
 
 
 def sc_kmap_build(h: Hash, ndim: int, K: int, dims, sync: bool = True, order: bool | None = None,
-                  stream=None) -> KernelMap:
+                  sort: bool | None = None, stream=None) -> KernelMap:
     """Kernel map of a K^ndim submanifold convolution over the hashed points.
 
     order: True / False forces the locality order on / off; None leaves the
-    library's default (on for n >= 262144)."""
+    library's default (on for n >= 262144).  sort: the same for the
+    signature sort of the convolution's rows (default on for n >= 262144 when
+    K^ndim <= 32)."""
     d = (ctypes.c_int32 * 3)(*(list(dims) + [1] * (3 - len(dims))))
     m = ctypes.c_void_p()
     flags = 0 if sync else SC_KMAP_NO_SYNC
@@ -222,6 +226,10 @@ def sc_kmap_build(h: Hash, ndim: int, K: int, dims, sync: bool = True, order: bo
         flags |= SC_KMAP_ORDER
     elif order is False:
         flags |= SC_KMAP_NO_ORDER
+    if sort is True:
+        flags |= SC_KMAP_SORT
+    elif sort is False:
+        flags |= SC_KMAP_NO_SORT
     _check(lib().sc_kmap_build(h._h, ndim, K, d, flags, _stream(stream), ctypes.byref(m)), "sc_kmap_build")
     return KernelMap(m, h.n, ndim, K, list(d), h.device)
 

@@ -398,6 +398,8 @@ sc_status sc_kmap_destroy(sc_kmap m, sc_stream stream) {
 
 // Inputs at least this large get a locality order by default.
 constexpr int64_t kOrderMinPoints = 262144;
+// ... and a signature sort of the convolution's rows (V <= 32).
+constexpr int64_t kSortMinPoints = 262144;
 
 sc_status sc_kmap_build(sc_hash h, int ndim, int K, const int32_t dims[3], unsigned flags, sc_stream stream,
                         sc_kmap* out) {
@@ -414,10 +416,12 @@ sc_status sc_kmap_build(sc_hash h, int ndim, int K, const int32_t dims[3], unsig
   if (!dims) return set_error(SC_ERR_INVALID_ARG, "dims is NULL");
   for (int a = 0; a < 3; ++a)
     if (dims[a] < 1 || dims[a] > 65535) return set_error(SC_ERR_INVALID_ARG, "dims must be in [1, 65535]");
-  if (flags & ~(SC_KMAP_NO_SYNC | SC_KMAP_ORDER | SC_KMAP_NO_ORDER))
+  if (flags & ~(SC_KMAP_NO_SYNC | SC_KMAP_ORDER | SC_KMAP_NO_ORDER | SC_KMAP_SORT | SC_KMAP_NO_SORT))
     return set_error(SC_ERR_INVALID_ARG, "unknown kmap flag");
   if ((flags & SC_KMAP_ORDER) && (flags & SC_KMAP_NO_ORDER))
     return set_error(SC_ERR_INVALID_ARG, "SC_KMAP_ORDER and SC_KMAP_NO_ORDER together");
+  if ((flags & SC_KMAP_SORT) && (flags & SC_KMAP_NO_SORT))
+    return set_error(SC_ERR_INVALID_ARG, "SC_KMAP_SORT and SC_KMAP_NO_SORT together");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   sc_kmap m = new sc_kmap_s();
   KernelMap& k = m->k;
@@ -429,6 +433,10 @@ sc_status sc_kmap_build(sc_hash h, int ndim, int K, const int32_t dims[3], unsig
   k.up = kmap_unit_points(V);
   k.nunits = static_cast<int>((k.n + k.up - 1) / k.up);
   const bool ordered = (flags & SC_KMAP_ORDER) || (!(flags & SC_KMAP_NO_ORDER) && k.n >= kOrderMinPoints);
+  // the signature sort needs one mask word per row (V <= 32)
+  const bool sorted = V <= 32 && k.n > 0 &&
+                      ((flags & SC_KMAP_SORT) || (!(flags & SC_KMAP_NO_SORT) && k.n >= kSortMinPoints));
+  const size_t nsig = sorted ? static_cast<size_t>(kmap_sig_buckets(k.n)) : 0;
   // every buffer of the map carved from one allocation, each 256-byte aligned
   const size_t n = static_cast<size_t>(k.n);
   struct Part {
@@ -446,6 +454,11 @@ sc_status sc_kmap_build(sc_hash h, int ndim, int K, const int32_t dims[3], unsig
       {reinterpret_cast<void**>(&k.status), sizeof(int) * 4},
       {reinterpret_cast<void**>(&k.order), ordered && k.n > 0 ? sizeof(int) * n : 0},
       {reinterpret_cast<void**>(&k.buckets), ordered && k.n > 0 ? sizeof(int) * kmap_order_buckets() : 0},
+      {reinterpret_cast<void**>(&k.rowmask), sorted ? sizeof(unsigned) * n : 0},
+      {reinterpret_cast<void**>(&k.sig_sel), sorted ? sizeof(int) * kmap_sig_bits() : 0},
+      {reinterpret_cast<void**>(&k.sigbuckets), sorted ? sizeof(int) * (nsig + nsig / 4096 + 1) : 0},
+      {reinterpret_cast<void**>(&k.perm), sorted ? sizeof(int) * n : 0},
+      {reinterpret_cast<void**>(&k.conv_order), sorted ? sizeof(int) * n : 0},
   };
   size_t total = 0;
   for (const Part& pt : parts) total += (pt.bytes + 255) & ~size_t(255);

@@ -227,7 +227,8 @@ struct TcParams {
   uint8_t* out;              // output-stationary: [n, c_out] 2-byte elements
   float* acc;                // weight-stationary: fp32 [n, c_out]
   const int* nbr;            // [n, V]
-  const int* order;          // [n] input row of each table row (null: identity); tiles are runs of table rows
+  const int* order;          // [n] input row of each tile row (null: identity); tiles are runs of 128 rows
+  const int* perm;           // [n] table row of each tile row (null: identity; set by the signature sort)
   const uint4* present;      // [tiles]: 128-bit mask of the offsets present in each 128-row tile
   const int* in_rows;        // weight-stationary lists: offset v's at v * n
   const int* out_rows;
@@ -420,10 +421,15 @@ __global__ void __launch_bounds__((NPW + 6) * 32, NPW == 4 ? 3 : (NPW == 8 ? 2 :
       // Lane j < RW of warp w fetches the source row of unit row RW w + j for
       // an offset; the warp's lanes then take the rows they copy by shuffle,
       // so each offset costs one index load per row, issued an offset ahead.
+      // this lane's row of the neighbour table (the tile row itself, or the
+      // row the signature sort put there)
+      int64_t trow_lane = 0;
+      if (MODE == kOutputStationary && lane < RW && rw0 + lane < t.nrows)
+        trow_lane = p.perm ? static_cast<int64_t>(__ldg(p.perm + t.row0 + rw0 + lane)) : t.row0 + rw0 + lane;
       auto fetch = [&](int vv) -> int {
         const int r = rw0 + lane;
         if (vv >= V || lane >= RW || r >= t.nrows) return -1;
-        if (MODE == kOutputStationary) return __ldg(p.nbr + (t.row0 + r) * V + vv);
+        if (MODE == kOutputStationary) return __ldg(p.nbr + trow_lane * V + vv);
         if (MODE == kWsScatter) return __ldg(p.in_rows + t.lb + r);
         return static_cast<int>(t.row0 + r);
       };
@@ -485,7 +491,7 @@ __global__ void __launch_bounds__((NPW + 6) * 32, NPW == 4 ? 3 : (NPW == 8 ? 2 :
     // of the neighbour table into L2.
     if (lane == 0) {
       uint32_t it = 0;
-      if (MODE == kOutputStationary && static_cast<int>(blockIdx.x) < p.num_units) {
+      if (MODE == kOutputStationary && !p.perm && static_cast<int>(blockIdx.x) < p.num_units) {
         const TileInfo t0 = tile_info<MODE, T>(p, blockIdx.x);
         const uint32_t bytes = (static_cast<uint32_t>(t0.nrows) * V * 4) & ~15u;
         if (bytes) bulk_prefetch_l2(p.nbr + t0.row0 * V, bytes);
@@ -497,7 +503,7 @@ __global__ void __launch_bounds__((NPW + 6) * 32, NPW == 4 ? 3 : (NPW == 8 ? 2 :
           m = unit_mask<T>(p, u);
           bv = next_present(m, -1, V);
           const int nu = u + gridDim.x;
-          if (nu < p.num_units) {
+          if (nu < p.num_units && !p.perm) {
             const TileInfo tn = tile_info<MODE, T>(p, nu);
             const uint32_t bytes = (static_cast<uint32_t>(tn.nrows) * V * 4) & ~15u;
             if (bytes) bulk_prefetch_l2(p.nbr + tn.row0 * V, bytes);
@@ -875,7 +881,8 @@ TcParams base_params(const ConvArgs& a, const Plan& pl, const uint8_t* img) {
   p.wimg = img;
   p.out = static_cast<uint8_t*>(a.out);
   p.nbr = a.m->nbr;
-  p.order = a.m->order;
+  p.order = a.m->perm ? a.m->conv_order : a.m->order;
+  p.perm = a.m->perm;
   p.present = reinterpret_cast<const uint4*>(a.m->present);
   p.in_rows = a.m->in_rows;
   p.out_rows = a.m->out_rows;

@@ -51,6 +51,8 @@ namespace {
 
 constexpr int kThreads = 256;    // threads per map-build block
 constexpr int kLookups = 2;      // hash lookups in flight per map-build thread
+constexpr int kSigBits = 16;     // signature sort: rare offsets in a row's key
+constexpr int kSigWindow = 65536;  // rows per signature-sort window
 constexpr int kWsRows = 128;     // rows per weight-stationary tile
 // shared memory of a build block: 128 points x V <= 128 (or 32 x V <= 343)
 // neighbour slots, the ballots and the per-offset bases
@@ -314,6 +316,8 @@ struct BuildArgs {
   int64_t* offs;                   // [V+1]
   int* ws_tiles;                   // [V+1]
   int64_t* map_size;
+  unsigned* rowmask;               // [n] offsets (< 32, centre excluded) with a neighbour, per row; or null
+  int* sig_sel;                    // [kSigBits] offsets of the row signature, rarest first (with rowmask)
 };
 
 // Dynamic shared memory: s_tile [up * V] ints, s_bal [V * up / 32], s_base [V].
@@ -420,6 +424,12 @@ __global__ void __launch_bounds__(kThreads, 5) k_kmap_build(const BuildArgs a) {
     s_base[v] = cnt ? atomicAdd(a.cursors + v, cnt) : 0;
     if (cnt && v < 128 && up == 128) atomicOr(s_pres + (v >> 5), 1u << (v & 31));
   }
+  if (a.rowmask && threadIdx.x < np) {  // V <= 32: one word per row
+    unsigned mk = 0;
+    for (int v = 0; v < V; ++v)
+      if (v != centre && s_tile[threadIdx.x * V + v] >= 0) mk |= 1u << v;
+    a.rowmask[i0 + threadIdx.x] = mk;
+  }
   __syncthreads();
 
   // ---- emit: lists, the table block, the unit's present offsets
@@ -473,6 +483,92 @@ __global__ void __launch_bounds__(kThreads, 5) k_kmap_build(const BuildArgs a) {
     a.ws_tiles[V] = static_cast<int>(carry_t);
     *a.map_size = a.n + carry;
   }
+  if (a.rowmask && warp == 0) {
+    // the kSigBits least frequent offsets that occur at all, rarest first:
+    // lane v holds (count, v); kSigBits rounds of a warp minimum (V <= 32)
+    const long long none = 0x7FFFFFFFFFFFFFFFll;
+    const int c = lane < V && lane != centre ? __ldcg(a.cursors + lane) : 0;
+    long long key = c > 0 ? (static_cast<long long>(c) << 8) | lane : none;
+    for (int k = 0; k < kSigBits; ++k) {
+      long long mn = key;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const long long other = __shfl_xor_sync(0xffffffffu, mn, o);
+        mn = other < mn ? other : mn;
+      }
+      if (lane == 0) a.sig_sel[k] = mn == none ? -1 : static_cast<int>(mn & 255);  // -1: no further offset occurs
+      if (key == mn) key = none;
+    }
+  }
+}
+
+// Signature sort, a counting sort on (window of kSigWindow rows, signature):
+// rows keep their window (a spatially compact run of the locality order, or
+// of the input order) and are grouped by which rare offsets they touch, so a
+// 128-row tile spans fewer offsets.  Rows with equal keys in a warp share one
+// atomic (__match_any_sync); the order inside a key is unspecified.
+__device__ __forceinline__ int64_t sig_key(int64_t k, unsigned mk, const int* __restrict__ sel) {
+  unsigned sg = 0;
+#pragma unroll
+  for (int b = 0; b < kSigBits; ++b) {
+    const int v = __ldg(sel + b);
+    if (v >= 0) sg |= ((mk >> v) & 1u) << (kSigBits - 1 - b);
+  }
+  return ((k / kSigWindow) << kSigBits) | sg;
+}
+
+__global__ void __launch_bounds__(256) k_sig_count(const unsigned* __restrict__ rowmask, int64_t n,
+                                                   const int* __restrict__ sel, int* __restrict__ buckets) {
+  const int lane = threadIdx.x & 31;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t nr = (n + 31) & ~int64_t(31);  // whole warps stay in the loop
+  for (int64_t k = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; k < nr; k += stride) {
+    const bool live = k < n;
+    const int64_t key = live ? sig_key(k, __ldg(rowmask + k), sel) : -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, key);
+    if (live && lane == __ffs(peers) - 1) atomicAdd(buckets + key, __popc(peers));
+  }
+}
+
+__global__ void __launch_bounds__(256) k_sig_scatter(const unsigned* __restrict__ rowmask, const int* __restrict__ order,
+                                                     int64_t n, const int* __restrict__ sel, int* __restrict__ cursors,
+                                                     int* __restrict__ perm, int* __restrict__ conv_order) {
+  const int lane = threadIdx.x & 31;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t nr = (n + 31) & ~int64_t(31);
+  for (int64_t k = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; k < nr; k += stride) {
+    const bool live = k < n;
+    const int64_t key = live ? sig_key(k, __ldg(rowmask + k), sel) : -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, key);
+    const int leader = __ffs(peers) - 1;
+    int base = 0;
+    if (live && lane == leader) base = atomicAdd(cursors + key, __popc(peers));
+    base = __shfl_sync(0xffffffffu, base, leader);
+    if (live) {
+      const int pos = base + __popc(peers & ((1u << lane) - 1u));
+      perm[pos] = static_cast<int>(k);
+      conv_order[pos] = order ? __ldg(order + k) : static_cast<int>(k);
+    }
+  }
+}
+
+// Present offsets of each 128-row tile of the sorted order, one warp per
+// tile (V <= 32: every offset, the centre included, is in the first word).
+__global__ void __launch_bounds__(256) k_sig_present(const int* __restrict__ perm, const unsigned* __restrict__ rowmask,
+                                                     int64_t n, int centre, unsigned* __restrict__ present) {
+  const int64_t ntiles = (n + 127) / 128;
+  const int lane = threadIdx.x & 31;
+  const int64_t wstride = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t t = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; t < ntiles; t += wstride) {
+    unsigned acc = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int64_t j = t * 128 + k * 32 + lane;
+      if (j < n) acc |= __ldg(rowmask + __ldg(perm + j));
+    }
+    acc = __reduce_or_sync(0xffffffffu, acc);
+    if (lane < 4) present[t * 4 + lane] = lane == 0 ? (acc | (1u << centre)) : 0u;
+  }
 }
 
 // Rows of the table in input order: dst[order[k], :] = nbr[k, :].
@@ -507,6 +603,8 @@ int grid_for(int64_t n, int threads) {
 
 int kmap_unit_points(int V) { return V <= 128 ? 128 : 32; }
 int kmap_order_buckets() { return kBuckets + kBucketBlocks; }
+int kmap_sig_bits() { return kSigBits; }
+int64_t kmap_sig_buckets(int64_t n) { return ((n + kSigWindow - 1) / kSigWindow) << kSigBits; }
 
 sc_status kmap_unpermute_nbr(const KernelMap* m, int* dst, cudaStream_t s) {
   if (m->n == 0) return SC_OK;
@@ -599,6 +697,8 @@ sc_status launch_kmap_build(const HashTable* h, KernelMap* m, cudaStream_t s) {
   a.offs = m->offs;
   a.ws_tiles = m->ws_tiles;
   a.map_size = m->map_size;
+  a.rowmask = m->rowmask;
+  a.sig_sel = m->sig_sel;
   const size_t smem = sizeof(int) * (static_cast<size_t>(m->up) * V + static_cast<size_t>(V) * (m->up / 32) + V);
   if (smem > 48 * 1024) {  // set once per device: the largest the build ever asks for
     static bool done[64] = {false};
@@ -612,7 +712,26 @@ sc_status launch_kmap_build(const HashTable* h, KernelMap* m, cudaStream_t s) {
   }
   SC_LAUNCH("kmap_build", s, k_kmap_build<<<m->nunits, kThreads, smem, s>>>(a));
   e = cudaGetLastError();
-  return e == cudaSuccess ? SC_OK : set_cuda_error(e, "kmap_build launch");
+  if (e != cudaSuccess) return set_cuda_error(e, "kmap_build launch");
+  if (!m->perm) return SC_OK;
+  // signature sort of the rows for the convolution's tiles
+  const int64_t nsig = kmap_sig_buckets(m->n);  // a multiple of kBucketChunk
+  int* partial = m->sigbuckets + nsig;
+  const int chunks = static_cast<int>(nsig / kBucketChunk);
+  e = cudaMemsetAsync(m->sigbuckets, 0, sizeof(int) * nsig, s);
+  if (e != cudaSuccess) return set_cuda_error(e, "signature bucket clear");
+  const int g = grid_for(m->n, 256);
+  SC_LAUNCH("sig_count", s, k_sig_count<<<g, 256, 0, s>>>(m->rowmask, m->n, m->sig_sel, m->sigbuckets));
+  SC_LAUNCH("sig_partials", s, k_order_partials<<<chunks, 256, 0, s>>>(m->sigbuckets, partial));
+  SC_LAUNCH("sig_scan", s, k_order_apply<<<chunks, 256, 0, s>>>(m->sigbuckets, partial));
+  SC_LAUNCH("sig_scatter", s,
+            k_sig_scatter<<<g, 256, 0, s>>>(m->rowmask, m->order, m->n, m->sig_sel, m->sigbuckets, m->perm,
+                                            m->conv_order));
+  SC_LAUNCH("sig_present", s,
+            k_sig_present<<<grid_for(((m->n + 127) / 128) * 32, 256), 256, 0, s>>>(m->perm, m->rowmask, m->n,
+                                                                                (V - 1) / 2, m->present));
+  e = cudaGetLastError();
+  return e == cudaSuccess ? SC_OK : set_cuda_error(e, "signature sort launch");
 }
 
 sc_status kmap_compact_lists(const KernelMap* m, const int* src, int* dst, int64_t total, cudaStream_t s) {

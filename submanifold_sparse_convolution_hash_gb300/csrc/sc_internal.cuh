@@ -88,6 +88,12 @@ struct KernelMap {
   int* out_rows = nullptr;
   unsigned* present = nullptr;       // [ceil(n/128), 4] offsets (< 128) with a hit in each 128-row tile of the row order
   int* cursors = nullptr;            // [V] list entries reserved per offset during the build
+  // signature sort (V <= 32): the convolution walks rows in a second order
+  unsigned* rowmask = nullptr;       // [n] offsets with a neighbour, per row of the table
+  int* sig_sel = nullptr;            // [16] signature offsets, rarest first
+  int* sigbuckets = nullptr;         // counting-sort buckets (+ scan partials)
+  int* perm = nullptr;               // [n] sorted position -> table row, or null: no sort
+  int* conv_order = nullptr;         // [n] sorted position -> input row
   int* ws_tiles = nullptr;           // [V+1] prefix of ceil(count/128) per offset
   int64_t* map_size = nullptr;       // device: n + offs[V]
   int* status = nullptr;             // [4]: map status, copy of the hash status, scan ticket
@@ -122,6 +128,8 @@ sc_status launch_kmap_build(const HashTable* h, KernelMap* m, cudaStream_t s);
 int kmap_unit_points(int V);
 sc_status kmap_compact_lists(const KernelMap* m, const int* src, int* dst, int64_t total, cudaStream_t s);
 int kmap_order_buckets();
+int kmap_sig_bits();
+int64_t kmap_sig_buckets(int64_t n);
 
 // kernels: convolution (conv_tc.cu, conv_simt.cu)
 struct ConvArgs {

@@ -30,10 +30,10 @@ def small_scenes():
 SCENES = small_scenes()
 
 
-def build(scene, K, sync=True, order=None):
+def build(scene, K, sync=True, order=None, sort=None):
     c = torch.from_numpy(scene.coords).cuda()
     h = sc.sc_hash_build(c)
-    m = sc.sc_kmap_build(h, scene.ndim, K, scene.dims, sync=sync, order=order)
+    m = sc.sc_kmap_build(h, scene.ndim, K, scene.dims, sync=sync, order=order, sort=sort)
     return c, h, m
 
 
@@ -63,10 +63,11 @@ def test_hash_query_finds_every_row_and_misses_absent_keys():
 
 @pytest.mark.parametrize("name,K", [("uniform2d", 3), ("uniform2d_dense", 5), ("lidar", 3), ("indoor", 3),
                                     ("indoor", 5), ("batch", 3), ("lidar", 1), ("indoor", 7)])
-@pytest.mark.parametrize("sync,order", [(True, False), (False, False), (True, True), (False, True)])
-def test_kmap_bit_exact(name, K, sync, order):
+@pytest.mark.parametrize("sync,order,sort", [(True, False, False), (False, False, False), (True, True, False),
+                                             (False, True, False), (True, False, True), (False, True, True)])
+def test_kmap_bit_exact(name, K, sync, order, sort):
     s = SCENES[name]
-    c, h, m = build(s, K, sync, order)
+    c, h, m = build(s, K, sync, order, sort)
     if not sync:
         m.check()
     ref = oracle.kmap(s.coords, s.ndim, K, s.dims)
@@ -164,11 +165,11 @@ CONV_CASES = [
 ]
 
 
-@pytest.mark.parametrize("order", [False, True])
+@pytest.mark.parametrize("order,sort", [(False, False), (True, False), (False, True), (True, True)])
 @pytest.mark.parametrize("name,K,c_in,c_out,dtype,relu,variant", CONV_CASES)
-def test_conv_matches_oracle(name, K, c_in, c_out, dtype, relu, variant, order):
+def test_conv_matches_oracle(name, K, c_in, c_out, dtype, relu, variant, order, sort):
     s = SCENES[name]
-    c, h, m = build(s, K, order=order)
+    c, h, m = build(s, K, order=order, sort=sort)
     f, w, f64, w64 = layer_inputs(s, K, c_in, c_out, dtype, seed=7 + c_in + K,
                                   w_std=1.0 if dtype == "f32" else None)
     out = sc.sc_subm_conv_fwd(m, f, w, relu=relu, variant=variant)
