@@ -66,6 +66,7 @@ namespace {
 
 constexpr int kRows = 128;        // rows per tile (MMA M)
 constexpr int kMaxStages = 8;
+constexpr int kAhead = 2;  // offsets whose neighbour indices a producer loads ahead (measured: 2 > 1, 3)
 constexpr int kBarriers = 2 * kMaxStages + 5;  // full[S], empty[S], acc_full[2], acc_empty[2], done
 constexpr unsigned long long kWaitNs = 2000000000ull;
 
@@ -104,8 +105,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 // Bounded wait for the phase of `parity` to complete; false on timeout/abort.
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-  if (mbar_try_wait(bar, parity)) return true;
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
   const unsigned long long t0 = globaltimer();
   for (uint32_t it = 1; it < (1u << 30); ++it) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -115,6 +115,11 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile i
     }
   }
   return false;
+}
+// The first test inline (the common case: already complete), the bounded
+// loop out of line.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  return mbar_try_wait(bar, parity) || mbar_wait_slow(bar, parity, abort_flag);
 }
 // Same bound, ignoring the abort flag: used to drain work already issued.
 __device__ __noinline__ bool mbar_drain(uint32_t bar, uint32_t parity) {
@@ -441,7 +446,17 @@ __global__ void __launch_bounds__((NPW + 6) * 32, NPW == 4 ? 3 : (NPW == 8 ? 2 :
         for (int k = 0; k < RPT; ++k) src[k] = __shfl_sync(0xffffffffu, cur, lane / CPR + RSTEP * k);
       };
       spread(fetch(v));
-      int nxt = MODE == kOutputStationary ? fetch(next_present(m, v, V)) : -1;
+      // neighbour indices of the next kAhead present offsets, loads in flight
+      int va[kAhead], na[kAhead];
+      {
+        int vv = v;
+#pragma unroll
+        for (int d = 0; d < kAhead; ++d) {
+          vv = MODE == kOutputStationary ? next_present(m, vv, V) : V;
+          va[d] = vv;
+          na[d] = MODE == kOutputStationary ? fetch(vv) : -1;
+        }
+      }
       int pnl = 0;
       for (int kb = 0; kb < nkb; kb += G, ++it) {
         const int s = static_cast<int>(it % S);
@@ -470,10 +485,16 @@ __global__ void __launch_bounds__((NPW + 6) * 32, NPW == 4 ? 3 : (NPW == 8 ? 2 :
           if (++pnl == P) {
             pnl = 0;
             if (MODE == kOutputStationary) {
-              v = next_present(m, v, V);
+              v = va[0];
               if (v < V) {
-                spread(nxt);
-                nxt = fetch(next_present(m, v, V));
+                spread(na[0]);
+#pragma unroll
+                for (int d = 0; d + 1 < kAhead; ++d) {
+                  va[d] = va[d + 1];
+                  na[d] = na[d + 1];
+                }
+                va[kAhead - 1] = next_present(m, va[kAhead - 1], V);
+                na[kAhead - 1] = fetch(va[kAhead - 1]);
               }
             }
           }
