@@ -103,13 +103,14 @@ def load_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
 
 
-def recorded_traffic(kernel: str):
-    """DRAM bytes per launch from a committed ncu summary, or None if absent
-    or taken on a different version of the kernel's source file."""
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` on `workload` from a committed ncu
+    summary, or None if absent or taken on a different version of the
+    kernel's source file."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
-    d = json.load(open(p)).get(kernel)
+    d = json.load(open(p)).get(f"{kernel}@{workload}")
     if not d:
         return None
     src = os.path.join(ROOT, d["source"])
@@ -416,7 +417,7 @@ def run_ours(args):
     roofline = {"kernel": dom, "launches_timed": prof[dom][0], "bound": "hbm", "achieved": round(achieved, 1) if achieved else None,
                 "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / peaks["hbm_gbs"], 4) if achieved else None,
-                "traffic": recorded_traffic(dom), "peak_source": f"{peaks['source']} hbm_gbs",
+                "traffic": recorded_traffic(dom, w.name), "peak_source": f"{peaks['source']} hbm_gbs",
                 "algorithmic_bytes_per_launch": ab}
     # each layer's roofline time: the slower of its FLOPs at tensor peak and
     # its gathered bytes at HBM bandwidth; summed over the layers of a step
