@@ -61,6 +61,12 @@ def _load():
                                          P, ctypes.c_int]
         lib.oracle_subm_conv.restype = ctypes.c_int
         lib.oracle_max_threads.restype = ctypes.c_int
+        lib.oracle_subm_conv_bwd_data.argtypes = [P, ctypes.c_int64, ctypes.c_int, ctypes.c_int, P, P, P,
+                                                  ctypes.c_int, ctypes.c_int, P, ctypes.c_int]
+        lib.oracle_subm_conv_bwd_data.restype = ctypes.c_int
+        lib.oracle_subm_conv_bwd_weight.argtypes = [P, ctypes.c_int64, ctypes.c_int, ctypes.c_int, P, P, P,
+                                                    ctypes.c_int, ctypes.c_int, P, ctypes.c_int]
+        lib.oracle_subm_conv_bwd_weight.restype = ctypes.c_int
         lib.oracle_hash_only.argtypes = [P, ctypes.c_int64, ctypes.c_int, ctypes.c_int, P]
         lib.oracle_hash_only.restype = ctypes.c_int
         _lib = lib
@@ -160,6 +166,39 @@ def subm_conv(coords, feats, W, ndim: int, K: int, dims, relu: bool = False,
     out = np.empty((nrows, c_out), dtype=np.float64)
     st = _load().oracle_subm_conv(_ptr(c), n, ndim, K, _ptr(_dims(dims)), _ptr(f), _ptr(w),
                                   c_in, c_out, int(bool(relu)), _ptr(r), nrows, _ptr(out), threads)
+    if st:
+        raise OracleError(st)
+    return out
+
+
+def subm_conv_bwd_data(coords, gout, W, ndim: int, K: int, dims, threads: int = 0) -> np.ndarray:
+    """fp64 gradient with respect to the layer's input features [N, C_in],
+    given the gradient with respect to its output [N, C_out]."""
+    c = _coords(coords)
+    n = c.shape[0]
+    w = np.ascontiguousarray(np.asarray(W, dtype=np.float64))
+    V, c_in, c_out = w.shape
+    g = np.ascontiguousarray(np.asarray(gout, dtype=np.float64).reshape(n, c_out))
+    if V != volume(ndim, K):
+        raise OracleError(1)
+    out = np.empty((n, c_in), dtype=np.float64)
+    st = _load().oracle_subm_conv_bwd_data(_ptr(c), n, ndim, K, _ptr(_dims(dims)), _ptr(g), _ptr(w), c_in, c_out,
+                                           _ptr(out), threads)
+    if st:
+        raise OracleError(st)
+    return out
+
+
+def subm_conv_bwd_weight(coords, feats, gout, ndim: int, K: int, dims, threads: int = 0) -> np.ndarray:
+    """fp64 gradient with respect to the weights [K^ndim, C_in, C_out]."""
+    c = _coords(coords)
+    n = c.shape[0]
+    f = np.ascontiguousarray(np.asarray(feats, dtype=np.float64).reshape(n, -1))
+    g = np.ascontiguousarray(np.asarray(gout, dtype=np.float64).reshape(n, -1))
+    V = volume(ndim, K)
+    out = np.empty((V, f.shape[1], g.shape[1]), dtype=np.float64)
+    st = _load().oracle_subm_conv_bwd_weight(_ptr(c), n, ndim, K, _ptr(_dims(dims)), _ptr(f), _ptr(g), f.shape[1],
+                                             g.shape[1], _ptr(out), threads)
     if st:
         raise OracleError(st)
     return out

@@ -20,6 +20,9 @@
 //     sheet, "The map and the update rule").
 //   * Update rule: f_out(Q) += f_in(P) x W_d for every tuple (exam sheet, "The
 //     map and the update rule").  Accumulated here in fp64.
+//   * Backward (the layer is linear in f and in W): the gradients of a loss
+//     with respect to f and W follow from the same tuples, written out below
+//     as their plain definitions.
 //
 // Offsets are indexed lexicographically with the first spatial axis slowest:
 // idx(d) = sum_k (d_k + r) * K^(ndim-1-k), r = (K-1)/2.  In 2D the offsets act
@@ -183,6 +186,79 @@ int oracle_subm_conv(const int32_t* coords, int64_t n, int ndim, int K, const in
     }
     if (relu)
       for (int co = 0; co < c_out; ++co) acc[co] = acc[co] > 0.0 ? acc[co] : 0.0;
+  }
+  return OR_OK;
+}
+
+// Gradient with respect to the input features of the layer above (without
+// its ReLU): the layer is linear in f, out[q] = sum_d f[p(q,d)] W_d with
+// p(q,d) the row at c_q + d, so d loss / d f[p] = sum over the pairs (q, d)
+// with c_p = c_q + d of gout[q] W_d^T.  For each input row p and offset d the
+// output row is the one at c_p - d.  gout [n, c_out], W [V, c_in, c_out],
+// gin [n, c_in], fp64.
+int oracle_subm_conv_bwd_data(const int32_t* coords, int64_t n, int ndim, int K, const int32_t* dims,
+                              const double* gout, const double* W, int c_in, int c_out, double* gin,
+                              int nthreads) {
+  Problem P;
+  int st = setup(P, coords, n, ndim, K, dims);
+  if (st) return st;
+  if (c_in < 1 || c_out < 1 || !W || (n > 0 && (!gout || !gin))) return OR_BAD_ARG;
+  const int V = P.volume;
+  std::vector<int> neg(size_t(V) * 3);
+  for (int v = 0; v < V; ++v) {
+    offset_of(v, ndim, K, &neg[3 * v]);
+    for (int a = 0; a < 3; ++a) neg[3 * v + a] = -neg[3 * v + a];
+  }
+  const int nt = threads_to_use(nthreads);
+#pragma omp parallel for schedule(dynamic, 64) num_threads(nt)
+  for (int64_t p = 0; p < n; ++p) {
+    double* acc = gin + p * c_in;
+    for (int ci = 0; ci < c_in; ++ci) acc[ci] = 0.0;
+    for (int v = 0; v < V; ++v) {
+      const int32_t q = neighbour(P, p, &neg[3 * v]);  // the output at c_p - d
+      if (q < 0) continue;
+      const double* g = gout + int64_t(q) * c_out;
+      const double* w = W + int64_t(v) * c_in * c_out;
+      for (int ci = 0; ci < c_in; ++ci) {
+        const double* wrow = w + int64_t(ci) * c_out;
+        double sum = 0.0;
+        for (int co = 0; co < c_out; ++co) sum += wrow[co] * g[co];
+        acc[ci] += sum;
+      }
+    }
+  }
+  return OR_OK;
+}
+
+// Gradient with respect to the weights: d loss / d W_d = sum over the pairs
+// (q, d) with an input p at c_q + d of f[p]^T gout[q].  feats [n, c_in],
+// gout [n, c_out], dW [V, c_in, c_out], fp64; one offset per thread.
+int oracle_subm_conv_bwd_weight(const int32_t* coords, int64_t n, int ndim, int K, const int32_t* dims,
+                                const double* feats, const double* gout, int c_in, int c_out, double* dW,
+                                int nthreads) {
+  Problem P;
+  int st = setup(P, coords, n, ndim, K, dims);
+  if (st) return st;
+  if (c_in < 1 || c_out < 1 || !dW || (n > 0 && (!feats || !gout))) return OR_BAD_ARG;
+  const int V = P.volume;
+  std::vector<int> offs(size_t(V) * 3);
+  for (int v = 0; v < V; ++v) offset_of(v, ndim, K, &offs[3 * v]);
+  const int nt = threads_to_use(nthreads);
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nt)
+  for (int v = 0; v < V; ++v) {
+    double* acc = dW + int64_t(v) * c_in * c_out;
+    for (int64_t e = 0; e < int64_t(c_in) * c_out; ++e) acc[e] = 0.0;
+    for (int64_t q = 0; q < n; ++q) {
+      const int32_t p = neighbour(P, q, &offs[3 * v]);
+      if (p < 0) continue;
+      const double* f = feats + int64_t(p) * c_in;
+      const double* g = gout + q * c_out;
+      for (int ci = 0; ci < c_in; ++ci) {
+        const double a = f[ci];
+        double* row = acc + int64_t(ci) * c_out;
+        for (int co = 0; co < c_out; ++co) row[co] += a * g[co];
+      }
+    }
   }
   return OR_OK;
 }

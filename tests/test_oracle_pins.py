@@ -360,3 +360,98 @@ def test_stack_rounds_between_layers():
         np.testing.assert_array_equal(outs[li], y)
         x = y
     assert (outs[0] >= 0).all() and (outs[1] >= 0).all() and (outs[2] < 0).any()
+
+
+# ---------------------------------------------------------------------------
+# backward (the layer is linear in f and in W)
+# ---------------------------------------------------------------------------
+
+def dense_conv_grads(coords, feats, W, gout, ndim, K, dims):
+    """Gradients of sum(out * gout) for the fp64 dense convolution (torch
+    autograd) with zeros at inactive sites, outputs read at active sites:
+    (d/d feats at active sites, d/d W in the [V, C_in, C_out] layout)."""
+    r = K // 2
+    n, c_in = feats.shape
+    c_out = W.shape[2]
+    Wt = torch.from_numpy(W.copy()).requires_grad_(True)
+    gin = np.zeros((n, c_in))
+    total = 0
+    for b in np.unique(coords[:, 0]):
+        sel = np.nonzero(coords[:, 0] == b)[0]
+        c = torch.from_numpy(coords[sel].astype(np.int64))
+        if ndim == 3:
+            grid = torch.zeros((1, c_in) + tuple(dims), dtype=torch.float64)
+            grid[0, :, c[:, 1], c[:, 2], c[:, 3]] = torch.from_numpy(feats[sel]).T
+            grid.requires_grad_(True)
+            w = Wt.reshape(K, K, K, c_in, c_out).permute(4, 3, 0, 1, 2)
+            y = torch.nn.functional.conv3d(grid, w, padding=r)[0, :, c[:, 1], c[:, 2], c[:, 3]].T
+        else:
+            grid = torch.zeros((1, c_in, dims[0], dims[1]), dtype=torch.float64)
+            grid[0, :, c[:, 1], c[:, 2]] = torch.from_numpy(feats[sel]).T
+            grid.requires_grad_(True)
+            w = Wt.reshape(K, K, c_in, c_out).permute(3, 2, 0, 1)
+            y = torch.nn.functional.conv2d(grid, w, padding=r)[0, :, c[:, 1], c[:, 2]].T
+        loss = (y * torch.from_numpy(gout[sel])).sum()
+        g_grid, = torch.autograd.grad(loss, grid, retain_graph=True)
+        if ndim == 3:
+            gin[sel] = g_grid[0, :, c[:, 1], c[:, 2], c[:, 3]].T.numpy()
+        else:
+            gin[sel] = g_grid[0, :, c[:, 1], c[:, 2]].T.numpy()
+        total = total + loss
+    gW, = torch.autograd.grad(total, Wt)
+    return gin, gW.numpy()
+
+
+@pytest.mark.parametrize("ndim,K,dims,n,batches,cin,cout", [
+    (2, 3, (9, 11, 1), 30, 2, 5, 3), (3, 3, (7, 6, 5), 70, 2, 4, 6), (3, 5, (7, 7, 6), 60, 1, 3, 2),
+])
+def test_backward_equals_dense_conv_autograd(ndim, K, dims, n, batches, cin, cout):
+    coords = random_scene(17 + n, n, dims, ndim, batches)
+    rng = np.random.default_rng(3 * n)
+    f = rng.standard_normal((coords.shape[0], cin))
+    W = rng.standard_normal((K ** ndim, cin, cout))
+    g = rng.standard_normal((coords.shape[0], cout))
+    want_gin, want_gW = dense_conv_grads(coords, f, W, g, ndim, K, dims)
+    np.testing.assert_allclose(oracle.subm_conv_bwd_data(coords, g, W, ndim, K, dims), want_gin, rtol=1e-12,
+                               atol=1e-12)
+    np.testing.assert_allclose(oracle.subm_conv_bwd_weight(coords, f, g, ndim, K, dims), want_gW, rtol=1e-12,
+                               atol=1e-11)
+
+
+def test_backward_adjoint_identities():
+    """<conv_W(f), g> = <f, dgrad_W(g)> = <W, wgrad(f, g)> (bilinear form)."""
+    coords = random_scene(5, 120, (10, 9, 8), 3, 2)
+    rng = np.random.default_rng(11)
+    n = coords.shape[0]
+    f = rng.standard_normal((n, 6))
+    W = rng.standard_normal((27, 6, 5))
+    g = rng.standard_normal((n, 5))
+    lhs = float(np.sum(oracle.subm_conv(coords, f, W, 3, 3, (10, 9, 8)) * g))
+    mid = float(np.sum(f * oracle.subm_conv_bwd_data(coords, g, W, 3, 3, (10, 9, 8))))
+    rhs = float(np.sum(W * oracle.subm_conv_bwd_weight(coords, f, g, 3, 3, (10, 9, 8))))
+    assert abs(lhs - mid) <= 1e-9 * max(1.0, abs(lhs))
+    assert abs(lhs - rhs) <= 1e-9 * max(1.0, abs(lhs))
+
+
+def test_backward_closed_forms():
+    """Two sites at offset d: out[q] = f[q] W_c + f[p] W_d (c_p = c_q + d),
+    out[p] = f[p] W_c + f[q] W_-d, so d/d f[p] = g[p] W_c^T + g[q] W_d^T and
+    d/d W_d = f[p]^T g[q]; an offset with no pair gets a zero gradient."""
+    coords = np.array([[0, 2, 2, 2], [0, 3, 2, 1]], dtype=np.int32)  # p - q = (1, 0, -1)
+    q, p = 0, 1
+    d = oracle.offset_index((1, 0, -1), 3)
+    md = oracle.offset_index((-1, 0, 1), 3)
+    c = 13
+    rng = np.random.default_rng(2)
+    f = rng.standard_normal((2, 3))
+    W = rng.standard_normal((27, 3, 4))
+    g = rng.standard_normal((2, 4))
+    gin = oracle.subm_conv_bwd_data(coords, g, W, 3, 3, (6, 6, 6))
+    np.testing.assert_allclose(gin[p], W[c] @ g[p] + W[d] @ g[q], rtol=1e-13)
+    np.testing.assert_allclose(gin[q], W[c] @ g[q] + W[md] @ g[p], rtol=1e-13)
+    gW = oracle.subm_conv_bwd_weight(coords, f, g, 3, 3, (6, 6, 6))
+    np.testing.assert_allclose(gW[d], np.outer(f[p], g[q]), rtol=1e-13)
+    np.testing.assert_allclose(gW[md], np.outer(f[q], g[p]), rtol=1e-13)
+    np.testing.assert_allclose(gW[c], np.outer(f[p], g[p]) + np.outer(f[q], g[q]), rtol=1e-13)
+    others = [v for v in range(27) if v not in (d, md, c)]
+    assert np.all(gW[others] == 0)
