@@ -224,6 +224,35 @@ sc_status sc_subm_conv_tune(sc_kmap m, const void* d_feats, const void* d_W, voi
                             unsigned* chosen);
 
 /*
+ * Backward pass of a layer computed by sc_subm_conv_fwd without SC_RELU (for
+ * a ReLU layer, mask d_gout by the forward output first).  The layer is
+ * linear in feats and in W, so both gradients come from the same map:
+ *
+ * sc_subm_conv_bwd_data: d_gin[p, :] = sum over the tuples (p, q, d) of
+ *   d_gout[q, :] @ W[d]^T.  The tuple (p, q, d) of the forward map is the
+ *   tuple (q, p, -d) of the same map (mirror symmetry), so this is a
+ *   submanifold layer from c_out to c_in channels with weights
+ *   W'[idx(d)] = W[idx(-d)]^T, and it runs on the forward kernels (the weight
+ *   packing transposes and mirrors W).
+ *   d_gout [n, c_out], d_W [V, c_in, c_out] (the forward layer's weights),
+ *   d_gin [n, c_in]; c_in and c_out are the forward layer's.  flags: 0 or one
+ *   SC_VARIANT_*.
+ *
+ * sc_subm_conv_bwd_weight: d_dW[d] = sum over the tuples (p, q, d) of
+ *   d_feats[p, :]^T d_gout[q, :], accumulated in fp32 from the map's
+ *   per-offset lists (the identity for the centre) and rounded once to dtype.
+ *   d_feats [n, c_in], d_gout [n, c_out], d_dW [V, c_in, c_out].  flags: 0.
+ *   Synchronises once if the map's host counts are not yet known.
+ *
+ * The source pages show the forward layer only; these follow from it by
+ * differentiation.  Argument rules as for sc_subm_conv_fwd.
+ */
+sc_status sc_subm_conv_bwd_data(sc_kmap m, const void* d_gout, const void* d_W, void* d_gin, int c_in, int c_out,
+                                sc_dtype dtype, unsigned flags, sc_stream stream);
+sc_status sc_subm_conv_bwd_weight(sc_kmap m, const void* d_feats, const void* d_gout, void* d_dW, int c_in,
+                                  int c_out, sc_dtype dtype, unsigned flags, sc_stream stream);
+
+/*
  * The layer of sc_subm_conv_fwd, computed by its fused tensor-core kernel,
  * without allocating any memory.  The source pages have no counterpart: this
  * entry point exists for callers that cannot call cudaMalloc (or any

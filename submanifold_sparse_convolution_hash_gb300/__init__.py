@@ -15,6 +15,8 @@ from .binding import (  # noqa: F401
     profile_reset,
     sc_hash_build,
     sc_kmap_build,
+    sc_subm_conv_bwd_data,
+    sc_subm_conv_bwd_weight,
     sc_subm_conv_fwd,
     sc_subm_conv_tune,
 )

@@ -63,6 +63,8 @@ def lib():
             "sc_kmap_export": ([P, P, P, P, P, P], I32),
             "sc_kmap_destroy": ([P, P], I32),
             "sc_subm_conv_fwd": ([P, P, P, P, I32, I32, I32, U, P], I32),
+            "sc_subm_conv_bwd_data": ([P, P, P, P, I32, I32, I32, U, P], I32),
+            "sc_subm_conv_bwd_weight": ([P, P, P, P, I32, I32, I32, U, P], I32),
             "sc_subm_conv_tune": ([P, P, P, P, I32, I32, I32, U, I32, P, P], I32),
             "sc_subm_conv_fwd_noalloc": ([P, P, P, P, I32, I32, I32, U, P], I32),
             "sc_status_str": ([I32], ctypes.c_char_p),
@@ -86,6 +88,7 @@ def exported_symbols() -> list:
     return [n for n in ("sc_hash_build", "sc_hash_query", "sc_hash_info", "sc_hash_check", "sc_hash_destroy",
                         "sc_kmap_build", "sc_kmap_info", "sc_kmap_check", "sc_kmap_export", "sc_kmap_destroy",
                         "sc_subm_conv_fwd", "sc_subm_conv_tune", "sc_subm_conv_fwd_noalloc",
+                        "sc_subm_conv_bwd_data", "sc_subm_conv_bwd_weight",
                         "sc_status_str", "sc_last_error",
                         "sc_launch_count", "sc_profile_enable", "sc_profile_only", "sc_profile_collect",
                         "sc_profile_reset",
@@ -259,6 +262,47 @@ def sc_subm_conv_fwd(kmap: KernelMap, feats: torch.Tensor, W: torch.Tensor, out:
     _check(lib().sc_subm_conv_fwd(kmap._h, _ptr(f), _ptr(w), _ptr(out), c_in, c_out, dt, flags,
                                   _stream(stream)), "sc_subm_conv_fwd")
     return out
+
+
+def sc_subm_conv_bwd_data(kmap: KernelMap, gout: torch.Tensor, W: torch.Tensor, gin: torch.Tensor | None = None,
+                          variant: str | None = None, stream=None) -> torch.Tensor:
+    """Gradient of a (ReLU-free) layer's loss with respect to its input
+    features: gin[p] = sum over map tuples (p, q, d) of gout[q] @ W[d]^T."""
+    g = _dev(gout, "gout")
+    w = _dev(W, "W")
+    if g.dtype not in _DTYPES or w.dtype != g.dtype:
+        raise ValueError("gout and W must share one dtype: float32, float16 or bfloat16")
+    if w.dim() != 3 or w.shape[0] != kmap.volume or g.dim() != 2 or g.shape[1] != w.shape[2] or g.shape[0] != kmap.n:
+        raise ValueError("shapes must be gout [N, C_out], W [K^ndim, C_in, C_out]")
+    c_in, c_out = w.shape[1], w.shape[2]
+    if gin is None:
+        gin = torch.empty((kmap.n, c_in), dtype=g.dtype, device=g.device)
+    elif gin.dtype != g.dtype or tuple(gin.shape) != (kmap.n, c_in):
+        raise ValueError("gin must be [N, C_in] of the gout dtype")
+    _check(lib().sc_subm_conv_bwd_data(kmap._h, _ptr(g), _ptr(w), _ptr(_dev(gin, "gin")), c_in, c_out,
+                                       _DTYPES[g.dtype], VARIANTS[variant] if variant else 0, _stream(stream)),
+           "sc_subm_conv_bwd_data")
+    return gin
+
+
+def sc_subm_conv_bwd_weight(kmap: KernelMap, feats: torch.Tensor, gout: torch.Tensor, dW: torch.Tensor | None = None,
+                            stream=None) -> torch.Tensor:
+    """Gradient with respect to the weights: dW[d] = sum over map tuples
+    (p, q, d) of feats[p]^T gout[q]."""
+    f = _dev(feats, "feats")
+    g = _dev(gout, "gout")
+    if f.dtype not in _DTYPES or g.dtype != f.dtype:
+        raise ValueError("feats and gout must share one dtype: float32, float16 or bfloat16")
+    if f.dim() != 2 or g.dim() != 2 or f.shape[0] != kmap.n or g.shape[0] != kmap.n:
+        raise ValueError("shapes must be feats [N, C_in], gout [N, C_out]")
+    c_in, c_out = f.shape[1], g.shape[1]
+    if dW is None:
+        dW = torch.empty((kmap.volume, c_in, c_out), dtype=f.dtype, device=f.device)
+    elif dW.dtype != f.dtype or tuple(dW.shape) != (kmap.volume, c_in, c_out):
+        raise ValueError("dW must be [K^ndim, C_in, C_out] of the feats dtype")
+    _check(lib().sc_subm_conv_bwd_weight(kmap._h, _ptr(f), _ptr(g), _ptr(_dev(dW, "dW")), c_in, c_out,
+                                         _DTYPES[f.dtype], 0, _stream(stream)), "sc_subm_conv_bwd_weight")
+    return dW
 
 
 def sc_subm_conv_tune(kmap: KernelMap, feats: torch.Tensor, W: torch.Tensor, out: torch.Tensor | None = None,

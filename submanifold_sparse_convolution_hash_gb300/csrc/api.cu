@@ -560,6 +560,32 @@ sc_status sc_subm_conv_fwd(sc_kmap m, const void* d_feats, const void* d_W, void
   return run_variant(&m->k, a, variant);
 }
 
+sc_status sc_subm_conv_bwd_data(sc_kmap m, const void* d_gout, const void* d_W, void* d_gin, int c_in, int c_out,
+                                sc_dtype dtype, unsigned flags, sc_stream stream) {
+  // the input gradient is a submanifold layer with c_out -> c_in channels
+  sc_status st = check_conv_args(m, d_gout, d_W, d_gin, c_out, c_in, dtype);
+  if (st) return st;
+  if (flags & ~SC_VARIANT_MASK) return set_error(SC_ERR_INVALID_ARG, "bwd_data takes an SC_VARIANT_* flag only");
+  ConvArgs a{&m->k, d_gout, d_W, d_gin, c_out, c_in, dtype, false, reinterpret_cast<cudaStream_t>(stream)};
+  a.wt = true;
+  unsigned variant = flags & SC_VARIANT_MASK;
+  if (!variant) variant = default_variant(&m->k, a);
+  return run_variant(&m->k, a, variant);
+}
+
+sc_status sc_subm_conv_bwd_weight(sc_kmap m, const void* d_feats, const void* d_gout, void* d_dW, int c_in,
+                                  int c_out, sc_dtype dtype, unsigned flags, sc_stream stream) {
+  sc_status st = check_conv_args(m, d_feats, d_dW, d_gout, c_in, c_out, dtype);
+  if (st) return st;
+  if (flags) return set_error(SC_ERR_INVALID_ARG, "bwd_weight takes no flags");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (!m->k.host_valid) {
+    st = sync_host(&m->k, s);
+    if (st) return st;
+  }
+  return conv_bwd_weight(&m->k, d_feats, d_gout, d_dW, c_in, c_out, dtype, s);
+}
+
 sc_status sc_subm_conv_fwd_noalloc(sc_kmap m, const void* d_feats, const void* d_W, void* d_out, int c_in,
                                    int c_out, sc_dtype dtype, unsigned flags, sc_stream stream) {
   sc_status st = check_conv_args(m, d_feats, d_W, d_out, c_in, c_out, dtype);

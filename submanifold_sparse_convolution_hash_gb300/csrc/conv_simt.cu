@@ -34,7 +34,7 @@ template <typename T>
 __global__ void __launch_bounds__(256) k_conv_simt(const T* __restrict__ feats, const T* __restrict__ W,
                                                    T* __restrict__ out, const int* __restrict__ nbr,
                                                    const int* __restrict__ order, int64_t n, int V, int c_in,
-                                                   int c_out, int relu) {
+                                                   int c_out, int relu, int wt) {
   const int64_t total = n * c_out;
   for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
        idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -45,8 +45,13 @@ __global__ void __launch_bounds__(256) k_conv_simt(const T* __restrict__ feats, 
       const int j = __ldg(nbr + q * V + v);
       if (j < 0) continue;
       const T* f = feats + static_cast<int64_t>(j) * c_in;
-      const T* w = W + static_cast<int64_t>(v) * c_in * c_out + co;
-      for (int ci = 0; ci < c_in; ++ci) acc = fmaf(to_f(f[ci]), to_f(w[static_cast<int64_t>(ci) * c_out]), acc);
+      if (wt) {  // W'[v][ci][co] = W[V-1-v][co][ci]
+        const T* w = W + (static_cast<int64_t>(V - 1 - v) * c_out + co) * c_in;
+        for (int ci = 0; ci < c_in; ++ci) acc = fmaf(to_f(f[ci]), to_f(w[ci]), acc);
+      } else {
+        const T* w = W + static_cast<int64_t>(v) * c_in * c_out + co;
+        for (int ci = 0; ci < c_in; ++ci) acc = fmaf(to_f(f[ci]), to_f(w[static_cast<int64_t>(ci) * c_out]), acc);
+      }
     }
     if (relu) acc = fmaxf(acc, 0.0f);
     const int64_t dst = order ? static_cast<int64_t>(__ldg(order + q)) : q;
@@ -63,7 +68,7 @@ sc_status launch(const ConvArgs& a) {
   SC_LAUNCH("subm_conv_simt", a.stream,
             k_conv_simt<T><<<static_cast<int>(g), 256, 0, a.stream>>>(
                 static_cast<const T*>(a.feats), static_cast<const T*>(a.W), static_cast<T*>(a.out), a.m->nbr,
-                a.m->order, a.m->n, a.m->V, a.c_in, a.c_out, a.relu ? 1 : 0));
+                a.m->order, a.m->n, a.m->V, a.c_in, a.c_out, a.relu ? 1 : 0, a.wt ? 1 : 0));
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? SC_OK : set_cuda_error(e, "subm_conv_simt launch");
 }

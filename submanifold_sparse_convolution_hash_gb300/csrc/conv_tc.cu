@@ -685,10 +685,12 @@ __global__ void __launch_bounds__((NPW + 6) * 32, NPW == 4 ? 3 : (NPW == 8 ? 2 :
 }
 
 // W [V, c_in, c_out] -> per (offset, panel) image of c_out rows x BK channels,
-// K-major, chunk-swizzled exactly as the kernel's shared-memory B tile.
+// K-major, chunk-swizzled exactly as the kernel's shared-memory B tile.  With
+// wt, W is a forward layer's [V, c_out, c_in] and the image is that of
+// W'[v] = W[V-1-v]^T (the layer that maps output gradients to input ones).
 template <int BK>
 __global__ void __launch_bounds__(256) k_pack_weights(const uint16_t* __restrict__ W, uint8_t* __restrict__ img,
-                                                      int V, int c_in, int c_out) {
+                                                      int V, int c_in, int c_out, int wt) {
   constexpr int ROWB = BK * 2, CPR = ROWB / 16;
   const int P = c_in / BK;
   const int64_t total = static_cast<int64_t>(V) * P * c_out * CPR;
@@ -703,7 +705,8 @@ __global__ void __launch_bounds__(256) k_pack_weights(const uint16_t* __restrict
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       const int ci = pnl * BK + c * 8 + k;
-      e[k] = __ldg(W + (static_cast<int64_t>(v) * c_in + ci) * c_out + co);
+      e[k] = wt ? __ldg(W + (static_cast<int64_t>(V - 1 - v) * c_out + co) * c_in + ci)
+                : __ldg(W + (static_cast<int64_t>(v) * c_in + ci) * c_out + co);
     }
     uint4 w;
     w.x = e[0] | (static_cast<uint32_t>(e[1]) << 16);
@@ -888,9 +891,9 @@ sc_status pack_weights(const ConvArgs& a, int bk, uint8_t* img) {
   if (grid < 1) grid = 1;
   const uint16_t* W = static_cast<const uint16_t*>(a.W);
   switch (bk) {
-    case 64: SC_LAUNCH("pack_weights", a.stream, k_pack_weights<64><<<grid, 256, 0, a.stream>>>(W, img, V, a.c_in, a.c_out)); break;
-    case 32: SC_LAUNCH("pack_weights", a.stream, k_pack_weights<32><<<grid, 256, 0, a.stream>>>(W, img, V, a.c_in, a.c_out)); break;
-    default: SC_LAUNCH("pack_weights", a.stream, k_pack_weights<16><<<grid, 256, 0, a.stream>>>(W, img, V, a.c_in, a.c_out)); break;
+    case 64: SC_LAUNCH("pack_weights", a.stream, k_pack_weights<64><<<grid, 256, 0, a.stream>>>(W, img, V, a.c_in, a.c_out, a.wt ? 1 : 0)); break;
+    case 32: SC_LAUNCH("pack_weights", a.stream, k_pack_weights<32><<<grid, 256, 0, a.stream>>>(W, img, V, a.c_in, a.c_out, a.wt ? 1 : 0)); break;
+    default: SC_LAUNCH("pack_weights", a.stream, k_pack_weights<16><<<grid, 256, 0, a.stream>>>(W, img, V, a.c_in, a.c_out, a.wt ? 1 : 0)); break;
   }
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? SC_OK : set_cuda_error(e, "pack_weights launch");

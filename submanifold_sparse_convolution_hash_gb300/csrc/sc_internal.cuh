@@ -141,7 +141,12 @@ struct ConvArgs {
   sc_dtype dtype;
   bool relu;
   cudaStream_t stream;
+  // W holds a forward layer's weights [V, c_out, c_in] and the layer applied
+  // is its input gradient: W'[v] = W[V-1-v]^T (mirrored offset, transposed)
+  bool wt = false;
 };
+sc_status conv_bwd_weight(const KernelMap* m, const void* feats, const void* gout, void* dW, int c_in, int c_out,
+                          sc_dtype dtype, cudaStream_t s);
 sc_status conv_fused(const ConvArgs& a);
 sc_status conv_weight_stationary(const ConvArgs& a);
 sc_status conv_simt(const ConvArgs& a);
