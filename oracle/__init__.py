@@ -62,7 +62,7 @@ def _load():
         lib.oracle_subm_conv.restype = ctypes.c_int
         lib.oracle_max_threads.restype = ctypes.c_int
         lib.oracle_subm_conv_bwd_data.argtypes = [P, ctypes.c_int64, ctypes.c_int, ctypes.c_int, P, P, P,
-                                                  ctypes.c_int, ctypes.c_int, P, ctypes.c_int]
+                                                  ctypes.c_int, ctypes.c_int, P, ctypes.c_int64, P, ctypes.c_int]
         lib.oracle_subm_conv_bwd_data.restype = ctypes.c_int
         lib.oracle_subm_conv_bwd_weight.argtypes = [P, ctypes.c_int64, ctypes.c_int, ctypes.c_int, P, P, P,
                                                     ctypes.c_int, ctypes.c_int, P, ctypes.c_int]
@@ -171,9 +171,9 @@ def subm_conv(coords, feats, W, ndim: int, K: int, dims, relu: bool = False,
     return out
 
 
-def subm_conv_bwd_data(coords, gout, W, ndim: int, K: int, dims, threads: int = 0) -> np.ndarray:
-    """fp64 gradient with respect to the layer's input features [N, C_in],
-    given the gradient with respect to its output [N, C_out]."""
+def subm_conv_bwd_data(coords, gout, W, ndim: int, K: int, dims, rows=None, threads: int = 0) -> np.ndarray:
+    """fp64 gradient with respect to the layer's input features [len(rows) or
+    N, C_in], given the gradient with respect to its output [N, C_out]."""
     c = _coords(coords)
     n = c.shape[0]
     w = np.ascontiguousarray(np.asarray(W, dtype=np.float64))
@@ -181,9 +181,11 @@ def subm_conv_bwd_data(coords, gout, W, ndim: int, K: int, dims, threads: int = 
     g = np.ascontiguousarray(np.asarray(gout, dtype=np.float64).reshape(n, c_out))
     if V != volume(ndim, K):
         raise OracleError(1)
-    out = np.empty((n, c_in), dtype=np.float64)
+    r = None if rows is None else np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    nrows = n if r is None else r.shape[0]
+    out = np.empty((nrows, c_in), dtype=np.float64)
     st = _load().oracle_subm_conv_bwd_data(_ptr(c), n, ndim, K, _ptr(_dims(dims)), _ptr(g), _ptr(w), c_in, c_out,
-                                           _ptr(out), threads)
+                                           _ptr(r), nrows, _ptr(out), threads)
     if st:
         raise OracleError(st)
     return out

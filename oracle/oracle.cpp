@@ -195,14 +195,17 @@ int oracle_subm_conv(const int32_t* coords, int64_t n, int ndim, int K, const in
 // p(q,d) the row at c_q + d, so d loss / d f[p] = sum over the pairs (q, d)
 // with c_p = c_q + d of gout[q] W_d^T.  For each input row p and offset d the
 // output row is the one at c_p - d.  gout [n, c_out], W [V, c_in, c_out],
-// gin [n, c_in], fp64.
+// gin [nrows, c_in] for the listed input rows (all rows if rows == NULL), fp64.
 int oracle_subm_conv_bwd_data(const int32_t* coords, int64_t n, int ndim, int K, const int32_t* dims,
-                              const double* gout, const double* W, int c_in, int c_out, double* gin,
-                              int nthreads) {
+                              const double* gout, const double* W, int c_in, int c_out, const int64_t* rows,
+                              int64_t nrows, double* gin, int nthreads) {
   Problem P;
   int st = setup(P, coords, n, ndim, K, dims);
   if (st) return st;
   if (c_in < 1 || c_out < 1 || !W || (n > 0 && (!gout || !gin))) return OR_BAD_ARG;
+  if (!rows) nrows = n;
+  for (int64_t k = 0; k < nrows; ++k)
+    if (rows && (rows[k] < 0 || rows[k] >= n)) return OR_BAD_ARG;
   const int V = P.volume;
   std::vector<int> neg(size_t(V) * 3);
   for (int v = 0; v < V; ++v) {
@@ -211,8 +214,9 @@ int oracle_subm_conv_bwd_data(const int32_t* coords, int64_t n, int ndim, int K,
   }
   const int nt = threads_to_use(nthreads);
 #pragma omp parallel for schedule(dynamic, 64) num_threads(nt)
-  for (int64_t p = 0; p < n; ++p) {
-    double* acc = gin + p * c_in;
+  for (int64_t k = 0; k < nrows; ++k) {
+    const int64_t p = rows ? rows[k] : k;
+    double* acc = gin + k * c_in;
     for (int ci = 0; ci < c_in; ++ci) acc[ci] = 0.0;
     for (int v = 0; v < V; ++v) {
       const int32_t q = neighbour(P, p, &neg[3 * v]);  // the output at c_p - d

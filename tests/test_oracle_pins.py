@@ -455,3 +455,13 @@ def test_backward_closed_forms():
     np.testing.assert_allclose(gW[c], np.outer(f[p], g[p]) + np.outer(f[q], g[q]), rtol=1e-13)
     others = [v for v in range(27) if v not in (d, md, c)]
     assert np.all(gW[others] == 0)
+
+
+def test_backward_data_rows_subset_equals_full():
+    coords = random_scene(9, 80, (8, 8, 8), 3, 1)
+    rng = np.random.default_rng(4)
+    g = rng.standard_normal((coords.shape[0], 3))
+    W = rng.standard_normal((27, 5, 3))
+    full = oracle.subm_conv_bwd_data(coords, g, W, 3, 3, (8, 8, 8))
+    rows = np.array([0, 7, 3, 79, 41])
+    np.testing.assert_array_equal(oracle.subm_conv_bwd_data(coords, g, W, 3, 3, (8, 8, 8), rows=rows), full[rows])
