@@ -51,6 +51,9 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--backward", action="store_true",
+                    help="a training step: after the forward layers, the input and weight gradients of every "
+                         "layer (a seeded output gradient, ReLU masks applied)")
     ap.add_argument("--variant", choices=["fused", "ws", "simt"], default=None,
                     help="run every layer with this variant instead of the measured choice")
     return ap.parse_args()
@@ -313,6 +316,11 @@ def run_ours(args):
         x = outs[li]
     ntiles = (s.n + 31) // 32
 
+    if args.backward:
+        gout_last = torch.from_numpy(sc_scenes.features(w.seed + 99, s.n, layers[-1][1])).to(tdt).to(dev)
+        gins = [torch.empty((s.n, ci), dtype=tdt, device=dev) for ci, _ in layers]
+        dWs = [torch.empty_like(W) for W in Ws]
+
     def step():
         h = sc.sc_hash_build(coords)
         m = sc.sc_kmap_build(h, s.ndim, w.K, s.dims, sync=False)
@@ -320,6 +328,14 @@ def run_ours(args):
         for li, W in enumerate(Ws):
             sc.sc_subm_conv_fwd(m, xin, W, out=outs[li], relu=li + 1 < len(Ws), variant=variants[li])
             xin = outs[li]
+        if args.backward:
+            g = gout_last
+            for li in range(len(Ws) - 1, -1, -1):
+                if li + 1 < len(Ws):  # ReLU after this layer: pass the gradient where the output was positive
+                    g = g * (outs[li] > 0)
+                sc.sc_subm_conv_bwd_weight(m, feats if li == 0 else outs[li - 1], g, dW=dWs[li])
+                sc.sc_subm_conv_bwd_data(m, g, Ws[li], gin=gins[li], variant=variants[li])
+                g = gins[li]
         return h, m
 
     for _ in range(max(args.warmup, 3)):
@@ -398,7 +414,7 @@ def run_ours(args):
 
     value = n_total * args.steps / total_s / 1e6
     ms_per_step = 1e3 * total_s / args.steps
-    flops = sum(2.0 * M * ci * co for ci, co in layers)
+    flops = sum(2.0 * M * ci * co for ci, co in layers) * (3 if args.backward else 1)
     per_kernel = {}
     tot_all = sum(v[1] for v in prof_all.values()) or 1.0
     for k, (n_l, tot) in prof_all.items():
@@ -430,6 +446,7 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": w.name, "N": s.n, "map_size": M, "K": w.K, "layers": layers,
+                   "pass": "forward+backward" if args.backward else "forward",
                    "variant": variants, "variant_choice": "given" if args.variant else "measured", "l2": "flushed before every step (256 MB write, outside the events)",
                    "kmap_sync": False, "parallelism": "replicas" if world > 1 else "single"},
         "layer_tflops": round(flops / (conv_ms / 1e3) / 1e12, 3) if conv_ms else None,

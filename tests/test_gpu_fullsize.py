@@ -141,3 +141,31 @@ def test_eight_layer_stack_end_to_end_reduced_scale():
                                  w.dtype)
     assert_close(x, ref[-1], w.dtype, "eight layers end to end")
     m.check()
+
+
+@pytest.mark.parametrize("idx", [1, 2, 4])
+def test_full_size_input_gradient_on_sampled_rows(idx):
+    F = full(idx)
+    s, w = F.s, F.w
+    _, W = F.layer(0)
+    c_out = W.shape[2]
+    g = torch.from_numpy(scenes.features(w.seed + 50, s.n, c_out)).to(W.dtype).cuda()
+    gin = sc.sc_subm_conv_bwd_data(F.m, g, W)
+    torch.cuda.synchronize()
+    ref = oracle.subm_conv_bwd_data(s.coords, g.double().cpu().numpy(), W.double().cpu().numpy(), s.ndim, w.K,
+                                    s.dims, rows=F.rows)
+    assert_close(gin[torch.from_numpy(F.rows).cuda()], ref, w.dtype, f"workload {idx} input gradient")
+
+
+@pytest.mark.parametrize("idx", [1, 2])
+def test_full_size_weight_gradient(idx):
+    F = full(idx)
+    s, w = F.s, F.w
+    x, W = F.layer(0)
+    c_out = W.shape[2]
+    g = torch.from_numpy(scenes.features(w.seed + 51, s.n, c_out)).to(W.dtype).cuda()
+    dW = sc.sc_subm_conv_bwd_weight(F.m, x, g)
+    torch.cuda.synchronize()
+    ref = oracle.subm_conv_bwd_weight(s.coords, x.double().cpu().numpy(), g.double().cpu().numpy(), s.ndim, w.K,
+                                      s.dims)
+    assert_close(dW, ref, w.dtype, f"workload {idx} weight gradient")
