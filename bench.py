@@ -78,11 +78,14 @@ def layer_tensors(w, s):
 
 
 # ------------------------------------------------------------- algorithmic bytes --
-def algo_bytes_step(kernel: str, N: int, V: int, M: int, layers, s: int, ntiles: int):
+def algo_bytes_step(kernel: str, N: int, V: int, M: int, layers, s: int, ntiles: int, backward: bool = False):
     """Bytes a kernel must move at minimum in one step (summed over its
-    launches in that step); None for kernels without a stated model."""
+    launches in that step); None for kernels without a stated model.  With
+    `backward`, the convolution kernels also run each layer's input gradient
+    (a layer from c_out to c_in channels)."""
     lists = 8 * (M - N)
-    conv = sum(M * ci * s + N * co * s + 4 * N * V + V * ci * co * s for ci, co in layers)
+    conv_layers = list(layers) + ([(co, ci) for ci, co in layers] if backward else [])
+    conv = sum(M * ci * s + N * co * s + 4 * N * V + V * ci * co * s for ci, co in conv_layers)
     table = {
         # coords in; row keys out; one row slot per point
         "hash_insert": 16 * N + 8 * N + 4 * N,
@@ -90,10 +93,13 @@ def algo_bytes_step(kernel: str, N: int, V: int, M: int, layers, s: int, ntiles:
         "kmap_build": 8 * N + 4 * N * V + lists,
         "order_count": 8 * N,
         "order_scatter": 8 * N + 4 * N,
-        "pack_weights": sum(2 * V * ci * co * s for ci, co in layers),
+        "pack_weights": sum(2 * V * ci * co * s for ci, co in conv_layers),
         # gathered neighbour rows + one write per output row + neighbour table + weights
         "subm_conv_fused": conv,
         "subm_conv_simt": conv,
+        # weight gradient: both gathered rows of every tuple, the list indices
+        # (the centre list is implicit), the fp32 gradient written once
+        "subm_conv_wgrad": sum(M * (ci + co) * s + 4 * V * ci * co for ci, co in layers) + lists * len(layers),
     }
     return table.get(kernel)
 
@@ -425,7 +431,7 @@ def run_ours(args):
     map_names = ("hash_insert", "order_count", "order_partials", "order_apply", "order_scatter", "kmap_build")
     map_ms = sum(prof_all[k][1] for k in map_names if k in prof_all) / bd_steps
     peaks = load_peaks()
-    ab_step = algo_bytes_step(dom, s.n, V, M, layers, esize, ntiles)
+    ab_step = algo_bytes_step(dom, s.n, V, M, layers, esize, ntiles, args.backward)
     launches_per_step = prof[dom][0] / args.steps
     ab = ab_step / launches_per_step if ab_step else None
     avg_s = prof[dom][1] / prof[dom][0] / 1e3
@@ -435,11 +441,16 @@ def run_ours(args):
                 "frac": round(achieved / peaks["hbm_gbs"], 4) if achieved else None,
                 "traffic": recorded_traffic(dom, w.name), "peak_source": f"{peaks['source']} hbm_gbs",
                 "algorithmic_bytes_per_launch": ab}
-    # each layer's roofline time: the slower of its FLOPs at tensor peak and
-    # its gathered bytes at HBM bandwidth; summed over the layers of a step
-    conv_roof_s = sum(max(2.0 * M * ci * co / (peaks["bf16_tflops"] * 1e12),
-                          algo_bytes_step("subm_conv_fused", s.n, V, M, [(ci, co)], esize, ntiles)
-                          / (peaks["hbm_gbs"] * 1e9)) for ci, co in layers)
+    # each layer op's roofline time: the slower of its FLOPs at tensor peak
+    # and its algorithmic bytes at HBM bandwidth; summed over the ops of a
+    # step (forward layers; with --backward also their input and weight
+    # gradients)
+    def roof_s(kernel, ci, co):
+        return max(2.0 * M * ci * co / (peaks["bf16_tflops"] * 1e12),
+                   algo_bytes_step(kernel, s.n, V, M, [(ci, co)], esize, ntiles) / (peaks["hbm_gbs"] * 1e9))
+    conv_roof_s = sum(roof_s("subm_conv_fused", ci, co) for ci, co in layers)
+    if args.backward:
+        conv_roof_s += sum(roof_s("subm_conv_fused", co, ci) + roof_s("subm_conv_wgrad", ci, co) for ci, co in layers)
 
     line = {
         "metric": METRIC, "value": round(value, 4), "unit": "Mvoxels/s", "n_gpus": world, "steps": args.steps,

@@ -64,6 +64,10 @@ def test_bwd_data_matches_oracle(name, K, c_in, c_out, dtype, variant, order, so
 @pytest.mark.parametrize("name,K,c_in,c_out,dtype", [
     ("lidar", 3, 32, 32, "f16"), ("indoor", 3, 64, 64, "bf16"), ("batch", 3, 128, 256, "f16"),
     ("indoor", 5, 48, 16, "bf16"), ("uniform2d", 3, 16, 16, "f32"), ("lidar", 1, 16, 32, "f16"),
+    # tensor-core shapes: two M halves (c_in 256), padded M panels (c_in 192, 48),
+    # three N panels (c_out 48), wide N (c_out 128, 256), one accumulator buffer
+    ("batch", 3, 256, 256, "bf16"), ("indoor", 3, 64, 128, "f16"), ("lidar", 3, 192, 64, "bf16"),
+    ("lidar", 3, 32, 48, "f16"), ("indoor", 3, 128, 32, "bf16"), ("uniform2d", 5, 16, 32, "f16"),
 ])
 def test_bwd_weight_matches_oracle(name, K, c_in, c_out, dtype):
     s = SC[name]
