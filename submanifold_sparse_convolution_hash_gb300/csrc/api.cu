@@ -453,6 +453,7 @@ sc_status sc_kmap_build(sc_hash h, int ndim, int K, const int32_t dims[3], unsig
       {reinterpret_cast<void**>(&k.map_size), sizeof(int64_t)},
       {reinterpret_cast<void**>(&k.status), sizeof(int) * 4},
       {reinterpret_cast<void**>(&k.order), ordered && k.n > 0 ? sizeof(int) * n : 0},
+      {reinterpret_cast<void**>(&k.skeys), ordered && k.n > 0 ? sizeof(unsigned long long) * n : 0},
       {reinterpret_cast<void**>(&k.buckets), ordered && k.n > 0 ? sizeof(int) * kmap_order_buckets() : 0},
       {reinterpret_cast<void**>(&k.rowmask), sorted ? sizeof(unsigned) * n : 0},
       {reinterpret_cast<void**>(&k.sig_sel), sorted ? sizeof(int) * kmap_sig_bits() : 0},

@@ -32,13 +32,16 @@
 //     point's neighbourhood (8 for a 3x3x3 kernel, 27 for 5x5x5); one lookup
 //     returns a block's 8 rows, which are filed under their offsets in a
 //     shared-memory copy of the unit's block of the table;
-//   * count: a ballot per (offset, 32 points) gives the hits; one atomic
-//     per offset on that offset's cursor reserves the unit's run of entries;
-//   * emit: the (in, out) entries go to offset v's list at v * n + the
-//     reserved start + rank, so a unit's entries stay together in row order
-//     (the order of units inside a list is the order their atomics ran); the
-//     table block is written with 16-byte stores, and the unit's 128-bit mask
-//     of present offsets with it.
+//   * the table block is written with 16-byte stores;
+//   * count and emit, a warp per offset: a ballot per (offset, 32 points)
+//     gives the hits; one atomic per offset on that offset's cursor (a
+//     warp's atomics issued together, one per lane) reserves the unit's run
+//     of entries, and the (in, out) entries go to offset v's list at v * n +
+//     the reserved start + rank, so a unit's entries stay together in row
+//     order (the order of units inside a list is the order their atomics
+//     ran); then the unit's 128-bit mask of present offsets.
+// With the locality order the points' keys are read in that order (the
+// order kernel stores them sorted), one coalesced load per point.
 // The last block to finish turns the per-offset totals into the segment
 // offsets, the weight-stationary tile prefix and |M|.  The lists live in
 // fixed strides of n entries per offset; the CSR that the boundary exports is
@@ -261,12 +264,15 @@ __global__ void __launch_bounds__(256) k_order_apply(int* __restrict__ buckets, 
 
 __global__ void __launch_bounds__(256) k_order_scatter(const unsigned long long* __restrict__ keys, int64_t n,
                                                        OrderBits ob, const int* __restrict__ hash_status,
-                                                       int* __restrict__ cursors, int* __restrict__ order) {
+                                                       int* __restrict__ cursors, int* __restrict__ order,
+                                                       unsigned long long* __restrict__ skeys) {
   const int tb = order_total_bits(ob, hash_status);
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
-    const int pos = atomicAdd(cursors + order_bucket(__ldg(keys + i), ob, tb), 1);
+    const unsigned long long key = __ldg(keys + i);
+    const int pos = atomicAdd(cursors + order_bucket(key, ob, tb), 1);
     order[pos] = static_cast<int>(i);
+    skeys[pos] = key;  // the map build then reads keys in order, coalesced
   }
 }
 
@@ -301,6 +307,7 @@ __device__ __forceinline__ T block_inclusive_scan(T x, T* warp_sums, T* total) {
 struct BuildArgs {
   const unsigned long long* keys;  // [n] packed key of each input row
   const int* order;                // [n] or null
+  const unsigned long long* skeys; // [n] keys in that order (with order)
   int64_t n;
   const BlockEntry* table;
   uint32_t mask;                   // table capacity - 1
@@ -320,7 +327,7 @@ struct BuildArgs {
   int* sig_sel;                    // [kSigBits] offsets of the row signature, rarest first (with rowmask)
 };
 
-// Dynamic shared memory: s_tile [up * V] ints, s_bal [V * up / 32], s_base [V].
+// Dynamic shared memory: s_tile [up * V] ints, s_bal [V * up / 32].
 // Five blocks per SM (register budget): 2560 lookups in flight per SM.
 __global__ void __launch_bounds__(kThreads, 5) k_kmap_build(const BuildArgs a) {
   extern __shared__ int4 smem4[];
@@ -328,14 +335,15 @@ __global__ void __launch_bounds__(kThreads, 5) k_kmap_build(const BuildArgs a) {
   const int ngroups = up / 32;
   int* s_tile = reinterpret_cast<int*>(smem4);
   unsigned* s_bal = reinterpret_cast<unsigned*>(s_tile + up * V);
-  int* s_base = reinterpret_cast<int*>(s_bal + V * ngroups);
   __shared__ int s_last;
   __shared__ int s_row[128];
   __shared__ unsigned s_pres[4];
+  __shared__ unsigned s_rmask[128];
   __shared__ long long warp_sums[32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int kWarps = kThreads / 32;
   if (threadIdx.x < 4) s_pres[threadIdx.x] = 0u;
+  if (threadIdx.x < 128) s_rmask[threadIdx.x] = 0u;
   for (int e = threadIdx.x; e < up * V; e += kThreads) s_tile[e] = -1;
   __syncthreads();
   const int u = blockIdx.x;
@@ -351,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 5) k_kmap_build(const BuildArgs a) {
     const bool live = p < np;
     const int row = live ? (a.order ? __ldg(a.order + i0 + p) : static_cast<int>(i0 + p)) : -1;
     if (part == 0 && p < up) s_row[p] = row;
-    const unsigned long long ck = live ? __ldg(a.keys + row) : kEmptyKey;
+    const unsigned long long ck = live ? (a.order ? __ldg(a.skeys + i0 + p) : __ldg(a.keys + row)) : kEmptyKey;
     bool valid = ck != kEmptyKey;
     const int x = static_cast<int>((ck >> 32) & 0xFFFF), y = static_cast<int>((ck >> 16) & 0xFFFF),
               z = static_cast<int>(ck & 0xFFFF);
@@ -409,51 +417,68 @@ __global__ void __launch_bounds__(kThreads, 5) k_kmap_build(const BuildArgs a) {
   }
   __syncthreads();
 
-  // ---- count: hit ballots per (offset, 32 points); reserve each offset's
-  // run of list entries with one atomic on that offset's cursor
-  for (int q = warp; q < V * ngroups; q += kWarps) {
-    const int v = q / ngroups, g = q - v * ngroups;
-    const int j = s_tile[(g * 32 + lane) * V + v];
-    const unsigned b = __ballot_sync(0xffffffffu, v != centre && j >= 0);
-    if (lane == 0) s_bal[q] = b;
-  }
-  __syncthreads();
-  for (int v = threadIdx.x; v < V; v += kThreads) {
-    int cnt = 0;
-    for (int g = 0; g < ngroups; ++g) cnt += __popc(s_bal[v * ngroups + g]);
-    s_base[v] = cnt ? atomicAdd(a.cursors + v, cnt) : 0;
-    if (cnt && v < 128 && up == 128) atomicOr(s_pres + (v >> 5), 1u << (v & 31));
-  }
-  if (a.rowmask && threadIdx.x < np) {  // V <= 32: one word per row
-    unsigned mk = 0;
-    for (int v = 0; v < V; ++v)
-      if (v != centre && s_tile[threadIdx.x * V + v] >= 0) mk |= 1u << v;
-    a.rowmask[i0 + threadIdx.x] = mk;
-  }
-  __syncthreads();
-
-  // ---- emit: lists, the table block, the unit's present offsets
-  for (int q = warp; q < V * ngroups; q += kWarps) {
-    const unsigned b = s_bal[q];
-    if (!b) continue;
-    const int v = q / ngroups, g = q - v * ngroups;
-    int before = s_base[v];
-    for (int gg = 0; gg < g; ++gg) before += __popc(s_bal[v * ngroups + gg]);
-    if ((b >> lane) & 1u) {
-      const int64_t at = static_cast<int64_t>(v) * a.n + before + __popc(b & ((1u << lane) - 1u));
-      a.in_rows[at] = s_tile[(g * 32 + lane) * V + v];
-      a.out_rows[at] = s_row[g * 32 + lane];
-    }
-  }
+  // ---- the unit's block of the table: contiguous, i0 * V * 4 bytes is a multiple of 128
   {
-    // the unit's block of the table is contiguous: i0 * V * 4 bytes is a multiple of 128
     int* dst = a.nbr + i0 * V;
     const int items = np * V;
     const int n4 = items >> 2;
     for (int e = threadIdx.x; e < n4; e += kThreads) reinterpret_cast<int4*>(dst)[e] = reinterpret_cast<const int4*>(s_tile)[e];
     for (int e = (n4 << 2) + threadIdx.x; e < items; e += kThreads) dst[e] = s_tile[e];
   }
+
+  // ---- count and emit, warp by warp: warp w takes offsets w, w + 8, ...
+  // (up to 32 per round, lane k holding the k-th).  A ballot per 32-point
+  // group gives an offset's hits; the round's atomics on the offsets'
+  // cursors go out together, one per lane, and reserve each offset's run of
+  // list entries; the (in, out) entries then fill the runs in row order.
+  {
+    const unsigned lt = (1u << lane) - 1u;
+    unsigned rm[4] = {0u, 0u, 0u, 0u};  // offsets with a hit, for the rows g * 32 + lane
+    for (int vb = warp; vb < V; vb += kWarps * 32) {
+      const int nk = min(32, (V - vb + kWarps - 1) / kWarps);
+      int cnt_mine = 0;
+      for (int k = 0; k < nk; ++k) {
+        const int v = vb + kWarps * k;
+        int cnt = 0;
+        for (int g = 0; g < ngroups; ++g) {
+          const int j = s_tile[(g * 32 + lane) * V + v];
+          const unsigned b = __ballot_sync(0xffffffffu, v != centre && j >= 0);
+          if (lane == 0) s_bal[v * ngroups + g] = b;
+          cnt += __popc(b);
+        }
+        if (lane == k) cnt_mine = cnt;
+      }
+      int base_mine = 0;
+      if (lane < nk && cnt_mine > 0) {
+        const int v = vb + kWarps * lane;
+        base_mine = atomicAdd(a.cursors + v, cnt_mine);
+        if (v < 128 && up == 128) atomicOr(s_pres + (v >> 5), 1u << (v & 31));
+      }
+      __syncwarp();
+      for (int k = 0; k < nk; ++k) {
+        const int v = vb + kWarps * k;
+        int at0 = __shfl_sync(0xffffffffu, base_mine, k);
+        const int64_t lb = static_cast<int64_t>(v) * a.n;
+        for (int g = 0; g < ngroups; ++g) {
+          const unsigned b = s_bal[v * ngroups + g];
+          if ((b >> lane) & 1u) {
+            const int64_t at = lb + at0 + __popc(b & lt);
+            a.in_rows[at] = s_tile[(g * 32 + lane) * V + v];
+            a.out_rows[at] = s_row[g * 32 + lane];
+            if (v < 32) rm[g] |= 1u << v;
+          }
+          at0 += __popc(b);
+        }
+      }
+    }
+    if (a.rowmask) {  // V <= 32: one word per row
+      for (int g = 0; g < ngroups; ++g)
+        if (rm[g]) atomicOr(s_rmask + g * 32 + lane, rm[g]);
+    }
+  }
+  __syncthreads();
   if (up == 128 && threadIdx.x < 4) a.present[static_cast<int64_t>(u) * 4 + threadIdx.x] = s_pres[threadIdx.x];
+  if (a.rowmask && threadIdx.x < np) a.rowmask[i0 + threadIdx.x] = s_rmask[threadIdx.x];
 
   // ---- the last block: segment offsets, weight-stationary tile prefix, |M|
   __threadfence();
@@ -668,7 +693,7 @@ sc_status launch_kmap_build(const HashTable* h, KernelMap* m, cudaStream_t s) {
     SC_LAUNCH("order_partials", s, k_order_partials<<<kBucketBlocks, 256, 0, s>>>(m->buckets, partial));
     SC_LAUNCH("order_apply", s, k_order_apply<<<kBucketBlocks, 256, 0, s>>>(m->buckets, partial));
     SC_LAUNCH("order_scatter", s,
-              k_order_scatter<<<og, 256, 0, s>>>(h->keys, m->n, ob, h->status, m->buckets, m->order));
+              k_order_scatter<<<og, 256, 0, s>>>(h->keys, m->n, ob, h->status, m->buckets, m->order, m->skeys));
     e = cudaGetLastError();
     if (e != cudaSuccess) return set_cuda_error(e, "locality order launch");
   }
@@ -677,6 +702,7 @@ sc_status launch_kmap_build(const HashTable* h, KernelMap* m, cudaStream_t s) {
   BuildArgs a;
   a.keys = h->keys;
   a.order = m->order;
+  a.skeys = m->skeys;
   a.n = m->n;
   a.table = h->table;
   a.mask = static_cast<uint32_t>(h->capacity - 1);
@@ -699,7 +725,7 @@ sc_status launch_kmap_build(const HashTable* h, KernelMap* m, cudaStream_t s) {
   a.map_size = m->map_size;
   a.rowmask = m->rowmask;
   a.sig_sel = m->sig_sel;
-  const size_t smem = sizeof(int) * (static_cast<size_t>(m->up) * V + static_cast<size_t>(V) * (m->up / 32) + V);
+  const size_t smem = sizeof(int) * (static_cast<size_t>(m->up) * V + static_cast<size_t>(V) * (m->up / 32));
   if (smem > 48 * 1024) {  // set once per device: the largest the build ever asks for
     static bool done[64] = {false};
     int dev = 0;

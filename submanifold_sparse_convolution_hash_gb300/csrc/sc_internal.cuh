@@ -81,6 +81,7 @@ struct KernelMap {
   int up = 128;                      // points per map-build unit (128; 32 when V > 128)
   int nunits = 0;                    // map-build units
   int* order = nullptr;              // [n] input rows in locality order, or null: input order
+  unsigned long long* skeys = nullptr;  // [n] packed keys in locality order (with order)
   int* buckets = nullptr;            // counting-sort buckets of that order (+ scan partials)
   int* nbr = nullptr;                // [n, V], rows in the row order (position k = input row order[k])
   int64_t* offs = nullptr;           // [V+1]
