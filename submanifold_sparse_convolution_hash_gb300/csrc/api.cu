@@ -446,7 +446,7 @@ sc_status sc_kmap_build(sc_hash h, int ndim, int K, const int32_t dims[3], unsig
       {reinterpret_cast<void**>(&k.nbr), sizeof(int) * n * V},
       {reinterpret_cast<void**>(&k.in_rows), sizeof(int) * n * V},
       {reinterpret_cast<void**>(&k.out_rows), sizeof(int) * n * V},
-      {reinterpret_cast<void**>(&k.cursors), sizeof(int) * V},
+      {reinterpret_cast<void**>(&k.cursors), sizeof(int) * V * kCursorStride},
       {reinterpret_cast<void**>(&k.present), sizeof(unsigned) * 4 * ((n + 127) / 128)},
       {reinterpret_cast<void**>(&k.offs), sizeof(int64_t) * (V + 1)},
       {reinterpret_cast<void**>(&k.ws_tiles), sizeof(int) * (V + 1)},

@@ -318,7 +318,7 @@ struct BuildArgs {
   unsigned* present;               // [nunits, 4] (up == 128 only)
   int* in_rows;                    // [V, n] strided lists
   int* out_rows;
-  int* cursors;                    // [V] entries reserved so far in each offset's list
+  int* cursors;                    // [V * kCursorStride] entries reserved so far in each offset's list
   int* status;                     // [4]: map status, hash status copy, -, done counter
   int64_t* offs;                   // [V+1]
   int* ws_tiles;                   // [V+1]
@@ -451,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 5) k_kmap_build(const BuildArgs a) {
       int base_mine = 0;
       if (lane < nk && cnt_mine > 0) {
         const int v = vb + kWarps * lane;
-        base_mine = atomicAdd(a.cursors + v, cnt_mine);
+        base_mine = atomicAdd(a.cursors + v * kCursorStride, cnt_mine);
         if (v < 128 && up == 128) atomicOr(s_pres + (v >> 5), 1u << (v & 31));
       }
       __syncwarp();
@@ -491,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 5) k_kmap_build(const BuildArgs a) {
   long long carry = 0, carry_t = 0;
   for (int v0 = 0; v0 < V; v0 += kThreads) {
     const int v = v0 + threadIdx.x;
-    const long long cnt = v < V ? static_cast<long long>(__ldcg(a.cursors + v)) : 0;
+    const long long cnt = v < V ? static_cast<long long>(__ldcg(a.cursors + v * kCursorStride)) : 0;
     long long tot, tot_t;
     const long long inc = block_inclusive_scan<long long>(cnt, warp_sums, &tot);
     const long long tl = (cnt + kWsRows - 1) / kWsRows;
@@ -512,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 5) k_kmap_build(const BuildArgs a) {
     // the kSigBits least frequent offsets that occur at all, rarest first:
     // lane v holds (count, v); kSigBits rounds of a warp minimum (V <= 32)
     const long long none = 0x7FFFFFFFFFFFFFFFll;
-    const int c = lane < V && lane != centre ? __ldcg(a.cursors + lane) : 0;
+    const int c = lane < V && lane != centre ? __ldcg(a.cursors + lane * kCursorStride) : 0;
     long long key = c > 0 ? (static_cast<long long>(c) << 8) | lane : none;
     for (int k = 0; k < kSigBits; ++k) {
       long long mn = key;
@@ -697,7 +697,7 @@ sc_status launch_kmap_build(const HashTable* h, KernelMap* m, cudaStream_t s) {
     e = cudaGetLastError();
     if (e != cudaSuccess) return set_cuda_error(e, "locality order launch");
   }
-  e = cudaMemsetAsync(m->cursors, 0, sizeof(int) * V, s);
+  e = cudaMemsetAsync(m->cursors, 0, sizeof(int) * V * kCursorStride, s);
   if (e != cudaSuccess) return set_cuda_error(e, "kmap cursor clear");
   BuildArgs a;
   a.keys = h->keys;

@@ -88,7 +88,7 @@ struct KernelMap {
   int* in_rows = nullptr;            // [V, n]: offset v's list at v * n, offs[v+1] - offs[v] entries
   int* out_rows = nullptr;
   unsigned* present = nullptr;       // [ceil(n/128), 4] offsets (< 128) with a hit in each 128-row tile of the row order
-  int* cursors = nullptr;            // [V] list entries reserved per offset during the build
+  int* cursors = nullptr;            // [V * kCursorStride] list entries reserved per offset during the build
   // signature sort (V <= 32): the convolution walks rows in a second order
   unsigned* rowmask = nullptr;       // [n] offsets with a neighbour, per row of the table
   int* sig_sel = nullptr;            // [16] signature offsets, rarest first
@@ -105,6 +105,10 @@ struct KernelMap {
   int64_t map_size_host = -1;
   std::vector<ConvChoice> tuned;
 };
+
+// The map build's per-offset list cursors sit one per 128-byte line: every
+// build block adds to each of them, and atomics on one line serialise.
+constexpr int kCursorStride = 32;
 
 // Size of the fixed packed-weight buffer behind sc_subm_conv_fwd_noalloc.
 constexpr size_t kNoAllocWeightBytes = size_t(4) << 20;
