@@ -14,7 +14,11 @@ Pins (tests/test_oracle_pins.py): the pages' worked examples (the 4x5 and 5x5
 grids, the 11-tuple map with its 2/1/5/1/2 split, the quiz answer Q = (2, 2)),
 the (2L+1)^d dilation counts, mirror symmetry, brute force over all point
 pairs, and an fp64 dense convolution from ``torch.nn.functional`` read at the
-active sites.  No function here is parity-unpinned.
+active sites.  The regular / strided layers are pinned to the same grid
+examples (17 then 20 active cells, 30 map entries), the dilation counts,
+stride-2 closed forms, brute force, and the strided dense convolution (its
+values at the output sites and its support as the output set).  No function
+here is parity-unpinned.
 """
 from __future__ import annotations
 
@@ -69,6 +73,15 @@ def _load():
         lib.oracle_subm_conv_bwd_weight.restype = ctypes.c_int
         lib.oracle_hash_only.argtypes = [P, ctypes.c_int64, ctypes.c_int, ctypes.c_int, P]
         lib.oracle_hash_only.restype = ctypes.c_int
+        I64, I = ctypes.c_int64, ctypes.c_int
+        lib.oracle_conv_out_coords.argtypes = [P, I64, I, I, I, P, P, I64, P]
+        lib.oracle_conv_out_coords.restype = I
+        lib.oracle_conv_kmap.argtypes = [P, I64, P, I64, I, I, I, P, P, I]
+        lib.oracle_conv_kmap.restype = I
+        lib.oracle_conv.argtypes = [P, I64, P, I64, I, I, I, P, P, P, I, I, I, P, I]
+        lib.oracle_conv.restype = I
+        lib.oracle_conv_bwd_weight.argtypes = [P, I64, P, I64, I, I, I, P, P, P, I, I, P, I]
+        lib.oracle_conv_bwd_weight.restype = I
         _lib = lib
     return _lib
 
@@ -236,3 +249,77 @@ def subm_conv_stack(coords, feats, Ws, ndim: int, K: int, dims, dtype: str,
         outs.append(y)
         x = y
     return outs
+
+
+# --------------------------------------------------------------------------
+# Regular (stride 1: dilating) and strided layers: the output set differs
+# from the input set ("SparseConvNet: from hash table to rulebook", sections
+# 2 and 3).  Output o reads the input at stride * o + d through W_d.
+# --------------------------------------------------------------------------
+
+def conv_out_coords(coords, ndim: int, K: int, stride: int, dims) -> np.ndarray:
+    """Output sites int32 [N_out, 4] of a regular / strided layer, sorted by
+    (batch, x, y, z): every o with an active input at stride * o + d."""
+    c = _coords(coords)
+    n = c.shape[0]
+    cap = n * volume(ndim, K)
+    out = np.empty((max(cap, 1), 4), dtype=np.int32)
+    n_out = ctypes.c_int64(0)
+    st = _load().oracle_conv_out_coords(_ptr(c), n, ndim, K, stride, _ptr(_dims(dims)), _ptr(out), cap,
+                                        ctypes.byref(n_out))
+    if st:
+        raise OracleError(st)
+    return out[: n_out.value].copy()
+
+
+def conv_out_extent(dims, ndim: int, stride: int) -> tuple:
+    """Extents of the output grid: ceil(dims / stride) on the strided axes."""
+    d = list(_dims(dims))
+    axes = 3 if ndim == 3 else 2
+    return tuple((d[a] + stride - 1) // stride if a < axes else d[a] for a in range(3))
+
+
+def conv_kmap(coords, out_coords, ndim: int, K: int, stride: int, dims, threads: int = 0) -> np.ndarray:
+    """Neighbour table int32 [N_out, K^ndim]: input row at stride * c_q + d, or -1."""
+    c, o = _coords(coords), _coords(out_coords)
+    V = volume(ndim, K)
+    nbr = np.empty((o.shape[0], V), dtype=np.int32)
+    st = _load().oracle_conv_kmap(_ptr(c), c.shape[0], _ptr(o), o.shape[0], ndim, K, stride, _ptr(_dims(dims)),
+                                  _ptr(nbr), threads)
+    if st:
+        raise OracleError(st)
+    return nbr
+
+
+def sparse_conv(coords, out_coords, feats, W, ndim: int, K: int, stride: int, dims, relu: bool = False,
+                threads: int = 0) -> np.ndarray:
+    """fp64 output features [N_out, C_out] of one regular / strided layer."""
+    c, o = _coords(coords), _coords(out_coords)
+    n = c.shape[0]
+    f = np.ascontiguousarray(np.asarray(feats, dtype=np.float64).reshape(n, -1))
+    w = np.ascontiguousarray(np.asarray(W, dtype=np.float64))
+    V, c_in, c_out = w.shape
+    if V != volume(ndim, K) or f.shape[1] != c_in:
+        raise OracleError(1)
+    out = np.empty((o.shape[0], c_out), dtype=np.float64)
+    st = _load().oracle_conv(_ptr(c), n, _ptr(o), o.shape[0], ndim, K, stride, _ptr(_dims(dims)), _ptr(f), _ptr(w),
+                             c_in, c_out, int(bool(relu)), _ptr(out), threads)
+    if st:
+        raise OracleError(st)
+    return out
+
+
+def sparse_conv_bwd_weight(coords, out_coords, feats, gout, ndim: int, K: int, stride: int, dims,
+                           threads: int = 0) -> np.ndarray:
+    """fp64 weight gradient [K^ndim, C_in, C_out] of a regular / strided layer."""
+    c, o = _coords(coords), _coords(out_coords)
+    f = np.ascontiguousarray(np.asarray(feats, dtype=np.float64).reshape(c.shape[0], -1))
+    g = np.ascontiguousarray(np.asarray(gout, dtype=np.float64).reshape(o.shape[0], -1))
+    V = volume(ndim, K)
+    out = np.empty((V, f.shape[1], g.shape[1]), dtype=np.float64)
+    st = _load().oracle_conv_bwd_weight(_ptr(c), c.shape[0], _ptr(o), o.shape[0], ndim, K, stride,
+                                        _ptr(_dims(dims)), _ptr(f), _ptr(g), f.shape[1], g.shape[1], _ptr(out),
+                                        threads)
+    if st:
+        raise OracleError(st)
+    return out

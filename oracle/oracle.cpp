@@ -23,6 +23,12 @@
 //   * Backward (the layer is linear in f and in W): the gradients of a loss
 //     with respect to f and W follow from the same tuples, written out below
 //     as their plain definitions.
+//   * Regular and strided layers (the other output definition of
+//     "SparseConvNet: from hash table to rulebook", section 2): an output
+//     exists wherever the kernel window covers at least one active input, so
+//     the active set grows; with a stride s the output grid is coarser and
+//     output o reads the input at s * o + d through W_d (section 3's index
+//     relation between input, output, offset and stride).
 //
 // Offsets are indexed lexicographically with the first spatial axis slowest:
 // idx(d) = sum_k (d_k + r) * K^(ndim-1-k), r = (K-1)/2.  In 2D the offsets act
@@ -32,6 +38,7 @@
 // pages' worked examples, brute force over point pairs, and an fp64 dense
 // convolution from a library routine.  Nothing here is "parity unpinned".
 
+#include <algorithm>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -275,5 +282,188 @@ int oracle_hash_only(const int32_t* coords, int64_t n, int ndim, int K, const in
 
 // Number of threads the OpenMP runtime would use by default.
 int oracle_max_threads(void) { return threads_to_use(0); }
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Regular (stride 1: dilating) and strided sparse convolution.
+//
+// Output grid: extents ceil(dims / s) along the strided axes (x, y, and z in
+// 3D; in 2D z is carried unchanged, like the offsets).  Output o is active iff
+// some offset d puts an active input at s * o + d; the layer is
+// out[o] = sum over those d of f[input at s * o + d] W_d.  At s = 1 the output
+// set is the input set dilated by the kernel window.
+// ---------------------------------------------------------------------------
+
+namespace {
+
+int out_extent(int dim, int s) { return (dim + s - 1) / s; }
+
+// The input row at coordinate (b, x, y, z), or -1 (outside the grid: absent).
+int32_t input_at(const Problem& P, int64_t b, int64_t x, int64_t y, int64_t z) {
+  if (x < 0 || x >= P.dims[0] || y < 0 || y >= P.dims[1] || z < 0 || z >= P.dims[2]) return -1;
+  auto it = P.table.find(pack_key(b, x, y, z));
+  return it == P.table.end() ? -1 : it->second;
+}
+
+// The input row that output coordinate c_o reads through offset d.
+int32_t strided_neighbour(const Problem& P, const int32_t* c_o, int stride, const int d[3]) {
+  const int64_t sz = P.ndim == 3 ? stride : 1;
+  return input_at(P, c_o[0], int64_t(c_o[1]) * stride + d[0], int64_t(c_o[2]) * stride + d[1],
+                  int64_t(c_o[3]) * sz + d[2]);
+}
+
+int check_out_coords(const Problem& P, const int32_t* out_coords, int64_t n_out, int stride) {
+  if (n_out < 0 || (n_out > 0 && !out_coords)) return OR_BAD_ARG;
+  for (int64_t q = 0; q < n_out; ++q) {
+    const int32_t* c = out_coords + 4 * q;
+    if (c[1] < 0 || c[1] >= out_extent(P.dims[0], stride) || c[2] < 0 || c[2] >= out_extent(P.dims[1], stride))
+      return OR_OUT_OF_RANGE;
+    const int zext = P.ndim == 3 ? out_extent(P.dims[2], stride) : P.dims[2];
+    if (c[3] < 0 || c[3] >= zext || c[0] < 0) return OR_OUT_OF_RANGE;
+  }
+  return OR_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+// Output set of a regular / strided layer, sorted by (batch, x, y, z):
+// every o with an active input at s * o + d for some offset d.  Writes up to
+// `cap` rows of out_coords and the count to *n_out (OR_BAD_ARG if cap is too
+// small; *n_out still holds the count).
+int oracle_conv_out_coords(const int32_t* coords, int64_t n, int ndim, int K, int stride, const int32_t* dims,
+                           int32_t* out_coords, int64_t cap, int64_t* n_out) {
+  Problem P;
+  int st = setup(P, coords, n, ndim, K, dims);
+  if (st) return st;
+  if (stride < 1 || !n_out) return OR_BAD_ARG;
+  const int V = P.volume;
+  const int64_t sz = ndim == 3 ? stride : 1;
+  const int ext[3] = {out_extent(dims[0], stride), out_extent(dims[1], stride),
+                      ndim == 3 ? out_extent(dims[2], stride) : dims[2]};
+  std::vector<uint64_t> keys;
+  {
+    std::unordered_map<uint64_t, int> seen;
+    for (int64_t i = 0; i < n; ++i) {
+      const int32_t* c = coords + 4 * i;
+      for (int v = 0; v < V; ++v) {
+        int d[3];
+        offset_of(v, ndim, K, d);
+        // o with s * o + d = c_i, where it is a whole grid point inside the output grid
+        const int64_t px = int64_t(c[1]) - d[0], py = int64_t(c[2]) - d[1], pz = int64_t(c[3]) - d[2];
+        if (px % stride || py % stride || pz % sz) continue;
+        const int64_t o[3] = {px / stride, py / stride, pz / sz};
+        if (o[0] < 0 || o[0] >= ext[0] || o[1] < 0 || o[1] >= ext[1] || o[2] < 0 || o[2] >= ext[2]) continue;
+        const uint64_t key = pack_key(c[0], o[0], o[1], o[2]);
+        if (seen.emplace(key, 1).second) keys.push_back(key);
+      }
+    }
+  }
+  std::sort(keys.begin(), keys.end());
+  *n_out = int64_t(keys.size());
+  if (int64_t(keys.size()) > cap || (cap > 0 && !out_coords)) return OR_BAD_ARG;
+  for (size_t q = 0; q < keys.size(); ++q) {
+    out_coords[4 * q + 0] = int32_t(keys[q] >> 48);
+    out_coords[4 * q + 1] = int32_t((keys[q] >> 32) & 0xFFFF);
+    out_coords[4 * q + 2] = int32_t((keys[q] >> 16) & 0xFFFF);
+    out_coords[4 * q + 3] = int32_t(keys[q] & 0xFFFF);
+  }
+  return OR_OK;
+}
+
+// Neighbour table of a regular / strided layer: nbr[q * V + idx(d)] = row of
+// the input at s * c_q + d (c_q = out_coords row q), or -1.
+int oracle_conv_kmap(const int32_t* coords, int64_t n, const int32_t* out_coords, int64_t n_out, int ndim, int K,
+                     int stride, const int32_t* dims, int32_t* nbr, int nthreads) {
+  Problem P;
+  int st = setup(P, coords, n, ndim, K, dims);
+  if (st) return st;
+  if (stride < 1 || (n_out > 0 && !nbr)) return OR_BAD_ARG;
+  st = check_out_coords(P, out_coords, n_out, stride);
+  if (st) return st;
+  const int V = P.volume;
+  std::vector<int> offs(size_t(V) * 3);
+  for (int v = 0; v < V; ++v) offset_of(v, ndim, K, &offs[3 * v]);
+  const int nt = threads_to_use(nthreads);
+#pragma omp parallel for schedule(static) num_threads(nt)
+  for (int64_t q = 0; q < n_out; ++q)
+    for (int v = 0; v < V; ++v) nbr[q * V + v] = strided_neighbour(P, out_coords + 4 * q, stride, &offs[3 * v]);
+  return OR_OK;
+}
+
+// Output features of a regular / strided layer for every output row:
+// out[q, :] = sum over offsets d with an input p at s * c_q + d of f[p, :] W_d,
+// fp64, then max(., 0) if relu != 0.  feats [n, c_in], W [V, c_in, c_out],
+// out [n_out, c_out].
+int oracle_conv(const int32_t* coords, int64_t n, const int32_t* out_coords, int64_t n_out, int ndim, int K,
+                int stride, const int32_t* dims, const double* feats, const double* W, int c_in, int c_out, int relu,
+                double* out, int nthreads) {
+  Problem P;
+  int st = setup(P, coords, n, ndim, K, dims);
+  if (st) return st;
+  if (stride < 1 || c_in < 1 || c_out < 1 || !W || (n > 0 && !feats) || (n_out > 0 && !out)) return OR_BAD_ARG;
+  st = check_out_coords(P, out_coords, n_out, stride);
+  if (st) return st;
+  const int V = P.volume;
+  std::vector<int> offs(size_t(V) * 3);
+  for (int v = 0; v < V; ++v) offset_of(v, ndim, K, &offs[3 * v]);
+  const int nt = threads_to_use(nthreads);
+#pragma omp parallel for schedule(dynamic, 64) num_threads(nt)
+  for (int64_t q = 0; q < n_out; ++q) {
+    double* acc = out + q * c_out;
+    for (int co = 0; co < c_out; ++co) acc[co] = 0.0;
+    for (int v = 0; v < V; ++v) {
+      const int32_t p = strided_neighbour(P, out_coords + 4 * q, stride, &offs[3 * v]);
+      if (p < 0) continue;
+      const double* f = feats + int64_t(p) * c_in;
+      const double* w = W + int64_t(v) * c_in * c_out;
+      for (int ci = 0; ci < c_in; ++ci) {
+        const double a = f[ci];
+        const double* wrow = w + int64_t(ci) * c_out;
+        for (int co = 0; co < c_out; ++co) acc[co] += a * wrow[co];
+      }
+    }
+    if (relu)
+      for (int co = 0; co < c_out; ++co) acc[co] = acc[co] > 0.0 ? acc[co] : 0.0;
+  }
+  return OR_OK;
+}
+
+// Weight gradient of a regular / strided layer: d loss / d W_d = sum over the
+// output rows q with an input p at s * c_q + d of f[p]^T gout[q].
+// feats [n, c_in], gout [n_out, c_out], dW [V, c_in, c_out], fp64.
+int oracle_conv_bwd_weight(const int32_t* coords, int64_t n, const int32_t* out_coords, int64_t n_out, int ndim,
+                           int K, int stride, const int32_t* dims, const double* feats, const double* gout, int c_in,
+                           int c_out, double* dW, int nthreads) {
+  Problem P;
+  int st = setup(P, coords, n, ndim, K, dims);
+  if (st) return st;
+  if (stride < 1 || c_in < 1 || c_out < 1 || !dW || (n > 0 && !feats) || (n_out > 0 && !gout)) return OR_BAD_ARG;
+  st = check_out_coords(P, out_coords, n_out, stride);
+  if (st) return st;
+  const int V = P.volume;
+  std::vector<int> offs(size_t(V) * 3);
+  for (int v = 0; v < V; ++v) offset_of(v, ndim, K, &offs[3 * v]);
+  const int nt = threads_to_use(nthreads);
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nt)
+  for (int v = 0; v < V; ++v) {
+    double* acc = dW + int64_t(v) * c_in * c_out;
+    for (int64_t e = 0; e < int64_t(c_in) * c_out; ++e) acc[e] = 0.0;
+    for (int64_t q = 0; q < n_out; ++q) {
+      const int32_t p = strided_neighbour(P, out_coords + 4 * q, stride, &offs[3 * v]);
+      if (p < 0) continue;
+      const double* f = feats + int64_t(p) * c_in;
+      const double* g = gout + q * c_out;
+      for (int ci = 0; ci < c_in; ++ci) {
+        const double a = f[ci];
+        double* row = acc + int64_t(ci) * c_out;
+        for (int co = 0; co < c_out; ++co) row[co] += a * g[co];
+      }
+    }
+  }
+  return OR_OK;
+}
 
 }  // extern "C"

@@ -465,3 +465,199 @@ def test_backward_data_rows_subset_equals_full():
     full = oracle.subm_conv_bwd_data(coords, g, W, 3, 3, (8, 8, 8))
     rows = np.array([0, 7, 3, 79, 41])
     np.testing.assert_array_equal(oracle.subm_conv_bwd_data(coords, g, W, 3, 3, (8, 8, 8), rows=rows), full[rows])
+
+
+# ---------------------------------------------------------------------------
+# regular (dilating) and strided layers: the output set differs from the input
+# ("SparseConvNet: from hash table to rulebook", sections 2 and 3)
+# ---------------------------------------------------------------------------
+
+def dense_strided(coords, feats, W, ndim, K, stride, dims):
+    """fp64 dense convolution (torch, cross-correlation, zero padding r,
+    stride s) of each batch's scattered features: {batch: [c_out, *out_ext]}.
+    Output o reads the inputs at s * o + d, d in [-r, r]."""
+    r = K // 2
+    c_in, c_out = W.shape[1], W.shape[2]
+    res = {}
+    for b in np.unique(coords[:, 0]):
+        sel = np.nonzero(coords[:, 0] == b)[0]
+        c = torch.from_numpy(coords[sel].astype(np.int64))
+        f = torch.from_numpy(np.asarray(feats)[sel]).T
+        if ndim == 3:
+            grid = torch.zeros((1, c_in) + tuple(dims), dtype=torch.float64)
+            grid[0, :, c[:, 1], c[:, 2], c[:, 3]] = f
+            w = torch.from_numpy(W).reshape(K, K, K, c_in, c_out).permute(4, 3, 0, 1, 2).contiguous()
+            res[int(b)] = torch.nn.functional.conv3d(grid, w, padding=r, stride=stride)[0]
+        else:
+            # 2D: the planes z are independent; stride and offsets act on (x, y)
+            outs = []
+            for z in range(dims[2]):
+                grid = torch.zeros((1, c_in, dims[0], dims[1]), dtype=torch.float64)
+                m = c[:, 3] == z
+                grid[0, :, c[m, 1], c[m, 2]] = f[:, m]
+                w = torch.from_numpy(W).reshape(K, K, c_in, c_out).permute(3, 2, 0, 1).contiguous()
+                outs.append(torch.nn.functional.conv2d(grid, w, padding=r, stride=stride)[0])
+            res[int(b)] = torch.stack(outs, dim=-1)
+    return res
+
+
+def read_dense(res, out_coords):
+    c_out = next(iter(res.values())).shape[0]
+    rows = [res[int(b)][:, x, y, z].numpy() for b, x, y, z in out_coords]
+    return np.stack(rows) if rows else np.zeros((0, c_out))
+
+
+def test_regular_four_point_grid():
+    """17 of 20 cells after one dilating layer (empties (0,3), (0,4), (3,0)),
+    all 20 after a second; the first layer's map holds the 30 entries of the
+    zero-skipping count."""
+    g = read_golden("four_point_grid.txt")
+    kv = {r[0]: r[1:] for r in g}
+    grid, names, coords = grid_points(g)
+    dims = (grid[0], grid[1], 1)
+    one = oracle.conv_out_coords(coords, 2, 3, 1, dims)
+    assert len(one) == int(kv["dense_active_after_1"][0])
+    empty = {f"{i},{j}" for i in range(grid[0]) for j in range(grid[1])} - {f"{x},{y}" for _, x, y, _ in one}
+    assert empty == set(kv["dense_empty_after_1"])
+    two = oracle.conv_out_coords(one, 2, 3, 1, dims)
+    assert len(two) == int(kv["dense_active_after_2"][0])
+    nbr = oracle.conv_kmap(coords, one, 2, 3, 1, dims)
+    assert int((nbr >= 0).sum()) == int(kv["entries_zero_skipping"][0])
+    # the oracle's output set is the independent dense dilation of the grid
+    active = np.zeros(grid, dtype=bool)
+    active[coords[:, 1], coords[:, 2]] = True
+    assert {(x, y) for _, x, y, _ in one} == {tuple(ij) for ij in np.argwhere(dense_dilate(active, 3))}
+
+
+def test_regular_dilation_counts():
+    """One site grows to (2L+1)^d sites after L dilating layers of width 3."""
+    for row in read_golden("dilation.txt"):
+        ndim, L, want = int(row[1]), int(row[2]), int(row[3])
+        dims = (11, 11, 11 if ndim == 3 else 1)
+        c = np.array([[0, 5, 5, 5 if ndim == 3 else 0]], dtype=np.int32)
+        for _ in range(L):
+            c = oracle.conv_out_coords(c, ndim, 3, 1, dims)
+        assert len(c) == want == (2 * L + 1) ** ndim
+
+
+def test_strided_single_site_closed_forms():
+    """Stride 2, width 3: output o reads inputs 2o - 1 .. 2o + 1, so an odd
+    site 5 feeds o = 2 (offset +1) and o = 3 (offset -1) on each axis, an even
+    site 4 only o = 2 (offset 0)."""
+    dims = (11, 11, 11)
+    odd = oracle.conv_out_coords(np.array([[0, 5, 5, 5]]), 3, 3, 2, dims)
+    assert sorted(map(tuple, odd[:, 1:].tolist())) == sorted(itertools.product((2, 3), repeat=3))
+    nbr = oracle.conv_kmap(np.array([[0, 5, 5, 5]]), odd, 3, 3, 2, dims)
+    for (b, x, y, z), row in zip(odd, nbr):
+        d = tuple(5 - 2 * v for v in (x, y, z))
+        assert (row >= 0).sum() == 1 and row[oracle.offset_index(d, 3)] == 0
+    even = oracle.conv_out_coords(np.array([[0, 4, 4, 4]]), 3, 3, 2, dims)
+    assert even.tolist() == [[0, 2, 2, 2]]
+    # width 1, stride 2: only even sites have an output, at half the coordinate
+    pts = np.array([[0, 4, 6, 2], [0, 5, 6, 2], [1, 8, 0, 10]], dtype=np.int32)
+    o = oracle.conv_out_coords(pts, 3, 1, 2, dims)
+    assert o.tolist() == [[0, 2, 3, 1], [1, 4, 0, 5]]
+    assert oracle.conv_out_extent((11, 11, 11), 3, 2) == (6, 6, 6)
+    assert oracle.conv_out_extent((11, 10, 3), 2, 2) == (6, 5, 3)
+
+
+def brute_force_strided(coords, out_coords, ndim, K, stride, dims):
+    """(offset, out, in) for every pair with c_in - stride * c_out in
+    [-r, r]^ndim, same batch (and same plane in 2D)."""
+    r = K // 2
+    res = []
+    for q, co in enumerate(out_coords):
+        for p, ci in enumerate(coords):
+            if ci[0] != co[0] or (ndim == 2 and ci[3] != co[3]):
+                continue
+            d = ci[1:1 + ndim] - stride * co[1:1 + ndim]
+            if np.all(np.abs(d) <= r):
+                res.append((oracle.offset_index(d, K), q, p))
+    res.sort()
+    return np.array(res, dtype=np.int64).reshape(-1, 3)
+
+
+@pytest.mark.parametrize("ndim,K,stride,dims,n,batches", [
+    (2, 3, 1, (9, 8, 1), 25, 1), (2, 3, 2, (9, 8, 2), 30, 2), (2, 5, 3, (12, 10, 1), 30, 1),
+    (3, 3, 1, (6, 5, 6), 30, 2), (3, 3, 2, (7, 6, 5), 40, 1), (3, 5, 2, (6, 6, 6), 30, 1),
+    (3, 1, 2, (6, 6, 6), 30, 1), (3, 3, 3, (8, 7, 9), 40, 2),
+])
+def test_strided_map_equals_brute_force(ndim, K, stride, dims, n, batches):
+    c = random_scene(ndim * 100 + K * 10 + stride, n, dims, ndim, batches)
+    o = oracle.conv_out_coords(c, ndim, K, stride, dims)
+    t = oracle.tuples(oracle.conv_kmap(c, o, ndim, K, stride, dims))
+    assert np.array_equal(t, brute_force_strided(c, o, ndim, K, stride, dims))
+    # every output has at least one tuple; every input reaches an output when
+    # the windows s * o + [-r, r] tile the axis without gaps (s <= r + 1)
+    assert set(t[:, 1].tolist()) == set(range(len(o)))
+    if stride <= K // 2 + 1:
+        assert set(t[:, 2].tolist()) == set(range(len(c)))
+
+
+@pytest.mark.parametrize("ndim,K,stride,dims,n,batches,cin,cout", [
+    (2, 3, 1, (10, 9, 1), 30, 1, 3, 4), (2, 3, 2, (10, 9, 2), 40, 2, 2, 5), (2, 5, 2, (11, 12, 1), 30, 1, 4, 3),
+    (3, 3, 1, (7, 6, 5), 40, 2, 3, 2), (3, 3, 2, (8, 7, 6), 50, 1, 4, 4), (3, 5, 3, (9, 8, 7), 40, 1, 2, 3),
+    (3, 1, 2, (6, 6, 6), 80, 1, 3, 3),
+])
+def test_strided_conv_equals_dense_conv(ndim, K, stride, dims, n, batches, cin, cout):
+    c = random_scene(ndim * 1000 + K * 100 + stride, n, dims, ndim, batches)
+    rng = np.random.default_rng(7)
+    f = rng.standard_normal((c.shape[0], cin))
+    W = rng.standard_normal((K ** ndim, cin, cout))
+    o = oracle.conv_out_coords(c, ndim, K, stride, dims)
+    got = oracle.sparse_conv(c, o, f, W, ndim, K, stride, dims)
+    dense = dense_strided(c, f, W, ndim, K, stride, dims)
+    assert np.allclose(got, read_dense(dense, o), rtol=1e-12, atol=1e-12)
+    # the output set is the support of the dense layer on the active-site
+    # indicator with a kernel of ones
+    ind = dense_strided(c, np.ones((c.shape[0], 1)), np.ones((K ** ndim, 1, 1)), ndim, K, stride, dims)
+    support = sorted((b, *map(int, idx[1:])) for b, g in ind.items() for idx in np.argwhere(g.numpy() > 0.5))
+    assert [tuple(r) for r in o.tolist()] == support
+    relu = oracle.sparse_conv(c, o, f, W, ndim, K, stride, dims, relu=True)
+    assert np.array_equal(relu, np.maximum(got, 0.0))
+
+
+def test_strided_conv_at_stride_one_agrees_with_submanifold_on_input_sites():
+    c = random_scene(5, 60, (8, 7, 6), 3, 2)
+    rng = np.random.default_rng(3)
+    f = rng.standard_normal((c.shape[0], 3))
+    W = rng.standard_normal((27, 3, 2))
+    o = oracle.conv_out_coords(c, 3, 3, 1, (8, 7, 6))
+    full = oracle.sparse_conv(c, o, f, W, 3, 3, 1, (8, 7, 6))
+    at = {tuple(r): k for k, r in enumerate(o.tolist())}
+    idx = np.array([at[tuple(r)] for r in c.tolist()])
+    assert np.allclose(full[idx], oracle.subm_conv(c, f, W, 3, 3, (8, 7, 6)), rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("ndim,K,stride,dims,n,cin,cout", [
+    (3, 3, 2, (7, 6, 8), 40, 3, 2), (2, 3, 1, (9, 9, 1), 30, 2, 3), (3, 5, 2, (6, 7, 6), 30, 2, 2),
+])
+def test_strided_weight_gradient_equals_dense_autograd(ndim, K, stride, dims, n, cin, cout):
+    c = random_scene(ndim * 7 + K + stride, n, dims, ndim, 1)
+    rng = np.random.default_rng(11)
+    f = rng.standard_normal((c.shape[0], cin))
+    W = rng.standard_normal((K ** ndim, cin, cout))
+    o = oracle.conv_out_coords(c, ndim, K, stride, dims)
+    g = rng.standard_normal((o.shape[0], cout))
+    dW = oracle.sparse_conv_bwd_weight(c, o, f, g, ndim, K, stride, dims)
+    Wt = torch.from_numpy(W).requires_grad_(True)
+    r = K // 2
+    ext = oracle.conv_out_extent(dims, ndim, stride)
+    cc = torch.from_numpy(c.astype(np.int64))
+    oo = torch.from_numpy(o.astype(np.int64))
+    if ndim == 3:
+        grid = torch.zeros((1, cin) + tuple(dims), dtype=torch.float64)
+        grid[0, :, cc[:, 1], cc[:, 2], cc[:, 3]] = torch.from_numpy(f).T
+        w = Wt.reshape(K, K, K, cin, cout).permute(4, 3, 0, 1, 2)
+        y = torch.nn.functional.conv3d(grid, w, padding=r, stride=stride)[0]
+        gy = torch.zeros((cout,) + ext, dtype=torch.float64)
+        gy[:, oo[:, 1], oo[:, 2], oo[:, 3]] = torch.from_numpy(g).T
+    else:
+        grid = torch.zeros((1, cin, dims[0], dims[1]), dtype=torch.float64)
+        grid[0, :, cc[:, 1], cc[:, 2]] = torch.from_numpy(f).T
+        w = Wt.reshape(K, K, cin, cout).permute(3, 2, 0, 1)
+        y = torch.nn.functional.conv2d(grid, w, padding=r, stride=stride)[0]
+        gy = torch.zeros((cout,) + ext[:2], dtype=torch.float64)
+        gy[:, oo[:, 1], oo[:, 2]] = torch.from_numpy(g).T
+    (y * gy).sum().backward()
+    assert np.allclose(dW, Wt.grad.numpy(), rtol=1e-10, atol=1e-10)
