@@ -113,6 +113,42 @@ sc_status sc_hash_check(sc_hash h, sc_stream stream);
 /* Releases the handle's buffers stream-ordered on `stream`. */
 sc_status sc_hash_destroy(sc_hash h, sc_stream stream);
 
+/*
+ * Output set of a regular (stride 1) or strided sparse convolution layer, as
+ * a new hash handle over the output points.  "SparseConvNet: from hash table
+ * to rulebook", section 2, gives the regular output definition: an output is
+ * computed wherever the kernel window covers at least one active input, so
+ * the active set grows (at stride 1, by the window: "Sparse inputs and sparse
+ * convolution", section "What a dense convolution does to empty space");
+ * section 3 relates input, output and offset under a stride.  Here output o
+ * reads the input at stride * o + d, d in [-(K-1)/2, (K-1)/2]^ndim, and o is
+ * an output iff one of those inputs is active.
+ *
+ * in       the input points' hash.
+ * ndim     2 or 3; in 2D the offsets and the stride act on (x, y) and z is
+ *          carried unchanged.
+ * K        odd, in [1, 7].
+ * stride   in [1, 64].
+ * dims     the input grid's extents (x, y, z); the outputs lie on the grid
+ *          of extents ceil(dims / stride) on the strided axes.
+ * out      receives the output set: n = its point count (sc_hash_info),
+ *          row ids 0 .. n - 1 in an unspecified order (their coordinates:
+ *          sc_hash_coords).  It serves as the input hash of the next layer
+ *          and as the output set of sc_kmap_build_conv.  The caller destroys
+ *          it with sc_hash_destroy.
+ *
+ * Synchronises the stream (twice: the input hash's status, then the output
+ * count).  Errors: the input hash's latched errors; SC_ERR_TABLE_FULL if the
+ * output table would exceed 2^28 entries.  Device memory is allocated
+ * stream-ordered on `stream` and owned by the handle.
+ */
+sc_status sc_hash_build_conv_out(sc_hash in, int ndim, int K, int stride, const int32_t dims[3], sc_stream stream,
+                                 sc_hash* out);
+
+/* Coordinates of every row of the hash: d_coords int32 [n, 4] = (batch, x,
+ * y, z), device memory, 16-byte aligned, written asynchronously. */
+sc_status sc_hash_coords(sc_hash h, int32_t* d_coords, sc_stream stream);
+
 /* ---------------------------------------------------------- kernel map -- */
 
 /*
@@ -164,6 +200,26 @@ sc_status sc_hash_destroy(sc_hash h, sc_stream stream);
  */
 sc_status sc_kmap_build(sc_hash h, int ndim, int K, const int32_t dims[3], unsigned flags,
                         sc_stream stream, sc_kmap* out);
+
+/*
+ * Kernel map of a regular / strided layer: the rows are the points of
+ * `out_set` (from sc_hash_build_conv_out with the same ndim, K, stride and
+ * dims), and nbr[q*V + idx(d)] is the row p of `in` with coords[p] = stride *
+ * coords[q] + d, or -1 (absent neighbours and the grid's edges: zero
+ * padding).  The tuples (p, q, d) follow "SparseConvNet: from hash table to
+ * rulebook", section 3 (rulebook grouped by offset).  Unlike a submanifold
+ * map the centre offset is searched like the others and has its own list
+ * segment; |M| = offs[V].  The map keeps neither hash: both stay owned by
+ * the caller.  Flags as for sc_kmap_build except SC_KMAP_SORT
+ * (SC_ERR_UNSUPPORTED: the signature sort is for submanifold maps).
+ *
+ * sc_subm_conv_fwd and sc_subm_conv_bwd_weight take such a map: feats then
+ * has the input's n_in rows and out / gout the map's n rows.  The
+ * weight-stationary variant and sc_subm_conv_bwd_data return
+ * SC_ERR_UNSUPPORTED for it.
+ */
+sc_status sc_kmap_build_conv(sc_hash in, sc_hash out_set, int ndim, int K, int stride, const int32_t dims[3],
+                             unsigned flags, sc_stream stream, sc_kmap* out);
 
 /* n, V and |M| (centre included).  Synchronises the stream when |M| is not
  * yet known on the host. */

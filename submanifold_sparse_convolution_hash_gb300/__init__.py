@@ -14,7 +14,9 @@ from .binding import (  # noqa: F401
     profile_only,
     profile_reset,
     sc_hash_build,
+    sc_hash_build_conv_out,
     sc_kmap_build,
+    sc_kmap_build_conv,
     sc_subm_conv_bwd_data,
     sc_subm_conv_bwd_weight,
     sc_subm_conv_fwd,

@@ -57,6 +57,9 @@ def lib():
             "sc_hash_info": ([P, P, P], I32),
             "sc_hash_check": ([P, P], I32),
             "sc_hash_destroy": ([P, P], I32),
+            "sc_hash_build_conv_out": ([P, I32, I32, I32, P, P, P], I32),
+            "sc_hash_coords": ([P, P, P], I32),
+            "sc_kmap_build_conv": ([P, P, I32, I32, I32, P, U, P, P], I32),
             "sc_kmap_build": ([P, I32, I32, P, U, P, P], I32),
             "sc_kmap_info": ([P, P, P, P, P], I32),
             "sc_kmap_check": ([P, P], I32),
@@ -86,6 +89,7 @@ def lib():
 
 def exported_symbols() -> list:
     return [n for n in ("sc_hash_build", "sc_hash_query", "sc_hash_info", "sc_hash_check", "sc_hash_destroy",
+                        "sc_hash_build_conv_out", "sc_hash_coords", "sc_kmap_build_conv",
                         "sc_kmap_build", "sc_kmap_info", "sc_kmap_check", "sc_kmap_export", "sc_kmap_destroy",
                         "sc_subm_conv_fwd", "sc_subm_conv_tune", "sc_subm_conv_fwd_noalloc",
                         "sc_subm_conv_bwd_data", "sc_subm_conv_bwd_weight",
@@ -136,6 +140,12 @@ class Hash:
     def check(self, stream=None):
         _check(lib().sc_hash_check(self._h, _stream(stream)), "sc_hash_check")
 
+    def coords(self, stream=None) -> torch.Tensor:
+        """int32 [n, 4] (batch, x, y, z) of every row (sc_hash_coords)."""
+        out = torch.empty((self.n, 4), dtype=torch.int32, device=self.device)
+        _check(lib().sc_hash_coords(self._h, _ptr(out), _stream(stream)), "sc_hash_coords")
+        return out
+
     def destroy(self, stream=None):
         if self._h:
             lib().sc_hash_destroy(self._h, _stream(stream))
@@ -151,9 +161,13 @@ class Hash:
 class KernelMap:
     """Handle of a kernel map built by sc_kmap_build."""
 
-    def __init__(self, handle, n: int, ndim: int, K: int, dims, device):
+    def __init__(self, handle, n: int, ndim: int, K: int, dims, device, n_in: int | None = None,
+                 stride: int = 1):
         self._h = handle
         self.n = n
+        self.n_in = n if n_in is None else n_in
+        self.stride = stride
+        self.identity = n_in is None  # submanifold: the centre list is the identity
         self.ndim = ndim
         self.K = K
         self.volume = K ** ndim
@@ -180,9 +194,10 @@ class KernelMap:
         return out
 
     def lists(self, stream=None):
-        """(offs [V+1], in_rows [L], out_rows [L]) of the non-centre offsets."""
+        """(offs [V+1], in_rows [L], out_rows [L]): the per-offset lists (a
+        submanifold map's centre segment is empty, its tuples implicit)."""
         offs = self.offsets(stream)
-        L = self.map_size(stream) - self.n
+        L = self.map_size(stream) - (self.n if self.identity else 0)
         i = torch.empty(max(L, 0), dtype=torch.int32, device=self.device)
         o = torch.empty(max(L, 0), dtype=torch.int32, device=self.device)
         _check(lib().sc_kmap_export(self._h, None, None, _ptr(i) if L else None, _ptr(o) if L else None,
@@ -237,13 +252,43 @@ def sc_kmap_build(h: Hash, ndim: int, K: int, dims, sync: bool = True, order: bo
     return KernelMap(m, h.n, ndim, K, list(d), h.device)
 
 
+def sc_hash_build_conv_out(h: Hash, ndim: int, K: int, stride: int, dims, stream=None) -> Hash:
+    """Output set of a regular (stride 1: dilating) or strided layer over the
+    points of `h`: every o with an input at stride * o + d (synchronises)."""
+    d = (ctypes.c_int32 * 3)(*(list(dims) + [1] * (3 - len(dims))))
+    o = ctypes.c_void_p()
+    _check(lib().sc_hash_build_conv_out(h._h, ndim, K, stride, d, _stream(stream), ctypes.byref(o)),
+           "sc_hash_build_conv_out")
+    n = ctypes.c_int64()
+    cap = ctypes.c_int64()
+    lib().sc_hash_info(o, ctypes.byref(n), ctypes.byref(cap))
+    return Hash(o, n.value, cap.value, h.device)
+
+
+def sc_kmap_build_conv(h_in: Hash, h_out: Hash, ndim: int, K: int, stride: int, dims, sync: bool = True,
+                       order: bool | None = None, stream=None) -> KernelMap:
+    """Kernel map of a regular / strided layer: rows = the points of `h_out`,
+    neighbours = rows of `h_in` at stride * o + d."""
+    d = (ctypes.c_int32 * 3)(*(list(dims) + [1] * (3 - len(dims))))
+    m = ctypes.c_void_p()
+    flags = 0 if sync else SC_KMAP_NO_SYNC
+    if order is True:
+        flags |= SC_KMAP_ORDER
+    elif order is False:
+        flags |= SC_KMAP_NO_ORDER
+    _check(lib().sc_kmap_build_conv(h_in._h, h_out._h, ndim, K, stride, d, flags, _stream(stream), ctypes.byref(m)),
+           "sc_kmap_build_conv")
+    return KernelMap(m, h_out.n, ndim, K, list(d), h_in.device, n_in=h_in.n, stride=stride)
+
+
 def _conv_args(kmap, feats, W, out):
     f = _dev(feats, "feats")
     w = _dev(W, "W")
     if f.dtype not in _DTYPES or w.dtype != f.dtype:
         raise ValueError("feats and W must share one dtype: float32, float16 or bfloat16")
-    if w.dim() != 3 or w.shape[0] != kmap.volume or f.dim() != 2 or f.shape[1] != w.shape[1] or f.shape[0] != kmap.n:
-        raise ValueError("shapes must be feats [N, C_in], W [K^ndim, C_in, C_out]")
+    if (w.dim() != 3 or w.shape[0] != kmap.volume or f.dim() != 2 or f.shape[1] != w.shape[1]
+            or f.shape[0] != kmap.n_in):
+        raise ValueError("shapes must be feats [N_in, C_in], W [K^ndim, C_in, C_out]")
     c_out = w.shape[2]
     if out is None:
         out = torch.empty((kmap.n, c_out), dtype=f.dtype, device=f.device)
@@ -293,8 +338,8 @@ def sc_subm_conv_bwd_weight(kmap: KernelMap, feats: torch.Tensor, gout: torch.Te
     g = _dev(gout, "gout")
     if f.dtype not in _DTYPES or g.dtype != f.dtype:
         raise ValueError("feats and gout must share one dtype: float32, float16 or bfloat16")
-    if f.dim() != 2 or g.dim() != 2 or f.shape[0] != kmap.n or g.shape[0] != kmap.n:
-        raise ValueError("shapes must be feats [N, C_in], gout [N, C_out]")
+    if f.dim() != 2 or g.dim() != 2 or f.shape[0] != kmap.n_in or g.shape[0] != kmap.n:
+        raise ValueError("shapes must be feats [N_in, C_in], gout [N, C_out]")
     c_in, c_out = f.shape[1], g.shape[1]
     if dW is None:
         dW = torch.empty((kmap.volume, c_in, c_out), dtype=f.dtype, device=f.device)

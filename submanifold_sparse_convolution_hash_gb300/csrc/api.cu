@@ -15,7 +15,8 @@
 // The opaque handle types of sc.h.
 struct sc_hash_s {
   sc::HashTable t;
-  void* arena = nullptr;  // one device allocation: table, keys, status
+  void* arena = nullptr;   // one device allocation: table, keys, status (an output set: table, status)
+  void* arena2 = nullptr;  // an output set's keys (sized once its count is known), or null
 };
 struct sc_kmap_s {
   sc::KernelMap k;
@@ -212,7 +213,7 @@ sc_status check_conv_args(sc_kmap m, const void* feats, const void* W, const voi
   if ((st = check_dev_ptr(feats, 16, "feats"))) return st;
   if ((st = check_dev_ptr(out, 16, "out"))) return st;
   const size_t eb = dtype_bytes(dtype);
-  const uintptr_t f0 = reinterpret_cast<uintptr_t>(feats), f1 = f0 + m->k.n * c_in * eb;
+  const uintptr_t f0 = reinterpret_cast<uintptr_t>(feats), f1 = f0 + m->k.n_in * c_in * eb;
   const uintptr_t o0 = reinterpret_cast<uintptr_t>(out), o1 = o0 + m->k.n * c_out * eb;
   if (f0 < o1 && o0 < f1) return set_error(SC_ERR_INVALID_ARG, "out overlaps feats");
   return SC_OK;
@@ -220,6 +221,7 @@ sc_status check_conv_args(sc_kmap m, const void* feats, const void* W, const voi
 
 unsigned default_variant(KernelMap* m, const ConvArgs& a) {
   if (a.dtype == SC_F32) return SC_VARIANT_SIMT;
+  if (!m->identity) return fused_supported(a) ? SC_VARIANT_FUSED : SC_VARIANT_SIMT;
   for (const ConvChoice& c : m->tuned)
     if (c.c_in == a.c_in && c.c_out == a.c_out && c.dtype == a.dtype) return c.variant;
   return fused_supported(a) ? SC_VARIANT_FUSED : SC_VARIANT_WS;
@@ -232,6 +234,8 @@ sc_status run_variant(KernelMap* m, const ConvArgs& a, unsigned variant) {
     case SC_VARIANT_FUSED:
       return conv_fused(a);
     case SC_VARIANT_WS:
+      if (!m->identity)
+        return set_error(SC_ERR_UNSUPPORTED, "the weight-stationary kernel needs a submanifold map");
       if (!m->host_valid) {
         sc_status st = sync_host(m, a.stream);
         if (st) return st;
@@ -383,8 +387,42 @@ sc_status sc_hash_destroy(sc_hash h, sc_stream stream) {
   if (!h) return SC_OK;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   dev_free(h->arena, s);
+  dev_free(h->arena2, s);
   delete h;
   return SC_OK;
+}
+
+sc_status sc_hash_build_conv_out(sc_hash in, int ndim, int K, int stride, const int32_t dims[3], sc_stream stream,
+                                 sc_hash* out) {
+  if (!out) return set_error(SC_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (!in) return set_error(SC_ERR_INVALID_ARG, "hash handle is NULL");
+  if (ndim != 2 && ndim != 3) return set_error(SC_ERR_INVALID_ARG, "ndim must be 2 or 3");
+  if (K < 1 || K % 2 == 0 || K > 7) return set_error(SC_ERR_INVALID_ARG, "K must be odd and in [1, 7]");
+  if (stride < 1 || stride > 64) return set_error(SC_ERR_INVALID_ARG, "stride must be in [1, 64]");
+  if (!dims) return set_error(SC_ERR_INVALID_ARG, "dims is NULL");
+  for (int a = 0; a < 3; ++a)
+    if (dims[a] < 1 || dims[a] > 65535) return set_error(SC_ERR_INVALID_ARG, "dims must be in [1, 65535]");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // the inputs must be valid points inside dims before their outputs are derived
+  sc_status st = sc_hash_check(in, stream);
+  if (st) return st;
+  sc_hash h = new sc_hash_s();
+  st = launch_conv_out(&in->t, ndim, K, stride, dims, &h->t, &h->arena, &h->arena2, s);
+  if (st) {
+    sc_hash_destroy(h, stream);
+    return st;
+  }
+  *out = h;
+  return SC_OK;
+}
+
+sc_status sc_hash_coords(sc_hash h, int32_t* d_coords, sc_stream stream) {
+  if (!h) return set_error(SC_ERR_INVALID_ARG, "hash handle is NULL");
+  if (h->t.n == 0) return SC_OK;
+  sc_status st = check_dev_ptr(d_coords, 16, "coords");
+  if (st) return st;
+  return launch_hash_coords(&h->t, d_coords, reinterpret_cast<cudaStream_t>(stream));
 }
 
 // ------------------------------------------------------------------- map --
@@ -401,11 +439,19 @@ constexpr int64_t kOrderMinPoints = 262144;
 // ... and a signature sort of the convolution's rows (V <= 32).
 constexpr int64_t kSortMinPoints = 262144;
 
-sc_status sc_kmap_build(sc_hash h, int ndim, int K, const int32_t dims[3], unsigned flags, sc_stream stream,
-                        sc_kmap* out) {
+namespace {
+
+// The map of the points of `ho` against the table of `hi`: a submanifold map
+// when ho == hi and stride == 1 (the centre list is the identity), else the
+// map of a regular / strided layer.
+sc_status kmap_build_impl(sc_hash hi, sc_hash ho, int ndim, int K, int stride, const int32_t dims[3],
+                          unsigned flags, sc_stream stream, sc_kmap* out) {
   if (!out) return set_error(SC_ERR_INVALID_ARG, "out is NULL");
   *out = nullptr;
-  if (!h) return set_error(SC_ERR_INVALID_ARG, "hash handle is NULL");
+  if (!hi || !ho) return set_error(SC_ERR_INVALID_ARG, "hash handle is NULL");
+  if (stride < 1 || stride > 64) return set_error(SC_ERR_INVALID_ARG, "stride must be in [1, 64]");
+  const bool identity = hi == ho && stride == 1;
+  sc_hash h = ho;
   if (ndim != 2 && ndim != 3) return set_error(SC_ERR_INVALID_ARG, "ndim must be 2 or 3");
   if (K < 1 || K % 2 == 0) return set_error(SC_ERR_INVALID_ARG, "K must be odd and >= 1");
   int V = 1;
@@ -426,6 +472,9 @@ sc_status sc_kmap_build(sc_hash h, int ndim, int K, const int32_t dims[3], unsig
   sc_kmap m = new sc_kmap_s();
   KernelMap& k = m->k;
   k.n = h->t.n;
+  k.n_in = hi->t.n;
+  k.stride = stride;
+  k.identity = identity;
   k.ndim = ndim;
   k.K = K;
   k.V = V;
@@ -434,7 +483,7 @@ sc_status sc_kmap_build(sc_hash h, int ndim, int K, const int32_t dims[3], unsig
   k.nunits = static_cast<int>((k.n + k.up - 1) / k.up);
   const bool ordered = (flags & SC_KMAP_ORDER) || (!(flags & SC_KMAP_NO_ORDER) && k.n >= kOrderMinPoints);
   // the signature sort needs one mask word per row (V <= 32)
-  const bool sorted = V <= 32 && k.n > 0 &&
+  const bool sorted = identity && V <= 32 && k.n > 0 &&
                       ((flags & SC_KMAP_SORT) || (!(flags & SC_KMAP_NO_SORT) && k.n >= kSortMinPoints));
   const size_t nsig = sorted ? static_cast<size_t>(kmap_sig_buckets(k.n)) : 0;
   // every buffer of the map carved from one allocation, each 256-byte aligned
@@ -474,10 +523,10 @@ sc_status sc_kmap_build(sc_hash h, int ndim, int K, const int32_t dims[3], unsig
   // status[1] carries the hash's latched insert status from here on
   if (!st) {
     cudaError_t e = cudaMemsetAsync(k.status, 0, sizeof(int) * 4, s);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(k.status + 1, h->t.status, sizeof(int), cudaMemcpyDeviceToDevice, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(k.status + 1, hi->t.status, sizeof(int), cudaMemcpyDeviceToDevice, s);
     if (e != cudaSuccess) st = set_cuda_error(e, "kmap status init");
   }
-  if (!st) st = launch_kmap_build(&h->t, &k, s);
+  if (!st) st = launch_kmap_build(&hi->t, &h->t, &k, s);
   if (!st && !(flags & SC_KMAP_NO_SYNC)) st = sync_host(&k, s);
   if (st) {
     sc_kmap_destroy(m, stream);
@@ -485,6 +534,20 @@ sc_status sc_kmap_build(sc_hash h, int ndim, int K, const int32_t dims[3], unsig
   }
   *out = m;
   return SC_OK;
+}
+
+}  // namespace
+
+sc_status sc_kmap_build(sc_hash h, int ndim, int K, const int32_t dims[3], unsigned flags, sc_stream stream,
+                        sc_kmap* out) {
+  return kmap_build_impl(h, h, ndim, K, 1, dims, flags, stream, out);
+}
+
+sc_status sc_kmap_build_conv(sc_hash in, sc_hash out_set, int ndim, int K, int stride, const int32_t dims[3],
+                             unsigned flags, sc_stream stream, sc_kmap* out) {
+  if (flags & (SC_KMAP_SORT))
+    return set_error(SC_ERR_UNSUPPORTED, "the signature sort applies to submanifold maps only");
+  return kmap_build_impl(in, out_set, ndim, K, stride, dims, flags | SC_KMAP_NO_SORT, stream, out);
 }
 
 sc_status sc_kmap_info(sc_kmap m, int64_t* n, int32_t* volume, int64_t* map_size, sc_stream stream) {
@@ -563,6 +626,8 @@ sc_status sc_subm_conv_fwd(sc_kmap m, const void* d_feats, const void* d_W, void
 
 sc_status sc_subm_conv_bwd_data(sc_kmap m, const void* d_gout, const void* d_W, void* d_gin, int c_in, int c_out,
                                 sc_dtype dtype, unsigned flags, sc_stream stream) {
+  if (m && !m->k.identity)
+    return set_error(SC_ERR_UNSUPPORTED, "input gradient of a regular or strided layer: needs the transposed map");
   // the input gradient is a submanifold layer with c_out -> c_in channels
   sc_status st = check_conv_args(m, d_gout, d_W, d_gin, c_out, c_in, dtype);
   if (st) return st;
@@ -610,7 +675,8 @@ sc_status sc_subm_conv_tune(sc_kmap m, const void* d_feats, const void* d_W, voi
     cands.push_back(SC_VARIANT_SIMT);
   } else {
     if (fused_supported(a)) cands.push_back(SC_VARIANT_FUSED);
-    cands.push_back(SC_VARIANT_WS);
+    if (m->k.identity) cands.push_back(SC_VARIANT_WS);
+    if (cands.empty()) return set_error(SC_ERR_UNSUPPORTED, "no tensor-core variant for this layer");
   }
   cudaEvent_t e0 = nullptr, e1 = nullptr;
   cudaEventCreate(&e0);

@@ -55,13 +55,14 @@ template <typename T>
 __global__ void __launch_bounds__(256) k_wgrad(const T* __restrict__ feats, const T* __restrict__ gout,
                                                const int* __restrict__ in_rows, const int* __restrict__ out_rows,
                                                const int64_t* __restrict__ offs, int64_t n, int V, int c_in,
-                                               int c_out, float* __restrict__ dw) {
+                                               int c_out, int identity, float* __restrict__ dw) {
   __shared__ float s_f[kStep][kTile + 1];
   __shared__ float s_g[kStep][kTile + 1];
   __shared__ int s_p[kStep], s_q[kStep];
   const int v = blockIdx.y;
   const int centre = (V - 1) / 2;
-  const int64_t count = v == centre ? n : __ldg(offs + v + 1) - __ldg(offs + v);
+  const bool implicit = v == centre && identity;  // the identity list of a submanifold map
+  const int64_t count = implicit ? n : __ldg(offs + v + 1) - __ldg(offs + v);
   const int64_t e0 = static_cast<int64_t>(blockIdx.x) * kChunk;
   if (e0 >= count) return;
   const int64_t e1 = min(count, e0 + kChunk);
@@ -75,7 +76,7 @@ __global__ void __launch_bounds__(256) k_wgrad(const T* __restrict__ feats, cons
     if (threadIdx.x < kStep) {
       int p = -1, q = -1;
       if (threadIdx.x < ne) {
-        if (v == centre) {  // the identity: every row with itself
+        if (implicit) {  // every row with itself
           p = q = static_cast<int>(e + threadIdx.x);
         } else {
           p = __ldg(in_rows + lb + e + threadIdx.x);
@@ -152,12 +153,13 @@ struct WgParams {
   int a_half;            // bytes between A's two M = 128 halves
   uint32_t lbo_a, lbo_b; // bytes between panels (M / N atoms)
   int n_m;               // M halves (1 or 2)
+  int identity;          // the centre list is the identity (submanifold map)
   int stages, acc_cols, nbuf, tmem_cols;
   int* status;
 };
 
 __device__ __forceinline__ int64_t list_count(const WgParams& p, int v) {
-  return v == (p.V - 1) / 2 ? p.n : __ldg(p.offs + v + 1) - __ldg(p.offs + v);
+  return v == (p.V - 1) / 2 && p.identity ? p.n : __ldg(p.offs + v + 1) - __ldg(p.offs + v);
 }
 
 // Work unit u: chunk c = u / V of offset v = u % V, the list entries
@@ -245,7 +247,7 @@ __global__ void __launch_bounds__((NPW + 5) * 32, NPW == 4 ? 3 : 2) k_wgrad_tc(c
         const int t = kt * KT + t0w + lane;
         pp = qq = -1;
         if (lane < TW && t < len) {
-          if (v == centre) {
+          if (v == centre && p.identity) {
             pp = qq = static_cast<int>(e0 + t);
           } else {
             pp = __ldg(p.in_rows + lb + t);
@@ -488,6 +490,7 @@ sc_status wgrad_tc(const KernelMap* m, const WgPlan& pl, const void* feats, cons
   prm.c_in = c_in;
   prm.c_out = c_out;
   prm.status = m->status;
+  prm.identity = m->identity ? 1 : 0;
   // about four units per resident CTA, at least two K tiles each on average
   const int64_t total = m->map_size_host;
   const int64_t slots = static_cast<int64_t>(device_sm_count()) * pl.cps;
@@ -525,7 +528,8 @@ sc_status run(const KernelMap* m, const void* feats, const void* gout, void* dW,
                     static_cast<unsigned>(tiles));
     SC_LAUNCH("subm_conv_wgrad", s,
               k_wgrad<T><<<grid, 256, 0, s>>>(static_cast<const T*>(feats), static_cast<const T*>(gout), m->in_rows,
-                                              m->out_rows, m->offs, m->n, m->V, c_in, c_out, acc));
+                                              m->out_rows, m->offs, m->n, m->V, c_in, c_out,
+                                              m->identity ? 1 : 0, acc));
   }
   int g = static_cast<int>((count + 255) / 256);
   if (g > device_sm_count() * 16) g = device_sm_count() * 16;

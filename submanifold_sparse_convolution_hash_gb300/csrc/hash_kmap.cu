@@ -311,7 +311,9 @@ struct BuildArgs {
   int64_t n;
   const BlockEntry* table;
   uint32_t mask;                   // table capacity - 1
-  int V, K, ndim, dimx, dimy, dimz;
+  int V, K, ndim, dimx, dimy, dimz;  // dims: the grid of the table's (input) points
+  int stride;                      // query point o looks up the inputs at stride * o + d
+  int identity;                    // the centre list is the identity (submanifold: queries = inputs)
   int up;                          // points per unit (128, or 32 when V > 128)
   int nunits;
   int* nbr;                        // [n, V] in row order
@@ -361,8 +363,9 @@ __global__ void __launch_bounds__(kThreads, 5) k_kmap_build(const BuildArgs a) {
     if (part == 0 && p < up) s_row[p] = row;
     const unsigned long long ck = live ? (a.order ? __ldg(a.skeys + i0 + p) : __ldg(a.keys + row)) : kEmptyKey;
     bool valid = ck != kEmptyKey;
-    const int x = static_cast<int>((ck >> 32) & 0xFFFF), y = static_cast<int>((ck >> 16) & 0xFFFF),
-              z = static_cast<int>(ck & 0xFFFF);
+    // the neighbourhood's centre in the input grid: stride * o (z too in 3D)
+    const int x = static_cast<int>((ck >> 32) & 0xFFFF) * a.stride, y = static_cast<int>((ck >> 16) & 0xFFFF) * a.stride,
+              z = static_cast<int>(ck & 0xFFFF) * (a.ndim == 3 ? a.stride : 1);
     if (valid && (x >= a.dimx || y >= a.dimy || z >= a.dimz)) {
       if (part == 0) atomicOr(a.status, kDevErrRange);
       valid = false;
@@ -442,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 5) k_kmap_build(const BuildArgs a) {
         int cnt = 0;
         for (int g = 0; g < ngroups; ++g) {
           const int j = s_tile[(g * 32 + lane) * V + v];
-          const unsigned b = __ballot_sync(0xffffffffu, v != centre && j >= 0);
+          const unsigned b = __ballot_sync(0xffffffffu, (v != centre || !a.identity) && j >= 0);
           if (lane == 0) s_bal[v * ngroups + g] = b;
           cnt += __popc(b);
         }
@@ -506,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 5) k_kmap_build(const BuildArgs a) {
   if (threadIdx.x == 0) {
     a.offs[V] = carry;
     a.ws_tiles[V] = static_cast<int>(carry_t);
-    *a.map_size = a.n + carry;
+    *a.map_size = (a.identity ? a.n : 0) + carry;
   }
   if (a.rowmask && warp == 0) {
     // the kSigBits least frequent offsets that occur at all, rarest first:
@@ -617,6 +620,149 @@ __global__ void __launch_bounds__(256) k_compact_lists(const int* __restrict__ s
     dst[b + e] = __ldg(src + static_cast<int64_t>(v) * n + e);
 }
 
+// ------------------------------------------------------------ output sets --
+// Output set of a regular (stride 1: dilating) or strided layer: an output
+// wherever the kernel window covers an active input ("SparseConvNet: from
+// hash table to rulebook", section 2), output o reading the input at
+// stride * o + d (section 3's index relation under a stride).  Every input
+// marks each output o with stride * o + d at that input (d in [-r, r], o
+// inside the output grid) in a block table of the input table's layout; the
+// marked voxel slots are then counted per chunk of entries, scanned, and
+// numbered 0 .. n_out - 1 in table order, which turns the table into the
+// output set's hash table; each output's key is written with its number.
+
+constexpr int kOutChunk = 256 * 8;  // table entries per counting block (8 per thread)
+
+struct OutGrid {
+  int ex, ey, ez;  // output extents
+  int stride;      // on x, y (and z in 3D)
+  int r, rz;       // offset radius on x, y and on z (0 in 2D)
+  int sz;          // stride on z (1 in 2D: z is carried)
+};
+
+__device__ __forceinline__ void mark_output(BlockEntry* __restrict__ table, uint32_t mask, unsigned long long key,
+                                            int* __restrict__ status) {
+  const unsigned long long bk = block_key(key);
+  uint32_t h = block_home(bk, mask);
+  for (uint32_t probe = 0; probe <= mask; ++probe) {
+    unsigned long long k = __ldcg(&table[h].key);
+    if (k == kEmptyKey) {
+      k = atomicCAS(&table[h].key, kEmptyKey, bk);
+      if (k == kEmptyKey) k = bk;
+    }
+    if (k == bk) {
+      table[h].rows[block_local(key)] = 0;  // present, numbered later (every writer stores the same value)
+      return;
+    }
+    h = (h + 1) & mask;
+  }
+  atomicOr(status, kDevErrFull);
+}
+
+__global__ void __launch_bounds__(256) k_out_mark(const unsigned long long* __restrict__ keys, int64_t n,
+                                                  BlockEntry* __restrict__ table, uint32_t mask, OutGrid g,
+                                                  int* __restrict__ status) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+    const unsigned long long key = __ldg(keys + i);
+    if (key == kEmptyKey) continue;
+    const unsigned long long batch = key & 0xFFFF000000000000ull;
+    const int x = static_cast<int>((key >> 32) & 0xFFFF), y = static_cast<int>((key >> 16) & 0xFFFF),
+              z = static_cast<int>(key & 0xFFFF);
+    for (int dx = -g.r; dx <= g.r; ++dx) {
+      const int px = x - dx;  // stride * o_x
+      if (px < 0 || px % g.stride) continue;
+      const int ox = px / g.stride;
+      if (ox >= g.ex) continue;
+      for (int dy = -g.r; dy <= g.r; ++dy) {
+        const int py = y - dy;
+        if (py < 0 || py % g.stride) continue;
+        const int oy = py / g.stride;
+        if (oy >= g.ey) continue;
+        for (int dz = -g.rz; dz <= g.rz; ++dz) {
+          const int pz = z - dz;
+          if (pz < 0 || pz % g.sz) continue;
+          const int oz = pz / g.sz;
+          if (oz >= g.ez) continue;
+          mark_output(table, mask, batch | pack_key(0, ox, oy, oz), status);
+        }
+      }
+    }
+  }
+}
+
+// Marked slots of the 8 entries blockIdx.x * kOutChunk + k * 256 + threadIdx.x.
+__device__ __forceinline__ int count_marked(const BlockEntry* __restrict__ table, int64_t cap) {
+  int cnt = 0;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int64_t e = static_cast<int64_t>(blockIdx.x) * kOutChunk + k * 256 + threadIdx.x;
+    if (e >= cap) break;
+    const int4 a = __ldcg(reinterpret_cast<const int4*>(table[e].rows));
+    const int4 b = __ldcg(reinterpret_cast<const int4*>(table[e].rows + 4));
+    cnt += (a.x != -1) + (a.y != -1) + (a.z != -1) + (a.w != -1) + (b.x != -1) + (b.y != -1) + (b.z != -1) +
+           (b.w != -1);
+  }
+  return cnt;
+}
+
+__global__ void __launch_bounds__(256) k_out_count(const BlockEntry* __restrict__ table, int64_t cap,
+                                                   int* __restrict__ partial) {
+  __shared__ int warp_sums[32];
+  int tot;
+  block_inclusive_scan<int>(count_marked(table, cap), warp_sums, &tot);
+  if (threadIdx.x == 0) partial[blockIdx.x] = tot;
+}
+
+// Exclusive prefix of the chunk counts, in place; the total into *total.
+__global__ void __launch_bounds__(1024) k_out_scan(int* __restrict__ partial, int nchunks, int64_t* __restrict__ total) {
+  __shared__ long long warp_sums[32];
+  long long carry = 0;
+  for (int c0 = 0; c0 < nchunks; c0 += 1024) {
+    const int c = c0 + threadIdx.x;
+    const long long v = c < nchunks ? partial[c] : 0;
+    long long tot;
+    const long long inc = block_inclusive_scan<long long>(v, warp_sums, &tot);
+    if (c < nchunks) partial[c] = static_cast<int>(carry + inc - v);
+    carry += tot;
+  }
+  if (threadIdx.x == 0) *total = carry;
+}
+
+// Numbers the marked slots: chunk base + the thread's exclusive prefix, then
+// entry by entry in slot order; writes each number into its slot and the
+// voxel key under that number.
+__global__ void __launch_bounds__(256) k_out_number(BlockEntry* __restrict__ table, int64_t cap,
+                                                    const int* __restrict__ partial,
+                                                    unsigned long long* __restrict__ keys_out) {
+  __shared__ int warp_sums[32];
+  const int cnt = count_marked(table, cap);
+  int tot;
+  int id = __ldg(partial + blockIdx.x) + block_inclusive_scan<int>(cnt, warp_sums, &tot) - cnt;
+  for (int k = 0; k < 8; ++k) {
+    const int64_t e = static_cast<int64_t>(blockIdx.x) * kOutChunk + k * 256 + threadIdx.x;
+    if (e >= cap) break;
+    const unsigned long long bk = table[e].key;
+    for (int l = 0; l < 8; ++l) {
+      if (table[e].rows[l] == -1) continue;
+      table[e].rows[l] = id;
+      keys_out[id] = bk | (static_cast<unsigned long long>((l >> 2) & 1) << 32) |
+                     (static_cast<unsigned long long>((l >> 1) & 1) << 16) | static_cast<unsigned long long>(l & 1);
+      ++id;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256) k_hash_coords(const unsigned long long* __restrict__ keys, int64_t n,
+                                                     int4* __restrict__ coords) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+    const unsigned long long k = __ldg(keys + i);
+    coords[i] = make_int4(static_cast<int>(k >> 48), static_cast<int>((k >> 32) & 0xFFFF),
+                          static_cast<int>((k >> 16) & 0xFFFF), static_cast<int>(k & 0xFFFF));
+  }
+}
+
 int grid_for(int64_t n, int threads) {
   const int64_t cap = static_cast<int64_t>(device_sm_count()) * 32;
   int64_t g = (n + threads - 1) / threads;
@@ -662,7 +808,7 @@ sc_status launch_hash_query(const HashTable* h, const int32_t* q, int64_t m, int
   return e == cudaSuccess ? SC_OK : set_cuda_error(e, "hash_query launch");
 }
 
-sc_status launch_kmap_build(const HashTable* h, KernelMap* m, cudaStream_t s) {
+sc_status launch_kmap_build(const HashTable* in, const HashTable* h, KernelMap* m, cudaStream_t s) {
   const int V = m->V;
   cudaError_t e;
   if (m->n == 0) {
@@ -704,8 +850,10 @@ sc_status launch_kmap_build(const HashTable* h, KernelMap* m, cudaStream_t s) {
   a.order = m->order;
   a.skeys = m->skeys;
   a.n = m->n;
-  a.table = h->table;
-  a.mask = static_cast<uint32_t>(h->capacity - 1);
+  a.table = in->table;
+  a.mask = static_cast<uint32_t>(in->capacity - 1);
+  a.stride = m->stride;
+  a.identity = m->identity ? 1 : 0;
   a.V = V;
   a.K = m->K;
   a.ndim = m->ndim;
@@ -758,6 +906,82 @@ sc_status launch_kmap_build(const HashTable* h, KernelMap* m, cudaStream_t s) {
                                                                                 (V - 1) / 2, m->present));
   e = cudaGetLastError();
   return e == cudaSuccess ? SC_OK : set_cuda_error(e, "signature sort launch");
+}
+
+sc_status launch_hash_coords(const HashTable* h, int32_t* coords, cudaStream_t s) {
+  if (h->n == 0) return SC_OK;
+  SC_LAUNCH("hash_coords", s,
+            k_hash_coords<<<grid_for(h->n, 256), 256, 0, s>>>(h->keys, h->n, reinterpret_cast<int4*>(coords)));
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? SC_OK : set_cuda_error(e, "hash_coords launch");
+}
+
+sc_status launch_conv_out(const HashTable* in, int ndim, int K, int stride, const int32_t dims[3], HashTable* out,
+                          void** arena_table, void** arena_keys, cudaStream_t s) {
+  OutGrid g;
+  g.stride = stride;
+  g.r = (K - 1) / 2;
+  g.rz = ndim == 3 ? g.r : 0;
+  g.sz = ndim == 3 ? stride : 1;
+  g.ex = (dims[0] + stride - 1) / stride;
+  g.ey = (dims[1] + stride - 1) / stride;
+  g.ez = ndim == 3 ? (dims[2] + stride - 1) / stride : dims[2];
+  // table size: the blocks one input's outputs fall in (per axis: its
+  // floor(2r / stride) + 1 output positions span at most that / 2 + 1
+  // blocks), a quarter of that per input (neighbouring inputs share output
+  // blocks), at most half full; a full table is retried four times larger
+  const int span = (2 * g.r) / stride + 1, bpa = span / 2 + 1;
+  const int64_t per = static_cast<int64_t>(bpa) * bpa * (ndim == 3 ? bpa : 1);
+  int64_t cap = 16;
+  while (cap < 2 * (in->n * per / 4 + 1)) cap <<= 1;
+  const int64_t kMaxCap = int64_t(1) << 28;
+  int64_t n_out = 0;
+  for (;;) {
+    if (cap > kMaxCap) return set_error(SC_ERR_TABLE_FULL, "output set: table would exceed 2^28 entries");
+    const int nchunks = static_cast<int>((cap + kOutChunk - 1) / kOutChunk);
+    const size_t tb = sizeof(BlockEntry) * static_cast<size_t>(cap);
+    const size_t pb = (sizeof(int) * static_cast<size_t>(nchunks) + 255) & ~size_t(255);
+    sc_status st = dev_alloc(arena_table, tb + pb + 256, s);
+    if (st) return st;
+    uint8_t* b = static_cast<uint8_t*>(*arena_table);
+    BlockEntry* table = reinterpret_cast<BlockEntry*>(b);
+    int* partial = reinterpret_cast<int*>(b + tb);
+    int* status = reinterpret_cast<int*>(b + tb + pb);        // [4]: latched errors, largest batch id
+    int64_t* total = reinterpret_cast<int64_t*>(status + 4);  // output count
+    cudaError_t e = cudaMemsetAsync(table, 0xFF, tb, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(status, 0, 256, s);
+    // the outputs carry the inputs' batches: copy the largest batch id
+    if (e == cudaSuccess) e = cudaMemcpyAsync(status + 1, in->status + 1, sizeof(int), cudaMemcpyDeviceToDevice, s);
+    if (e != cudaSuccess) return set_cuda_error(e, "output set init");
+    const uint32_t mask = static_cast<uint32_t>(cap - 1);
+    if (in->n > 0)
+      SC_LAUNCH("out_mark", s, k_out_mark<<<grid_for(in->n, 256), 256, 0, s>>>(in->keys, in->n, table, mask, g, status));
+    SC_LAUNCH("out_count", s, k_out_count<<<nchunks, 256, 0, s>>>(table, cap, partial));
+    SC_LAUNCH("out_scan", s, k_out_scan<<<1, 1024, 0, s>>>(partial, nchunks, total));
+    int bits = 0;
+    e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&bits, status, sizeof(int), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&n_out, total, sizeof(int64_t), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return set_cuda_error(e, "output set count");
+    if (bits & kDevErrFull) {
+      dev_free(*arena_table, s);
+      *arena_table = nullptr;
+      cap <<= 2;
+      continue;
+    }
+    if (n_out >= (int64_t(1) << 31)) return set_error(SC_ERR_UNSUPPORTED, "output set: more than 2^31 - 1 points");
+    st = dev_alloc(arena_keys, sizeof(unsigned long long) * static_cast<size_t>(n_out > 0 ? n_out : 1), s);
+    if (st) return st;
+    out->n = n_out;
+    out->capacity = cap;
+    out->table = table;
+    out->status = status;
+    out->keys = static_cast<unsigned long long*>(*arena_keys);
+    SC_LAUNCH("out_number", s, k_out_number<<<nchunks, 256, 0, s>>>(table, cap, partial, out->keys));
+    e = cudaGetLastError();
+    return e == cudaSuccess ? SC_OK : set_cuda_error(e, "output set numbering");
+  }
 }
 
 sc_status kmap_compact_lists(const KernelMap* m, const int* src, int* dst, int64_t total, cudaStream_t s) {

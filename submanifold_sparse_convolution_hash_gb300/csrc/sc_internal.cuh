@@ -75,7 +75,10 @@ struct ConvChoice {
 };
 
 struct KernelMap {
-  int64_t n = 0;
+  int64_t n = 0;                     // rows of the map (output points)
+  int64_t n_in = 0;                  // rows of the input (= n for a submanifold map)
+  int stride = 1;                    // output o reads the inputs at stride * o + d
+  bool identity = true;              // submanifold: outputs = inputs, the centre list is the identity
   int ndim = 3, K = 3, V = 27;
   int dims[3] = {1, 1, 1};
   int up = 128;                      // points per map-build unit (128; 32 when V > 128)
@@ -129,7 +132,13 @@ int device_sm_count();
 sc_status launch_hash_insert(const int32_t* coords, int64_t n, HashTable* h, cudaStream_t s);
 sc_status launch_hash_query(const HashTable* h, const int32_t* q, int64_t m, int32_t* rows,
                             cudaStream_t s);
-sc_status launch_kmap_build(const HashTable* h, KernelMap* m, cudaStream_t s);
+// Map of the points of `out` against the table of `in` (out == in for a submanifold map).
+sc_status launch_kmap_build(const HashTable* in, const HashTable* out, KernelMap* m, cudaStream_t s);
+// Output set of a regular / strided layer as a new hash table `out` (its table
+// in *arena_table, its keys in *arena_keys); synchronises once to size it.
+sc_status launch_conv_out(const HashTable* in, int ndim, int K, int stride, const int32_t dims[3], HashTable* out,
+                          void** arena_table, void** arena_keys, cudaStream_t s);
+sc_status launch_hash_coords(const HashTable* h, int32_t* coords, cudaStream_t s);
 int kmap_unit_points(int V);
 sc_status kmap_compact_lists(const KernelMap* m, const int* src, int* dst, int64_t total, cudaStream_t s);
 int kmap_order_buckets();
