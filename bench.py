@@ -15,6 +15,10 @@ algorithmic bytes over its average event-timed launch duration against the
 measured HBM copy bandwidth.  `cpu_baseline` times the CPU oracle on the same
 scene on this host's cores.
 
+--layer-type regular | strided replaces the workload's layer stack by its
+first layer as a dilating (stride 1) or strided layer: a step is then
+sc_hash_build -> sc_hash_build_conv_out -> sc_kmap_build_conv -> the layer.
+
 --impl reference times the CPU oracle alone (the reference arm).
 Under torchrun (WORLD_SIZE > 1) every rank runs an independent replica on
 its own scene (replicas only; no data-path collective).
@@ -56,6 +60,10 @@ def parse_args():
                          "layer (a seeded output gradient, ReLU masks applied)")
     ap.add_argument("--variant", choices=["fused", "ws", "simt"], default=None,
                     help="run every layer with this variant instead of the measured choice")
+    ap.add_argument("--layer-type", choices=["submanifold", "regular", "strided"], default="submanifold",
+                    help="regular: a dilating layer (stride 1, output set grown by the kernel window); strided: "
+                         "a layer on the grid coarsened by --stride; both run the workload's first layer only")
+    ap.add_argument("--stride", type=int, default=2, help="stride of --layer-type strided")
     return ap.parse_args()
 
 
@@ -78,19 +86,22 @@ def layer_tensors(w, s):
 
 
 # ------------------------------------------------------------- algorithmic bytes --
-def algo_bytes_step(kernel: str, N: int, V: int, M: int, layers, s: int, ntiles: int, backward: bool = False):
+def algo_bytes_step(kernel: str, N: int, V: int, M: int, layers, s: int, ntiles: int, backward: bool = False,
+                    n_out: int | None = None):
     """Bytes a kernel must move at minimum in one step (summed over its
     launches in that step); None for kernels without a stated model.  With
     `backward`, the convolution kernels also run each layer's input gradient
-    (a layer from c_out to c_in channels)."""
-    lists = 8 * (M - N)
+    (a layer from c_out to c_in channels).  n_out: output rows of a regular /
+    strided layer (its map lists every tuple, the centre's included)."""
+    No = N if n_out is None else n_out
+    lists = 8 * (M - N) if n_out is None else 8 * M
     conv_layers = list(layers) + ([(co, ci) for ci, co in layers] if backward else [])
-    conv = sum(M * ci * s + N * co * s + 4 * N * V + V * ci * co * s for ci, co in conv_layers)
+    conv = sum(M * ci * s + No * co * s + 4 * No * V + V * ci * co * s for ci, co in conv_layers)
     table = {
         # coords in; row keys out; one row slot per point
         "hash_insert": 16 * N + 8 * N + 4 * N,
         # row keys in; neighbour table and (in, out) lists out
-        "kmap_build": 8 * N + 4 * N * V + lists,
+        "kmap_build": 8 * No + 4 * No * V + lists,
         "order_count": 8 * N,
         "order_scatter": 8 * N + 4 * N,
         "pack_weights": sum(2 * V * ci * co * s for ci, co in conv_layers),
@@ -185,16 +196,22 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------- CPU --
-def cpu_oracle_run(s, K, f, W, seconds: float):
-    """Times the oracle (map + layer) on the full scene, repeated to ~`seconds`."""
+def cpu_oracle_run(s, K, f, W, seconds: float, stride: int = 0):
+    """Times the oracle (map + layer) on the full scene, repeated to ~`seconds`.
+    stride > 0: the regular / strided layer (output set + map + layer)."""
     import oracle
     f64 = f.astype(np.float64)
     W64 = W.astype(np.float64)
     t0 = time.perf_counter()
     passes = 0
     while True:
-        oracle.kmap(s.coords, s.ndim, K, s.dims)
-        oracle.subm_conv(s.coords, f64, W64, s.ndim, K, s.dims)
+        if stride:
+            oc = oracle.conv_out_coords(s.coords, s.ndim, K, stride, s.dims)
+            oracle.conv_kmap(s.coords, oc, s.ndim, K, stride, s.dims)
+            oracle.sparse_conv(s.coords, oc, f64, W64, s.ndim, K, stride, s.dims)
+        else:
+            oracle.kmap(s.coords, s.ndim, K, s.dims)
+            oracle.subm_conv(s.coords, f64, W64, s.ndim, K, s.dims)
         passes += 1
         el = time.perf_counter() - t0
         if el >= seconds or el * (passes + 1) / passes > 3 * seconds:
@@ -296,6 +313,13 @@ def run_ours(args):
     esize = 4 if w.dtype == "f32" else 2
     V = w.K ** s.ndim
     layers = list(zip(w.channels[:-1], w.channels[1:]))  # (c_in, c_out) of each layer on the one map
+    general = args.layer_type != "submanifold"
+    if general:
+        layers = layers[:1]
+        if args.backward:
+            raise SystemExit("--backward runs submanifold layers only (the input gradient of a regular or strided "
+                             "layer needs the transposed map)")
+    conv_stride = args.stride if args.layer_type == "strided" else 1
     f_np, W0 = layer_tensors(w, s)
     Ws = [torch.from_numpy(W0).to(tdt).to(dev)]
     for li, (ci, co) in enumerate(layers[1:], start=1):
@@ -303,14 +327,23 @@ def run_ours(args):
     c_in, c_out = layers[0]
     coords = torch.from_numpy(s.coords).to(dev)
     feats = torch.from_numpy(f_np).to(tdt).to(dev)
-    outs = [torch.empty((s.n, co), dtype=tdt, device=dev) for _, co in layers]
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
+    def build_map(c, sync):
+        """hash -> kernel map (submanifold), or hash -> output set -> map
+        (regular / strided; the output set's count is read on the host)."""
+        h = sc.sc_hash_build(c)
+        if not general:
+            return (h,), sc.sc_kmap_build(h, s.ndim, w.K, s.dims, sync=sync)
+        ho = sc.sc_hash_build_conv_out(h, s.ndim, w.K, conv_stride, s.dims)
+        return (h, ho), sc.sc_kmap_build_conv(h, ho, s.ndim, w.K, conv_stride, s.dims, sync=sync)
+
     # variant of each layer chosen from measured time on this map
-    h0 = sc.sc_hash_build(coords)
-    m0 = sc.sc_kmap_build(h0, s.ndim, w.K, s.dims)
+    hs0, m0 = build_map(coords, True)
     M = m0.map_size()
+    n_out = m0.n
+    outs = [torch.empty((n_out, co), dtype=tdt, device=dev) for _, co in layers]
     variants = []
     x = feats
     for li, W in enumerate(Ws):
@@ -328,8 +361,7 @@ def run_ours(args):
         dWs = [torch.empty_like(W) for W in Ws]
 
     def step():
-        h = sc.sc_hash_build(coords)
-        m = sc.sc_kmap_build(h, s.ndim, w.K, s.dims, sync=False)
+        h, m = build_map(coords, False)
         xin = feats
         for li, W in enumerate(Ws):
             sc.sc_subm_conv_fwd(m, xin, W, out=outs[li], relu=li + 1 < len(Ws), variant=variants[li])
@@ -375,8 +407,7 @@ def run_ours(args):
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        h = sc.sc_hash_build(coords)
-        m = sc.sc_kmap_build(h, s.ndim, w.K, s.dims, sync=False)
+        h, m = build_map(coords, False)
         e1.record(stream)
         keep.append((h, m, e0, e1))
         if len(keep) > 4:
@@ -431,7 +462,7 @@ def run_ours(args):
     map_names = ("hash_insert", "order_count", "order_partials", "order_apply", "order_scatter", "kmap_build")
     map_ms = sum(prof_all[k][1] for k in map_names if k in prof_all) / bd_steps
     peaks = load_peaks()
-    ab_step = algo_bytes_step(dom, s.n, V, M, layers, esize, ntiles, args.backward)
+    ab_step = algo_bytes_step(dom, s.n, V, M, layers, esize, ntiles, args.backward, n_out if general else None)
     launches_per_step = prof[dom][0] / args.steps
     ab = ab_step / launches_per_step if ab_step else None
     avg_s = prof[dom][1] / prof[dom][0] / 1e3
@@ -447,7 +478,8 @@ def run_ours(args):
     # gradients)
     def roof_s(kernel, ci, co):
         return max(2.0 * M * ci * co / (peaks["bf16_tflops"] * 1e12),
-                   algo_bytes_step(kernel, s.n, V, M, [(ci, co)], esize, ntiles) / (peaks["hbm_gbs"] * 1e9))
+                   algo_bytes_step(kernel, s.n, V, M, [(ci, co)], esize, ntiles, False, n_out if general else None)
+                   / (peaks["hbm_gbs"] * 1e9))
     conv_roof_s = sum(roof_s("subm_conv_fused", ci, co) for ci, co in layers)
     if args.backward:
         conv_roof_s += sum(roof_s("subm_conv_fused", co, ci) + roof_s("subm_conv_wgrad", ci, co) for ci, co in layers)
@@ -457,6 +489,7 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": w.name, "N": s.n, "map_size": M, "K": w.K, "layers": layers,
+                   "layer_type": args.layer_type, "stride": conv_stride, "N_out": n_out,
                    "pass": "forward+backward" if args.backward else "forward",
                    "variant": variants, "variant_choice": "given" if args.variant else "measured", "l2": "flushed before every step (256 MB write, outside the events)",
                    "kmap_sync": False, "parallelism": "replicas" if world > 1 else "single"},
@@ -473,9 +506,10 @@ def run_ours(args):
     }
 
     if not args.no_e2e and rank == 0:
-        line["e2e"] = run_e2e(args, w, s, f_np, Ws, tdt, dev, variants, world)
+        line["e2e"] = run_e2e(args, w, s, f_np, Ws, tdt, dev, variants, world, build_map, n_out)
     if not args.no_cpu_baseline and rank == 0:
-        line["cpu_baseline"] = cpu_oracle_run(s, w.K, feats.float().cpu().numpy(), W0, args.cpu_seconds)
+        line["cpu_baseline"] = cpu_oracle_run(s, w.K, feats.float().cpu().numpy(), W0, args.cpu_seconds,
+                                              conv_stride if general else 0)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -483,7 +517,7 @@ def run_ours(args):
         torch.distributed.destroy_process_group()
 
 
-def run_e2e(args, w, s, f_np, Ws_dev, tdt, dev, variants, world):
+def run_e2e(args, w, s, f_np, Ws_dev, tdt, dev, variants, world, build_map, n_out):
     """Same metric through the public calls, host buffers in and out: every
     step copies coords, features and all layer weights from pinned host
     memory, builds the map with the default (synchronising, error-checking)
@@ -493,15 +527,14 @@ def run_e2e(args, w, s, f_np, Ws_dev, tdt, dev, variants, world):
     c_h = torch.from_numpy(s.coords).pin_memory()
     f_h = torch.from_numpy(f_np).to(tdt).pin_memory()
     W_h = [W.cpu().pin_memory() for W in Ws_dev]
-    o_h = torch.empty((s.n, Ws_dev[-1].shape[2]), dtype=tdt).pin_memory()
+    o_h = torch.empty((n_out, Ws_dev[-1].shape[2]), dtype=tdt).pin_memory()
     stream = torch.cuda.current_stream(dev)
 
     def step():
         c = c_h.to(dev, non_blocking=True)
         x = f_h.to(dev, non_blocking=True)
         Ws = [W.to(dev, non_blocking=True) for W in W_h]
-        h = sc.sc_hash_build(c)
-        m = sc.sc_kmap_build(h, s.ndim, w.K, s.dims)  # default: synchronises and checks errors
+        h, m = build_map(c, True)  # the default map build: synchronises and checks errors
         for li, W in enumerate(Ws):
             x = sc.sc_subm_conv_fwd(m, x, W, relu=li + 1 < len(Ws), variant=variants[li])
         o_h.copy_(x, non_blocking=True)

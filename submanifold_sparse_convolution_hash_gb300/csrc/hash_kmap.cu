@@ -626,10 +626,12 @@ __global__ void __launch_bounds__(256) k_compact_lists(const int* __restrict__ s
 // hash table to rulebook", section 2), output o reading the input at
 // stride * o + d (section 3's index relation under a stride).  Every input
 // marks each output o with stride * o + d at that input (d in [-r, r], o
-// inside the output grid) in a block table of the input table's layout; the
-// marked voxel slots are then counted per chunk of entries, scanned, and
-// numbered 0 .. n_out - 1 in table order, which turns the table into the
-// output set's hash table; each output's key is written with its number.
+// inside the output grid) in a block table of the input table's layout:
+// those outputs form a box, marked block by block with one atomic on the
+// block entry's occupancy word.  The marked voxels are then counted per chunk
+// of entries, scanned, and numbered 0 .. n_out - 1 in table order, which
+// turns the table into the output set's hash table; each output's key is
+// written with its number.
 
 constexpr int kOutChunk = 256 * 8;  // table entries per counting block (8 per thread)
 
@@ -640,18 +642,24 @@ struct OutGrid {
   int sz;          // stride on z (1 in 2D: z is carried)
 };
 
-__device__ __forceinline__ void mark_output(BlockEntry* __restrict__ table, uint32_t mask, unsigned long long key,
-                                            int* __restrict__ status) {
-  const unsigned long long bk = block_key(key);
+// Marks the voxels `bits` (bit 4*lx + 2*ly + lz) of output block bk: finds
+// or claims its entry, then clears those bits of the entry's occupancy word
+// (the second word, all ones in an empty table).  A probe run longer than
+// kOutProbeLimit latches kDevErrFull: the table is too small and the host
+// retries with a larger one.
+constexpr uint32_t kOutProbeLimit = 256;
+__device__ __forceinline__ void mark_output_block(BlockEntry* __restrict__ table, uint32_t mask, unsigned long long bk,
+                                                  unsigned bits, int* __restrict__ status) {
   uint32_t h = block_home(bk, mask);
-  for (uint32_t probe = 0; probe <= mask; ++probe) {
+  const uint32_t limit = mask < kOutProbeLimit ? mask + 1 : kOutProbeLimit;
+  for (uint32_t probe = 0; probe < limit; ++probe) {
     unsigned long long k = __ldcg(&table[h].key);
     if (k == kEmptyKey) {
       k = atomicCAS(&table[h].key, kEmptyKey, bk);
       if (k == kEmptyKey) k = bk;
     }
     if (k == bk) {
-      table[h].rows[block_local(key)] = 0;  // present, numbered later (every writer stores the same value)
+      atomicAnd(&table[h].occupancy, ~static_cast<unsigned long long>(bits));
       return;
     }
     h = (h + 1) & mask;
@@ -659,6 +667,20 @@ __device__ __forceinline__ void mark_output(BlockEntry* __restrict__ table, uint
   atomicOr(status, kDevErrFull);
 }
 
+// Output range [lo, hi] along one axis for an input at coordinate c: the o
+// with c - r <= stride * o <= c + r inside [0, ext).  Empty when lo > hi.
+__device__ __forceinline__ void out_range(int c, int r, int stride, int ext, int& lo, int& hi) {
+  lo = c - r <= 0 ? 0 : (c - r + stride - 1) / stride;
+  hi = min((c + r) / stride, ext - 1);
+}
+
+// Voxels of block b (2b, 2b + 1) inside [lo, hi], as a 2-bit mask.
+__device__ __forceinline__ unsigned pair_mask(int b, int lo, int hi) {
+  return (2 * b >= lo && 2 * b <= hi ? 1u : 0u) | (2 * b + 1 >= lo && 2 * b + 1 <= hi ? 2u : 0u);
+}
+
+// Each input's outputs form a box in the output grid (the product of its
+// per-axis ranges); the box is marked block by block, one atomic per block.
 __global__ void __launch_bounds__(256) k_out_mark(const unsigned long long* __restrict__ keys, int64_t n,
                                                   BlockEntry* __restrict__ table, uint32_t mask, OutGrid g,
                                                   int* __restrict__ status) {
@@ -669,39 +691,41 @@ __global__ void __launch_bounds__(256) k_out_mark(const unsigned long long* __re
     const unsigned long long batch = key & 0xFFFF000000000000ull;
     const int x = static_cast<int>((key >> 32) & 0xFFFF), y = static_cast<int>((key >> 16) & 0xFFFF),
               z = static_cast<int>(key & 0xFFFF);
-    for (int dx = -g.r; dx <= g.r; ++dx) {
-      const int px = x - dx;  // stride * o_x
-      if (px < 0 || px % g.stride) continue;
-      const int ox = px / g.stride;
-      if (ox >= g.ex) continue;
-      for (int dy = -g.r; dy <= g.r; ++dy) {
-        const int py = y - dy;
-        if (py < 0 || py % g.stride) continue;
-        const int oy = py / g.stride;
-        if (oy >= g.ey) continue;
-        for (int dz = -g.rz; dz <= g.rz; ++dz) {
-          const int pz = z - dz;
-          if (pz < 0 || pz % g.sz) continue;
-          const int oz = pz / g.sz;
-          if (oz >= g.ez) continue;
-          mark_output(table, mask, batch | pack_key(0, ox, oy, oz), status);
+    int xl, xh, yl, yh, zl, zh;
+    out_range(x, g.r, g.stride, g.ex, xl, xh);
+    out_range(y, g.r, g.stride, g.ey, yl, yh);
+    out_range(z, g.rz, g.sz, g.ez, zl, zh);
+    if (xl > xh || yl > yh || zl > zh) continue;
+    for (int bx = xl >> 1; bx <= xh >> 1; ++bx) {
+      const unsigned mx = pair_mask(bx, xl, xh);
+      for (int by = yl >> 1; by <= yh >> 1; ++by) {
+        const unsigned my = pair_mask(by, yl, yh);
+        for (int bz = zl >> 1; bz <= zh >> 1; ++bz) {
+          const unsigned mz = pair_mask(bz, zl, zh);
+          unsigned bits = 0;
+#pragma unroll
+          for (int l = 0; l < 8; ++l)
+            if (((mx >> (l >> 2)) & (my >> ((l >> 1) & 1)) & (mz >> (l & 1))) & 1u) bits |= 1u << l;
+          mark_output_block(table, mask, batch | pack_key(0, 2 * bx, 2 * by, 2 * bz), bits, status);
         }
       }
     }
   }
 }
 
-// Marked slots of the 8 entries blockIdx.x * kOutChunk + k * 256 + threadIdx.x.
+// The marked voxels of an entry: the cleared low bits of its occupancy word.
+__device__ __forceinline__ unsigned marked_bits(const BlockEntry& e) {
+  return static_cast<unsigned>(~__ldcg(&e.occupancy)) & 0xFFu;
+}
+
+// Marked voxels of the 8 entries blockIdx.x * kOutChunk + k * 256 + threadIdx.x.
 __device__ __forceinline__ int count_marked(const BlockEntry* __restrict__ table, int64_t cap) {
   int cnt = 0;
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
     const int64_t e = static_cast<int64_t>(blockIdx.x) * kOutChunk + k * 256 + threadIdx.x;
     if (e >= cap) break;
-    const int4 a = __ldcg(reinterpret_cast<const int4*>(table[e].rows));
-    const int4 b = __ldcg(reinterpret_cast<const int4*>(table[e].rows + 4));
-    cnt += (a.x != -1) + (a.y != -1) + (a.z != -1) + (a.w != -1) + (b.x != -1) + (b.y != -1) + (b.z != -1) +
-           (b.w != -1);
+    cnt += __popc(marked_bits(table[e]));
   }
   return cnt;
 }
@@ -743,8 +767,9 @@ __global__ void __launch_bounds__(256) k_out_number(BlockEntry* __restrict__ tab
     const int64_t e = static_cast<int64_t>(blockIdx.x) * kOutChunk + k * 256 + threadIdx.x;
     if (e >= cap) break;
     const unsigned long long bk = table[e].key;
+    const unsigned bits = marked_bits(table[e]);
     for (int l = 0; l < 8; ++l) {
-      if (table[e].rows[l] == -1) continue;
+      if (!((bits >> l) & 1u)) continue;
       table[e].rows[l] = id;
       keys_out[id] = bk | (static_cast<unsigned long long>((l >> 2) & 1) << 32) |
                      (static_cast<unsigned long long>((l >> 1) & 1) << 16) | static_cast<unsigned long long>(l & 1);
@@ -926,14 +951,15 @@ sc_status launch_conv_out(const HashTable* in, int ndim, int K, int stride, cons
   g.ex = (dims[0] + stride - 1) / stride;
   g.ey = (dims[1] + stride - 1) / stride;
   g.ez = ndim == 3 ? (dims[2] + stride - 1) / stride : dims[2];
-  // table size: the blocks one input's outputs fall in (per axis: its
-  // floor(2r / stride) + 1 output positions span at most that / 2 + 1
-  // blocks), a quarter of that per input (neighbouring inputs share output
-  // blocks), at most half full; a full table is retried four times larger
-  const int span = (2 * g.r) / stride + 1, bpa = span / 2 + 1;
-  const int64_t per = static_cast<int64_t>(bpa) * bpa * (ndim == 3 ? bpa : 1);
-  int64_t cap = 16;
-  while (cap < 2 * (in->n * per / 4 + 1)) cap <<= 1;
+  // table size: about n (K / stride)^ndim / 5 outputs on surface data (each
+  // output shared by the inputs of its window), about three to a 2x2x2
+  // block, at most half full; a table too small for its probe runs is
+  // retried four times larger
+  double per = 1.0;
+  for (int a = 0; a < ndim; ++a) per *= static_cast<double>(K) / stride;
+  const double blocks = static_cast<double>(in->n) * per / 15.0;
+  int64_t cap = 64;
+  while (static_cast<double>(cap) < 2.0 * blocks) cap <<= 1;
   const int64_t kMaxCap = int64_t(1) << 28;
   int64_t n_out = 0;
   for (;;) {

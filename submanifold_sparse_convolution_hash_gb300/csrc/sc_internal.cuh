@@ -43,7 +43,7 @@ __host__ __device__ __forceinline__ unsigned long long pack_key(uint32_t b, uint
 // return every neighbour, present or absent.
 struct __align__(64) BlockEntry {
   unsigned long long key;
-  unsigned long long pad0;
+  unsigned long long occupancy;  // output-set construction only: a cleared bit l marks voxel l
   int rows[8];
   int pad1[4];
 };
