@@ -82,6 +82,8 @@ def _load():
         lib.oracle_conv.restype = I
         lib.oracle_conv_bwd_weight.argtypes = [P, I64, P, I64, I, I, I, P, P, P, I, I, P, I]
         lib.oracle_conv_bwd_weight.restype = I
+        lib.oracle_conv_bwd_data.argtypes = [P, I64, P, I64, I, I, I, P, P, P, I, I, P, I]
+        lib.oracle_conv_bwd_data.restype = I
         _lib = lib
     return _lib
 
@@ -320,6 +322,24 @@ def sparse_conv_bwd_weight(coords, out_coords, feats, gout, ndim: int, K: int, s
     st = _load().oracle_conv_bwd_weight(_ptr(c), c.shape[0], _ptr(o), o.shape[0], ndim, K, stride,
                                         _ptr(_dims(dims)), _ptr(f), _ptr(g), f.shape[1], g.shape[1], _ptr(out),
                                         threads)
+    if st:
+        raise OracleError(st)
+    return out
+
+
+def sparse_conv_bwd_data(coords, out_coords, gout, W, ndim: int, K: int, stride: int, dims,
+                         threads: int = 0) -> np.ndarray:
+    """fp64 input gradient [N, C_in] of a regular / strided layer, given the
+    gradient with respect to its output [N_out, C_out]."""
+    c, o = _coords(coords), _coords(out_coords)
+    w = np.ascontiguousarray(np.asarray(W, dtype=np.float64))
+    V, c_in, c_out = w.shape
+    g = np.ascontiguousarray(np.asarray(gout, dtype=np.float64).reshape(o.shape[0], c_out))
+    if V != volume(ndim, K):
+        raise OracleError(1)
+    out = np.empty((c.shape[0], c_in), dtype=np.float64)
+    st = _load().oracle_conv_bwd_data(_ptr(c), c.shape[0], _ptr(o), o.shape[0], ndim, K, stride, _ptr(_dims(dims)),
+                                      _ptr(g), _ptr(w), c_in, c_out, _ptr(out), threads)
     if st:
         raise OracleError(st)
     return out

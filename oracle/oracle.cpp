@@ -467,3 +467,67 @@ int oracle_conv_bwd_weight(const int32_t* coords, int64_t n, const int32_t* out_
 }
 
 }  // extern "C"
+
+namespace {
+
+// The output row at coordinate (b, x, y, z) of an output set, or -1.
+int32_t output_at(const std::unordered_map<uint64_t, int32_t>& out_table, int64_t b, int64_t x, int64_t y, int64_t z) {
+  if (x < 0 || y < 0 || z < 0) return -1;
+  auto it = out_table.find(pack_key(b, x, y, z));
+  return it == out_table.end() ? -1 : it->second;
+}
+
+}  // namespace
+
+extern "C" {
+
+// Input gradient of a regular / strided layer (linear in f): d loss / d f[p]
+// = sum over the offsets d and outputs q with stride * c_q + d = c_p of
+// gout[q] W_d^T.  For each input p and offset d the output is the one at
+// (c_p - d) / stride, where that is a whole grid point of the output set.
+// gout [n_out, c_out], W [V, c_in, c_out], gin [n, c_in], fp64.
+int oracle_conv_bwd_data(const int32_t* coords, int64_t n, const int32_t* out_coords, int64_t n_out, int ndim, int K,
+                         int stride, const int32_t* dims, const double* gout, const double* W, int c_in, int c_out,
+                         double* gin, int nthreads) {
+  Problem P;
+  int st = setup(P, coords, n, ndim, K, dims);
+  if (st) return st;
+  if (stride < 1 || c_in < 1 || c_out < 1 || !W || (n > 0 && !gin) || (n_out > 0 && !gout)) return OR_BAD_ARG;
+  st = check_out_coords(P, out_coords, n_out, stride);
+  if (st) return st;
+  std::unordered_map<uint64_t, int32_t> out_table;
+  out_table.reserve(size_t(n_out) * 2 + 1);
+  for (int64_t q = 0; q < n_out; ++q) {
+    const int32_t* c = out_coords + 4 * q;
+    if (!out_table.emplace(pack_key(c[0], c[1], c[2], c[3]), int32_t(q)).second) return OR_DUPLICATE;
+  }
+  const int V = P.volume;
+  const int64_t sz = ndim == 3 ? stride : 1;
+  std::vector<int> offs(size_t(V) * 3);
+  for (int v = 0; v < V; ++v) offset_of(v, ndim, K, &offs[3 * v]);
+  const int nt = threads_to_use(nthreads);
+#pragma omp parallel for schedule(dynamic, 64) num_threads(nt)
+  for (int64_t p = 0; p < n; ++p) {
+    const int32_t* c = coords + 4 * p;
+    double* acc = gin + p * c_in;
+    for (int ci = 0; ci < c_in; ++ci) acc[ci] = 0.0;
+    for (int v = 0; v < V; ++v) {
+      const int* d = &offs[3 * v];
+      const int64_t px = int64_t(c[1]) - d[0], py = int64_t(c[2]) - d[1], pz = int64_t(c[3]) - d[2];
+      if (px % stride || py % stride || pz % sz) continue;
+      const int32_t q = output_at(out_table, c[0], px / stride, py / stride, pz / sz);
+      if (q < 0) continue;
+      const double* g = gout + int64_t(q) * c_out;
+      const double* w = W + int64_t(v) * c_in * c_out;
+      for (int ci = 0; ci < c_in; ++ci) {
+        const double* wrow = w + int64_t(ci) * c_out;
+        double sum = 0.0;
+        for (int co = 0; co < c_out; ++co) sum += wrow[co] * g[co];
+        acc[ci] += sum;
+      }
+    }
+  }
+  return OR_OK;
+}
+
+}  // extern "C"

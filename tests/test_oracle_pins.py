@@ -661,3 +661,47 @@ def test_strided_weight_gradient_equals_dense_autograd(ndim, K, stride, dims, n,
         gy[:, oo[:, 1], oo[:, 2]] = torch.from_numpy(g).T
     (y * gy).sum().backward()
     assert np.allclose(dW, Wt.grad.numpy(), rtol=1e-10, atol=1e-10)
+
+
+@pytest.mark.parametrize("ndim,K,stride,dims,n,cin,cout", [
+    (3, 3, 2, (7, 6, 8), 40, 3, 2), (2, 3, 1, (9, 9, 1), 30, 2, 3), (3, 5, 2, (6, 7, 6), 30, 2, 2),
+    (3, 3, 3, (8, 7, 9), 40, 2, 3), (2, 5, 2, (11, 9, 2), 40, 3, 2),
+])
+def test_strided_input_gradient_equals_dense_autograd(ndim, K, stride, dims, n, cin, cout):
+    c = random_scene(ndim * 11 + K + 3 * stride, n, dims, ndim, 1)
+    rng = np.random.default_rng(13)
+    f = rng.standard_normal((c.shape[0], cin))
+    W = rng.standard_normal((K ** ndim, cin, cout))
+    o = oracle.conv_out_coords(c, ndim, K, stride, dims)
+    g = rng.standard_normal((o.shape[0], cout))
+    gin = oracle.sparse_conv_bwd_data(c, o, g, W, ndim, K, stride, dims)
+    r = K // 2
+    ext = oracle.conv_out_extent(dims, ndim, stride)
+    cc = torch.from_numpy(c.astype(np.int64))
+    oo = torch.from_numpy(o.astype(np.int64))
+    Wt = torch.from_numpy(W)
+    if ndim == 3:
+        grid = torch.zeros((1, cin) + tuple(dims), dtype=torch.float64, requires_grad=True)
+        y = torch.nn.functional.conv3d(grid, Wt.reshape(K, K, K, cin, cout).permute(4, 3, 0, 1, 2), padding=r,
+                                       stride=stride)[0]
+        gy = torch.zeros((cout,) + ext, dtype=torch.float64)
+        gy[:, oo[:, 1], oo[:, 2], oo[:, 3]] = torch.from_numpy(g).T
+        (y * gy).sum().backward()
+        want = grid.grad[0][:, cc[:, 1], cc[:, 2], cc[:, 3]].T.numpy()
+    else:
+        assert dims[2] <= 2
+        want = np.zeros_like(gin)
+        for z in range(dims[2]):
+            grid = torch.zeros((1, cin, dims[0], dims[1]), dtype=torch.float64, requires_grad=True)
+            y = torch.nn.functional.conv2d(grid, Wt.reshape(K, K, cin, cout).permute(3, 2, 0, 1), padding=r,
+                                           stride=stride)[0]
+            gy = torch.zeros((cout,) + ext[:2], dtype=torch.float64)
+            mo = oo[:, 3] == z
+            gy[:, oo[mo, 1], oo[mo, 2]] = torch.from_numpy(g[mo.numpy()]).T
+            (y * gy).sum().backward()
+            mc = (cc[:, 3] == z).numpy()
+            want[mc] = grid.grad[0][:, cc[mc, 1], cc[mc, 2]].T.numpy()
+    assert np.allclose(gin, want, rtol=1e-10, atol=1e-10)
+    # adjoint identity: <conv(f), g> = <f, gin>
+    lhs = float((oracle.sparse_conv(c, o, f, W, ndim, K, stride, dims) * g).sum())
+    assert abs(lhs - float((f * gin).sum())) <= 1e-9 * max(1.0, abs(lhs))
