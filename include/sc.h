@@ -71,6 +71,7 @@ typedef enum { SC_F32 = 0, SC_F16 = 1, SC_BF16 = 2 } sc_dtype;
 #define SC_KMAP_NO_ORDER 0x400u /* never compute it: tiles follow the input row order */
 #define SC_KMAP_SORT 0x800u     /* always sort the convolution's rows by signature (default: n >= 262144, V <= 32) */
 #define SC_KMAP_NO_SORT 0x1000u /* never sort them */
+#define SC_KMAP_TRANSPOSE 0x2000u /* sc_kmap_build_conv: the transposed map (rows = the layer's inputs) */
 
 typedef struct sc_hash_s* sc_hash;
 typedef struct sc_kmap_s* sc_kmap;
@@ -215,8 +216,16 @@ sc_status sc_kmap_build(sc_hash h, int ndim, int K, const int32_t dims[3], unsig
  *
  * sc_subm_conv_fwd and sc_subm_conv_bwd_weight take such a map: feats then
  * has the input's n_in rows and out / gout the map's n rows.  The
- * weight-stationary variant and sc_subm_conv_bwd_data return
- * SC_ERR_UNSUPPORTED for it.
+ * weight-stationary variant returns SC_ERR_UNSUPPORTED for it.
+ *
+ * With SC_KMAP_TRANSPOSE the map is transposed: its rows are the points of
+ * `in` (the layer's inputs) and nbr[p*V + idx(-d)] is the row q of `out_set`
+ * with stride * coords[q] + d = coords[p], or -1 (the outputs whose windows
+ * contain p, at the mirrored offset).  sc_subm_conv_bwd_data takes the
+ * transposed map of a layer, with d_gout [n_out, c_out] and d_gin [n, c_in]:
+ * gin[p] = sum over those (q, d) of gout[q] @ W[idx(d)]^T, the layer's input
+ * gradient, on the same kernels as the submanifold one.  A forward map
+ * returns SC_ERR_UNSUPPORTED there.
  */
 sc_status sc_kmap_build_conv(sc_hash in, sc_hash out_set, int ndim, int K, int stride, const int32_t dims[3],
                              unsigned flags, sc_stream stream, sc_kmap* out);

@@ -24,6 +24,7 @@ SC_KMAP_ORDER = 0x200
 SC_KMAP_NO_ORDER = 0x400
 SC_KMAP_SORT = 0x800
 SC_KMAP_NO_SORT = 0x1000
+SC_KMAP_TRANSPOSE = 0x2000
 VARIANTS = {"fused": SC_VARIANT_FUSED, "ws": SC_VARIANT_WS, "simt": SC_VARIANT_SIMT}
 VARIANT_NAMES = {v: k for k, v in VARIANTS.items()}
 _DTYPES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
@@ -266,18 +267,24 @@ def sc_hash_build_conv_out(h: Hash, ndim: int, K: int, stride: int, dims, stream
 
 
 def sc_kmap_build_conv(h_in: Hash, h_out: Hash, ndim: int, K: int, stride: int, dims, sync: bool = True,
-                       order: bool | None = None, stream=None) -> KernelMap:
+                       order: bool | None = None, transpose: bool = False, stream=None) -> KernelMap:
     """Kernel map of a regular / strided layer: rows = the points of `h_out`,
-    neighbours = rows of `h_in` at stride * o + d."""
+    neighbours = rows of `h_in` at stride * o + d.  transpose: the transposed
+    map (rows = the points of `h_in`, neighbours = the outputs whose windows
+    hold them, at the mirrored offset), which sc_subm_conv_bwd_data takes."""
     d = (ctypes.c_int32 * 3)(*(list(dims) + [1] * (3 - len(dims))))
     m = ctypes.c_void_p()
     flags = 0 if sync else SC_KMAP_NO_SYNC
+    if transpose:
+        flags |= SC_KMAP_TRANSPOSE
     if order is True:
         flags |= SC_KMAP_ORDER
     elif order is False:
         flags |= SC_KMAP_NO_ORDER
     _check(lib().sc_kmap_build_conv(h_in._h, h_out._h, ndim, K, stride, d, flags, _stream(stream), ctypes.byref(m)),
            "sc_kmap_build_conv")
+    if transpose:
+        return KernelMap(m, h_in.n, ndim, K, list(d), h_in.device, n_in=h_out.n, stride=stride)
     return KernelMap(m, h_out.n, ndim, K, list(d), h_in.device, n_in=h_in.n, stride=stride)
 
 
@@ -317,8 +324,10 @@ def sc_subm_conv_bwd_data(kmap: KernelMap, gout: torch.Tensor, W: torch.Tensor, 
     w = _dev(W, "W")
     if g.dtype not in _DTYPES or w.dtype != g.dtype:
         raise ValueError("gout and W must share one dtype: float32, float16 or bfloat16")
-    if w.dim() != 3 or w.shape[0] != kmap.volume or g.dim() != 2 or g.shape[1] != w.shape[2] or g.shape[0] != kmap.n:
-        raise ValueError("shapes must be gout [N, C_out], W [K^ndim, C_in, C_out]")
+    if (w.dim() != 3 or w.shape[0] != kmap.volume or g.dim() != 2 or g.shape[1] != w.shape[2]
+            or g.shape[0] != kmap.n_in):
+        raise ValueError("shapes must be gout [N_out, C_out], W [K^ndim, C_in, C_out] (a submanifold map: "
+                         "N_out = N; a transposed map: N_out = the layer's output count)")
     c_in, c_out = w.shape[1], w.shape[2]
     if gin is None:
         gin = torch.empty((kmap.n, c_in), dtype=g.dtype, device=g.device)

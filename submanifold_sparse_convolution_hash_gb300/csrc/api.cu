@@ -451,7 +451,11 @@ sc_status kmap_build_impl(sc_hash hi, sc_hash ho, int ndim, int K, int stride, c
   if (!hi || !ho) return set_error(SC_ERR_INVALID_ARG, "hash handle is NULL");
   if (stride < 1 || stride > 64) return set_error(SC_ERR_INVALID_ARG, "stride must be in [1, 64]");
   const bool identity = hi == ho && stride == 1;
-  sc_hash h = ho;
+  const bool transposed = (flags & SC_KMAP_TRANSPOSE) != 0;
+  if (transposed && identity) return set_error(SC_ERR_INVALID_ARG, "SC_KMAP_TRANSPOSE is for regular / strided maps");
+  // rows: the queries (outputs; a transposed map's are the inputs); table: the other set
+  sc_hash h = transposed ? hi : ho;
+  sc_hash ht = transposed ? ho : hi;
   if (ndim != 2 && ndim != 3) return set_error(SC_ERR_INVALID_ARG, "ndim must be 2 or 3");
   if (K < 1 || K % 2 == 0) return set_error(SC_ERR_INVALID_ARG, "K must be odd and >= 1");
   int V = 1;
@@ -462,7 +466,7 @@ sc_status kmap_build_impl(sc_hash hi, sc_hash ho, int ndim, int K, int stride, c
   if (!dims) return set_error(SC_ERR_INVALID_ARG, "dims is NULL");
   for (int a = 0; a < 3; ++a)
     if (dims[a] < 1 || dims[a] > 65535) return set_error(SC_ERR_INVALID_ARG, "dims must be in [1, 65535]");
-  if (flags & ~(SC_KMAP_NO_SYNC | SC_KMAP_ORDER | SC_KMAP_NO_ORDER | SC_KMAP_SORT | SC_KMAP_NO_SORT))
+  if (flags & ~(SC_KMAP_NO_SYNC | SC_KMAP_ORDER | SC_KMAP_NO_ORDER | SC_KMAP_SORT | SC_KMAP_NO_SORT | SC_KMAP_TRANSPOSE))
     return set_error(SC_ERR_INVALID_ARG, "unknown kmap flag");
   if ((flags & SC_KMAP_ORDER) && (flags & SC_KMAP_NO_ORDER))
     return set_error(SC_ERR_INVALID_ARG, "SC_KMAP_ORDER and SC_KMAP_NO_ORDER together");
@@ -472,9 +476,10 @@ sc_status kmap_build_impl(sc_hash hi, sc_hash ho, int ndim, int K, int stride, c
   sc_kmap m = new sc_kmap_s();
   KernelMap& k = m->k;
   k.n = h->t.n;
-  k.n_in = hi->t.n;
+  k.n_in = ht->t.n;
   k.stride = stride;
   k.identity = identity;
+  k.transposed = transposed;
   k.ndim = ndim;
   k.K = K;
   k.V = V;
@@ -526,7 +531,7 @@ sc_status kmap_build_impl(sc_hash hi, sc_hash ho, int ndim, int K, int stride, c
     if (e == cudaSuccess) e = cudaMemcpyAsync(k.status + 1, hi->t.status, sizeof(int), cudaMemcpyDeviceToDevice, s);
     if (e != cudaSuccess) st = set_cuda_error(e, "kmap status init");
   }
-  if (!st) st = launch_kmap_build(&hi->t, &h->t, &k, s);
+  if (!st) st = launch_kmap_build(&ht->t, &h->t, &k, s);
   if (!st && !(flags & SC_KMAP_NO_SYNC)) st = sync_host(&k, s);
   if (st) {
     sc_kmap_destroy(m, stream);
@@ -626,8 +631,9 @@ sc_status sc_subm_conv_fwd(sc_kmap m, const void* d_feats, const void* d_W, void
 
 sc_status sc_subm_conv_bwd_data(sc_kmap m, const void* d_gout, const void* d_W, void* d_gin, int c_in, int c_out,
                                 sc_dtype dtype, unsigned flags, sc_stream stream) {
-  if (m && !m->k.identity)
-    return set_error(SC_ERR_UNSUPPORTED, "input gradient of a regular or strided layer: needs the transposed map");
+  if (m && !m->k.identity && !m->k.transposed)
+    return set_error(SC_ERR_UNSUPPORTED,
+                     "input gradient of a regular or strided layer: pass its transposed map (SC_KMAP_TRANSPOSE)");
   // the input gradient is a submanifold layer with c_out -> c_in channels
   sc_status st = check_conv_args(m, d_gout, d_W, d_gin, c_out, c_in, dtype);
   if (st) return st;

@@ -277,6 +277,13 @@ __global__ void __launch_bounds__(256) k_order_scatter(const unsigned long long*
 }
 
 
+// Output range [lo, hi] along one axis for an input at coordinate c: the o
+// with c - r <= stride * o <= c + r inside [0, ext).  Empty when lo > hi.
+__device__ __forceinline__ void out_range(int c, int r, int stride, int ext, int& lo, int& hi) {
+  lo = c - r <= 0 ? 0 : (c - r + stride - 1) / stride;
+  hi = min((c + r) / stride, ext - 1);
+}
+
 // Block-wide inclusive scan of one value per thread (blockDim <= 1024).
 template <typename T>
 __device__ __forceinline__ T block_inclusive_scan(T x, T* warp_sums, T* total) {
@@ -311,8 +318,11 @@ struct BuildArgs {
   int64_t n;
   const BlockEntry* table;
   uint32_t mask;                   // table capacity - 1
-  int V, K, ndim, dimx, dimy, dimz;  // dims: the grid of the table's (input) points
-  int stride;                      // query point o looks up the inputs at stride * o + d
+  int V, K, ndim, dimx, dimy, dimz;  // extents of the table's grid
+  int qex, qey, qez;               // extents of the queries' grid
+  int stride;                      // forward: query o looks up the table points at stride * o + d
+  int transposed;                  // the queries are a layer's inputs c, the table its outputs o with
+                                   // stride * o + d = c; the offset stored is -d (index V - 1 - idx(d))
   int identity;                    // the centre list is the identity (submanifold: queries = inputs)
   int up;                          // points per unit (128, or 32 when V > 128)
   int nunits;
@@ -363,17 +373,42 @@ __global__ void __launch_bounds__(kThreads, 5) k_kmap_build(const BuildArgs a) {
     if (part == 0 && p < up) s_row[p] = row;
     const unsigned long long ck = live ? (a.order ? __ldg(a.skeys + i0 + p) : __ldg(a.keys + row)) : kEmptyKey;
     bool valid = ck != kEmptyKey;
-    // the neighbourhood's centre in the input grid: stride * o (z too in 3D)
-    const int x = static_cast<int>((ck >> 32) & 0xFFFF) * a.stride, y = static_cast<int>((ck >> 16) & 0xFFFF) * a.stride,
-              z = static_cast<int>(ck & 0xFFFF) * (a.ndim == 3 ? a.stride : 1);
-    if (valid && (x >= a.dimx || y >= a.dimy || z >= a.dimz)) {
+    const int qx = static_cast<int>((ck >> 32) & 0xFFFF), qy = static_cast<int>((ck >> 16) & 0xFFFF),
+              qz = static_cast<int>(ck & 0xFFFF);
+    if (valid && (qx >= a.qex || qy >= a.qey || qz >= a.qez)) {
       if (part == 0) atomicOr(a.status, kDevErrRange);
       valid = false;
     }
+    // per axis: the table voxels [lo, hi] of this point's neighbourhood and
+    // the offset of voxel t, d = t * mul - ctr:
+    //   forward:    t in [s q - r, s q + r] (inside the table's grid), d = t - s q
+    //   transposed: t with q - r <= s t <= q + r (inside it),           d = s t - q
+    const int sz = a.ndim == 3 ? a.stride : 1;
+    int xl, xh, yl, yh, zl, zh, mxy, mz, cx, cy, cz;
+    if (!a.transposed) {
+      cx = qx * a.stride;
+      cy = qy * a.stride;
+      cz = qz * sz;
+      xl = max(cx - r, 0);
+      xh = min(cx + r, a.dimx - 1);
+      yl = max(cy - r, 0);
+      yh = min(cy + r, a.dimy - 1);
+      zl = max(cz - rz, 0);
+      zh = min(cz + rz, a.dimz - 1);
+      mxy = mz = 1;
+    } else {
+      cx = qx;
+      cy = qy;
+      cz = qz;
+      out_range(qx, r, a.stride, a.dimx, xl, xh);
+      out_range(qy, r, a.stride, a.dimy, yl, yh);
+      out_range(qz, rz, sz, a.dimz, zl, zh);
+      mxy = a.stride;
+      mz = sz;
+      if (xl > xh || yl > yh || zl > zh) valid = false;  // no table point can hold one
+    }
     const unsigned long long batch = ck & 0xFFFF000000000000ull;
-    const int xlo = max(x - r, 0) >> 1, xhi = min(x + r, a.dimx - 1) >> 1;
-    const int ylo = max(y - r, 0) >> 1, yhi = min(y + r, a.dimy - 1) >> 1;
-    const int zlo = max(z - rz, 0) >> 1, zhi = min(z + rz, a.dimz - 1) >> 1;
+    const int xlo = xl >> 1, xhi = xh >> 1, ylo = yl >> 1, yhi = yh >> 1, zlo = zl >> 1, zhi = zh >> 1;
     const int nb = r + 1, nbz = rz + 1;  // covering blocks per axis, at most
     const int ntrip = nb * nb * nbz;
     {
@@ -408,8 +443,9 @@ __global__ void __launch_bounds__(kThreads, 5) k_kmap_build(const BuildArgs a) {
           const int bx = xlo + t / (nb * nbz), by = ylo + (t / nbz) % nb, bz = zlo + t % nbz;
 #pragma unroll
           for (int l = 0; l < 8; ++l) {
-            const int dx = 2 * bx + (l >> 2) - x, dy = 2 * by + ((l >> 1) & 1) - y, dz = 2 * bz + (l & 1) - z;
-            if (dx >= -r && dx <= r && dy >= -r && dy <= r && dz >= -rz && dz <= rz) {
+            const int tx = 2 * bx + (l >> 2), ty = 2 * by + ((l >> 1) & 1), tz = 2 * bz + (l & 1);
+            if (tx >= xl && tx <= xh && ty >= yl && ty <= yh && tz >= zl && tz <= zh) {
+              const int dx = tx * mxy - cx, dy = ty * mxy - cy, dz = tz * mz - cz;
               const int v = a.ndim == 3 ? ((dx + r) * a.K + (dy + r)) * a.K + (dz + r) : (dx + r) * a.K + (dy + r);
               s_tile[p * V + v] = pick(r0[q], r1[q], l);
             }
@@ -667,13 +703,6 @@ __device__ __forceinline__ void mark_output_block(BlockEntry* __restrict__ table
   atomicOr(status, kDevErrFull);
 }
 
-// Output range [lo, hi] along one axis for an input at coordinate c: the o
-// with c - r <= stride * o <= c + r inside [0, ext).  Empty when lo > hi.
-__device__ __forceinline__ void out_range(int c, int r, int stride, int ext, int& lo, int& hi) {
-  lo = c - r <= 0 ? 0 : (c - r + stride - 1) / stride;
-  hi = min((c + r) / stride, ext - 1);
-}
-
 // Voxels of block b (2b, 2b + 1) inside [lo, hi], as a 2-bit mask.
 __device__ __forceinline__ unsigned pair_mask(int b, int lo, int hi) {
   return (2 * b >= lo && 2 * b <= hi ? 1u : 0u) | (2 * b + 1 >= lo && 2 * b + 1 <= hi ? 2u : 0u);
@@ -882,9 +911,20 @@ sc_status launch_kmap_build(const HashTable* in, const HashTable* h, KernelMap* 
   a.V = V;
   a.K = m->K;
   a.ndim = m->ndim;
-  a.dimx = m->dims[0];
-  a.dimy = m->dims[1];
-  a.dimz = m->dims[2];
+  // the grids of the queries and of the table: a layer's inputs have the
+  // extents dims, its outputs ceil(dims / stride) on the strided axes
+  const int st = m->stride, stz = m->ndim == 3 ? st : 1;
+  const int in_ext[3] = {m->dims[0], m->dims[1], m->dims[2]};
+  const int out_ext[3] = {(m->dims[0] + st - 1) / st, (m->dims[1] + st - 1) / st, (m->dims[2] + stz - 1) / stz};
+  const int* t_ext = m->transposed ? out_ext : in_ext;
+  const int* q_ext = m->transposed ? in_ext : out_ext;
+  a.dimx = t_ext[0];
+  a.dimy = t_ext[1];
+  a.dimz = t_ext[2];
+  a.qex = q_ext[0];
+  a.qey = q_ext[1];
+  a.qez = q_ext[2];
+  a.transposed = m->transposed ? 1 : 0;
   a.up = m->up;
   a.nunits = m->nunits;
   a.nbr = m->nbr;

@@ -79,6 +79,7 @@ struct KernelMap {
   int64_t n_in = 0;                  // rows of the input (= n for a submanifold map)
   int stride = 1;                    // output o reads the inputs at stride * o + d
   bool identity = true;              // submanifold: outputs = inputs, the centre list is the identity
+  bool transposed = false;           // rows = a layer's inputs, neighbours = its outputs at mirrored offsets
   int ndim = 3, K = 3, V = 27;
   int dims[3] = {1, 1, 1};
   int up = 128;                      // points per map-build unit (128; 32 when V > 128)

@@ -141,8 +141,9 @@ def test_regular_then_submanifold_chain():
 def test_unsupported_paths_and_empty_input():
     s = SC["lidar"]
     h, ho, m = build(s, 3, 2)
-    g = torch.zeros((ho.n, 32), dtype=torch.float16, device="cuda")
     W = torch.zeros((27, 32, 32), dtype=torch.float16, device="cuda")
+    # the input gradient needs the transposed map; the forward map is refused
+    g = torch.zeros((m.n_in, 32), dtype=torch.float16, device="cuda")
     with pytest.raises(sc.ScError) as e:
         sc.sc_subm_conv_bwd_data(m, g, W)
     assert e.value.code == 5
@@ -181,3 +182,36 @@ def test_full_size_strided_layer_on_lidar_scan():
                                      np.arange(max(0, ho.n - 200), ho.n)]))
     ref = oracle.sparse_conv(s.coords, oc[rows], f.double().cpu().numpy(), W.double().cpu().numpy(), 3, 3, 2, s.dims)
     assert_close(out[torch.from_numpy(rows).cuda()], ref, "f16", "full-size strided layer")
+
+
+@pytest.mark.parametrize("name,K,stride,c_in,c_out,dtype,order", [
+    ("lidar", 3, 2, 32, 32, "f16", False), ("lidar", 3, 1, 32, 64, "f16", True),
+    ("indoor", 3, 2, 64, 64, "bf16", True), ("indoor", 5, 2, 32, 48, "bf16", False),
+    ("indoor", 3, 3, 64, 32, "f16", False), ("batch", 3, 2, 128, 256, "bf16", False),
+    ("batch", 1, 2, 32, 32, "f16", False), ("uniform2d", 3, 2, 16, 16, "f32", False),
+    ("uniform2d", 5, 3, 16, 32, "f16", False),
+])
+def test_transposed_map_and_input_gradient(name, K, stride, c_in, c_out, dtype, order):
+    """The transposed map holds, for each input p, the outputs whose windows
+    contain it at the mirrored offset; the input gradient runs on it."""
+    s = SC[name]
+    h, ho, m = build(s, K, stride)
+    mt = sc.sc_kmap_build_conv(h, ho, s.ndim, K, stride, s.dims, order=order, transpose=True)
+    assert mt.n == s.n and mt.n_in == ho.n
+    oc = ho.coords().cpu().numpy()
+    V = K ** s.ndim
+    fwd = oracle.conv_kmap(s.coords, oc, s.ndim, K, stride, s.dims)
+    want = np.full((s.n, V), -1, dtype=np.int32)
+    q, v = np.nonzero(fwd >= 0)
+    want[fwd[q, v], V - 1 - v] = q  # a relabelling of the forward tuples
+    assert np.array_equal(mt.nbr().cpu().numpy(), want), "transposed neighbour table differs"
+    assert mt.map_size() == m.map_size()
+    dt = TORCH_DT[dtype]
+    g = torch.from_numpy(scenes.features(31, ho.n, c_out)).to(dt).cuda()
+    W = torch.from_numpy(scenes.weights(32, V, c_in, c_out, std=1.0 if dtype == "f32" else None)).to(dt).cuda()
+    gin = sc.sc_subm_conv_bwd_data(mt, g, W)
+    torch.cuda.synchronize()
+    ref = oracle.sparse_conv_bwd_data(s.coords, oc, g.double().cpu().numpy(), W.double().cpu().numpy(), s.ndim, K,
+                                      stride, s.dims)
+    assert_close(gin, ref, dtype, f"{name} K={K} s={stride} input gradient")
+    mt.check()
