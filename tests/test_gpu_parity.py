@@ -327,3 +327,43 @@ def test_profile_only_brackets_the_named_kernels():
         sc.profile_only(None)
     timed = {k for k, (launches, _) in prof.items() if launches}
     assert timed == {"subm_conv_fused"} and prof["subm_conv_fused"][0] == 1
+
+
+@pytest.mark.parametrize("order", [False, True])
+@pytest.mark.parametrize("K", [3, 5])
+def test_coordinates_at_the_top_of_the_key_fields(K, order):
+    """Points in the far corner of the largest grid (every axis 65535 wide,
+    coordinates up to 65534) and at the largest batch id, next to points at
+    the origin: the map bit-exact, the layer within the bar, and a stride-2
+    layer's output set (extents 32768) exact."""
+    rng = np.random.default_rng(K)
+    dims = (65535, 65535, 65535)
+    corner = np.stack(np.meshgrid(np.arange(65528, 65535), np.arange(65528, 65535), np.arange(65530, 65535),
+                                  indexing="ij"), -1).reshape(-1, 3)
+    corner = corner[rng.random(len(corner)) < 0.45]
+    origin = np.stack(np.meshgrid(np.arange(0, 6), np.arange(0, 6), np.arange(0, 4), indexing="ij"), -1).reshape(-1, 3)
+    origin = origin[rng.random(len(origin)) < 0.5]
+    coords = np.concatenate([np.c_[np.full(len(corner), 65534), corner], np.c_[np.zeros(len(corner), int), corner],
+                             np.c_[np.full(len(origin), 65534), origin], np.c_[np.zeros(len(origin), int), origin]])
+    coords = coords[rng.permutation(len(coords))].astype(np.int32)
+    c = torch.from_numpy(coords).cuda()
+    h = sc.sc_hash_build(c)
+    m = sc.sc_kmap_build(h, 3, K, dims, order=order)
+    nbr_ref = oracle.kmap(coords, 3, K, dims)
+    assert np.array_equal(m.nbr().cpu().numpy(), nbr_ref)
+    V = K ** 3
+    f = torch.from_numpy(scenes.features(K, len(coords), 32)).half().cuda()
+    W = torch.from_numpy(scenes.weights(K + 1, V, 32, 32)).half().cuda()
+    out = sc.sc_subm_conv_fwd(m, f, W)
+    ref = oracle.subm_conv(coords, f.double().cpu().numpy(), W.double().cpu().numpy(), 3, K, dims)
+    assert_close(out, ref, "f16", f"K={K} at the top of the key fields")
+    ho = sc.sc_hash_build_conv_out(h, 3, K, 2, dims)
+    oc = ho.coords().cpu().numpy()
+    want = oracle.conv_out_coords(coords, 3, K, 2, dims)
+    got = oc[np.lexsort((oc[:, 3], oc[:, 2], oc[:, 1], oc[:, 0]))]
+    assert np.array_equal(got, want)
+    assert int(oc[:, 1:].max()) <= 32767
+    ms = sc.sc_kmap_build_conv(h, ho, 3, K, 2, dims, order=order)
+    assert np.array_equal(ms.nbr().cpu().numpy(), oracle.conv_kmap(coords, oc, 3, K, 2, dims))
+    m.check()
+    ms.check()
