@@ -234,7 +234,8 @@ sc_status sc_kmap_build_conv(sc_hash in, sc_hash out_set, int ndim, int K, int s
  * yet known on the host. */
 sc_status sc_kmap_info(sc_kmap m, int64_t* n, int32_t* volume, int64_t* map_size, sc_stream stream);
 
-/* Synchronises and returns the latched hash and map status. */
+/* Synchronises the stream and returns the latched hash and map status (it
+ * reads the two status words only). */
 sc_status sc_kmap_check(sc_kmap m, sc_stream stream);
 
 /*

@@ -571,7 +571,13 @@ sc_status sc_kmap_info(sc_kmap m, int64_t* n, int32_t* volume, int64_t* map_size
 
 sc_status sc_kmap_check(sc_kmap m, sc_stream stream) {
   if (!m) return set_error(SC_ERR_INVALID_ARG, "kmap handle is NULL");
-  return sync_host(&m->k, reinterpret_cast<cudaStream_t>(stream));
+  // the status words only (the map's and the hash's copy): one small read
+  int bits[2] = {0, 0};
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(bits, m->k.status, 2 * sizeof(int), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return set_cuda_error(e, "kmap check");
+  return status_from_bits(bits[0] | bits[1]);
 }
 
 sc_status sc_kmap_export(sc_kmap m, int32_t* nbr, int64_t* offs, int32_t* in_rows, int32_t* out_rows,
