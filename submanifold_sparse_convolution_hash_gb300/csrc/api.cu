@@ -6,6 +6,7 @@
 #include <atomic>
 #include <cstdio>
 #include <cstring>
+#include <map>
 #include <mutex>
 #include <string>
 #include <vector>
@@ -117,6 +118,41 @@ int device_sm_count() {
     cache[dev] = v > 0 ? v : 1;
   }
   return cache[dev];
+}
+
+sc_status kernel_setup(const void* kern, size_t smem, int* num_regs) {
+  struct Entry {
+    size_t smem = 0;
+    int regs = 0;
+  };
+  static std::mutex mu;
+  static std::map<std::pair<int, const void*>, Entry> cache;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return set_cuda_error(e, "cudaGetDevice");
+  std::lock_guard<std::mutex> lk(mu);
+  auto it = cache.find({dev, kern});
+  if (it == cache.end()) {
+    cudaFuncAttributes fa{};
+    e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return set_cuda_error(e, "kernel attribute query");
+    // the kernels live in shared memory: the largest carveout (occupancy
+    // planning assumes it)
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return set_cuda_error(e, "kernel carveout attribute");
+    Entry en;
+    en.regs = fa.numRegs;
+    it = cache.emplace(std::make_pair(dev, kern), en).first;
+  }
+  if (smem > it->second.smem) {
+    if (smem > 48 * 1024) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+      if (e != cudaSuccess) return set_cuda_error(e, "kernel shared-memory attribute");
+    }
+    it->second.smem = smem;
+  }
+  if (num_regs) *num_regs = it->second.regs;
+  return SC_OK;
 }
 
 // The device's default stream-ordered pool keeps freed blocks for reuse

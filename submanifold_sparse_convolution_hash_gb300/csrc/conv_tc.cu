@@ -672,17 +672,11 @@ template <int BK, int MODE, bool BF16, int NPW, int T>
 sc_status launch_tc(const TcParams& prm, const Plan& pl, cudaStream_t s, const char* name) {
   auto kern = k_conv_tc<BK, MODE, BF16, NPW, T>;
   constexpr int threads = (NPW + 6) * 32;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(pl.smem));
-  if (e != cudaSuccess) return set_cuda_error(e, "conv smem attribute");
-  // the kernel lives in shared memory: ask for the largest carveout (the
-  // occupancy query below also assumes it)
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
-  if (e != cudaSuccess) return set_cuda_error(e, "conv carveout attribute");
+  int num_regs = 0;
+  sc_status st = kernel_setup(reinterpret_cast<const void*>(kern), pl.smem, &num_regs);
+  if (st) return st;
   // resident CTAs per SM: the plan's count, or fewer if registers say so
-  cudaFuncAttributes fa{};
-  e = cudaFuncGetAttributes(&fa, kern);
-  if (e != cudaSuccess) return set_cuda_error(e, "conv attribute query");
-  const int regs_cta = ((fa.numRegs + 7) / 8) * 8 * threads;
+  const int regs_cta = ((num_regs + 7) / 8) * 8 * threads;
   const int fit = regs_cta > 0 ? 65536 / regs_cta : pl.ctas_per_sm;
   int cps = fit < pl.ctas_per_sm ? (fit < 1 ? 1 : fit) : pl.ctas_per_sm;
   if (const char* ev = getenv("SC_DEV_FORCECPS")) cps = atoi(ev);
@@ -690,10 +684,10 @@ sc_status launch_tc(const TcParams& prm, const Plan& pl, cudaStream_t s, const c
   const int grid = prm.num_units < slots ? prm.num_units : slots;
   if (getenv("SC_DEV_VERBOSE")) {
     fprintf(stderr, "%s: bk %d npw %d t %d nbuf %d group %d stages %d smem %zu plan cps %d fit %d grid %d regs %d\n",
-            name, BK, NPW, T, pl.nbuf, pl.group, pl.stages, pl.smem, pl.ctas_per_sm, fit, grid, fa.numRegs);
+            name, BK, NPW, T, pl.nbuf, pl.group, pl.stages, pl.smem, pl.ctas_per_sm, fit, grid, num_regs);
   }
   SC_LAUNCH(name, s, kern<<<grid, threads, pl.smem, s>>>(prm));
-  e = cudaGetLastError();
+  cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? SC_OK : set_cuda_error(e, name);
 }
 

@@ -456,14 +456,12 @@ bool wg_plan(int c_in, int c_out, WgPlan* pl) {
 template <bool BF16, int NPW, int KT>
 sc_status launch_wgrad_tc(const WgParams& prm, const WgPlan& pl, cudaStream_t s) {
   auto kern = k_wgrad_tc<BF16, NPW, KT>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(pl.smem));
-  if (e != cudaSuccess) return set_cuda_error(e, "wgrad smem attribute");
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
-  if (e != cudaSuccess) return set_cuda_error(e, "wgrad carveout attribute");
+  sc_status st = kernel_setup(reinterpret_cast<const void*>(kern), pl.smem, nullptr);
+  if (st) return st;
   const int slots = device_sm_count() * pl.cps;
   const int grid = prm.num_units < slots ? prm.num_units : slots;
   SC_LAUNCH("subm_conv_wgrad", s, kern<<<grid, (NPW + 5) * 32, pl.smem, s>>>(prm));
-  e = cudaGetLastError();
+  cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? SC_OK : set_cuda_error(e, "wgrad launch");
 }
 

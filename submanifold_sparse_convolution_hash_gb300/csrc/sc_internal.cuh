@@ -129,6 +129,13 @@ sc_status set_error(sc_status s, const char* msg);
 
 int device_sm_count();
 
+// Prepares a kernel for a launch with `smem` bytes of dynamic shared memory:
+// raises its shared-memory limit (and asks for the largest carveout) the
+// first time a device needs that much, and reports its registers per
+// thread.  Cached per device and kernel, so a launch costs no attribute
+// calls once warm.
+sc_status kernel_setup(const void* kern, size_t smem, int* num_regs);
+
 // kernels: hash + map (hash_kmap.cu)
 sc_status launch_hash_insert(const int32_t* coords, int64_t n, HashTable* h, cudaStream_t s);
 sc_status launch_hash_query(const HashTable* h, const int32_t* q, int64_t m, int32_t* rows,
