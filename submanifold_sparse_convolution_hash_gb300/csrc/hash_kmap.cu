@@ -321,8 +321,6 @@ struct BuildArgs {
   int V, K, ndim, dimx, dimy, dimz;  // extents of the table's grid
   int qex, qey, qez;               // extents of the queries' grid
   int stride;                      // forward: query o looks up the table points at stride * o + d
-  int transposed;                  // the queries are a layer's inputs c, the table its outputs o with
-                                   // stride * o + d = c; the offset stored is -d (index V - 1 - idx(d))
   int identity;                    // the centre list is the identity (submanifold: queries = inputs)
   int up;                          // points per unit (128, or 32 when V > 128)
   int nunits;
@@ -341,6 +339,12 @@ struct BuildArgs {
 
 // Dynamic shared memory: s_tile [up * V] ints, s_bal [V * up / 32].
 // Five blocks per SM (register budget): 2560 lookups in flight per SM.
+// TR: a transposed map: the queries are a layer's inputs c, the table its
+// outputs o with stride * o + d = c, and the offset stored is -d (index
+// V - 1 - idx(d)).
+// Measured: four lookups in flight at three blocks per SM were no faster at
+// 5x5x5 (1.04 ms against 1.02 ms at 2M voxels).
+template <bool TR>
 __global__ void __launch_bounds__(kThreads, 5) k_kmap_build(const BuildArgs a) {
   extern __shared__ int4 smem4[];
   const int up = a.up, V = a.V;
@@ -384,8 +388,8 @@ __global__ void __launch_bounds__(kThreads, 5) k_kmap_build(const BuildArgs a) {
     //   forward:    t in [s q - r, s q + r] (inside the table's grid), d = t - s q
     //   transposed: t with q - r <= s t <= q + r (inside it),           d = s t - q
     const int sz = a.ndim == 3 ? a.stride : 1;
-    int xl, xh, yl, yh, zl, zh, mxy, mz, cx, cy, cz;
-    if (!a.transposed) {
+    int xl, xh, yl, yh, zl, zh, cx, cy, cz;
+    if (!TR) {
       cx = qx * a.stride;
       cy = qy * a.stride;
       cz = qz * sz;
@@ -395,7 +399,6 @@ __global__ void __launch_bounds__(kThreads, 5) k_kmap_build(const BuildArgs a) {
       yh = min(cy + r, a.dimy - 1);
       zl = max(cz - rz, 0);
       zh = min(cz + rz, a.dimz - 1);
-      mxy = mz = 1;
     } else {
       cx = qx;
       cy = qy;
@@ -403,8 +406,6 @@ __global__ void __launch_bounds__(kThreads, 5) k_kmap_build(const BuildArgs a) {
       out_range(qx, r, a.stride, a.dimx, xl, xh);
       out_range(qy, r, a.stride, a.dimy, yl, yh);
       out_range(qz, rz, sz, a.dimz, zl, zh);
-      mxy = a.stride;
-      mz = sz;
       if (xl > xh || yl > yh || zl > zh) valid = false;  // no table point can hold one
     }
     const unsigned long long batch = ck & 0xFFFF000000000000ull;
@@ -443,9 +444,13 @@ __global__ void __launch_bounds__(kThreads, 5) k_kmap_build(const BuildArgs a) {
           const int bx = xlo + t / (nb * nbz), by = ylo + (t / nbz) % nb, bz = zlo + t % nbz;
 #pragma unroll
           for (int l = 0; l < 8; ++l) {
+            // offset of voxel t: t - c (forward), stride * t - c (transposed);
+            // a voxel outside the neighbourhood has |d| > r on some axis (the
+            // table holds no point outside its grid, so no bound is needed)
             const int tx = 2 * bx + (l >> 2), ty = 2 * by + ((l >> 1) & 1), tz = 2 * bz + (l & 1);
-            if (tx >= xl && tx <= xh && ty >= yl && ty <= yh && tz >= zl && tz <= zh) {
-              const int dx = tx * mxy - cx, dy = ty * mxy - cy, dz = tz * mz - cz;
+            const int dx = (TR ? tx * a.stride : tx) - cx, dy = (TR ? ty * a.stride : ty) - cy,
+                      dz = (TR ? tz * sz : tz) - cz;
+            if (dx >= -r && dx <= r && dy >= -r && dy <= r && dz >= -rz && dz <= rz) {
               const int v = a.ndim == 3 ? ((dx + r) * a.K + (dy + r)) * a.K + (dz + r) : (dx + r) * a.K + (dy + r);
               s_tile[p * V + v] = pick(r0[q], r1[q], l);
             }
@@ -924,7 +929,6 @@ sc_status launch_kmap_build(const HashTable* in, const HashTable* h, KernelMap* 
   a.qex = q_ext[0];
   a.qey = q_ext[1];
   a.qez = q_ext[2];
-  a.transposed = m->transposed ? 1 : 0;
   a.up = m->up;
   a.nunits = m->nunits;
   a.nbr = m->nbr;
@@ -944,12 +948,19 @@ sc_status launch_kmap_build(const HashTable* in, const HashTable* h, KernelMap* 
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64 || !done[dev]) {
-      e = cudaFuncSetAttribute(k_kmap_build, cudaFuncAttributeMaxDynamicSharedMemorySize, kBuildSmemMax);
+      const void* kerns[2] = {reinterpret_cast<const void*>(k_kmap_build<false>),
+                              reinterpret_cast<const void*>(k_kmap_build<true>)};
+      e = cudaSuccess;
+      for (int k = 0; k < 2 && e == cudaSuccess; ++k)
+        e = cudaFuncSetAttribute(kerns[k], cudaFuncAttributeMaxDynamicSharedMemorySize, kBuildSmemMax);
       if (e != cudaSuccess) return set_cuda_error(e, "kmap_build smem attribute");
       if (dev >= 0 && dev < 64) done[dev] = true;
     }
   }
-  SC_LAUNCH("kmap_build", s, k_kmap_build<<<m->nunits, kThreads, smem, s>>>(a));
+  if (m->transposed)
+    SC_LAUNCH("kmap_build", s, (k_kmap_build<true><<<m->nunits, kThreads, smem, s>>>(a)));
+  else
+    SC_LAUNCH("kmap_build", s, (k_kmap_build<false><<<m->nunits, kThreads, smem, s>>>(a)));
   e = cudaGetLastError();
   if (e != cudaSuccess) return set_cuda_error(e, "kmap_build launch");
   if (!m->perm) return SC_OK;
