@@ -97,9 +97,10 @@ __device__ __forceinline__ bool coord_fields_ok(int4 c) {
          static_cast<unsigned>(c.z) < 65535u && static_cast<unsigned>(c.w) < 65535u;
 }
 
-// Insert: find or claim the entry of the voxel's block (CAS on the block
-// key), then CAS the voxel's row slot from -1 to its row id; a slot that is
-// already taken means two rows share the coordinate.
+// Insert: find or claim the entry of the voxel's block (a compare-and-swap
+// of the block key against the empty key, which returns the key found), then
+// CAS the voxel's row slot from -1 to its row id; a slot that is already
+// taken means two rows share the coordinate.
 __global__ void __launch_bounds__(256) k_hash_insert(const int4* __restrict__ coords, int64_t n,
                                                      BlockEntry* __restrict__ table, uint32_t mask,
                                                      unsigned long long* __restrict__ keys,
@@ -123,12 +124,10 @@ __global__ void __launch_bounds__(256) k_hash_insert(const int4* __restrict__ co
     uint32_t h = block_home(bk, mask);
     int e = -1;
     for (uint32_t probe = 0; probe <= mask; ++probe) {
-      unsigned long long k = __ldcg(&table[h].key);
-      if (k == kEmptyKey) {
-        k = atomicCAS(&table[h].key, kEmptyKey, bk);
-        if (k == kEmptyKey) k = bk;
-      }
-      if (k == bk) {
+      // one round trip: the swap either claims an empty entry or returns the
+      // key already there
+      unsigned long long k = atomicCAS(&table[h].key, kEmptyKey, bk);
+      if (k == kEmptyKey || k == bk) {
         e = static_cast<int>(h);
         break;
       }
