@@ -347,6 +347,34 @@ sc_status sc_subm_conv_bwd_weight(sc_kmap m, const void* d_feats, const void* d_
 sc_status sc_subm_conv_fwd_noalloc(sc_kmap m, const void* d_feats, const void* d_W, void* d_out, int c_in,
                                    int c_out, sc_dtype dtype, unsigned flags, sc_stream stream);
 
+/* ------------------------------------------------------- device memory -- */
+
+/*
+ * Where the library's device memory comes from: the buffers a hash or map
+ * handle owns and the temporaries of a call (packed weights, accumulators).
+ * By default CUDA's stream-ordered pool (cudaMallocAsync / cudaFreeAsync on
+ * the call's stream; the pool keeps freed blocks for reuse).  With
+ * sc_set_allocator the library asks the caller's allocator instead, so an
+ * application can keep all device memory in one pool (the Python binding
+ * offers PyTorch's caching allocator).  The source pages have no counterpart.
+ *
+ * alloc(bytes, stream, ctx) returns device memory of at least `bytes`,
+ * 256-byte aligned, usable in stream order on `stream` (the stream of the
+ * call that allocates), or NULL (the call then fails with SC_ERR_OOM).
+ * free(ptr, stream, ctx) releases it; `stream` is the stream of the call
+ * that frees (a handle's destroy, or the allocating call for temporaries),
+ * after whose queued work the memory may be reused.  A buffer goes back to
+ * the allocator that made it, whatever is set when it is freed.  Pass
+ * NULL, NULL to return to the stream-ordered pool; both or neither must be
+ * set (else SC_ERR_INVALID_ARG).  The setting is global to the process and
+ * thread-safe; the callbacks run on the thread of the library call and must
+ * not call back into the library.  sc_subm_conv_fwd_noalloc allocates
+ * nothing either way.
+ */
+typedef void* (*sc_alloc_fn)(size_t bytes, sc_stream stream, void* ctx);
+typedef void (*sc_free_fn)(void* ptr, sc_stream stream, void* ctx);
+sc_status sc_set_allocator(sc_alloc_fn alloc, sc_free_fn free_fn, void* ctx);
+
 /* ---------------------------------------------------------- diagnostics -- */
 
 const char* sc_status_str(sc_status s);

@@ -71,6 +71,7 @@ def lib():
             "sc_subm_conv_bwd_weight": ([P, P, P, P, I32, I32, I32, U, P], I32),
             "sc_subm_conv_tune": ([P, P, P, P, I32, I32, I32, U, I32, P, P], I32),
             "sc_subm_conv_fwd_noalloc": ([P, P, P, P, I32, I32, I32, U, P], I32),
+            "sc_set_allocator": ([P, P, P], I32),
             "sc_status_str": ([I32], ctypes.c_char_p),
             "sc_last_error": ([], ctypes.c_char_p),
             "sc_launch_count": ([], I64),
@@ -93,7 +94,7 @@ def exported_symbols() -> list:
                         "sc_hash_build_conv_out", "sc_hash_coords", "sc_kmap_build_conv",
                         "sc_kmap_build", "sc_kmap_info", "sc_kmap_check", "sc_kmap_export", "sc_kmap_destroy",
                         "sc_subm_conv_fwd", "sc_subm_conv_tune", "sc_subm_conv_fwd_noalloc",
-                        "sc_subm_conv_bwd_data", "sc_subm_conv_bwd_weight",
+                        "sc_subm_conv_bwd_data", "sc_subm_conv_bwd_weight", "sc_set_allocator",
                         "sc_status_str", "sc_last_error",
                         "sc_launch_count", "sc_profile_enable", "sc_profile_only", "sc_profile_collect",
                         "sc_profile_reset",
@@ -368,6 +369,34 @@ def sc_subm_conv_tune(kmap: KernelMap, feats: torch.Tensor, W: torch.Tensor, out
                                    SC_RELU if relu else 0, reps, _stream(stream), ctypes.byref(chosen)),
            "sc_subm_conv_tune")
     return VARIANT_NAMES[chosen.value]
+
+
+_ALLOC_FN = ctypes.CFUNCTYPE(ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p)
+_FREE_FN = ctypes.CFUNCTYPE(None, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p)
+_torch_allocator = None  # the callbacks stay alive: buffers they made are freed through them
+
+
+def use_torch_allocator(on: bool = True):
+    """Route the library's device memory through PyTorch's caching allocator
+    (on) or back to CUDA's stream-ordered pool (off) (sc_set_allocator)."""
+    global _torch_allocator
+    if not on:
+        _check(lib().sc_set_allocator(None, None, None), "sc_set_allocator")
+        return
+    if _torch_allocator is None:
+        def _alloc(nbytes, stream, ctx):
+            try:
+                return torch.cuda.caching_allocator_alloc(int(nbytes), stream=int(stream or 0))
+            except Exception:
+                return None
+
+        def _free(ptr, stream, ctx):
+            torch.cuda.caching_allocator_delete(int(ptr))
+
+        _torch_allocator = (_ALLOC_FN(_alloc), _FREE_FN(_free))
+    a = ctypes.cast(_torch_allocator[0], ctypes.c_void_p)
+    f = ctypes.cast(_torch_allocator[1], ctypes.c_void_p)
+    _check(lib().sc_set_allocator(a, f, None), "sc_set_allocator")
 
 
 def launch_count() -> int:

@@ -8,6 +8,7 @@
 #include <cstring>
 #include <map>
 #include <mutex>
+#include <unordered_map>
 #include <string>
 #include <vector>
 
@@ -171,10 +172,41 @@ void keep_pool_memory() {
   done[dev] = true;
 }
 
+namespace {
+// The caller's allocator (sc_set_allocator), if any, and the allocator that
+// made each live buffer it handed out, so a buffer goes back to its own
+// allocator whatever is set when it is freed.
+struct Allocator {
+  sc_alloc_fn alloc = nullptr;
+  sc_free_fn free = nullptr;
+  void* ctx = nullptr;
+};
+std::mutex g_alloc_mu;
+Allocator g_alloc;
+std::unordered_map<void*, Allocator> g_alloc_owner;
+}  // namespace
+
 sc_status dev_alloc(void** p, size_t bytes, cudaStream_t s) {
   *p = nullptr;
-  keep_pool_memory();
   if (bytes == 0) bytes = 16;
+  Allocator a;
+  {
+    std::lock_guard<std::mutex> lk(g_alloc_mu);
+    a = g_alloc;
+  }
+  if (a.alloc) {
+    void* q = a.alloc(bytes, reinterpret_cast<sc_stream>(s), a.ctx);
+    if (!q) return set_error(SC_ERR_OOM, "the caller's allocator returned NULL");
+    if (reinterpret_cast<uintptr_t>(q) % 256) {
+      a.free(q, reinterpret_cast<sc_stream>(s), a.ctx);
+      return set_error(SC_ERR_INVALID_ARG, "the caller's allocator returned memory that is not 256-byte aligned");
+    }
+    std::lock_guard<std::mutex> lk(g_alloc_mu);
+    g_alloc_owner[q] = a;
+    *p = q;
+    return SC_OK;
+  }
+  keep_pool_memory();
   cudaError_t e = cudaMallocAsync(p, bytes, s);
   if (e != cudaSuccess) {
     *p = nullptr;
@@ -184,7 +216,20 @@ sc_status dev_alloc(void** p, size_t bytes, cudaStream_t s) {
 }
 
 void dev_free(void* p, cudaStream_t s) {
-  if (p) cudaFreeAsync(p, s);
+  if (!p) return;
+  Allocator a;
+  bool caller = false;
+  {
+    std::lock_guard<std::mutex> lk(g_alloc_mu);
+    auto it = g_alloc_owner.find(p);
+    if (it != g_alloc_owner.end()) {
+      a = it->second;
+      g_alloc_owner.erase(it);
+      caller = true;
+    }
+  }
+  if (caller) a.free(p, reinterpret_cast<sc_stream>(s), a.ctx);
+  else cudaFreeAsync(p, s);
 }
 
 namespace {
@@ -303,6 +348,16 @@ const char* sc_status_str(sc_status s) {
     case SC_ERR_TIMEOUT: return "device-side wait timed out";
   }
   return "unknown status";
+}
+
+sc_status sc_set_allocator(sc_alloc_fn alloc, sc_free_fn free_fn, void* ctx) {
+  if ((alloc == nullptr) != (free_fn == nullptr))
+    return set_error(SC_ERR_INVALID_ARG, "set both alloc and free, or neither");
+  std::lock_guard<std::mutex> lk(g_alloc_mu);
+  g_alloc.alloc = alloc;
+  g_alloc.free = free_fn;
+  g_alloc.ctx = ctx;
+  return SC_OK;
 }
 
 const char* sc_last_error(void) { return g_last_error.c_str(); }
