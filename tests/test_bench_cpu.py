@@ -1,0 +1,68 @@
+"""Host logic of bench.py (no GPU): the algorithmic-byte models behind the
+roofline, the staleness check of recorded DRAM traffic, and the parsing of
+sampled clocks and throttle reasons."""
+import hashlib
+import json
+import os
+
+import bench
+
+
+def test_algorithmic_bytes_of_the_fused_layer():
+    N, V, M, s = 1000, 27, 9000, 2
+    # gathered rows M C_in s, one write per output row N C_out s, the
+    # neighbour table 4 N V, the weights V C_in C_out s
+    want = M * 32 * s + N * 64 * s + 4 * N * V + V * 32 * 64 * s
+    assert bench.algo_bytes_step("subm_conv_fused", N, V, M, [(32, 64)], s, 0) == want
+    # two layers add up; the backward pass adds each layer's input gradient (64 -> 32)
+    two = bench.algo_bytes_step("subm_conv_fused", N, V, M, [(32, 64), (64, 64)], s, 0)
+    assert two == want + (M * 64 * s + N * 64 * s + 4 * N * V + V * 64 * 64 * s)
+    bwd = bench.algo_bytes_step("subm_conv_fused", N, V, M, [(32, 64)], s, 0, backward=True)
+    assert bwd == want + (M * 64 * s + N * 32 * s + 4 * N * V + V * 64 * 32 * s)
+
+
+def test_algorithmic_bytes_of_map_and_gradient_kernels():
+    N, V, M, s = 1000, 27, 9000, 2
+    lists = 8 * (M - N)  # the centre's tuples are implicit in a submanifold map
+    assert bench.algo_bytes_step("kmap_build", N, V, M, [(32, 32)], s, 0) == 8 * N + 4 * N * V + lists
+    assert bench.algo_bytes_step("hash_insert", N, V, M, [(32, 32)], s, 0) == 28 * N
+    wg = bench.algo_bytes_step("subm_conv_wgrad", N, V, M, [(32, 64)], s, 0)
+    assert wg == M * (32 + 64) * s + 4 * V * 32 * 64 + lists
+    # a strided layer's map lists every tuple and has n_out rows
+    n_out = 400
+    assert bench.algo_bytes_step("kmap_build", N, V, M, [(32, 32)], s, 0, n_out=n_out) == \
+        8 * n_out + 4 * n_out * V + 8 * M
+    assert bench.algo_bytes_step("no_such_kernel", N, V, M, [(32, 32)], s, 0) is None
+
+
+def test_recorded_traffic_is_dropped_once_the_source_changes(tmp_path, monkeypatch):
+    src = tmp_path / "kernel.cu"
+    src.write_text("// version 1\n")
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    rec = {"k@w": {"source": "kernel.cu", "sha256": hashlib.sha256(src.read_bytes()).hexdigest(),
+                   "dram_bytes_per_launch": 1234}}
+    (prof / "traffic.json").write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.recorded_traffic("k", "w") == 1234
+    assert bench.recorded_traffic("k", "other") is None
+    src.write_text("// version 2\n")
+    assert bench.recorded_traffic("k", "w") is None
+
+
+def test_committed_traffic_records_name_existing_sources():
+    d = json.load(open(os.path.join(bench.ROOT, "profiles", "traffic.json")))
+    for key, r in d.items():
+        assert os.path.exists(os.path.join(bench.ROOT, r["source"])), key
+        assert r["dram_bytes_per_launch"] > 0 and len(r["sha256"]) == 64
+        assert r["command"].startswith("ncu ") and "--clock-control none" in r["command"], key
+
+
+def test_clock_summary_reads_reasons():
+    c = bench.ClockSampler(0)
+    c.lines = ["2070, 2070, 900.5, 0x0, Not Active, Not Active, Not Active, Not Active",
+               "1980, 2070, 1390.0, 0x4, Not Active, Not Active, Not Active, Active",
+               "garbage"]
+    s = c.summary()
+    assert s["samples"] == 2 and s["sm_max_mhz"] == 2070.0 and s["reasons"] == ["sw_power_cap"]
+    assert s["sm_mhz"] == (2070.0 + 1980.0) / 2
