@@ -5,6 +5,7 @@
 
 #include <atomic>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -431,6 +432,15 @@ sc_status sc_hash_build(const int32_t* d_coords, int64_t n, sc_stream stream, sc
   int64_t cap = 16;
   const int64_t want = 2 * n * static_cast<int64_t>(sizeof(BlockEntry)) <= (int64_t(256) << 20) ? 2 * n : n;
   while (cap < want) cap <<= 1;
+  // developer override for testing the full-table path: SC_DEV_HASH_CAPACITY
+  // entries (rounded up to a power of two, at least 16)
+  if (const char* ev = getenv("SC_DEV_HASH_CAPACITY")) {
+    const long long c = atoll(ev);
+    if (c > 0) {
+      cap = 16;
+      while (cap < c) cap <<= 1;
+    }
+  }
   t.capacity = cap;
   const size_t tb = sizeof(BlockEntry) * static_cast<size_t>(cap);
   const size_t kb = (sizeof(unsigned long long) * static_cast<size_t>(n > 0 ? n : 1) + 255) & ~size_t(255);

@@ -367,3 +367,27 @@ def test_coordinates_at_the_top_of_the_key_fields(K, order):
     assert np.array_equal(ms.nbr().cpu().numpy(), oracle.conv_kmap(coords, oc, 3, K, 2, dims))
     m.check()
     ms.check()
+
+
+def test_full_table_is_reported(monkeypatch):
+    """A table forced too small (developer capacity override) makes the
+    insert latch SC_ERR_TABLE_FULL after probing every entry; the map build
+    reports it and the library stays usable.  Every probe loop is bounded by
+    the table's size, so nothing waits."""
+    rng = np.random.default_rng(4)
+    pts = np.unique(rng.integers(0, 200, size=(400, 3)) * 2, axis=0)  # one point per 2x2x2 block
+    coords = torch.from_numpy(np.c_[np.zeros(len(pts), int), pts].astype(np.int32)).cuda()
+    monkeypatch.setenv("SC_DEV_HASH_CAPACITY", "16")
+    h = sc.sc_hash_build(coords)
+    monkeypatch.delenv("SC_DEV_HASH_CAPACITY")
+    assert h.capacity == 16
+    with pytest.raises(ScError) as e:
+        h.check()
+    assert e.value.code == 4
+    with pytest.raises(ScError) as e:
+        sc.sc_kmap_build(h, 3, 3, (400, 400, 400))
+    assert e.value.code == 4
+    h2 = sc.sc_hash_build(coords)
+    assert h2.capacity >= 2 * len(pts)
+    m2 = sc.sc_kmap_build(h2, 3, 3, (400, 400, 400))
+    assert np.array_equal(m2.nbr().cpu().numpy(), oracle.kmap(coords.cpu().numpy(), 3, 3, (400, 400, 400)))
