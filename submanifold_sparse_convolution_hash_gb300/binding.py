@@ -309,7 +309,9 @@ def _conv_args(kmap, feats, W, out):
 
 def sc_subm_conv_fwd(kmap: KernelMap, feats: torch.Tensor, W: torch.Tensor, out: torch.Tensor | None = None,
                      relu: bool = False, variant: str | None = None, stream=None) -> torch.Tensor:
-    """out[q] = act(sum over map tuples (p, q, d) of feats[p] @ W[d]); same rows as feats."""
+    """out[q] = act(sum over map tuples (p, q, d) of feats[p] @ W[d]).  feats has
+    the map's input rows (kmap.n_in), out its rows (kmap.n): the same for a
+    submanifold map, the output set's for a regular / strided one."""
     f, w, out, c_in, c_out, dt = _conv_args(kmap, feats, W, out)
     flags = (SC_RELU if relu else 0) | (VARIANTS[variant] if variant else 0)
     _check(lib().sc_subm_conv_fwd(kmap._h, _ptr(f), _ptr(w), _ptr(out), c_in, c_out, dt, flags,
@@ -320,7 +322,10 @@ def sc_subm_conv_fwd(kmap: KernelMap, feats: torch.Tensor, W: torch.Tensor, out:
 def sc_subm_conv_bwd_data(kmap: KernelMap, gout: torch.Tensor, W: torch.Tensor, gin: torch.Tensor | None = None,
                           variant: str | None = None, stream=None) -> torch.Tensor:
     """Gradient of a (ReLU-free) layer's loss with respect to its input
-    features: gin[p] = sum over map tuples (p, q, d) of gout[q] @ W[d]^T."""
+    features: gin[p] = sum over map tuples (p, q, d) of gout[q] @ W[d]^T.
+    kmap: the layer's submanifold map, or the transposed map of a regular /
+    strided layer (sc_kmap_build_conv(..., transpose=True)): gout has
+    kmap.n_in rows (the layer's outputs), gin kmap.n (its inputs)."""
     g = _dev(gout, "gout")
     w = _dev(W, "W")
     if g.dtype not in _DTYPES or w.dtype != g.dtype:
