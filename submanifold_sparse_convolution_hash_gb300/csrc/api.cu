@@ -157,6 +157,33 @@ sc_status kernel_setup(const void* kern, size_t smem, int* num_regs) {
   return SC_OK;
 }
 
+sc_status kernel_carveout(const void* kern, int ctas_per_sm, size_t smem) {
+  static std::mutex mu;
+  static std::map<std::pair<int, const void*>, int> last;
+  static int max_smem[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return set_cuda_error(e, "cudaGetDevice");
+  std::lock_guard<std::mutex> lk(mu);
+  int per_sm = dev >= 0 && dev < 64 ? max_smem[dev] : 0;
+  if (!per_sm) {
+    e = cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    if (e != cudaSuccess || per_sm <= 0) return set_cuda_error(e, "shared memory per SM query");
+    if (dev >= 0 && dev < 64) max_smem[dev] = per_sm;
+  }
+  // the CTAs' dynamic shared memory plus the 1 KB the system reserves per CTA
+  const double need = static_cast<double>(ctas_per_sm) * static_cast<double>(smem + 1024);
+  int pct = static_cast<int>((need * 100.0 + per_sm - 1) / per_sm);
+  if (pct > 100) pct = 100;
+  if (pct < 1) pct = 1;
+  auto it = last.find({dev, kern});
+  if (it != last.end() && it->second == pct) return SC_OK;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, pct);
+  if (e != cudaSuccess) return set_cuda_error(e, "kernel carveout attribute");
+  last[{dev, kern}] = pct;
+  return SC_OK;
+}
+
 // The device's default stream-ordered pool keeps freed blocks for reuse
 // (release threshold = unlimited) instead of trimming them at every
 // synchronisation; set once per device on first use.

@@ -612,7 +612,8 @@ size_t plan_smem(const Plan& pl, size_t stage_bytes) {  // stage_bytes: one stag
 // allow, and gives each CTA 4 producer warps at three CTAs per SM, else 8.
 // Developer overrides for measurement sweeps (environment, read per call):
 // SC_DEV_BK, SC_DEV_T, SC_DEV_STAGES, SC_DEV_GROUP, SC_DEV_NPW, SC_DEV_CPS
-// (an upper bound), SC_DEV_FORCECPS (launch that many CTAs per SM) and
+// (an upper bound), SC_DEV_FORCECPS (launch that many CTAs per SM),
+// SC_DEV_MAX_CARVEOUT (keep the largest shared-memory carveout) and
 // SC_DEV_VERBOSE (print each launch's plan).  None changes the result.
 bool make_plan(int c_in, int c_out, bool output_stationary, Plan* pl) {
   pl->bk = pick_bk(c_in);
@@ -680,6 +681,13 @@ sc_status launch_tc(const TcParams& prm, const Plan& pl, cudaStream_t s, const c
   const int fit = regs_cta > 0 ? 65536 / regs_cta : pl.ctas_per_sm;
   int cps = fit < pl.ctas_per_sm ? (fit < 1 ? 1 : fit) : pl.ctas_per_sm;
   if (const char* ev = getenv("SC_DEV_FORCECPS")) cps = atoi(ev);
+  // carveout for exactly these CTAs: the remainder is L1, where the
+  // producers' neighbour-index loads stay resident across a tile's offsets
+  // (with the largest carveout they were re-read from L2 about 7 times)
+  if (!getenv("SC_DEV_MAX_CARVEOUT")) {
+    st = kernel_carveout(reinterpret_cast<const void*>(kern), cps, pl.smem);
+    if (st) return st;
+  }
   const int slots = device_sm_count() * cps;
   const int grid = prm.num_units < slots ? prm.num_units : slots;
   if (getenv("SC_DEV_VERBOSE")) {

@@ -135,6 +135,10 @@ int device_sm_count();
 // thread.  Cached per device and kernel, so a launch costs no attribute
 // calls once warm.
 sc_status kernel_setup(const void* kern, size_t smem, int* num_regs);
+// Sets a kernel's shared-memory carveout to what `ctas_per_sm` CTAs of
+// `smem` bytes need (the rest of the SM's L1/shared array stays L1, which
+// holds the neighbour-index loads); cached, so set only when it changes.
+sc_status kernel_carveout(const void* kern, int ctas_per_sm, size_t smem);
 
 // kernels: hash + map (hash_kmap.cu)
 sc_status launch_hash_insert(const int32_t* coords, int64_t n, HashTable* h, cudaStream_t s);
