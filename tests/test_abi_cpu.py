@@ -24,7 +24,7 @@ def libsc():
     return binding.lib()
 
 
-def test_header_declares_the_north_star_entry_points():
+def test_header_declares_the_hash_map_and_layer_entry_points():
     fns = header_functions()
     for name in ("sc_hash_build", "sc_kmap_build", "sc_subm_conv_fwd"):
         assert name in fns
