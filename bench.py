@@ -40,6 +40,11 @@ import time
 import numpy as np
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
+# the kernels of the map build (hash insert, output set, row order, map,
+# signature sort): their event-timed sum is the step's map-build kernel time
+MAP_KERNELS = ("hash_insert", "out_mark", "out_count", "out_scan", "out_number", "order_count", "order_partials",
+               "order_apply", "order_scatter", "kmap_build", "sig_count", "sig_partials", "sig_scan", "sig_scatter",
+               "sig_present")
 sys.path.insert(0, ROOT)
 
 METRIC = "subm-conv layer effective TFLOP/s, Mvoxels/s & % roofline; kernel-map build ms"
@@ -461,8 +466,7 @@ def run_ours(args):
                          "share": round(tot / tot_all, 4)}
     conv_k = [k for k in prof_all if k.startswith("subm_conv")]
     conv_ms = sum(prof_all[k][1] for k in conv_k) / bd_steps
-    map_names = ("hash_insert", "order_count", "order_partials", "order_apply", "order_scatter", "kmap_build")
-    map_ms = sum(prof_all[k][1] for k in map_names if k in prof_all) / bd_steps
+    map_ms = sum(prof_all[k][1] for k in MAP_KERNELS if k in prof_all) / bd_steps
     peaks = load_peaks()
     ab_step = algo_bytes_step(dom, s.n, V, M, layers, esize, ntiles, args.backward, n_out if general else None)
     launches_per_step = prof[dom][0] / args.steps

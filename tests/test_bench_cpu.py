@@ -66,3 +66,15 @@ def test_clock_summary_reads_reasons():
     s = c.summary()
     assert s["samples"] == 2 and s["sm_max_mhz"] == 2070.0 and s["reasons"] == ["sw_power_cap"]
     assert s["sm_mhz"] == (2070.0 + 1980.0) / 2
+
+
+def test_map_build_time_counts_every_map_kernel():
+    """Every named launch of the hash / map source that runs inside a map
+    build (not the export, query or coordinate read-back helpers) is in the
+    bench's map-build kernel set."""
+    import re
+    src = open(os.path.join(bench.ROOT, "submanifold_sparse_convolution_hash_gb300", "csrc", "hash_kmap.cu")).read()
+    names = set(re.findall(r'SC_LAUNCH\("([a-z_0-9]+)"', src))
+    helpers = {"hash_query", "hash_coords", "kmap_compact", "kmap_unpermute"}
+    assert names - helpers <= set(bench.MAP_KERNELS), sorted(names - helpers - set(bench.MAP_KERNELS))
+    assert not set(bench.MAP_KERNELS) & helpers
