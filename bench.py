@@ -122,6 +122,64 @@ def algo_bytes_step(kernel: str, N: int, V: int, M: int, layers, s: int, ntiles:
     return table.get(kernel)
 
 
+def unique_bytes_op(op: str, N: int, V: int, M: int, ci: int, co: int, s: int, n_out: int | None = None):
+    """The stricter byte model of one layer op: every input row, output row,
+    neighbour-table entry and weight moved once (the algorithmic model counts
+    a gathered row once per tuple).  op "conv": a layer from ci to co channels
+    (an input gradient is the layer from co to ci); op "wgrad": a weight
+    gradient (both row sets once, the lists, the fp32 gradient written)."""
+    No = N if n_out is None else n_out
+    if op == "conv":
+        return N * ci * s + No * co * s + 4 * No * V + V * ci * co * s
+    lists = 8 * (M - N) if n_out is None else 8 * M
+    return N * ci * s + No * co * s + lists + 4 * V * ci * co
+
+
+def unique_bytes_step(N: int, V: int, M: int, layers, s: int, backward: bool = False, n_out: int | None = None):
+    """unique_bytes_op summed over the layer ops of one step: each layer, and
+    with `backward` its input gradient and weight gradient."""
+    total = sum(unique_bytes_op("conv", N, V, M, ci, co, s, n_out) for ci, co in layers)
+    if backward:
+        total += sum(unique_bytes_op("conv", N, V, M, co, ci, s, n_out) + unique_bytes_op("wgrad", N, V, M, ci, co, s,
+                                                                                        n_out) for ci, co in layers)
+    return total
+
+
+def map_build_hbm_frac(prof_all: dict, steps: int, bytes_of, hbm_gbs: float):
+    """Algorithmic bytes over time of the map-build kernels that have a byte
+    model (prof_all: name -> (launches, total ms) over `steps` steps;
+    bytes_of(name): bytes per step or None), as a fraction of `hbm_gbs`."""
+    b = t_ms = 0.0
+    for k in MAP_KERNELS:
+        if k not in prof_all:
+            continue
+        kb = bytes_of(k)
+        if kb:
+            b += kb
+            t_ms += prof_all[k][1] / steps
+    return round(b / (t_ms / 1e3) / (hbm_gbs * 1e9), 4) if t_ms > 0 else None
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine)."""
+    import platform
+    import subprocess
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().lower().startswith("model name:"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for ln in open("/proc/cpuinfo"):
+            if ln.lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.machine() or "unknown"
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -223,7 +281,7 @@ def cpu_oracle_run(s, K, f, W, seconds: float, stride: int = 0):
         el = time.perf_counter() - t0
         if el >= seconds or el * (passes + 1) / passes > 3 * seconds:
             break
-    return {"value": s.n * passes / el / 1e6, "unit": "Mvoxels/s", "cores": oracle.max_threads(),
+    return {"value": s.n * passes / el / 1e6, "unit": "Mvoxels/s", "cores": oracle.max_threads(), "cpu_model": cpu_model(),
             "kind": "oracle",
             "sample": f"full scene (N={s.n}) x {passes} pass(es): hash + map + fp64 layer, {el:.1f} s"}
 
@@ -278,7 +336,7 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "N": s.n, "K": w.K, "c_in": w.channels[0], "c_out": w.channels[1]},
-        "cpu_baseline": {"value": round(value, 4), "unit": "Mvoxels/s", "cores": oracle.max_threads(),
+        "cpu_baseline": {"value": round(value, 4), "unit": "Mvoxels/s", "cores": oracle.max_threads(), "cpu_model": cpu_model(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "Mvoxels/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -489,6 +547,13 @@ def run_ours(args):
     conv_roof_s = sum(roof_s("subm_conv_fused", ci, co) for ci, co in layers)
     if args.backward:
         conv_roof_s += sum(roof_s("subm_conv_fused", co, ci) + roof_s("subm_conv_wgrad", ci, co) for ci, co in layers)
+    # the same with the stricter unique-bytes model of each layer op
+    def roof_unique_s(op, ci, co):
+        return max(2.0 * M * ci * co / (peaks["bf16_tflops"] * 1e12),
+                   unique_bytes_op(op, s.n, V, M, ci, co, esize, n_out if general else None) / (peaks["hbm_gbs"] * 1e9))
+    conv_unique_s = sum(roof_unique_s("conv", ci, co) for ci, co in layers)
+    if args.backward:
+        conv_unique_s += sum(roof_unique_s("conv", co, ci) + roof_unique_s("wgrad", ci, co) for ci, co in layers)
 
     line = {
         "metric": METRIC, "value": round(value, 4), "unit": "Mvoxels/s", "n_gpus": world, "steps": args.steps,
@@ -502,6 +567,11 @@ def run_ours(args):
         "layer_tflops": round(flops / (conv_ms / 1e3) / 1e12, 3) if conv_ms else None,
         "layer_ms": round(conv_ms, 5),
         "layer_roofline_frac": round(conv_roof_s / (conv_ms / 1e3), 4) if conv_ms else None,
+        "layer_unique_roofline_frac": round(conv_unique_s / (conv_ms / 1e3), 4) if conv_ms else None,
+        "kmap_build_hbm_frac": map_build_hbm_frac(
+            prof_all, bd_steps,
+            lambda k: algo_bytes_step(k, s.n, V, M, layers, esize, ntiles, args.backward, n_out if general else None),
+            peaks["hbm_gbs"]),
         "kmap_build_ms": round(map_e2e_ms, 5),
         "kmap_build_kernels_ms": round(map_ms, 5),
         "roofline": roofline,

@@ -78,3 +78,33 @@ def test_map_build_time_counts_every_map_kernel():
     helpers = {"hash_query", "hash_coords", "kmap_compact", "kmap_unpermute"}
     assert names - helpers <= set(bench.MAP_KERNELS), sorted(names - helpers - set(bench.MAP_KERNELS))
     assert not set(bench.MAP_KERNELS) & helpers
+
+
+def test_unique_bytes_model_is_the_stricter_one():
+    N, V, M, s = 1000, 27, 9000, 2
+    # rows once: N C_in s in, N C_out s out, the neighbour table, the weights
+    assert bench.unique_bytes_op("conv", N, V, M, 32, 64, s) == N * 32 * s + N * 64 * s + 4 * N * V + V * 32 * 64 * s
+    assert bench.unique_bytes_op("wgrad", N, V, M, 32, 64, s) == N * (32 + 64) * s + 8 * (M - N) + 4 * V * 32 * 64
+    fwd = bench.unique_bytes_step(N, V, M, [(32, 64)], s)
+    assert fwd < bench.algo_bytes_step("subm_conv_fused", N, V, M, [(32, 64)], s, 0)
+    bwd = bench.unique_bytes_step(N, V, M, [(32, 64)], s, backward=True)
+    assert bwd == fwd + bench.unique_bytes_op("conv", N, V, M, 64, 32, s) + bench.unique_bytes_op("wgrad", N, V, M, 32,
+                                                                                                   64, s)
+    # a strided layer: n_out output rows, every tuple listed
+    assert bench.unique_bytes_op("conv", N, V, M, 32, 32, s, n_out=400) == \
+        N * 32 * s + 400 * 32 * s + 4 * 400 * V + V * 32 * 32 * s
+    assert bench.unique_bytes_op("wgrad", N, V, M, 32, 32, s, n_out=400) == \
+        N * 32 * s + 400 * 32 * s + 8 * M + 4 * V * 32 * 32
+
+
+def test_map_build_hbm_fraction():
+    # two modelled kernels of 1 ms each per step over 4 steps, one unmodelled
+    prof = {"hash_insert": (4, 4.0), "kmap_build": (4, 4.0), "sig_count": (4, 40.0), "subm_conv_fused": (4, 1.0)}
+    nbytes = {"hash_insert": 1e9, "kmap_build": 3e9}
+    frac = bench.map_build_hbm_frac(prof, 4, nbytes.get, 1000.0)
+    assert frac == round(4e9 / 2e-3 / 1e12, 4)  # 2 TB/s of 1 TB/s
+    assert bench.map_build_hbm_frac({"subm_conv_fused": (1, 1.0)}, 1, nbytes.get, 1000.0) is None
+
+
+def test_cpu_model_is_named():
+    assert isinstance(bench.cpu_model(), str) and bench.cpu_model()
