@@ -68,3 +68,42 @@ def test_product_path_does_not_touch_the_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert "oracle" not in text.lower(), f"{f} mentions the oracle"
+
+
+C_CONSUMER = r"""
+#include <stdio.h>
+#include <string.h>
+#include "sc.h"
+
+int main(void) {
+  sc_hash h = NULL;
+  if (strcmp(sc_status_str(SC_OK), "ok") != 0) return 2;
+  /* argument errors come back synchronously, without touching a device */
+  if (sc_hash_build(NULL, -1, NULL, &h) != SC_ERR_INVALID_ARG) return 3;
+  if (h != NULL) return 4;
+  if (sc_last_error() == NULL || strlen(sc_last_error()) == 0) return 5;
+  printf("%s\n", sc_last_error());
+  return 0;
+}
+"""
+
+
+def test_header_serves_a_plain_c_program(libsc, tmp_path):
+    """include/sc.h compiles as strict C99, and a C program links against
+    libsc.so and gets the synchronous argument errors the header states."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "consumer.c"
+    src.write_text(C_CONSUMER)
+    exe = tmp_path / "consumer"
+    libdir = os.path.join(ROOT, "submanifold_sparse_convolution_hash_gb300")
+    cmd = [gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I", os.path.join(ROOT, "include"),
+           str(src), "-o", str(exe), "-L", libdir, "-l:libsc.so", f"-Wl,-rpath,{libdir}"]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, (r.returncode, r.stdout, r.stderr)
+    assert r.stdout.strip()
