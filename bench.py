@@ -281,7 +281,7 @@ def cpu_oracle_run(s, K, f, W, seconds: float, stride: int = 0):
         el = time.perf_counter() - t0
         if el >= seconds or el * (passes + 1) / passes > 3 * seconds:
             break
-    return {"value": s.n * passes / el / 1e6, "unit": "Mvoxels/s", "cores": oracle.max_threads(), "cpu_model": cpu_model(),
+    return {"value": s.n * passes / el / 1e6, "unit": "Mvoxels/s", "cores": oracle.max_threads(), "host_cpus": os.cpu_count(), "cpu_model": cpu_model(),
             "kind": "oracle",
             "sample": f"full scene (N={s.n}) x {passes} pass(es): hash + map + fp64 layer, {el:.1f} s"}
 
@@ -336,7 +336,7 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "N": s.n, "K": w.K, "c_in": w.channels[0], "c_out": w.channels[1]},
-        "cpu_baseline": {"value": round(value, 4), "unit": "Mvoxels/s", "cores": oracle.max_threads(), "cpu_model": cpu_model(),
+        "cpu_baseline": {"value": round(value, 4), "unit": "Mvoxels/s", "cores": oracle.max_threads(), "host_cpus": os.cpu_count(), "cpu_model": cpu_model(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "Mvoxels/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
