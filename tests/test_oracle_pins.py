@@ -233,6 +233,7 @@ def test_dilation_counts():
 @pytest.mark.parametrize("ndim,K,dims,n,batches", [
     (2, 3, (12, 9, 1), 40, 1), (2, 5, (10, 10, 1), 35, 2),
     (3, 3, (6, 7, 5), 60, 2), (3, 5, (6, 6, 6), 50, 1), (3, 1, (4, 4, 4), 10, 1),
+    (3, 7, (9, 9, 8), 80, 2), (2, 7, (12, 11, 1), 50, 1),
 ])
 def test_kmap_equals_brute_force(ndim, K, dims, n, batches):
     coords = random_scene(ndim * 100 + K * 10 + n, n, dims, ndim, batches)
@@ -286,6 +287,8 @@ def test_kmap_errors():
 
 @pytest.mark.parametrize("ndim,K,dims,n,batches,cin,cout", [
     (2, 3, (9, 11, 1), 30, 2, 5, 3), (3, 3, (7, 6, 5), 70, 2, 4, 6), (3, 5, (7, 7, 6), 60, 1, 3, 2),
+    (2, 5, (10, 9, 1), 40, 1, 3, 3), (3, 7, (9, 8, 9), 90, 1, 2, 3), (3, 1, (5, 5, 5), 30, 2, 4, 3),
+    (3, 5, (8, 7, 6), 60, 3, 2, 2),
 ])
 def test_conv_equals_dense_conv(ndim, K, dims, n, batches, cin, cout):
     coords = random_scene(7 + n, n, dims, ndim, batches)
@@ -404,6 +407,7 @@ def dense_conv_grads(coords, feats, W, gout, ndim, K, dims):
 
 @pytest.mark.parametrize("ndim,K,dims,n,batches,cin,cout", [
     (2, 3, (9, 11, 1), 30, 2, 5, 3), (3, 3, (7, 6, 5), 70, 2, 4, 6), (3, 5, (7, 7, 6), 60, 1, 3, 2),
+    (2, 5, (10, 9, 1), 40, 1, 3, 3), (3, 7, (9, 8, 9), 90, 1, 2, 3), (3, 1, (5, 5, 5), 30, 2, 4, 3),
 ])
 def test_backward_equals_dense_conv_autograd(ndim, K, dims, n, batches, cin, cout):
     coords = random_scene(17 + n, n, dims, ndim, batches)
