@@ -107,3 +107,14 @@ def test_header_serves_a_plain_c_program(libsc, tmp_path):
     r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
     assert r.returncode == 0, (r.returncode, r.stdout, r.stderr)
     assert r.stdout.strip()
+
+
+def test_binding_refuses_host_tensors():
+    """No CPU path: a tensor that is not on a CUDA device is refused before
+    any library call."""
+    import torch
+    from submanifold_sparse_convolution_hash_gb300 import binding
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        binding.sc_hash_build(torch.zeros((4, 4), dtype=torch.int32))
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        binding.sc_hash_build(torch.zeros((4, 4), dtype=torch.int32).numpy())
