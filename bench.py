@@ -2,9 +2,12 @@
 """Benchmark of the submanifold sparse convolution hot path on one GPU.
 
 One step = one pass of the whole path over one synthetic scene:
-    sc_hash_build -> sc_kmap_build -> sc_subm_conv_fwd
-on the LiDAR-like workload (1440x1440x41 grid, ~100k voxels, 3x3x3 kernel,
-C_in = C_out = 32, fp16 features and weights, fp32 accumulation).
+    sc_hash_build -> sc_kmap_build -> sc_subm_conv_fwd (every layer)
+By default on the largest single-GPU workload: 2048x2048x64 grid, ~2M
+voxels on synthetic surfaces, 5x5x5 kernel (125 offsets), C_in = C_out =
+128, bf16 features and weights, fp32 accumulation.  --workload 0..3 selects
+the others (2D 200 cells; LiDAR ~100k C 32; indoor ~1M C 64; four LiDAR
+scans with an 8-layer stack 32 -> 256).
 
 Prints one JSON line.  `value` is Mvoxels/s over the timed steps with inputs
 resident in device memory and L2 flushed (a 256 MB write) before every step,
@@ -14,8 +17,12 @@ public API calls: asynchronous map builds with each step's error status
 checked, double-buffered so one step's copies overlap the previous step's
 layers.  `roofline` reports the dominant kernel's
 algorithmic bytes over its average event-timed launch duration against the
-measured HBM copy bandwidth.  `cpu_baseline` times the CPU oracle on the same
-scene on this host's cores.
+measured HBM copy bandwidth.  `cpu_baseline` times the CPU oracle on a
+bounded sample of the same scene on this host's cores (the coordinate table
+over every point, then the map rows and fp64 outputs of evenly spaced rows,
+scaled to the scene).  `clocks` summarises read-only NVML samples of the SM
+clock and its throttle reasons, taken from the first warm-up step to the end
+of the timed steps.
 
 --layer-type regular | strided replaces the workload's layer stack by its
 first layer as a dilating (stride 1) or strided layer: a step is then
@@ -57,7 +64,10 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", type=int, default=1)
+    ap.add_argument("--workload", type=int, default=4,
+                    help="0..4; the default, 4, is the largest single-GPU configuration (2M voxels, 5x5x5, C 128 bf16)")
+    ap.add_argument("--scale", type=float, default=1.0,
+                    help="shrink the scene (N and grid) for small profiling captures; the workload name records it")
     ap.add_argument("--e2e-steps", type=int, default=300)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -78,9 +88,9 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
-def make_workload(idx: int, rank: int):
+def make_workload(idx: int, rank: int, scale: float = 1.0):
     from submanifold_sparse_convolution_hash_gb300 import scenes
-    return scenes.workload(idx, replica=rank)  # each replica draws its own scene of the recipe
+    return scenes.workload(idx, scale=scale, replica=rank)  # each replica draws its own scene of the recipe
 
 
 def layer_tensors(w, s):
@@ -205,139 +215,299 @@ def recorded_traffic(kernel: str, workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+    """Read-only sampling of the GPU's SM clock, power draw and clock-event
+    (throttle) reasons while the bench runs.
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
-              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-              "clocks_event_reasons.sw_power_cap")
+    In-process NVML (libnvidia-ml) every `period` seconds from a thread; the
+    device is found by its PCI bus id (else its UUID), never by index, so
+    CUDA_VISIBLE_DEVICES cannot point the sampler at another GPU.  Without
+    NVML it runs `nvidia-smi -i <bus id> -lms 100`.  Every sample carries the
+    phase set by mark() (warm-up, breakdown, timed ...).  Queries only:
+    nothing here changes a clock, a power limit or any other setting."""
 
-    def __init__(self, index: int):
-        self.index = index
-        self.proc = None
-        self.lines = []
+    # clock-event reason bits of NVML's current-reasons mask
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown"}
+    SMI_FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+                  "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                  "clocks_event_reasons.sw_power_cap")
+    SMI_NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, bus_id: str | None = None, uuid: str | None = None, period: float = 0.005):
+        self.bus_id, self.uuid, self.period = bus_id, uuid, period
+        self.samples = []  # (phase, sm_mhz, sm_max_mhz, reasons frozenset)
+        self.phase = "idle"
+        self.source = None
+        self._stop = threading.Event()
+        self._t = None
+        self._proc = None
+
+    @staticmethod
+    def for_torch_device(dev_index: int, period: float = 0.005):
+        import torch
+        p = torch.cuda.get_device_properties(dev_index)
+        bus = None
+        if hasattr(p, "pci_bus_id"):
+            bus = f"{getattr(p, 'pci_domain_id', 0):08X}:{p.pci_bus_id:02X}:{getattr(p, 'pci_device_id', 0):02X}.0"
+        uuid = str(getattr(p, "uuid", "")) or None
+        return ClockSampler(bus, uuid, period)
+
+    def mark(self, phase: str):
+        self.phase = phase
+
+    # ---- NVML
+    def _nvml_open(self):
+        import ctypes
+        nv = ctypes.CDLL("libnvidia-ml.so.1")
+        if nv.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        ok = False
+        if self.bus_id:
+            ok = nv.nvmlDeviceGetHandleByPciBusId_v2(self.bus_id.encode(), ctypes.byref(h)) == 0
+        if not ok and self.uuid:
+            for u in (self.uuid, "GPU-" + self.uuid):
+                if nv.nvmlDeviceGetHandleByUUID(u.encode(), ctypes.byref(h)) == 0:
+                    ok = True
+                    break
+        if not ok:
+            raise OSError("NVML: device not found by bus id or UUID")
+        reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        return nv, h, reasons_fn
+
+    def _nvml_loop(self, nv, h, reasons_fn):
+        import ctypes
+        clk, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if (nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0 and  # 1 = SM clock
+                    nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0 and
+                    reasons_fn(h, ctypes.byref(rs)) == 0):
+                r = frozenset(nm for bit, nm in self.REASONS.items() if rs.value & bit)
+                self.samples.append((self.phase, float(clk.value), float(mx.value), r))
+            time.sleep(self.period)
+
+    # ---- nvidia-smi fallback
+    def parse_smi_line(self, line: str, phase: str = "idle"):
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) < 8:
+            return None
+        try:
+            sm, mx = float(parts[0]), float(parts[1])
+        except ValueError:
+            return None
+        r = frozenset(nm for nm, v in zip(self.SMI_NAMES, parts[4:8]) if v.lower() == "active")
+        return (phase, sm, mx, r)
+
+    def _smi_loop(self):
+        for line in self._proc.stdout:
+            s = self.parse_smi_line(line, self.phase)
+            if s:
+                self.samples.append(s)
 
     def __enter__(self):
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.t = threading.Thread(target=self._read, daemon=True)
-            self.t.start()
-        except Exception:
-            self.proc = None
+            nv, h, fn = self._nvml_open()
+            self.source = "nvml"
+            self._t = threading.Thread(target=self._nvml_loop, args=(nv, h, fn), daemon=True)
+            self._t.start()
+            return self
+        except (OSError, AttributeError):
+            pass
+        if self.bus_id or self.uuid:
+            try:
+                self._proc = subprocess.Popen(
+                    ["nvidia-smi", "-i", self.bus_id or ("GPU-" + self.uuid), f"--query-gpu={self.SMI_FIELDS}",
+                     "--format=csv,noheader,nounits", "-lms", "100"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                self.source = "nvidia-smi"
+                self._t = threading.Thread(target=self._smi_loop, daemon=True)
+                self._t.start()
+            except OSError:
+                self._proc = None
         return self
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
-
     def __exit__(self, *exc):
-        if self.proc:
-            self.proc.terminate()
+        self._stop.set()
+        if self._proc:
+            self._proc.terminate()
             try:
-                self.proc.wait(timeout=5)
+                self._proc.wait(timeout=5)
             except Exception:
-                self.proc.kill()
+                self._proc.kill()
+        if self._t:
+            self._t.join(timeout=5)
 
-    def summary(self):
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 8:
-                continue
-            try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
-            except ValueError:
-                continue
-            for nm, v in zip(names, parts[4:8]):
-                if v.lower() == "active":
-                    reasons.add(nm)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+    def summary(self, phases=("timed",), min_samples: int = 10, load_phases=None):
+        """Median SM MHz, max SM MHz and the union of the reasons over the
+        samples of `phases`; if those are fewer than `min_samples`, over the
+        samples of every phase in `load_phases` (all GPU-busy phases), which
+        the `window` key then names."""
+        def pick(ph):
+            return [s for s in self.samples if s[0] in ph]
+        sel, window = pick(phases), list(phases)
+        if len(sel) < min_samples and load_phases:
+            sel, window = pick(load_phases), list(load_phases)
+        out = {"samples": len(sel), "samples_timed": len(pick(phases)), "window": window, "source": self.source}
+        if not sel:
+            out.update({"sm_mhz": None, "sm_max_mhz": None, "reasons": []})
+            return out
+        out.update({"sm_mhz": statistics.median(s[1] for s in sel), "sm_max_mhz": max(s[2] for s in sel),
+                    "reasons": sorted(set().union(*(s[3] for s in sel)))})
+        return out
 
 
 # ---------------------------------------------------------------------- CPU --
-def cpu_oracle_run(s, K, f, W, seconds: float, stride: int = 0):
-    """Times the oracle (map + layer) on the full scene, repeated to ~`seconds`.
-    stride > 0: the regular / strided layer (output set + map + layer)."""
-    import oracle
-    f64 = f.astype(np.float64)
-    W64 = W.astype(np.float64)
-    t0 = time.perf_counter()
-    passes = 0
-    while True:
-        if stride:
-            oc = oracle.conv_out_coords(s.coords, s.ndim, K, stride, s.dims)
-            oracle.conv_kmap(s.coords, oc, s.ndim, K, stride, s.dims)
-            oracle.sparse_conv(s.coords, oc, f64, W64, s.ndim, K, stride, s.dims)
+def oracle_layer_inputs(w, s):
+    """fp64 (feats, W) of every layer of the workload for timing the oracle:
+    the first layer's seeded inputs, and seeded features of the right width
+    for the later layers (their values do not change the oracle's time)."""
+    from submanifold_sparse_convolution_hash_gb300 import scenes
+    V = w.K ** s.ndim
+    layers = list(zip(w.channels[:-1], w.channels[1:]))
+
+    def rnd(a):
+        return a.astype(np.float64)
+
+    feats_by_width = {}
+    out = []
+    for li, (ci, co) in enumerate(layers):
+        if li == 0:
+            f = rnd(scenes.features(w.seed, s.n, ci))
+            W = rnd(scenes.weights(w.seed, V, ci, co, std=1.0 if w.w_std_unit else None))
         else:
-            oracle.kmap(s.coords, s.ndim, K, s.dims)
-            oracle.subm_conv(s.coords, f64, W64, s.ndim, K, s.dims)
-        passes += 1
-        el = time.perf_counter() - t0
-        if el >= seconds or el * (passes + 1) / passes > 3 * seconds:
-            break
-    return {"value": s.n * passes / el / 1e6, "unit": "Mvoxels/s", "cores": oracle.max_threads(), "host_cpus": os.cpu_count(), "cpu_model": cpu_model(),
-            "kind": "oracle",
-            "sample": f"full scene (N={s.n}) x {passes} pass(es): hash + map + fp64 layer, {el:.1f} s"}
+            if ci not in feats_by_width:
+                feats_by_width[ci] = rnd(scenes.features(w.seed + 50 + ci, s.n, ci))
+            f = feats_by_width[ci]
+            W = rnd(scenes.weights(w.seed + li, V, ci, co))
+        out.append((f, W))
+    return out
 
 
-def run_reference(args):
-    """The reference arm: the CPU oracle, as it stands, on this host's cores.
-
-    Each step builds the oracle's coordinate table over the whole scene and
-    computes the map and the fp64 layer for a fixed sample of output rows
-    (evenly spaced); the step's time is scaled to the whole scene as
-    t_table + (t_step - t_table) * N / rows, with t_table measured alone.
-    The sample is sized so that warm-up plus timed steps take a few minutes.
-    """
-    rank, world, _ = dist_env()
-    if rank != 0:
-        return
+def oracle_sampled_plan(w, s, seconds: float):
+    """Sizes a bounded sample of the oracle's work on the workload so that
+    one pass takes about `seconds`: returns (inputs, rows, t_table)."""
     import oracle
     oracle.build()
-    w, s = make_workload(args.workload, 0)
-    f, W = layer_tensors(w, s)
-    if w.dtype == "f16":
-        f = f.astype(np.float16).astype(np.float32)
-        W = W.astype(np.float16).astype(np.float32)
-    f64, W64 = f.astype(np.float64), W.astype(np.float64)
+    ins = oracle_layer_inputs(w, s)
     t_tab = []
     for _ in range(3):
         t0 = time.perf_counter()
         oracle.hash_only(s.coords, s.ndim, w.K, s.dims)
         t_tab.append(time.perf_counter() - t0)
     t_table = statistics.median(t_tab)
-    probe = np.linspace(0, s.n - 1, min(s.n, 4000)).astype(np.int64)
-    t0 = time.perf_counter()
-    oracle.subm_conv(s.coords, f64, W64, s.ndim, w.K, s.dims, rows=probe)
-    per_row = max((time.perf_counter() - t0 - t_table) / len(probe), 1e-9)
-    budget = 150.0 / max(1, args.steps + args.warmup)
-    k = int(max(256, min(s.n, (budget - t_table) / per_row)))
-    rows = np.linspace(0, s.n - 1, k).astype(np.int64)
-    for _ in range(args.warmup):
-        oracle.subm_conv(s.coords, f64, W64, s.ndim, w.K, s.dims, rows=rows)
-    times = []
-    for _ in range(args.steps):
+    probe = np.linspace(0, s.n - 1, min(s.n, 256)).astype(np.int64)
+    per_row = 0.0
+    for f, W in ins:
         t0 = time.perf_counter()
-        oracle.subm_conv(s.coords, f64, W64, s.ndim, w.K, s.dims, rows=rows)
+        oracle.subm_conv(s.coords, f, W, s.ndim, w.K, s.dims, rows=probe)
+        per_row += max(time.perf_counter() - t0 - t_table, 1e-7) / len(probe)
+    k = int(max(256, min(s.n, (seconds - t_table) / max(per_row, 1e-9))))
+    rows = np.linspace(0, s.n - 1, k).astype(np.int64)
+    return ins, rows, t_table
+
+
+def oracle_sampled_pass(w, s, ins, rows, t_table) -> float:
+    """One oracle pass on the sample, scaled to the whole scene (seconds):
+    the coordinate table over all N, then for each sampled output row its
+    V neighbour lookups (the row of the map) and its fp64 output, layer by
+    layer.  Each layer call rebuilds the table, so the scaled time is
+    t_table + sum over layers of (t_layer - t_table) * N / k."""
+    import oracle
+    total = t_table
+    for f, W in ins:
+        t0 = time.perf_counter()
+        oracle.subm_conv(s.coords, f, W, s.ndim, w.K, s.dims, rows=rows)
+        total += max(time.perf_counter() - t0 - t_table, 0.0) * s.n / len(rows)
+    return total
+
+
+def oracle_sample_text(w, s, k: int) -> str:
+    V = w.K ** s.ndim
+    nl = len(w.channels) - 1
+    return (f"coordinate table (hash) over all N={s.n}, then for {k} evenly spaced output rows the row's {V} "
+            f"neighbour lookups (its map row) and its fp64 output in each of the {nl} layer(s); time scaled to N "
+            f"as t_table + t_rows * N / {k}; phases: hash + map + layers, as in the GPU step")
+
+
+def cpu_oracle_sampled(w, s, seconds: float):
+    """cpu_baseline of the GPU line: the oracle on a bounded sample."""
+    import oracle
+    ins, rows, t_table = oracle_sampled_plan(w, s, seconds)
+    t0 = time.perf_counter()
+    t = oracle_sampled_pass(w, s, ins, rows, t_table)
+    el = time.perf_counter() - t0
+    return {"value": round(s.n / t / 1e6, 4), "unit": "Mvoxels/s", "cores": oracle.max_threads(),
+            "host_cpus": os.cpu_count(), "cpu_model": cpu_model(), "kind": "oracle",
+            "sample": oracle_sample_text(w, s, len(rows)) + f"; one pass, {el:.1f} s of CPU work"}
+
+
+def cpu_oracle_run(s, K, f, W, seconds: float, stride: int = 0):
+    """Times the oracle on the full scene (regular / strided layer: output
+    set + map + layer; stride > 0), repeated to ~`seconds`."""
+    import oracle
+    f64 = f.astype(np.float64)
+    W64 = W.astype(np.float64)
+    t0 = time.perf_counter()
+    passes = 0
+    while True:
+        oc = oracle.conv_out_coords(s.coords, s.ndim, K, stride, s.dims)
+        oracle.conv_kmap(s.coords, oc, s.ndim, K, stride, s.dims)
+        oracle.sparse_conv(s.coords, oc, f64, W64, s.ndim, K, stride, s.dims)
+        passes += 1
         el = time.perf_counter() - t0
-        times.append(t_table + max(el - t_table, 0.0) * s.n / k)
+        if el >= seconds or el * (passes + 1) / passes > 3 * seconds:
+            break
+    return {"value": s.n * passes / el / 1e6, "unit": "Mvoxels/s", "cores": oracle.max_threads(),
+            "host_cpus": os.cpu_count(), "cpu_model": cpu_model(), "kind": "oracle",
+            "sample": f"full scene (N={s.n}) x {passes} pass(es): output set + map + fp64 layer, {el:.1f} s"}
+
+
+def workload_config(w, s, M: int, world: int, layer_type: str = "submanifold", stride: int = 1,
+                    n_out: int | None = None, backward: bool = False, scale: float = 1.0):
+    """The line's `config`: what the workload is, identical in both arms."""
+    cfg = {"workload": w.name if scale == 1.0 else f"{w.name}_scale{scale:g}", "N": s.n, "map_size": int(M),
+           "K": w.K, "ndim": s.ndim, "dims": list(s.dims), "layers": [list(l) for l in zip(w.channels[:-1], w.channels[1:])],
+           "layer_type": layer_type, "stride": stride, "N_out": int(s.n if n_out is None else n_out),
+           "pass": "forward+backward" if backward else "forward",
+           "l2": "GPU arm: flushed before every step (256 MB write, outside the events); CPU arm: no flush",
+           "parallelism": "replicas" if world > 1 else "single"}
+    if layer_type != "submanifold":
+        cfg["layers"] = cfg["layers"][:1]
+    return cfg
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle, as it stands, on this host's cores.
+
+    Each step is one oracle pass on a bounded sample of the workload (the
+    coordinate table over the whole scene, then for a fixed set of evenly
+    spaced output rows their map rows and fp64 outputs in every layer),
+    scaled to the whole scene (oracle_sampled_pass).  The sample is sized so
+    that warm-up plus timed steps take a few minutes.  |M| for the config is
+    counted from the oracle's own map (outside the timed steps).
+    """
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    w, s = make_workload(args.workload, 0, args.scale)
+    M = int((oracle.kmap(s.coords, s.ndim, w.K, s.dims) >= 0).sum())
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    ins, rows, t_table = oracle_sampled_plan(w, s, budget)
+    for _ in range(args.warmup):
+        oracle_sampled_pass(w, s, ins, rows, t_table)
+    times = [oracle_sampled_pass(w, s, ins, rows, t_table) for _ in range(args.steps)]
     ms = 1e3 * statistics.mean(times)
     value = s.n / (ms / 1e3) / 1e6
-    sample = (f"coordinate table over all N={s.n} + map and fp64 layer for {k} evenly spaced output rows per "
-              f"step, scaled to N")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "Mvoxels/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "N": s.n, "K": w.K, "c_in": w.channels[0], "c_out": w.channels[1]},
-        "cpu_baseline": {"value": round(value, 4), "unit": "Mvoxels/s", "cores": oracle.max_threads(), "host_cpus": os.cpu_count(), "cpu_model": cpu_model(),
-                         "kind": "oracle", "sample": sample},
+        "config": workload_config(w, s, M, world, scale=args.scale),
+        "cpu_baseline": {"value": round(value, 4), "unit": "Mvoxels/s", "cores": oracle.max_threads(),
+                         "host_cpus": os.cpu_count(), "cpu_model": cpu_model(), "kind": "oracle",
+                         "sample": oracle_sample_text(w, s, len(rows))},
         "e2e": {"value": round(value, 4), "unit": "Mvoxels/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -372,7 +542,7 @@ def run_ours(args):
     __graft_entry__.build()
     from submanifold_sparse_convolution_hash_gb300 import binding as sc
 
-    w, s = make_workload(args.workload, rank)
+    w, s = make_workload(args.workload, rank, args.scale)
     from submanifold_sparse_convolution_hash_gb300 import scenes as sc_scenes
     tdt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[w.dtype]
     esize = 4 if w.dtype == "f32" else 2
@@ -441,6 +611,11 @@ def run_ours(args):
                 g = gins[li]
         return h, m
 
+    # clocks are sampled from the first warm-up step to the end of the timed
+    # steps, each sample tagged with its phase
+    clk = ClockSampler.for_torch_device(dev.index if dev.index is not None else torch.cuda.current_device())
+    clk.__enter__()
+    clk.mark("warmup")
     for _ in range(max(args.warmup, 3)):
         flush.zero_()
         step()
@@ -453,6 +628,7 @@ def run_ours(args):
     sc.profile_only(None)
     sc.profile_enable(True)
     bd_steps = min(args.steps, 100)
+    clk.mark("breakdown")
     for _ in range(bd_steps):
         flush.zero_()
         keep.append(step())
@@ -467,6 +643,7 @@ def run_ours(args):
     # map build end to end (sc_hash_build .. sc_kmap_build, events on the
     # stream, no per-kernel brackets), untimed pass
     map_e2e = []
+    clk.mark("map_build")
     for _ in range(bd_steps):
         flush.zero_()
         e0 = torch.cuda.Event(enable_timing=True)
@@ -492,15 +669,17 @@ def run_ours(args):
     sc.profile_only(dom)
     sc.profile_enable(True)
     launches0 = sc.launch_count()
-    with ClockSampler(torch.cuda.current_device()) as clk:
-        for i in range(args.steps):
-            flush.zero_()
-            starts[i].record(stream)
-            keep.append(step())
-            ends[i].record(stream)
-            if len(keep) > 4:
-                keep.pop(0)
-        torch.cuda.synchronize()
+    clk.mark("timed")
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        keep.append(step())
+        ends[i].record(stream)
+        if len(keep) > 4:
+            keep.pop(0)
+    torch.cuda.synchronize()
+    clk.mark("after")
+    clk.__exit__(None, None, None)
     launches = sc.launch_count() - launches0
     sc.profile_enable(False)
     sc.profile_only(None)
@@ -559,11 +738,8 @@ def run_ours(args):
         "metric": METRIC, "value": round(value, 4), "unit": "Mvoxels/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": {"workload": w.name, "N": s.n, "map_size": M, "K": w.K, "layers": layers,
-                   "layer_type": args.layer_type, "stride": conv_stride, "N_out": n_out,
-                   "pass": "forward+backward" if args.backward else "forward",
-                   "variant": variants, "variant_choice": "given" if args.variant else "measured", "l2": "flushed before every step (256 MB write, outside the events)",
-                   "kmap_sync": False, "parallelism": "replicas" if world > 1 else "single"},
+        "config": workload_config(w, s, M, world, args.layer_type, conv_stride, n_out, args.backward, args.scale),
+        "run": {"variant": variants, "variant_choice": "given" if args.variant else "measured", "kmap_sync": False},
         "layer_tflops": round(flops / (conv_ms / 1e3) / 1e12, 3) if conv_ms else None,
         "layer_ms": round(conv_ms, 5),
         "layer_roofline_frac": round(conv_roof_s / (conv_ms / 1e3), 4) if conv_ms else None,
@@ -578,14 +754,17 @@ def run_ours(args):
         "per_kernel": per_kernel,
         "per_kernel_source": f"untimed pass of {bd_steps} steps, every launch bracketed by CUDA events",
         "gpu_launches": launches,
-        "clocks": clk.summary(),
+        "clocks": clk.summary(("timed",), 10, ("warmup", "breakdown", "map_build", "timed")),
     }
 
     if not args.no_e2e and rank == 0:
         line["e2e"] = run_e2e(args, w, s, f_np, Ws, tdt, dev, variants, world, build_map, n_out)
     if not args.no_cpu_baseline and rank == 0:
-        line["cpu_baseline"] = cpu_oracle_run(s, w.K, feats.float().cpu().numpy(), W0, args.cpu_seconds,
-                                              conv_stride if general else 0)
+        if general:
+            line["cpu_baseline"] = cpu_oracle_run(s, w.K, feats.float().cpu().numpy(), W0, args.cpu_seconds,
+                                                  conv_stride)
+        else:
+            line["cpu_baseline"] = cpu_oracle_sampled(w, s, args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

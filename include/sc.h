@@ -338,7 +338,10 @@ sc_status sc_subm_conv_bwd_weight(sc_kmap m, const void* d_feats, const void* d_
  *
  * The first call on each device looks up the array's device address with
  * cudaGetSymbolAddress while that device is current; make that first call
- * before any stream capture.  Every call reuses the one array and overwrites
+ * before any stream capture.  The address is cached per device and per CUDA
+ * context: a call made after the device's context was replaced (for example
+ * after cudaDeviceReset) looks it up again, so it too should come before any
+ * capture.  Every call reuses the one array and overwrites
  * all of the packed weights it uses, so nothing carries over between calls
  * except stale bytes that are never read.  Calls whose GPU work overlaps (on
  * different streams, or from different threads) race on the array: order

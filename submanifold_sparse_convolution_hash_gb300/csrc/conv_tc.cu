@@ -851,22 +851,57 @@ sc_status conv_weight_stationary(const ConvArgs& a) {
   return st;
 }
 
-// Device address of g_noalloc_weights on the current device, looked up once
-// per device (host code only holds a stand-in for the symbol, which is not a
-// device address).
+// Id of the calling thread's current CUDA context (0 if the driver cannot
+// say), through the driver entry point, so the library needs no link-time
+// dependency on the driver library.  A context made after cudaDeviceReset
+// gets a new id even where it reuses an old handle.
+static unsigned long long current_context_id() {
+  typedef int (*get_current_fn)(void**);
+  typedef int (*get_id_fn)(void*, unsigned long long*);
+  static get_current_fn get_current = nullptr;
+  static get_id_fn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<get_current_fn>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<get_id_fn>(f);
+    cudaGetLastError();
+  });
+  void* ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current && get_id && get_current(&ctx) == 0 && ctx && get_id(ctx, &id) == 0) return id;
+  return 0;
+}
+
+// Device address of g_noalloc_weights in the current device's context,
+// looked up once per device and context (host code only holds a stand-in
+// for the symbol, which is not a device address).  The cache is keyed on the
+// context id as well, so a context that replaced the old one (after
+// cudaDeviceReset) gets the array's address in the new context.
 static sc_status noalloc_weights_ptr(void** out) {
   static std::mutex mu;
   static void* addr[64] = {nullptr};
+  static unsigned long long ctx_of[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return set_cuda_error(e, "cudaGetDevice");
   if (dev < 0 || dev >= 64) return set_error(SC_ERR_UNSUPPORTED, "device index above 63");
+  // 0 when no context is current on this thread yet: the lookup below
+  // makes the device's primary context current, and its id is read again
+  unsigned long long ctx = current_context_id();
   std::lock_guard<std::mutex> lk(mu);
-  if (!addr[dev]) {
+  if (!addr[dev] || ctx == 0 || ctx_of[dev] != ctx) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_weights);
     if (e != cudaSuccess || !p) return set_cuda_error(e, "cudaGetSymbolAddress(g_noalloc_weights)");
     addr[dev] = p;
+    ctx_of[dev] = ctx ? ctx : current_context_id();
   }
   *out = addr[dev];
   return SC_OK;

@@ -59,13 +59,39 @@ def test_committed_traffic_records_name_existing_sources():
 
 
 def test_clock_summary_reads_reasons():
-    c = bench.ClockSampler(0)
-    c.lines = ["2070, 2070, 900.5, 0x0, Not Active, Not Active, Not Active, Not Active",
-               "1980, 2070, 1390.0, 0x4, Not Active, Not Active, Not Active, Active",
-               "garbage"]
-    s = c.summary()
+    c = bench.ClockSampler("00000000:01:00.0")
+    for ln, ph in [("2070, 2070, 900.5, 0x0, Not Active, Not Active, Not Active, Not Active", "timed"),
+                   ("1980, 2070, 1390.0, 0x4, Not Active, Not Active, Not Active, Active", "timed"),
+                   ("garbage", "timed")]:
+        s = c.parse_smi_line(ln, ph)
+        if s:
+            c.samples.append(s)
+    s = c.summary(("timed",), min_samples=1)
     assert s["samples"] == 2 and s["sm_max_mhz"] == 2070.0 and s["reasons"] == ["sw_power_cap"]
     assert s["sm_mhz"] == (2070.0 + 1980.0) / 2
+
+
+def test_clock_summary_widens_to_the_load_phases_when_the_timed_steps_are_short():
+    c = bench.ClockSampler("00000000:01:00.0")
+    c.samples += [("warmup", 2000.0, 2070.0, frozenset())] * 30
+    c.samples += [("timed", 2070.0, 2070.0, frozenset({"sw_power_cap"}))] * 3
+    c.samples += [("idle", 500.0, 2070.0, frozenset({"hw_slowdown"}))] * 50
+    s = c.summary(("timed",), 10, ("warmup", "timed"))
+    # too few timed samples: the summary covers warm-up + timed, never idle
+    assert s["samples"] == 33 and s["samples_timed"] == 3 and s["window"] == ["warmup", "timed"]
+    assert s["sm_mhz"] == 2000.0 and s["reasons"] == ["sw_power_cap"]
+    s = c.summary(("timed",), 3, ("warmup", "timed"))
+    assert s["samples"] == 3 and s["window"] == ["timed"] and s["sm_mhz"] == 2070.0
+
+
+def test_default_workload_is_the_largest_single_gpu_configuration(monkeypatch):
+    import sys
+    monkeypatch.setattr(sys, "argv", ["bench.py"])
+    a = bench.parse_args()
+    assert a.workload == 4 and a.gpus == 1 and a.scale == 1.0
+    from submanifold_sparse_convolution_hash_gb300 import scenes
+    w, _ = scenes.workload(4, scale=0.001)
+    assert w.K == 5 and w.channels == (128, 128) and w.dtype == "bf16"
 
 
 def test_map_build_time_counts_every_map_kernel():
@@ -115,8 +141,8 @@ def test_reference_arm_prints_one_json_line():
     the contract's JSON line (no GPU involved)."""
     import subprocess
     import sys
-    r = subprocess.run([sys.executable, os.path.join(bench.ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
-                        "--warmup", "1"], capture_output=True, text=True, timeout=600, cwd=bench.ROOT)
+    r = subprocess.run([sys.executable, os.path.join(bench.ROOT, "bench.py"), "--impl", "reference", "--workload", "1",
+                        "--steps", "1", "--warmup", "1"], capture_output=True, text=True, timeout=600, cwd=bench.ROOT)
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
     assert len(lines) == 1
@@ -126,4 +152,12 @@ def test_reference_arm_prints_one_json_line():
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": "Mvoxels/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
-    assert d["config"]["workload"].startswith("lidar_")
+    cfg = d["config"]
+    assert cfg["workload"].startswith("lidar_") and cfg["layers"] == [[32, 32]] and cfg["K"] == 3
+    # |M| counted from the oracle's map; the same keys the GPU arm's config carries
+    from submanifold_sparse_convolution_hash_gb300 import scenes
+    import oracle
+    w, s = scenes.workload(1)
+    assert cfg["N"] == s.n and cfg["map_size"] == int((oracle.kmap(s.coords, 3, 3, s.dims) >= 0).sum())
+    assert cfg == bench.workload_config(w, s, cfg["map_size"], 1)
+    assert "hash + map + layers" in cb["sample"]
