@@ -69,7 +69,7 @@ typedef enum { SC_F32 = 0, SC_F16 = 1, SC_BF16 = 2 } sc_dtype;
 #define SC_KMAP_NO_SYNC 0x100u  /* do not synchronise; check errors later with sc_kmap_check */
 #define SC_KMAP_ORDER 0x200u    /* always compute the locality order (default: n >= 262144) */
 #define SC_KMAP_NO_ORDER 0x400u /* never compute it: tiles follow the input row order */
-#define SC_KMAP_SORT 0x800u     /* always sort the convolution's rows by signature (default: n >= 262144, V <= 32) */
+#define SC_KMAP_SORT 0x800u     /* always sort the convolution's rows by signature (default: n >= 262144, V <= 128) */
 #define SC_KMAP_NO_SORT 0x1000u /* never sort them */
 #define SC_KMAP_TRANSPOSE 0x2000u /* sc_kmap_build_conv: the transposed map (rows = the layer's inputs) */
 
@@ -175,13 +175,16 @@ sc_status sc_hash_coords(sc_hash h, int32_t* d_coords, sc_stream stream);
  * neighbour rows.  It changes no result: outputs still land on their own
  * rows and nbr stays in input row order.
  *
- * Signature sort (V <= 32; for n >= 262144 or with SC_KMAP_SORT): inside
+ * Signature sort (V <= 128; for n >= 262144 or with SC_KMAP_SORT): inside
  * windows of 65536 consecutive rows of that order, the convolution's rows
  * are counting-sorted by a 16-bit signature, which of the 16 least frequent
- * offsets (over the whole map) the row has a neighbour under.  Rows that
- * touch the same rare offsets then share 128-row tiles, and a tile walks
- * fewer offsets (the bitmask reordering of "TorchSparse optimizations",
- * section "TorchSparse++").  It too changes no result.
+ * features (over the whole map) the row has a neighbour under.  The
+ * features are the offsets when V <= 32, else the 26 coarse directions
+ * (sign(dx), sign(dy), sign(dz)), a feature's frequency being the tuple
+ * count of its offsets.  Rows that touch the same rare features then share
+ * 128-row tiles, and a tile walks fewer offsets (the bitmask reordering of
+ * "TorchSparse optimizations", section "TorchSparse++").  It too changes no
+ * result.
  *
  * Products, owned by the handle:
  *   nbr      int32 [n, V]: nbr[q*V + idx(d)] = row p with coords[p] =

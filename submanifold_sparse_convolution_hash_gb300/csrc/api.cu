@@ -566,7 +566,7 @@ sc_status sc_kmap_destroy(sc_kmap m, sc_stream stream) {
 
 // Inputs at least this large get a locality order by default.
 constexpr int64_t kOrderMinPoints = 262144;
-// ... and a signature sort of the convolution's rows (V <= 32).
+// ... and a signature sort of the convolution's rows (V <= 128).
 constexpr int64_t kSortMinPoints = 262144;
 
 namespace {
@@ -617,9 +617,10 @@ sc_status kmap_build_impl(sc_hash hi, sc_hash ho, int ndim, int K, int stride, c
   k.up = kmap_unit_points(V);
   k.nunits = static_cast<int>((k.n + k.up - 1) / k.up);
   const bool ordered = (flags & SC_KMAP_ORDER) || (!(flags & SC_KMAP_NO_ORDER) && k.n >= kOrderMinPoints);
-  // the signature sort needs one mask word per row (V <= 32)
-  const bool sorted = identity && V <= 32 && k.n > 0 &&
+  // the signature sort keeps a mask of up to 128 offsets per row (V <= 128)
+  const bool sorted = identity && V <= 128 && k.n > 0 &&
                       ((flags & SC_KMAP_SORT) || (!(flags & SC_KMAP_NO_SORT) && k.n >= kSortMinPoints));
+  const size_t mask_words = V <= 32 ? 1 : 4;
   const size_t nsig = sorted ? static_cast<size_t>(kmap_sig_buckets(k.n)) : 0;
   // every buffer of the map carved from one allocation, each 256-byte aligned
   const size_t n = static_cast<size_t>(k.n);
@@ -639,7 +640,8 @@ sc_status kmap_build_impl(sc_hash hi, sc_hash ho, int ndim, int K, int stride, c
       {reinterpret_cast<void**>(&k.order), ordered && k.n > 0 ? sizeof(int) * n : 0},
       {reinterpret_cast<void**>(&k.skeys), ordered && k.n > 0 ? sizeof(unsigned long long) * n : 0},
       {reinterpret_cast<void**>(&k.buckets), ordered && k.n > 0 ? sizeof(int) * kmap_order_buckets() : 0},
-      {reinterpret_cast<void**>(&k.rowmask), sorted ? sizeof(unsigned) * n : 0},
+      {reinterpret_cast<void**>(&k.rowmask), sorted ? sizeof(unsigned) * n * mask_words : 0},
+      {reinterpret_cast<void**>(&k.rowdir), sorted && V > 32 ? sizeof(unsigned) * n : 0},
       {reinterpret_cast<void**>(&k.sig_sel), sorted ? sizeof(int) * kmap_sig_bits() : 0},
       {reinterpret_cast<void**>(&k.sigbuckets), sorted ? sizeof(int) * (nsig + nsig / 4096 + 1) : 0},
       {reinterpret_cast<void**>(&k.perm), sorted ? sizeof(int) * n : 0},

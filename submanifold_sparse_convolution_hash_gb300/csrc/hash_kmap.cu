@@ -332,9 +332,33 @@ struct BuildArgs {
   int64_t* offs;                   // [V+1]
   int* ws_tiles;                   // [V+1]
   int64_t* map_size;
-  unsigned* rowmask;               // [n] offsets (< 32, centre excluded) with a neighbour, per row; or null
-  int* sig_sel;                    // [kSigBits] offsets of the row signature, rarest first (with rowmask)
+  // signature sort: the offsets (centre excluded) with a neighbour, per row:
+  // one word per row when V <= 32, four (a 128-bit mask) when V <= 128; or null
+  unsigned* rowmask;
+  // V > 32: the coarse directions (sign(dx), sign(dy), sign(dz)), 27 bits,
+  // with a neighbour, per row: the signature's features; else null (the
+  // features are the offsets themselves, in rowmask)
+  unsigned* rowdir;
+  int* sig_sel;                    // [kSigBits] features of the row signature, rarest first (with rowmask)
 };
+
+// Coarse direction of offset v: (sign(dx) + 1) * 9 + (sign(dy) + 1) * 3 +
+// (sign(dz) + 1), in [0, 27), the centre 13 (dz = 0 in 2D).
+__device__ __forceinline__ int offset_direction(int v, int K, int ndim) {
+  const int r = (K - 1) / 2;
+  int dx, dy, dz;
+  if (ndim == 3) {
+    dx = v / (K * K) - r;
+    dy = (v / K) % K - r;
+    dz = v % K - r;
+  } else {
+    dx = v / K - r;
+    dy = v % K - r;
+    dz = 0;
+  }
+  const int sx = (dx > 0) - (dx < 0) + 1, sy = (dy > 0) - (dy < 0) + 1, sz = (dz > 0) - (dz < 0) + 1;
+  return sx * 9 + sy * 3 + sz;
+}
 
 // Dynamic shared memory: s_tile [up * V] ints, s_bal [V * up / 32].
 // Five blocks per SM (register budget): 2560 lookups in flight per SM.
@@ -353,20 +377,38 @@ __global__ void __launch_bounds__(kThreads, 5) k_kmap_build(const BuildArgs a) {
   __shared__ int s_last;
   __shared__ int s_row[128];
   __shared__ unsigned s_pres[4];
-  __shared__ unsigned s_rmask[128];
+  __shared__ unsigned s_rmask[128];         // V <= 32: offsets per row; V > 32: directions per row
+  __shared__ __align__(16) unsigned s_rmask4[128 * 4];  // V > 32: 128-bit offset mask per row
+  __shared__ unsigned char s_dir[128];  // V <= 128 with rowdir: coarse direction of each offset
+  // covering blocks of a neighbourhood, relative to its lowest one: block t
+  // at (t & 0xFF, (t >> 8) & 0xFF, t >> 16); at most (r + 1)^3 <= 81
+  __shared__ uint32_t s_trip[128];
+  __shared__ int s_ntrip;
   __shared__ long long warp_sums[32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int kWarps = kThreads / 32;
   if (threadIdx.x < 4) s_pres[threadIdx.x] = 0u;
   if (threadIdx.x < 128) s_rmask[threadIdx.x] = 0u;
+  if (a.rowdir)
+    for (int e = threadIdx.x; e < 128 * 4; e += kThreads) s_rmask4[e] = 0u;
+  if (a.rowdir && threadIdx.x < V) s_dir[threadIdx.x] = static_cast<unsigned char>(offset_direction(threadIdx.x, a.K, a.ndim));
   for (int e = threadIdx.x; e < up * V; e += kThreads) s_tile[e] = -1;
-  __syncthreads();
   const int u = blockIdx.x;
   const int64_t i0 = static_cast<int64_t>(u) * up;
   const int np = static_cast<int>(min(static_cast<int64_t>(up), a.n - i0));
   const int r = (a.K - 1) / 2;
   const int rz = a.ndim == 3 ? r : 0;
   const int centre = (V - 1) / 2;
+  {
+    const int nb = r + 1, nbz = rz + 1;  // covering blocks per axis, at most
+    if (threadIdx.x == 0) s_ntrip = nb * nb * nbz;
+    if (threadIdx.x < nb * nb * nbz) {
+      const int t = threadIdx.x;
+      s_trip[t] = static_cast<uint32_t>(t / (nb * nbz)) | (static_cast<uint32_t>((t / nbz) % nb) << 8) |
+                  (static_cast<uint32_t>(t % nbz) << 16);
+    }
+  }
+  __syncthreads();
 
   // ---- probe: thread = (point p, part); parts split the covering blocks
   {
@@ -409,51 +451,54 @@ __global__ void __launch_bounds__(kThreads, 5) k_kmap_build(const BuildArgs a) {
     }
     const unsigned long long batch = ck & 0xFFFF000000000000ull;
     const int xlo = xl >> 1, xhi = xh >> 1, ylo = yl >> 1, yhi = yh >> 1, zlo = zl >> 1, zhi = zh >> 1;
-    const int nb = r + 1, nbz = rz + 1;  // covering blocks per axis, at most
-    const int ntrip = nb * nb * nbz;
-    {
-      // kLookups lookups in flight per thread: home entries first, then the
-      // (rare) further probes of each
-      for (int t0 = part; t0 < ntrip; t0 += kLookups * nparts) {
-        unsigned long long bk[kLookups], kk[kLookups];
-        uint32_t hh[kLookups];
-        int4 r0[kLookups], r1[kLookups];
-        bool act[kLookups];
+    // voxel e in {0, 1} of block coordinate b has the offset d = A (2b + e) - c
+    // on each axis (A = 1 forward, the stride when transposed); its index
+    // contribution is (d + r) * mul, mul = (K^2, K, 1) in 3D, (K, 1, 0) in 2D
+    const int ax = TR ? a.stride : 1, az = TR ? sz : 1;
+    const int mx = a.ndim == 3 ? a.K * a.K : a.K, my = a.ndim == 3 ? a.K : 1, mz = a.ndim == 3 ? 1 : 0;
+    const int ntrip = s_ntrip;
+    // kLookups lookups in flight per thread: home entries first, then the
+    // (rare) further probes of each
+    for (int t0 = part; t0 < ntrip; t0 += kLookups * nparts) {
+      unsigned long long bk[kLookups], kk[kLookups];
+      int4 r0[kLookups], r1[kLookups];
+      int bxs[kLookups], bys[kLookups], bzs[kLookups];
+      bool act[kLookups];
 #pragma unroll
-        for (int q = 0; q < kLookups; ++q) {
-          const int t = t0 + q * nparts;
-          const int bx = xlo + t / (nb * nbz), by = ylo + (t / nbz) % nb, bz = zlo + t % nbz;
-          act[q] = valid && t < ntrip && bx <= xhi && by <= yhi && bz <= zhi;
-          bk[q] = batch | pack_key(0, 2 * bx, 2 * by, 2 * bz);
-          hh[q] = block_home(bk[q], a.mask);
-          if (act[q]) {
-            const BlockEntry* e = a.table + hh[q];
-            kk[q] = __ldg(&e->key);
-            r0[q] = __ldg(reinterpret_cast<const int4*>(e->rows));
-            r1[q] = __ldg(reinterpret_cast<const int4*>(e->rows + 4));
-          }
+      for (int q = 0; q < kLookups; ++q) {
+        const int t = t0 + q * nparts;
+        const uint32_t tr = t < ntrip ? s_trip[t] : 0u;
+        bxs[q] = xlo + static_cast<int>(tr & 0xFF);
+        bys[q] = ylo + static_cast<int>((tr >> 8) & 0xFF);
+        bzs[q] = zlo + static_cast<int>(tr >> 16);
+        act[q] = valid && t < ntrip && bxs[q] <= xhi && bys[q] <= yhi && bzs[q] <= zhi;
+        bk[q] = batch | pack_key(0, 2 * bxs[q], 2 * bys[q], 2 * bzs[q]);
+        if (act[q]) {
+          const BlockEntry* e = a.table + block_home(bk[q], a.mask);
+          kk[q] = __ldg(&e->key);
+          r0[q] = __ldg(reinterpret_cast<const int4*>(e->rows));
+          r1[q] = __ldg(reinterpret_cast<const int4*>(e->rows + 4));
         }
+      }
 #pragma unroll
-        for (int q = 0; q < kLookups; ++q) {
-          if (!act[q]) continue;
-          bool hit = kk[q] == bk[q];
-          if (!hit && kk[q] != kEmptyKey) hit = lookup_block(a.table, a.mask, bk[q], r0[q], r1[q]);
-          if (!hit) continue;
-          const int t = t0 + q * nparts;
-          const int bx = xlo + t / (nb * nbz), by = ylo + (t / nbz) % nb, bz = zlo + t % nbz;
+      for (int q = 0; q < kLookups; ++q) {
+        if (!act[q]) continue;
+        bool hit = kk[q] == bk[q];
+        if (!hit && kk[q] != kEmptyKey) hit = lookup_block(a.table, a.mask, bk[q], r0[q], r1[q]);
+        if (!hit) continue;
+        // per axis: which of the block's two voxels fall in the neighbourhood
+        // (|d| <= r; the table holds no point outside its grid, so no other
+        // bound is needed), and the index of voxel (0, 0, 0)
+        const int dx0 = ax * 2 * bxs[q] - cx, dy0 = ax * 2 * bys[q] - cy, dz0 = az * 2 * bzs[q] - cz;
+        const unsigned ex = (dx0 >= -r && dx0 <= r ? 1u : 0u) | (dx0 + ax >= -r && dx0 + ax <= r ? 2u : 0u);
+        const unsigned ey = (dy0 >= -r && dy0 <= r ? 1u : 0u) | (dy0 + ax >= -r && dy0 + ax <= r ? 2u : 0u);
+        const unsigned ez = (dz0 >= -rz && dz0 <= rz ? 1u : 0u) | (dz0 + az >= -rz && dz0 + az <= rz ? 2u : 0u);
+        const int base = p * V + (dx0 + r) * mx + (dy0 + r) * my + (dz0 + rz) * mz;
+        const int sx = ax * mx, sy = ax * my, sz2 = az * mz;
 #pragma unroll
-          for (int l = 0; l < 8; ++l) {
-            // offset of voxel t: t - c (forward), stride * t - c (transposed);
-            // a voxel outside the neighbourhood has |d| > r on some axis (the
-            // table holds no point outside its grid, so no bound is needed)
-            const int tx = 2 * bx + (l >> 2), ty = 2 * by + ((l >> 1) & 1), tz = 2 * bz + (l & 1);
-            const int dx = (TR ? tx * a.stride : tx) - cx, dy = (TR ? ty * a.stride : ty) - cy,
-                      dz = (TR ? tz * sz : tz) - cz;
-            if (dx >= -r && dx <= r && dy >= -r && dy <= r && dz >= -rz && dz <= rz) {
-              const int v = a.ndim == 3 ? ((dx + r) * a.K + (dy + r)) * a.K + (dz + r) : (dx + r) * a.K + (dy + r);
-              s_tile[p * V + v] = pick(r0[q], r1[q], l);
-            }
-          }
+        for (int l = 0; l < 8; ++l) {
+          const int lx = l >> 2, ly = (l >> 1) & 1, lz = l & 1;
+          if ((ex >> lx) & (ey >> ly) & (ez >> lz) & 1u) s_tile[base + lx * sx + ly * sy + lz * sz2] = pick(r0[q], r1[q], l);
         }
       }
     }
@@ -509,19 +554,27 @@ __global__ void __launch_bounds__(kThreads, 5) k_kmap_build(const BuildArgs a) {
             a.in_rows[at] = s_tile[(g * 32 + lane) * V + v];
             a.out_rows[at] = s_row[g * 32 + lane];
             if (v < 32) rm[g] |= 1u << v;
+            if (a.rowdir) {  // V > 32: the row's offset and direction bits
+              atomicOr(s_rmask4 + (g * 32 + lane) * 4 + (v >> 5), 1u << (v & 31));
+              atomicOr(s_rmask + g * 32 + lane, 1u << s_dir[v]);
+            }
           }
           at0 += __popc(b);
         }
       }
     }
-    if (a.rowmask) {  // V <= 32: one word per row
+    if (a.rowmask && !a.rowdir) {  // V <= 32: one word per row
       for (int g = 0; g < ngroups; ++g)
         if (rm[g]) atomicOr(s_rmask + g * 32 + lane, rm[g]);
     }
   }
   __syncthreads();
   if (up == 128 && threadIdx.x < 4) a.present[static_cast<int64_t>(u) * 4 + threadIdx.x] = s_pres[threadIdx.x];
-  if (a.rowmask && threadIdx.x < np) a.rowmask[i0 + threadIdx.x] = s_rmask[threadIdx.x];
+  if (a.rowmask && !a.rowdir && threadIdx.x < np) a.rowmask[i0 + threadIdx.x] = s_rmask[threadIdx.x];
+  if (a.rowdir && threadIdx.x < np) {  // V > 32: 128-bit offset mask and direction bits per row
+    reinterpret_cast<uint4*>(a.rowmask)[i0 + threadIdx.x] = reinterpret_cast<const uint4*>(s_rmask4)[threadIdx.x];
+    a.rowdir[i0 + threadIdx.x] = s_rmask[threadIdx.x];
+  }
 
   // ---- the last block: segment offsets, weight-stationary tile prefix, |M|
   __threadfence();
@@ -551,12 +604,28 @@ __global__ void __launch_bounds__(kThreads, 5) k_kmap_build(const BuildArgs a) {
     a.ws_tiles[V] = static_cast<int>(carry_t);
     *a.map_size = (a.identity ? a.n : 0) + carry;
   }
+  if (a.rowmask && a.rowdir) {
+    // V > 32: a direction's count is the sum of its offsets' tuple counts
+    __syncthreads();
+    long long* s_dc = warp_sums;  // 27 counters (the scans above are done with it)
+    if (threadIdx.x < 27) s_dc[threadIdx.x] = 0;
+    __syncthreads();
+    for (int v = threadIdx.x; v < V; v += kThreads)
+      if (v != centre)
+        atomicAdd(reinterpret_cast<unsigned long long*>(s_dc + offset_direction(v, a.K, a.ndim)),
+                  static_cast<unsigned long long>(__ldcg(a.cursors + v * kCursorStride)));
+    __syncthreads();
+  }
   if (a.rowmask && warp == 0) {
-    // the kSigBits least frequent offsets that occur at all, rarest first:
-    // lane v holds (count, v); kSigBits rounds of a warp minimum (V <= 32)
+    // the kSigBits least frequent features (offsets when V <= 32, coarse
+    // directions when V > 32) that occur at all, rarest first: lane f holds
+    // (count, f); kSigBits rounds of a warp minimum
     const long long none = 0x7FFFFFFFFFFFFFFFll;
-    const int c = lane < V && lane != centre ? __ldcg(a.cursors + lane * kCursorStride) : 0;
-    long long key = c > 0 ? (static_cast<long long>(c) << 8) | lane : none;
+    const int nf = a.rowdir ? 27 : V, cf = a.rowdir ? 13 : centre;
+    const long long c = lane < nf && lane != cf ? (a.rowdir ? warp_sums[lane]
+                                                           : static_cast<long long>(__ldcg(a.cursors + lane * kCursorStride)))
+                                                : 0;
+    long long key = c > 0 ? (c << 8) | lane : none;
     for (int k = 0; k < kSigBits; ++k) {
       long long mn = key;
 #pragma unroll
@@ -621,21 +690,39 @@ __global__ void __launch_bounds__(256) k_sig_scatter(const unsigned* __restrict_
 }
 
 // Present offsets of each 128-row tile of the sorted order, one warp per
-// tile (V <= 32: every offset, the centre included, is in the first word).
+// tile, the centre added: the OR of the rows' offset masks (MW = 1 word per
+// row when V <= 32, 4 words when V <= 128).
+template <int MW>
 __global__ void __launch_bounds__(256) k_sig_present(const int* __restrict__ perm, const unsigned* __restrict__ rowmask,
                                                      int64_t n, int centre, unsigned* __restrict__ present) {
   const int64_t ntiles = (n + 127) / 128;
   const int lane = threadIdx.x & 31;
   const int64_t wstride = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
   for (int64_t t = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; t < ntiles; t += wstride) {
-    unsigned acc = 0;
+    unsigned acc[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const int64_t j = t * 128 + k * 32 + lane;
-      if (j < n) acc |= __ldg(rowmask + __ldg(perm + j));
+      if (j < n) {
+        const int64_t row = __ldg(perm + j);
+        if (MW == 1) {
+          acc[0] |= __ldg(rowmask + row);
+        } else {
+          const uint4 m = __ldg(reinterpret_cast<const uint4*>(rowmask) + row);
+          acc[0] |= m.x;
+          acc[1] |= m.y;
+          acc[2] |= m.z;
+          acc[3] |= m.w;
+        }
+      }
     }
-    acc = __reduce_or_sync(0xffffffffu, acc);
-    if (lane < 4) present[t * 4 + lane] = lane == 0 ? (acc | (1u << centre)) : 0u;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) acc[w] = __reduce_or_sync(0xffffffffu, acc[w]);
+    if (lane < 4) {
+      unsigned x = lane == 0 ? acc[0] : (lane == 1 ? acc[1] : (lane == 2 ? acc[2] : acc[3]));
+      if (lane == (centre >> 5)) x |= 1u << (centre & 31);
+      present[t * 4 + lane] = x;
+    }
   }
 }
 
@@ -940,6 +1027,7 @@ sc_status launch_kmap_build(const HashTable* in, const HashTable* h, KernelMap* 
   a.ws_tiles = m->ws_tiles;
   a.map_size = m->map_size;
   a.rowmask = m->rowmask;
+  a.rowdir = m->rowdir;
   a.sig_sel = m->sig_sel;
   const size_t smem = sizeof(int) * (static_cast<size_t>(m->up) * V + static_cast<size_t>(V) * (m->up / 32));
   if (smem > 48 * 1024) {  // set once per device: the largest the build ever asks for
@@ -970,15 +1058,19 @@ sc_status launch_kmap_build(const HashTable* in, const HashTable* h, KernelMap* 
   e = cudaMemsetAsync(m->sigbuckets, 0, sizeof(int) * nsig, s);
   if (e != cudaSuccess) return set_cuda_error(e, "signature bucket clear");
   const int g = grid_for(m->n, 256);
-  SC_LAUNCH("sig_count", s, k_sig_count<<<g, 256, 0, s>>>(m->rowmask, m->n, m->sig_sel, m->sigbuckets));
+  // the signature's features: the offsets (V <= 32) or the coarse directions
+  const unsigned* feat = m->rowdir ? m->rowdir : m->rowmask;
+  SC_LAUNCH("sig_count", s, k_sig_count<<<g, 256, 0, s>>>(feat, m->n, m->sig_sel, m->sigbuckets));
   SC_LAUNCH("sig_partials", s, k_order_partials<<<chunks, 256, 0, s>>>(m->sigbuckets, partial));
   SC_LAUNCH("sig_scan", s, k_order_apply<<<chunks, 256, 0, s>>>(m->sigbuckets, partial));
   SC_LAUNCH("sig_scatter", s,
-            k_sig_scatter<<<g, 256, 0, s>>>(m->rowmask, m->order, m->n, m->sig_sel, m->sigbuckets, m->perm,
+            k_sig_scatter<<<g, 256, 0, s>>>(feat, m->order, m->n, m->sig_sel, m->sigbuckets, m->perm,
                                             m->conv_order));
-  SC_LAUNCH("sig_present", s,
-            k_sig_present<<<grid_for(((m->n + 127) / 128) * 32, 256), 256, 0, s>>>(m->perm, m->rowmask, m->n,
-                                                                                (V - 1) / 2, m->present));
+  const int pg = grid_for(((m->n + 127) / 128) * 32, 256);
+  if (m->rowdir)
+    SC_LAUNCH("sig_present", s, k_sig_present<4><<<pg, 256, 0, s>>>(m->perm, m->rowmask, m->n, (V - 1) / 2, m->present));
+  else
+    SC_LAUNCH("sig_present", s, k_sig_present<1><<<pg, 256, 0, s>>>(m->perm, m->rowmask, m->n, (V - 1) / 2, m->present));
   e = cudaGetLastError();
   return e == cudaSuccess ? SC_OK : set_cuda_error(e, "signature sort launch");
 }

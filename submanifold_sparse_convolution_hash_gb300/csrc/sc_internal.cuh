@@ -93,9 +93,10 @@ struct KernelMap {
   int* out_rows = nullptr;
   unsigned* present = nullptr;       // [ceil(n/128), 4] offsets (< 128) with a hit in each 128-row tile of the row order
   int* cursors = nullptr;            // [V * kCursorStride] list entries reserved per offset during the build
-  // signature sort (V <= 32): the convolution walks rows in a second order
-  unsigned* rowmask = nullptr;       // [n] offsets with a neighbour, per row of the table
-  int* sig_sel = nullptr;            // [16] signature offsets, rarest first
+  // signature sort (V <= 128): the convolution walks rows in a second order
+  unsigned* rowmask = nullptr;       // [n] (V <= 32) or [n, 4] (V <= 128) offsets with a neighbour, per row of the table
+  unsigned* rowdir = nullptr;        // V > 32: [n] coarse directions with a neighbour, per row; else null
+  int* sig_sel = nullptr;            // [16] signature features (offsets or directions), rarest first
   int* sigbuckets = nullptr;         // counting-sort buckets (+ scan partials)
   int* perm = nullptr;               // [n] sorted position -> table row, or null: no sort
   int* conv_order = nullptr;         // [n] sorted position -> input row

@@ -155,6 +155,8 @@ CONV_CASES = [
     ("uniform2d", 3, 16, 16, "f16", False, "fused"),
     ("uniform2d_dense", 5, 16, 48, "bf16", True, "fused"),
     ("uniform2d_dense", 5, 48, 16, "bf16", True, "ws"),
+    ("uniform2d_dense", 7, 32, 32, "bf16", False, "fused"),  # 2D with V = 49 > 32: direction signature
+    ("indoor", 5, 64, 32, "f16", True, "fused"),
     ("lidar", 1, 32, 32, "f16", False, "fused"),
     ("lidar", 1, 32, 32, "f16", False, "ws"),
     ("indoor", 7, 32, 32, "bf16", False, None),  # V = 343: auto picks weight-stationary
