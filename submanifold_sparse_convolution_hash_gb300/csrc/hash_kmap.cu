@@ -59,7 +59,7 @@ constexpr int kSigWindow = 65536;  // rows per signature-sort window
 constexpr int kWsRows = 128;     // rows per weight-stationary tile
 // shared memory of a build block: 128 points x V <= 128 (or 32 x V <= 343)
 // neighbour slots, the ballots and the per-offset bases
-constexpr int kBuildSmemMax = 4 * (128 * 128 + 128 * 4 + 128);
+constexpr int kBuildSmemMax = 4 * (128 * 128 + 128 * 4) + 16 + 4 * 128 * 4;
 constexpr int kBucketBits = 20;    // locality-order buckets
 constexpr int kBuckets = 1 << kBucketBits;
 constexpr int kBucketBlocks = 256;                   // blocks of the bucket scan
@@ -367,23 +367,31 @@ __device__ __forceinline__ int offset_direction(int v, int K, int ndim) {
 // V - 1 - idx(d)).
 // Measured: four lookups in flight at three blocks per SM were no faster at
 // 5x5x5 (1.04 ms against 1.02 ms at 2M voxels).
-template <bool TR>
+// UP: points per unit (128, or 32 when V > 128), a compile-time constant so
+// that the count and emit loops over the unit's 32-point groups unroll and
+// their shared-memory loads overlap.
+template <bool TR, int UP>
 __global__ void __launch_bounds__(kThreads, 5) k_kmap_build(const BuildArgs a) {
   extern __shared__ int4 smem4[];
-  const int up = a.up, V = a.V;
-  const int ngroups = up / 32;
+  constexpr int up = UP;
+  constexpr int ngroups = UP / 32;
+  const int V = a.V;
   int* s_tile = reinterpret_cast<int*>(smem4);
   unsigned* s_bal = reinterpret_cast<unsigned*>(s_tile + up * V);
+  // V > 32 with the signature sort: the 128-bit offset mask of each row (in
+  // the dynamic allocation only when used), 16-byte aligned
+  unsigned* s_rmask4 = reinterpret_cast<unsigned*>(
+      (reinterpret_cast<uintptr_t>(s_bal + V * ngroups) + 15) & ~static_cast<uintptr_t>(15));
   __shared__ int s_last;
   __shared__ int s_row[128];
   __shared__ unsigned s_pres[4];
   __shared__ unsigned s_rmask[128];         // V <= 32: offsets per row; V > 32: directions per row
-  __shared__ __align__(16) unsigned s_rmask4[128 * 4];  // V > 32: 128-bit offset mask per row
   __shared__ unsigned char s_dir[128];  // V <= 128 with rowdir: coarse direction of each offset
   // covering blocks of a neighbourhood, relative to its lowest one: block t
   // at (t & 0xFF, (t >> 8) & 0xFF, t >> 16); at most (r + 1)^3 <= 81
   __shared__ uint32_t s_trip[128];
   __shared__ int s_ntrip;
+
   __shared__ long long warp_sums[32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int kWarps = kThreads / 32;
@@ -528,6 +536,7 @@ __global__ void __launch_bounds__(kThreads, 5) k_kmap_build(const BuildArgs a) {
       for (int k = 0; k < nk; ++k) {
         const int v = vb + kWarps * k;
         int cnt = 0;
+#pragma unroll
         for (int g = 0; g < ngroups; ++g) {
           const int j = s_tile[(g * 32 + lane) * V + v];
           const unsigned b = __ballot_sync(0xffffffffu, (v != centre || !a.identity) && j >= 0);
@@ -547,8 +556,12 @@ __global__ void __launch_bounds__(kThreads, 5) k_kmap_build(const BuildArgs a) {
         const int v = vb + kWarps * k;
         int at0 = __shfl_sync(0xffffffffu, base_mine, k);
         const int64_t lb = static_cast<int64_t>(v) * a.n;
+        unsigned bs[ngroups];
+#pragma unroll
+        for (int g = 0; g < ngroups; ++g) bs[g] = s_bal[v * ngroups + g];
+#pragma unroll
         for (int g = 0; g < ngroups; ++g) {
-          const unsigned b = s_bal[v * ngroups + g];
+          const unsigned b = bs[g];
           if ((b >> lane) & 1u) {
             const int64_t at = lb + at0 + __popc(b & lt);
             a.in_rows[at] = s_tile[(g * 32 + lane) * V + v];
@@ -564,6 +577,7 @@ __global__ void __launch_bounds__(kThreads, 5) k_kmap_build(const BuildArgs a) {
       }
     }
     if (a.rowmask && !a.rowdir) {  // V <= 32: one word per row
+#pragma unroll
       for (int g = 0; g < ngroups; ++g)
         if (rm[g]) atomicOr(s_rmask + g * 32 + lane, rm[g]);
     }
@@ -1029,25 +1043,35 @@ sc_status launch_kmap_build(const HashTable* in, const HashTable* h, KernelMap* 
   a.rowmask = m->rowmask;
   a.rowdir = m->rowdir;
   a.sig_sel = m->sig_sel;
-  const size_t smem = sizeof(int) * (static_cast<size_t>(m->up) * V + static_cast<size_t>(V) * (m->up / 32));
+  const size_t smem = sizeof(int) * (static_cast<size_t>(m->up) * V + static_cast<size_t>(V) * (m->up / 32)) +
+                      (m->rowdir ? 16 + sizeof(unsigned) * 128 * 4 : 0);
   if (smem > 48 * 1024) {  // set once per device: the largest the build ever asks for
     static bool done[64] = {false};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64 || !done[dev]) {
-      const void* kerns[2] = {reinterpret_cast<const void*>(k_kmap_build<false>),
-                              reinterpret_cast<const void*>(k_kmap_build<true>)};
+      const void* kerns[4] = {reinterpret_cast<const void*>(k_kmap_build<false, 128>),
+                              reinterpret_cast<const void*>(k_kmap_build<true, 128>),
+                              reinterpret_cast<const void*>(k_kmap_build<false, 32>),
+                              reinterpret_cast<const void*>(k_kmap_build<true, 32>)};
       e = cudaSuccess;
-      for (int k = 0; k < 2 && e == cudaSuccess; ++k)
+      for (int k = 0; k < 4 && e == cudaSuccess; ++k)
         e = cudaFuncSetAttribute(kerns[k], cudaFuncAttributeMaxDynamicSharedMemorySize, kBuildSmemMax);
       if (e != cudaSuccess) return set_cuda_error(e, "kmap_build smem attribute");
       if (dev >= 0 && dev < 64) done[dev] = true;
     }
   }
-  if (m->transposed)
-    SC_LAUNCH("kmap_build", s, (k_kmap_build<true><<<m->nunits, kThreads, smem, s>>>(a)));
-  else
-    SC_LAUNCH("kmap_build", s, (k_kmap_build<false><<<m->nunits, kThreads, smem, s>>>(a)));
+  if (m->up == 128) {
+    if (m->transposed)
+      SC_LAUNCH("kmap_build", s, (k_kmap_build<true, 128><<<m->nunits, kThreads, smem, s>>>(a)));
+    else
+      SC_LAUNCH("kmap_build", s, (k_kmap_build<false, 128><<<m->nunits, kThreads, smem, s>>>(a)));
+  } else {
+    if (m->transposed)
+      SC_LAUNCH("kmap_build", s, (k_kmap_build<true, 32><<<m->nunits, kThreads, smem, s>>>(a)));
+    else
+      SC_LAUNCH("kmap_build", s, (k_kmap_build<false, 32><<<m->nunits, kThreads, smem, s>>>(a)));
+  }
   e = cudaGetLastError();
   if (e != cudaSuccess) return set_cuda_error(e, "kmap_build launch");
   if (!m->perm) return SC_OK;
