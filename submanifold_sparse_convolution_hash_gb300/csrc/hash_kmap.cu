@@ -321,10 +321,10 @@ struct BuildArgs {
   int qex, qey, qez;               // extents of the queries' grid
   int stride;                      // forward: query o looks up the table points at stride * o + d
   int identity;                    // the centre list is the identity (submanifold: queries = inputs)
-  int up;                          // points per unit (128, or 32 when V > 128)
+  int up;                          // points per unit (128; 64 when V > 64; 32 when V > 128)
   int nunits;
   int* nbr;                        // [n, V] in row order
-  unsigned* present;               // [nunits, 4] (up == 128 only)
+  unsigned* present;               // [ceil(n / 128), 4] per 128-row tile (units of 128 or 64 points)
   int* in_rows;                    // [V, n] strided lists
   int* out_rows;
   int* cursors;                    // [V * kCursorStride] entries reserved so far in each offset's list
@@ -549,7 +549,7 @@ __global__ void __launch_bounds__(kThreads, 5) k_kmap_build(const BuildArgs a) {
       if (lane < nk && cnt_mine > 0) {
         const int v = vb + kWarps * lane;
         base_mine = atomicAdd(a.cursors + v * kCursorStride, cnt_mine);
-        if (v < 128 && up == 128) atomicOr(s_pres + (v >> 5), 1u << (v & 31));
+        if (v < 128 && up >= 64) atomicOr(s_pres + (v >> 5), 1u << (v & 31));
       }
       __syncwarp();
       for (int k = 0; k < nk; ++k) {
@@ -583,7 +583,10 @@ __global__ void __launch_bounds__(kThreads, 5) k_kmap_build(const BuildArgs a) {
     }
   }
   __syncthreads();
+  // present offsets of the unit's 128-row tile (two 64-point units share one: OR, on a zeroed mask)
   if (up == 128 && threadIdx.x < 4) a.present[static_cast<int64_t>(u) * 4 + threadIdx.x] = s_pres[threadIdx.x];
+  if (up == 64 && threadIdx.x < 4 && s_pres[threadIdx.x])
+    atomicOr(a.present + static_cast<int64_t>(u >> 1) * 4 + threadIdx.x, s_pres[threadIdx.x]);
   if (a.rowmask && !a.rowdir && threadIdx.x < np) a.rowmask[i0 + threadIdx.x] = s_rmask[threadIdx.x];
   if (a.rowdir && threadIdx.x < np) {  // V > 32: 128-bit offset mask and direction bits per row
     reinterpret_cast<uint4*>(a.rowmask)[i0 + threadIdx.x] = reinterpret_cast<const uint4*>(s_rmask4)[threadIdx.x];
@@ -931,7 +934,10 @@ int grid_for(int64_t n, int threads) {
 
 }  // namespace
 
-int kmap_unit_points(int V) { return V <= 128 ? 128 : 32; }
+// Points per map-build unit: 128 (one convolution tile) up to 64 offsets;
+// 64 up to 128 offsets, so that a unit's neighbour slots (64 x V ints) let
+// five blocks share an SM instead of three; 32 beyond.
+int kmap_unit_points(int V) { return V <= 64 ? 128 : (V <= 128 ? 64 : 32); }
 int kmap_order_buckets() { return kBuckets + kBucketBlocks; }
 int kmap_sig_bits() { return kSigBits; }
 int64_t kmap_sig_buckets(int64_t n) { return ((n + kSigWindow - 1) / kSigWindow) << kSigBits; }
@@ -1003,6 +1009,8 @@ sc_status launch_kmap_build(const HashTable* in, const HashTable* h, KernelMap* 
     if (e != cudaSuccess) return set_cuda_error(e, "locality order launch");
   }
   e = cudaMemsetAsync(m->cursors, 0, sizeof(int) * V * kCursorStride, s);
+  if (e == cudaSuccess && m->up == 64)  // two units OR into each tile's mask
+    e = cudaMemsetAsync(m->present, 0, sizeof(unsigned) * 4 * ((m->n + 127) / 128), s);
   if (e != cudaSuccess) return set_cuda_error(e, "kmap cursor clear");
   BuildArgs a;
   a.keys = h->keys;
@@ -1050,12 +1058,14 @@ sc_status launch_kmap_build(const HashTable* in, const HashTable* h, KernelMap* 
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64 || !done[dev]) {
-      const void* kerns[4] = {reinterpret_cast<const void*>(k_kmap_build<false, 128>),
+      const void* kerns[6] = {reinterpret_cast<const void*>(k_kmap_build<false, 128>),
                               reinterpret_cast<const void*>(k_kmap_build<true, 128>),
+                              reinterpret_cast<const void*>(k_kmap_build<false, 64>),
+                              reinterpret_cast<const void*>(k_kmap_build<true, 64>),
                               reinterpret_cast<const void*>(k_kmap_build<false, 32>),
                               reinterpret_cast<const void*>(k_kmap_build<true, 32>)};
       e = cudaSuccess;
-      for (int k = 0; k < 4 && e == cudaSuccess; ++k)
+      for (int k = 0; k < 6 && e == cudaSuccess; ++k)
         e = cudaFuncSetAttribute(kerns[k], cudaFuncAttributeMaxDynamicSharedMemorySize, kBuildSmemMax);
       if (e != cudaSuccess) return set_cuda_error(e, "kmap_build smem attribute");
       if (dev >= 0 && dev < 64) done[dev] = true;
@@ -1066,6 +1076,11 @@ sc_status launch_kmap_build(const HashTable* in, const HashTable* h, KernelMap* 
       SC_LAUNCH("kmap_build", s, (k_kmap_build<true, 128><<<m->nunits, kThreads, smem, s>>>(a)));
     else
       SC_LAUNCH("kmap_build", s, (k_kmap_build<false, 128><<<m->nunits, kThreads, smem, s>>>(a)));
+  } else if (m->up == 64) {
+    if (m->transposed)
+      SC_LAUNCH("kmap_build", s, (k_kmap_build<true, 64><<<m->nunits, kThreads, smem, s>>>(a)));
+    else
+      SC_LAUNCH("kmap_build", s, (k_kmap_build<false, 64><<<m->nunits, kThreads, smem, s>>>(a)));
   } else {
     if (m->transposed)
       SC_LAUNCH("kmap_build", s, (k_kmap_build<true, 32><<<m->nunits, kThreads, smem, s>>>(a)));

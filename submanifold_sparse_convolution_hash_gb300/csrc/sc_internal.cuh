@@ -82,7 +82,7 @@ struct KernelMap {
   bool transposed = false;           // rows = a layer's inputs, neighbours = its outputs at mirrored offsets
   int ndim = 3, K = 3, V = 27;
   int dims[3] = {1, 1, 1};
-  int up = 128;                      // points per map-build unit (128; 32 when V > 128)
+  int up = 128;                      // points per map-build unit (128; 64 when V > 64; 32 when V > 128)
   int nunits = 0;                    // map-build units
   int* order = nullptr;              // [n] input rows in locality order, or null: input order
   unsigned long long* skeys = nullptr;  // [n] packed keys in locality order (with order)

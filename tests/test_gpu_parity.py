@@ -61,8 +61,8 @@ def test_hash_query_finds_every_row_and_misses_absent_keys():
 
 # ------------------------------------------------------------------- map --
 
-@pytest.mark.parametrize("name,K", [("uniform2d", 3), ("uniform2d_dense", 5), ("lidar", 3), ("indoor", 3),
-                                    ("indoor", 5), ("batch", 3), ("lidar", 1), ("indoor", 7)])
+@pytest.mark.parametrize("name,K", [("uniform2d", 3), ("uniform2d_dense", 5), ("uniform2d_dense", 9), ("lidar", 3),
+                                    ("indoor", 3), ("indoor", 5), ("batch", 3), ("lidar", 1), ("indoor", 7)])
 @pytest.mark.parametrize("sync,order,sort", [(True, False, False), (False, False, False), (True, True, False),
                                              (False, True, False), (True, False, True), (False, True, True)])
 def test_kmap_bit_exact(name, K, sync, order, sort):
@@ -156,6 +156,7 @@ CONV_CASES = [
     ("uniform2d_dense", 5, 16, 48, "bf16", True, "fused"),
     ("uniform2d_dense", 5, 48, 16, "bf16", True, "ws"),
     ("uniform2d_dense", 7, 32, 32, "bf16", False, "fused"),  # 2D with V = 49 > 32: direction signature
+    ("uniform2d_dense", 9, 16, 32, "f16", False, "fused"),   # V = 81: 64-point map-build units
     ("indoor", 5, 64, 32, "f16", True, "fused"),
     ("lidar", 1, 32, 32, "f16", False, "fused"),
     ("lidar", 1, 32, 32, "f16", False, "ws"),
