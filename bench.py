@@ -50,8 +50,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 # the kernels of the map build (hash insert, output set, row order, map,
 # signature sort): their event-timed sum is the step's map-build kernel time
 MAP_KERNELS = ("hash_insert", "out_mark", "out_count", "out_scan", "out_number", "order_count", "order_partials",
-               "order_apply", "order_scatter", "kmap_build", "sig_count", "sig_partials", "sig_scan", "sig_scatter",
-               "sig_present")
+               "order_apply", "order_scatter", "kmap_clear", "kmap_build", "kmap_masks", "sig_count", "sig_partials",
+               "sig_scan", "sig_scatter", "sig_present")
 sys.path.insert(0, ROOT)
 
 METRIC = "subm-conv layer effective TFLOP/s, Mvoxels/s & % roofline; kernel-map build ms"
@@ -81,6 +81,8 @@ def parse_args():
                     help="regular: a dilating layer (stride 1, output set grown by the kernel window); strided: "
                          "a layer on the grid coarsened by --stride; both run the workload's first layer only")
     ap.add_argument("--stride", type=int, default=2, help="stride of --layer-type strided")
+    ap.add_argument("--kmap-half", action="store_true",
+                    help="build submanifold maps with the half probe (mirror symmetry) instead of the full probe")
     return ap.parse_args()
 
 
@@ -119,6 +121,10 @@ def algo_bytes_step(kernel: str, N: int, V: int, M: int, layers, s: int, ntiles:
         "hash_insert": 16 * N + 8 * N + 4 * N,
         # row keys in; neighbour table and (in, out) lists out
         "kmap_build": 8 * No + 4 * No * V + lists,
+        # the half probe's clear of the columns before the centre, and its mask
+        # pass (reads the table once, writes the tile masks)
+        "kmap_clear": 4 * No * ((V - 1) // 2),
+        "kmap_masks": 4 * No * V + 16 * ((No + 127) // 128),
         "order_count": 8 * N,
         "order_scatter": 8 * N + 4 * N,
         "pack_weights": sum(2 * V * ci * co * s for ci, co in conv_layers),
@@ -570,7 +576,7 @@ def run_ours(args):
         (regular / strided; the output set's count is read on the host)."""
         h = sc.sc_hash_build(c)
         if not general:
-            return (h,), sc.sc_kmap_build(h, s.ndim, w.K, s.dims, sync=sync)
+            return (h,), sc.sc_kmap_build(h, s.ndim, w.K, s.dims, sync=sync, half=args.kmap_half)
         ho = sc.sc_hash_build_conv_out(h, s.ndim, w.K, conv_stride, s.dims)
         return (h, ho), sc.sc_kmap_build_conv(h, ho, s.ndim, w.K, conv_stride, s.dims, sync=sync)
 
@@ -739,7 +745,8 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": workload_config(w, s, M, world, args.layer_type, conv_stride, n_out, args.backward, args.scale),
-        "run": {"variant": variants, "variant_choice": "given" if args.variant else "measured", "kmap_sync": False},
+        "run": {"variant": variants, "variant_choice": "given" if args.variant else "measured", "kmap_sync": False,
+                "kmap_probe": "half (mirror symmetry)" if args.kmap_half else "full"},
         "layer_tflops": round(flops / (conv_ms / 1e3) / 1e12, 3) if conv_ms else None,
         "layer_ms": round(conv_ms, 5),
         "layer_roofline_frac": round(conv_roof_s / (conv_ms / 1e3), 4) if conv_ms else None,

@@ -26,10 +26,12 @@
  * asynchronous on the given stream unless stated.  Errors in the arguments
  * are returned synchronously; no call aborts, throws or traps.
  *
- * Memory.  Handles own their device buffers, allocated stream-ordered
- * (cudaMallocAsync) on the stream passed at build time and released
- * stream-ordered on the stream passed to *_destroy.  The caller owns coords,
- * feats, W and out.
+ * Memory.  Handles own their device buffers, allocated on the stream passed
+ * at build time from the allocator passed to the build call (NULL: the
+ * process-wide one, see sc_set_allocator; by default CUDA's stream-ordered
+ * pool) and released stream-ordered on the stream passed to *_destroy, each
+ * buffer to the allocator that made it.  The caller owns coords, feats, W and
+ * out.
  */
 #ifndef SC_H_
 #define SC_H_
@@ -72,9 +74,26 @@ typedef enum { SC_F32 = 0, SC_F16 = 1, SC_BF16 = 2 } sc_dtype;
 #define SC_KMAP_SORT 0x800u     /* always sort the convolution's rows by signature (default: n >= 262144, V <= 128) */
 #define SC_KMAP_NO_SORT 0x1000u /* never sort them */
 #define SC_KMAP_TRANSPOSE 0x2000u /* sc_kmap_build_conv: the transposed map (rows = the layer's inputs) */
+#define SC_KMAP_HALF 0x4000u    /* sc_kmap_build: half probe by mirror symmetry (same map, another build) */
 
 typedef struct sc_hash_s* sc_hash;
 typedef struct sc_kmap_s* sc_kmap;
+
+/*
+ * A caller's device-memory allocator (see "Device memory" below).
+ * alloc(bytes, stream, ctx) returns device memory of at least `bytes`,
+ * 256-byte aligned, usable in stream order on `stream`, or NULL (the call
+ * then fails with SC_ERR_OOM); free(ptr, stream, ctx) releases it after the
+ * work queued on `stream`.  The callbacks run on the calling host thread and
+ * must not call back into the library.
+ */
+typedef void* (*sc_alloc_fn)(size_t bytes, sc_stream stream, void* ctx);
+typedef void (*sc_free_fn)(void* ptr, sc_stream stream, void* ctx);
+typedef struct {
+  sc_alloc_fn alloc;
+  sc_free_fn free;
+  void* ctx;
+} sc_allocator;
 
 /* ---------------------------------------------------------------- hash -- */
 
@@ -88,6 +107,9 @@ typedef struct sc_kmap_s* sc_kmap;
  * d_coords  int32 [n, 4] row-major (batch, x, y, z), 16-byte aligned.
  *           batch in [0, 65535), x, y, z in [0, 65535).
  * n         number of points, 0 <= n < 2^31.
+ * alloc     the allocator of the handle's buffers, or NULL (the process-wide
+ *           one).  The struct is copied; its callbacks and ctx must stay
+ *           valid until the handle is destroyed.
  * out       receives the handle.
  *
  * Keys are packed into 64 bits (16 bits per field, batch highest).  The
@@ -98,7 +120,8 @@ typedef struct sc_kmap_s* sc_kmap;
  * duplicate or out-of-range coordinate is latched in the handle and reported
  * by sc_hash_check, sc_kmap_build or sc_kmap_check.
  */
-sc_status sc_hash_build(const int32_t* d_coords, int64_t n, sc_stream stream, sc_hash* out);
+sc_status sc_hash_build(const int32_t* d_coords, int64_t n, const sc_allocator* alloc, sc_stream stream,
+                        sc_hash* out);
 
 /* Row id of each query coordinate, -1 where it is not in the table.
  * d_query int32 [m, 4] (16-byte aligned), d_rows int32 [m]. Asynchronous. */
@@ -143,8 +166,8 @@ sc_status sc_hash_destroy(sc_hash h, sc_stream stream);
  * output table would exceed 2^28 entries.  Device memory is allocated
  * stream-ordered on `stream` and owned by the handle.
  */
-sc_status sc_hash_build_conv_out(sc_hash in, int ndim, int K, int stride, const int32_t dims[3], sc_stream stream,
-                                 sc_hash* out);
+sc_status sc_hash_build_conv_out(sc_hash in, int ndim, int K, int stride, const int32_t dims[3],
+                                 const sc_allocator* alloc, sc_stream stream, sc_hash* out);
 
 /* Coordinates of every row of the hash: d_coords int32 [n, 4] = (batch, x,
  * y, z), device memory, 16-byte aligned, written asynchronously. */
@@ -203,7 +226,7 @@ sc_status sc_hash_coords(sc_hash h, int32_t* d_coords, sc_stream stream);
  * surface in sc_kmap_check.
  */
 sc_status sc_kmap_build(sc_hash h, int ndim, int K, const int32_t dims[3], unsigned flags,
-                        sc_stream stream, sc_kmap* out);
+                        const sc_allocator* alloc, sc_stream stream, sc_kmap* out);
 
 /*
  * Kernel map of a regular / strided layer: the rows are the points of
@@ -231,7 +254,7 @@ sc_status sc_kmap_build(sc_hash h, int ndim, int K, const int32_t dims[3], unsig
  * returns SC_ERR_UNSUPPORTED there.
  */
 sc_status sc_kmap_build_conv(sc_hash in, sc_hash out_set, int ndim, int K, int stride, const int32_t dims[3],
-                             unsigned flags, sc_stream stream, sc_kmap* out);
+                             unsigned flags, const sc_allocator* alloc, sc_stream stream, sc_kmap* out);
 
 /* n, V and |M| (centre included).  Synchronises the stream when |M| is not
  * yet known on the host. */
@@ -248,6 +271,28 @@ sc_status sc_kmap_check(sc_kmap m, sc_stream stream);
  */
 sc_status sc_kmap_export(sc_kmap m, int32_t* nbr, int64_t* offs, int32_t* in_rows, int32_t* out_rows,
                          sc_stream stream);
+
+/*
+ * Borrowed device pointers to the products (the rulebook grouped by weight
+ * offset, "SparseConvNet: from hash table to rulebook", section 3; the map as
+ * the computation, "Sparse inputs and sparse convolution", section "The map
+ * is the computation"), in the layout sc_kmap_export writes:
+ *   *d_nbr   int32 [n, V], rows in input row order (nbr[q*V + idx(d)]);
+ *   *d_offs  int64 [V+1], the segments of the lists;
+ *   *d_in, *d_out  int32 [offs[V]], the list entries (p, q) by segment;
+ *   *map_size      |M| (host value).
+ * Any output may be NULL to skip it.  The pointers stay valid, and their
+ * contents unchanged, until the handle is destroyed; the caller must not
+ * write through them.  The first call materialises the forms the handle does
+ * not keep internally (rows back in input order when the locality order is
+ * on; the lists compacted from their fixed per-offset strides) into buffers
+ * the handle owns, from the handle's allocator, on the stream the map was
+ * built on, and synchronises that stream (which must still exist); later
+ * calls return the same pointers without device work.  Errors: the map's
+ * latched status (as sc_kmap_check), SC_ERR_OOM, SC_ERR_CUDA.
+ */
+sc_status sc_kmap_view(sc_kmap m, const int32_t** d_nbr, const int64_t** d_offs, const int32_t** d_in,
+                       const int32_t** d_out, int64_t* map_size);
 
 /* Releases the handle's buffers stream-ordered on `stream`. */
 sc_status sc_kmap_destroy(sc_kmap m, sc_stream stream);
@@ -362,7 +407,11 @@ sc_status sc_subm_conv_fwd_noalloc(sc_kmap m, const void* d_feats, const void* d
  * the call's stream; the pool keeps freed blocks for reuse).  With
  * sc_set_allocator the library asks the caller's allocator instead, so an
  * application can keep all device memory in one pool (the Python binding
- * offers PyTorch's caching allocator).  The source pages have no counterpart.
+ * offers PyTorch's caching allocator).  A build call (sc_hash_build,
+ * sc_hash_build_conv_out, sc_kmap_build, sc_kmap_build_conv) given a non-NULL
+ * sc_allocator uses that one for the handle it makes, whatever the
+ * process-wide setting is; the handle keeps a copy for the buffers it
+ * allocates later (sc_kmap_view).  The source pages have no counterpart.
  *
  * alloc(bytes, stream, ctx) returns device memory of at least `bytes`,
  * 256-byte aligned, usable in stream order on `stream` (the stream of the
@@ -377,8 +426,6 @@ sc_status sc_subm_conv_fwd_noalloc(sc_kmap m, const void* d_feats, const void* d
  * not call back into the library.  sc_subm_conv_fwd_noalloc allocates
  * nothing either way.
  */
-typedef void* (*sc_alloc_fn)(size_t bytes, sc_stream stream, void* ctx);
-typedef void (*sc_free_fn)(void* ptr, sc_stream stream, void* ctx);
 sc_status sc_set_allocator(sc_alloc_fn alloc, sc_free_fn free_fn, void* ctx);
 
 /* ---------------------------------------------------------- diagnostics -- */

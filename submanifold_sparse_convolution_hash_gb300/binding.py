@@ -25,6 +25,7 @@ SC_KMAP_NO_ORDER = 0x400
 SC_KMAP_SORT = 0x800
 SC_KMAP_NO_SORT = 0x1000
 SC_KMAP_TRANSPOSE = 0x2000
+SC_KMAP_HALF = 0x4000
 VARIANTS = {"fused": SC_VARIANT_FUSED, "ws": SC_VARIANT_WS, "simt": SC_VARIANT_SIMT}
 VARIANT_NAMES = {v: k for k, v in VARIANTS.items()}
 _DTYPES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
@@ -53,15 +54,16 @@ def lib():
         L = ctypes.CDLL(_LIB_PATH)
         P, I64, I32, U = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint
         sig = {
-            "sc_hash_build": ([P, I64, P, P], I32),
+            "sc_hash_build": ([P, I64, P, P, P], I32),
             "sc_hash_query": ([P, P, I64, P, P], I32),
             "sc_hash_info": ([P, P, P], I32),
             "sc_hash_check": ([P, P], I32),
             "sc_hash_destroy": ([P, P], I32),
-            "sc_hash_build_conv_out": ([P, I32, I32, I32, P, P, P], I32),
+            "sc_hash_build_conv_out": ([P, I32, I32, I32, P, P, P, P], I32),
             "sc_hash_coords": ([P, P, P], I32),
-            "sc_kmap_build_conv": ([P, P, I32, I32, I32, P, U, P, P], I32),
-            "sc_kmap_build": ([P, I32, I32, P, U, P, P], I32),
+            "sc_kmap_build_conv": ([P, P, I32, I32, I32, P, U, P, P, P], I32),
+            "sc_kmap_build": ([P, I32, I32, P, U, P, P, P], I32),
+            "sc_kmap_view": ([P, P, P, P, P, P], I32),
             "sc_kmap_info": ([P, P, P, P, P], I32),
             "sc_kmap_check": ([P, P], I32),
             "sc_kmap_export": ([P, P, P, P, P, P], I32),
@@ -92,7 +94,8 @@ def lib():
 def exported_symbols() -> list:
     return [n for n in ("sc_hash_build", "sc_hash_query", "sc_hash_info", "sc_hash_check", "sc_hash_destroy",
                         "sc_hash_build_conv_out", "sc_hash_coords", "sc_kmap_build_conv",
-                        "sc_kmap_build", "sc_kmap_info", "sc_kmap_check", "sc_kmap_export", "sc_kmap_destroy",
+                        "sc_kmap_build", "sc_kmap_info", "sc_kmap_check", "sc_kmap_export", "sc_kmap_view",
+                        "sc_kmap_destroy",
                         "sc_subm_conv_fwd", "sc_subm_conv_tune", "sc_subm_conv_fwd_noalloc",
                         "sc_subm_conv_bwd_data", "sc_subm_conv_bwd_weight", "sc_set_allocator",
                         "sc_status_str", "sc_last_error",
@@ -206,6 +209,36 @@ class KernelMap:
                                     _stream(stream)), "sc_kmap_export")
         return offs, i, o
 
+    def view(self):
+        """Borrowed, zero-copy device tensors of the products (sc_kmap_view):
+        {"nbr": int32 [n, V], "offs": int64 [V+1], "in": int32 [L], "out":
+        int32 [L], "map_size": |M|}.  They alias memory the handle owns: valid
+        while this map is alive (each tensor keeps a reference to it), and not
+        to be written."""
+        nbr, offs, i, o = (ctypes.c_void_p() for _ in range(4))
+        ms = ctypes.c_int64()
+        _check(lib().sc_kmap_view(self._h, ctypes.byref(nbr), ctypes.byref(offs), ctypes.byref(i), ctypes.byref(o),
+                                  ctypes.byref(ms)), "sc_kmap_view")
+        L = ms.value - (self.n if self.identity else 0)
+
+        def wrap(ptr, shape, typestr):
+            n_el = 1
+            for d in shape:
+                n_el *= d
+            if n_el == 0 or not ptr.value:
+                return torch.empty(shape, dtype=torch.int64 if typestr == "<i8" else torch.int32, device=self.device)
+            owner = self
+
+            class _Borrowed:
+                # torch takes only writable interfaces; the memory is read-only by contract
+                __cuda_array_interface__ = {"shape": tuple(shape), "typestr": typestr, "data": (ptr.value, False),
+                                            "version": 3, "strides": None}
+                keep = owner  # the map outlives the tensor's view of it
+            return torch.as_tensor(_Borrowed(), device=self.device)
+
+        return {"nbr": wrap(nbr, (self.n, self.volume), "<i4"), "offs": wrap(offs, (self.volume + 1,), "<i8"),
+                "in": wrap(i, (max(L, 0),), "<i4"), "out": wrap(o, (max(L, 0),), "<i4"), "map_size": ms.value}
+
     def destroy(self, stream=None):
         if self._h:
             lib().sc_kmap_destroy(self._h, _stream(stream))
@@ -218,13 +251,14 @@ class KernelMap:
             pass
 
 
-def sc_hash_build(coords: torch.Tensor, stream=None) -> Hash:
+def sc_hash_build(coords: torch.Tensor, stream=None, allocator=None) -> Hash:
     """Hash table over int32 coords [N, 4] = (batch, x, y, z) on a CUDA device."""
     c = _dev(coords, "coords")
     if c.dtype != torch.int32 or c.dim() != 2 or c.shape[1] != 4:
         raise ValueError("coords must be int32 [N, 4]")
     h = ctypes.c_void_p()
-    _check(lib().sc_hash_build(_ptr(c), c.shape[0], _stream(stream), ctypes.byref(h)), "sc_hash_build")
+    _check(lib().sc_hash_build(_ptr(c), c.shape[0], _alloc_arg(allocator), _stream(stream), ctypes.byref(h)),
+           "sc_hash_build")
     n = ctypes.c_int64()
     cap = ctypes.c_int64()
     lib().sc_hash_info(h, ctypes.byref(n), ctypes.byref(cap))
@@ -232,16 +266,19 @@ def sc_hash_build(coords: torch.Tensor, stream=None) -> Hash:
 
 
 def sc_kmap_build(h: Hash, ndim: int, K: int, dims, sync: bool = True, order: bool | None = None,
-                  sort: bool | None = None, stream=None) -> KernelMap:
+                  sort: bool | None = None, half: bool = False, stream=None, allocator=None) -> KernelMap:
     """Kernel map of a K^ndim submanifold convolution over the hashed points.
 
     order: True / False forces the locality order on / off; None leaves the
     library's default (on for n >= 262144).  sort: the same for the
     signature sort of the convolution's rows (default on for n >= 262144 when
-    K^ndim <= 32)."""
+    K^ndim <= 128).  half: build it by the half probe (mirror symmetry); the
+    map is the same."""
     d = (ctypes.c_int32 * 3)(*(list(dims) + [1] * (3 - len(dims))))
     m = ctypes.c_void_p()
     flags = 0 if sync else SC_KMAP_NO_SYNC
+    if half:
+        flags |= SC_KMAP_HALF
     if order is True:
         flags |= SC_KMAP_ORDER
     elif order is False:
@@ -250,16 +287,18 @@ def sc_kmap_build(h: Hash, ndim: int, K: int, dims, sync: bool = True, order: bo
         flags |= SC_KMAP_SORT
     elif sort is False:
         flags |= SC_KMAP_NO_SORT
-    _check(lib().sc_kmap_build(h._h, ndim, K, d, flags, _stream(stream), ctypes.byref(m)), "sc_kmap_build")
+    _check(lib().sc_kmap_build(h._h, ndim, K, d, flags, _alloc_arg(allocator), _stream(stream), ctypes.byref(m)),
+           "sc_kmap_build")
     return KernelMap(m, h.n, ndim, K, list(d), h.device)
 
 
-def sc_hash_build_conv_out(h: Hash, ndim: int, K: int, stride: int, dims, stream=None) -> Hash:
+def sc_hash_build_conv_out(h: Hash, ndim: int, K: int, stride: int, dims, stream=None, allocator=None) -> Hash:
     """Output set of a regular (stride 1: dilating) or strided layer over the
     points of `h`: every o with an input at stride * o + d (synchronises)."""
     d = (ctypes.c_int32 * 3)(*(list(dims) + [1] * (3 - len(dims))))
     o = ctypes.c_void_p()
-    _check(lib().sc_hash_build_conv_out(h._h, ndim, K, stride, d, _stream(stream), ctypes.byref(o)),
+    _check(lib().sc_hash_build_conv_out(h._h, ndim, K, stride, d, _alloc_arg(allocator), _stream(stream),
+                                        ctypes.byref(o)),
            "sc_hash_build_conv_out")
     n = ctypes.c_int64()
     cap = ctypes.c_int64()
@@ -268,7 +307,7 @@ def sc_hash_build_conv_out(h: Hash, ndim: int, K: int, stride: int, dims, stream
 
 
 def sc_kmap_build_conv(h_in: Hash, h_out: Hash, ndim: int, K: int, stride: int, dims, sync: bool = True,
-                       order: bool | None = None, transpose: bool = False, stream=None) -> KernelMap:
+                       order: bool | None = None, transpose: bool = False, stream=None, allocator=None) -> KernelMap:
     """Kernel map of a regular / strided layer: rows = the points of `h_out`,
     neighbours = rows of `h_in` at stride * o + d.  transpose: the transposed
     map (rows = the points of `h_in`, neighbours = the outputs whose windows
@@ -282,7 +321,8 @@ def sc_kmap_build_conv(h_in: Hash, h_out: Hash, ndim: int, K: int, stride: int, 
         flags |= SC_KMAP_ORDER
     elif order is False:
         flags |= SC_KMAP_NO_ORDER
-    _check(lib().sc_kmap_build_conv(h_in._h, h_out._h, ndim, K, stride, d, flags, _stream(stream), ctypes.byref(m)),
+    _check(lib().sc_kmap_build_conv(h_in._h, h_out._h, ndim, K, stride, d, flags, _alloc_arg(allocator),
+                                    _stream(stream), ctypes.byref(m)),
            "sc_kmap_build_conv")
     if transpose:
         return KernelMap(m, h_in.n, ndim, K, list(d), h_in.device, n_in=h_out.n, stride=stride)
@@ -381,13 +421,25 @@ _FREE_FN = ctypes.CFUNCTYPE(None, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_voi
 _torch_allocator = None  # the callbacks stay alive: buffers they made are freed through them
 
 
-def use_torch_allocator(on: bool = True):
-    """Route the library's device memory through PyTorch's caching allocator
-    (on) or back to CUDA's stream-ordered pool (off) (sc_set_allocator)."""
+class Allocator(ctypes.Structure):
+    """sc_allocator: a caller's device allocator for one build call."""
+    _fields_ = [("alloc", ctypes.c_void_p), ("free", ctypes.c_void_p), ("ctx", ctypes.c_void_p)]
+
+
+def _alloc_arg(allocator):
+    return ctypes.byref(allocator) if allocator is not None else None
+
+
+def torch_allocator() -> Allocator:
+    """An sc_allocator over PyTorch's caching allocator, for the allocator
+    argument of the build calls (the callbacks live as long as the module)."""
+    _torch_callbacks()
+    return Allocator(ctypes.cast(_torch_allocator[0], ctypes.c_void_p).value,
+                     ctypes.cast(_torch_allocator[1], ctypes.c_void_p).value, None)
+
+
+def _torch_callbacks():
     global _torch_allocator
-    if not on:
-        _check(lib().sc_set_allocator(None, None, None), "sc_set_allocator")
-        return
     if _torch_allocator is None:
         def _alloc(nbytes, stream, ctx):
             try:
@@ -399,6 +451,16 @@ def use_torch_allocator(on: bool = True):
             torch.cuda.caching_allocator_delete(int(ptr))
 
         _torch_allocator = (_ALLOC_FN(_alloc), _FREE_FN(_free))
+    return _torch_allocator
+
+
+def use_torch_allocator(on: bool = True):
+    """Route the library's device memory through PyTorch's caching allocator
+    (on) or back to CUDA's stream-ordered pool (off) (sc_set_allocator)."""
+    if not on:
+        _check(lib().sc_set_allocator(None, None, None), "sc_set_allocator")
+        return
+    _torch_callbacks()
     a = ctypes.cast(_torch_allocator[0], ctypes.c_void_p)
     f = ctypes.cast(_torch_allocator[1], ctypes.c_void_p)
     _check(lib().sc_set_allocator(a, f, None), "sc_set_allocator")

@@ -24,6 +24,18 @@ struct sc_hash_s {
 struct sc_kmap_s {
   sc::KernelMap k;
   void* arena = nullptr;  // one device allocation holding every buffer of k
+  // the build call's allocator (if one was given) and stream, for the
+  // buffers made later (the exported forms behind sc_kmap_view)
+  bool has_alloc = false;
+  sc_allocator alloc{};
+  cudaStream_t stream = nullptr;
+  // sc_kmap_view: rows in input order (k.nbr itself without the locality
+  // order) and the compacted lists, materialised on first use
+  bool view_ready = false;
+  void* view_arena = nullptr;
+  const int32_t* view_nbr = nullptr;
+  const int32_t* view_in = nullptr;
+  const int32_t* view_out = nullptr;
 };
 
 namespace sc {
@@ -214,11 +226,15 @@ Allocator g_alloc;
 std::unordered_map<void*, Allocator> g_alloc_owner;
 }  // namespace
 
-sc_status dev_alloc(void** p, size_t bytes, cudaStream_t s) {
+sc_status dev_alloc(void** p, size_t bytes, cudaStream_t s, const sc_allocator* with) {
   *p = nullptr;
   if (bytes == 0) bytes = 16;
   Allocator a;
-  {
+  if (with && with->alloc) {
+    a.alloc = with->alloc;
+    a.free = with->free;
+    a.ctx = with->ctx;
+  } else {
     std::lock_guard<std::mutex> lk(g_alloc_mu);
     a = g_alloc;
   }
@@ -439,10 +455,12 @@ sc_status sc_profile_get(int index, const char** name, int64_t* launches, double
 }
 
 // ------------------------------------------------------------------ hash --
-sc_status sc_hash_build(const int32_t* d_coords, int64_t n, sc_stream stream, sc_hash* out) {
+sc_status sc_hash_build(const int32_t* d_coords, int64_t n, const sc_allocator* alloc, sc_stream stream, sc_hash* out) {
   if (!out) return set_error(SC_ERR_INVALID_ARG, "out is NULL");
   *out = nullptr;
   if (n < 0 || n >= (int64_t(1) << 31)) return set_error(SC_ERR_INVALID_ARG, "n must be in [0, 2^31)");
+  if (alloc && (alloc->alloc == nullptr) != (alloc->free == nullptr))
+    return set_error(SC_ERR_INVALID_ARG, "an sc_allocator needs both alloc and free, or neither");
   if (n > 0) {
     sc_status st = check_dev_ptr(d_coords, 16, "coords");
     if (st) return st;
@@ -471,7 +489,7 @@ sc_status sc_hash_build(const int32_t* d_coords, int64_t n, sc_stream stream, sc
   t.capacity = cap;
   const size_t tb = sizeof(BlockEntry) * static_cast<size_t>(cap);
   const size_t kb = (sizeof(unsigned long long) * static_cast<size_t>(n > 0 ? n : 1) + 255) & ~size_t(255);
-  sc_status st = dev_alloc(&h->arena, tb + kb + 256, s);
+  sc_status st = dev_alloc(&h->arena, tb + kb + 256, s, alloc);
   if (!st) {
     uint8_t* b = static_cast<uint8_t*>(h->arena);
     t.table = reinterpret_cast<BlockEntry*>(b);
@@ -522,8 +540,8 @@ sc_status sc_hash_destroy(sc_hash h, sc_stream stream) {
   return SC_OK;
 }
 
-sc_status sc_hash_build_conv_out(sc_hash in, int ndim, int K, int stride, const int32_t dims[3], sc_stream stream,
-                                 sc_hash* out) {
+sc_status sc_hash_build_conv_out(sc_hash in, int ndim, int K, int stride, const int32_t dims[3],
+                                 const sc_allocator* alloc, sc_stream stream, sc_hash* out) {
   if (!out) return set_error(SC_ERR_INVALID_ARG, "out is NULL");
   *out = nullptr;
   if (!in) return set_error(SC_ERR_INVALID_ARG, "hash handle is NULL");
@@ -533,12 +551,14 @@ sc_status sc_hash_build_conv_out(sc_hash in, int ndim, int K, int stride, const 
   if (!dims) return set_error(SC_ERR_INVALID_ARG, "dims is NULL");
   for (int a = 0; a < 3; ++a)
     if (dims[a] < 1 || dims[a] > 65535) return set_error(SC_ERR_INVALID_ARG, "dims must be in [1, 65535]");
+  if (alloc && (alloc->alloc == nullptr) != (alloc->free == nullptr))
+    return set_error(SC_ERR_INVALID_ARG, "an sc_allocator needs both alloc and free, or neither");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // the inputs must be valid points inside dims before their outputs are derived
   sc_status st = sc_hash_check(in, stream);
   if (st) return st;
   sc_hash h = new sc_hash_s();
-  st = launch_conv_out(&in->t, ndim, K, stride, dims, &h->t, &h->arena, &h->arena2, s);
+  st = launch_conv_out(&in->t, ndim, K, stride, dims, &h->t, &h->arena, &h->arena2, alloc, s);
   if (st) {
     sc_hash_destroy(h, stream);
     return st;
@@ -559,6 +579,7 @@ sc_status sc_hash_coords(sc_hash h, int32_t* d_coords, sc_stream stream) {
 sc_status sc_kmap_destroy(sc_kmap m, sc_stream stream) {
   if (!m) return SC_OK;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  dev_free(m->view_arena, s);
   dev_free(m->arena, s);
   delete m;
   return SC_OK;
@@ -575,7 +596,7 @@ namespace {
 // when ho == hi and stride == 1 (the centre list is the identity), else the
 // map of a regular / strided layer.
 sc_status kmap_build_impl(sc_hash hi, sc_hash ho, int ndim, int K, int stride, const int32_t dims[3],
-                          unsigned flags, sc_stream stream, sc_kmap* out) {
+                          unsigned flags, const sc_allocator* alloc, sc_stream stream, sc_kmap* out) {
   if (!out) return set_error(SC_ERR_INVALID_ARG, "out is NULL");
   *out = nullptr;
   if (!hi || !ho) return set_error(SC_ERR_INVALID_ARG, "hash handle is NULL");
@@ -596,8 +617,11 @@ sc_status kmap_build_impl(sc_hash hi, sc_hash ho, int ndim, int K, int stride, c
   if (!dims) return set_error(SC_ERR_INVALID_ARG, "dims is NULL");
   for (int a = 0; a < 3; ++a)
     if (dims[a] < 1 || dims[a] > 65535) return set_error(SC_ERR_INVALID_ARG, "dims must be in [1, 65535]");
-  if (flags & ~(SC_KMAP_NO_SYNC | SC_KMAP_ORDER | SC_KMAP_NO_ORDER | SC_KMAP_SORT | SC_KMAP_NO_SORT | SC_KMAP_TRANSPOSE))
+  if (flags & ~(SC_KMAP_NO_SYNC | SC_KMAP_ORDER | SC_KMAP_NO_ORDER | SC_KMAP_SORT | SC_KMAP_NO_SORT | SC_KMAP_TRANSPOSE |
+                SC_KMAP_HALF))
     return set_error(SC_ERR_INVALID_ARG, "unknown kmap flag");
+  if ((flags & SC_KMAP_HALF) && !identity)
+    return set_error(SC_ERR_UNSUPPORTED, "SC_KMAP_HALF builds submanifold maps only");
   if ((flags & SC_KMAP_ORDER) && (flags & SC_KMAP_NO_ORDER))
     return set_error(SC_ERR_INVALID_ARG, "SC_KMAP_ORDER and SC_KMAP_NO_ORDER together");
   if ((flags & SC_KMAP_SORT) && (flags & SC_KMAP_NO_SORT))
@@ -614,6 +638,7 @@ sc_status kmap_build_impl(sc_hash hi, sc_hash ho, int ndim, int K, int stride, c
   k.K = K;
   k.V = V;
   for (int a = 0; a < 3; ++a) k.dims[a] = dims[a];
+  k.half = (flags & SC_KMAP_HALF) != 0;
   k.up = kmap_unit_points(V);
   k.nunits = static_cast<int>((k.n + k.up - 1) / k.up);
   const bool ordered = (flags & SC_KMAP_ORDER) || (!(flags & SC_KMAP_NO_ORDER) && k.n >= kOrderMinPoints);
@@ -639,6 +664,7 @@ sc_status kmap_build_impl(sc_hash hi, sc_hash ho, int ndim, int K, int stride, c
       {reinterpret_cast<void**>(&k.status), sizeof(int) * 4},
       {reinterpret_cast<void**>(&k.order), ordered && k.n > 0 ? sizeof(int) * n : 0},
       {reinterpret_cast<void**>(&k.skeys), ordered && k.n > 0 ? sizeof(unsigned long long) * n : 0},
+      {reinterpret_cast<void**>(&k.inv_order), ordered && k.half && k.n > 0 ? sizeof(int) * n : 0},
       {reinterpret_cast<void**>(&k.buckets), ordered && k.n > 0 ? sizeof(int) * kmap_order_buckets() : 0},
       {reinterpret_cast<void**>(&k.rowmask), sorted ? sizeof(unsigned) * n * mask_words : 0},
       {reinterpret_cast<void**>(&k.rowdir), sorted && V > 32 ? sizeof(unsigned) * n : 0},
@@ -649,7 +675,16 @@ sc_status kmap_build_impl(sc_hash hi, sc_hash ho, int ndim, int K, int stride, c
   };
   size_t total = 0;
   for (const Part& pt : parts) total += (pt.bytes + 255) & ~size_t(255);
-  sc_status st = dev_alloc(&m->arena, total, s);
+  if (alloc && (alloc->alloc == nullptr) != (alloc->free == nullptr)) {
+    delete m;
+    return set_error(SC_ERR_INVALID_ARG, "an sc_allocator needs both alloc and free, or neither");
+  }
+  m->stream = s;
+  if (alloc && alloc->alloc) {
+    m->has_alloc = true;
+    m->alloc = *alloc;
+  }
+  sc_status st = dev_alloc(&m->arena, total, s, m->has_alloc ? &m->alloc : nullptr);
   if (!st) {
     uint8_t* base = static_cast<uint8_t*>(m->arena);
     for (const Part& pt : parts) {
@@ -675,16 +710,16 @@ sc_status kmap_build_impl(sc_hash hi, sc_hash ho, int ndim, int K, int stride, c
 
 }  // namespace
 
-sc_status sc_kmap_build(sc_hash h, int ndim, int K, const int32_t dims[3], unsigned flags, sc_stream stream,
-                        sc_kmap* out) {
-  return kmap_build_impl(h, h, ndim, K, 1, dims, flags, stream, out);
+sc_status sc_kmap_build(sc_hash h, int ndim, int K, const int32_t dims[3], unsigned flags, const sc_allocator* alloc,
+                        sc_stream stream, sc_kmap* out) {
+  return kmap_build_impl(h, h, ndim, K, 1, dims, flags, alloc, stream, out);
 }
 
 sc_status sc_kmap_build_conv(sc_hash in, sc_hash out_set, int ndim, int K, int stride, const int32_t dims[3],
-                             unsigned flags, sc_stream stream, sc_kmap* out) {
+                             unsigned flags, const sc_allocator* alloc, sc_stream stream, sc_kmap* out) {
   if (flags & (SC_KMAP_SORT))
     return set_error(SC_ERR_UNSUPPORTED, "the signature sort applies to submanifold maps only");
-  return kmap_build_impl(in, out_set, ndim, K, stride, dims, flags | SC_KMAP_NO_SORT, stream, out);
+  return kmap_build_impl(in, out_set, ndim, K, stride, dims, flags | SC_KMAP_NO_SORT, alloc, stream, out);
 }
 
 sc_status sc_kmap_info(sc_kmap m, int64_t* n, int32_t* volume, int64_t* map_size, sc_stream stream) {
@@ -751,6 +786,52 @@ sc_status sc_kmap_export(sc_kmap m, int32_t* nbr, int64_t* offs, int32_t* in_row
     dev_free(tmp, s);
     if (st) return st;
   }
+  return SC_OK;
+}
+
+sc_status sc_kmap_view(sc_kmap m, const int32_t** d_nbr, const int64_t** d_offs, const int32_t** d_in,
+                       const int32_t** d_out, int64_t* map_size) {
+  if (!m) return set_error(SC_ERR_INVALID_ARG, "kmap handle is NULL");
+  KernelMap& k = m->k;
+  cudaStream_t s = m->stream;
+  if (!m->view_ready) {
+    // the latched status and the segment offsets on the host
+    sc_status st = k.host_valid ? sc_kmap_check(m, reinterpret_cast<sc_stream>(s)) : sync_host(&k, s);
+    if (st) return st;
+    const int64_t L = k.offs_host[k.V];
+    const size_t nb = k.order ? sizeof(int) * static_cast<size_t>(k.n) * k.V : 0;
+    const size_t nb_al = (nb + 255) & ~size_t(255);
+    const size_t lb = (sizeof(int) * static_cast<size_t>(L) + 255) & ~size_t(255);
+    if (nb + 2 * lb > 0) {
+      st = dev_alloc(&m->view_arena, nb_al + 2 * lb, s, m->has_alloc ? &m->alloc : nullptr);
+      if (st) return st;
+    }
+    uint8_t* base = static_cast<uint8_t*>(m->view_arena);
+    int* vn = k.order ? reinterpret_cast<int*>(base) : k.nbr;
+    int* vi = L ? reinterpret_cast<int*>(base + nb_al) : nullptr;
+    int* vo = L ? reinterpret_cast<int*>(base + nb_al + lb) : nullptr;
+    if (k.order && k.n) st = kmap_unpermute_nbr(&k, vn, s);
+    if (!st && L) st = kmap_compact_lists(&k, k.in_rows, vi, L, s);
+    if (!st && L) st = kmap_compact_lists(&k, k.out_rows, vo, L, s);
+    if (!st) {
+      cudaError_t e = cudaStreamSynchronize(s);
+      if (e != cudaSuccess) st = set_cuda_error(e, "kmap view");
+    }
+    if (st) {
+      dev_free(m->view_arena, s);
+      m->view_arena = nullptr;
+      return st;
+    }
+    m->view_nbr = vn;
+    m->view_in = vi;
+    m->view_out = vo;
+    m->view_ready = true;
+  }
+  if (d_nbr) *d_nbr = m->view_nbr;
+  if (d_offs) *d_offs = k.offs;
+  if (d_in) *d_in = m->view_in;
+  if (d_out) *d_out = m->view_out;
+  if (map_size) *map_size = k.map_size_host;
   return SC_OK;
 }
 

@@ -264,7 +264,8 @@ __global__ void __launch_bounds__(256) k_order_apply(int* __restrict__ buckets, 
 __global__ void __launch_bounds__(256) k_order_scatter(const unsigned long long* __restrict__ keys, int64_t n,
                                                        OrderBits ob, const int* __restrict__ hash_status,
                                                        int* __restrict__ cursors, int* __restrict__ order,
-                                                       unsigned long long* __restrict__ skeys) {
+                                                       unsigned long long* __restrict__ skeys,
+                                                       int* __restrict__ inv_order) {
   const int tb = order_total_bits(ob, hash_status);
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
@@ -272,6 +273,7 @@ __global__ void __launch_bounds__(256) k_order_scatter(const unsigned long long*
     const int pos = atomicAdd(cursors + order_bucket(key, ob, tb), 1);
     order[pos] = static_cast<int>(i);
     skeys[pos] = key;  // the map build then reads keys in order, coalesced
+    if (inv_order) inv_order[i] = pos;  // half probe: the table row of input row i
   }
 }
 
@@ -340,6 +342,7 @@ struct BuildArgs {
   // features are the offsets themselves, in rowmask)
   unsigned* rowdir;
   int* sig_sel;                    // [kSigBits] features of the row signature, rarest first (with rowmask)
+  const int* inv_order;            // half probe with the row order: table row of each input row; else null
 };
 
 // Coarse direction of offset v: (sign(dx) + 1) * 9 + (sign(dy) + 1) * 3 +
@@ -370,7 +373,17 @@ __device__ __forceinline__ int offset_direction(int v, int K, int ndim) {
 // UP: points per unit (128, or 32 when V > 128), a compile-time constant so
 // that the count and emit loops over the unit's 32-point groups unroll and
 // their shared-memory loads overlap.
-template <bool TR, int UP>
+// HALF: the half probe of a submanifold map (mirror symmetry: (p, q, d) is
+// in the map iff (q, p, -d) is).  A unit probes only the offsets after the
+// centre (lexicographically positive d) for its points and stores those
+// columns and the centre; each hit p of point q at d also gives q as p's
+// neighbour at -d, written straight into p's row of the table (whose
+// columns before the centre were set to -1 beforehand and are written by
+// nobody else), and one cursor reservation for d places both d's entry
+// (p, q) and -d's entry (q, p) at the same positions of their lists.  The
+// tile offset masks and row masks are then derived from the finished table
+// (k_kmap_masks).
+template <bool TR, int UP, bool HALF>
 __global__ void __launch_bounds__(kThreads, 5) k_kmap_build(const BuildArgs a) {
   extern __shared__ int4 smem4[];
   constexpr int up = UP;
@@ -480,6 +493,15 @@ __global__ void __launch_bounds__(kThreads, 5) k_kmap_build(const BuildArgs a) {
         bys[q] = ylo + static_cast<int>((tr >> 8) & 0xFF);
         bzs[q] = zlo + static_cast<int>(tr >> 16);
         act[q] = valid && t < ntrip && bxs[q] <= xhi && bys[q] <= yhi && bzs[q] <= zhi;
+        if (HALF && act[q]) {
+          // the block's lexicographically last voxel inside the neighbourhood
+          // (the higher of its two voxels on each axis when that one is in
+          // range) must lie after the centre, else the block is not probed
+          const int dx0 = 2 * bxs[q] - cx, dy0 = 2 * bys[q] - cy, dz0 = 2 * bzs[q] - cz;
+          const int dxm = dx0 + 1 <= r ? dx0 + 1 : dx0, dym = dy0 + 1 <= r ? dy0 + 1 : dy0,
+                    dzm = dz0 + 1 <= rz ? dz0 + 1 : dz0;
+          act[q] = dxm > 0 || (dxm == 0 && (dym > 0 || (dym == 0 && dzm > 0)));
+        }
         bk[q] = batch | pack_key(0, 2 * bxs[q], 2 * bys[q], 2 * bzs[q]);
         if (act[q]) {
           const BlockEntry* e = a.table + block_home(bk[q], a.mask);
@@ -506,20 +528,33 @@ __global__ void __launch_bounds__(kThreads, 5) k_kmap_build(const BuildArgs a) {
 #pragma unroll
         for (int l = 0; l < 8; ++l) {
           const int lx = l >> 2, ly = (l >> 1) & 1, lz = l & 1;
-          if ((ex >> lx) & (ey >> ly) & (ez >> lz) & 1u) s_tile[base + lx * sx + ly * sy + lz * sz2] = pick(r0[q], r1[q], l);
+          const int at = base + lx * sx + ly * sy + lz * sz2;
+          if ((ex >> lx) & (ey >> ly) & (ez >> lz) & 1u && (!HALF || at > p * V + centre))
+            s_tile[at] = pick(r0[q], r1[q], l);
         }
       }
     }
+    if (HALF && part == 0 && valid) s_tile[p * V + centre] = row;
   }
   __syncthreads();
 
   // ---- the unit's block of the table: contiguous, i0 * V * 4 bytes is a multiple of 128
-  {
+  if (HALF) {
+    // columns [centre, V) of each row; the columns before the centre are the
+    // mirrored hits, written by the units that found them
+    const int w = V - centre;
+    for (int e = threadIdx.x; e < np * w; e += kThreads) {
+      const int rr = e / w, c = centre + e - rr * w;
+      __stcs(a.nbr + (i0 + rr) * V + c, s_tile[rr * V + c]);
+    }
+  } else {
     int* dst = a.nbr + i0 * V;
     const int items = np * V;
     const int n4 = items >> 2;
-    for (int e = threadIdx.x; e < n4; e += kThreads) reinterpret_cast<int4*>(dst)[e] = reinterpret_cast<const int4*>(s_tile)[e];
-    for (int e = (n4 << 2) + threadIdx.x; e < items; e += kThreads) dst[e] = s_tile[e];
+    // streaming stores (evict-first in L2): the table and lists are written
+    // once here, and should not push the hash table out of L2
+    for (int e = threadIdx.x; e < n4; e += kThreads) __stcs(reinterpret_cast<int4*>(dst) + e, reinterpret_cast<const int4*>(s_tile)[e]);
+    for (int e = (n4 << 2) + threadIdx.x; e < items; e += kThreads) __stcs(dst + e, s_tile[e]);
   }
 
   // ---- count and emit, warp by warp: warp w takes offsets w, w + 8, ...
@@ -549,7 +584,7 @@ __global__ void __launch_bounds__(kThreads, 5) k_kmap_build(const BuildArgs a) {
       if (lane < nk && cnt_mine > 0) {
         const int v = vb + kWarps * lane;
         base_mine = atomicAdd(a.cursors + v * kCursorStride, cnt_mine);
-        if (v < 128 && up >= 64) atomicOr(s_pres + (v >> 5), 1u << (v & 31));
+        if (!HALF && v < 128 && up >= 64) atomicOr(s_pres + (v >> 5), 1u << (v & 31));
       }
       __syncwarp();
       for (int k = 0; k < nk; ++k) {
@@ -564,10 +599,21 @@ __global__ void __launch_bounds__(kThreads, 5) k_kmap_build(const BuildArgs a) {
           const unsigned b = bs[g];
           if ((b >> lane) & 1u) {
             const int64_t at = lb + at0 + __popc(b & lt);
-            a.in_rows[at] = s_tile[(g * 32 + lane) * V + v];
-            a.out_rows[at] = s_row[g * 32 + lane];
+            const int jn = s_tile[(g * 32 + lane) * V + v], iq = s_row[g * 32 + lane];
+            __stcs(a.in_rows + at, jn);
+            __stcs(a.out_rows + at, iq);
+            if (HALF) {
+              // the mirrored tuple (iq, jn, -d): -d's list at the same position,
+              // and iq in jn's row of the table at -d
+              const int64_t atm = at + static_cast<int64_t>(V - 1 - 2 * v) * a.n;
+              __stcs(a.in_rows + atm, iq);
+              __stcs(a.out_rows + atm, jn);
+              const int64_t pj = a.inv_order ? __ldg(a.inv_order + jn) : jn;
+              a.nbr[pj * V + (V - 1 - v)] = iq;
+            } else {
             if (v < 32) rm[g] |= 1u << v;
-            if (a.rowdir) {  // V > 32: the row's offset and direction bits
+            }
+            if (!HALF && a.rowdir) {  // V > 32: the row's offset and direction bits
               atomicOr(s_rmask4 + (g * 32 + lane) * 4 + (v >> 5), 1u << (v & 31));
               atomicOr(s_rmask + g * 32 + lane, 1u << s_dir[v]);
             }
@@ -576,19 +622,20 @@ __global__ void __launch_bounds__(kThreads, 5) k_kmap_build(const BuildArgs a) {
         }
       }
     }
-    if (a.rowmask && !a.rowdir) {  // V <= 32: one word per row
+    if (!HALF && a.rowmask && !a.rowdir) {  // V <= 32: one word per row
 #pragma unroll
       for (int g = 0; g < ngroups; ++g)
         if (rm[g]) atomicOr(s_rmask + g * 32 + lane, rm[g]);
     }
   }
   __syncthreads();
-  // present offsets of the unit's 128-row tile (two 64-point units share one: OR, on a zeroed mask)
-  if (up == 128 && threadIdx.x < 4) a.present[static_cast<int64_t>(u) * 4 + threadIdx.x] = s_pres[threadIdx.x];
-  if (up == 64 && threadIdx.x < 4 && s_pres[threadIdx.x])
+  // present offsets of the unit's 128-row tile (two 64-point units share one:
+  // OR, on a zeroed mask); the half probe derives them from the table later
+  if (!HALF && up == 128 && threadIdx.x < 4) a.present[static_cast<int64_t>(u) * 4 + threadIdx.x] = s_pres[threadIdx.x];
+  if (!HALF && up == 64 && threadIdx.x < 4 && s_pres[threadIdx.x])
     atomicOr(a.present + static_cast<int64_t>(u >> 1) * 4 + threadIdx.x, s_pres[threadIdx.x]);
-  if (a.rowmask && !a.rowdir && threadIdx.x < np) a.rowmask[i0 + threadIdx.x] = s_rmask[threadIdx.x];
-  if (a.rowdir && threadIdx.x < np) {  // V > 32: 128-bit offset mask and direction bits per row
+  if (!HALF && a.rowmask && !a.rowdir && threadIdx.x < np) a.rowmask[i0 + threadIdx.x] = s_rmask[threadIdx.x];
+  if (!HALF && a.rowdir && threadIdx.x < np) {  // V > 32: 128-bit offset mask and direction bits per row
     reinterpret_cast<uint4*>(a.rowmask)[i0 + threadIdx.x] = reinterpret_cast<const uint4*>(s_rmask4)[threadIdx.x];
     a.rowdir[i0 + threadIdx.x] = s_rmask[threadIdx.x];
   }
@@ -604,7 +651,9 @@ __global__ void __launch_bounds__(kThreads, 5) k_kmap_build(const BuildArgs a) {
   long long carry = 0, carry_t = 0;
   for (int v0 = 0; v0 < V; v0 += kThreads) {
     const int v = v0 + threadIdx.x;
-    const long long cnt = v < V ? static_cast<long long>(__ldcg(a.cursors + v * kCursorStride)) : 0;
+    // the half probe counts each pair of offsets d, -d on d's cursor
+    const int vc = HALF && v < centre ? V - 1 - v : v;
+    const long long cnt = v < V ? static_cast<long long>(__ldcg(a.cursors + vc * kCursorStride)) : 0;
     long long tot, tot_t;
     const long long inc = block_inclusive_scan<long long>(cnt, warp_sums, &tot);
     const long long tl = (cnt + kWsRows - 1) / kWsRows;
@@ -630,7 +679,8 @@ __global__ void __launch_bounds__(kThreads, 5) k_kmap_build(const BuildArgs a) {
     for (int v = threadIdx.x; v < V; v += kThreads)
       if (v != centre)
         atomicAdd(reinterpret_cast<unsigned long long*>(s_dc + offset_direction(v, a.K, a.ndim)),
-                  static_cast<unsigned long long>(__ldcg(a.cursors + v * kCursorStride)));
+                  static_cast<unsigned long long>(
+                      __ldcg(a.cursors + (HALF && v < centre ? V - 1 - v : v) * kCursorStride)));
     __syncthreads();
   }
   if (a.rowmask && warp == 0) {
@@ -639,8 +689,9 @@ __global__ void __launch_bounds__(kThreads, 5) k_kmap_build(const BuildArgs a) {
     // (count, f); kSigBits rounds of a warp minimum
     const long long none = 0x7FFFFFFFFFFFFFFFll;
     const int nf = a.rowdir ? 27 : V, cf = a.rowdir ? 13 : centre;
+    const int lc = HALF && lane < centre ? V - 1 - lane : lane;
     const long long c = lane < nf && lane != cf ? (a.rowdir ? warp_sums[lane]
-                                                           : static_cast<long long>(__ldcg(a.cursors + lane * kCursorStride)))
+                                                           : static_cast<long long>(__ldcg(a.cursors + lc * kCursorStride)))
                                                 : 0;
     long long key = c > 0 ? (c << 8) | lane : none;
     for (int k = 0; k < kSigBits; ++k) {
@@ -653,6 +704,83 @@ __global__ void __launch_bounds__(kThreads, 5) k_kmap_build(const BuildArgs a) {
       if (lane == 0) a.sig_sel[k] = mn == none ? -1 : static_cast<int>(mn & 255);  // -1: no further offset occurs
       if (key == mn) key = none;
     }
+  }
+}
+
+// The half probe's starting table: -1 in the columns before the centre of
+// every row (warp per row, a row's columns written together).
+__global__ void __launch_bounds__(256) k_clear_lower_half(int* __restrict__ nbr, int64_t n, int V) {
+  const int lane = threadIdx.x & 31, half = (V - 1) / 2;
+  const int64_t wstride = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t row = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; row < n; row += wstride)
+    for (int c = lane; c < half; c += 32) __stcs(nbr + row * V + c, -1);
+}
+
+// Tile offset masks (present) and, with the signature sort, row masks of a
+// map, derived from its finished neighbour table: after the half probe a
+// row's columns before the centre arrive from other units, so its masks are
+// known only once the whole table is written.  One warp per 32 rows (a
+// coalesced load and a ballot per 32 offsets of a row); W mask words per row
+// (1 when V <= 32, else 4).
+template <int W>
+__global__ void __launch_bounds__(128) k_kmap_masks(const int* __restrict__ nbr, int64_t n, int V, int K, int ndim,
+                                                    unsigned* __restrict__ present, unsigned* __restrict__ rowmask,
+                                                    unsigned* __restrict__ rowdir) {
+  __shared__ unsigned s_p[4][4];
+  __shared__ unsigned char s_dir[128];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int centre = (V - 1) / 2;
+  if (rowdir && threadIdx.x < V) s_dir[threadIdx.x] = static_cast<unsigned char>(offset_direction(threadIdx.x, K, ndim));
+  __syncthreads();
+  const int64_t ntiles = (n + 127) / 128;
+  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+    unsigned m[W];
+#pragma unroll
+    for (int k = 0; k < W; ++k) m[k] = 0u;  // offsets of row t * 128 + warp * 32 + lane
+    const int64_t r0 = t * 128 + warp * 32;
+    // eight rows' loads in flight at a time
+    for (int rb = 0; rb < 32; rb += 8) {
+      int x[8][W];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int64_t row = r0 + rb + i;
+#pragma unroll
+        for (int k = 0; k < W; ++k) {
+          const int v = 32 * k + lane;
+          x[i][k] = row < n && v < V ? __ldcs(nbr + row * V + v) : -1;
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+#pragma unroll
+        for (int k = 0; k < W; ++k) {
+          const unsigned b = __ballot_sync(0xffffffffu, x[i][k] >= 0 && 32 * k + lane != centre);
+          if (lane == rb + i) m[k] = b;
+        }
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < W; ++k) {
+      const unsigned o = __reduce_or_sync(0xffffffffu, m[k]);
+      if (lane == 0) s_p[warp][k] = o;
+    }
+    const int64_t row = r0 + lane;
+    if (rowmask && row < n) {
+      if (W == 1) rowmask[row] = m[0];
+      else reinterpret_cast<uint4*>(rowmask)[row] = make_uint4(m[0], m[W > 1 ? 1 : 0], m[W > 2 ? 2 : 0], m[W > 3 ? 3 : 0]);
+    }
+    if (rowdir && row < n) {
+      unsigned dir = 0u;
+#pragma unroll
+      for (int k = 0; k < W; ++k)
+        for (unsigned x = m[k]; x; x &= x - 1u) dir |= 1u << s_dir[32 * k + __ffs(x) - 1];
+      rowdir[row] = dir;
+    }
+    __syncthreads();
+    if (threadIdx.x < 4)
+      present[t * 4 + threadIdx.x] =
+          threadIdx.x < W ? (s_p[0][threadIdx.x] | s_p[1][threadIdx.x] | s_p[2][threadIdx.x] | s_p[3][threadIdx.x]) : 0u;
+    __syncthreads();
   }
 }
 
@@ -1004,7 +1132,8 @@ sc_status launch_kmap_build(const HashTable* in, const HashTable* h, KernelMap* 
     SC_LAUNCH("order_partials", s, k_order_partials<<<kBucketBlocks, 256, 0, s>>>(m->buckets, partial));
     SC_LAUNCH("order_apply", s, k_order_apply<<<kBucketBlocks, 256, 0, s>>>(m->buckets, partial));
     SC_LAUNCH("order_scatter", s,
-              k_order_scatter<<<og, 256, 0, s>>>(h->keys, m->n, ob, h->status, m->buckets, m->order, m->skeys));
+              k_order_scatter<<<og, 256, 0, s>>>(h->keys, m->n, ob, h->status, m->buckets, m->order, m->skeys,
+                                                 m->inv_order));
     e = cudaGetLastError();
     if (e != cudaSuccess) return set_cuda_error(e, "locality order launch");
   }
@@ -1051,6 +1180,7 @@ sc_status launch_kmap_build(const HashTable* in, const HashTable* h, KernelMap* 
   a.rowmask = m->rowmask;
   a.rowdir = m->rowdir;
   a.sig_sel = m->sig_sel;
+  a.inv_order = m->inv_order;
   const size_t smem = sizeof(int) * (static_cast<size_t>(m->up) * V + static_cast<size_t>(V) * (m->up / 32)) +
                       (m->rowdir ? 16 + sizeof(unsigned) * 128 * 4 : 0);
   if (smem > 48 * 1024) {  // set once per device: the largest the build ever asks for
@@ -1058,34 +1188,63 @@ sc_status launch_kmap_build(const HashTable* in, const HashTable* h, KernelMap* 
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64 || !done[dev]) {
-      const void* kerns[6] = {reinterpret_cast<const void*>(k_kmap_build<false, 128>),
-                              reinterpret_cast<const void*>(k_kmap_build<true, 128>),
-                              reinterpret_cast<const void*>(k_kmap_build<false, 64>),
-                              reinterpret_cast<const void*>(k_kmap_build<true, 64>),
-                              reinterpret_cast<const void*>(k_kmap_build<false, 32>),
-                              reinterpret_cast<const void*>(k_kmap_build<true, 32>)};
+      const void* kerns[9] = {reinterpret_cast<const void*>(k_kmap_build<false, 128, false>),
+                              reinterpret_cast<const void*>(k_kmap_build<true, 128, false>),
+                              reinterpret_cast<const void*>(k_kmap_build<false, 64, false>),
+                              reinterpret_cast<const void*>(k_kmap_build<true, 64, false>),
+                              reinterpret_cast<const void*>(k_kmap_build<false, 32, false>),
+                              reinterpret_cast<const void*>(k_kmap_build<true, 32, false>),
+                              reinterpret_cast<const void*>(k_kmap_build<false, 128, true>),
+                              reinterpret_cast<const void*>(k_kmap_build<false, 64, true>),
+                              reinterpret_cast<const void*>(k_kmap_build<false, 32, true>)};
       e = cudaSuccess;
-      for (int k = 0; k < 6 && e == cudaSuccess; ++k)
+      for (int k = 0; k < 9 && e == cudaSuccess; ++k)
         e = cudaFuncSetAttribute(kerns[k], cudaFuncAttributeMaxDynamicSharedMemorySize, kBuildSmemMax);
       if (e != cudaSuccess) return set_cuda_error(e, "kmap_build smem attribute");
       if (dev >= 0 && dev < 64) done[dev] = true;
     }
   }
-  if (m->up == 128) {
-    if (m->transposed)
-      SC_LAUNCH("kmap_build", s, (k_kmap_build<true, 128><<<m->nunits, kThreads, smem, s>>>(a)));
+  const int V2 = (V - 1) / 2;
+  if (m->half) {
+    // the half probe: every column before the centre starts at -1 (absent)
+    // and receives only the mirrored hits
+    if (V2 > 0)
+      SC_LAUNCH("kmap_clear", s, (k_clear_lower_half<<<grid_for(m->n * 32, 256), 256, 0, s>>>(m->nbr, m->n, V)));
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return set_cuda_error(e, "half-probe table clear");
+    if (m->up == 128)
+      SC_LAUNCH("kmap_build", s, (k_kmap_build<false, 128, true><<<m->nunits, kThreads, smem, s>>>(a)));
+    else if (m->up == 64)
+      SC_LAUNCH("kmap_build", s, (k_kmap_build<false, 64, true><<<m->nunits, kThreads, smem, s>>>(a)));
     else
-      SC_LAUNCH("kmap_build", s, (k_kmap_build<false, 128><<<m->nunits, kThreads, smem, s>>>(a)));
+      SC_LAUNCH("kmap_build", s, (k_kmap_build<false, 32, true><<<m->nunits, kThreads, smem, s>>>(a)));
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return set_cuda_error(e, "kmap_build launch");
+    if (V <= 128) {  // tile masks for the fused kernel, row masks for the signature sort
+      const int64_t ntiles = (m->n + 127) / 128;
+      int g = static_cast<int>(ntiles < static_cast<int64_t>(device_sm_count()) * 16 ? ntiles : device_sm_count() * 16);
+      if (V <= 32)
+        SC_LAUNCH("kmap_masks", s, (k_kmap_masks<1><<<g, 128, 0, s>>>(m->nbr, m->n, V, m->K, m->ndim, m->present,
+                                                                      m->rowmask, m->rowdir)));
+      else
+        SC_LAUNCH("kmap_masks", s, (k_kmap_masks<4><<<g, 128, 0, s>>>(m->nbr, m->n, V, m->K, m->ndim, m->present,
+                                                                      m->rowmask, m->rowdir)));
+    }
+  } else if (m->up == 128) {
+    if (m->transposed)
+      SC_LAUNCH("kmap_build", s, (k_kmap_build<true, 128, false><<<m->nunits, kThreads, smem, s>>>(a)));
+    else
+      SC_LAUNCH("kmap_build", s, (k_kmap_build<false, 128, false><<<m->nunits, kThreads, smem, s>>>(a)));
   } else if (m->up == 64) {
     if (m->transposed)
-      SC_LAUNCH("kmap_build", s, (k_kmap_build<true, 64><<<m->nunits, kThreads, smem, s>>>(a)));
+      SC_LAUNCH("kmap_build", s, (k_kmap_build<true, 64, false><<<m->nunits, kThreads, smem, s>>>(a)));
     else
-      SC_LAUNCH("kmap_build", s, (k_kmap_build<false, 64><<<m->nunits, kThreads, smem, s>>>(a)));
+      SC_LAUNCH("kmap_build", s, (k_kmap_build<false, 64, false><<<m->nunits, kThreads, smem, s>>>(a)));
   } else {
     if (m->transposed)
-      SC_LAUNCH("kmap_build", s, (k_kmap_build<true, 32><<<m->nunits, kThreads, smem, s>>>(a)));
+      SC_LAUNCH("kmap_build", s, (k_kmap_build<true, 32, false><<<m->nunits, kThreads, smem, s>>>(a)));
     else
-      SC_LAUNCH("kmap_build", s, (k_kmap_build<false, 32><<<m->nunits, kThreads, smem, s>>>(a)));
+      SC_LAUNCH("kmap_build", s, (k_kmap_build<false, 32, false><<<m->nunits, kThreads, smem, s>>>(a)));
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return set_cuda_error(e, "kmap_build launch");
@@ -1123,7 +1282,7 @@ sc_status launch_hash_coords(const HashTable* h, int32_t* coords, cudaStream_t s
 }
 
 sc_status launch_conv_out(const HashTable* in, int ndim, int K, int stride, const int32_t dims[3], HashTable* out,
-                          void** arena_table, void** arena_keys, cudaStream_t s) {
+                          void** arena_table, void** arena_keys, const sc_allocator* alloc, cudaStream_t s) {
   OutGrid g;
   g.stride = stride;
   g.r = (K - 1) / 2;
@@ -1148,7 +1307,7 @@ sc_status launch_conv_out(const HashTable* in, int ndim, int K, int stride, cons
     const int nchunks = static_cast<int>((cap + kOutChunk - 1) / kOutChunk);
     const size_t tb = sizeof(BlockEntry) * static_cast<size_t>(cap);
     const size_t pb = (sizeof(int) * static_cast<size_t>(nchunks) + 255) & ~size_t(255);
-    sc_status st = dev_alloc(arena_table, tb + pb + 256, s);
+    sc_status st = dev_alloc(arena_table, tb + pb + 256, s, alloc);
     if (st) return st;
     uint8_t* b = static_cast<uint8_t*>(*arena_table);
     BlockEntry* table = reinterpret_cast<BlockEntry*>(b);
@@ -1178,7 +1337,7 @@ sc_status launch_conv_out(const HashTable* in, int ndim, int K, int stride, cons
       continue;
     }
     if (n_out >= (int64_t(1) << 31)) return set_error(SC_ERR_UNSUPPORTED, "output set: more than 2^31 - 1 points");
-    st = dev_alloc(arena_keys, sizeof(unsigned long long) * static_cast<size_t>(n_out > 0 ? n_out : 1), s);
+    st = dev_alloc(arena_keys, sizeof(unsigned long long) * static_cast<size_t>(n_out > 0 ? n_out : 1), s, alloc);
     if (st) return st;
     out->n = n_out;
     out->capacity = cap;

@@ -84,7 +84,9 @@ struct KernelMap {
   int dims[3] = {1, 1, 1};
   int up = 128;                      // points per map-build unit (128; 64 when V > 64; 32 when V > 128)
   int nunits = 0;                    // map-build units
+  bool half = false;                 // built by the half probe (mirror symmetry)
   int* order = nullptr;              // [n] input rows in locality order, or null: input order
+  int* inv_order = nullptr;          // half probe with the order: [n] table row of each input row
   unsigned long long* skeys = nullptr;  // [n] packed keys in locality order (with order)
   int* buckets = nullptr;            // counting-sort buckets of that order (+ scan partials)
   int* nbr = nullptr;                // [n, V], rows in the row order (position k = input row order[k])
@@ -150,7 +152,7 @@ sc_status launch_kmap_build(const HashTable* in, const HashTable* out, KernelMap
 // Output set of a regular / strided layer as a new hash table `out` (its table
 // in *arena_table, its keys in *arena_keys); synchronises once to size it.
 sc_status launch_conv_out(const HashTable* in, int ndim, int K, int stride, const int32_t dims[3], HashTable* out,
-                          void** arena_table, void** arena_keys, cudaStream_t s);
+                          void** arena_table, void** arena_keys, const sc_allocator* alloc, cudaStream_t s);
 sc_status launch_hash_coords(const HashTable* h, int32_t* coords, cudaStream_t s);
 int kmap_unit_points(int V);
 sc_status kmap_compact_lists(const KernelMap* m, const int* src, int* dst, int64_t total, cudaStream_t s);
@@ -182,8 +184,10 @@ sc_status kmap_unpermute_nbr(const KernelMap* m, int* dst, cudaStream_t s);
 bool fused_supported(const ConvArgs& a);
 sc_status conv_fused_noalloc(const ConvArgs& a);
 
-// stream-ordered allocation helpers
-sc_status dev_alloc(void** p, size_t bytes, cudaStream_t s);
+// stream-ordered allocation helpers: `with` (if not null) is the caller's
+// allocator of a build call, else the process-wide setting is used; a buffer
+// goes back to whichever allocator made it
+sc_status dev_alloc(void** p, size_t bytes, cudaStream_t s, const sc_allocator* with = nullptr);
 void dev_free(void* p, cudaStream_t s);
 
 }  // namespace sc

@@ -46,9 +46,14 @@ def test_host_only_calls(libsc):
     assert libsc.sc_launch_count() >= 0
     # argument errors return synchronously, before any CUDA call
     out = ctypes.c_void_p()
-    assert libsc.sc_hash_build(None, -1, None, ctypes.byref(out)) == 1
-    assert libsc.sc_hash_build(None, 5, None, None) == 1
-    assert libsc.sc_kmap_build(None, 3, 3, None, 0, None, ctypes.byref(out)) == 1
+    assert libsc.sc_hash_build(None, -1, None, None, ctypes.byref(out)) == 1
+    assert libsc.sc_hash_build(None, 5, None, None, None) == 1
+    assert libsc.sc_kmap_build(None, 3, 3, None, 0, None, None, ctypes.byref(out)) == 1
+    assert libsc.sc_kmap_view(None, None, None, None, None, None) == 1
+    # an allocator with only one of its two callbacks is refused
+    from submanifold_sparse_convolution_hash_gb300 import binding
+    half_alloc = binding.Allocator(1, None, None)
+    assert libsc.sc_hash_build(None, 0, ctypes.byref(half_alloc), None, ctypes.byref(out)) == 1
     assert libsc.sc_subm_conv_fwd(None, None, None, None, 32, 32, 1, 0, None) == 1
     assert b"NULL" in libsc.sc_last_error()
 
@@ -79,7 +84,8 @@ int main(void) {
   sc_hash h = NULL;
   if (strcmp(sc_status_str(SC_OK), "ok") != 0) return 2;
   /* argument errors come back synchronously, without touching a device */
-  if (sc_hash_build(NULL, -1, NULL, &h) != SC_ERR_INVALID_ARG) return 3;
+  sc_allocator a = {NULL, NULL, NULL};
+  if (sc_hash_build(NULL, -1, &a, NULL, &h) != SC_ERR_INVALID_ARG) return 3;
   if (h != NULL) return 4;
   if (sc_last_error() == NULL || strlen(sc_last_error()) == 0) return 5;
   printf("%s\n", sc_last_error());

@@ -62,3 +62,32 @@ def test_allocator_arguments():
         sc._check(sc.lib().sc_set_allocator(sc.ctypes.c_void_p(1), None, None), "sc_set_allocator")
     assert e.value.code == 1
     sc.use_torch_allocator(False)
+
+
+def test_allocator_argument_of_a_build_call():
+    """A build call given an sc_allocator takes the handle's memory from it
+    (here PyTorch's caching allocator), whatever the process-wide setting;
+    the map's later buffers (sc_kmap_view) come from it too."""
+    s = scenes.lidar_scan(64, 3000, (160, 160, 41))
+    coords = torch.from_numpy(s.coords).cuda()
+    sc.use_torch_allocator(False)  # process-wide: the stream-ordered pool
+    alloc = sc.torch_allocator()
+    before = _allocs()
+    h = sc.sc_hash_build(coords, allocator=alloc)
+    m = sc.sc_kmap_build(h, 3, 3, s.dims, order=True, allocator=alloc)
+    after_build = _allocs()
+    assert after_build - before >= 2  # the hash arena and the map arena
+    v = m.view()  # materialises the exported forms from the same allocator
+    assert _allocs() - after_build >= 1
+    assert np.array_equal(v["nbr"].cpu().numpy(), oracle.kmap(s.coords, 3, 3, s.dims))
+    # a build without the argument leaves torch's pool alone
+    mid = _allocs()
+    h2 = sc.sc_hash_build(coords)
+    m2 = sc.sc_kmap_build(h2, 3, 3, s.dims)
+    assert _allocs() == mid
+    del v
+    m.destroy()
+    h.destroy()
+    m2.destroy()
+    h2.destroy()
+    torch.cuda.synchronize()

@@ -69,17 +69,34 @@ def test_full_size_kmap_matches_oracle(idx):
     s = F.s
     ref = oracle.kmap(s.coords, s.ndim, F.w.K, s.dims)
     nbr = F.m.nbr().cpu().numpy()
+    check_full_map(F, s, ref, nbr, F.m)
+
+
+@pytest.mark.parametrize("idx", [2, 4])
+def test_full_size_half_probe_map_matches_oracle(idx):
+    """The half-probe build (mirror symmetry) at full size, in the bench's
+    asynchronous launch configuration: the same map as the oracle's."""
+    F = full(idx)
+    s = F.s
+    m = sc.sc_kmap_build(F.h, s.ndim, F.w.K, s.dims, sync=False, half=True)
+    m.check()
+    ref = oracle.kmap(s.coords, s.ndim, F.w.K, s.dims)
+    check_full_map(F, s, ref, m.nbr().cpu().numpy(), m)
+    m.destroy()
+
+
+def check_full_map(F, s, ref, nbr, m):
     assert nbr.shape == ref.shape
-    assert np.array_equal(nbr, ref), f"workload {idx}: {int((nbr != ref).sum())} neighbour entries differ"
+    assert np.array_equal(nbr, ref), f"{F.w.name}: {int((nbr != ref).sum())} neighbour entries differ"
     centre = (F.V - 1) // 2
     assert np.array_equal(ref[:, centre], np.arange(s.n, dtype=np.int32))
     # per-offset lists: same counts, every pair a real neighbour pair, no
     # output row twice in a segment -- together the same set as the oracle's
-    offs, ins, outs = (t.cpu().numpy() for t in F.m.lists())
+    offs, ins, outs = (t.cpu().numpy() for t in m.lists())
     counts = (ref >= 0).sum(axis=0)
     counts[centre] = 0
     assert np.array_equal(np.diff(offs), counts)
-    assert F.m.map_size() == int(counts.sum()) + s.n
+    assert m.map_size() == int(counts.sum()) + s.n
     for v in range(F.V):
         i = ins[offs[v]:offs[v + 1]].astype(np.int64)
         o = outs[offs[v]:offs[v + 1]].astype(np.int64)

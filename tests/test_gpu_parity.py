@@ -5,6 +5,8 @@ Sizes here finish in the oracle within seconds and still span several
 within max|gpu - ref| <= 5e-3 * max(1, max|ref|) (f16/bf16 inputs, fp32
 accumulation) or 1e-5 * max(1, max|ref|) (fp32).
 """
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -30,10 +32,10 @@ def small_scenes():
 SCENES = small_scenes()
 
 
-def build(scene, K, sync=True, order=None, sort=None):
+def build(scene, K, sync=True, order=None, sort=None, half=False):
     c = torch.from_numpy(scene.coords).cuda()
     h = sc.sc_hash_build(c)
-    m = sc.sc_kmap_build(h, scene.ndim, K, scene.dims, sync=sync, order=order, sort=sort)
+    m = sc.sc_kmap_build(h, scene.ndim, K, scene.dims, sync=sync, order=order, sort=sort, half=half)
     return c, h, m
 
 
@@ -65,9 +67,12 @@ def test_hash_query_finds_every_row_and_misses_absent_keys():
                                     ("indoor", 3), ("indoor", 5), ("batch", 3), ("lidar", 1), ("indoor", 7)])
 @pytest.mark.parametrize("sync,order,sort", [(True, False, False), (False, False, False), (True, True, False),
                                              (False, True, False), (True, False, True), (False, True, True)])
-def test_kmap_bit_exact(name, K, sync, order, sort):
+@pytest.mark.parametrize("half", [False, True])
+def test_kmap_bit_exact(name, K, sync, order, sort, half):
+    """half: the half-probe build (mirror symmetry, "Sparse inputs and sparse
+    convolution", section "A symmetry you can check") must give the same map."""
     s = SCENES[name]
-    c, h, m = build(s, K, sync, order, sort)
+    c, h, m = build(s, K, sync, order, sort, half)
     if not sync:
         m.check()
     ref = oracle.kmap(s.coords, s.ndim, K, s.dims)
@@ -180,6 +185,42 @@ def test_conv_matches_oracle(name, K, c_in, c_out, dtype, relu, variant, order, 
     ref = oracle.subm_conv(s.coords, f64, w64, s.ndim, K, s.dims, relu=relu)
     assert_close(out, ref, dtype, f"{name} K={K} {c_in}->{c_out} {dtype} {variant}")
     m.check()
+
+
+HALF_CASES = [
+    ("lidar", 3, 32, 32, "f16", False),
+    ("indoor", 3, 64, 64, "bf16", True),
+    ("batch", 3, 64, 128, "f16", False),
+    ("indoor", 5, 128, 128, "bf16", False),
+    ("uniform2d_dense", 5, 16, 48, "bf16", True),
+    ("uniform2d_dense", 9, 16, 32, "f16", False),
+]
+
+
+@pytest.mark.parametrize("order,sort", [(False, False), (True, True)])
+@pytest.mark.parametrize("name,K,c_in,c_out,dtype,relu", HALF_CASES)
+def test_conv_on_half_probe_map(name, K, c_in, c_out, dtype, relu, order, sort):
+    """The layer on a map built by the half probe (its tile and row masks are
+    derived from the finished table)."""
+    s = SCENES[name]
+    c, h, m = build(s, K, order=order, sort=sort, half=True)
+    f, w, f64, w64 = layer_inputs(s, K, c_in, c_out, dtype, seed=9 + c_in + K)
+    for variant in ("fused", "ws"):
+        out = sc.sc_subm_conv_fwd(m, f, w, relu=relu, variant=variant)
+        torch.cuda.synchronize()
+        ref = oracle.subm_conv(s.coords, f64, w64, s.ndim, K, s.dims, relu=relu)
+        assert_close(out, ref, dtype, f"half probe {name} K={K} {variant}")
+    m.check()
+
+
+def test_half_probe_is_submanifold_only():
+    s = SCENES["lidar"]
+    h = sc.sc_hash_build(torch.from_numpy(s.coords).cuda())
+    ho = sc.sc_hash_build_conv_out(h, 3, 3, 2, s.dims)
+    d = (ctypes.c_int32 * 3)(*s.dims)
+    m = ctypes.c_void_p()
+    st = sc.lib().sc_kmap_build_conv(h._h, ho._h, 3, 3, 2, d, sc.SC_KMAP_HALF, None, None, ctypes.byref(m))
+    assert st == 5  # SC_ERR_UNSUPPORTED
 
 
 def test_every_row_written_once_no_stale_values():
@@ -394,3 +435,38 @@ def test_full_table_is_reported(monkeypatch):
     assert h2.capacity >= 2 * len(pts)
     m2 = sc.sc_kmap_build(h2, 3, 3, (400, 400, 400))
     assert np.array_equal(m2.nbr().cpu().numpy(), oracle.kmap(coords.cpu().numpy(), 3, 3, (400, 400, 400)))
+
+
+@pytest.mark.parametrize("name,K,order,half", [("lidar", 3, False, False), ("lidar", 3, True, False),
+                                               ("indoor", 5, True, False), ("indoor", 3, True, True),
+                                               ("uniform2d_dense", 5, False, True)])
+def test_kmap_view_matches_oracle(name, K, order, half):
+    """sc_kmap_view (borrowed device pointers, the rulebook grouped by
+    offset): the neighbour table in input row order, equal to the oracle's,
+    and the CSR lists, equal to the oracle's per-offset lists as pair sets;
+    a second call returns the same pointers."""
+    s = SCENES[name]
+    c, h, m = build(s, K, sync=False, order=order, half=half)
+    L = sc.lib()
+    ptrs = [ctypes.c_void_p() for _ in range(4)]
+    ms = ctypes.c_int64()
+    assert L.sc_kmap_view(m._h, *(ctypes.byref(p) for p in ptrs), ctypes.byref(ms)) == 0, L.sc_last_error()
+    again = [ctypes.c_void_p() for _ in range(4)]
+    assert L.sc_kmap_view(m._h, *(ctypes.byref(p) for p in again), None) == 0
+    assert [p.value for p in ptrs] == [p.value for p in again]
+    v = m.view()
+    ref = oracle.kmap(s.coords, s.ndim, K, s.dims)
+    assert v["nbr"].data_ptr() == ptrs[0].value
+    np.testing.assert_array_equal(v["nbr"].cpu().numpy(), ref)
+    assert ms.value == v["map_size"] == len(oracle.tuples(ref))
+    offs = v["offs"].cpu().numpy()
+    gi, go = v["in"].cpu().numpy(), v["out"].cpu().numpy()
+    centre = (K ** s.ndim - 1) // 2
+    for off, ((ri, ro)) in enumerate(oracle.offset_lists(ref)):
+        a, b = offs[off], offs[off + 1]
+        if off == centre:
+            assert a == b  # the identity is implied
+            continue
+        k = np.lexsort((gi[a:b], go[a:b]))
+        np.testing.assert_array_equal(go[a:b][k], ro)
+        np.testing.assert_array_equal(gi[a:b][k], ri)
