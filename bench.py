@@ -75,7 +75,7 @@ def parse_args():
     ap.add_argument("--backward", action="store_true",
                     help="a training step: after the forward layers, the input and weight gradients of every "
                          "layer (a seeded output gradient, ReLU masks applied)")
-    ap.add_argument("--variant", choices=["fused", "ws", "simt"], default=None,
+    ap.add_argument("--variant", choices=["fused", "ws", "simt", "split"], default=None,
                     help="run every layer with this variant instead of the measured choice")
     ap.add_argument("--layer-type", choices=["submanifold", "regular", "strided"], default="submanifold",
                     help="regular: a dilating layer (stride 1, output set grown by the kernel window); strided: "
@@ -83,6 +83,9 @@ def parse_args():
     ap.add_argument("--stride", type=int, default=2, help="stride of --layer-type strided")
     ap.add_argument("--kmap-half", action="store_true",
                     help="build submanifold maps with the half probe (mirror symmetry) instead of the full probe")
+    ap.add_argument("--kmap-split", action="store_true",
+                    help="also build the row orders of column splitting (K^ndim <= 32), so each layer's measured "
+                         "variant choice includes the split kernel")
     return ap.parse_args()
 
 
@@ -130,6 +133,7 @@ def algo_bytes_step(kernel: str, N: int, V: int, M: int, layers, s: int, ntiles:
         "pack_weights": sum(2 * V * ci * co * s for ci, co in conv_layers),
         # gathered neighbour rows + one write per output row + neighbour table + weights
         "subm_conv_fused": conv,
+        "subm_conv_split": conv,
         "subm_conv_simt": conv,
         # weight gradient: both gathered rows of every tuple, the list indices
         # (the centre list is implicit), the fp32 gradient written once
@@ -576,7 +580,8 @@ def run_ours(args):
         (regular / strided; the output set's count is read on the host)."""
         h = sc.sc_hash_build(c)
         if not general:
-            return (h,), sc.sc_kmap_build(h, s.ndim, w.K, s.dims, sync=sync, half=args.kmap_half)
+            return (h,), sc.sc_kmap_build(h, s.ndim, w.K, s.dims, sync=sync, half=args.kmap_half,
+                                          split=args.kmap_split)
         ho = sc.sc_hash_build_conv_out(h, s.ndim, w.K, conv_stride, s.dims)
         return (h, ho), sc.sc_kmap_build_conv(h, ho, s.ndim, w.K, conv_stride, s.dims, sync=sync)
 
@@ -746,7 +751,8 @@ def run_ours(args):
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": workload_config(w, s, M, world, args.layer_type, conv_stride, n_out, args.backward, args.scale),
         "run": {"variant": variants, "variant_choice": "given" if args.variant else "measured", "kmap_sync": False,
-                "kmap_probe": "half (mirror symmetry)" if args.kmap_half else "full"},
+                "kmap_probe": "half (mirror symmetry)" if args.kmap_half else "full",
+                "column_split_orders": bool(args.kmap_split)},
         "layer_tflops": round(flops / (conv_ms / 1e3) / 1e12, 3) if conv_ms else None,
         "layer_ms": round(conv_ms, 5),
         "layer_roofline_frac": round(conv_roof_s / (conv_ms / 1e3), 4) if conv_ms else None,

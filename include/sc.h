@@ -65,7 +65,8 @@ typedef enum { SC_F32 = 0, SC_F16 = 1, SC_BF16 = 2 } sc_dtype;
 #define SC_VARIANT_FUSED 0x10u  /* force the output-stationary tcgen05 kernel */
 #define SC_VARIANT_WS 0x20u     /* force the weight-stationary gather/GEMM/scatter kernels */
 #define SC_VARIANT_SIMT 0x40u   /* force the CUDA-core kernel (the only one for SC_F32) */
-#define SC_VARIANT_MASK 0x70u
+#define SC_VARIANT_SPLIT 0x80u  /* force the fused kernel with column splitting (a map built with SC_KMAP_SPLIT) */
+#define SC_VARIANT_MASK 0xF0u
 
 /* flags for sc_kmap_build */
 #define SC_KMAP_NO_SYNC 0x100u  /* do not synchronise; check errors later with sc_kmap_check */
@@ -75,6 +76,7 @@ typedef enum { SC_F32 = 0, SC_F16 = 1, SC_BF16 = 2 } sc_dtype;
 #define SC_KMAP_NO_SORT 0x1000u /* never sort them */
 #define SC_KMAP_TRANSPOSE 0x2000u /* sc_kmap_build_conv: the transposed map (rows = the layer's inputs) */
 #define SC_KMAP_HALF 0x4000u    /* sc_kmap_build: half probe by mirror symmetry (same map, another build) */
+#define SC_KMAP_SPLIT 0x8000u   /* sc_kmap_build, K^ndim <= 32: row orders for column splitting (see below) */
 
 typedef struct sc_hash_s* sc_hash;
 typedef struct sc_kmap_s* sc_kmap;
@@ -188,8 +190,11 @@ sc_status sc_hash_coords(sc_hash h, int32_t* d_coords, sc_stream stream);
  * dims      spatial extents (x, y, z), each in [1, 65535]; every point must
  *           lie inside; neighbours outside are absent (zero padding).
  * flags     0, SC_KMAP_NO_SYNC, at most one of SC_KMAP_ORDER /
- *           SC_KMAP_NO_ORDER, and at most one of SC_KMAP_SORT /
- *           SC_KMAP_NO_SORT.
+ *           SC_KMAP_NO_ORDER, at most one of SC_KMAP_SORT /
+ *           SC_KMAP_NO_SORT, SC_KMAP_HALF (build by the half probe: the
+ *           offsets after the centre are looked up and each hit is mirrored
+ *           by symmetry, "Sparse inputs and sparse convolution", section "A
+ *           symmetry you can check"; the same map), SC_KMAP_SPLIT (below).
  *
  * Locality order: for n >= 262144 (or with SC_KMAP_ORDER) the build first
  * sorts the points into spatially compact groups (a counting sort on the top
@@ -208,6 +213,17 @@ sc_status sc_hash_coords(sc_hash h, int32_t* d_coords, sc_stream stream);
  * 128-row tiles, and a tile walks fewer offsets (the bitmask reordering of
  * "TorchSparse optimizations", section "TorchSparse++").  It too changes no
  * result.
+ *
+ * Column splitting (SC_KMAP_SPLIT, V <= 32; implies the signature sort): the
+ * offset range is cut at the centre into part 0 (offsets up to and including
+ * the centre) and part 1 (the rest), and each part gets a row order of its
+ * own, sorted by the signature of its own offsets, with tile masks of its
+ * offsets only ("TorchSparse optimizations", section "TorchSparse++": the
+ * column split that lets each part's tiles walk fewer offsets).  The layer
+ * then uses them when run with SC_VARIANT_SPLIT (or when sc_subm_conv_tune
+ * measured that variant fastest): two launches, the first storing fp32
+ * partial sums, the second adding its own to them and rounding once.  The map
+ * itself is unchanged.
  *
  * Products, owned by the handle:
  *   nbr      int32 [n, V]: nbr[q*V + idx(d)] = row p with coords[p] =
@@ -317,8 +333,10 @@ sc_status sc_kmap_destroy(sc_kmap m, sc_stream stream);
  * dtype    SC_F16 / SC_BF16 (tensor-core kernels) or SC_F32 (CUDA cores).
  * flags    SC_RELU, optionally one SC_VARIANT_* to force a kernel family.
  *
- * The fused kernel covers V <= 125; larger kernels use the weight-stationary
- * one.  Variant: forced by flags, else the one sc_subm_conv_tune measured fastest
+ * The fused kernel covers V <= 128; larger kernels use the weight-stationary
+ * one.  SC_VARIANT_SPLIT (a map built with SC_KMAP_SPLIT) runs the fused
+ * kernel with column splitting and an fp32 partial-sum buffer [n, c_out]
+ * allocated for the call.  Variant: forced by flags, else the one sc_subm_conv_tune measured fastest
  * for (c_in, c_out, dtype) on this map, else the fused output-stationary
  * kernel (f16/bf16) or the CUDA-core kernel (f32).  Temporary device memory
  * (packed weights, the fp32 accumulator of the weight-stationary variant) is

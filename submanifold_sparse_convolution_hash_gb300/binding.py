@@ -19,6 +19,7 @@ SC_RELU = 0x1
 SC_VARIANT_FUSED = 0x10
 SC_VARIANT_WS = 0x20
 SC_VARIANT_SIMT = 0x40
+SC_VARIANT_SPLIT = 0x80
 SC_KMAP_NO_SYNC = 0x100
 SC_KMAP_ORDER = 0x200
 SC_KMAP_NO_ORDER = 0x400
@@ -26,7 +27,8 @@ SC_KMAP_SORT = 0x800
 SC_KMAP_NO_SORT = 0x1000
 SC_KMAP_TRANSPOSE = 0x2000
 SC_KMAP_HALF = 0x4000
-VARIANTS = {"fused": SC_VARIANT_FUSED, "ws": SC_VARIANT_WS, "simt": SC_VARIANT_SIMT}
+SC_KMAP_SPLIT = 0x8000
+VARIANTS = {"fused": SC_VARIANT_FUSED, "ws": SC_VARIANT_WS, "simt": SC_VARIANT_SIMT, "split": SC_VARIANT_SPLIT}
 VARIANT_NAMES = {v: k for k, v in VARIANTS.items()}
 _DTYPES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 STATUS = {0: "SC_OK", 1: "SC_ERR_INVALID_ARG", 2: "SC_ERR_OUT_OF_RANGE", 3: "SC_ERR_DUPLICATE_COORD",
@@ -266,19 +268,23 @@ def sc_hash_build(coords: torch.Tensor, stream=None, allocator=None) -> Hash:
 
 
 def sc_kmap_build(h: Hash, ndim: int, K: int, dims, sync: bool = True, order: bool | None = None,
-                  sort: bool | None = None, half: bool = False, stream=None, allocator=None) -> KernelMap:
+                  sort: bool | None = None, half: bool = False, split: bool = False, stream=None,
+                  allocator=None) -> KernelMap:
     """Kernel map of a K^ndim submanifold convolution over the hashed points.
 
     order: True / False forces the locality order on / off; None leaves the
     library's default (on for n >= 262144).  sort: the same for the
     signature sort of the convolution's rows (default on for n >= 262144 when
     K^ndim <= 128).  half: build it by the half probe (mirror symmetry); the
-    map is the same."""
+    map is the same.  split: also compute the row orders of column splitting
+    (K^ndim <= 32), which the "split" layer variant uses."""
     d = (ctypes.c_int32 * 3)(*(list(dims) + [1] * (3 - len(dims))))
     m = ctypes.c_void_p()
     flags = 0 if sync else SC_KMAP_NO_SYNC
     if half:
         flags |= SC_KMAP_HALF
+    if split:
+        flags |= SC_KMAP_SPLIT
     if order is True:
         flags |= SC_KMAP_ORDER
     elif order is False:

@@ -368,6 +368,8 @@ sc_status run_variant(KernelMap* m, const ConvArgs& a, unsigned variant) {
       return conv_weight_stationary(a);
     case SC_VARIANT_SIMT:
       return conv_simt(a);
+    case SC_VARIANT_SPLIT:
+      return conv_fused_split(a);
   }
   return set_error(SC_ERR_INVALID_ARG, "more than one variant flag");
 }
@@ -618,7 +620,7 @@ sc_status kmap_build_impl(sc_hash hi, sc_hash ho, int ndim, int K, int stride, c
   for (int a = 0; a < 3; ++a)
     if (dims[a] < 1 || dims[a] > 65535) return set_error(SC_ERR_INVALID_ARG, "dims must be in [1, 65535]");
   if (flags & ~(SC_KMAP_NO_SYNC | SC_KMAP_ORDER | SC_KMAP_NO_ORDER | SC_KMAP_SORT | SC_KMAP_NO_SORT | SC_KMAP_TRANSPOSE |
-                SC_KMAP_HALF))
+                SC_KMAP_HALF | SC_KMAP_SPLIT))
     return set_error(SC_ERR_INVALID_ARG, "unknown kmap flag");
   if ((flags & SC_KMAP_HALF) && !identity)
     return set_error(SC_ERR_UNSUPPORTED, "SC_KMAP_HALF builds submanifold maps only");
@@ -627,6 +629,10 @@ sc_status kmap_build_impl(sc_hash hi, sc_hash ho, int ndim, int K, int stride, c
   if ((flags & SC_KMAP_SORT) && (flags & SC_KMAP_NO_SORT))
     return set_error(SC_ERR_INVALID_ARG, "SC_KMAP_SORT and SC_KMAP_NO_SORT together");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if ((flags & SC_KMAP_SPLIT) && (!identity || V > 32))
+    return set_error(SC_ERR_UNSUPPORTED, "SC_KMAP_SPLIT: submanifold maps with K^ndim <= 32 only");
+  if ((flags & SC_KMAP_SPLIT) && (flags & SC_KMAP_NO_SORT))
+    return set_error(SC_ERR_INVALID_ARG, "SC_KMAP_SPLIT needs the signature sort (not SC_KMAP_NO_SORT)");
   sc_kmap m = new sc_kmap_s();
   KernelMap& k = m->k;
   k.n = h->t.n;
@@ -639,12 +645,19 @@ sc_status kmap_build_impl(sc_hash hi, sc_hash ho, int ndim, int K, int stride, c
   k.V = V;
   for (int a = 0; a < 3; ++a) k.dims[a] = dims[a];
   k.half = (flags & SC_KMAP_HALF) != 0;
+  if ((flags & SC_KMAP_SPLIT) && k.n > 0) {
+    k.nparts = 2;
+    k.split_at = (V - 1) / 2 + 1;  // part 0: offsets up to and including the centre
+  }
   k.up = kmap_unit_points(V);
   k.nunits = static_cast<int>((k.n + k.up - 1) / k.up);
   const bool ordered = (flags & SC_KMAP_ORDER) || (!(flags & SC_KMAP_NO_ORDER) && k.n >= kOrderMinPoints);
   // the signature sort keeps a mask of up to 128 offsets per row (V <= 128)
+  // column splitting (SC_KMAP_SPLIT): submanifold maps with V <= 32; it
+  // brings the signature sort with it
+  const bool split = (flags & SC_KMAP_SPLIT) != 0;
   const bool sorted = identity && V <= 128 && k.n > 0 &&
-                      ((flags & SC_KMAP_SORT) || (!(flags & SC_KMAP_NO_SORT) && k.n >= kSortMinPoints));
+                      (split || (flags & SC_KMAP_SORT) || (!(flags & SC_KMAP_NO_SORT) && k.n >= kSortMinPoints));
   const size_t mask_words = V <= 32 ? 1 : 4;
   const size_t nsig = sorted ? static_cast<size_t>(kmap_sig_buckets(k.n)) : 0;
   // every buffer of the map carved from one allocation, each 256-byte aligned
@@ -668,7 +681,13 @@ sc_status kmap_build_impl(sc_hash hi, sc_hash ho, int ndim, int K, int stride, c
       {reinterpret_cast<void**>(&k.buckets), ordered && k.n > 0 ? sizeof(int) * kmap_order_buckets() : 0},
       {reinterpret_cast<void**>(&k.rowmask), sorted ? sizeof(unsigned) * n * mask_words : 0},
       {reinterpret_cast<void**>(&k.rowdir), sorted && V > 32 ? sizeof(unsigned) * n : 0},
-      {reinterpret_cast<void**>(&k.sig_sel), sorted ? sizeof(int) * kmap_sig_bits() : 0},
+      {reinterpret_cast<void**>(&k.sig_sel), sorted ? sizeof(int) * kmap_sig_bits() * (split ? 3 : 1) : 0},
+      {reinterpret_cast<void**>(&k.part_perm[0]), sorted && split ? sizeof(int) * n : 0},
+      {reinterpret_cast<void**>(&k.part_perm[1]), sorted && split ? sizeof(int) * n : 0},
+      {reinterpret_cast<void**>(&k.part_order[0]), sorted && split ? sizeof(int) * n : 0},
+      {reinterpret_cast<void**>(&k.part_order[1]), sorted && split ? sizeof(int) * n : 0},
+      {reinterpret_cast<void**>(&k.part_present[0]), sorted && split ? sizeof(unsigned) * 4 * ((n + 127) / 128) : 0},
+      {reinterpret_cast<void**>(&k.part_present[1]), sorted && split ? sizeof(unsigned) * 4 * ((n + 127) / 128) : 0},
       {reinterpret_cast<void**>(&k.sigbuckets), sorted ? sizeof(int) * (nsig + nsig / 4096 + 1) : 0},
       {reinterpret_cast<void**>(&k.perm), sorted ? sizeof(int) * n : 0},
       {reinterpret_cast<void**>(&k.conv_order), sorted ? sizeof(int) * n : 0},
@@ -900,6 +919,7 @@ sc_status sc_subm_conv_tune(sc_kmap m, const void* d_feats, const void* d_W, voi
     cands.push_back(SC_VARIANT_SIMT);
   } else {
     if (fused_supported(a)) cands.push_back(SC_VARIANT_FUSED);
+    if (fused_supported(a) && m->k.nparts == 2) cands.push_back(SC_VARIANT_SPLIT);
     if (m->k.identity) cands.push_back(SC_VARIANT_WS);
     if (cands.empty()) return set_error(SC_ERR_UNSUPPORTED, "no tensor-core variant for this layer");
   }

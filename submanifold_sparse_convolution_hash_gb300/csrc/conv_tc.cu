@@ -91,6 +91,12 @@ struct TcParams {
   int V, c_in, c_out, relu, stages, group, acc_cols, tmem_cols;
   int nbuf;                  // accumulator buffers (2: the epilogue overlaps the next unit)
   int* status;
+  // column splitting (output-stationary): this launch walks only the
+  // offsets of one part of the offset range, in that part's row order;
+  // epi 0 casts and stores the output (one part), 1 stores the fp32 partial
+  // sums in acc, 2 adds acc to them and casts and stores the output
+  int epi;
+  int centre_in;             // the centre offset (every row's own) belongs to this launch's offsets
 };
 
 // Next offset after v whose bit is set in the 4-word mask m (V if none).
@@ -115,6 +121,7 @@ __device__ __forceinline__ int next_present(const uint4& m, int v, int V) {
 // at least one row, and every row has itself as a neighbour).
 __device__ __forceinline__ uint4 tile_mask(const TcParams& p, int tile) {
   uint4 m = __ldg(p.present + tile);
+  if (!p.centre_in) return m;
   const int c = (p.V - 1) / 2;
   const uint32_t bit = 1u << (c & 31);
   if (c < 32) m.x |= bit; else if (c < 64) m.y |= bit; else if (c < 96) m.z |= bit; else m.w |= bit;
@@ -486,7 +493,25 @@ __global__ void __launch_bounds__((NPW + 6) * 32, NPW == 4 ? 3 : (NPW == 8 ? 2 :
           float a[16];
           tmem_ld16(trow + static_cast<uint32_t>(c0), a);
           if (dst_row < 0) continue;
+          if (MODE == kOutputStationary && p.epi == 1) {
+            // first part of a split layer: fp32 partial sums
+            float4* dst = reinterpret_cast<float4*>(p.acc + static_cast<int64_t>(dst_row) * p.c_out + c0);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) dst[k] = make_float4(a[4 * k], a[4 * k + 1], a[4 * k + 2], a[4 * k + 3]);
+            continue;
+          }
           if (MODE == kOutputStationary) {
+            if (p.epi == 2) {  // last part: add the earlier parts' sums
+              const float4* src = reinterpret_cast<const float4*>(p.acc + static_cast<int64_t>(dst_row) * p.c_out + c0);
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const float4 q = __ldcs(src + k);
+                a[4 * k] += q.x;
+                a[4 * k + 1] += q.y;
+                a[4 * k + 2] += q.z;
+                a[4 * k + 3] += q.w;
+              }
+            }
             if (p.relu) {
 #pragma unroll
               for (int k = 0; k < 16; ++k) a[k] = fmaxf(a[k], 0.0f);
@@ -773,6 +798,8 @@ TcParams base_params(const ConvArgs& a, const Plan& pl, const uint8_t* img) {
   p.tmem_cols = pl.tmem_cols;
   p.nbuf = pl.nbuf;
   p.status = a.m->status;
+  p.epi = 0;
+  p.centre_in = 1;
   return p;
 }
 
@@ -804,6 +831,47 @@ sc_status conv_fused(const ConvArgs& a) {
   if (st) return st;
   st = pack_weights(a, pl.bk, static_cast<uint8_t*>(img));
   if (!st) st = run_fused(a, pl, static_cast<const uint8_t*>(img));
+  dev_free(img, a.stream);
+  return st;
+}
+
+// Column splitting ("TorchSparse optimizations", section "TorchSparse++"):
+// the offset loop of each output tile runs in two launches, one per part of
+// the offset range, each over that part's own signature-sorted row order (a
+// tile then walks fewer offsets of its part).  The first stores its fp32
+// partial sums, the second adds them to its own, applies the activation and
+// rounds once to the output dtype; the fp32 sums never leave fp32.
+sc_status conv_fused_split(const ConvArgs& a) {
+  Plan pl;
+  if (!fused_ok(a, &pl))
+    return set_error(SC_ERR_UNSUPPORTED, "fused kernel: f16/bf16 only, V <= 128, tile must fit shared memory");
+  const KernelMap* m = a.m;
+  if (m->nparts != 2)
+    return set_error(SC_ERR_UNSUPPORTED, "the split layer needs a map built with SC_KMAP_SPLIT");
+  if (m->n == 0) return SC_OK;
+  const size_t img_bytes = static_cast<size_t>(m->V) * a.c_in * a.c_out * 2;
+  const size_t acc_bytes = static_cast<size_t>(m->n) * a.c_out * sizeof(float);
+  void* img = nullptr;
+  void* acc = nullptr;
+  sc_status st = dev_alloc(&img, img_bytes, a.stream);
+  if (st) return st;
+  st = dev_alloc(&acc, acc_bytes, a.stream);
+  if (st) {
+    dev_free(img, a.stream);
+    return st;
+  }
+  st = pack_weights(a, pl.bk, static_cast<uint8_t*>(img));
+  for (int part = 0; part < 2 && !st; ++part) {
+    TcParams prm = base_params(a, pl, static_cast<const uint8_t*>(img));
+    prm.perm = m->part_perm[part];
+    prm.order = m->part_order[part];
+    prm.present = reinterpret_cast<const uint4*>(m->part_present[part]);
+    prm.acc = static_cast<float*>(acc);
+    prm.epi = part == 0 ? 1 : 2;
+    prm.centre_in = part == 0 ? 1 : 0;  // the centre opens part 1 of the range at index split_at - 1
+    st = dispatch_tc<kOutputStationary>(prm, pl, a.dtype == SC_BF16, a.stream, "subm_conv_split");
+  }
+  dev_free(acc, a.stream);
   dev_free(img, a.stream);
   return st;
 }

@@ -343,6 +343,7 @@ struct BuildArgs {
   unsigned* rowdir;
   int* sig_sel;                    // [kSigBits] features of the row signature, rarest first (with rowmask)
   const int* inv_order;            // half probe with the row order: table row of each input row; else null
+  int split_at;                    // column splitting: first offset of part 1 (0: no split)
 };
 
 // Coarse direction of offset v: (sign(dx) + 1) * 9 + (sign(dy) + 1) * 3 +
@@ -693,16 +694,23 @@ __global__ void __launch_bounds__(kThreads, 5) k_kmap_build(const BuildArgs a) {
     const long long c = lane < nf && lane != cf ? (a.rowdir ? warp_sums[lane]
                                                            : static_cast<long long>(__ldcg(a.cursors + lc * kCursorStride)))
                                                 : 0;
-    long long key = c > 0 ? (c << 8) | lane : none;
-    for (int k = 0; k < kSigBits; ++k) {
-      long long mn = key;
+    // selection 0 over every feature; with column splitting, selections 1
+    // and 2 over the offsets of each part ([0, split_at) and [split_at, V))
+    const int nsel = a.split_at ? 3 : 1;
+    for (int sidx = 0; sidx < nsel; ++sidx) {
+      const bool in_part = sidx == 0 || (sidx == 1 ? lane < a.split_at : lane >= a.split_at);
+      long long key = c > 0 && in_part ? (c << 8) | lane : none;
+      for (int k = 0; k < kSigBits; ++k) {
+        long long mn = key;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const long long other = __shfl_xor_sync(0xffffffffu, mn, o);
-        mn = other < mn ? other : mn;
+        for (int o = 16; o > 0; o >>= 1) {
+          const long long other = __shfl_xor_sync(0xffffffffu, mn, o);
+          mn = other < mn ? other : mn;
+        }
+        // -1: no further feature occurs
+        if (lane == 0) a.sig_sel[sidx * kSigBits + k] = mn == none ? -1 : static_cast<int>(mn & 255);
+        if (key == mn) key = none;
       }
-      if (lane == 0) a.sig_sel[k] = mn == none ? -1 : static_cast<int>(mn & 255);  // -1: no further offset occurs
-      if (key == mn) key = none;
     }
   }
 }
@@ -839,7 +847,8 @@ __global__ void __launch_bounds__(256) k_sig_scatter(const unsigned* __restrict_
 // row when V <= 32, 4 words when V <= 128).
 template <int MW>
 __global__ void __launch_bounds__(256) k_sig_present(const int* __restrict__ perm, const unsigned* __restrict__ rowmask,
-                                                     int64_t n, int centre, unsigned* __restrict__ present) {
+                                                     int64_t n, int centre, unsigned* __restrict__ present,
+                                                     unsigned pmask = 0xFFFFFFFFu, int with_centre = 1) {
   const int64_t ntiles = (n + 127) / 128;
   const int lane = threadIdx.x & 31;
   const int64_t wstride = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -851,7 +860,7 @@ __global__ void __launch_bounds__(256) k_sig_present(const int* __restrict__ per
       if (j < n) {
         const int64_t row = __ldg(perm + j);
         if (MW == 1) {
-          acc[0] |= __ldg(rowmask + row);
+          acc[0] |= __ldg(rowmask + row) & pmask;  // column splitting: the part's offsets only
         } else {
           const uint4 m = __ldg(reinterpret_cast<const uint4*>(rowmask) + row);
           acc[0] |= m.x;
@@ -865,7 +874,7 @@ __global__ void __launch_bounds__(256) k_sig_present(const int* __restrict__ per
     for (int w = 0; w < 4; ++w) acc[w] = __reduce_or_sync(0xffffffffu, acc[w]);
     if (lane < 4) {
       unsigned x = lane == 0 ? acc[0] : (lane == 1 ? acc[1] : (lane == 2 ? acc[2] : acc[3]));
-      if (lane == (centre >> 5)) x |= 1u << (centre & 31);
+      if (with_centre && lane == (centre >> 5)) x |= 1u << (centre & 31);
       present[t * 4 + lane] = x;
     }
   }
@@ -1181,6 +1190,7 @@ sc_status launch_kmap_build(const HashTable* in, const HashTable* h, KernelMap* 
   a.rowdir = m->rowdir;
   a.sig_sel = m->sig_sel;
   a.inv_order = m->inv_order;
+  a.split_at = m->nparts == 2 ? m->split_at : 0;
   const size_t smem = sizeof(int) * (static_cast<size_t>(m->up) * V + static_cast<size_t>(V) * (m->up / 32)) +
                       (m->rowdir ? 16 + sizeof(unsigned) * 128 * 4 : 0);
   if (smem > 48 * 1024) {  // set once per device: the largest the build ever asks for
@@ -1270,7 +1280,27 @@ sc_status launch_kmap_build(const HashTable* in, const HashTable* h, KernelMap* 
   else
     SC_LAUNCH("sig_present", s, k_sig_present<1><<<pg, 256, 0, s>>>(m->perm, m->rowmask, m->n, (V - 1) / 2, m->present));
   e = cudaGetLastError();
-  return e == cudaSuccess ? SC_OK : set_cuda_error(e, "signature sort launch");
+  if (e != cudaSuccess) return set_cuda_error(e, "signature sort launch");
+  // column splitting (V <= 32): each part of the offset range gets its own
+  // sort, keyed by the part's rarest offsets, and tile masks of its offsets
+  for (int part = 0; part < (m->nparts == 2 ? 2 : 0); ++part) {
+    const int* sel = m->sig_sel + (1 + part) * kSigBits;
+    const unsigned pmask = part == 0 ? ((1u << m->split_at) - 1u) : ~((1u << m->split_at) - 1u);
+    e = cudaMemsetAsync(m->sigbuckets, 0, sizeof(int) * nsig, s);
+    if (e != cudaSuccess) return set_cuda_error(e, "signature bucket clear");
+    SC_LAUNCH("sig_count", s, k_sig_count<<<g, 256, 0, s>>>(feat, m->n, sel, m->sigbuckets));
+    SC_LAUNCH("sig_partials", s, k_order_partials<<<chunks, 256, 0, s>>>(m->sigbuckets, partial));
+    SC_LAUNCH("sig_scan", s, k_order_apply<<<chunks, 256, 0, s>>>(m->sigbuckets, partial));
+    SC_LAUNCH("sig_scatter", s,
+              k_sig_scatter<<<g, 256, 0, s>>>(feat, m->order, m->n, sel, m->sigbuckets, m->part_perm[part],
+                                              m->part_order[part]));
+    SC_LAUNCH("sig_present", s,
+              k_sig_present<1><<<pg, 256, 0, s>>>(m->part_perm[part], m->rowmask, m->n, (V - 1) / 2,
+                                                  m->part_present[part], pmask, part == 0 ? 1 : 0));
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return set_cuda_error(e, "split signature sort launch");
+  }
+  return SC_OK;
 }
 
 sc_status launch_hash_coords(const HashTable* h, int32_t* coords, cudaStream_t s) {

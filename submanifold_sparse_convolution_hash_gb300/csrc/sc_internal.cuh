@@ -98,10 +98,18 @@ struct KernelMap {
   // signature sort (V <= 128): the convolution walks rows in a second order
   unsigned* rowmask = nullptr;       // [n] (V <= 32) or [n, 4] (V <= 128) offsets with a neighbour, per row of the table
   unsigned* rowdir = nullptr;        // V > 32: [n] coarse directions with a neighbour, per row; else null
-  int* sig_sel = nullptr;            // [16] signature features (offsets or directions), rarest first
+  int* sig_sel = nullptr;            // [16 (x 3 when split)] signature features (offsets or directions), rarest first
   int* sigbuckets = nullptr;         // counting-sort buckets (+ scan partials)
   int* perm = nullptr;               // [n] sorted position -> table row, or null: no sort
   int* conv_order = nullptr;         // [n] sorted position -> input row
+  // column splitting (V <= 32): offsets [0, split_at) form part 0 (the
+  // centre is the last of them), [split_at, V) part 1; each part has its own
+  // signature sort of the rows and tile masks restricted to its offsets
+  int nparts = 1;
+  int split_at = 0;
+  int* part_perm[2] = {nullptr, nullptr};
+  int* part_order[2] = {nullptr, nullptr};
+  unsigned* part_present[2] = {nullptr, nullptr};
   int* ws_tiles = nullptr;           // [V+1] prefix of ceil(count/128) per offset
   int64_t* map_size = nullptr;       // device: n + offs[V]
   int* status = nullptr;             // [4]: map status, copy of the hash status, scan ticket
@@ -177,6 +185,7 @@ struct ConvArgs {
 sc_status conv_bwd_weight(const KernelMap* m, const void* feats, const void* gout, void* dW, int c_in, int c_out,
                           sc_dtype dtype, cudaStream_t s);
 sc_status conv_fused(const ConvArgs& a);
+sc_status conv_fused_split(const ConvArgs& a);
 sc_status conv_weight_stationary(const ConvArgs& a);
 sc_status conv_simt(const ConvArgs& a);
 // nbr rows in input order (undoing the row order) into a device buffer

@@ -470,3 +470,57 @@ def test_kmap_view_matches_oracle(name, K, order, half):
         k = np.lexsort((gi[a:b], go[a:b]))
         np.testing.assert_array_equal(go[a:b][k], ro)
         np.testing.assert_array_equal(gi[a:b][k], ri)
+
+
+SPLIT_CASES = [
+    ("lidar", 3, 32, 32, "f16", False),
+    ("indoor", 3, 64, 64, "bf16", True),
+    ("batch", 3, 128, 256, "f16", True),
+    ("batch", 3, 256, 256, "f16", False),
+    ("uniform2d_dense", 5, 16, 48, "bf16", True),
+]
+
+
+@pytest.mark.parametrize("order", [False, True])
+@pytest.mark.parametrize("name,K,c_in,c_out,dtype,relu", SPLIT_CASES)
+def test_conv_with_column_splitting(name, K, c_in, c_out, dtype, relu, order):
+    """Column splitting ("TorchSparse optimizations", section "TorchSparse++"):
+    two launches over the two halves of the offset range, each in its own
+    signature-sorted row order, fp32 partial sums between them.  The layer,
+    its input gradient and the unsplit kernel on the same map all match the
+    oracle."""
+    s = SCENES[name]
+    c, h, m = build(s, K, order=order, sort=True)
+    hs = sc.sc_hash_build(c)
+    ms = sc.sc_kmap_build(hs, s.ndim, K, s.dims, order=order, split=True)
+    np.testing.assert_array_equal(ms.nbr().cpu().numpy(), m.nbr().cpu().numpy())
+    f, w, f64, w64 = layer_inputs(s, K, c_in, c_out, dtype, seed=11 + c_in + K)
+    ref = oracle.subm_conv(s.coords, f64, w64, s.ndim, K, s.dims, relu=relu)
+    for variant in ("split", "fused"):
+        out = torch.full((s.n, c_out), float("nan"), dtype=f.dtype, device="cuda")
+        sc.sc_subm_conv_fwd(ms, f, w, out=out, relu=relu, variant=variant)
+        torch.cuda.synchronize()
+        assert_close(out, ref, dtype, f"column split {name} K={K} {c_in}->{c_out} {variant}")
+    g = torch.from_numpy(scenes.features(77, s.n, c_out)).to(f.dtype).cuda()
+    gin = sc.sc_subm_conv_bwd_data(ms, g, w, variant="split")
+    torch.cuda.synchronize()
+    ref_g = oracle.subm_conv_bwd_data(s.coords, g.double().cpu().numpy(), w64, s.ndim, K, s.dims)
+    assert_close(gin, ref_g, dtype, f"column split input gradient {name}")
+    ms.check()
+
+
+def test_column_splitting_arguments():
+    s = SCENES["indoor"]
+    h = sc.sc_hash_build(torch.from_numpy(s.coords).cuda())
+    with pytest.raises(ScError) as e:  # V = 125 > 32
+        sc.sc_kmap_build(h, 3, 5, s.dims, split=True)
+    assert e.value.code == 5
+    with pytest.raises(ScError) as e:
+        sc.sc_kmap_build(h, 3, 3, s.dims, split=True, sort=False)
+    assert e.value.code == 1
+    m = sc.sc_kmap_build(h, 3, 3, s.dims)  # no split orders: the split variant is refused
+    f = torch.zeros((s.n, 32), dtype=torch.float16, device="cuda")
+    w = torch.zeros((27, 32, 32), dtype=torch.float16, device="cuda")
+    with pytest.raises(ScError) as e:
+        sc.sc_subm_conv_fwd(m, f, w, variant="split")
+    assert e.value.code == 5
