@@ -636,7 +636,7 @@ size_t plan_smem(const Plan& pl, size_t stage_bytes) {  // stage_bytes: one stag
 // many CTAs per SM as shared memory (about 220 KB) and TMEM (512 columns)
 // allow, and gives each CTA 4 producer warps at three CTAs per SM, else 8.
 // Developer overrides for measurement sweeps (environment, read per call):
-// SC_DEV_BK, SC_DEV_T, SC_DEV_STAGES, SC_DEV_GROUP, SC_DEV_NPW, SC_DEV_CPS
+// SC_DEV_BK, SC_DEV_T, SC_DEV_STAGES, SC_DEV_GROUP, SC_DEV_NPW, SC_DEV_NBUF, SC_DEV_CPS
 // (an upper bound), SC_DEV_FORCECPS (launch that many CTAs per SM),
 // SC_DEV_MAX_CARVEOUT (keep the largest shared-memory carveout) and
 // SC_DEV_VERBOSE (print each launch's plan).  None changes the result.
@@ -653,6 +653,7 @@ bool make_plan(int c_in, int c_out, bool output_stationary, Plan* pl) {
   pl->t = (output_stationary && pl->bk == 64 && c_out >= 256) ? 2 : 1;
   if (const char* e = getenv("SC_DEV_T")) pl->t = (atoi(e) == 2 && output_stationary && pl->bk >= 32) ? 2 : 1;
   pl->nbuf = 2 * pl->t * cols <= 512 ? 2 : 1;
+  if (const char* e = getenv("SC_DEV_NBUF")) pl->nbuf = atoi(e) == 1 ? 1 : pl->nbuf;
   pl->tmem_cols = pl->nbuf * pl->t * cols;
   if (pl->tmem_cols > 512) return false;
   const size_t a = static_cast<size_t>(kRows) * pl->bk * 2 * pl->t;
