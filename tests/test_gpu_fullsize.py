@@ -174,7 +174,7 @@ def test_full_size_input_gradient_on_sampled_rows(idx):
     assert_close(gin[torch.from_numpy(F.rows).cuda()], ref, w.dtype, f"workload {idx} input gradient")
 
 
-@pytest.mark.parametrize("idx", [1, 2])
+@pytest.mark.parametrize("idx", [1, 2, 4])
 def test_full_size_weight_gradient(idx):
     F = full(idx)
     s, w = F.s, F.w
@@ -186,3 +186,30 @@ def test_full_size_weight_gradient(idx):
     ref = oracle.subm_conv_bwd_weight(s.coords, x.double().cpu().numpy(), g.double().cpu().numpy(), s.ndim, w.K,
                                       s.dims)
     assert_close(dW, ref, w.dtype, f"workload {idx} weight gradient")
+
+
+def test_full_size_eight_layer_stack_backward_per_layer():
+    """The batched-LiDAR stack's backward pass at full size, layer by layer:
+    each layer's input gradient on sampled rows and, for the 32 -> 64,
+    64 -> 128 and 256 -> 256 layers, its whole weight gradient, against the
+    oracle fed the GPU's own layer input and a seeded output gradient."""
+    F = full(3)
+    s, w = F.s, F.w
+    x = None
+    for li in range(len(w.channels) - 1):
+        x, W = F.layer(li, x)
+        c_out = W.shape[2]
+        g = torch.from_numpy(scenes.features(w.seed + 60 + li, s.n, c_out)).to(W.dtype).cuda()
+        gin = sc.sc_subm_conv_bwd_data(F.m, g, W)
+        torch.cuda.synchronize()
+        ref = oracle.subm_conv_bwd_data(s.coords, g.double().cpu().numpy(), W.double().cpu().numpy(), s.ndim, w.K,
+                                        s.dims, rows=F.rows)
+        assert_close(gin[torch.from_numpy(F.rows).cuda()], ref, w.dtype, f"layer {li} input gradient")
+        if li in (1, 3, 7):
+            dW = sc.sc_subm_conv_bwd_weight(F.m, x, g)
+            torch.cuda.synchronize()
+            ref_w = oracle.subm_conv_bwd_weight(s.coords, x.double().cpu().numpy(), g.double().cpu().numpy(), s.ndim,
+                                                w.K, s.dims)
+            assert_close(dW, ref_w, w.dtype, f"layer {li} weight gradient")
+        x = sc.sc_subm_conv_fwd(F.m, x, W, relu=li + 2 < len(w.channels))
+    F.m.check()
