@@ -504,9 +504,16 @@ __global__ void __launch_bounds__(kThreads, 5) k_kmap_build(const BuildArgs a) {
           act[q] = dxm > 0 || (dxm == 0 && (dym > 0 || (dym == 0 && dzm > 0)));
         }
         bk[q] = batch | pack_key(0, 2 * bxs[q], 2 * bys[q], 2 * bzs[q]);
-        if (act[q]) {
+        if (act[q]) kk[q] = __ldg(&a.table[block_home(bk[q], a.mask)].key);
+      }
+      // the rows only of the entries found at home (most covering blocks of a
+      // surface point are absent, and the L1 pipe bounds this kernel)
+      bool hit[kLookups];
+#pragma unroll
+      for (int q = 0; q < kLookups; ++q) {
+        hit[q] = act[q] && kk[q] == bk[q];
+        if (hit[q]) {
           const BlockEntry* e = a.table + block_home(bk[q], a.mask);
-          kk[q] = __ldg(&e->key);
           r0[q] = __ldg(reinterpret_cast<const int4*>(e->rows));
           r1[q] = __ldg(reinterpret_cast<const int4*>(e->rows + 4));
         }
@@ -514,9 +521,8 @@ __global__ void __launch_bounds__(kThreads, 5) k_kmap_build(const BuildArgs a) {
 #pragma unroll
       for (int q = 0; q < kLookups; ++q) {
         if (!act[q]) continue;
-        bool hit = kk[q] == bk[q];
-        if (!hit && kk[q] != kEmptyKey) hit = lookup_block(a.table, a.mask, bk[q], r0[q], r1[q]);
-        if (!hit) continue;
+        if (!hit[q] && kk[q] != kEmptyKey) hit[q] = lookup_block(a.table, a.mask, bk[q], r0[q], r1[q]);
+        if (!hit[q]) continue;
         // per axis: which of the block's two voxels fall in the neighbourhood
         // (|d| <= r; the table holds no point outside its grid, so no other
         // bound is needed), and the index of voxel (0, 0, 0)
