@@ -393,7 +393,8 @@ __global__ void __launch_bounds__(kThreads, 5) k_kmap_build(const BuildArgs a) {
   int* s_tile = reinterpret_cast<int*>(smem4);
   unsigned* s_bal = reinterpret_cast<unsigned*>(s_tile + up * V);
   // V > 32 with the signature sort: the 128-bit offset mask of each row (in
-  // the dynamic allocation only when used), 16-byte aligned
+  // the dynamic allocation only when used), word-major ([4][128]: the emit
+  // phase's atomics of a warp's 32 rows fall in 32 banks), 16-byte aligned
   unsigned* s_rmask4 = reinterpret_cast<unsigned*>(
       (reinterpret_cast<uintptr_t>(s_bal + V * ngroups) + 15) & ~static_cast<uintptr_t>(15));
   __shared__ int s_last;
@@ -572,6 +573,9 @@ __global__ void __launch_bounds__(kThreads, 5) k_kmap_build(const BuildArgs a) {
   {
     const unsigned lt = (1u << lane) - 1u;
     unsigned rm[4] = {0u, 0u, 0u, 0u};  // offsets with a hit, for the rows g * 32 + lane
+    int my_row[ngroups];                // input row of unit row g * 32 + lane
+#pragma unroll
+    for (int g = 0; g < ngroups; ++g) my_row[g] = s_row[g * 32 + lane];
     for (int vb = warp; vb < V; vb += kWarps * 32) {
       const int nk = min(32, (V - vb + kWarps - 1) / kWarps);
       int cnt_mine = 0;
@@ -606,7 +610,7 @@ __global__ void __launch_bounds__(kThreads, 5) k_kmap_build(const BuildArgs a) {
           const unsigned b = bs[g];
           if ((b >> lane) & 1u) {
             const int64_t at = lb + at0 + __popc(b & lt);
-            const int jn = s_tile[(g * 32 + lane) * V + v], iq = s_row[g * 32 + lane];
+            const int jn = s_tile[(g * 32 + lane) * V + v], iq = my_row[g];
             __stcs(a.in_rows + at, jn);
             __stcs(a.out_rows + at, iq);
             if (HALF) {
@@ -621,7 +625,7 @@ __global__ void __launch_bounds__(kThreads, 5) k_kmap_build(const BuildArgs a) {
             if (v < 32) rm[g] |= 1u << v;
             }
             if (!HALF && a.rowdir) {  // V > 32: the row's offset and direction bits
-              atomicOr(s_rmask4 + (g * 32 + lane) * 4 + (v >> 5), 1u << (v & 31));
+              atomicOr(s_rmask4 + (v >> 5) * 128 + g * 32 + lane, 1u << (v & 31));
               atomicOr(s_rmask + g * 32 + lane, 1u << s_dir[v]);
             }
           }
@@ -643,7 +647,9 @@ __global__ void __launch_bounds__(kThreads, 5) k_kmap_build(const BuildArgs a) {
     atomicOr(a.present + static_cast<int64_t>(u >> 1) * 4 + threadIdx.x, s_pres[threadIdx.x]);
   if (!HALF && a.rowmask && !a.rowdir && threadIdx.x < np) a.rowmask[i0 + threadIdx.x] = s_rmask[threadIdx.x];
   if (!HALF && a.rowdir && threadIdx.x < np) {  // V > 32: 128-bit offset mask and direction bits per row
-    reinterpret_cast<uint4*>(a.rowmask)[i0 + threadIdx.x] = reinterpret_cast<const uint4*>(s_rmask4)[threadIdx.x];
+    const int t = threadIdx.x;
+    reinterpret_cast<uint4*>(a.rowmask)[i0 + t] =
+        make_uint4(s_rmask4[t], s_rmask4[128 + t], s_rmask4[256 + t], s_rmask4[384 + t]);
     a.rowdir[i0 + threadIdx.x] = s_rmask[threadIdx.x];
   }
 
