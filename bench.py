@@ -72,6 +72,9 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the extras of the default line: the training step and the stride-2 layer of the same "
+                         "workload, each measured by a child run of this script")
     ap.add_argument("--backward", action="store_true",
                     help="a training step: after the forward layers, the input and weight gradients of every "
                          "layer (a seeded output gradient, ReLU masks applied)")
@@ -83,6 +86,9 @@ def parse_args():
     ap.add_argument("--stride", type=int, default=2, help="stride of --layer-type strided")
     ap.add_argument("--kmap-half", action="store_true",
                     help="build submanifold maps with the half probe (mirror symmetry) instead of the full probe")
+    ap.add_argument("--kmap-sort", choices=["auto", "on", "off"], default="auto",
+                    help="signature sort of the map's rows: the library's default (auto: at 262,144 rows and more), "
+                         "always, or never")
     ap.add_argument("--kmap-split", action="store_true",
                     help="also build the row orders of column splitting (K^ndim <= 32), so each layer's measured "
                          "variant choice includes the split kernel")
@@ -575,15 +581,17 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
+    sort_arg = {"auto": None, "on": True, "off": False}[args.kmap_sort]
+
     def build_map(c, sync):
         """hash -> kernel map (submanifold), or hash -> output set -> map
         (regular / strided; the output set's count is read on the host)."""
         h = sc.sc_hash_build(c)
         if not general:
             return (h,), sc.sc_kmap_build(h, s.ndim, w.K, s.dims, sync=sync, half=args.kmap_half,
-                                          split=args.kmap_split)
+                                          split=args.kmap_split, sort=sort_arg)
         ho = sc.sc_hash_build_conv_out(h, s.ndim, w.K, conv_stride, s.dims)
-        return (h, ho), sc.sc_kmap_build_conv(h, ho, s.ndim, w.K, conv_stride, s.dims, sync=sync)
+        return (h, ho), sc.sc_kmap_build_conv(h, ho, s.ndim, w.K, conv_stride, s.dims, sync=sync, sort=sort_arg)
 
     # variant of each layer chosen from measured time on this map
     hs0, m0 = build_map(coords, True)
@@ -752,7 +760,7 @@ def run_ours(args):
         "config": workload_config(w, s, M, world, args.layer_type, conv_stride, n_out, args.backward, args.scale),
         "run": {"variant": variants, "variant_choice": "given" if args.variant else "measured", "kmap_sync": False,
                 "kmap_probe": "half (mirror symmetry)" if args.kmap_half else "full",
-                "column_split_orders": bool(args.kmap_split)},
+                "column_split_orders": bool(args.kmap_split), "kmap_sort": args.kmap_sort},
         "layer_tflops": round(flops / (conv_ms / 1e3) / 1e12, 3) if conv_ms else None,
         "layer_ms": round(conv_ms, 5),
         "layer_roofline_frac": round(conv_roof_s / (conv_ms / 1e3), 4) if conv_ms else None,
@@ -772,6 +780,15 @@ def run_ours(args):
 
     if not args.no_e2e and rank == 0:
         line["e2e"] = run_e2e(args, w, s, f_np, Ws, tdt, dev, variants, world, build_map, n_out)
+    if args.backward:
+        # the weight gradient against its own algorithmic bytes (both gathered
+        # rows of every tuple, the lists, the fp32 gradient)
+        if "subm_conv_wgrad" in prof_all:
+            t_w = prof_all["subm_conv_wgrad"][1] / 1e3 / bd_steps
+            b_w = algo_bytes_step("subm_conv_wgrad", s.n, V, M, layers, esize, ntiles, False, None)
+            line["wgrad_roofline_frac"] = round(b_w / t_w / (peaks["hbm_gbs"] * 1e9), 4)
+    if not args.no_extras and rank == 0 and world == 1 and not args.backward and not general:
+        line["extras"] = run_extras(args)
     if not args.no_cpu_baseline and rank == 0:
         if general:
             line["cpu_baseline"] = cpu_oracle_run(s, w.K, feats.float().cpu().numpy(), W0, args.cpu_seconds,
@@ -783,6 +800,36 @@ def run_ours(args):
     if world > 1:
         torch.distributed.barrier()
         torch.distributed.destroy_process_group()
+
+
+def run_extras(args):
+    """The training step (--backward) and the stride-2 layer (--layer-type
+    strided) of the same workload, each measured by a child run of this
+    script with the same timing rules (L2 flushed per step, CUDA events),
+    after this run's own timed steps.  Returns their key figures."""
+    base = [sys.executable, os.path.join(ROOT, "bench.py"), "--workload", str(args.workload), "--scale",
+            str(args.scale), "--steps", str(min(args.steps, 20)), "--warmup", str(args.warmup), "--no-e2e",
+            "--no-cpu-baseline", "--no-extras"]
+    keys = ("value", "ms_per_step", "layer_ms", "layer_roofline_frac", "layer_unique_roofline_frac",
+            "wgrad_roofline_frac", "kmap_build_ms", "clocks")
+    out = {}
+    for name, extra in (("training_step", ["--backward"]), ("stride2_layer", ["--layer-type", "strided"])):
+        try:
+            r = subprocess.run(base + extra, capture_output=True, text=True, timeout=900, cwd=ROOT)
+            lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+            if r.returncode != 0 or not lines:
+                out[name] = {"error": (r.stderr or "no output")[-300:]}
+                continue
+            d = json.loads(lines[-1])
+            e = {k: d[k] for k in keys if k in d}
+            e["pass"] = d["config"]["pass"]
+            if name == "stride2_layer":
+                e["N_out"] = d["config"]["N_out"]
+                e["map_size"] = d["config"]["map_size"]
+            out[name] = e
+        except (subprocess.SubprocessError, OSError, ValueError) as ex:
+            out[name] = {"error": str(ex)[-300:]}
+    return out
 
 
 def run_e2e(args, w, s, f_np, Ws_dev, tdt, dev, variants, world, build_map, n_out):

@@ -253,8 +253,11 @@ sc_status sc_kmap_build(sc_hash h, int ndim, int K, const int32_t dims[3], unsig
  * rulebook", section 3 (rulebook grouped by offset).  Unlike a submanifold
  * map the centre offset is searched like the others and has its own list
  * segment; |M| = offs[V].  The map keeps neither hash: both stay owned by
- * the caller.  Flags as for sc_kmap_build except SC_KMAP_SORT
- * (SC_ERR_UNSUPPORTED: the signature sort is for submanifold maps).
+ * the caller.  Flags as for sc_kmap_build except SC_KMAP_HALF and
+ * SC_KMAP_SPLIT (SC_ERR_UNSUPPORTED: submanifold maps only); the locality
+ * order and the signature sort apply to the map's rows (the outputs, or the
+ * inputs of a transposed map) as for a submanifold map, except that the sort
+ * is on by default only when V > 32 as well.
  *
  * sc_subm_conv_fwd and sc_subm_conv_bwd_weight take such a map: feats then
  * has the input's n_in rows and out / gout the map's n rows.  The

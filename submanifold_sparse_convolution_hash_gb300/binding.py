@@ -313,7 +313,8 @@ def sc_hash_build_conv_out(h: Hash, ndim: int, K: int, stride: int, dims, stream
 
 
 def sc_kmap_build_conv(h_in: Hash, h_out: Hash, ndim: int, K: int, stride: int, dims, sync: bool = True,
-                       order: bool | None = None, transpose: bool = False, stream=None, allocator=None) -> KernelMap:
+                       order: bool | None = None, sort: bool | None = None, transpose: bool = False, stream=None,
+                       allocator=None) -> KernelMap:
     """Kernel map of a regular / strided layer: rows = the points of `h_out`,
     neighbours = rows of `h_in` at stride * o + d.  transpose: the transposed
     map (rows = the points of `h_in`, neighbours = the outputs whose windows
@@ -327,6 +328,10 @@ def sc_kmap_build_conv(h_in: Hash, h_out: Hash, ndim: int, K: int, stride: int, 
         flags |= SC_KMAP_ORDER
     elif order is False:
         flags |= SC_KMAP_NO_ORDER
+    if sort is True:
+        flags |= SC_KMAP_SORT
+    elif sort is False:
+        flags |= SC_KMAP_NO_SORT
     _check(lib().sc_kmap_build_conv(h_in._h, h_out._h, ndim, K, stride, d, flags, _alloc_arg(allocator),
                                     _stream(stream), ctypes.byref(m)),
            "sc_kmap_build_conv")

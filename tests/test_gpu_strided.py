@@ -27,10 +27,10 @@ SC = {
 }
 
 
-def build(s, K, stride, order=None):
+def build(s, K, stride, order=None, sort=None):
     h = sc.sc_hash_build(torch.from_numpy(s.coords).cuda())
     ho = sc.sc_hash_build_conv_out(h, s.ndim, K, stride, s.dims)
-    m = sc.sc_kmap_build_conv(h, ho, s.ndim, K, stride, s.dims, order=order)
+    m = sc.sc_kmap_build_conv(h, ho, s.ndim, K, stride, s.dims, order=order, sort=sort)
     return h, ho, m
 
 
@@ -80,11 +80,12 @@ CONV = [
 ]
 
 
-@pytest.mark.parametrize("relu", [False, True])
+@pytest.mark.parametrize("relu,sort", [(False, None), (True, None), (False, True), (True, True)])
 @pytest.mark.parametrize("name,K,stride,c_in,c_out,dtype,variant", CONV)
-def test_conv_matches_oracle(name, K, stride, c_in, c_out, dtype, variant, relu):
+def test_conv_matches_oracle(name, K, stride, c_in, c_out, dtype, variant, relu, sort):
+    """sort: the layer on a map whose output rows are signature-sorted."""
     s = SC[name]
-    h, ho, m = build(s, K, stride)
+    h, ho, m = build(s, K, stride, order=True if sort else None, sort=sort)
     oc = ho.coords().cpu().numpy()
     V = K ** s.ndim
     f = scenes.features(7 + stride, s.n, c_in)
@@ -164,12 +165,13 @@ def test_unsupported_paths_and_empty_input():
     assert out.shape == (0, 16)
 
 
-def test_full_size_strided_layer_on_lidar_scan():
+@pytest.mark.parametrize("sort", [None, True])
+def test_full_size_strided_layer_on_lidar_scan(sort):
     """The LiDAR workload (1440 x 1440 x 41, ~100k voxels) through a stride-2
     3x3x3 layer, C 32 -> 64 f16: the output set in full, the map in full, the
-    features on sampled output rows."""
+    features on sampled output rows (sort: with the signature-sorted rows)."""
     w, s = scenes.workload(1)
-    h, ho, m = build(s, 3, 2)
+    h, ho, m = build(s, 3, 2, order=True if sort else None, sort=sort)
     oc = ho.coords().cpu().numpy()
     assert np.array_equal(sort_rows(oc), oracle.conv_out_coords(s.coords, 3, 3, 2, s.dims))
     nbr_ref = oracle.conv_kmap(s.coords, oc, 3, 3, 2, s.dims)
@@ -193,10 +195,12 @@ def test_full_size_strided_layer_on_lidar_scan():
 ])
 def test_transposed_map_and_input_gradient(name, K, stride, c_in, c_out, dtype, order):
     """The transposed map holds, for each input p, the outputs whose windows
-    contain it at the mirrored offset; the input gradient runs on it."""
+    contain it at the mirrored offset; the input gradient runs on it (with the
+    row order, also on signature-sorted rows)."""
     s = SC[name]
     h, ho, m = build(s, K, stride)
-    mt = sc.sc_kmap_build_conv(h, ho, s.ndim, K, stride, s.dims, order=order, transpose=True)
+    mt = sc.sc_kmap_build_conv(h, ho, s.ndim, K, stride, s.dims, order=order, sort=True if order else None,
+                               transpose=True)
     assert mt.n == s.n and mt.n_in == ho.n
     oc = ho.coords().cpu().numpy()
     V = K ** s.ndim
