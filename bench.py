@@ -659,6 +659,31 @@ def run_ours(args):
     keep.clear()
     dom = max(prof_all, key=lambda k: prof_all[k][1])
 
+    # each forward layer alone (events around its call on one map, flushed
+    # L2 before every layer), untimed pass: per-layer roofline fractions
+    layer_detail = []
+    if len(layers) > 1 and not args.backward:
+        hs_l, m_l = build_map(coords, False)
+        reps = min(bd_steps, 20)
+        ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+              for _ in layers]
+        for rep in range(reps):
+            xin = feats
+            for li, W in enumerate(Ws):
+                flush.zero_()
+                ev[li][rep][0].record(stream)
+                sc.sc_subm_conv_fwd(m_l, xin, W, out=outs[li], relu=li + 1 < len(Ws), variant=variants[li])
+                ev[li][rep][1].record(stream)
+                xin = outs[li]
+        torch.cuda.synchronize()
+        for li, (ci, co) in enumerate(layers):
+            t_l = statistics.median(a.elapsed_time(b) for a, b in ev[li]) / 1e3
+            b_l = algo_bytes_step("subm_conv_fused", s.n, V, M, [(ci, co)], esize, ntiles, False, None)
+            roof_l = max(2.0 * M * ci * co / (load_peaks()["bf16_tflops"] * 1e12), b_l / (load_peaks()["hbm_gbs"] * 1e9))
+            layer_detail.append({"c_in": ci, "c_out": co, "us": round(t_l * 1e6, 2),
+                                 "roofline_frac": round(roof_l / t_l, 4), "variant": variants[li]})
+        del hs_l, m_l
+
     # map build end to end (sc_hash_build .. sc_kmap_build, events on the
     # stream, no per-kernel brackets), untimed pass
     map_e2e = []
@@ -774,6 +799,7 @@ def run_ours(args):
         "roofline": roofline,
         "per_kernel": per_kernel,
         "per_kernel_source": f"untimed pass of {bd_steps} steps, every launch bracketed by CUDA events",
+        "layers_detail": layer_detail or None,
         "gpu_launches": launches,
         "clocks": clk.summary(("timed",), 10, ("warmup", "breakdown", "map_build", "timed")),
     }
