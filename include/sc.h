@@ -204,7 +204,7 @@ sc_status sc_hash_coords(sc_hash h, int32_t* d_coords, sc_stream stream);
  * rows and nbr stays in input row order.
  *
  * Signature sort (V <= 128; for n >= 262144 or with SC_KMAP_SORT): inside
- * windows of 65536 consecutive rows of that order, the convolution's rows
+ * windows of 524288 consecutive rows of that order, the convolution's rows
  * are counting-sorted by a 16-bit signature, which of the 16 least frequent
  * features (over the whole map) the row has a neighbour under.  The
  * features are the offsets when V <= 32, else the 26 coarse directions

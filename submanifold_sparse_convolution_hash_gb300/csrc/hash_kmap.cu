@@ -55,7 +55,10 @@ namespace {
 constexpr int kThreads = 256;    // threads per map-build block
 constexpr int kLookups = 2;      // hash lookups in flight per map-build thread
 constexpr int kSigBits = 16;     // signature sort: rare offsets in a row's key
-constexpr int kSigWindow = 65536;  // rows per signature-sort window
+// rows per signature-sort window: 524,288 (measured against 2^15 .. 2^20:
+// the batched-LiDAR stack 3.18 ms at 2^16 against 2.96 ms, the 1M-voxel
+// layer 293 against 282 us, the 2M-voxel 5x5x5 layer 3.02 against 2.99 ms)
+constexpr int kSigWindowLog2 = 19;
 constexpr int kWsRows = 128;     // rows per weight-stationary tile
 // shared memory of a build block: 128 points x V <= 128 (or 32 x V <= 343)
 // neighbour slots, the ballots and the per-offset bases
@@ -804,29 +807,29 @@ __global__ void __launch_bounds__(128) k_kmap_masks(const int* __restrict__ nbr,
   }
 }
 
-// Signature sort, a counting sort on (window of kSigWindow rows, signature):
+// Signature sort, a counting sort on (window of 2^wlog2 rows, signature):
 // rows keep their window (a spatially compact run of the locality order, or
 // of the input order) and are grouped by which rare offsets they touch, so a
 // 128-row tile spans fewer offsets.  Rows with equal keys in a warp share one
 // atomic (__match_any_sync); the order inside a key is unspecified.
-__device__ __forceinline__ int64_t sig_key(int64_t k, unsigned mk, const int* __restrict__ sel) {
+__device__ __forceinline__ int64_t sig_key(int64_t k, unsigned mk, const int* __restrict__ sel, int wlog2) {
   unsigned sg = 0;
 #pragma unroll
   for (int b = 0; b < kSigBits; ++b) {
     const int v = __ldg(sel + b);
     if (v >= 0) sg |= ((mk >> v) & 1u) << (kSigBits - 1 - b);
   }
-  return ((k / kSigWindow) << kSigBits) | sg;
+  return ((k >> wlog2) << kSigBits) | sg;
 }
 
 __global__ void __launch_bounds__(256) k_sig_count(const unsigned* __restrict__ rowmask, int64_t n,
-                                                   const int* __restrict__ sel, int* __restrict__ buckets) {
+                                                   const int* __restrict__ sel, int* __restrict__ buckets, int wlog2) {
   const int lane = threadIdx.x & 31;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   const int64_t nr = (n + 31) & ~int64_t(31);  // whole warps stay in the loop
   for (int64_t k = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; k < nr; k += stride) {
     const bool live = k < n;
-    const int64_t key = live ? sig_key(k, __ldg(rowmask + k), sel) : -1;
+    const int64_t key = live ? sig_key(k, __ldg(rowmask + k), sel, wlog2) : -1;
     const unsigned peers = __match_any_sync(0xffffffffu, key);
     if (live && lane == __ffs(peers) - 1) atomicAdd(buckets + key, __popc(peers));
   }
@@ -834,13 +837,13 @@ __global__ void __launch_bounds__(256) k_sig_count(const unsigned* __restrict__ 
 
 __global__ void __launch_bounds__(256) k_sig_scatter(const unsigned* __restrict__ rowmask, const int* __restrict__ order,
                                                      int64_t n, const int* __restrict__ sel, int* __restrict__ cursors,
-                                                     int* __restrict__ perm, int* __restrict__ conv_order) {
+                                                     int* __restrict__ perm, int* __restrict__ conv_order, int wlog2) {
   const int lane = threadIdx.x & 31;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   const int64_t nr = (n + 31) & ~int64_t(31);
   for (int64_t k = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; k < nr; k += stride) {
     const bool live = k < n;
-    const int64_t key = live ? sig_key(k, __ldg(rowmask + k), sel) : -1;
+    const int64_t key = live ? sig_key(k, __ldg(rowmask + k), sel, wlog2) : -1;
     const unsigned peers = __match_any_sync(0xffffffffu, key);
     const int leader = __ffs(peers) - 1;
     int base = 0;
@@ -1089,7 +1092,21 @@ int grid_for(int64_t n, int threads) {
 int kmap_unit_points(int V) { return V <= 64 ? 128 : (V <= 128 ? 64 : 32); }
 int kmap_order_buckets() { return kBuckets + kBucketBlocks; }
 int kmap_sig_bits() { return kSigBits; }
-int64_t kmap_sig_buckets(int64_t n) { return ((n + kSigWindow - 1) / kSigWindow) << kSigBits; }
+// The signature-sort window (log2 rows): 19 by default; developer override
+// SC_DEV_SIG_WINDOW_LOG2 in [12, 20] for measurement sweeps (the result is
+// the same, only the row order of the tiles changes).
+int kmap_sig_window_log2() {
+  static int w = [] {
+    const char* e = getenv("SC_DEV_SIG_WINDOW_LOG2");
+    const int v = e ? atoi(e) : kSigWindowLog2;
+    return v >= 12 && v <= 20 ? v : kSigWindowLog2;
+  }();
+  return w;
+}
+int64_t kmap_sig_buckets(int64_t n) {
+  const int64_t win = int64_t(1) << kmap_sig_window_log2();
+  return ((n + win - 1) / win) << kSigBits;
+}
 
 sc_status kmap_unpermute_nbr(const KernelMap* m, int* dst, cudaStream_t s) {
   if (m->n == 0) return SC_OK;
@@ -1280,12 +1297,13 @@ sc_status launch_kmap_build(const HashTable* in, const HashTable* h, KernelMap* 
   const int g = grid_for(m->n, 256);
   // the signature's features: the offsets (V <= 32) or the coarse directions
   const unsigned* feat = m->rowdir ? m->rowdir : m->rowmask;
-  SC_LAUNCH("sig_count", s, k_sig_count<<<g, 256, 0, s>>>(feat, m->n, m->sig_sel, m->sigbuckets));
+  const int wl2 = kmap_sig_window_log2();
+  SC_LAUNCH("sig_count", s, k_sig_count<<<g, 256, 0, s>>>(feat, m->n, m->sig_sel, m->sigbuckets, wl2));
   SC_LAUNCH("sig_partials", s, k_order_partials<<<chunks, 256, 0, s>>>(m->sigbuckets, partial));
   SC_LAUNCH("sig_scan", s, k_order_apply<<<chunks, 256, 0, s>>>(m->sigbuckets, partial));
   SC_LAUNCH("sig_scatter", s,
             k_sig_scatter<<<g, 256, 0, s>>>(feat, m->order, m->n, m->sig_sel, m->sigbuckets, m->perm,
-                                            m->conv_order));
+                                            m->conv_order, wl2));
   const int pg = grid_for(((m->n + 127) / 128) * 32, 256);
   if (m->rowdir)
     SC_LAUNCH("sig_present", s, k_sig_present<4><<<pg, 256, 0, s>>>(m->perm, m->rowmask, m->n, (V - 1) / 2, m->present));
@@ -1300,12 +1318,12 @@ sc_status launch_kmap_build(const HashTable* in, const HashTable* h, KernelMap* 
     const unsigned pmask = part == 0 ? ((1u << m->split_at) - 1u) : ~((1u << m->split_at) - 1u);
     e = cudaMemsetAsync(m->sigbuckets, 0, sizeof(int) * nsig, s);
     if (e != cudaSuccess) return set_cuda_error(e, "signature bucket clear");
-    SC_LAUNCH("sig_count", s, k_sig_count<<<g, 256, 0, s>>>(feat, m->n, sel, m->sigbuckets));
+    SC_LAUNCH("sig_count", s, k_sig_count<<<g, 256, 0, s>>>(feat, m->n, sel, m->sigbuckets, wl2));
     SC_LAUNCH("sig_partials", s, k_order_partials<<<chunks, 256, 0, s>>>(m->sigbuckets, partial));
     SC_LAUNCH("sig_scan", s, k_order_apply<<<chunks, 256, 0, s>>>(m->sigbuckets, partial));
     SC_LAUNCH("sig_scatter", s,
               k_sig_scatter<<<g, 256, 0, s>>>(feat, m->order, m->n, sel, m->sigbuckets, m->part_perm[part],
-                                              m->part_order[part]));
+                                              m->part_order[part], wl2));
     SC_LAUNCH("sig_present", s,
               k_sig_present<1><<<pg, 256, 0, s>>>(m->part_perm[part], m->rowmask, m->n, (V - 1) / 2,
                                                   m->part_present[part], pmask, part == 0 ? 1 : 0));
