@@ -205,7 +205,7 @@ sc_status sc_hash_coords(sc_hash h, int32_t* d_coords, sc_stream stream);
  *
  * Signature sort (V <= 128; for n >= 262144 or with SC_KMAP_SORT): inside
  * windows of 524288 consecutive rows of that order, the convolution's rows
- * are counting-sorted by a 16-bit signature, which of the 16 least frequent
+ * are counting-sorted by a 20-bit signature, which of the 20 least frequent
  * features (over the whole map) the row has a neighbour under.  The
  * features are the offsets when V <= 32, else the 26 coarse directions
  * (sign(dx), sign(dy), sign(dz)), a feature's frequency being the tuple

@@ -54,7 +54,7 @@ namespace {
 
 constexpr int kThreads = 256;    // threads per map-build block
 constexpr int kLookups = 2;      // hash lookups in flight per map-build thread
-constexpr int kSigBits = 16;     // signature sort: rare offsets in a row's key
+constexpr int kSigBits = 20;     // signature sort: rare features in a row's key
 // rows per signature-sort window: 524,288 (measured against 2^15 .. 2^20:
 // the batched-LiDAR stack 3.18 ms at 2^16 against 2.96 ms, the 1M-voxel
 // layer 293 against 282 us, the 2M-voxel 5x5x5 layer 3.02 against 2.99 ms)
