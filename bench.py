@@ -400,8 +400,10 @@ def oracle_layer_inputs(w, s):
 
 
 def oracle_sampled_plan(w, s, seconds: float):
-    """Sizes a bounded sample of the oracle's work on the workload so that
-    one pass takes about `seconds`: returns (inputs, rows, t_table)."""
+    """Sizes a bounded sample of the oracle's work on the workload: the
+    coordinate table over all N, timed on its own (median of three builds),
+    and evenly spaced output rows whose layer outputs take about `seconds`
+    against a table built once.  Returns (table, inputs, rows, t_table)."""
     import oracle
     oracle.build()
     ins = oracle_layer_inputs(w, s)
@@ -411,46 +413,49 @@ def oracle_sampled_plan(w, s, seconds: float):
         oracle.hash_only(s.coords, s.ndim, w.K, s.dims)
         t_tab.append(time.perf_counter() - t0)
     t_table = statistics.median(t_tab)
-    probe = np.linspace(0, s.n - 1, min(s.n, 256)).astype(np.int64)
+    table = oracle.Table(s.coords, s.ndim, w.K, s.dims)
+    # at least 64 rows per thread, so every thread of the oracle's loop works
+    kmin = min(s.n, 64 * max(1, oracle.max_threads()))
+    probe = np.linspace(0, s.n - 1, kmin).astype(np.int64)
     per_row = 0.0
     for f, W in ins:
         t0 = time.perf_counter()
-        oracle.subm_conv(s.coords, f, W, s.ndim, w.K, s.dims, rows=probe)
-        per_row += max(time.perf_counter() - t0 - t_table, 1e-7) / len(probe)
-    k = int(max(256, min(s.n, (seconds - t_table) / max(per_row, 1e-9))))
+        table.subm_conv(f, W, rows=probe)
+        per_row += (time.perf_counter() - t0) / len(probe)
+    k = int(max(kmin, min(s.n, seconds / max(per_row, 1e-12))))
     rows = np.linspace(0, s.n - 1, k).astype(np.int64)
-    return ins, rows, t_table
+    return table, ins, rows, t_table
 
 
-def oracle_sampled_pass(w, s, ins, rows, t_table) -> float:
+def oracle_sampled_pass(w, s, table, ins, rows, t_table) -> float:
     """One oracle pass on the sample, scaled to the whole scene (seconds):
-    the coordinate table over all N, then for each sampled output row its
-    V neighbour lookups (the row of the map) and its fp64 output, layer by
-    layer.  Each layer call rebuilds the table, so the scaled time is
-    t_table + sum over layers of (t_layer - t_table) * N / k."""
-    import oracle
+    t_table (the coordinate table over all N) plus, layer by layer, the time
+    of the sampled rows' V neighbour lookups (their map rows) and fp64
+    outputs against the kept table, scaled by N / k."""
     total = t_table
     for f, W in ins:
         t0 = time.perf_counter()
-        oracle.subm_conv(s.coords, f, W, s.ndim, w.K, s.dims, rows=rows)
-        total += max(time.perf_counter() - t0 - t_table, 0.0) * s.n / len(rows)
+        table.subm_conv(f, W, rows=rows)
+        total += (time.perf_counter() - t0) * s.n / len(rows)
     return total
 
 
 def oracle_sample_text(w, s, k: int) -> str:
     V = w.K ** s.ndim
     nl = len(w.channels) - 1
-    return (f"coordinate table (hash) over all N={s.n}, then for {k} evenly spaced output rows the row's {V} "
-            f"neighbour lookups (its map row) and its fp64 output in each of the {nl} layer(s); time scaled to N "
-            f"as t_table + t_rows * N / {k}; phases: hash + map + layers, as in the GPU step")
+    return (f"coordinate table (hash) over all N={s.n}, its build timed on its own (median of 3, t_table); "
+            f"then for {k} evenly spaced output rows the row's {V} neighbour lookups (its map row) and its "
+            f"fp64 output in each of the {nl} layer(s), against that table; time scaled to N as "
+            f"t_table + t_rows * N / {k}; phases: hash + map + layers, as in the GPU step")
 
 
 def cpu_oracle_sampled(w, s, seconds: float):
     """cpu_baseline of the GPU line: the oracle on a bounded sample."""
     import oracle
-    ins, rows, t_table = oracle_sampled_plan(w, s, seconds)
     t0 = time.perf_counter()
-    t = oracle_sampled_pass(w, s, ins, rows, t_table)
+    table, ins, rows, t_table = oracle_sampled_plan(w, s, seconds)
+    t = oracle_sampled_pass(w, s, table, ins, rows, t_table)
+    table.close()
     el = time.perf_counter() - t0
     return {"value": round(s.n / t / 1e6, 4), "unit": "Mvoxels/s", "cores": oracle.max_threads(),
             "host_cpus": os.cpu_count(), "cpu_model": cpu_model(), "kind": "oracle",
@@ -495,12 +500,14 @@ def workload_config(w, s, M: int, world: int, layer_type: str = "submanifold", s
 def run_reference(args):
     """The reference arm: the CPU oracle, as it stands, on this host's cores.
 
-    Each step is one oracle pass on a bounded sample of the workload (the
-    coordinate table over the whole scene, then for a fixed set of evenly
-    spaced output rows their map rows and fp64 outputs in every layer),
-    scaled to the whole scene (oracle_sampled_pass).  The sample is sized so
-    that warm-up plus timed steps take a few minutes.  |M| for the config is
-    counted from the oracle's own map (outside the timed steps).
+    Each step is one oracle pass on a bounded sample of the workload, the
+    same estimate as the GPU line's cpu_baseline: the coordinate table's
+    build time over the whole scene (timed once, before the steps), plus,
+    for a fixed set of evenly spaced output rows, their map rows and fp64
+    outputs in every layer against that table, scaled to the whole scene
+    (oracle_sampled_pass).  The sample is sized so that warm-up plus timed
+    steps take a few minutes.  |M| for the config is counted from the
+    oracle's own map (outside the timed steps).
     """
     rank, world, _ = dist_env()
     if rank != 0:
@@ -510,10 +517,11 @@ def run_reference(args):
     w, s = make_workload(args.workload, 0, args.scale)
     M = int((oracle.kmap(s.coords, s.ndim, w.K, s.dims) >= 0).sum())
     budget = 150.0 / max(1, args.steps + args.warmup)
-    ins, rows, t_table = oracle_sampled_plan(w, s, budget)
+    table, ins, rows, t_table = oracle_sampled_plan(w, s, budget)
     for _ in range(args.warmup):
-        oracle_sampled_pass(w, s, ins, rows, t_table)
-    times = [oracle_sampled_pass(w, s, ins, rows, t_table) for _ in range(args.steps)]
+        oracle_sampled_pass(w, s, table, ins, rows, t_table)
+    times = [oracle_sampled_pass(w, s, table, ins, rows, t_table) for _ in range(args.steps)]
+    table.close()
     ms = 1e3 * statistics.mean(times)
     value = s.n / (ms / 1e3) / 1e6
     line = {

@@ -84,6 +84,12 @@ def _load():
         lib.oracle_conv_bwd_weight.restype = I
         lib.oracle_conv_bwd_data.argtypes = [P, I64, P, I64, I, I, I, P, P, P, I, I, P, I]
         lib.oracle_conv_bwd_data.restype = I
+        lib.oracle_table_build.argtypes = [P, I64, I, I, P, ctypes.POINTER(ctypes.c_int)]
+        lib.oracle_table_build.restype = P
+        lib.oracle_table_subm_conv.argtypes = [P, P, P, I, I, I, P, I64, P, I]
+        lib.oracle_table_subm_conv.restype = I
+        lib.oracle_table_free.argtypes = [P]
+        lib.oracle_table_free.restype = None
         _lib = lib
     return _lib
 
@@ -184,6 +190,54 @@ def subm_conv(coords, feats, W, ndim: int, K: int, dims, relu: bool = False,
     if st:
         raise OracleError(st)
     return out
+
+
+class Table:
+    """The coordinate table (step 1) built once and kept, so that layer
+    outputs of listed rows can be computed against it repeatedly: used to
+    time the table and the rows apart.  subm_conv here equals the module's
+    subm_conv for the same arguments."""
+
+    def __init__(self, coords, ndim: int, K: int, dims):
+        self._c = _coords(coords)  # the table refers to these coordinates
+        self.n = self._c.shape[0]
+        self.ndim, self.K = ndim, K
+        st = ctypes.c_int(0)
+        self._h = _load().oracle_table_build(_ptr(self._c), self.n, ndim, K, _ptr(_dims(dims)), ctypes.byref(st))
+        if not self._h:
+            raise OracleError(st.value)
+
+    def subm_conv(self, feats, W, relu: bool = False, rows=None, threads: int = 0) -> np.ndarray:
+        f = np.ascontiguousarray(np.asarray(feats, dtype=np.float64).reshape(self.n, -1))
+        w = np.ascontiguousarray(np.asarray(W, dtype=np.float64))
+        V, c_in, c_out = w.shape
+        if V != volume(self.ndim, self.K) or f.shape[1] != c_in:
+            raise OracleError(1)
+        r = None if rows is None else np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        nrows = self.n if r is None else r.shape[0]
+        out = np.empty((nrows, c_out), dtype=np.float64)
+        st = _load().oracle_table_subm_conv(self._h, _ptr(f), _ptr(w), c_in, c_out, int(bool(relu)), _ptr(r),
+                                            nrows, _ptr(out), threads)
+        if st:
+            raise OracleError(st)
+        return out
+
+    def close(self) -> None:
+        if self._h:
+            _load().oracle_table_free(self._h)
+            self._h = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def subm_conv_bwd_data(coords, gout, W, ndim: int, K: int, dims, rows=None, threads: int = 0) -> np.ndarray:

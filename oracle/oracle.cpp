@@ -136,6 +136,42 @@ int threads_to_use(int nthreads) {
 #endif
 }
 
+// Output features of the listed rows against a built table (step 2's
+// lookups and step 3's accumulation; see oracle_subm_conv).
+int conv_rows(const Problem& P, const double* feats, const double* W, int c_in, int c_out, int relu,
+              const int64_t* rows, int64_t nrows, double* out, int nthreads) {
+  const int64_t n = P.n;
+  const int ndim = P.ndim, K = P.K;
+  const int V = P.volume;
+  std::vector<int> offs(size_t(V) * 3);
+  for (int v = 0; v < V; ++v) offset_of(v, ndim, K, &offs[3 * v]);
+  for (int64_t k = 0; k < nrows; ++k)
+    if (rows && (rows[k] < 0 || rows[k] >= n)) return OR_BAD_ARG;
+  const int nt = threads_to_use(nthreads);
+  // small chunks: a sample of a few hundred rows per thread still spreads
+  // evenly over the threads (rows are independent; the result is the same)
+#pragma omp parallel for schedule(dynamic, 4) num_threads(nt)
+  for (int64_t k = 0; k < nrows; ++k) {
+    const int64_t q = rows ? rows[k] : k;
+    double* acc = out + k * c_out;
+    for (int co = 0; co < c_out; ++co) acc[co] = 0.0;
+    for (int v = 0; v < V; ++v) {
+      const int32_t p = neighbour(P, q, &offs[3 * v]);
+      if (p < 0) continue;
+      const double* f = feats + int64_t(p) * c_in;
+      const double* w = W + int64_t(v) * c_in * c_out;
+      for (int ci = 0; ci < c_in; ++ci) {
+        const double a = f[ci];
+        const double* wrow = w + int64_t(ci) * c_out;
+        for (int co = 0; co < c_out; ++co) acc[co] += a * wrow[co];
+      }
+    }
+    if (relu)
+      for (int co = 0; co < c_out; ++co) acc[co] = acc[co] > 0.0 ? acc[co] : 0.0;
+  }
+  return OR_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -169,32 +205,7 @@ int oracle_subm_conv(const int32_t* coords, int64_t n, int ndim, int K, const in
   if (st) return st;
   if (c_in < 1 || c_out < 1 || !W || (n > 0 && !feats) || !out) return OR_BAD_ARG;
   if (!rows) nrows = n;
-  const int V = P.volume;
-  std::vector<int> offs(size_t(V) * 3);
-  for (int v = 0; v < V; ++v) offset_of(v, ndim, K, &offs[3 * v]);
-  for (int64_t k = 0; k < nrows; ++k)
-    if (rows && (rows[k] < 0 || rows[k] >= n)) return OR_BAD_ARG;
-  const int nt = threads_to_use(nthreads);
-#pragma omp parallel for schedule(dynamic, 64) num_threads(nt)
-  for (int64_t k = 0; k < nrows; ++k) {
-    const int64_t q = rows ? rows[k] : k;
-    double* acc = out + k * c_out;
-    for (int co = 0; co < c_out; ++co) acc[co] = 0.0;
-    for (int v = 0; v < V; ++v) {
-      const int32_t p = neighbour(P, q, &offs[3 * v]);
-      if (p < 0) continue;
-      const double* f = feats + int64_t(p) * c_in;
-      const double* w = W + int64_t(v) * c_in * c_out;
-      for (int ci = 0; ci < c_in; ++ci) {
-        const double a = f[ci];
-        const double* wrow = w + int64_t(ci) * c_out;
-        for (int co = 0; co < c_out; ++co) acc[co] += a * wrow[co];
-      }
-    }
-    if (relu)
-      for (int co = 0; co < c_out; ++co) acc[co] = acc[co] > 0.0 ? acc[co] : 0.0;
-  }
-  return OR_OK;
+  return conv_rows(P, feats, W, c_in, c_out, relu, rows, nrows, out, nthreads);
 }
 
 // Gradient with respect to the input features of the layer above (without
@@ -282,6 +293,31 @@ int oracle_hash_only(const int32_t* coords, int64_t n, int ndim, int K, const in
 
 // Number of threads the OpenMP runtime would use by default.
 int oracle_max_threads(void) { return threads_to_use(0); }
+
+// The coordinate table (step 1) built once and kept, and layer outputs of
+// listed rows computed against it: lets a caller time the table and the rows
+// apart.  coords must stay alive and unchanged while the table lives.
+void* oracle_table_build(const int32_t* coords, int64_t n, int ndim, int K, const int32_t* dims, int* status) {
+  Problem* P = new Problem;
+  const int st = setup(*P, coords, n, ndim, K, dims);
+  if (status) *status = st;
+  if (st) {
+    delete P;
+    return nullptr;
+  }
+  return P;
+}
+
+int oracle_table_subm_conv(const void* table, const double* feats, const double* W, int c_in, int c_out, int relu,
+                           const int64_t* rows, int64_t nrows, double* out, int nthreads) {
+  if (!table) return OR_BAD_ARG;
+  const Problem& P = *static_cast<const Problem*>(table);
+  if (c_in < 1 || c_out < 1 || !W || (P.n > 0 && !feats) || !out) return OR_BAD_ARG;
+  if (!rows) nrows = P.n;
+  return conv_rows(P, feats, W, c_in, c_out, relu, rows, nrows, out, nthreads);
+}
+
+void oracle_table_free(void* table) { delete static_cast<Problem*>(table); }
 
 }  // extern "C"
 

@@ -161,3 +161,19 @@ def test_reference_arm_prints_one_json_line():
     assert cfg["N"] == s.n and cfg["map_size"] == int((oracle.kmap(s.coords, 3, 3, s.dims) >= 0).sum())
     assert cfg == bench.workload_config(w, s, cfg["map_size"], 1)
     assert "hash + map + layers" in cb["sample"]
+
+
+def test_the_two_oracle_timings_estimate_the_same_quantity():
+    """cpu_baseline (one large sample) and the reference arm's steps (small
+    samples) time the oracle the same way: the coordinate table's build once,
+    the sampled rows against a kept table, scaled to N.  Their estimates of
+    the whole-scene rate agree within timing noise."""
+    import statistics
+    w, s = bench.make_workload(1, 0, 0.3)
+    cb = bench.cpu_oracle_sampled(w, s, 1.0)
+    table, ins, rows, t_table = bench.oracle_sampled_plan(w, s, 0.02)
+    ref = statistics.median(s.n / bench.oracle_sampled_pass(w, s, table, ins, rows, t_table) / 1e6
+                            for _ in range(9))
+    table.close()
+    assert len(rows) < s.n
+    assert 0.6 < ref / cb["value"] < 1.6, (ref, cb["value"])

@@ -29,8 +29,8 @@ MUTATIONS = [
      "for (int v = 0; v < V; ++v) {\n      const int32_t p = neighbour(P, q, &offs[3 * v]);",
      "for (int v = 0; v < V - 1; ++v) {\n      const int32_t p = neighbour(P, q, &offs[3 * v]);"),
     ("ReLU ignored",
-     "    if (relu)\n      for (int co = 0; co < c_out; ++co) acc[co] = acc[co] > 0.0 ? acc[co] : 0.0;\n  }\n  return OR_OK;\n}\n\n// Gradient",
-     "    if (relu && false)\n      for (int co = 0; co < c_out; ++co) acc[co] = acc[co] > 0.0 ? acc[co] : 0.0;\n  }\n  return OR_OK;\n}\n\n// Gradient"),
+     "    if (relu)\n      for (int co = 0; co < c_out; ++co) acc[co] = acc[co] > 0.0 ? acc[co] : 0.0;\n  }\n  return OR_OK;\n}\n\n}  // namespace",
+     "    if (relu && false)\n      for (int co = 0; co < c_out; ++co) acc[co] = acc[co] > 0.0 ? acc[co] : 0.0;\n  }\n  return OR_OK;\n}\n\n}  // namespace"),
     ("duplicate coordinates merged instead of rejected",
      "if (!ins.second) return OR_DUPLICATE;",
      "if (!ins.second) continue;"),

@@ -298,6 +298,11 @@ def test_conv_equals_dense_conv(ndim, K, dims, n, batches, cin, cout):
     got = oracle.subm_conv(coords, f, W, ndim, K, dims)
     want = dense_conv_reference(coords, f, W, ndim, K, dims)
     np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
+    # the kept-table entry point (used to time the oracle) gives the same rows
+    with oracle.Table(coords, ndim, K, dims) as t:
+        np.testing.assert_allclose(t.subm_conv(f, W), want, rtol=1e-12, atol=1e-12)
+        rows = np.arange(coords.shape[0])[::-3]
+        np.testing.assert_allclose(t.subm_conv(f, W, rows=rows), want[rows], rtol=1e-12, atol=1e-12)
 
 
 def test_conv_single_site_two_sites_linearity_relu():
