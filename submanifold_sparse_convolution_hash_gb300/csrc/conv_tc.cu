@@ -423,8 +423,18 @@ __global__ void __launch_bounds__((NPW + 6) * 32, NPW == 4 ? 3 : (NPW == 8 ? 2 :
       const uint32_t b_lo0 = static_cast<uint32_t>(smem_desc(smem_u32(sB), SBO, LAYOUT));
       uint32_t it = 0;
       int j = 0;
+      // output-stationary: each unit's offset mask is loaded one unit ahead,
+      // so the issuer does not wait on it when the unit's first stage is
+      // already full (measured: 100k voxels 37.9 -> 37.0 us; no change at
+      // 1M and 2M voxels)
+      uint4 m_nx = make_uint4(0, 0, 0, 0);
+      if (MODE == kOutputStationary && static_cast<int>(blockIdx.x) < p.num_units) m_nx = unit_mask<T>(p, blockIdx.x);
       for (int u = blockIdx.x; u < p.num_units && !*s_abort; u += gridDim.x, ++j) {
-        const int nkb = unit_kblocks<MODE, T>(p, u, P);
+        int nkb = P;
+        if (MODE == kOutputStationary) {
+          nkb = (__popc(m_nx.x) + __popc(m_nx.y) + __popc(m_nx.z) + __popc(m_nx.w)) * P;
+          if (u + static_cast<int>(gridDim.x) < p.num_units) m_nx = unit_mask<T>(p, u + gridDim.x);
+        }
         const int b = j % NB;
         if (!mbar_wait(acce0 + 8 * b, ((j / NB) & 1) ^ 1, s_abort)) {
           *s_abort = 1;
