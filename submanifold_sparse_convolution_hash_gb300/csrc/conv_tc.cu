@@ -499,6 +499,53 @@ __global__ void __launch_bounds__((NPW + 6) * 32, NPW == 4 ? 3 : (NPW == 8 ? 2 :
           else if (MODE == kOutputStationary && p.order) dst_row = __ldg(p.order + t.row0 + r);
           else dst_row = static_cast<int>(t.row0 + r);
         }
+        if (MODE == kOutputStationary && p.epi == 0 && (p.c_out & 31) == 0) {
+          // 32 columns at a time, transposed across groups of four lanes so
+          // that a store instruction writes 64 contiguous bytes of each of 8
+          // rows (instead of 16 bytes of each of 32): lane 4 g + c stores
+          // 16-byte chunk c of rows 4 g + i, i = 0..3
+          int drow[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) drow[i] = __shfl_sync(0xffffffffu, dst_row, (lane & ~3) + i);
+          const int c = lane & 3;
+          for (int c0 = 0; c0 < p.c_out; c0 += 32) {
+            float a[32];
+            tmem_ld32(trow + static_cast<uint32_t>(c0), a);
+            if (p.relu) {
+#pragma unroll
+              for (int k = 0; k < 32; ++k) a[k] = fmaxf(a[k], 0.0f);
+            }
+            uint4 x[4];  // x[k]: columns c0 + 8 k .. c0 + 8 k + 7 of this lane's row
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              x[k] = make_uint4(pack2<BF16>(a[8 * k], a[8 * k + 1]), pack2<BF16>(a[8 * k + 2], a[8 * k + 3]),
+                                pack2<BF16>(a[8 * k + 4], a[8 * k + 5]), pack2<BF16>(a[8 * k + 6], a[8 * k + 7]));
+            // butterfly over lane distances 2 and 1: afterwards lane 4 g + c
+            // holds chunk c of row 4 g + i in x[i]
+#pragma unroll
+            for (int m = 2; m >= 1; m >>= 1) {
+              const bool up = (lane & m) != 0;
+#pragma unroll
+              for (int lo = 0; lo < 4; ++lo) {
+                if (lo & m) continue;
+                const int hi = lo | m;
+                const uint4 snd = up ? x[lo] : x[hi];
+                uint4 rcv;
+                rcv.x = __shfl_xor_sync(0xffffffffu, snd.x, m);
+                rcv.y = __shfl_xor_sync(0xffffffffu, snd.y, m);
+                rcv.z = __shfl_xor_sync(0xffffffffu, snd.z, m);
+                rcv.w = __shfl_xor_sync(0xffffffffu, snd.w, m);
+                if (up) x[lo] = rcv;
+                else x[hi] = rcv;
+              }
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              if (drow[i] >= 0)
+                *reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(drow[i]) * p.c_out + c0 + 8 * c) * 2) = x[i];
+          }
+          continue;
+        }
         for (int c0 = 0; c0 < p.c_out; c0 += 16) {
           float a[16];
           tmem_ld16(trow + static_cast<uint32_t>(c0), a);
