@@ -845,8 +845,11 @@ def run_extras(args):
     strided) of the same workload, each measured by a child run of this
     script with the same timing rules (L2 flushed per step, CUDA events),
     after this run's own timed steps.  Returns their key figures."""
+    # up to 200 timed steps: a stride-2 step at 1M voxels is 0.5 ms (with its
+    # host read-back of the output count), and 20 of them read up to 4x slow
+    # from one host stall
     base = [sys.executable, os.path.join(ROOT, "bench.py"), "--workload", str(args.workload), "--scale",
-            str(args.scale), "--steps", str(min(args.steps, 20)), "--warmup", str(args.warmup), "--no-e2e",
+            str(args.scale), "--steps", str(min(args.steps, 200)), "--warmup", str(args.warmup), "--no-e2e",
             "--no-cpu-baseline", "--no-extras"]
     keys = ("value", "ms_per_step", "layer_ms", "layer_roofline_frac", "layer_unique_roofline_frac",
             "wgrad_roofline_frac", "kmap_build_ms", "clocks")
