@@ -40,7 +40,9 @@
 //              issues tcgen05.mma (M = 128, N = C_out, K = 16) and commits.
 //   4 warps    epilogue: TMEM lane quadrant (warp % 4) -> registers -> global,
 //              overlapping the next tile's mainloop through the second
-//              accumulator.
+//              accumulator; output rows are transposed across groups of four
+//              lanes, so each store instruction writes 64 contiguous bytes of
+//              8 rows.
 // The row gathers use the load/store path: a TMA tile::gather4 moves four
 // rows per instruction but its row rate, not its byte rate, bounds it, and
 // for 32-256 byte rows that rate is several times below what cp.async from
