@@ -48,10 +48,11 @@ import numpy as np
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 # the kernels of the map build (hash insert, output set, row order, map,
-# signature sort): their event-timed sum is the step's map-build kernel time
+# signature sort, the fused layer's tile table): their event-timed sum is the
+# step's map-build kernel time
 MAP_KERNELS = ("hash_insert", "out_mark", "out_count", "out_scan", "out_number", "order_count", "order_partials",
                "order_apply", "order_scatter", "kmap_clear", "kmap_build", "kmap_masks", "sig_count", "sig_partials",
-               "sig_scan", "sig_scatter", "sig_present")
+               "sig_scan", "sig_scatter", "sig_present", "tile_table")
 sys.path.insert(0, ROOT)
 
 METRIC = "subm-conv layer effective TFLOP/s, Mvoxels/s & % roofline; kernel-map build ms"
@@ -92,6 +93,9 @@ def parse_args():
     ap.add_argument("--kmap-split", action="store_true",
                     help="also build the row orders of column splitting (K^ndim <= 32), so each layer's measured "
                          "variant choice includes the split kernel")
+    ap.add_argument("--kmap-tile-table", choices=["auto", "on", "off"], default="auto",
+                    help="build the fused layer's tile-transposed index table with the map (SC_KMAP_TILE_TABLE): "
+                         "auto = when one map serves several layers (the eight-layer stack), else not")
     return ap.parse_args()
 
 
@@ -134,6 +138,9 @@ def algo_bytes_step(kernel: str, N: int, V: int, M: int, layers, s: int, ntiles:
         # pass (reads the table once, writes the tile masks)
         "kmap_clear": 4 * No * ((V - 1) // 2),
         "kmap_masks": 4 * No * V + 16 * ((No + 127) // 128),
+        # the fused layer's tile-transposed table: the table and the row
+        # order read, the same entries written in tile order
+        "tile_table": 8 * No * V + 4 * No,
         "order_count": 8 * N,
         "order_scatter": 8 * N + 4 * N,
         "pack_weights": sum(2 * V * ci * co * s for ci, co in conv_layers),
@@ -590,6 +597,9 @@ def run_ours(args):
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
     sort_arg = {"auto": None, "on": True, "off": False}[args.kmap_sort]
+    # the tile table pays when one map serves several layers
+    tile_table = (args.kmap_tile_table == "on" or (args.kmap_tile_table == "auto" and len(layers) > 1)) \
+        and not args.kmap_split and w.K ** s.ndim <= 128
 
     def build_map(c, sync):
         """hash -> kernel map (submanifold), or hash -> output set -> map
@@ -597,9 +607,10 @@ def run_ours(args):
         h = sc.sc_hash_build(c)
         if not general:
             return (h,), sc.sc_kmap_build(h, s.ndim, w.K, s.dims, sync=sync, half=args.kmap_half,
-                                          split=args.kmap_split, sort=sort_arg)
+                                          split=args.kmap_split, sort=sort_arg, tile_table=tile_table)
         ho = sc.sc_hash_build_conv_out(h, s.ndim, w.K, conv_stride, s.dims)
-        return (h, ho), sc.sc_kmap_build_conv(h, ho, s.ndim, w.K, conv_stride, s.dims, sync=sync, sort=sort_arg)
+        return (h, ho), sc.sc_kmap_build_conv(h, ho, s.ndim, w.K, conv_stride, s.dims, sync=sync, sort=sort_arg,
+                                              tile_table=tile_table)
 
     # variant of each layer chosen from measured time on this map
     hs0, m0 = build_map(coords, True)
@@ -793,7 +804,8 @@ def run_ours(args):
         "config": workload_config(w, s, M, world, args.layer_type, conv_stride, n_out, args.backward, args.scale),
         "run": {"variant": variants, "variant_choice": "given" if args.variant else "measured", "kmap_sync": False,
                 "kmap_probe": "half (mirror symmetry)" if args.kmap_half else "full",
-                "column_split_orders": bool(args.kmap_split), "kmap_sort": args.kmap_sort},
+                "column_split_orders": bool(args.kmap_split), "kmap_sort": args.kmap_sort,
+                "kmap_tile_table": bool(tile_table)},
         "layer_tflops": round(flops / (conv_ms / 1e3) / 1e12, 3) if conv_ms else None,
         "layer_ms": round(conv_ms, 5),
         "layer_roofline_frac": round(conv_roof_s / (conv_ms / 1e3), 4) if conv_ms else None,

@@ -77,6 +77,7 @@ typedef enum { SC_F32 = 0, SC_F16 = 1, SC_BF16 = 2 } sc_dtype;
 #define SC_KMAP_TRANSPOSE 0x2000u /* sc_kmap_build_conv: the transposed map (rows = the layer's inputs) */
 #define SC_KMAP_HALF 0x4000u    /* sc_kmap_build: half probe by mirror symmetry (same map, another build) */
 #define SC_KMAP_SPLIT 0x8000u   /* sc_kmap_build, K^ndim <= 32: row orders for column splitting (see below) */
+#define SC_KMAP_TILE_TABLE 0x10000u /* K^ndim <= 128: also the fused layer's tile-transposed index table (see below) */
 
 typedef struct sc_hash_s* sc_hash;
 typedef struct sc_kmap_s* sc_kmap;
@@ -194,7 +195,8 @@ sc_status sc_hash_coords(sc_hash h, int32_t* d_coords, sc_stream stream);
  *           SC_KMAP_NO_SORT, SC_KMAP_HALF (build by the half probe: the
  *           offsets after the centre are looked up and each hit is mirrored
  *           by symmetry, "Sparse inputs and sparse convolution", section "A
- *           symmetry you can check"; the same map), SC_KMAP_SPLIT (below).
+ *           symmetry you can check"; the same map), SC_KMAP_SPLIT (below),
+ *           SC_KMAP_TILE_TABLE (below).
  *
  * Locality order: for n >= 262144 (or with SC_KMAP_ORDER) the build first
  * sorts the points into spatially compact groups (a counting sort on the top
@@ -225,6 +227,18 @@ sc_status sc_hash_coords(sc_hash h, int32_t* d_coords, sc_stream stream);
  * partial sums, the second adding its own to them and rounding once.  The map
  * itself is unchanged.
  *
+ * Tile table (SC_KMAP_TILE_TABLE, V <= 128, not with SC_KMAP_SPLIT): the
+ * build also writes the fused layer's neighbour indices in that layer's row
+ * order, transposed within each 128-row tile ([ceil(n/128)][V][128] int32,
+ * 4 n V more bytes held by the handle), so that a tile's indices for one
+ * offset are one contiguous 512-byte run.  Every fused layer (and input
+ * gradient) on the map then reads them there instead of nbr.  Results are
+ * unchanged.  It costs one pass over nbr after the build and pays when the
+ * map serves several layers: on a batch of four 120k-point LiDAR scans
+ * (3x3x3) eight layers 32 -> 256 took 2.37 ms instead of 2.65 ms for a 34 us
+ * pass, while a single layer does not recover it (1M voxels 3x3x3: the layer
+ * 25 us faster, the pass 60 us; 2M voxels 5x5x5: 100 us and 388 us).
+ *
  * Products, owned by the handle:
  *   nbr      int32 [n, V]: nbr[q*V + idx(d)] = row p with coords[p] =
  *            coords[q] + d, or -1.  Column (V-1)/2 is the identity.
@@ -253,8 +267,9 @@ sc_status sc_kmap_build(sc_hash h, int ndim, int K, const int32_t dims[3], unsig
  * rulebook", section 3 (rulebook grouped by offset).  Unlike a submanifold
  * map the centre offset is searched like the others and has its own list
  * segment; |M| = offs[V].  The map keeps neither hash: both stay owned by
- * the caller.  Flags as for sc_kmap_build except SC_KMAP_HALF and
- * SC_KMAP_SPLIT (SC_ERR_UNSUPPORTED: submanifold maps only); the locality
+ * the caller.  Flags as for sc_kmap_build (SC_KMAP_TILE_TABLE included)
+ * except SC_KMAP_HALF and SC_KMAP_SPLIT (SC_ERR_UNSUPPORTED: submanifold maps
+ * only); the locality
  * order and the signature sort apply to the map's rows (the outputs, or the
  * inputs of a transposed map) as for a submanifold map, except that the sort
  * is on by default only when V > 32 as well.

@@ -28,6 +28,7 @@ SC_KMAP_NO_SORT = 0x1000
 SC_KMAP_TRANSPOSE = 0x2000
 SC_KMAP_HALF = 0x4000
 SC_KMAP_SPLIT = 0x8000
+SC_KMAP_TILE_TABLE = 0x10000
 VARIANTS = {"fused": SC_VARIANT_FUSED, "ws": SC_VARIANT_WS, "simt": SC_VARIANT_SIMT, "split": SC_VARIANT_SPLIT}
 VARIANT_NAMES = {v: k for k, v in VARIANTS.items()}
 _DTYPES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
@@ -269,7 +270,7 @@ def sc_hash_build(coords: torch.Tensor, stream=None, allocator=None) -> Hash:
 
 def sc_kmap_build(h: Hash, ndim: int, K: int, dims, sync: bool = True, order: bool | None = None,
                   sort: bool | None = None, half: bool = False, split: bool = False, stream=None,
-                  allocator=None) -> KernelMap:
+                  allocator=None, tile_table: bool = False) -> KernelMap:
     """Kernel map of a K^ndim submanifold convolution over the hashed points.
 
     order: True / False forces the locality order on / off; None leaves the
@@ -277,7 +278,9 @@ def sc_kmap_build(h: Hash, ndim: int, K: int, dims, sync: bool = True, order: bo
     signature sort of the convolution's rows (default on for n >= 262144 when
     K^ndim <= 128).  half: build it by the half probe (mirror symmetry); the
     map is the same.  split: also compute the row orders of column splitting
-    (K^ndim <= 32), which the "split" layer variant uses."""
+    (K^ndim <= 32), which the "split" layer variant uses.  tile_table: also
+    build the fused layer's tile-transposed index table (K^ndim <= 128),
+    which pays when the map serves several layers."""
     d = (ctypes.c_int32 * 3)(*(list(dims) + [1] * (3 - len(dims))))
     m = ctypes.c_void_p()
     flags = 0 if sync else SC_KMAP_NO_SYNC
@@ -285,6 +288,8 @@ def sc_kmap_build(h: Hash, ndim: int, K: int, dims, sync: bool = True, order: bo
         flags |= SC_KMAP_HALF
     if split:
         flags |= SC_KMAP_SPLIT
+    if tile_table:
+        flags |= SC_KMAP_TILE_TABLE
     if order is True:
         flags |= SC_KMAP_ORDER
     elif order is False:
@@ -314,16 +319,19 @@ def sc_hash_build_conv_out(h: Hash, ndim: int, K: int, stride: int, dims, stream
 
 def sc_kmap_build_conv(h_in: Hash, h_out: Hash, ndim: int, K: int, stride: int, dims, sync: bool = True,
                        order: bool | None = None, sort: bool | None = None, transpose: bool = False, stream=None,
-                       allocator=None) -> KernelMap:
+                       allocator=None, tile_table: bool = False) -> KernelMap:
     """Kernel map of a regular / strided layer: rows = the points of `h_out`,
     neighbours = rows of `h_in` at stride * o + d.  transpose: the transposed
     map (rows = the points of `h_in`, neighbours = the outputs whose windows
-    hold them, at the mirrored offset), which sc_subm_conv_bwd_data takes."""
+    hold them, at the mirrored offset), which sc_subm_conv_bwd_data takes.
+    tile_table: as for sc_kmap_build."""
     d = (ctypes.c_int32 * 3)(*(list(dims) + [1] * (3 - len(dims))))
     m = ctypes.c_void_p()
     flags = 0 if sync else SC_KMAP_NO_SYNC
     if transpose:
         flags |= SC_KMAP_TRANSPOSE
+    if tile_table:
+        flags |= SC_KMAP_TILE_TABLE
     if order is True:
         flags |= SC_KMAP_ORDER
     elif order is False:

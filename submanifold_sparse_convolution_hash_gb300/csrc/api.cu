@@ -620,8 +620,10 @@ sc_status kmap_build_impl(sc_hash hi, sc_hash ho, int ndim, int K, int stride, c
   for (int a = 0; a < 3; ++a)
     if (dims[a] < 1 || dims[a] > 65535) return set_error(SC_ERR_INVALID_ARG, "dims must be in [1, 65535]");
   if (flags & ~(SC_KMAP_NO_SYNC | SC_KMAP_ORDER | SC_KMAP_NO_ORDER | SC_KMAP_SORT | SC_KMAP_NO_SORT | SC_KMAP_TRANSPOSE |
-                SC_KMAP_HALF | SC_KMAP_SPLIT))
+                SC_KMAP_HALF | SC_KMAP_SPLIT | SC_KMAP_TILE_TABLE))
     return set_error(SC_ERR_INVALID_ARG, "unknown kmap flag");
+  if ((flags & SC_KMAP_TILE_TABLE) && (V > 128 || (flags & SC_KMAP_SPLIT)))
+    return set_error(SC_ERR_UNSUPPORTED, "SC_KMAP_TILE_TABLE: K^ndim <= 128, and not with SC_KMAP_SPLIT");
   if ((flags & SC_KMAP_HALF) && !identity)
     return set_error(SC_ERR_UNSUPPORTED, "SC_KMAP_HALF builds submanifold maps only");
   if ((flags & SC_KMAP_ORDER) && (flags & SC_KMAP_NO_ORDER))
@@ -663,6 +665,8 @@ sc_status kmap_build_impl(sc_hash hi, sc_hash ho, int ndim, int K, int stride, c
   const bool sorted = V <= 128 && k.n > 0 &&
                       (split || (flags & SC_KMAP_SORT) || (!(flags & SC_KMAP_NO_SORT) && sort_default));
   const size_t mask_words = V <= 32 ? 1 : 4;
+  const bool tile_table = (flags & SC_KMAP_TILE_TABLE) && k.n > 0;
+  const size_t tiles = static_cast<size_t>((k.n + 127) / 128);
   const size_t nsig = sorted ? static_cast<size_t>(kmap_sig_buckets(k.n)) : 0;
   // every buffer of the map carved from one allocation, each 256-byte aligned
   const size_t n = static_cast<size_t>(k.n);
@@ -695,6 +699,7 @@ sc_status kmap_build_impl(sc_hash hi, sc_hash ho, int ndim, int K, int stride, c
       {reinterpret_cast<void**>(&k.sigbuckets), sorted ? sizeof(int) * (nsig + nsig / 4096 + 1) : 0},
       {reinterpret_cast<void**>(&k.perm), sorted ? sizeof(int) * n : 0},
       {reinterpret_cast<void**>(&k.conv_order), sorted ? sizeof(int) * n : 0},
+      {reinterpret_cast<void**>(&k.tnbr), tile_table ? sizeof(int) * tiles * 128 * V : 0},
   };
   size_t total = 0;
   for (const Part& pt : parts) total += (pt.bytes + 255) & ~size_t(255);

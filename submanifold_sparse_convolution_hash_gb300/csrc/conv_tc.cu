@@ -82,6 +82,7 @@ struct TcParams {
   const int* nbr;            // [n, V]
   const int* order;          // [n] input row of each tile row (null: identity); tiles are runs of 128 rows
   const int* perm;           // [n] table row of each tile row (null: identity; set by the signature sort)
+  const int* tnbr;           // or null: the map's tile-transposed index table, [tiles][V][128] in tile row order
   const uint4* present;      // [tiles]: 128-bit mask of the offsets present in each 128-row tile
   const int* in_rows;        // weight-stationary lists: offset v's at v * n
   const int* out_rows;
@@ -201,7 +202,9 @@ __device__ __forceinline__ int unit_kblocks(const TcParams& p, int u, int P) {
 }
 
 // Register budget: 4 producer warps run three CTAs per SM, 8 run two, 16 one.
-template <int BK, int MODE, bool BF16, int NPW, int T>
+// TT (output-stationary): the neighbour indices come from the map's
+// tile-transposed table (p.tnbr) instead of nbr through perm.
+template <int BK, int MODE, bool BF16, int NPW, int T, bool TT>
 __global__ void __launch_bounds__((NPW + 6) * 32, NPW == 4 ? 3 : (NPW == 8 ? 2 : 1)) k_conv_tc(const TcParams p) {
   constexpr int ROWB = BK * 2;          // bytes per tile row (= swizzle width)
   constexpr int A_PART = kRows * ROWB;  // one 128-row MMA operand of a sub-block
@@ -283,12 +286,18 @@ __global__ void __launch_bounds__((NPW + 6) * 32, NPW == 4 ? 3 : (NPW == 8 ? 2 :
       // so each offset costs one index load per row, issued an offset ahead.
       // this lane's row of the neighbour table (the tile row itself, or the
       // row the signature sort put there)
+      // (TT: this lane's entries in the tile-transposed table, 128 apart per
+      // offset; a warp's rows of one offset are consecutive ints)
       int64_t trow_lane = 0;
-      if (MODE == kOutputStationary && lane < RW && rw0 + lane < t.nrows)
-        trow_lane = p.perm ? static_cast<int64_t>(__ldg(p.perm + t.row0 + rw0 + lane)) : t.row0 + rw0 + lane;
+      if (MODE == kOutputStationary && lane < RW && rw0 + lane < t.nrows) {
+        const int64_t k = t.row0 + rw0 + lane;
+        if constexpr (TT) trow_lane = (k >> 7) * static_cast<int64_t>(V) * 128 + (k & 127);
+        else trow_lane = p.perm ? static_cast<int64_t>(__ldg(p.perm + k)) : k;
+      }
       auto fetch = [&](int vv) -> int {
         const int r = rw0 + lane;
         if (vv >= V || lane >= RW || r >= t.nrows) return -1;
+        if constexpr (MODE == kOutputStationary && TT) return __ldg(p.tnbr + trow_lane + static_cast<int64_t>(vv) * 128);
         if (MODE == kOutputStationary) return __ldg(p.nbr + trow_lane * V + vv);
         if (MODE == kWsScatter) return __ldg(p.in_rows + t.lb + r);
         return static_cast<int>(t.row0 + r);
@@ -367,11 +376,21 @@ __global__ void __launch_bounds__((NPW + 6) * 32, NPW == 4 ? 3 : (NPW == 8 ? 2 :
     // of the neighbour table into L2.
     if (lane == 0) {
       uint32_t it = 0;
-      if (MODE == kOutputStationary && !p.perm && static_cast<int>(blockIdx.x) < p.num_units) {
-        const TileInfo t0 = tile_info<MODE, T>(p, blockIdx.x);
-        const uint32_t bytes = (static_cast<uint32_t>(t0.nrows) * V * 4) & ~15u;
-        if (bytes) bulk_prefetch_l2(p.nbr + t0.row0 * V, bytes);
-      }
+      // each unit's block of neighbour indices into L2: its tiles of the
+      // tile-transposed table, or its rows of nbr when those are contiguous
+      auto prefetch_unit = [&](int uu) {
+        const TileInfo tu = tile_info<MODE, T>(p, uu);
+        if constexpr (TT) {
+          const int nt = (tu.nrows + kRows - 1) / kRows;
+          bulk_prefetch_l2(p.tnbr + (tu.row0 >> 7) * static_cast<int64_t>(V) * 128,
+                           static_cast<uint32_t>(nt) * static_cast<uint32_t>(V) * 512u);
+        } else {
+          const uint32_t bytes = (static_cast<uint32_t>(tu.nrows) * V * 4) & ~15u;
+          if (bytes) bulk_prefetch_l2(p.nbr + tu.row0 * V, bytes);
+        }
+      };
+      if (MODE == kOutputStationary && (TT || !p.perm) && static_cast<int>(blockIdx.x) < p.num_units)
+        prefetch_unit(blockIdx.x);
       for (int u = blockIdx.x; u < p.num_units && !*s_abort; u += gridDim.x) {
         uint4 m = make_uint4(0, 0, 0, 0);
         int bv = tile_info<MODE, T>(p, u).v;
@@ -379,11 +398,7 @@ __global__ void __launch_bounds__((NPW + 6) * 32, NPW == 4 ? 3 : (NPW == 8 ? 2 :
           m = unit_mask<T>(p, u);
           bv = next_present(m, -1, V);
           const int nu = u + gridDim.x;
-          if (nu < p.num_units && !p.perm) {
-            const TileInfo tn = tile_info<MODE, T>(p, nu);
-            const uint32_t bytes = (static_cast<uint32_t>(tn.nrows) * V * 4) & ~15u;
-            if (bytes) bulk_prefetch_l2(p.nbr + tn.row0 * V, bytes);
-          }
+          if (nu < p.num_units && (TT || !p.perm)) prefetch_unit(nu);
         }
         const int nkb = unit_kblocks<MODE, T>(p, u, P);
         int bp = 0;
@@ -754,9 +769,9 @@ bool make_plan(int c_in, int c_out, bool output_stationary, Plan* pl) {
   return true;
 }
 
-template <int BK, int MODE, bool BF16, int NPW, int T>
+template <int BK, int MODE, bool BF16, int NPW, int T, bool TT>
 sc_status launch_tc(const TcParams& prm, const Plan& pl, cudaStream_t s, const char* name) {
-  auto kern = k_conv_tc<BK, MODE, BF16, NPW, T>;
+  auto kern = k_conv_tc<BK, MODE, BF16, NPW, T, TT>;
   constexpr int threads = (NPW + 6) * 32;
   int num_regs = 0;
   sc_status st = kernel_setup(reinterpret_cast<const void*>(kern), pl.smem, &num_regs);
@@ -784,36 +799,44 @@ sc_status launch_tc(const TcParams& prm, const Plan& pl, cudaStream_t s, const c
   return e == cudaSuccess ? SC_OK : set_cuda_error(e, name);
 }
 
-template <int BK, int MODE, bool BF16>
+template <int BK, int MODE, bool BF16, bool TT>
 sc_status launch_npw(const TcParams& prm, const Plan& pl, cudaStream_t s, const char* name) {
   if constexpr (BK == 16) {
-    return pl.npw == 8 ? launch_tc<BK, MODE, BF16, 8, 1>(prm, pl, s, name)
-                       : launch_tc<BK, MODE, BF16, 4, 1>(prm, pl, s, name);
+    return pl.npw == 8 ? launch_tc<BK, MODE, BF16, 8, 1, TT>(prm, pl, s, name)
+                       : launch_tc<BK, MODE, BF16, 4, 1, TT>(prm, pl, s, name);
   } else {
     if constexpr (MODE == kOutputStationary) {
       if (pl.t == 2)
-        return pl.npw == 16 ? launch_tc<BK, MODE, BF16, 16, 2>(prm, pl, s, name)
-                            : launch_tc<BK, MODE, BF16, 8, 2>(prm, pl, s, name);
+        return pl.npw == 16 ? launch_tc<BK, MODE, BF16, 16, 2, TT>(prm, pl, s, name)
+                            : launch_tc<BK, MODE, BF16, 8, 2, TT>(prm, pl, s, name);
     }
     switch (pl.npw) {
-      case 16: return launch_tc<BK, MODE, BF16, 16, 1>(prm, pl, s, name);
-      case 8: return launch_tc<BK, MODE, BF16, 8, 1>(prm, pl, s, name);
-      default: return launch_tc<BK, MODE, BF16, 4, 1>(prm, pl, s, name);
+      case 16: return launch_tc<BK, MODE, BF16, 16, 1, TT>(prm, pl, s, name);
+      case 8: return launch_tc<BK, MODE, BF16, 8, 1, TT>(prm, pl, s, name);
+      default: return launch_tc<BK, MODE, BF16, 4, 1, TT>(prm, pl, s, name);
     }
+  }
+}
+
+template <int MODE, bool TT>
+sc_status dispatch_bk(const TcParams& prm, const Plan& pl, bool bf16, cudaStream_t s, const char* name) {
+  switch (pl.bk) {
+    case 64:
+      return bf16 ? launch_npw<64, MODE, true, TT>(prm, pl, s, name) : launch_npw<64, MODE, false, TT>(prm, pl, s, name);
+    case 32:
+      return bf16 ? launch_npw<32, MODE, true, TT>(prm, pl, s, name) : launch_npw<32, MODE, false, TT>(prm, pl, s, name);
+    default:
+      return bf16 ? launch_npw<16, MODE, true, TT>(prm, pl, s, name) : launch_npw<16, MODE, false, TT>(prm, pl, s, name);
   }
 }
 
 template <int MODE>
 sc_status dispatch_tc(const TcParams& prm, const Plan& pl, bool bf16, cudaStream_t s, const char* name) {
   if (prm.num_units <= 0) return SC_OK;
-  switch (pl.bk) {
-    case 64:
-      return bf16 ? launch_npw<64, MODE, true>(prm, pl, s, name) : launch_npw<64, MODE, false>(prm, pl, s, name);
-    case 32:
-      return bf16 ? launch_npw<32, MODE, true>(prm, pl, s, name) : launch_npw<32, MODE, false>(prm, pl, s, name);
-    default:
-      return bf16 ? launch_npw<16, MODE, true>(prm, pl, s, name) : launch_npw<16, MODE, false>(prm, pl, s, name);
+  if constexpr (MODE == kOutputStationary) {
+    if (prm.tnbr) return dispatch_bk<MODE, true>(prm, pl, bf16, s, name);
   }
+  return dispatch_bk<MODE, false>(prm, pl, bf16, s, name);
 }
 
 sc_status pack_weights(const ConvArgs& a, int bk, uint8_t* img) {
@@ -840,6 +863,7 @@ TcParams base_params(const ConvArgs& a, const Plan& pl, const uint8_t* img) {
   p.nbr = a.m->nbr;
   p.order = a.m->perm ? a.m->conv_order : a.m->order;
   p.perm = a.m->perm;
+  p.tnbr = a.m->tnbr;
   p.present = reinterpret_cast<const uint4*>(a.m->present);
   p.in_rows = a.m->in_rows;
   p.out_rows = a.m->out_rows;
@@ -924,6 +948,7 @@ sc_status conv_fused_split(const ConvArgs& a) {
   for (int part = 0; part < 2 && !st; ++part) {
     TcParams prm = base_params(a, pl, static_cast<const uint8_t*>(img));
     prm.perm = m->part_perm[part];
+    prm.tnbr = nullptr;  // the part's own row order reads nbr
     prm.order = m->part_order[part];
     prm.present = reinterpret_cast<const uint4*>(m->part_present[part]);
     prm.acc = static_cast<float*>(acc);

@@ -906,6 +906,53 @@ __global__ void __launch_bounds__(256) k_unpermute_rows(const int* __restrict__ 
   }
 }
 
+// The fused layer's tile-transposed index table (SC_KMAP_TILE_TABLE):
+// tnbr[(t * V + v) * 128 + r] = nbr[src, v] for the table row src at
+// position t * 128 + r of the layer's row order (perm, or the identity), -1
+// past the last row.  A tile's indices for one offset are then one
+// contiguous 512-byte run instead of 128 loads from rows V * 4 bytes apart.
+// One block per tile: the tile's table rows are staged in shared memory (a
+// warp takes four rows at a time, lanes across each row's V <= 128 entries,
+// all sixteen loads in flight), then the block writes them out offset by
+// offset (V is odd, so the column reads fall in distinct banks).
+__global__ void __launch_bounds__(256) k_tile_table(const int* __restrict__ nbr, const int* __restrict__ perm,
+                                                    int64_t n, int V, int* __restrict__ tnbr) {
+  extern __shared__ int s_t[];  // [128 * V]
+  __shared__ int64_t s_src[128];
+  const int64_t t = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x < 128) {
+    const int64_t k = t * 128 + threadIdx.x;
+    s_src[threadIdx.x] = k < n ? (perm ? static_cast<int64_t>(__ldg(perm + k)) : k) : -1;
+  }
+  __syncthreads();
+  for (int r0 = warp * 4; r0 < 128; r0 += 32) {
+    int x[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int64_t src = s_src[r0 + i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int v = lane + 32 * j;
+        x[i][j] = src >= 0 && v < V ? __ldcs(nbr + src * V + v) : -1;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int v = lane + 32 * j;
+        if (v < V) s_t[(r0 + i) * V + v] = x[i][j];
+      }
+  }
+  __syncthreads();
+  int* dst = tnbr + t * V * 128;
+  for (int e = threadIdx.x; e < V * 128; e += blockDim.x) {
+    const int v = e >> 7, r = e & 127;
+    dst[e] = s_t[r * V + v];
+  }
+}
+
 // The strided lists (offset v at v * n) compacted into CSR order.
 __global__ void __launch_bounds__(256) k_compact_lists(const int* __restrict__ src, const int64_t* __restrict__ offs,
                                                        int64_t n, int* __restrict__ dst) {
@@ -1139,7 +1186,7 @@ sc_status launch_hash_query(const HashTable* h, const int32_t* q, int64_t m, int
   return e == cudaSuccess ? SC_OK : set_cuda_error(e, "hash_query launch");
 }
 
-sc_status launch_kmap_build(const HashTable* in, const HashTable* h, KernelMap* m, cudaStream_t s) {
+static sc_status launch_kmap_steps(const HashTable* in, const HashTable* h, KernelMap* m, cudaStream_t s) {
   const int V = m->V;
   cudaError_t e;
   if (m->n == 0) {
@@ -1331,6 +1378,31 @@ sc_status launch_kmap_build(const HashTable* in, const HashTable* h, KernelMap* 
     if (e != cudaSuccess) return set_cuda_error(e, "split signature sort launch");
   }
   return SC_OK;
+}
+
+
+// The map's kernels, then (SC_KMAP_TILE_TABLE) the fused layer's
+// tile-transposed index table in its final row order.
+sc_status launch_kmap_build(const HashTable* in, const HashTable* h, KernelMap* m, cudaStream_t s) {
+  sc_status st = launch_kmap_steps(in, h, m, s);
+  if (st || !m->tnbr || m->n == 0) return st;
+  const size_t smem = sizeof(int) * 128 * static_cast<size_t>(m->V);
+  if (smem > 48 * 1024) {  // set once per device: the most it asks for (V = 128)
+    static bool done[64] = {false};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64 || !done[dev]) {
+      cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(k_tile_table),
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, 128 * 128 * 4);
+      if (e != cudaSuccess) return set_cuda_error(e, "tile table smem attribute");
+      if (dev >= 0 && dev < 64) done[dev] = true;
+    }
+  }
+  const int64_t tiles = (m->n + 127) / 128;
+  SC_LAUNCH("tile_table", s,
+            (k_tile_table<<<static_cast<unsigned>(tiles), 256, smem, s>>>(m->nbr, m->perm, m->n, m->V, m->tnbr)));
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? SC_OK : set_cuda_error(e, "tile table launch");
 }
 
 sc_status launch_hash_coords(const HashTable* h, int32_t* coords, cudaStream_t s) {

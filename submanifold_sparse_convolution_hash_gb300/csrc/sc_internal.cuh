@@ -102,6 +102,10 @@ struct KernelMap {
   int* sigbuckets = nullptr;         // counting-sort buckets (+ scan partials)
   int* perm = nullptr;               // [n] sorted position -> table row, or null: no sort
   int* conv_order = nullptr;         // [n] sorted position -> input row
+  // SC_KMAP_TILE_TABLE: the fused layer's neighbour indices in its row order
+  // (perm, or the table's own), transposed within each 128-row tile,
+  // [ceil(n/128)][V][128], -1 past the last row; null: the layer reads nbr
+  int* tnbr = nullptr;
   // column splitting (V <= 32): offsets [0, split_at) form part 0 (the
   // centre is the last of them), [split_at, V) part 1; each part has its own
   // signature sort of the rows and tile masks restricted to its offsets

@@ -33,6 +33,9 @@ def test_algorithmic_bytes_of_map_and_gradient_kernels():
     assert bench.algo_bytes_step("kmap_build", N, V, M, [(32, 32)], s, 0, n_out=n_out) == \
         8 * n_out + 4 * n_out * V + 8 * M
     assert bench.algo_bytes_step("no_such_kernel", N, V, M, [(32, 32)], s, 0) is None
+    # the tile-transposed table: table and row order read, table written
+    assert bench.algo_bytes_step("tile_table", N, V, M, [(32, 32)], s, 0) == 8 * N * V + 4 * N
+    assert "tile_table" in bench.MAP_KERNELS
 
 
 def test_recorded_traffic_is_dropped_once_the_source_changes(tmp_path, monkeypatch):
