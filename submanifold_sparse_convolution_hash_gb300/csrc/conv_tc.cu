@@ -52,6 +52,8 @@
 // expiry the CTA latches kDevErrTimeout, stops issuing work, waits (bounded)
 // for what it issued, and still frees its TMEM.
 
+#include <cuda.h>  // CUtensorMap and its encoding enums (the encoder is resolved at run time)
+
 #include <cstdio>
 #include <cstdlib>
 #include <mutex>
@@ -75,8 +77,20 @@ constexpr int kBarriers = 2 * kMaxStages + 5;  // full[S], empty[S], acc_full[2]
 enum Mode { kOutputStationary = 0, kWsScatter = 1, kWsCentre = 2 };
 
 struct TcParams {
+  // wmode 1 / 2: the weights' tensor map (W itself, read by TMA); passed in
+  // the kernel's __grid_constant__ parameter block
+  CUtensorMap wmap;
+  // how the weight loader fetches each (offset, panel) slice of W:
+  //   0: bulk copy from a packed image (wimg)
+  //   1: TMA from W [V][c_in][c_out] (a layer): B MN-major, boxes of wnb
+  //      output channels x BK input channels, wnb-column swizzle
+  //   2: TMA from W [V][c_out][c_in] of the forward layer whose input
+  //      gradient this is (W'[v] = W[V-1-v]^T): B K-major, one box of c_out
+  //      rows x BK channels, the same layout as the packed image
+  int wmode;
+  int wnb;
   const uint8_t* feats;      // [n, c_in] 2-byte elements
-  const uint8_t* wimg;       // packed weight images [V][P][c_out rows][BK*2 bytes]
+  const uint8_t* wimg;       // wmode 0: packed weight images [V][P][c_out rows][BK*2 bytes]
   uint8_t* out;              // output-stationary: [n, c_out] 2-byte elements
   float* acc;                // weight-stationary: fp32 [n, c_out]
   const int* nbr;            // [n, V]
@@ -205,7 +219,8 @@ __device__ __forceinline__ int unit_kblocks(const TcParams& p, int u, int P) {
 // TT (output-stationary): the neighbour indices come from the map's
 // tile-transposed table (p.tnbr) instead of nbr through perm.
 template <int BK, int MODE, bool BF16, int NPW, int T, bool TT>
-__global__ void __launch_bounds__((NPW + 6) * 32, NPW == 4 ? 3 : (NPW == 8 ? 2 : 1)) k_conv_tc(const TcParams p) {
+__global__ void __launch_bounds__((NPW + 6) * 32, NPW == 4 ? 3 : (NPW == 8 ? 2 : 1))
+    k_conv_tc(const __grid_constant__ TcParams p) {
   constexpr int ROWB = BK * 2;          // bytes per tile row (= swizzle width)
   constexpr int A_PART = kRows * ROWB;  // one 128-row MMA operand of a sub-block
   constexpr int A_SUB = T * A_PART;     // one (offset, panel) sub-block of A
@@ -412,8 +427,19 @@ __global__ void __launch_bounds__((NPW + 6) * 32, NPW == 4 ? 3 : (NPW == 8 ? 2 :
           const int gc = min(G, nkb - kb);
           mbar_arrive_expect_tx(full0 + 8 * s, static_cast<uint32_t>(gc * B_SUB));
           for (int g = 0; g < gc; ++g) {
-            bulk_g2s(smem_u32(sB + (s * G + g) * B_SUB), p.wimg + (static_cast<size_t>(bv) * P + bp) * B_SUB,
-                     static_cast<uint32_t>(B_SUB), full0 + 8 * s);
+            const uint32_t dstb = smem_u32(sB + (s * G + g) * B_SUB);
+            if (p.wmode == 1) {
+              // W[v] rows bp * BK .. + BK (input channels), wnb output channels per box
+              const int y = bv * p.c_in + bp * BK;
+              for (int i = 0; i * p.wnb < p.c_out; ++i)
+                tma_load_2d(dstb + static_cast<uint32_t>(i * BK * p.wnb * 2), &p.wmap, i * p.wnb, y, full0 + 8 * s);
+            } else if (p.wmode == 2) {
+              // rows (V-1-v) * c_out .. + c_out of the forward W, channels bp * BK .. + BK
+              tma_load_2d(dstb, &p.wmap, bp * BK, (V - 1 - bv) * p.c_out, full0 + 8 * s);
+            } else {
+              bulk_g2s(dstb, p.wimg + (static_cast<size_t>(bv) * P + bp) * B_SUB, static_cast<uint32_t>(B_SUB),
+                       full0 + 8 * s);
+            }
             if (++bp == P) {
               bp = 0;
               if (MODE == kOutputStationary) bv = next_present(m, bv, V);
@@ -430,14 +456,31 @@ __global__ void __launch_bounds__((NPW + 6) * 32, NPW == 4 ? 3 : (NPW == 8 ? 2 :
   } else if (warp == NPW) {
     // ======================================================= MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = make_idesc(BF16, kRows, p.c_out);
+      // B MN-major (wmode 1: the slice as W holds it, output channels
+      // contiguous) or K-major (the packed image's layout)
+      const bool b_mn = p.wmode == 1;
+      const uint32_t idesc = make_idesc(BF16, kRows, p.c_out) | (b_mn ? (1u << 16) : 0u);
       // descriptor halves: low = start address >> 4 (14 bits; shared memory
-      // is below 256 KB, so offsets add without carry) | LBO 1; high = SBO,
+      // is below 256 KB, so offsets add without carry) | LBO; high = SBO,
       // version 1, swizzle layout
       const uint64_t d0 = smem_desc(smem_u32(sA), SBO, LAYOUT);
       const uint32_t desc_hi = static_cast<uint32_t>(d0 >> 32);
       const uint32_t a_lo0 = static_cast<uint32_t>(d0);
-      const uint32_t b_lo0 = static_cast<uint32_t>(smem_desc(smem_u32(sB), SBO, LAYOUT));
+      uint32_t b_lo0, b_hi, b_step;
+      if (b_mn) {
+        // rows of wnb * 2 bytes (one input channel each), 8-row atoms along
+        // K, boxes of wnb output channels BK rows apart along N; a K = 16
+        // step advances 16 rows
+        const uint32_t rb = static_cast<uint32_t>(p.wnb * 2);
+        const uint64_t bd = smem_desc_mn(smem_u32(sB), BK * rb, 8 * rb, rb == 128 ? 2u : (rb == 64 ? 4u : 6u));
+        b_lo0 = static_cast<uint32_t>(bd);
+        b_hi = static_cast<uint32_t>(bd >> 32);
+        b_step = 16 * rb / 16;
+      } else {
+        b_lo0 = static_cast<uint32_t>(smem_desc(smem_u32(sB), SBO, LAYOUT));
+        b_hi = desc_hi;
+        b_step = 2;  // 16 channels of a K-major row: 32 bytes
+      }
       uint32_t it = 0;
       int j = 0;
       // output-stationary: each unit's offset mask is loaded one unit ahead,
@@ -479,8 +522,8 @@ __global__ void __launch_bounds__((NPW + 6) * 32, NPW == 4 ? 3 : (NPW == 8 ? 2 :
             for (int k = 0; k < BK / 16; ++k) {
 #pragma unroll
               for (int tp = 0; tp < T; ++tp)
-                tc_mma_lohi(d + static_cast<uint32_t>(tp * p.acc_cols), a_lo + tp * (A_PART >> 4) + 2 * k,
-                            b_lo + 2 * k, desc_hi, idesc, accumulate);
+                tc_mma_lohi2(d + static_cast<uint32_t>(tp * p.acc_cols), a_lo + tp * (A_PART >> 4) + 2 * k, desc_hi,
+                             b_lo + b_step * k, b_hi, idesc, accumulate);
               accumulate = 1;
             }
           }
@@ -712,7 +755,8 @@ size_t plan_smem(const Plan& pl, size_t stage_bytes) {  // stage_bytes: one stag
 // Developer overrides for measurement sweeps (environment, read per call):
 // SC_DEV_BK, SC_DEV_T, SC_DEV_STAGES, SC_DEV_GROUP, SC_DEV_NPW, SC_DEV_NBUF, SC_DEV_CPS
 // (an upper bound), SC_DEV_FORCECPS (launch that many CTAs per SM),
-// SC_DEV_MAX_CARVEOUT (keep the largest shared-memory carveout) and
+// SC_DEV_MAX_CARVEOUT (keep the largest shared-memory carveout),
+// SC_DEV_NO_WEIGHT_TMA (pack W instead of reading its slices by TMA) and
 // SC_DEV_VERBOSE (print each launch's plan).  None changes the result.
 bool make_plan(int c_in, int c_out, bool output_stationary, Plan* pl) {
   pl->bk = pick_bk(c_in);
@@ -891,6 +935,79 @@ bool fused_ok(const ConvArgs& a, Plan* pl) {
   return a.dtype != SC_F32 && a.m->V <= 128 && make_plan(a.c_in, a.c_out, true, pl);
 }
 
+// cuTensorMapEncodeTiled, resolved once through the runtime's driver entry
+// point (the library does not link the driver library).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn tensor_map_encoder() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+CUtensorMapSwizzle swizzle_for(int row_bytes) {
+  return row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                          : (row_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
+}
+
+// The fused layer's weight slices read by TMA straight from W (no packed
+// image): the tensor map of W and the mode (TcParams::wmode).  False when the
+// shapes do not fit a TMA box (then the caller packs W as before).
+// Developer override SC_DEV_NO_WEIGHT_TMA=1: always pack.
+bool setup_weight_tma(const ConvArgs& a, const Plan& pl, TcParams* p) {
+  if (getenv("SC_DEV_NO_WEIGHT_TMA")) return false;
+  if (reinterpret_cast<uintptr_t>(a.W) % 16) return false;
+  const EncodeTiledFn enc = tensor_map_encoder();
+  if (!enc) return false;
+  const int V = a.m->V, BK = pl.bk;
+  cuuint64_t dims[2];
+  cuuint64_t strides[1];
+  cuuint32_t box[2];
+  const cuuint32_t estr[2] = {1, 1};
+  CUtensorMapSwizzle sw;
+  int mode, nb = 0;
+  if (!a.wt) {
+    // W [V][c_in][c_out]: rows v * c_in + ci, columns co; a slice is BK rows,
+    // fetched as c_out / nb boxes of nb columns (a 32, 64 or 128-byte swizzle)
+    nb = a.c_out >= 64 ? 64 : a.c_out;
+    if ((nb != 16 && nb != 32 && nb != 64) || a.c_out % nb) return false;
+    dims[0] = static_cast<cuuint64_t>(a.c_out);
+    dims[1] = static_cast<cuuint64_t>(V) * a.c_in;
+    strides[0] = static_cast<cuuint64_t>(a.c_out) * 2;
+    box[0] = static_cast<cuuint32_t>(nb);
+    box[1] = static_cast<cuuint32_t>(BK);
+    sw = swizzle_for(nb * 2);
+    mode = 1;
+  } else {
+    // the forward W [V][c_out][c_in] (this call's c_out rows per offset, its
+    // c_in channels contiguous): one box of c_out rows x BK channels
+    if (a.c_out > 256) return false;
+    dims[0] = static_cast<cuuint64_t>(a.c_in);
+    dims[1] = static_cast<cuuint64_t>(V) * a.c_out;
+    strides[0] = static_cast<cuuint64_t>(a.c_in) * 2;
+    box[0] = static_cast<cuuint32_t>(BK);
+    box[1] = static_cast<cuuint32_t>(a.c_out);
+    sw = swizzle_for(BK * 2);
+    mode = 2;
+  }
+  const CUresult r = enc(&p->wmap, a.dtype == SC_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                         2, const_cast<void*>(a.W), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return false;
+  p->wmode = mode;
+  p->wnb = nb;
+  return true;
+}
+
 // The output-stationary launch on an already packed weight image.
 sc_status run_fused(const ConvArgs& a, const Plan& pl, const uint8_t* img) {
   TcParams prm = base_params(a, pl, img);
@@ -909,6 +1026,12 @@ sc_status conv_fused(const ConvArgs& a) {
   if (!fused_ok(a, &pl))
     return set_error(SC_ERR_UNSUPPORTED, "fused kernel: f16/bf16 only, V <= 128, tile must fit shared memory");
   if (a.m->n == 0) return SC_OK;
+  {
+    // the weight slices straight from W by TMA: no packed image
+    TcParams prm = base_params(a, pl, nullptr);
+    if (setup_weight_tma(a, pl, &prm))
+      return dispatch_tc<kOutputStationary>(prm, pl, a.dtype == SC_BF16, a.stream, "subm_conv_fused");
+  }
   const size_t img_bytes = static_cast<size_t>(a.m->V) * a.c_in * a.c_out * 2;
   void* img = nullptr;
   sc_status st = dev_alloc(&img, img_bytes, a.stream);

@@ -350,10 +350,12 @@ def test_launch_count_and_profile():
     finally:
         sc.profile_enable(False)
     launched = sc.launch_count() - before
-    # insert, the single-pass map build, weight pack, fused conv
-    assert launched == 4
-    for k in ("hash_insert", "kmap_build", "pack_weights", "subm_conv_fused"):
+    # insert, the single-pass map build, the fused conv (which reads the
+    # weight slices from W by TMA: no pack)
+    assert launched == 3
+    for k in ("hash_insert", "kmap_build", "subm_conv_fused"):
         assert k in prof and prof[k][0] == 1 and prof[k][1] > 0
+    assert "pack_weights" not in prof
 
 
 def test_profile_only_brackets_the_named_kernels():

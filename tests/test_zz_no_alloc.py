@@ -98,8 +98,8 @@ def test_noalloc_on_a_strided_map():
 def test_noalloc_allocates_nothing():
     """With the library's allocator set to PyTorch's caching allocator, any
     library allocation would show in torch's allocation counter; the
-    no-allocation call leaves it unchanged (the fused call, which allocates
-    its packed weights, moves it)."""
+    no-allocation call leaves it unchanged (the weight-stationary call, which
+    allocates its packed weights and fp32 sums, moves it)."""
     s = scenes.lidar_scan(95, 3000, (160, 160, 41))
     h = sc.sc_hash_build(torch.from_numpy(s.coords).cuda())
     m = sc.sc_kmap_build(h, 3, 3, s.dims)
@@ -113,7 +113,7 @@ def test_noalloc_allocates_nothing():
         for _ in range(3):
             assert _noalloc(m, f, W, out) == 0, sc.lib().sc_last_error()
         assert _allocs() == before
-        sc.sc_subm_conv_fwd(m, f, W, out=out2, variant="fused")
+        sc.sc_subm_conv_fwd(m, f, W, out=out2, variant="ws")
         assert _allocs() > before
     finally:
         sc.use_torch_allocator(False)
