@@ -33,9 +33,13 @@
 //              thread's arrival on the stage barrier fires when its copies
 //              land (cp.async.mbarrier.arrive.noinc), so a warp never waits
 //              for its own copies.
-//   1 warp     weight loader: one thread bulk-copies the matching W slices
-//              from a pre-swizzled image into each stage and prefetches the
-//              next tile's neighbour-table block into L2.
+//   1 warp     weight loader: one thread loads the matching W slices into
+//              each stage, by TMA straight from W (cp.async.bulk.tensor: the
+//              slice lands swizzled; a layer's B is MN-major, an input
+//              gradient's K-major) or by bulk copies from a pre-swizzled image
+//              (widths that fit no TMA box, the weight-stationary modes, the
+//              no-allocation entry point), and prefetches the next tile's
+//              neighbour-table block into L2.
 //   1 warp     MMA issuer: allocates TMEM (two accumulators of C_out fp32 columns); lane 0
 //              issues tcgen05.mma (M = 128, N = C_out, K = 16) and commits.
 //   4 warps    epilogue: TMEM lane quadrant (warp % 4) -> registers -> global,
