@@ -764,7 +764,10 @@ def run_ours(args):
     for k, (n_l, tot) in prof_all.items():
         per_kernel[k] = {"launches_per_step": round(n_l / bd_steps, 3), "avg_us": round(1e3 * tot / max(n_l, 1), 3),
                          "share": round(tot / tot_all, 4)}
-    conv_k = [k for k in prof_all if k.startswith("subm_conv")]
+    # the layers' kernels: the convolution kernels, and the weight pack of a
+    # layer that packs its weights (the weight-stationary and CUDA-core
+    # variants; the fused kernel reads W's slices by TMA and launches none)
+    conv_k = [k for k in prof_all if k.startswith("subm_conv") or k in ("pack_weights", "cast_out", "wgrad_cast")]
     conv_ms = sum(prof_all[k][1] for k in conv_k) / bd_steps
     map_ms = sum(prof_all[k][1] for k in MAP_KERNELS if k in prof_all) / bd_steps
     peaks = load_peaks()
