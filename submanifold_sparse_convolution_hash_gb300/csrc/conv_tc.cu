@@ -81,10 +81,9 @@ constexpr int kBarriers = 2 * kMaxStages + 5;  // full[S], empty[S], acc_full[2]
 enum Mode { kOutputStationary = 0, kWsScatter = 1, kWsCentre = 2 };
 
 struct TcParams {
-  // wmode 1 / 2: the weights' tensor map (W itself, read by TMA); passed in
-  // the kernel's __grid_constant__ parameter block
-  CUtensorMap wmap;
-  // how the weight loader fetches each (offset, panel) slice of W:
+  // how the weight loader fetches each (offset, panel) slice of W (wmode 1
+  // and 2 read W by TMA through the tensor map passed as the kernel's
+  // second, __grid_constant__ argument):
   //   0: bulk copy from a packed image (wimg)
   //   1: TMA from W [V][c_in][c_out] (a layer): B MN-major, boxes of wnb
   //      output channels x BK input channels, wnb-column swizzle
@@ -224,7 +223,7 @@ __device__ __forceinline__ int unit_kblocks(const TcParams& p, int u, int P) {
 // tile-transposed table (p.tnbr) instead of nbr through perm.
 template <int BK, int MODE, bool BF16, int NPW, int T, bool TT>
 __global__ void __launch_bounds__((NPW + 6) * 32, NPW == 4 ? 3 : (NPW == 8 ? 2 : 1))
-    k_conv_tc(const __grid_constant__ TcParams p) {
+    k_conv_tc(const TcParams p, const __grid_constant__ CUtensorMap wmap) {
   constexpr int ROWB = BK * 2;          // bytes per tile row (= swizzle width)
   constexpr int A_PART = kRows * ROWB;  // one 128-row MMA operand of a sub-block
   constexpr int A_SUB = T * A_PART;     // one (offset, panel) sub-block of A
@@ -436,10 +435,10 @@ __global__ void __launch_bounds__((NPW + 6) * 32, NPW == 4 ? 3 : (NPW == 8 ? 2 :
               // W[v] rows bp * BK .. + BK (input channels), wnb output channels per box
               const int y = bv * p.c_in + bp * BK;
               for (int i = 0; i * p.wnb < p.c_out; ++i)
-                tma_load_2d(dstb + static_cast<uint32_t>(i * BK * p.wnb * 2), &p.wmap, i * p.wnb, y, full0 + 8 * s);
+                tma_load_2d(dstb + static_cast<uint32_t>(i * BK * p.wnb * 2), &wmap, i * p.wnb, y, full0 + 8 * s);
             } else if (p.wmode == 2) {
               // rows (V-1-v) * c_out .. + c_out of the forward W, channels bp * BK .. + BK
-              tma_load_2d(dstb, &p.wmap, bp * BK, (V - 1 - bv) * p.c_out, full0 + 8 * s);
+              tma_load_2d(dstb, &wmap, bp * BK, (V - 1 - bv) * p.c_out, full0 + 8 * s);
             } else {
               bulk_g2s(dstb, p.wimg + (static_cast<size_t>(bv) * P + bp) * B_SUB, static_cast<uint32_t>(B_SUB),
                        full0 + 8 * s);
@@ -818,7 +817,7 @@ bool make_plan(int c_in, int c_out, bool output_stationary, Plan* pl) {
 }
 
 template <int BK, int MODE, bool BF16, int NPW, int T, bool TT>
-sc_status launch_tc(const TcParams& prm, const Plan& pl, cudaStream_t s, const char* name) {
+sc_status launch_tc(const TcParams& prm, const CUtensorMap& wmap, const Plan& pl, cudaStream_t s, const char* name) {
   auto kern = k_conv_tc<BK, MODE, BF16, NPW, T, TT>;
   constexpr int threads = (NPW + 6) * 32;
   int num_regs = 0;
@@ -842,49 +841,57 @@ sc_status launch_tc(const TcParams& prm, const Plan& pl, cudaStream_t s, const c
     fprintf(stderr, "%s: bk %d npw %d t %d nbuf %d group %d stages %d smem %zu plan cps %d fit %d grid %d regs %d\n",
             name, BK, NPW, T, pl.nbuf, pl.group, pl.stages, pl.smem, pl.ctas_per_sm, fit, grid, num_regs);
   }
-  SC_LAUNCH(name, s, kern<<<grid, threads, pl.smem, s>>>(prm));
+  SC_LAUNCH(name, s, kern<<<grid, threads, pl.smem, s>>>(prm, wmap));
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? SC_OK : set_cuda_error(e, name);
 }
 
 template <int BK, int MODE, bool BF16, bool TT>
-sc_status launch_npw(const TcParams& prm, const Plan& pl, cudaStream_t s, const char* name) {
+sc_status launch_npw(const TcParams& prm, const CUtensorMap& wm, const Plan& pl, cudaStream_t s, const char* name) {
   if constexpr (BK == 16) {
-    return pl.npw == 8 ? launch_tc<BK, MODE, BF16, 8, 1, TT>(prm, pl, s, name)
-                       : launch_tc<BK, MODE, BF16, 4, 1, TT>(prm, pl, s, name);
+    return pl.npw == 8 ? launch_tc<BK, MODE, BF16, 8, 1, TT>(prm, wm, pl, s, name)
+                       : launch_tc<BK, MODE, BF16, 4, 1, TT>(prm, wm, pl, s, name);
   } else {
     if constexpr (MODE == kOutputStationary) {
       if (pl.t == 2)
-        return pl.npw == 16 ? launch_tc<BK, MODE, BF16, 16, 2, TT>(prm, pl, s, name)
-                            : launch_tc<BK, MODE, BF16, 8, 2, TT>(prm, pl, s, name);
+        return pl.npw == 16 ? launch_tc<BK, MODE, BF16, 16, 2, TT>(prm, wm, pl, s, name)
+                            : launch_tc<BK, MODE, BF16, 8, 2, TT>(prm, wm, pl, s, name);
     }
     switch (pl.npw) {
-      case 16: return launch_tc<BK, MODE, BF16, 16, 1, TT>(prm, pl, s, name);
-      case 8: return launch_tc<BK, MODE, BF16, 8, 1, TT>(prm, pl, s, name);
-      default: return launch_tc<BK, MODE, BF16, 4, 1, TT>(prm, pl, s, name);
+      case 16: return launch_tc<BK, MODE, BF16, 16, 1, TT>(prm, wm, pl, s, name);
+      case 8: return launch_tc<BK, MODE, BF16, 8, 1, TT>(prm, wm, pl, s, name);
+      default: return launch_tc<BK, MODE, BF16, 4, 1, TT>(prm, wm, pl, s, name);
     }
   }
 }
 
 template <int MODE, bool TT>
-sc_status dispatch_bk(const TcParams& prm, const Plan& pl, bool bf16, cudaStream_t s, const char* name) {
+sc_status dispatch_bk(const TcParams& prm, const CUtensorMap& wm, const Plan& pl, bool bf16, cudaStream_t s,
+                      const char* name) {
   switch (pl.bk) {
     case 64:
-      return bf16 ? launch_npw<64, MODE, true, TT>(prm, pl, s, name) : launch_npw<64, MODE, false, TT>(prm, pl, s, name);
+      return bf16 ? launch_npw<64, MODE, true, TT>(prm, wm, pl, s, name)
+                  : launch_npw<64, MODE, false, TT>(prm, wm, pl, s, name);
     case 32:
-      return bf16 ? launch_npw<32, MODE, true, TT>(prm, pl, s, name) : launch_npw<32, MODE, false, TT>(prm, pl, s, name);
+      return bf16 ? launch_npw<32, MODE, true, TT>(prm, wm, pl, s, name)
+                  : launch_npw<32, MODE, false, TT>(prm, wm, pl, s, name);
     default:
-      return bf16 ? launch_npw<16, MODE, true, TT>(prm, pl, s, name) : launch_npw<16, MODE, false, TT>(prm, pl, s, name);
+      return bf16 ? launch_npw<16, MODE, true, TT>(prm, wm, pl, s, name)
+                  : launch_npw<16, MODE, false, TT>(prm, wm, pl, s, name);
   }
 }
 
+// wm: the weights' tensor map when prm.wmode reads W by TMA (else unused)
 template <int MODE>
-sc_status dispatch_tc(const TcParams& prm, const Plan& pl, bool bf16, cudaStream_t s, const char* name) {
+sc_status dispatch_tc(const TcParams& prm, const Plan& pl, bool bf16, cudaStream_t s, const char* name,
+                      const CUtensorMap* wm = nullptr) {
   if (prm.num_units <= 0) return SC_OK;
+  static const CUtensorMap kNoMap{};
+  const CUtensorMap& m = wm ? *wm : kNoMap;
   if constexpr (MODE == kOutputStationary) {
-    if (prm.tnbr) return dispatch_bk<MODE, true>(prm, pl, bf16, s, name);
+    if (prm.tnbr) return dispatch_bk<MODE, true>(prm, m, pl, bf16, s, name);
   }
-  return dispatch_bk<MODE, false>(prm, pl, bf16, s, name);
+  return dispatch_bk<MODE, false>(prm, m, pl, bf16, s, name);
 }
 
 sc_status pack_weights(const ConvArgs& a, int bk, uint8_t* img) {
@@ -967,7 +974,7 @@ CUtensorMapSwizzle swizzle_for(int row_bytes) {
 // image): the tensor map of W and the mode (TcParams::wmode).  False when the
 // shapes do not fit a TMA box (then the caller packs W as before).
 // Developer override SC_DEV_NO_WEIGHT_TMA=1: always pack.
-bool setup_weight_tma(const ConvArgs& a, const Plan& pl, TcParams* p) {
+bool setup_weight_tma(const ConvArgs& a, const Plan& pl, TcParams* p, CUtensorMap* wmap) {
   if (getenv("SC_DEV_NO_WEIGHT_TMA")) return false;
   if (reinterpret_cast<uintptr_t>(a.W) % 16) return false;
   const EncodeTiledFn enc = tensor_map_encoder();
@@ -1003,7 +1010,7 @@ bool setup_weight_tma(const ConvArgs& a, const Plan& pl, TcParams* p) {
     sw = swizzle_for(BK * 2);
     mode = 2;
   }
-  const CUresult r = enc(&p->wmap, a.dtype == SC_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+  const CUresult r = enc(wmap, a.dtype == SC_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                          2, const_cast<void*>(a.W), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return false;
@@ -1033,8 +1040,9 @@ sc_status conv_fused(const ConvArgs& a) {
   {
     // the weight slices straight from W by TMA: no packed image
     TcParams prm = base_params(a, pl, nullptr);
-    if (setup_weight_tma(a, pl, &prm))
-      return dispatch_tc<kOutputStationary>(prm, pl, a.dtype == SC_BF16, a.stream, "subm_conv_fused");
+    CUtensorMap wmap;
+    if (setup_weight_tma(a, pl, &prm, &wmap))
+      return dispatch_tc<kOutputStationary>(prm, pl, a.dtype == SC_BF16, a.stream, "subm_conv_fused", &wmap);
   }
   const size_t img_bytes = static_cast<size_t>(a.m->V) * a.c_in * a.c_out * 2;
   void* img = nullptr;
