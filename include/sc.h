@@ -356,9 +356,13 @@ sc_status sc_kmap_destroy(sc_kmap m, sc_stream stream);
  * kernel with column splitting and an fp32 partial-sum buffer [n, c_out]
  * allocated for the call.  Variant: forced by flags, else the one sc_subm_conv_tune measured fastest
  * for (c_in, c_out, dtype) on this map, else the fused output-stationary
- * kernel (f16/bf16) or the CUDA-core kernel (f32).  Temporary device memory
- * (packed weights, the fp32 accumulator of the weight-stationary variant) is
- * allocated and freed stream-ordered on `stream`.
+ * kernel (f16/bf16) or the CUDA-core kernel (f32).  The fused kernel reads
+ * each weight slice by TMA straight from d_W (which must then be 16-byte
+ * aligned; otherwise, and for output widths that fit no TMA box such as 48
+ * or 80 channels, it repacks W into a temporary first) and allocates
+ * nothing.  Temporary device memory of the other variants (packed weights,
+ * the fp32 accumulator of the weight-stationary variant) is allocated and
+ * freed stream-ordered on `stream`.
  */
 sc_status sc_subm_conv_fwd(sc_kmap m, const void* d_feats, const void* d_W, void* d_out, int c_in,
                            int c_out, sc_dtype dtype, unsigned flags, sc_stream stream);
@@ -411,10 +415,11 @@ sc_status sc_subm_conv_bwd_weight(sc_kmap m, const void* d_feats, const void* d_
  * themselves, or latency-critical code where an allocation that may block or
  * fail is not acceptable.
  *
- * The fused kernel needs temporary device memory for the weights repacked
- * into its shared-memory layout.  Here that memory is one fixed 4 MiB device
- * array inside the library, present on every GPU that loads the library
- * until the process exits.  The caller still passes every input and output.
+ * This entry point always repacks the weights into the fused kernel's
+ * shared-memory layout (rather than reading W by TMA as sc_subm_conv_fwd
+ * does), into one fixed 4 MiB device array inside the library, present on
+ * every GPU that loads the library until the process exits.  The caller still
+ * passes every input and output.
  *
  * Limits: f16/bf16 only; V <= 128; V * c_in * c_out * 2 bytes <= 4 MiB
  * (4,194,304), else SC_ERR_UNSUPPORTED with a message in sc_last_error().
