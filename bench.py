@@ -490,6 +490,16 @@ def cpu_oracle_run(s, K, f, W, seconds: float, stride: int = 0):
             "sample": f"full scene (N={s.n}) x {passes} pass(es): output set + map + fp64 layer, {el:.1f} s"}
 
 
+def use_tile_table(mode: str, n_layers: int, V: int, split: bool) -> bool:
+    """Whether the map is built with the fused layer's tile table
+    (SC_KMAP_TILE_TABLE): "on", "off", or "auto" = when one map serves more
+    than one layer (the pass costs more than a single layer gains).  Never
+    with column splitting or above 128 offsets, which the library refuses."""
+    if split or V > 128:
+        return False
+    return mode == "on" or (mode == "auto" and n_layers > 1)
+
+
 def workload_config(w, s, M: int, world: int, layer_type: str = "submanifold", stride: int = 1,
                     n_out: int | None = None, backward: bool = False, scale: float = 1.0):
     """The line's `config`: what the workload is, identical in both arms."""
@@ -597,9 +607,7 @@ def run_ours(args):
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
     sort_arg = {"auto": None, "on": True, "off": False}[args.kmap_sort]
-    # the tile table pays when one map serves several layers
-    tile_table = (args.kmap_tile_table == "on" or (args.kmap_tile_table == "auto" and len(layers) > 1)) \
-        and not args.kmap_split and w.K ** s.ndim <= 128
+    tile_table = use_tile_table(args.kmap_tile_table, len(layers), w.K ** s.ndim, args.kmap_split)
 
     def build_map(c, sync):
         """hash -> kernel map (submanifold), or hash -> output set -> map

@@ -180,3 +180,15 @@ def test_the_two_oracle_timings_estimate_the_same_quantity():
     table.close()
     assert len(rows) < s.n
     assert 0.6 < ref / cb["value"] < 1.6, (ref, cb["value"])
+
+
+def test_tile_table_policy():
+    """auto: only when one map serves several layers; never with column
+    splitting or above 128 offsets (the library refuses those)."""
+    assert bench.use_tile_table("auto", 8, 27, False)
+    assert not bench.use_tile_table("auto", 1, 27, False)
+    assert not bench.use_tile_table("auto", 1, 125, False)
+    assert bench.use_tile_table("on", 1, 125, False)
+    assert not bench.use_tile_table("on", 8, 343, False)
+    assert not bench.use_tile_table("on", 8, 27, True)
+    assert not bench.use_tile_table("off", 8, 27, False)
