@@ -607,7 +607,7 @@ def run_ours(args):
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
     sort_arg = {"auto": None, "on": True, "off": False}[args.kmap_sort]
-    tile_table = use_tile_table(args.kmap_tile_table, len(layers), w.K ** s.ndim, args.kmap_split)
+    tile_table = use_tile_table(args.kmap_tile_table, len(layers), V, args.kmap_split)
 
     def build_map(c, sync):
         """hash -> kernel map (submanifold), or hash -> output set -> map
