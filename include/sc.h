@@ -386,8 +386,11 @@ sc_status sc_subm_conv_tune(sc_kmap m, const void* d_feats, const void* d_W, voi
  *   d_gout[q, :] @ W[d]^T.  The tuple (p, q, d) of the forward map is the
  *   tuple (q, p, -d) of the same map (mirror symmetry), so this is a
  *   submanifold layer from c_out to c_in channels with weights
- *   W'[idx(d)] = W[idx(-d)]^T, and it runs on the forward kernels (the weight
- *   packing transposes and mirrors W).
+ *   W'[idx(d)] = W[idx(-d)]^T, and it runs on the forward kernels: the fused
+ *   kernel reads each slice W[idx(-d)]^T by TMA straight from d_W (16-byte
+ *   aligned, c_in at most 256), with no temporary; otherwise,
+ *   and in the weight-stationary variant, the weight packing transposes and
+ *   mirrors W into a temporary.
  *   d_gout [n, c_out], d_W [V, c_in, c_out] (the forward layer's weights),
  *   d_gin [n, c_in]; c_in and c_out are the forward layer's.  flags: 0 or one
  *   SC_VARIANT_*.
