@@ -102,6 +102,17 @@ def _coords(coords):
     return np.ascontiguousarray(np.asarray(coords, dtype=np.int32).reshape(-1, 4))
 
 
+def _rows(a, n: int) -> np.ndarray:
+    """fp64, C-contiguous [n, width] copy of a feature array: a 2-D array as it
+    is (it must have n rows), anything else reshaped to n rows.  n may be 0."""
+    a = np.asarray(a, dtype=np.float64)
+    if a.ndim != 2:
+        a = a.reshape(n, -1)
+    if a.shape[0] != n:
+        raise OracleError(1)
+    return np.ascontiguousarray(a)
+
+
 def _dims(dims):
     d = np.ones(3, dtype=np.int32)
     d[: len(dims)] = dims
@@ -177,7 +188,7 @@ def subm_conv(coords, feats, W, ndim: int, K: int, dims, relu: bool = False,
     """fp64 output features [len(rows) or N, C_out] of one submanifold layer."""
     c = _coords(coords)
     n = c.shape[0]
-    f = np.ascontiguousarray(np.asarray(feats, dtype=np.float64).reshape(n, -1))
+    f = _rows(feats, n)
     w = np.ascontiguousarray(np.asarray(W, dtype=np.float64))
     V, c_in, c_out = w.shape
     if V != volume(ndim, K) or f.shape[1] != c_in:
@@ -208,7 +219,7 @@ class Table:
             raise OracleError(st.value)
 
     def subm_conv(self, feats, W, relu: bool = False, rows=None, threads: int = 0) -> np.ndarray:
-        f = np.ascontiguousarray(np.asarray(feats, dtype=np.float64).reshape(self.n, -1))
+        f = _rows(feats, self.n)
         w = np.ascontiguousarray(np.asarray(W, dtype=np.float64))
         V, c_in, c_out = w.shape
         if V != volume(self.ndim, self.K) or f.shape[1] != c_in:
@@ -264,8 +275,8 @@ def subm_conv_bwd_weight(coords, feats, gout, ndim: int, K: int, dims, threads: 
     """fp64 gradient with respect to the weights [K^ndim, C_in, C_out]."""
     c = _coords(coords)
     n = c.shape[0]
-    f = np.ascontiguousarray(np.asarray(feats, dtype=np.float64).reshape(n, -1))
-    g = np.ascontiguousarray(np.asarray(gout, dtype=np.float64).reshape(n, -1))
+    f = _rows(feats, n)
+    g = _rows(gout, n)
     V = volume(ndim, K)
     out = np.empty((V, f.shape[1], g.shape[1]), dtype=np.float64)
     st = _load().oracle_subm_conv_bwd_weight(_ptr(c), n, ndim, K, _ptr(_dims(dims)), _ptr(f), _ptr(g), f.shape[1],
@@ -352,7 +363,7 @@ def sparse_conv(coords, out_coords, feats, W, ndim: int, K: int, stride: int, di
     """fp64 output features [N_out, C_out] of one regular / strided layer."""
     c, o = _coords(coords), _coords(out_coords)
     n = c.shape[0]
-    f = np.ascontiguousarray(np.asarray(feats, dtype=np.float64).reshape(n, -1))
+    f = _rows(feats, n)
     w = np.ascontiguousarray(np.asarray(W, dtype=np.float64))
     V, c_in, c_out = w.shape
     if V != volume(ndim, K) or f.shape[1] != c_in:
@@ -369,8 +380,8 @@ def sparse_conv_bwd_weight(coords, out_coords, feats, gout, ndim: int, K: int, s
                            threads: int = 0) -> np.ndarray:
     """fp64 weight gradient [K^ndim, C_in, C_out] of a regular / strided layer."""
     c, o = _coords(coords), _coords(out_coords)
-    f = np.ascontiguousarray(np.asarray(feats, dtype=np.float64).reshape(c.shape[0], -1))
-    g = np.ascontiguousarray(np.asarray(gout, dtype=np.float64).reshape(o.shape[0], -1))
+    f = _rows(feats, c.shape[0])
+    g = _rows(gout, o.shape[0])
     V = volume(ndim, K)
     out = np.empty((V, f.shape[1], g.shape[1]), dtype=np.float64)
     st = _load().oracle_conv_bwd_weight(_ptr(c), c.shape[0], _ptr(o), o.shape[0], ndim, K, stride,

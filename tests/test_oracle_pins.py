@@ -714,3 +714,37 @@ def test_strided_input_gradient_equals_dense_autograd(ndim, K, stride, dims, n, 
     # adjoint identity: <conv(f), g> = <f, gin>
     lhs = float((oracle.sparse_conv(c, o, f, W, ndim, K, stride, dims) * g).sum())
     assert abs(lhs - float((f * gin).sum())) <= 1e-9 * max(1.0, abs(lhs))
+
+
+def test_empty_scene_gives_empty_outputs_and_zero_weight_gradients():
+    """No active site: every layer output has no rows, and a weight gradient,
+    a sum over the map's tuples, is the empty sum 0.  The kept table agrees."""
+    c = np.zeros((0, 4), dtype=np.int32)
+    o = np.zeros((0, 4), dtype=np.int32)
+    dims = (8, 8, 8)
+    W = np.ones((27, 16, 8))
+    assert oracle.kmap(c, 3, 3, dims).shape == (0, 27)
+    assert oracle.subm_conv(c, np.zeros((0, 16)), W, 3, 3, dims, relu=True).shape == (0, 8)
+    assert oracle.subm_conv_bwd_data(c, np.zeros((0, 8)), W, 3, 3, dims).shape == (0, 16)
+    gw = oracle.subm_conv_bwd_weight(c, np.zeros((0, 16)), np.zeros((0, 8)), 3, 3, dims)
+    assert gw.shape == (27, 16, 8) and not gw.any()
+    outs = oracle.subm_conv_stack(c, np.zeros((0, 16)), [np.ones((27, 16, 16))] * 2, 3, 3, dims, "f16")
+    assert [x.shape for x in outs] == [(0, 16), (0, 16)]
+    with oracle.Table(c, 3, 3, dims) as t:
+        assert t.subm_conv(np.zeros((0, 16)), W).shape == (0, 8)
+    assert oracle.conv_out_coords(c, 3, 3, 2, dims).shape == (0, 4)
+    assert oracle.sparse_conv(c, o, np.zeros((0, 16)), W, 3, 3, 2, dims).shape == (0, 8)
+    assert oracle.sparse_conv_bwd_data(c, o, np.zeros((0, 8)), W, 3, 3, 2, dims).shape == (0, 16)
+    gw = oracle.sparse_conv_bwd_weight(c, o, np.zeros((0, 16)), np.zeros((0, 8)), 3, 3, 2, dims)
+    assert gw.shape == (27, 16, 8) and not gw.any()
+
+
+def test_feature_rows_must_match_the_points():
+    """A feature array whose row count differs from the number of points is
+    an argument error, not silently reshaped."""
+    c = np.array([[0, 1, 1, 1], [0, 2, 1, 1]], dtype=np.int32)
+    W = np.ones((27, 4, 4))
+    with pytest.raises(oracle.OracleError):
+        oracle.subm_conv(c, np.zeros((4, 4)), W, 3, 3, (8, 8, 8))
+    with pytest.raises(oracle.OracleError):
+        oracle.subm_conv_bwd_weight(c, np.zeros((2, 4)), np.zeros((1, 8)), 3, 3, (8, 8, 8))
