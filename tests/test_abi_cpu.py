@@ -124,3 +124,20 @@ def test_binding_refuses_host_tensors():
         binding.sc_hash_build(torch.zeros((4, 4), dtype=torch.int32))
     with pytest.raises(ValueError, match="CUDA tensor"):
         binding.sc_hash_build(torch.zeros((4, 4), dtype=torch.int32).numpy())
+
+
+def test_readme_names_only_declared_entry_points_and_flags():
+    """Every sc_* name (function or type) and SC_* flag the README names is
+    declared in include/sc.h, and every declared function appears in the
+    README."""
+    header = open(os.path.join(ROOT, "include", "sc.h")).read()
+    code = re.sub(r"/\*.*?\*/", "", header, flags=re.S)
+    readme = open(os.path.join(ROOT, "README.md")).read()
+    fns = set(header_functions())
+    declared = set(re.findall(r"\b(sc_[a-z_]+)\b", code))
+    flags = set(re.findall(r"#define (SC_[A-Z0-9_]+)", header))
+    named_fns = set(re.findall(r"`(sc_[a-z_]+)`", readme))
+    named_flags = set(re.findall(r"`(SC_[A-Z0-9_]+)`", readme))
+    assert named_fns <= declared, named_fns - declared
+    assert named_flags <= flags, named_flags - flags
+    assert fns <= set(re.findall(r"\b(sc_[a-z_]+)\b", readme)), fns - set(re.findall(r"\b(sc_[a-z_]+)\b", readme))
